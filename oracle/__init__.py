@@ -1,0 +1,258 @@
+"""CPU fp64 oracle for the sparse top-k MoE FFN layer forward.
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package. The product library
+(``sparse_mixture_experts_router_gb300``) never imports it and shares no code
+with it.
+
+This module is argument marshalling around ``moe_oracle.c`` (numpy arrays in,
+numpy arrays out); all arithmetic lives in the C file, which states the
+definition it follows for every function, citing the pages by title and
+section. Stored bf16 inputs are passed as their uint16 bit patterns and are
+widened exactly inside the C code.
+
+Parity unpinned: the SwiGLU expert at realistic sizes (no printed value on the
+pages; pinned only by reduction to library routines and by brute force on
+tiny inputs).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libmoe_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16, F64 = 0, 1, 2
+GATE_TOPK_SOFTMAX, GATE_ALL_SOFTMAX_RENORM = 0, 1
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+
+
+def compile_oracle(src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the oracle C file into a shared library (gcc, OpenMP, -O2,
+    strict IEEE arithmetic: no fast-math, no FMA contraction)."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _declare(lib):
+    lib.oracle_num_threads.restype = _I
+    lib.oracle_softmax.argtypes = [_I, _P, _P]
+    lib.oracle_topk.argtypes = [_I, _I, _P, _P]
+    lib.oracle_gates.argtypes = [_I, _I, _I, _P, _P, _P]
+    lib.oracle_router_logits.argtypes = [_I, _I, _I, _I, _P, _I, _P, _P, _P, _P]
+    lib.oracle_route.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P]
+    lib.oracle_permute.argtypes = [_I, _I, _I, _P, _P, _P, _P]
+    lib.oracle_expert_swiglu.argtypes = [_I, _I, _I, _P, _P, _P, _P, _P]
+    lib.oracle_gated_sum.argtypes = [_I, _I, _P, _P, _P]
+    lib.oracle_layer_rows.restype = _I
+    lib.oracle_layer_rows.argtypes = [_I, _I, _I, _I, _I, _I, _I, _P, _I,
+                                      _P, _P, _P, _P, _P, _I, _P, _P]
+    lib.oracle_balance_loss.restype = ctypes.c_double
+    lib.oracle_balance_loss.argtypes = [_I, _P, _P, ctypes.c_double]
+    lib.oracle_balance_stats.restype = ctypes.c_double
+    lib.oracle_balance_stats.argtypes = [_I, _I, _I, _P, _P, ctypes.c_double,
+                                         _P, _P]
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (compiling first if needed) the oracle library. ``path`` loads a
+    specific build instead (used by the planted-mistake tests)."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            if (not os.path.exists(_LIB_PATH)
+                    or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+                compile_oracle()
+            _lib = _declare(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_P)
+
+
+def _stored(a):
+    """(dtype code, contiguous array) of a stored input: float32, float64, or
+    uint16 holding bf16 bit patterns."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float32:
+        return F32, a
+    if a.dtype == np.float64:
+        return F64, a
+    if a.dtype == np.uint16:
+        return BF16, a
+    raise TypeError(f"oracle inputs are float32, float64 or bf16 bits (uint16), got {a.dtype}")
+
+
+class Oracle:
+    """Thin marshalling layer over one loaded oracle library."""
+
+    def __init__(self, lib=None):
+        self.lib = lib if lib is not None else load()
+
+    def num_threads(self) -> int:
+        return int(self.lib.oracle_num_threads())
+
+    def softmax(self, r):
+        r = _c(r, np.float64)
+        p = np.empty_like(r)
+        self.lib.oracle_softmax(r.size, _ptr(r), _ptr(p))
+        return p
+
+    def topk(self, key, k):
+        key = _c(key, np.float32)
+        idx = np.empty(k, np.int32)
+        self.lib.oracle_topk(key.size, k, _ptr(key), _ptr(idx))
+        return idx
+
+    def gates(self, r, idx, mode=GATE_TOPK_SOFTMAX):
+        r = _c(r, np.float64)
+        idx = _c(idx, np.int32)
+        g = np.empty(idx.size, np.float64)
+        self.lib.oracle_gates(r.size, idx.size, mode, _ptr(r), _ptr(idx), _ptr(g))
+        return g
+
+    def router_logits(self, x, w_router, logit_bias=None):
+        """(r64 [T,N] fp64, r32 [T,N] fp32)."""
+        xd, x = _stored(x)
+        wd, w = _stored(w_router)
+        T, d = x.shape
+        N = w.shape[0]
+        assert w.shape[1] == d
+        lb = None if logit_bias is None else _c(logit_bias, np.float64)
+        r64 = np.empty((T, N), np.float64)
+        r32 = np.empty((T, N), np.float32)
+        self.lib.oracle_router_logits(T, d, N, xd, _ptr(x), wd, _ptr(w), _ptr(lb),
+                                      _ptr(r64), _ptr(r32))
+        return r64, r32
+
+    def route(self, r32, k, gate_mode=GATE_TOPK_SOFTMAX, sel_bias=None):
+        """(topk_idx [T,k] int32, topk_w [T,k] fp64, counts [N] int32,
+        prob_sum [N] fp64) from fp32 router scores."""
+        r32 = _c(r32, np.float32)
+        T, N = r32.shape
+        sb = None if sel_bias is None else _c(sel_bias, np.float32)
+        idx = np.empty((T, k), np.int32)
+        w = np.empty((T, k), np.float64)
+        counts = np.empty(N, np.int32)
+        prob_sum = np.empty(N, np.float64)
+        self.lib.oracle_route(T, N, k, gate_mode, _ptr(r32), _ptr(sb), _ptr(idx),
+                              _ptr(w), _ptr(counts), _ptr(prob_sum))
+        return idx, w, counts, prob_sum
+
+    def permute(self, topk_idx, N):
+        """(offsets [N+1], sorted_pair [T*k], inv_pos [T*k]) int32."""
+        topk_idx = _c(topk_idx, np.int32)
+        T, k = topk_idx.shape
+        offsets = np.empty(N + 1, np.int32)
+        sp = np.empty(T * k, np.int32)
+        inv = np.empty(T * k, np.int32)
+        self.lib.oracle_permute(T, k, N, _ptr(topk_idx), _ptr(offsets), _ptr(sp), _ptr(inv))
+        return offsets, sp, inv
+
+    def expert_swiglu(self, x_row, wg, wu, wd):
+        wdt, wg = _stored(wg)
+        wdt2, wu = _stored(wu)
+        wdt3, wd = _stored(wd)
+        assert wdt == wdt2 == wdt3
+        d_ff, d = wg.shape
+        x_row = _c(x_row, np.float64)
+        out = np.empty(d, np.float64)
+        self.lib.oracle_expert_swiglu(d, d_ff, wdt, _ptr(wg), _ptr(wu), _ptr(wd),
+                                      _ptr(x_row), _ptr(out))
+        return out
+
+    def gated_sum(self, G, E):
+        G = _c(G, np.float64)
+        E = _c(E, np.float64).reshape(G.size, -1)
+        y = np.empty(E.shape[1], np.float64)
+        self.lib.oracle_gated_sum(G.size, E.shape[1], _ptr(G), _ptr(E), _ptr(y))
+        return y
+
+    def layer_rows(self, x, experts, topk_idx, topk_w, rows, N, n_shared=0):
+        """y [len(rows), d] fp64 for the listed tokens. ``experts`` maps an
+        expert index (0..N+n_shared-1; shared ones last) to its (wg, wu, wd)
+        stored arrays; experts no listed token uses may be absent."""
+        xd, x = _stored(x)
+        T, d = x.shape
+        topk_idx = _c(topk_idx, np.int32)
+        topk_w = _c(topk_w, np.float64)
+        k = topk_idx.shape[1]
+        rows = _c(rows, np.int32)
+        E = N + n_shared
+        keep = []
+        tabs = [(_P * E)(), (_P * E)(), (_P * E)()]
+        wdt = None
+        d_ff = None
+        for e, mats in experts.items():
+            for j, m in enumerate(mats):
+                dt, m = _stored(m)
+                wdt = dt if wdt is None else wdt
+                assert dt == wdt
+                keep.append(m)
+                tabs[j][e] = m.ctypes.data
+            d_ff = mats[0].shape[0]
+        y = np.empty((rows.size, d), np.float64)
+        rc = self.lib.oracle_layer_rows(T, d, d_ff, N, k, n_shared, xd, _ptr(x), wdt,
+                                        tabs[0], tabs[1], tabs[2], _ptr(topk_idx),
+                                        _ptr(topk_w), rows.size, _ptr(rows), _ptr(y))
+        if rc != 0:
+            raise ValueError("oracle_layer_rows: a token needs an expert that was not supplied")
+        return y
+
+    def balance_loss(self, f, P, alpha=0.01):
+        f = _c(f, np.float64)
+        P = _c(P, np.float64)
+        return float(self.lib.oracle_balance_loss(f.size, _ptr(f), _ptr(P), alpha))
+
+    def balance_stats(self, counts, prob_sum, T, k, alpha=0.01):
+        """(f, P, aux)."""
+        counts = _c(counts, np.int32)
+        prob_sum = _c(prob_sum, np.float64)
+        N = counts.size
+        f = np.empty(N, np.float64)
+        P = np.empty(N, np.float64)
+        aux = self.lib.oracle_balance_stats(N, T, k, _ptr(counts), _ptr(prob_sum),
+                                            alpha, _ptr(f), _ptr(P))
+        return f, P, float(aux)
+
+    # ---- composition: the full layer for a token subset ---------------------
+    def layer(self, x, w_router, wg, wu, wd, k, gate_mode=GATE_TOPK_SOFTMAX,
+              logit_bias=None, sel_bias=None, n_shared=0, rows=None):
+        """Full forward: router scores for all tokens, routing for all tokens,
+        expert outputs for ``rows`` (all tokens when None). wg/wu/wd are the
+        stacked [N+n_shared, ...] stored arrays (or dicts expert -> array).
+        Returns a dict with r32, topk_idx, topk_w, counts, prob_sum, y."""
+        _, r32 = self.router_logits(x, w_router, logit_bias)
+        idx, w, counts, prob_sum = self.route(r32, k, gate_mode, sel_bias)
+        N = r32.shape[1]
+        T = r32.shape[0]
+        if rows is None:
+            rows = np.arange(T, dtype=np.int32)
+        rows = np.asarray(rows, np.int32)
+        need = sorted(set(idx[rows].ravel().tolist()) | set(range(N, N + n_shared)))
+        experts = {e: (wg[e], wu[e], wd[e]) for e in need}
+        y = self.layer_rows(x, experts, idx, w, rows, N, n_shared)
+        return dict(r32=r32, topk_idx=idx, topk_w=w, counts=counts,
+                    prob_sum=prob_sum, y=y, rows=rows)

@@ -1,0 +1,332 @@
+/*
+ * CPU oracle for the sparse top-k Mixture-of-Experts FFN layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the plain, slow, obviously correct
+ * definition that the CUDA library is checked against. Only the test suite,
+ * the smoke check and the benchmark's CPU-baseline leg may load it. The
+ * product library never links, loads or calls it, and it shares no code,
+ * header or table with the CUDA path.
+ *
+ * Every stored input (bf16 bit patterns or fp32) is widened exactly to fp64
+ * and all arithmetic is done in fp64, one token at a time, in the order the
+ * pages state the method. The only fp32 steps are the ones the routing
+ * decision is defined on: the router score is rounded to fp32 once, and the
+ * selection key is the fp32 sum of that score and the selection bias, so
+ * that both sides of a parity test take the top-k decision in the same
+ * precision.
+ *
+ * Sources (page title, then section):
+ *  [P1] "Mixture of experts and speculative decoding":
+ *       "Following one token through an MoE layer" (steps 1-4),
+ *       "Opening the hood: the MoE layer precisely" (the layer equation),
+ *       "Keeping the experts busy" (the balance-loss equation),
+ *       "A toy MoE layer in PyTorch" (dispatch semantics).
+ *  [P2] "Mixture of Experts and Guided Decoding": the gated-sum example with
+ *       three experts, the dense and sparse four-expert examples, and the
+ *       auxiliary-loss formula with its balanced / collapsed example.
+ *  [P3] "MoE inference: the call centre with 256 specialists and 8 taking
+ *       each call": "The bare mechanism" (router, top-k, normalised weights,
+ *       SwiGLU experts, shared experts, bias-adjusted routing).
+ *
+ * Readings taken where the pages are silent or garbled:
+ *  - The SwiGLU expert is down( SiLU(gate(x)) * up(x) ) without biases; the
+ *    page prints the activation around the product, which is garbled.
+ *  - The selection bias enters only the key used to choose the top k; gate
+ *    weights and the balance statistics use the unbiased router scores.
+ *  - Ties in the selection key go to the lower expert index.
+ *  - Shared experts always run with weight 1 and are not part of f or P.
+ *  - f_i = count_i / (T*k) and P_i = mean over tokens of softmax(r)_i over
+ *    all N routed experts, so both sum to one as in the pages' example.
+ *
+ * Parity unpinned: the SwiGLU expert at realistic sizes has no printed value
+ * on the pages; it is pinned by reduction to library routines (N=1, k=1 is a
+ * plain SwiGLU FFN) and by the dense-with-zeroed-gates brute force, not by a
+ * printed number.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Stored element types of the inputs. */
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F64 = 2 };
+/* Gate modes. */
+enum { ORACLE_GATE_TOPK_SOFTMAX = 0, ORACLE_GATE_ALL_SOFTMAX_RENORM = 1 };
+
+/* Exact widening of one stored element to fp64. A bf16 value is the upper
+ * half of an fp32 bit pattern, so shifting it up gives the fp32 value. */
+static double widen(int dtype, const void* base, size_t i) {
+  if (dtype == ORACLE_F64) return ((const double*)base)[i];
+  if (dtype == ORACLE_F32) return (double)((const float*)base)[i];
+  uint32_t u = (uint32_t)((const uint16_t*)base)[i] << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* softmax(r) over n scores, max-subtracted, fp64. [P1] step 3; [P2] dense
+ * four-expert example. */
+void oracle_softmax(int n, const double* r, double* p) {
+  double m = r[0];
+  for (int i = 1; i < n; ++i)
+    if (r[i] > m) m = r[i];
+  double s = 0.0;
+  for (int i = 0; i < n; ++i) {
+    p[i] = exp(r[i] - m);
+    s += p[i];
+  }
+  for (int i = 0; i < n; ++i) p[i] /= s;
+}
+
+/* Indices of the k largest keys, best first. A key only displaces the
+ * current best when it is strictly larger, so equal keys go to the lower
+ * index. [P1] step 2 and the layer equation's TopK set; [P3] top-k
+ * selection. */
+void oracle_topk(int n, int k, const float* key, int32_t* idx) {
+  char* taken = (char*)calloc((size_t)n, 1);
+  for (int s = 0; s < k; ++s) {
+    int best = -1;
+    for (int i = 0; i < n; ++i) {
+      if (taken[i]) continue;
+      if (best < 0 || key[i] > key[best]) best = i;
+    }
+    idx[s] = best;
+    taken[best] = 1;
+  }
+  free(taken);
+}
+
+/* Gate weights of the kept experts from the unbiased scores r (fp64).
+ *  TOPK_SOFTMAX: softmax over the k kept scores only ([P1] step 3 and the
+ *    layer equation; [P2] sparse example).
+ *  ALL_SOFTMAX_RENORM: softmax over all n scores, then the kept
+ *    probabilities divided by their sum ([P1] step 3's parenthesis; [P3] the
+ *    router's affinity softmax and the renormalised top-k weights). */
+void oracle_gates(int n, int k, int mode, const double* r, const int32_t* idx,
+                  double* g) {
+  if (mode == ORACLE_GATE_TOPK_SOFTMAX) {
+    double* kept = (double*)malloc(sizeof(double) * (size_t)k);
+    for (int s = 0; s < k; ++s) kept[s] = r[idx[s]];
+    oracle_softmax(k, kept, g);
+    free(kept);
+  } else {
+    double* p = (double*)malloc(sizeof(double) * (size_t)n);
+    oracle_softmax(n, r, p);
+    double z = 0.0;
+    for (int s = 0; s < k; ++s) z += p[idx[s]];
+    for (int s = 0; s < k; ++s) g[s] = p[idx[s]] / z;
+    free(p);
+  }
+}
+
+/* Router scores r[t][e] = sum_j x[t][j] * W_r[e][j] + logit_bias[e], fp64.
+ * W_r is stored [N][d] (one row per expert, the linear-layer weight layout
+ * of the pages' toy code). Also writes the scores rounded once to fp32 when
+ * r32 is given: that is the value routing decisions are taken on.
+ * [P1] step 1 and "r = x W_r"; [P3] the router projection. */
+void oracle_router_logits(int T, int d, int N, int xdtype, const void* x,
+                          int wdtype, const void* w_router,
+                          const double* logit_bias, double* r64, float* r32) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    for (int e = 0; e < N; ++e) {
+      double acc = 0.0;
+      for (int j = 0; j < d; ++j)
+        acc += widen(xdtype, x, (size_t)t * d + j) *
+               widen(wdtype, w_router, (size_t)e * d + j);
+      if (logit_bias) acc += logit_bias[e];
+      if (r64) r64[(size_t)t * N + e] = acc;
+      if (r32) r32[(size_t)t * N + e] = (float)acc;
+    }
+  }
+}
+
+/* Routing of T tokens from fp32 scores r32[T][N].
+ *  key = fp32(r + sel_bias) (sel_bias may be NULL); top-k on the key;
+ *  gate weights from the unbiased scores; per-expert counts; and
+ *  prob_sum[e] = sum_t softmax(r_t)[e] over all N experts.
+ * The fp32 sum of two fp32 values is taken as their exact fp64 sum rounded
+ * once to fp32, which is the correctly rounded fp32 sum.
+ * [P1] steps 1-3; [P3] "The bare mechanism" (bias-adjusted routing keeps the
+ * bias out of the weights); [P1] "Keeping the experts busy" for f and P. */
+void oracle_route(int T, int N, int k, int gate_mode, const float* r32,
+                  const float* sel_bias, int32_t* topk_idx, double* topk_w,
+                  int32_t* counts, double* prob_sum) {
+  if (counts) memset(counts, 0, sizeof(int32_t) * (size_t)N);
+  if (prob_sum) memset(prob_sum, 0, sizeof(double) * (size_t)N);
+  float* key = (float*)malloc(sizeof(float) * (size_t)N);
+  double* r = (double*)malloc(sizeof(double) * (size_t)N);
+  double* p = (double*)malloc(sizeof(double) * (size_t)N);
+  for (int t = 0; t < T; ++t) {
+    const float* rt = r32 + (size_t)t * N;
+    for (int e = 0; e < N; ++e) {
+      r[e] = (double)rt[e];
+      key[e] = sel_bias ? (float)((double)rt[e] + (double)sel_bias[e]) : rt[e];
+    }
+    int32_t* it = topk_idx + (size_t)t * k;
+    oracle_topk(N, k, key, it);
+    oracle_gates(N, k, gate_mode, r, it, topk_w + (size_t)t * k);
+    if (counts)
+      for (int s = 0; s < k; ++s) counts[it[s]] += 1;
+    if (prob_sum) {
+      oracle_softmax(N, r, p);
+      for (int e = 0; e < N; ++e) prob_sum[e] += p[e];
+    }
+  }
+  free(key);
+  free(r);
+  free(p);
+}
+
+/* Grouping of the T*k (token, slot) pairs by expert: expert-major, and
+ * within one expert by ascending pair id t*k+slot (a token never picks the
+ * same expert twice, so this is ascending token order). offsets is the
+ * exclusive prefix sum of the per-expert counts, sorted_pair[row] is the
+ * pair id stored at that row, inv_pos[pair] is the row of that pair.
+ * This is the data layout of the toy layer's per-expert dispatch loop
+ * ([P1] "A toy MoE layer in PyTorch"; [P2] sparse MoE code): every token
+ * that chose expert e, and only those, is processed by e. */
+void oracle_permute(int T, int k, int N, const int32_t* topk_idx,
+                    int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos) {
+  int32_t row = 0;
+  for (int e = 0; e < N; ++e) {
+    offsets[e] = row;
+    for (int t = 0; t < T; ++t)
+      for (int s = 0; s < k; ++s)
+        if (topk_idx[(size_t)t * k + s] == e) {
+          int32_t pair = t * k + s;
+          sorted_pair[row] = pair;
+          inv_pos[pair] = row;
+          ++row;
+        }
+  }
+  offsets[N] = row;
+}
+
+/* SiLU(z) = z / (1 + e^-z). */
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* One SwiGLU expert on one token row x[d] (fp64):
+ *   out[c] = sum_j Wd[c][j] * SiLU(sum_i Wg[j][i] x[i]) * (sum_i Wu[j][i] x[i])
+ * Wg and Wu are stored [d_ff][d], Wd is stored [d][d_ff] (linear-layer
+ * layout, output rows). [P3] "The bare mechanism": the dense FFN in SwiGLU
+ * form, read as down(SiLU(gate(x)) * up(x)). */
+void oracle_expert_swiglu(int d, int d_ff, int wdtype, const void* wg,
+                          const void* wu, const void* wd, const double* x,
+                          double* out) {
+  double* h = (double*)malloc(sizeof(double) * (size_t)d_ff);
+  for (int j = 0; j < d_ff; ++j) {
+    double a = 0.0, b = 0.0;
+    for (int i = 0; i < d; ++i) {
+      a += widen(wdtype, wg, (size_t)j * d + i) * x[i];
+      b += widen(wdtype, wu, (size_t)j * d + i) * x[i];
+    }
+    h[j] = silu(a) * b;
+  }
+  for (int c = 0; c < d; ++c) {
+    double acc = 0.0;
+    for (int j = 0; j < d_ff; ++j)
+      acc += widen(wdtype, wd, (size_t)c * d_ff + j) * h[j];
+    out[c] = acc;
+  }
+  free(h);
+}
+
+/* y[c] = sum_i G[i] * E[i][c]: the gate-weighted sum of expert outputs.
+ * [P1] step 4 and the layer equation; [P2] the three-expert example. */
+void oracle_gated_sum(int n_terms, int dim, const double* G, const double* E,
+                      double* y) {
+  for (int c = 0; c < dim; ++c) {
+    double acc = 0.0;
+    for (int i = 0; i < n_terms; ++i) acc += G[i] * E[(size_t)i * dim + c];
+    y[c] = acc;
+  }
+}
+
+/* Layer output for a list of token rows, given the routing:
+ *   y_t = sum_{slot} g[t][slot] * E_{idx[t][slot]}(x_t)
+ *         + sum_{shared s} E_{N+s}(x_t)
+ * Shared experts are stored after the N routed experts and always run with
+ * weight one. wg/wu/wd are per-expert pointer tables of length N+n_shared;
+ * an entry may be NULL when no listed token uses that expert (it is then
+ * never read; a NULL that is needed makes the call return -1).
+ * [P1] layer equation; [P2] sparse MoE; [P3] "The bare mechanism" (shared
+ * experts always run, the routed ones are gate-weighted). */
+int oracle_layer_rows(int T, int d, int d_ff, int N, int k, int n_shared,
+                      int xdtype, const void* x, int wdtype,
+                      const void* const* wg, const void* const* wu,
+                      const void* const* wd, const int32_t* topk_idx,
+                      const double* topk_w, int n_rows, const int32_t* rows,
+                      double* y) {
+  int bad = 0;
+  for (int r = 0; r < n_rows; ++r) {
+    int t = rows[r];
+    if (t < 0 || t >= T) return -1;
+    for (int s = 0; s < k; ++s) {
+      int e = topk_idx[(size_t)t * k + s];
+      if (e < 0 || e >= N || !wg[e] || !wu[e] || !wd[e]) bad = 1;
+    }
+  }
+  for (int s = 0; s < n_shared; ++s)
+    if (!wg[N + s] || !wu[N + s] || !wd[N + s]) bad = 1;
+  if (bad) return -1;
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int r = 0; r < n_rows; ++r) {
+    int t = rows[r];
+    double* xt = (double*)malloc(sizeof(double) * (size_t)d);
+    double* E = (double*)malloc(sizeof(double) * (size_t)(k + n_shared) * d);
+    double* G = (double*)malloc(sizeof(double) * (size_t)(k + n_shared));
+    for (int i = 0; i < d; ++i) xt[i] = widen(xdtype, x, (size_t)t * d + i);
+    for (int s = 0; s < k; ++s) {
+      int e = topk_idx[(size_t)t * k + s];
+      G[s] = topk_w[(size_t)t * k + s];
+      oracle_expert_swiglu(d, d_ff, wdtype, wg[e], wu[e], wd[e], xt,
+                           E + (size_t)s * d);
+    }
+    for (int s = 0; s < n_shared; ++s) {
+      G[k + s] = 1.0;
+      oracle_expert_swiglu(d, d_ff, wdtype, wg[N + s], wu[N + s], wd[N + s],
+                           xt, E + (size_t)(k + s) * d);
+    }
+    oracle_gated_sum(k + n_shared, d, G, E, y + (size_t)r * d);
+    free(xt);
+    free(E);
+    free(G);
+  }
+  return 0;
+}
+
+/* Load-balance term alpha * N * sum_i f_i * P_i. [P1] "Keeping the experts
+ * busy"; [P2] auxiliary-loss formula and its N = 4 example. */
+double oracle_balance_loss(int N, const double* f, const double* P,
+                           double alpha) {
+  double s = 0.0;
+  for (int i = 0; i < N; ++i) s += f[i] * P[i];
+  return alpha * (double)N * s;
+}
+
+/* f_i = counts_i / (T*k), P_i = prob_sum_i / T, and the balance loss built
+ * from them. [P1] "Keeping the experts busy" (f = fraction of tokens sent to
+ * expert i, P = average router probability); with k > 1 a token is counted
+ * once per expert it is sent to, so f sums to one. */
+double oracle_balance_stats(int N, int T, int k, const int32_t* counts,
+                            const double* prob_sum, double alpha, double* f,
+                            double* P) {
+  for (int i = 0; i < N; ++i) {
+    f[i] = (double)counts[i] / ((double)T * (double)k);
+    P[i] = prob_sum[i] / (double)T;
+  }
+  return oracle_balance_loss(N, f, P, alpha);
+}

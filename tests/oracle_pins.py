@@ -1,0 +1,359 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each ``pin_*`` function takes an :class:`oracle.Oracle` and raises
+``AssertionError`` when the oracle disagrees with:
+
+* values the pages print for a worked example (``tests/golden/*.json``, each
+  with its citation),
+* closed forms worked out by hand in the pin,
+* special cases that reduce to a library routine (numpy / torch fp64 matmul,
+  ``torch.nn.functional.silu``, ``torch.topk`` on distinct keys), or
+* brute force on tiny inputs (every expert evaluated densely, unselected ones
+  given weight zero).
+
+``test_oracle_pins.py`` runs them against the real oracle;
+``test_oracle_mutations.py`` runs them against builds of the oracle with one
+planted mistake each and checks that some pin fails for every mistake.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ---------------------------------------------------------------- the pages --
+def pin_worked_example_top2_of_4(o):
+    """Mixture of experts and speculative decoding, 'Following one token
+    through an MoE layer': scores -> kept experts -> weights -> blend."""
+    g = golden("worked_example_top2_of_4.json")
+    tol = g["tolerance"]
+    r32 = np.array([g["scores"]], np.float32)
+    idx, w, counts, _ = o.route(r32, g["k"], gate_mode=0)
+    assert idx[0].tolist() == g["kept_experts_0_based"], idx
+    assert np.allclose(w[0], g["top2_softmax_weights"], atol=tol), w
+    idx2, w2, _, _ = o.route(r32, g["k"], gate_mode=1)
+    assert idx2[0].tolist() == g["kept_experts_0_based"]
+    assert np.allclose(w2[0], g["top2_softmax_weights"], atol=tol), w2
+    p = o.softmax(np.array(g["scores"]))
+    assert np.allclose(p[g["kept_experts_0_based"]], g["all_expert_softmax_of_kept"], atol=tol), p
+    y = o.gated_sum(w[0], np.array(g["expert_outputs_of_kept"]))
+    assert np.allclose(y, g["blend"], atol=tol), y
+    assert counts.tolist() == [1, 0, 1, 0]
+
+
+def pin_dense_and_sparse_4_experts(o):
+    """Mixture of Experts and Guided Decoding: dense softmax over 4 gate
+    scores, and the sparse top-2 weights with zeros elsewhere."""
+    g = golden("dense_and_sparse_4_experts.json")
+    s = np.array(g["scores"])
+    p = o.softmax(s)
+    assert np.allclose(p, g["dense_softmax_printed"], atol=g["dense_softmax_tolerance"]), p
+    idx, w, _, _ = o.route(np.array([s], np.float32), g["k"], gate_mode=0)
+    dense = np.zeros(s.size)
+    dense[idx[0]] = w[0]
+    assert np.allclose(dense, g["sparse_weights_printed"], atol=g["sparse_tolerance"]), dense
+
+
+def pin_gated_sum_3_experts(o):
+    """Mixture of Experts and Guided Decoding: 0.5*2 + 0.3*4 + 0.2*0 = 2.2."""
+    g = golden("gated_sum_3_experts.json")
+    y = o.gated_sum(np.array(g["gates"]), np.array(g["expert_outputs"])[:, None])
+    assert abs(y[0] - g["output"]) <= g["tolerance"], y
+
+
+def pin_balance_loss_n4(o):
+    """Balanced routing gives 1.0*alpha, the collapsed one 2.8*alpha, both
+    from the printed f and P and realised as actual routings of 4 tokens."""
+    g = golden("balance_loss_n4.json")
+    a, tol = g["alpha"], g["tolerance"]
+    for case in ("balanced", "collapsed"):
+        c = g[case]
+        loss = o.balance_loss(c["f"], c["P"], a)
+        assert abs(loss - c["loss_over_alpha"] * a) <= tol, (case, loss)
+    # Realised: token t strongly prefers expert t (k = 1); by symmetry every
+    # expert gets one token and mean probability exactly 1/4.
+    r = np.full((4, 4), -3.0, np.float32)
+    np.fill_diagonal(r, 2.0)
+    idx, _, counts, ps = o.route(r, 1)
+    f, P, aux = o.balance_stats(counts, ps, 4, 1, a)
+    assert idx[:, 0].tolist() == [0, 1, 2, 3]
+    assert np.allclose(f, 0.25, atol=1e-15) and np.allclose(P, 0.25, atol=1e-9)
+    assert abs(aux - 1.0 * a) <= 1e-9, aux
+    # Collapsed: every token has softmax [0.7, 0.1, 0.1, 0.1] and picks 0.
+    r = np.tile(np.log(np.array([0.7, 0.1, 0.1, 0.1])), (4, 1)).astype(np.float32)
+    idx, _, counts, ps = o.route(r, 1)
+    f, P, aux = o.balance_stats(counts, ps, 4, 1, a)
+    assert idx[:, 0].tolist() == [0, 0, 0, 0]
+    assert np.allclose(f, [1, 0, 0, 0]) and np.allclose(P, [0.7, 0.1, 0.1, 0.1], atol=1e-6)
+    assert abs(aux - 2.8 * a) <= 1e-7, aux
+
+
+# ------------------------------------------------------------- closed forms --
+def pin_renormalised_all_softmax_equals_topk_softmax(o):
+    """Softmax over all N then renormalising the kept k equals the softmax
+    over the kept k (exact identity; equal up to rounding)."""
+    rng = _rng(1)
+    r = rng.normal(0, 2, (50, 16)).astype(np.float32)
+    for k in (1, 2, 5, 16):
+        i0, w0, _, _ = o.route(r, k, gate_mode=0)
+        i1, w1, _, _ = o.route(r, k, gate_mode=1)
+        assert (i0 == i1).all()
+        assert np.allclose(w0, w1, atol=1e-12, rtol=0), np.abs(w0 - w1).max()
+        assert np.allclose(w0.sum(1), 1.0, atol=1e-12)
+
+
+def pin_tie_break_lower_index(o):
+    """Equal keys go to the lower expert index; slots are ordered best first."""
+    key = np.array([1.0, 3.0, 3.0, 2.0, 3.0], np.float32)
+    assert o.topk(key, 2).tolist() == [1, 2]
+    assert o.topk(key, 4).tolist() == [1, 2, 4, 3]
+    assert o.topk(np.zeros(6, np.float32), 3).tolist() == [0, 1, 2]
+    # -0.0 and +0.0 compare equal, so they tie as well
+    assert o.topk(np.array([-0.0, 0.0], np.float32), 1).tolist() == [0]
+
+
+def pin_selection_bias_chooses_but_does_not_weigh(o):
+    """A selection bias changes which experts are chosen, not their weights:
+    scores [2.0, 0.5, 1.5, -1.0] with +1.2 on expert 1 keep experts {0, 1},
+    weighted by the softmax of the unbiased scores [2.0, 0.5]."""
+    r = np.array([[2.0, 0.5, 1.5, -1.0]], np.float32)
+    sb = np.array([0.0, 1.2, 0.0, 0.0], np.float32)
+    e = math.exp(1.5)
+    for mode in (0, 1):
+        idx, w, _, ps = o.route(r, 2, gate_mode=mode, sel_bias=sb)
+        assert idx[0].tolist() == [0, 1], idx
+        assert np.allclose(w[0], [e / (1 + e), 1 / (1 + e)], atol=1e-7), w
+        # P_i uses the unbiased scores too
+        assert np.allclose(ps, o.softmax(r[0].astype(np.float64)), atol=1e-15)
+
+
+def pin_router_logits_small(o):
+    """r = x W_r^T + logit_bias, worked by hand: x = [1, 2], rows of W_r
+    [1, 0], [0, 1], [1, 1], [-2, 0.5] -> [1, 2, 3, -1], plus the bias."""
+    x = np.array([[1.0, 2.0]], np.float32)
+    W = np.array([[1, 0], [0, 1], [1, 1], [-2, 0.5]], np.float32)
+    lb = np.array([0.5, -0.25, 0.0, 4.0])
+    r64, r32 = o.router_logits(x, W, lb)
+    assert r64[0].tolist() == [1.5, 1.75, 3.0, 3.0]
+    assert r32.dtype == np.float32 and r32[0].tolist() == [1.5, 1.75, 3.0, 3.0]
+    # bf16 inputs are read from their bit patterns: 0x3F80 = 1.0,
+    # 0xC000 = -2.0, 0x3E20 = 0.15625, 0xBF40 = -0.75
+    xb = np.array([[0x3F80, 0xC000]], np.uint16)
+    Wb = np.array([[0x3E20, 0xBF40]], np.uint16)
+    r64, _ = o.router_logits(xb, Wb)
+    assert r64[0, 0] == 1.0 * 0.15625 + (-2.0) * (-0.75)
+
+
+def pin_permute_small(o):
+    """Pairs grouped by expert, ascending pair id inside an expert, worked
+    by hand for topk_idx [[1,0],[1,2],[0,2]] (pair ids 0..5)."""
+    off, sp, inv = o.permute(np.array([[1, 0], [1, 2], [0, 2]]), 3)
+    assert off.tolist() == [0, 2, 4, 6]
+    assert sp.tolist() == [1, 4, 0, 2, 3, 5]
+    assert inv.tolist() == [2, 0, 3, 4, 1, 5]
+    off, sp, inv = o.permute(np.zeros((0, 2), np.int32), 3)
+    assert off.tolist() == [0, 0, 0, 0] and sp.size == 0
+
+
+# ---------------------------------------------------- library reductions ------
+def _torch_swiglu(x, wg, wu, wd):
+    x, wg, wu, wd = (torch.from_numpy(np.asarray(a, np.float64)) for a in (x, wg, wu, wd))
+    return (torch.nn.functional.silu(x @ wg.T) * (x @ wu.T)) @ wd.T
+
+
+def pin_router_logits_match_matmul(o):
+    rng = _rng(2)
+    x = rng.normal(0, 1, (20, 24)).astype(np.float32)
+    W = rng.normal(0, 0.5, (7, 24)).astype(np.float32)
+    lb = rng.normal(0, 1, 7)
+    r64, r32 = o.router_logits(x, W, lb)
+    ref = x.astype(np.float64) @ W.astype(np.float64).T + lb
+    assert np.allclose(r64, ref, atol=1e-12, rtol=0)
+    assert (r32 == ref.astype(np.float32)).all()
+
+
+def pin_route_matches_library(o):
+    """Distinct keys: top-k equals torch.topk (sorted, descending); counts
+    equal bincount; prob_sum equals the summed library softmax."""
+    rng = _rng(3)
+    r = rng.normal(0, 1, (200, 32)).astype(np.float32)
+    for k in (1, 2, 8):
+        idx, w, counts, ps = o.route(r, k)
+        tv, ti = torch.topk(torch.from_numpy(r), k, dim=1, sorted=True)
+        assert (idx == ti.numpy()).all()
+        ref_w = torch.softmax(tv.double(), dim=1).numpy()
+        assert np.allclose(w, ref_w, atol=1e-13)
+        assert (counts == np.bincount(idx.ravel(), minlength=32)).all()
+        ref_ps = torch.softmax(torch.from_numpy(r).double(), dim=1).sum(0).numpy()
+        assert np.allclose(ps, ref_ps, atol=1e-12)
+
+
+def pin_expert_swiglu_matches_library(o):
+    """One expert = silu(x Wg^T) * (x Wu^T) then Wd^T; d != d_ff so a
+    transposed operand cannot pass."""
+    rng = _rng(4)
+    d, dff = 12, 20
+    x = rng.normal(0, 1, d)
+    wg, wu = rng.normal(0, 0.5, (2, dff, d)).astype(np.float32)
+    wd = rng.normal(0, 0.5, (d, dff)).astype(np.float32)
+    out = o.expert_swiglu(x, wg, wu, wd)
+    ref = _torch_swiglu(x[None], wg, wu, wd)[0].numpy()
+    assert np.allclose(out, ref, atol=1e-12, rtol=0), np.abs(out - ref).max()
+
+
+def pin_single_expert_layer_is_plain_ffn(o):
+    """N = 1, k = 1: the layer is one SwiGLU FFN with weight 1."""
+    rng = _rng(5)
+    T, d, dff = 6, 8, 16
+    x = rng.normal(0, 1, (T, d)).astype(np.float32)
+    Wr = rng.normal(0, 1, (1, d)).astype(np.float32)
+    wg, wu = rng.normal(0, 0.5, (2, 1, dff, d)).astype(np.float32)
+    wd = rng.normal(0, 0.5, (1, d, dff)).astype(np.float32)
+    out = o.layer(x, Wr, wg, wu, wd, k=1)
+    ref = _torch_swiglu(x, wg[0], wu[0], wd[0]).numpy()
+    assert np.allclose(out["y"], ref, atol=1e-12, rtol=0)
+    assert np.allclose(out["topk_w"], 1.0)
+
+
+def pin_k_equals_n_is_dense_softmax_moe(o):
+    """k = N with the top-k softmax is the dense MoE: every expert runs,
+    weighted by the softmax over all scores."""
+    rng = _rng(6)
+    T, d, dff, N = 5, 8, 12, 4
+    x = rng.normal(0, 1, (T, d)).astype(np.float32)
+    Wr = rng.normal(0, 1, (N, d)).astype(np.float32)
+    wg, wu = rng.normal(0, 0.5, (2, N, dff, d)).astype(np.float32)
+    wd = rng.normal(0, 0.5, (N, d, dff)).astype(np.float32)
+    out = o.layer(x, Wr, wg, wu, wd, k=N)
+    r = torch.from_numpy(x).double() @ torch.from_numpy(Wr).double().T
+    G = torch.softmax(r.float().double(), dim=1)
+    ref = sum(G[:, e:e + 1] * _torch_swiglu(x, wg[e], wu[e], wd[e]) for e in range(N))
+    assert np.allclose(out["y"], ref.numpy(), atol=1e-12, rtol=0)
+
+
+# ------------------------------------------------------------- brute force ----
+def _brute_force_layer(x, Wr, wg, wu, wd, k, N, n_shared, mode, lb=None, sb=None):
+    """Dense evaluation: every expert on every token; the routed ones
+    weighted by a length-N gate vector that is zero off the top-k."""
+    xt = torch.from_numpy(np.asarray(x, np.float64))
+    r = xt @ torch.from_numpy(np.asarray(Wr, np.float64)).T
+    if lb is not None:
+        r = r + torch.from_numpy(np.asarray(lb, np.float64))
+    r32 = r.float()
+    key = r32 + (torch.from_numpy(np.asarray(sb, np.float32)) if sb is not None else 0)
+    T = xt.shape[0]
+    y = torch.zeros(T, xt.shape[1], dtype=torch.float64)
+    for t in range(T):
+        # rank experts by (key desc, index asc) without a sort routine
+        order = sorted(range(N), key=lambda e: (-float(key[t, e]), e))[:k]
+        rt = r32[t].double()
+        G = torch.zeros(N, dtype=torch.float64)
+        if mode == 0:
+            z = sum(math.exp(float(rt[e]) - float(rt[order].max())) for e in order)
+            for e in order:
+                G[e] = math.exp(float(rt[e]) - float(rt[order].max())) / z
+        else:
+            p = torch.softmax(rt, 0)
+            for e in order:
+                G[e] = p[e] / p[order].sum()
+        for e in range(N):
+            y[t] += G[e] * _torch_swiglu(xt[t:t + 1].numpy(), wg[e], wu[e], wd[e])[0]
+        for s in range(n_shared):
+            y[t] += _torch_swiglu(xt[t:t + 1].numpy(), wg[N + s], wu[N + s], wd[N + s])[0]
+    return y.numpy()
+
+
+def pin_brute_force_dense_with_zeroed_gates(o):
+    rng = _rng(7)
+    T, d, dff, N, k, s = 7, 10, 6, 6, 2, 1
+    for mode in (0, 1):
+        x = rng.normal(0, 1, (T, d)).astype(np.float32)
+        Wr = rng.normal(0, 1, (N, d)).astype(np.float32)
+        lb = rng.normal(0, 0.5, N)
+        sb = rng.uniform(-0.3, 0.3, N).astype(np.float32)
+        wg, wu = rng.normal(0, 0.5, (2, N + s, dff, d)).astype(np.float32)
+        wd = rng.normal(0, 0.5, (N + s, d, dff)).astype(np.float32)
+        out = o.layer(x, Wr, wg, wu, wd, k=k, gate_mode=mode, logit_bias=lb,
+                      sel_bias=sb, n_shared=s)
+        ref = _brute_force_layer(x, Wr, wg, wu, wd, k, N, s, mode, lb, sb)
+        assert np.allclose(out["y"], ref, atol=1e-12, rtol=0), np.abs(out["y"] - ref).max()
+
+
+# -------------------------------------------------------------- invariants ---
+def pin_permute_invariants(o):
+    rng = _rng(8)
+    T, N, k = 300, 9, 3
+    idx = np.stack([rng.permutation(N)[:k] for _ in range(T)]).astype(np.int32)
+    off, sp, inv = o.permute(idx, N)
+    P = T * k
+    assert off[0] == 0 and off[-1] == P and (np.diff(off) >= 0).all()
+    assert (np.diff(off) == np.bincount(idx.ravel(), minlength=N)).all()
+    assert sorted(sp.tolist()) == list(range(P))
+    assert (inv[sp] == np.arange(P)).all()
+    flat = idx.ravel()
+    for e in range(N):
+        seg = sp[off[e]:off[e + 1]]
+        assert (flat[seg] == e).all() and (np.diff(seg) > 0).all()
+
+
+def pin_expert_relabelling_is_equivariant(o):
+    """Relabelling the experts (router rows, biases and weights together)
+    relabels topk_idx and counts the same way and leaves y unchanged."""
+    rng = _rng(9)
+    T, d, dff, N, k = 9, 8, 6, 5, 2
+    x = rng.normal(0, 1, (T, d)).astype(np.float32)
+    Wr = rng.normal(0, 1, (N, d)).astype(np.float32)
+    lb = rng.normal(0, 0.5, N)
+    sb = rng.uniform(-0.2, 0.2, N).astype(np.float32)
+    wg, wu = rng.normal(0, 0.5, (2, N, dff, d)).astype(np.float32)
+    wd = rng.normal(0, 0.5, (N, d, dff)).astype(np.float32)
+    a = o.layer(x, Wr, wg, wu, wd, k, 1, lb, sb)
+    perm = rng.permutation(N)            # new expert j is old expert perm[j]
+    b = o.layer(x, Wr[perm], wg[perm], wu[perm], wd[perm], k, 1, lb[perm], sb[perm])
+    assert (perm[b["topk_idx"]] == a["topk_idx"]).all()
+    assert (b["counts"] == a["counts"][perm]).all()
+    assert np.allclose(a["y"], b["y"], atol=1e-12)
+
+
+def pin_shared_expert_always_runs_with_weight_one(o):
+    """Adding a shared expert adds exactly its plain FFN output."""
+    rng = _rng(10)
+    T, d, dff, N, k = 4, 8, 6, 3, 1
+    x = rng.normal(0, 1, (T, d)).astype(np.float32)
+    Wr = rng.normal(0, 1, (N, d)).astype(np.float32)
+    wg, wu = rng.normal(0, 0.5, (2, N + 1, dff, d)).astype(np.float32)
+    wd = rng.normal(0, 0.5, (N + 1, d, dff)).astype(np.float32)
+    a = o.layer(x, Wr, wg[:N], wu[:N], wd[:N], k)
+    b = o.layer(x, Wr, wg, wu, wd, k, n_shared=1)
+    ref = _torch_swiglu(x, wg[N], wu[N], wd[N]).numpy()
+    assert np.allclose(b["y"] - a["y"], ref, atol=1e-12)
+    assert (b["counts"] == a["counts"]).all()
+
+
+def pin_balance_stats_sum_to_one(o):
+    rng = _rng(11)
+    T, N, k = 64, 8, 2
+    r = rng.normal(0, 1, (T, N)).astype(np.float32)
+    _, _, counts, ps = o.route(r, k)
+    f, P, aux = o.balance_stats(counts, ps, T, k, 0.01)
+    assert abs(f.sum() - 1) < 1e-12 and abs(P.sum() - 1) < 1e-12
+    assert abs(aux - 0.01 * N * (f * P).sum()) < 1e-15
+    assert counts.sum() == T * k
+
+
+ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]

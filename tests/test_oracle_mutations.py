@@ -1,0 +1,62 @@
+"""Planted mistakes: each case copies the oracle's C source, changes one
+expression into a plausible mistake (a dropped term, a wrong sign, index or
+operand order), builds it on the CPU and checks that at least one pin in
+``oracle_pins.py`` rejects that build. This shows the pins constrain every
+part of the oracle rather than restating it."""
+import os
+import tempfile
+
+import pytest
+
+import oracle as oracle_pkg
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle_pkg.__file__), "moe_oracle.c")
+
+# (name, exact text in the source, replacement). Each original must occur
+# exactly once.
+MUTATIONS = [
+    ("silu_on_up_branch", "h[j] = silu(a) * b;", "h[j] = a * silu(b);"),
+    ("silu_sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    ("down_weight_transposed", "widen(wdtype, wd, (size_t)c * d_ff + j)", "widen(wdtype, wd, (size_t)j * d + c)"),
+    ("gate_weight_transposed", "a += widen(wdtype, wg, (size_t)j * d + i) * x[i];", "a += widen(wdtype, wg, (size_t)i * d_ff + j) * x[i];"),
+    ("router_weight_transposed", "widen(wdtype, w_router, (size_t)e * d + j)", "widen(wdtype, w_router, (size_t)j * N + e)"),
+    ("tie_to_higher_index", "if (best < 0 || key[i] > key[best]) best = i;", "if (best < 0 || key[i] >= key[best]) best = i;"),
+    ("softmax_sign", "p[i] = exp(r[i] - m);", "p[i] = exp(m - r[i]);"),
+    ("selection_bias_in_gates", "r[e] = (double)rt[e];", "r[e] = (double)rt[e] + (sel_bias ? (double)sel_bias[e] : 0.0);"),
+    ("logit_bias_dropped", "if (logit_bias) acc += logit_bias[e];", ""),
+    ("no_renormalisation", "g[s] = p[idx[s]] / z;", "g[s] = p[idx[s]];"),
+    ("shared_expert_dropped", "G[k + s] = 1.0;", "G[k + s] = 0.0;"),
+    ("permute_descending_tokens", "for (int t = 0; t < T; ++t)\n      for (int s = 0; s < k; ++s)\n        if (topk_idx", "for (int t = T - 1; t >= 0; --t)\n      for (int s = 0; s < k; ++s)\n        if (topk_idx"),
+    ("balance_loss_without_N", "return alpha * (double)N * s;", "return alpha * s;"),
+    ("f_over_tokens_not_assignments", "f[i] = (double)counts[i] / ((double)T * (double)k);", "f[i] = (double)counts[i] / (double)T;"),
+    ("gated_sum_transposed", "acc += G[i] * E[(size_t)i * dim + c];", "acc += G[i] * E[(size_t)c * n_terms + i];"),
+    ("prob_sum_from_gates", "for (int e = 0; e < N; ++e) prob_sum[e] += p[e];", "for (int s = 0; s < k; ++s) prob_sum[it[s]] += topk_w[(size_t)t * k + s];"),
+    ("bf16_widen_wrong_half", "uint32_t u = (uint32_t)((const uint16_t*)base)[i] << 16;", "uint32_t u = (uint32_t)((const uint16_t*)base)[i];"),
+    ("selection_ignores_bias", "key[e] = sel_bias ? (float)((double)rt[e] + (double)sel_bias[e]) : rt[e];", "key[e] = rt[e];"),
+]
+
+
+def _all_pins_pass(o):
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(o)
+        except Exception as e:  # a crash in a mutant counts as a failed pin
+            failed.append((pin.__name__, type(e).__name__))
+    return failed
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} must occur exactly once"
+    with tempfile.TemporaryDirectory() as tmp:
+        c = os.path.join(tmp, "mutant.c")
+        so = os.path.join(tmp, "libmutant.so")
+        with open(c, "w") as f:
+            f.write(src.replace(old, new))
+        oracle_pkg.compile_oracle(c, so)
+        o = oracle_pkg.Oracle(oracle_pkg.load(so))
+        failed = _all_pins_pass(o)
+    assert failed, f"no pin caught the planted mistake {name}"
