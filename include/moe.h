@@ -1,0 +1,284 @@
+/*
+ * moe.h - C ABI of libmoe.so: the sparse top-k Mixture-of-Experts FFN layer
+ * forward on one GB300 (sm_103a).
+ *
+ * The layer, for each token row x (d_model values):
+ *   r = x W_r^T (+ logit_bias)                  router scores, one per expert
+ *   TopK = the k experts with the largest r + sel_bias
+ *   g = softmax over the kept scores            (or: softmax over all N
+ *                                                scores, kept ones renormalised)
+ *   y = sum_{i in TopK} g_i E_i(x) + sum_{shared s} E_s(x)
+ *   E(x) = W_down ( SiLU(W_gate x) * (W_up x) )  (SwiGLU expert, no biases)
+ * Sources: "Mixture of experts and speculative decoding", sections
+ * "Following one token through an MoE layer" and "Opening the hood: the MoE
+ * layer precisely"; "Mixture of Experts and Guided Decoding", the sparse
+ * top-k example; "MoE inference: the call centre with 256 specialists and 8
+ * taking each call", section "The bare mechanism" (SwiGLU experts, shared
+ * experts, bias-adjusted routing).
+ *
+ * Conventions for every entry point below:
+ *  - Pointers marked [device] are device pointers owned by the caller. The
+ *    library never allocates, frees or synchronises device memory except
+ *    where a function says it synchronises (moe_stream_status,
+ *    moe_profile_collect).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and returns before it runs.
+ *  - Row-major layouts. Weights follow the linear-layer convention [out][in]:
+ *    w_router [N][d_model]; w_gate, w_up [N+n_shared][d_ff][d_model];
+ *    w_down [N+n_shared][d_model][d_ff]; shared experts are stored after
+ *    the N routed experts in the same arrays.
+ *  - Element type of x, the weights, x_perm, y_perm and y is cfg->dtype
+ *    (fp32, or bf16 stored as its 16-bit pattern). Router scores, gate
+ *    weights, biases and statistics are always fp32; indices are int32.
+ *  - Every device pointer must be 16-byte aligned, and a workspace 256-byte
+ *    aligned; otherwise MOE_ERR_MISALIGNED and nothing is launched.
+ *  - Host-side argument errors return a negative status and launch nothing.
+ *    Errors found on the device while the work runs (an expert index out of
+ *    range, a wait that timed out) are recorded in a status word at the
+ *    start of the workspace and read back by moe_stream_status().
+ *  - T = 0 is valid: nothing is launched except zeroing the outputs that
+ *    are sums (counts, prob_sum).
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+
+/* Status codes. */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)  /* NULL pointer, bad shape or bad enum      */
+#define MOE_ERR_UNSUPPORTED (-2)  /* valid but not built: see moe_check_config */
+#define MOE_ERR_MISALIGNED (-3)   /* a pointer is not 16-byte (ws: 256) aligned */
+#define MOE_ERR_WORKSPACE (-4)    /* ws_bytes smaller than the *_workspace_size */
+#define MOE_ERR_CUDA (-5)         /* a CUDA call failed; see moe_last_cuda_error */
+#define MOE_ERR_TIMEOUT (-6)      /* a bounded device wait ran out              */
+#define MOE_ERR_DEVICE_CHECK (-7) /* a device-side input check failed          */
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef enum {
+  /* g = softmax over the k kept scores ("Mixture of experts and speculative
+   * decoding", step 3 and the layer equation). */
+  MOE_GATE_TOPK_SOFTMAX = 0,
+  /* g = softmax over all N scores, kept probabilities divided by their sum
+   * (same page, step 3's alternative; "MoE inference ...", "The bare
+   * mechanism"). Equal to the above up to rounding. */
+  MOE_GATE_ALL_SOFTMAX_RENORM = 1
+} moe_gate_mode;
+
+typedef struct moe_config {
+  int32_t T;         /* tokens in this call, >= 0                             */
+  int32_t d_model;   /* >= 8, multiple of 8                                   */
+  int32_t n_experts; /* N routed experts, 1..256                              */
+  int32_t top_k;     /* k, 1..min(N, 8)                                       */
+  int32_t n_shared;  /* shared (always-run) experts, 0..4; use d_ff too       */
+  int32_t d_ff;      /* expert hidden width, >= 8, multiple of 8              */
+  int32_t dtype;     /* moe_dtype                                             */
+  int32_t gate_mode; /* moe_gate_mode                                         */
+} moe_config;
+
+/* Library version (major*10000 + minor*100 + patch). */
+MOE_API int moe_version(void);
+
+/* Text for a status code. Never NULL. */
+MOE_API const char* moe_status_string(int status);
+
+/* The cudaError_t of the most recent MOE_ERR_CUDA on the calling thread. */
+MOE_API int moe_last_cuda_error(void);
+
+/* Host-only validation of a configuration against the limits above; touches
+ * no GPU. MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED. */
+MOE_API int moe_check_config(const moe_config* cfg);
+
+/* Workspace bytes each entry point needs (0 if cfg is invalid). The
+ * workspace is caller-owned device memory, 256-byte aligned; its contents
+ * need not be initialised and are clobbered. */
+MOE_API size_t moe_router_workspace_size(const moe_config* cfg);
+MOE_API size_t moe_permute_workspace_size(const moe_config* cfg);
+MOE_API size_t moe_grouped_workspace_size(const moe_config* cfg);
+MOE_API size_t moe_workspace_size(const moe_config* cfg); /* moe_layer_forward */
+
+/*
+ * Router scores, top-k selection, gate weights and the per-expert
+ * statistics of the balance loss, for T tokens.
+ * ("Mixture of experts and speculative decoding", steps 1-3 and section
+ * "Keeping the experts busy"; "MoE inference ...", "The bare mechanism".)
+ *
+ *  x          [device] [T][d_model] cfg->dtype. Ignored when logits_in is set.
+ *  w_router   [device] [N][d_model] cfg->dtype. Ignored when logits_in is set.
+ *  logit_bias [device] [N] fp32 or NULL: added to every token's scores
+ *             (it moves selection, gate weights and P alike).
+ *  sel_bias   [device] [N] fp32 or NULL: added only to the key the top-k is
+ *             chosen on, key = fp32(r + sel_bias); never enters g or P.
+ *  logits_in  [device] [T][N] fp32 or NULL: when set, these are the scores
+ *             r verbatim (no GEMM; logit_bias must then be NULL).
+ *  logits_out [device] [T][N] fp32 or NULL: receives r.
+ *  topk_idx   [device] [T][k] int32 out: experts by descending key, equal
+ *             keys ordered by lower index.
+ *  topk_w     [device] [T][k] fp32 out: gate weights (cfg->gate_mode).
+ *  counts     [device] [N] int32 out: tokens routed to each expert.
+ *  prob_sum   [device] [N] fp32 out: sum over tokens of softmax(r) over all
+ *             N experts (P_i = prob_sum_i / T). Summed in a fixed order, so
+ *             repeated calls give identical bits.
+ *  ws         [device] moe_router_workspace_size(cfg) bytes.
+ */
+MOE_API int moe_router_topk(const moe_config* cfg, const void* x, const void* w_router,
+                    const float* logit_bias, const float* sel_bias,
+                    const float* logits_in, float* logits_out,
+                    int32_t* topk_idx, float* topk_w, int32_t* counts,
+                    float* prob_sum, void* ws, size_t ws_bytes,
+                    moe_stream_t stream);
+
+/*
+ * Groups the T*k (token, slot) pairs by expert and gathers their token rows.
+ * Pair p = t*k + slot. Rows are expert-major; inside one expert, ascending
+ * pair id (a token cannot pick an expert twice, so ascending token). This
+ * is the batched form of the per-expert dispatch loop of the pages' toy
+ * layers ("Mixture of experts and speculative decoding", "A toy MoE layer
+ * in PyTorch"; "Mixture of Experts and Guided Decoding", sparse MoE code).
+ * The result is unique, so it is bit-exact and deterministic.
+ *
+ *  x              [device] [T][d_model] cfg->dtype.
+ *  topk_idx       [device] [T][k] int32, each in [0, N). An index out of
+ *                 range sets MOE_ERR_DEVICE_CHECK in the workspace status;
+ *                 that pair is then left out and the outputs are undefined.
+ *  expert_offsets [device] [N+1] int32 out: exclusive prefix sum of the
+ *                 per-expert pair counts; expert_offsets[N] = T*k.
+ *  sorted_pair    [device] [T*k] int32 out: pair id stored at each row.
+ *  inv_pos        [device] [T*k] int32 out: row of each pair id.
+ *  x_perm         [device] [T*k][d_model] cfg->dtype out: x_perm[row] =
+ *                 x[sorted_pair[row] / k], byte for byte.
+ *  ws             [device] moe_permute_workspace_size(cfg) bytes.
+ */
+MOE_API int moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                int32_t* expert_offsets, int32_t* sorted_pair,
+                int32_t* inv_pos, void* x_perm, void* ws, size_t ws_bytes,
+                moe_stream_t stream);
+
+/*
+ * Every expert's SwiGLU FFN over its rows, for all experts in one pass:
+ * routed expert e over x_perm rows [expert_offsets[e], expert_offsets[e+1]),
+ * and each shared expert s over all T rows of x.
+ *   y_perm[row] = w_row * W_down[e] ( SiLU(W_gate[e] a) * (W_up[e] a) )
+ * where a is the row's input, w_row = topk_w[sorted_pair[row]] for routed
+ * rows when topk_w is given, else 1. ("MoE inference ...", "The bare
+ * mechanism": SwiGLU experts, shared experts; "Mixture of experts and
+ * speculative decoding", layer equation.)
+ * bf16: gate/up and down run on the tcgen05 tensor cores (bf16 operands,
+ * fp32 accumulation), the SwiGLU hidden row is rounded to bf16 once.
+ * fp32: CUDA-core fp32 throughout.
+ *
+ *  x_perm         [device] [T*k][d_model] cfg->dtype (from moe_permute).
+ *  x              [device] [T][d_model] cfg->dtype: input of shared experts
+ *                 (may be NULL when n_shared = 0).
+ *  expert_offsets [device] [N+1] int32 (from moe_permute).
+ *  sorted_pair    [device] [T*k] int32 (from moe_permute); may be NULL when
+ *                 topk_w is NULL.
+ *  topk_w         [device] [T][k] fp32 or NULL (then rows are unweighted).
+ *  w_gate, w_up   [device] [N+n_shared][d_ff][d_model] cfg->dtype.
+ *  w_down         [device] [N+n_shared][d_model][d_ff] cfg->dtype.
+ *  y_perm         [device] [T*k + n_shared*T][d_model] cfg->dtype out:
+ *                 routed rows first (x_perm order), then shared expert s at
+ *                 rows T*k + s*T + t.
+ *  ws             [device] moe_grouped_workspace_size(cfg) bytes (holds the
+ *                 SwiGLU hidden rows).
+ */
+MOE_API int moe_grouped_swiglu(const moe_config* cfg, const void* x_perm,
+                       const void* x, const int32_t* expert_offsets,
+                       const int32_t* sorted_pair, const float* topk_w,
+                       const void* w_gate, const void* w_up,
+                       const void* w_down, void* y_perm, void* ws,
+                       size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * The gate-weighted sum back into token order, without atomics: each output
+ * element is written once, summing in fp32 over slots 0..k-1 in order and
+ * then the shared experts in order.
+ *   y[t] = sum_slot w * y_perm[inv_pos[t*k+slot]] + sum_s y_perm[T*k+s*T+t]
+ * with w = topk_w[t*k+slot] when topk_w is given, else 1 (rows already
+ * weighted by moe_grouped_swiglu).
+ * ("Mixture of experts and speculative decoding", step 4; "Mixture of
+ * Experts and Guided Decoding", the three-expert gated sum.)
+ *
+ *  y_perm  [device] [T*k + n_shared*T][d_model] cfg->dtype.
+ *  inv_pos [device] [T*k] int32 (from moe_permute). An entry outside
+ *          [0, T*k) contributes zero.
+ *  topk_w  [device] [T][k] fp32 or NULL.
+ *  y       [device] [T][d_model] cfg->dtype out.
+ */
+MOE_API int moe_combine(const moe_config* cfg, const void* y_perm,
+                const int32_t* inv_pos, const float* topk_w, void* y,
+                moe_stream_t stream);
+
+/*
+ * The whole layer: moe_router_topk, moe_permute, moe_grouped_swiglu (rows
+ * weighted by their gate) and moe_combine, enqueued back to back with no
+ * host synchronisation.
+ *
+ *  x, w_router, logit_bias, sel_bias: as moe_router_topk.
+ *  w_gate, w_up, w_down: as moe_grouped_swiglu.
+ *  y        [device] [T][d_model] cfg->dtype out.
+ *  topk_idx [device] [T][k] int32 out, or NULL.
+ *  topk_w   [device] [T][k] fp32 out, or NULL.
+ *  counts   [device] [N] int32 out, or NULL.
+ *  prob_sum [device] [N] fp32 out, or NULL.
+ *  ws       [device] moe_workspace_size(cfg) bytes.
+ */
+MOE_API int moe_layer_forward(const moe_config* cfg, const void* x,
+                      const void* w_router, const float* logit_bias,
+                      const float* sel_bias, const void* w_gate,
+                      const void* w_up, const void* w_down, void* y,
+                      int32_t* topk_idx, float* topk_w, int32_t* counts,
+                      float* prob_sum, void* ws, size_t ws_bytes,
+                      moe_stream_t stream);
+
+/*
+ * The load-balance statistics on the device: f_i = counts_i / (T*k),
+ * P_i = prob_sum_i / T and aux = alpha * N * sum_i f_i P_i (one fixed-order
+ * sum). ("Mixture of experts and speculative decoding", "Keeping the
+ * experts busy"; "Mixture of Experts and Guided Decoding", auxiliary loss.)
+ *
+ *  counts   [device] [N] int32;  prob_sum [device] [N] fp32.
+ *  f, P     [device] [N] fp32 out;  aux [device] [1] fp32 out.
+ * With T = 0 all outputs are 0.
+ */
+MOE_API int moe_balance_stats(int32_t n_experts, int32_t T, int32_t top_k,
+                      const int32_t* counts, const float* prob_sum,
+                      float alpha, float* f, float* P, float* aux,
+                      moe_stream_t stream);
+
+/* Synchronises `stream`, then returns the device-side status recorded in the
+ * workspace `ws` by the last call that used it (MOE_OK, MOE_ERR_TIMEOUT or
+ * MOE_ERR_DEVICE_CHECK), or MOE_ERR_CUDA if the stream reports an error. */
+MOE_API int moe_stream_status(const void* ws, moe_stream_t stream);
+
+/* Kernel-level profiling. While enabled, each kernel launch of this library
+ * is bracketed by CUDA events recorded on the launching stream (events are
+ * created by the library, host-side). moe_profile_collect synchronises on
+ * the last event, writes up to `max_kernels` entries of per-kernel total
+ * milliseconds and launch counts (names by moe_profile_kernel_name) and
+ * clears the record; it returns the number of kernel kinds. */
+MOE_API void moe_profile_enable(int on);
+MOE_API int moe_profile_collect(float* total_ms, int32_t* launches, int max_kernels);
+MOE_API const char* moe_profile_kernel_name(int id);
+
+/* Number of kernels this library has launched since it was loaded. */
+MOE_API uint64_t moe_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

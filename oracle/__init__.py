@@ -66,6 +66,7 @@ def _declare(lib):
     lib.oracle_balance_stats.restype = ctypes.c_double
     lib.oracle_balance_stats.argtypes = [_I, _I, _I, _P, _P, ctypes.c_double,
                                          _P, _P]
+    lib.oracle_selection_margin.argtypes = [_I, _I, _I, _P, _P, _P]
     return lib
 
 
@@ -220,6 +221,15 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_layer_rows: a token needs an expert that was not supplied")
         return y
+
+    def selection_margin(self, r64, k, sel_bias=None):
+        """Per-token gap between the k-th and (k+1)-th largest fp64 key."""
+        r64 = _c(r64, np.float64)
+        T, N = r64.shape
+        sb = None if sel_bias is None else _c(sel_bias, np.float32)
+        m = np.empty(T, np.float64)
+        self.lib.oracle_selection_margin(T, N, k, _ptr(r64), _ptr(sb), _ptr(m))
+        return m
 
     def balance_loss(self, f, P, alpha=0.01):
         f = _c(f, np.float64)

@@ -282,29 +282,33 @@ int oracle_layer_rows(int T, int d, int d_ff, int N, int k, int n_shared,
     if (!wg[N + s] || !wu[N + s] || !wd[N + s]) bad = 1;
   if (bad) return -1;
 
+  /* Every (row, term) expert evaluation is independent: evaluate them all
+   * (in parallel), then form each row's gated sum in term order. */
+  const int terms = k + n_shared;
+  double* E = (double*)malloc(sizeof(double) * (size_t)n_rows * terms * d);
+  double* G = (double*)malloc(sizeof(double) * (size_t)n_rows * terms);
 #pragma omp parallel for schedule(dynamic, 1)
-  for (int r = 0; r < n_rows; ++r) {
-    int t = rows[r];
+  for (long long q = 0; q < (long long)n_rows * terms; ++q) {
+    const int r = (int)(q / terms), s = (int)(q % terms);
+    const int t = rows[r];
     double* xt = (double*)malloc(sizeof(double) * (size_t)d);
-    double* E = (double*)malloc(sizeof(double) * (size_t)(k + n_shared) * d);
-    double* G = (double*)malloc(sizeof(double) * (size_t)(k + n_shared));
     for (int i = 0; i < d; ++i) xt[i] = widen(xdtype, x, (size_t)t * d + i);
-    for (int s = 0; s < k; ++s) {
-      int e = topk_idx[(size_t)t * k + s];
-      G[s] = topk_w[(size_t)t * k + s];
-      oracle_expert_swiglu(d, d_ff, wdtype, wg[e], wu[e], wd[e], xt,
-                           E + (size_t)s * d);
+    int e;
+    if (s < k) {
+      e = topk_idx[(size_t)t * k + s];
+      G[q] = topk_w[(size_t)t * k + s];
+    } else {
+      e = N + (s - k);
+      G[q] = 1.0;
     }
-    for (int s = 0; s < n_shared; ++s) {
-      G[k + s] = 1.0;
-      oracle_expert_swiglu(d, d_ff, wdtype, wg[N + s], wu[N + s], wd[N + s],
-                           xt, E + (size_t)(k + s) * d);
-    }
-    oracle_gated_sum(k + n_shared, d, G, E, y + (size_t)r * d);
+    oracle_expert_swiglu(d, d_ff, wdtype, wg[e], wu[e], wd[e], xt, E + (size_t)q * d);
     free(xt);
-    free(E);
-    free(G);
   }
+  for (int r = 0; r < n_rows; ++r)
+    oracle_gated_sum(terms, d, G + (size_t)r * terms, E + (size_t)r * terms * d,
+                     y + (size_t)r * d);
+  free(E);
+  free(G);
   return 0;
 }
 
@@ -329,4 +333,28 @@ double oracle_balance_stats(int N, int T, int k, const int32_t* counts,
     P[i] = prob_sum[i] / (double)T;
   }
   return oracle_balance_loss(N, f, P, alpha);
+}
+
+/* Selection margin of each token: the gap between the k-th and (k+1)-th
+ * largest fp64 key r64 + sel_bias (infinity when k = N). Inputs whose margin
+ * is at least 1e-3 have a top-k set that no fp32 rounding of the scores can
+ * change, so routing can be compared bit for bit. */
+void oracle_selection_margin(int T, int N, int k, const double* r64,
+                             const float* sel_bias, double* margin) {
+  double* key = (double*)malloc(sizeof(double) * (size_t)N);
+  for (int t = 0; t < T; ++t) {
+    for (int e = 0; e < N; ++e)
+      key[e] = r64[(size_t)t * N + e] + (sel_bias ? (double)sel_bias[e] : 0.0);
+    /* k-th and (k+1)-th largest by partial selection sort */
+    for (int s = 0; s <= k && s < N; ++s) {
+      int best = s;
+      for (int i = s + 1; i < N; ++i)
+        if (key[i] > key[best]) best = i;
+      double tmp = key[s];
+      key[s] = key[best];
+      key[best] = tmp;
+    }
+    margin[t] = (k < N) ? key[k - 1] - key[k] : INFINITY;
+  }
+  free(key);
 }

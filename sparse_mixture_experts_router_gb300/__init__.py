@@ -1,0 +1,220 @@
+"""Python binding of libmoe.so, the sparse top-k MoE FFN layer forward for
+one GB300 (sm_103a).
+
+Argument marshalling only: every function below checks nothing itself, takes
+torch tensors (or None), passes their device pointers and sizes to the C ABI
+of the same name (``include/moe.h``) on the current CUDA stream, and raises
+:class:`MoeError` on a non-zero status. All computation runs in the library's
+CUDA kernels; there is no CPU fallback. If ``libmoe.so`` has not been built,
+the first call raises instead of computing anything.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED = -2
+MOE_ERR_MISALIGNED = -3
+MOE_ERR_WORKSPACE = -4
+MOE_ERR_CUDA = -5
+MOE_ERR_TIMEOUT = -6
+MOE_ERR_DEVICE_CHECK = -7
+
+MOE_F32, MOE_BF16 = 0, 1
+MOE_GATE_TOPK_SOFTMAX, MOE_GATE_ALL_SOFTMAX_RENORM = 0, 1
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, status, text):
+        super().__init__(f"{fn}: status {status} ({text})")
+        self.status = status
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d_model", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("d_ff", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("gate_mode", ctypes.c_int32)]
+
+    def __repr__(self):
+        return "moe_config(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
+
+
+def config(T, d_model, n_experts, top_k, d_ff, n_shared=0, dtype=MOE_BF16,
+           gate_mode=MOE_GATE_TOPK_SOFTMAX) -> moe_config:
+    return moe_config(T, d_model, n_experts, top_k, n_shared, d_ff, dtype, gate_mode)
+
+
+_P = ctypes.c_void_p
+_SZ = ctypes.c_size_t
+_I = ctypes.c_int
+_CFG = ctypes.POINTER(moe_config)
+_SIGS = {
+    "moe_version": (_I, []),
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_last_cuda_error": (_I, []),
+    "moe_check_config": (_I, [_CFG]),
+    "moe_router_workspace_size": (_SZ, [_CFG]),
+    "moe_permute_workspace_size": (_SZ, [_CFG]),
+    "moe_grouped_workspace_size": (_SZ, [_CFG]),
+    "moe_workspace_size": (_SZ, [_CFG]),
+    "moe_router_topk": (_I, [_CFG] + [_P] * 10 + [_P, _SZ, _P]),
+    "moe_permute": (_I, [_CFG] + [_P] * 6 + [_P, _SZ, _P]),
+    "moe_grouped_swiglu": (_I, [_CFG] + [_P] * 9 + [_P, _SZ, _P]),
+    "moe_combine": (_I, [_CFG, _P, _P, _P, _P, _P]),
+    "moe_layer_forward": (_I, [_CFG] + [_P] * 12 + [_P, _SZ, _P]),
+    "moe_balance_stats": (_I, [ctypes.c_int32] * 3 + [_P, _P, ctypes.c_float, _P, _P, _P, _P]),
+    "moe_stream_status": (_I, [_P, _P]),
+    "moe_profile_enable": (None, [_I]),
+    "moe_profile_collect": (_I, [_P, _P, _I]),
+    "moe_profile_kernel_name": (ctypes.c_char_p, [_I]),
+    "moe_launch_count": (ctypes.c_uint64, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """The loaded libmoe.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` "
+                    "(there is no fallback implementation)")
+            l = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                f = getattr(l, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = l
+    return _lib
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn, rc):
+    if rc != MOE_OK:
+        raise MoeError(fn, rc, status_string(rc))
+
+
+def status_string(rc: int) -> str:
+    return lib().moe_status_string(rc).decode()
+
+
+def check_config(cfg: moe_config) -> int:
+    return lib().moe_check_config(ctypes.byref(cfg))
+
+
+def workspace_size(cfg: moe_config, kind: str = "layer") -> int:
+    fn = {"layer": "moe_workspace_size", "router": "moe_router_workspace_size",
+          "permute": "moe_permute_workspace_size", "grouped": "moe_grouped_workspace_size"}[kind]
+    return int(getattr(lib(), fn)(ctypes.byref(cfg)))
+
+
+def workspace(cfg: moe_config, kind: str = "layer", device="cuda"):
+    """A caller-owned workspace tensor of the size the library asks for."""
+    import torch
+    n = workspace_size(cfg, kind)
+    if n == 0:
+        raise MoeError("workspace_size", check_config(cfg), "invalid configuration")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def moe_router_topk(cfg, x, w_router, logit_bias, sel_bias, logits_in, logits_out, topk_idx,
+                    topk_w, counts, prob_sum, ws, stream=None):
+    _check("moe_router_topk", lib().moe_router_topk(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(sel_bias),
+        _ptr(logits_in), _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _ptr(counts),
+        _ptr(prob_sum), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def moe_permute(cfg, x, topk_idx, expert_offsets, sorted_pair, inv_pos, x_perm, ws, stream=None):
+    _check("moe_permute", lib().moe_permute(
+        ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(expert_offsets), _ptr(sorted_pair),
+        _ptr(inv_pos), _ptr(x_perm), _ptr(ws), ws.numel() if ws is not None else 0,
+        _stream(stream)))
+
+
+def moe_grouped_swiglu(cfg, x_perm, x, expert_offsets, sorted_pair, topk_w, w_gate, w_up, w_down,
+                       y_perm, ws, stream=None):
+    _check("moe_grouped_swiglu", lib().moe_grouped_swiglu(
+        ctypes.byref(cfg), _ptr(x_perm), _ptr(x), _ptr(expert_offsets), _ptr(sorted_pair),
+        _ptr(topk_w), _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(y_perm), _ptr(ws),
+        ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def moe_combine(cfg, y_perm, inv_pos, topk_w, y, stream=None):
+    _check("moe_combine", lib().moe_combine(
+        ctypes.byref(cfg), _ptr(y_perm), _ptr(inv_pos), _ptr(topk_w), _ptr(y), _stream(stream)))
+
+
+def moe_layer_forward(cfg, x, w_router, logit_bias, sel_bias, w_gate, w_up, w_down, y, topk_idx,
+                      topk_w, counts, prob_sum, ws, stream=None):
+    _check("moe_layer_forward", lib().moe_layer_forward(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(sel_bias),
+        _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(y), _ptr(topk_idx), _ptr(topk_w),
+        _ptr(counts), _ptr(prob_sum), _ptr(ws), ws.numel() if ws is not None else 0,
+        _stream(stream)))
+
+
+def moe_balance_stats(n_experts, T, top_k, counts, prob_sum, alpha, f, P, aux, stream=None):
+    _check("moe_balance_stats", lib().moe_balance_stats(
+        n_experts, T, top_k, _ptr(counts), _ptr(prob_sum), ctypes.c_float(alpha), _ptr(f), _ptr(P),
+        _ptr(aux), _stream(stream)))
+
+
+def moe_stream_status(ws, stream=None) -> int:
+    return int(lib().moe_stream_status(_ptr(ws), _stream(stream)))
+
+
+def profile_enable(on: bool = True):
+    lib().moe_profile_enable(1 if on else 0)
+
+
+def profile_collect() -> dict:
+    """{kernel name: (total ms, launches)} of the launches since the last
+    collect while profiling was on (synchronises on the last event)."""
+    n = 32
+    ms = (ctypes.c_float * n)()
+    cnt = (ctypes.c_int32 * n)()
+    k = lib().moe_profile_collect(ms, cnt, n)
+    out = {}
+    for i in range(k):
+        name = lib().moe_profile_kernel_name(i).decode()
+        if cnt[i]:
+            out[name] = (float(ms[i]), int(cnt[i]))
+    return out
+
+
+def launch_count() -> int:
+    return int(lib().moe_launch_count())
+
+
+def version() -> int:
+    return int(lib().moe_version())

@@ -1,0 +1,448 @@
+// The C ABI of libmoe.so (include/moe.h): argument checks, workspace
+// layout, the call sequence of the layer, device status, and the optional
+// per-kernel event profiler. Every computation runs in the kernels of the
+// other translation units; nothing here touches tensor data on the host.
+#include <atomic>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+std::atomic<uint64_t> g_launches{0};
+
+int fail_cuda(cudaError_t e) {
+  g_last_cuda_error = (int)e;
+  return MOE_ERR_CUDA;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Carves 256-byte-aligned regions out of a workspace; with base == nullptr
+// it only measures.
+struct Carver {
+  char* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<char*>(b)) {}
+  template <typename T>
+  T* take(size_t bytes) {
+    off = align_up(off, 256);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+long long pairs(const moe_config& c) { return (long long)c.T * c.top_k; }
+long long rows_total(const moe_config& c) { return pairs(c) + (long long)c.n_shared * c.T; }
+
+struct RouterWs {
+  int* status;
+  float* partials;
+};
+RouterWs carve_router(Carver& cv, const moe_config& c) {
+  RouterWs w;
+  w.status = cv.take<int>(256);
+  w.partials = cv.take<float>(router_partials_bytes(c));
+  return w;
+}
+struct PermuteWs {
+  int* status;
+  int32_t* hist;
+};
+PermuteWs carve_permute(Carver& cv, const moe_config& c) {
+  PermuteWs w;
+  w.status = cv.take<int>(256);
+  w.hist = cv.take<int32_t>(permute_scratch_bytes(c));
+  return w;
+}
+struct GroupedWs {
+  int* status;
+  int32_t* seg;
+  void* h;
+};
+GroupedWs carve_grouped(Carver& cv, const moe_config& c) {
+  GroupedWs w;
+  w.status = cv.take<int>(256);
+  w.seg = cv.take<int32_t>(sizeof(int32_t) * seg_table_words(c.n_experts + c.n_shared));
+  w.h = cv.take<void>((size_t)rows_total(c) * c.d_ff * elem_bytes(c.dtype));
+  return w;
+}
+struct LayerWs {
+  int* status;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* counts;
+  float* prob_sum;
+  int32_t* offsets;
+  int32_t* sorted_pair;
+  int32_t* inv_pos;
+  void* x_perm;
+  void* y_perm;
+  float* partials;
+  int32_t* hist;
+  int32_t* seg;
+  void* h;
+};
+LayerWs carve_layer(Carver& cv, const moe_config& c) {
+  LayerWs w;
+  const size_t P = (size_t)pairs(c), N = (size_t)c.n_experts, eb = elem_bytes(c.dtype);
+  w.status = cv.take<int>(256);
+  w.topk_idx = cv.take<int32_t>(sizeof(int32_t) * P);
+  w.topk_w = cv.take<float>(sizeof(float) * P);
+  w.counts = cv.take<int32_t>(sizeof(int32_t) * N);
+  w.prob_sum = cv.take<float>(sizeof(float) * N);
+  w.offsets = cv.take<int32_t>(sizeof(int32_t) * (N + 1));
+  w.sorted_pair = cv.take<int32_t>(sizeof(int32_t) * P);
+  w.inv_pos = cv.take<int32_t>(sizeof(int32_t) * P);
+  w.x_perm = cv.take<void>(P * c.d_model * eb);
+  w.y_perm = cv.take<void>((size_t)rows_total(c) * c.d_model * eb);
+  w.partials = cv.take<float>(router_partials_bytes(c));
+  w.hist = cv.take<int32_t>(permute_scratch_bytes(c));
+  w.seg = cv.take<int32_t>(sizeof(int32_t) * seg_table_words(c.n_experts + c.n_shared));
+  w.h = cv.take<void>((size_t)rows_total(c) * c.d_ff * eb);
+  return w;
+}
+
+int check_ws(const moe_config& c, void* ws, size_t ws_bytes, size_t need) {
+  (void)c;
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return MOE_ERR_MISALIGNED;
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+// All non-null device pointers 16-byte aligned.
+bool all_aligned(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (p && !aligned(p, 16)) return false;
+  return true;
+}
+
+int reset_status(int* status, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
+  return e == cudaSuccess ? MOE_OK : fail_cuda(e);
+}
+
+// The bf16 path is built for sm_103a only.
+int check_device(const moe_config& c) {
+  if (c.dtype != MOE_BF16) return MOE_OK;
+  int dev = 0, major = 0, minor = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return (major == 10 && minor == 3) ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+int grouped_impl(const moe_config& c, const void* x_perm, const void* x, const int32_t* offsets,
+                 const int32_t* sorted_pair, const float* topk_w, const void* wg, const void* wu,
+                 const void* wd, void* y_perm, int32_t* seg, void* h, int* status,
+                 cudaStream_t s) {
+  if (rows_total(c) == 0) return MOE_OK;
+  cudaError_t e = launch_seg_table(c, offsets, seg, status, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = (c.dtype == MOE_BF16)
+          ? launch_grouped_bf16(c, x_perm, x, seg, sorted_pair, topk_w, wg, wu, wd, h, y_perm, status, s)
+          : launch_grouped_f32(c, x_perm, x, seg, sorted_pair, topk_w, wg, wu, wd, h, y_perm, status, s);
+  return e == cudaSuccess ? MOE_OK : fail_cuda(e);
+}
+
+// ---- profiler ---------------------------------------------------------------
+const char* kKernelNames[K_NUM] = {"router_topk",    "router_reduce", "permute_hist",
+                                   "permute_scan",   "permute_rank",  "permute_gather",
+                                   "seg_table",      "gate_up",       "down",
+                                   "combine",        "balance_stats"};
+struct Prof {
+  std::mutex mu;
+  bool on = false;
+  std::vector<cudaEvent_t> pool;
+  std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> done;
+  cudaEvent_t open[K_NUM] = {};
+  cudaEvent_t get() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+};
+Prof& prof() {
+  static Prof* p = new Prof();  // never destroyed: events may outlive static teardown order
+  return *p;
+}
+
+}  // namespace
+
+void prof_begin(int id, cudaStream_t s) {
+  Prof& p = prof();
+  std::lock_guard<std::mutex> g(p.mu);
+  if (!p.on) return;
+  cudaEvent_t e = p.get();
+  cudaEventRecord(e, s);
+  p.open[id] = e;
+}
+void prof_end(int id, cudaStream_t s) {
+  Prof& p = prof();
+  std::lock_guard<std::mutex> g(p.mu);
+  if (!p.on || !p.open[id]) return;
+  cudaEvent_t e = p.get();
+  cudaEventRecord(e, s);
+  p.done.push_back({id, {p.open[id], e}});
+  p.open[id] = nullptr;
+}
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_version(void) { return 100; }
+
+const char* moe_status_string(int s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null pointer, bad shape or bad enum)";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case MOE_ERR_MISALIGNED: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error (see moe_last_cuda_error)";
+    case MOE_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case MOE_ERR_DEVICE_CHECK: return "device-side input check failed";
+    default: return "unknown status";
+  }
+}
+
+int moe_last_cuda_error(void) { return g_last_cuda_error; }
+
+int moe_check_config(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->d_model < 1 || c->n_experts < 1 || c->top_k < 1 || c->n_shared < 0 ||
+      c->d_ff < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->gate_mode != MOE_GATE_TOPK_SOFTMAX && c->gate_mode != MOE_GATE_ALL_SOFTMAX_RENORM)
+    return MOE_ERR_INVALID_ARG;
+  if (c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
+  if (c->n_experts > kMaxExperts || c->top_k > kMaxTopK || c->n_shared > kMaxShared)
+    return MOE_ERR_UNSUPPORTED;
+  if (c->d_model % 8 != 0 || c->d_ff % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  // Row indices, TMA coordinates and pair ids are 32-bit.
+  const long long R = (long long)c->T * (c->top_k + c->n_shared);
+  if (R >= (1LL << 30) || (long long)(c->n_experts + c->n_shared) * (c->d_ff > c->d_model ? c->d_ff : c->d_model) >= (1LL << 31))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+size_t moe_router_workspace_size(const moe_config* c) {
+  if (moe_check_config(c) != MOE_OK) return 0;
+  Carver cv(nullptr);
+  carve_router(cv, *c);
+  return align_up(cv.off, 256);
+}
+size_t moe_permute_workspace_size(const moe_config* c) {
+  if (moe_check_config(c) != MOE_OK) return 0;
+  Carver cv(nullptr);
+  carve_permute(cv, *c);
+  return align_up(cv.off, 256);
+}
+size_t moe_grouped_workspace_size(const moe_config* c) {
+  if (moe_check_config(c) != MOE_OK) return 0;
+  Carver cv(nullptr);
+  carve_grouped(cv, *c);
+  return align_up(cv.off, 256);
+}
+size_t moe_workspace_size(const moe_config* c) {
+  if (moe_check_config(c) != MOE_OK) return 0;
+  Carver cv(nullptr);
+  carve_layer(cv, *c);
+  return align_up(cv.off, 256);
+}
+
+int moe_router_topk(const moe_config* cfg, const void* x, const void* w_router,
+                    const float* logit_bias, const float* sel_bias, const float* logits_in,
+                    float* logits_out, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                    float* prob_sum, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  int rc = moe_check_config(cfg);
+  if (rc != MOE_OK) return rc;
+  const moe_config& c = *cfg;
+  if (!counts || !prob_sum) return MOE_ERR_INVALID_ARG;
+  if (c.T > 0 && (!topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
+  if (c.T > 0 && !logits_in && (!x || !w_router)) return MOE_ERR_INVALID_ARG;
+  if (logits_in && logit_bias) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned({x, w_router, logit_bias, sel_bias, logits_in, logits_out, topk_idx, topk_w,
+                    counts, prob_sum}))
+    return MOE_ERR_MISALIGNED;
+  if ((rc = check_ws(c, ws, ws_bytes, moe_router_workspace_size(cfg))) != MOE_OK) return rc;
+  Carver cv(ws);
+  RouterWs w = carve_router(cv, c);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
+  cudaError_t e = launch_router(c, x, w_router, logit_bias, sel_bias, logits_in, logits_out,
+                                topk_idx, topk_w, counts, prob_sum, w.partials, w.status, s);
+  return e == cudaSuccess ? MOE_OK : fail_cuda(e);
+}
+
+int moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                int32_t* expert_offsets, int32_t* sorted_pair, int32_t* inv_pos, void* x_perm,
+                void* ws, size_t ws_bytes, moe_stream_t stream) {
+  int rc = moe_check_config(cfg);
+  if (rc != MOE_OK) return rc;
+  const moe_config& c = *cfg;
+  if (!expert_offsets) return MOE_ERR_INVALID_ARG;
+  if (c.T > 0 && (!x || !topk_idx || !sorted_pair || !inv_pos || !x_perm))
+    return MOE_ERR_INVALID_ARG;
+  if (!all_aligned({x, topk_idx, expert_offsets, sorted_pair, inv_pos, x_perm}))
+    return MOE_ERR_MISALIGNED;
+  if ((rc = check_ws(c, ws, ws_bytes, moe_permute_workspace_size(cfg))) != MOE_OK) return rc;
+  Carver cv(ws);
+  PermuteWs w = carve_permute(cv, c);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
+  cudaError_t e = launch_permute(c, x, topk_idx, expert_offsets, sorted_pair, inv_pos, x_perm,
+                                 w.hist, w.status, s);
+  return e == cudaSuccess ? MOE_OK : fail_cuda(e);
+}
+
+int moe_grouped_swiglu(const moe_config* cfg, const void* x_perm, const void* x,
+                       const int32_t* expert_offsets, const int32_t* sorted_pair,
+                       const float* topk_w, const void* w_gate, const void* w_up,
+                       const void* w_down, void* y_perm, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+  int rc = moe_check_config(cfg);
+  if (rc != MOE_OK) return rc;
+  const moe_config& c = *cfg;
+  if (rows_total(c) > 0) {
+    if (!expert_offsets || !w_gate || !w_up || !w_down || !y_perm) return MOE_ERR_INVALID_ARG;
+    if (pairs(c) > 0 && !x_perm) return MOE_ERR_INVALID_ARG;
+    if (c.n_shared > 0 && !x) return MOE_ERR_INVALID_ARG;
+    if (topk_w && !sorted_pair) return MOE_ERR_INVALID_ARG;
+  }
+  if (!all_aligned({x_perm, x, expert_offsets, sorted_pair, topk_w, w_gate, w_up, w_down, y_perm}))
+    return MOE_ERR_MISALIGNED;
+  if ((rc = check_ws(c, ws, ws_bytes, moe_grouped_workspace_size(cfg))) != MOE_OK) return rc;
+  if ((rc = check_device(c)) != MOE_OK) return rc;
+  Carver cv(ws);
+  GroupedWs w = carve_grouped(cv, c);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
+  return grouped_impl(c, x_perm, x, expert_offsets, sorted_pair, topk_w, w_gate, w_up, w_down,
+                      y_perm, w.seg, w.h, w.status, s);
+}
+
+int moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* inv_pos,
+                const float* topk_w, void* y, moe_stream_t stream) {
+  int rc = moe_check_config(cfg);
+  if (rc != MOE_OK) return rc;
+  const moe_config& c = *cfg;
+  if (c.T > 0 && (!y_perm || !inv_pos || !y)) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned({y_perm, inv_pos, topk_w, y})) return MOE_ERR_MISALIGNED;
+  cudaError_t e = launch_combine(c, y_perm, inv_pos, topk_w, y, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : fail_cuda(e);
+}
+
+int moe_layer_forward(const moe_config* cfg, const void* x, const void* w_router,
+                      const float* logit_bias, const float* sel_bias, const void* w_gate,
+                      const void* w_up, const void* w_down, void* y, int32_t* topk_idx,
+                      float* topk_w, int32_t* counts, float* prob_sum, void* ws, size_t ws_bytes,
+                      moe_stream_t stream) {
+  int rc = moe_check_config(cfg);
+  if (rc != MOE_OK) return rc;
+  const moe_config& c = *cfg;
+  if (c.T > 0 && (!x || !w_router || !w_gate || !w_up || !w_down || !y)) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned({x, w_router, logit_bias, sel_bias, w_gate, w_up, w_down, y, topk_idx, topk_w,
+                    counts, prob_sum}))
+    return MOE_ERR_MISALIGNED;
+  if ((rc = check_ws(c, ws, ws_bytes, moe_workspace_size(cfg))) != MOE_OK) return rc;
+  if ((rc = check_device(c)) != MOE_OK) return rc;
+  Carver cv(ws);
+  LayerWs w = carve_layer(cv, c);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
+  int32_t* idx = topk_idx ? topk_idx : w.topk_idx;
+  float* tw = topk_w ? topk_w : w.topk_w;
+  int32_t* cnt = counts ? counts : w.counts;
+  float* ps = prob_sum ? prob_sum : w.prob_sum;
+  cudaError_t e = launch_router(c, x, w_router, logit_bias, sel_bias, nullptr, nullptr, idx, tw,
+                                cnt, ps, w.partials, w.status, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (c.T == 0) return MOE_OK;
+  e = launch_permute(c, x, idx, w.offsets, w.sorted_pair, w.inv_pos, w.x_perm, w.hist, w.status, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  rc = grouped_impl(c, w.x_perm, x, w.offsets, w.sorted_pair, tw, w_gate, w_up, w_down, w.y_perm,
+                    w.seg, w.h, w.status, s);
+  if (rc != MOE_OK) return rc;
+  e = launch_combine(c, w.y_perm, w.inv_pos, nullptr, y, s);
+  return e == cudaSuccess ? MOE_OK : fail_cuda(e);
+}
+
+int moe_balance_stats(int32_t n_experts, int32_t T, int32_t top_k, const int32_t* counts,
+                      const float* prob_sum, float alpha, float* f, float* P, float* aux,
+                      moe_stream_t stream) {
+  if (n_experts < 1 || n_experts > kMaxExperts || T < 0 || top_k < 1 || top_k > n_experts)
+    return MOE_ERR_INVALID_ARG;
+  if (!counts || !prob_sum || !f || !P || !aux) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned({counts, prob_sum, f, P}) || ((uintptr_t)aux % 4)) return MOE_ERR_MISALIGNED;
+  cudaError_t e = launch_balance_stats(n_experts, T, top_k, counts, prob_sum, alpha, f, P, aux,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : fail_cuda(e);
+}
+
+int moe_stream_status(const void* ws, moe_stream_t stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return MOE_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  int st = 0;
+  e = cudaMemcpy(&st, ws, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return st;
+}
+
+void moe_profile_enable(int on) {
+  Prof& p = prof();
+  std::lock_guard<std::mutex> g(p.mu);
+  p.on = on != 0;
+}
+
+int moe_profile_collect(float* total_ms, int32_t* launches, int max_kernels) {
+  Prof& p = prof();
+  std::lock_guard<std::mutex> g(p.mu);
+  std::vector<double> ms(K_NUM, 0.0);
+  std::vector<int> n(K_NUM, 0);
+  if (!p.done.empty()) cudaEventSynchronize(p.done.back().second.second);
+  for (auto& d : p.done) {
+    float t = 0.f;
+    cudaEventSynchronize(d.second.second);
+    if (cudaEventElapsedTime(&t, d.second.first, d.second.second) == cudaSuccess) {
+      ms[d.first] += t;
+      n[d.first] += 1;
+    }
+    p.pool.push_back(d.second.first);
+    p.pool.push_back(d.second.second);
+  }
+  p.done.clear();
+  for (int i = 0; i < K_NUM && i < max_kernels; ++i) {
+    if (total_ms) total_ms[i] = (float)ms[i];
+    if (launches) launches[i] = n[i];
+  }
+  return K_NUM;
+}
+
+const char* moe_profile_kernel_name(int id) {
+  return (id >= 0 && id < K_NUM) ? kKernelNames[id] : "";
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,132 @@
+// K5: gate-weighted sum back into token order, and the balance statistics.
+//
+// y[t] = sum_slot w * y_perm[inv_pos[t*k+slot]] + sum_shared y_perm[T*k+s*T+t]
+// ("Mixture of experts and speculative decoding", step 4 and the layer
+// equation; "Mixture of Experts and Guided Decoding", the three-expert gated
+// sum). One warp per token; each lane accumulates 16-byte vectors of the
+// k + n_shared rows in fp32 in a fixed order (slots, then shared experts)
+// and writes each output element exactly once, so there are no atomics and
+// the result is reproducible.
+#include "device_util.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+template <typename TE>
+struct Vec;
+template <>
+struct Vec<float> {
+  static constexpr int n = 4;
+  __device__ static void load(const float* p, float (&v)[4]) {
+    const float4 q = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+  }
+  __device__ static void store(float* p, const float (&v)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+};
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int n = 8;
+  __device__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
+    bf16x2_to_f32(q.x, v[0], v[1]);
+    bf16x2_to_f32(q.y, v[2], v[3]);
+    bf16x2_to_f32(q.z, v[4], v[5]);
+    bf16x2_to_f32(q.w, v[6], v[7]);
+  }
+  __device__ static void store(__nv_bfloat16* p, const float (&v)[8]) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(f32x2_to_bf16x2(v[0], v[1]), f32x2_to_bf16x2(v[2], v[3]),
+                                              f32x2_to_bf16x2(v[4], v[5]), f32x2_to_bf16x2(v[6], v[7]));
+  }
+};
+
+template <typename TE>
+__global__ void __launch_bounds__(kThreads) combine_kernel(const TE* __restrict__ yp,
+                                                           const int32_t* __restrict__ inv_pos,
+                                                           const float* __restrict__ topk_w,
+                                                           TE* __restrict__ y, int T, int d, int k,
+                                                           int n_shared) {
+  constexpr int V = Vec<TE>::n;
+  const int t = blockIdx.x * kWarps + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (t >= T) return;
+  const long long P = (long long)T * k;
+  long long src[kMaxTopK + kMaxShared];
+  float w[kMaxTopK + kMaxShared];
+  int n = 0;
+  for (int s = 0; s < k; ++s) {
+    const int pos = __ldg(inv_pos + (size_t)t * k + s);
+    if (pos < 0 || pos >= P) continue;  // contributes zero
+    src[n] = (long long)pos * d;
+    w[n] = topk_w ? __ldg(topk_w + (size_t)t * k + s) : 1.0f;
+    ++n;
+  }
+  for (int s = 0; s < n_shared; ++s) {
+    src[n] = (P + (long long)s * T + t) * d;
+    w[n] = 1.0f;
+    ++n;
+  }
+  const int nvec = d / V;
+  for (int v = lane; v < nvec; v += 32) {
+    float acc[V];
+#pragma unroll
+    for (int q = 0; q < V; ++q) acc[q] = 0.f;
+    for (int j = 0; j < n; ++j) {
+      float val[V];
+      Vec<TE>::load(yp + src[j] + (long long)v * V, val);
+#pragma unroll
+      for (int q = 0; q < V; ++q) acc[q] = fmaf(w[j], val[q], acc[q]);
+    }
+    Vec<TE>::store(y + (size_t)t * d + (size_t)v * V, acc);
+  }
+}
+
+__global__ void balance_stats_kernel(const int32_t* counts, const float* prob_sum, int N, int T,
+                                     int k, float alpha, float* f, float* P, float* aux) {
+  __shared__ float fp[kMaxExperts];
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    const float fe = T > 0 ? (float)counts[e] / ((float)T * (float)k) : 0.f;
+    const float pe = T > 0 ? prob_sum[e] / (float)T : 0.f;
+    f[e] = fe;
+    P[e] = pe;
+    fp[e] = fe * pe;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int e = 0; e < N; ++e) s += fp[e];
+    *aux = alpha * (float)N * s;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_t* inv_pos,
+                           const float* topk_w, void* y, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  const int grid = ceil_div(c.T, kWarps);
+  ProfScope p(K_COMBINE, s);
+  if (c.dtype == MOE_BF16)
+    combine_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(y_perm), inv_pos, topk_w, static_cast<__nv_bfloat16*>(y),
+        c.T, c.d_model, c.top_k, c.n_shared);
+  else
+    combine_kernel<float><<<grid, kThreads, 0, s>>>(static_cast<const float*>(y_perm), inv_pos,
+                                                    topk_w, static_cast<float*>(y), c.T, c.d_model,
+                                                    c.top_k, c.n_shared);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_balance_stats(int N, int T, int k, const int32_t* counts, const float* prob_sum,
+                                 float alpha, float* f, float* P, float* aux, cudaStream_t s) {
+  ProfScope p(K_BALANCE, s);
+  balance_stats_kernel<<<1, 256, 0, s>>>(counts, prob_sum, N, T, k, alpha, f, P, aux);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,490 @@
+// K3/K4: grouped SwiGLU expert GEMMs on the 5th-generation tensor cores.
+//
+// Every expert of the layer is an ordinary SwiGLU FFN ("MoE inference: the
+// call centre with 256 specialists and 8 taking each call", "The bare
+// mechanism"; read as down(SiLU(gate(x)) * up(x))). After the permutation,
+// expert e owns a contiguous, ragged segment of rows, so all experts run as
+// one grouped GEMM per projection:
+//
+//   gate/up  H[row]  = SiLU(A[row] Wg[e]^T) * (A[row] Wu[e]^T)     (bf16 out)
+//   down     Yp[row] = w_row * (H[row] Wd[e]^T)                    (bf16 out)
+//
+// with A = x_perm for routed experts and A = x for shared experts, w_row the
+// row's gate weight (1 for shared rows). This is the dense contraction of the
+// layer, and the only place it uses tensor cores ("Mixture of experts and
+// speculative decoding": an expert costs about 2 flops per parameter).
+//
+// Design (sm_103a, one CTA per SM, persistent):
+//  - Tiles: 128 rows of one segment x 256 accumulator columns. For gate/up
+//    the B tile stacks 128 gate rows over the matching 128 up rows, so one
+//    128x256x16 tcgen05.mma computes both projections into one TMEM
+//    accumulator; the epilogue pairs column j with column 128+j. For down the
+//    256 columns are 256 output features.
+//  - Tile list: segment-major, then N tile, then M tile (fastest), so the
+//    CTAs running at the same time share weight tiles through L2. CTA b takes
+//    tiles b, b+grid, ...; the list length and segment table live on the
+//    device (no host synchronisation on the routing). Rows of a tile past its
+//    segment's end are computed on whatever rows follow and never stored.
+//  - Warp roles (192 threads): warp 0 issues TMA loads (128-byte swizzle,
+//    64-wide K blocks) into a 4-stage shared-memory ring; warp 1 allocates
+//    512 TMEM columns (two 256-column accumulators) and issues tcgen05.mma
+//    from one thread, releasing ring slots and publishing finished
+//    accumulators with tcgen05.commit; warps 2-5 drain an accumulator with
+//    tcgen05.ld (each warp owns the 32 TMEM lanes its index allows), apply
+//    the SwiGLU or gate-weight epilogue and store bf16 rows, while the MMA
+//    warp fills the other accumulator.
+//  - Every wait is bounded (2 s of %globaltimer). A wait that runs out
+//    records MOE_ERR_TIMEOUT in the status word and sets a shared abort flag
+//    that ends the other roles' loops; the producer then waits (bounded) for
+//    its own TMA copies in flight, the MMA thread for its own MMAs, and TMEM
+//    is freed before the CTA exits.
+#include <cuda.h>
+#include <mutex>
+
+#include "device_util.cuh"
+#include "moe_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = kTileM;       // 128 rows
+constexpr int BK = 64;           // 64 bf16 = one 128-byte swizzle row
+constexpr int BN = 256;          // accumulator columns per tile
+constexpr int UMMA_K = 16;       // K of one tcgen05.mma kind::f16
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;           // 16 KB
+constexpr int B_HALF_BYTES = 128 * BK * 2;     // 16 KB
+constexpr int B_BYTES = BN * BK * 2;           // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES; // 48 KB
+constexpr int NUM_ACC = 2;
+constexpr int TMEM_COLS = BN * NUM_ACC;        // 512
+constexpr int THREADS = 192;
+constexpr int EPI_THREADS = 128;
+constexpr size_t DYN_SMEM = (size_t)STAGES * STAGE_BYTES + 1024;  // + 1 KB alignment slack
+constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+constexpr uint64_t kDrainLimitNs = 50000000ull;    // 50 ms
+
+enum { EPI_SWIGLU = 0, EPI_DOWN = 1 };
+
+struct GemmArgs {
+  const int32_t* seg;          // segment table (moe_internal.h)
+  const int32_t* sorted_pair;  // down: row -> pair id (may be null when topk_w is null)
+  const float* topk_w;         // down: pair -> gate weight, or null
+  void* out;                   // bf16 [rows][ldo]
+  int* status;
+  long long ldo;
+  int n_routed;
+  int n_pairs;                 // T*k, bound for sorted_pair values
+  int K;                       // reduction length
+  int n_out;                   // valid output columns
+  int NT;                      // N tiles per segment
+  int b_rows;                  // rows of one expert's weight matrix
+};
+
+struct __align__(8) SharedState {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t acc_full[NUM_ACC];
+  uint64_t acc_empty[NUM_ACC];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct Tile {
+  int s, m, n;
+};
+
+// Segment-major, N tile, then M tile fastest (see file comment).
+__device__ __forceinline__ Tile decode_tile(const int32_t* __restrict__ seg, int E, int NT,
+                                            int tile) {
+  const int32_t* mts = seg + 2;
+  int lo = 0, hi = E;  // invariant: mts[lo]*NT <= tile < mts[hi]*NT
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(mts + mid) * NT <= tile) lo = mid;
+    else hi = mid;
+  }
+  const int m0 = __ldg(mts + lo);
+  const int mt = __ldg(mts + lo + 1) - m0;
+  const int local = tile - m0 * NT;
+  return Tile{lo, local % mt, local / mt};
+}
+
+// Bounded wait on one mbarrier phase. Returns false if the wait ran out (and
+// then records the timeout and raises the abort flag) or if another role
+// already aborted.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int* status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      set_status(status, MOE_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+// Short bounded wait used only while draining after an abort.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > kDrainLimitNs) return;
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                        const __grid_constant__ CUtensorMap map_a_shared,
+                        const __grid_constant__ CUtensorMap map_b0,
+                        const __grid_constant__ CUtensorMap map_b1, const GemmArgs args) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ SharedState st;
+
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x / 32), 0);
+  const int lane = threadIdx.x % 32;
+  const uint32_t ring = (ptx::smem_addr(dyn_smem) + 1023u) & ~1023u;
+
+  const int32_t* seg = args.seg;
+  const int E = __ldg(seg);
+  const int total = __ldg(seg + 1) * args.NT;
+  const int KB = (args.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&st.full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&st.empty[i]), 1);
+    }
+    for (int i = 0; i < NUM_ACC; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&st.acc_full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&st.acc_empty[i]), EPI_THREADS);
+    }
+    ptx::mbar_init(ptx::smem_addr(&st.drain), 1);
+    st.abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&map_a);
+    ptx::prefetch_tmap(&map_a_shared);
+    ptx::prefetch_tmap(&map_b0);
+    ptx::prefetch_tmap(&map_b1);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(&st.tmem_base), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = st.tmem_base;
+  volatile int* abort_flag = &st.abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------- TMA producer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode_tile(seg, E, args.NT, tile);
+        const CUtensorMap* am = &map_a;
+        int a_row;
+        if (EPI == EPI_SWIGLU) {
+          a_row = __ldg(seg + 3 + 2 * E + t.s) + t.m * BM;
+          if (t.s >= args.n_routed) am = &map_a_shared;
+        } else {
+          a_row = __ldg(seg + 3 + 3 * E + t.s) + t.m * BM;
+        }
+        const int b_row = t.s * args.b_rows + t.n * (EPI == EPI_SWIGLU ? 128 : 256);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait_phase(ptx::smem_addr(&st.empty[stage]), phase ^ 1u, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = ptx::smem_addr(&st.full[stage]);
+          const uint32_t a_dst = ring + stage * STAGE_BYTES;
+          const uint32_t b_dst = a_dst + A_BYTES;
+          ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          ptx::tma_load_2d(a_dst, am, fb, kb * BK, a_row);
+          if (EPI == EPI_SWIGLU) {
+            ptx::tma_load_2d(b_dst, &map_b0, fb, kb * BK, b_row);
+            ptx::tma_load_2d(b_dst + B_HALF_BYTES, &map_b1, fb, kb * BK, b_row);
+          } else {
+            ptx::tma_load_2d(b_dst, &map_b0, fb, kb * BK, b_row);
+            ptx::tma_load_2d(b_dst + B_HALF_BYTES, &map_b0, fb, kb * BK, b_row + 128);
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Let the copies already issued land before the CTA can exit.
+        const long long n = issued < STAGES ? issued : STAGES;
+        for (long long i = 1; i <= n; ++i) {
+          const long long q = issued - i;
+          drain_wait(ptx::smem_addr(&st.full[q % STAGES]), (uint32_t)((q / STAGES) & 1));
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        if (!wait_phase(ptx::smem_addr(&st.acc_empty[acc]), acc_phase ^ 1u, abort_flag,
+                        args.status)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait_phase(ptx::smem_addr(&st.full[stage]), phase, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_src = ring + stage * STAGE_BYTES;
+          const uint64_t adesc = ptx::sdesc_k128(a_src);
+          const uint64_t bdesc = ptx::sdesc_k128(a_src + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            // +32 bytes of K per step = +2 in the descriptor's address field
+            ptx::mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
+          }
+          ptx::mma_commit(ptx::smem_addr(&st.empty[stage]));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(ptx::smem_addr(&st.acc_full[acc]));
+        if (++acc == NUM_ACC) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        ptx::mma_commit(ptx::smem_addr(&st.drain));
+        drain_wait(ptx::smem_addr(&st.drain), 0);
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- epilogue --
+    const int sub = warp & 3;  // TMEM lanes [32*sub, 32*sub+32) are this warp's
+    const int row_in_tile = sub * 32 + lane;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const Tile t = decode_tile(seg, E, args.NT, tile);
+      bool ok = wait_phase(ptx::smem_addr(&st.acc_full[acc]), acc_phase, abort_flag, args.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      ptx::tc_fence_after();
+      const int rows = __ldg(seg + 3 + E + t.s);
+      const int r = t.m * BM + row_in_tile;
+      const bool valid = r < rows;
+      const long long orow = (long long)__ldg(seg + 3 + 3 * E + t.s) + r;
+      const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * BN);
+      if (EPI == EPI_SWIGLU) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t g[32], u[32];
+          ptx::tmem_ld32(tbase + c * 32, g);
+          ptx::tmem_ld32(tbase + 128 + c * 32, u);
+          ptx::tmem_ld_wait();
+          const int col0 = t.n * 128 + c * 32;
+          if (valid) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float h0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+              const float h1 = silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+              pk[j] = f32x2_to_bf16x2(h0, h1);
+            }
+            __nv_bfloat16* dst = out + orow * args.ldo + col0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (col0 + q * 8 < args.n_out)
+                *reinterpret_cast<uint4*>(dst + q * 8) =
+                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+      } else {
+        float scale = 1.0f;
+        if (valid && t.s < args.n_routed && args.topk_w) {
+          const int pair = __ldg(args.sorted_pair + orow);
+          scale = (pair >= 0 && pair < args.n_pairs) ? __ldg(args.topk_w + pair) : 0.0f;
+        }
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld32(tbase + c * 32, v);
+          ptx::tmem_ld_wait();
+          const int col0 = t.n * 256 + c * 32;
+          if (valid) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              pk[j] = f32x2_to_bf16x2(scale * __uint_as_float(v[2 * j]),
+                                      scale * __uint_as_float(v[2 * j + 1]));
+            __nv_bfloat16* dst = out + orow * args.ldo + col0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (col0 + q * 8 < args.n_out)
+                *reinterpret_cast<uint4*>(dst + q * 8) =
+                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_addr(&st.acc_empty[acc]));
+      if (++acc == NUM_ACC) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------- teardown --
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side --
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows][cols] read in boxes of 128 rows x 64 columns
+// with the 128-byte swizzle; out-of-range elements read as zero.
+bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, 128u};
+  cuuint32_t estr[2] = {1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+template <int EPI>
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_sh, const CUtensorMap& b0,
+                        const CUtensorMap& b1, const GemmArgs& args, int max_tiles,
+                        cudaStream_t s) {
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DYN_SMEM);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const int grid = max_tiles < num_sms() ? max_tiles : num_sms();
+  if (grid <= 0) return cudaSuccess;
+  ProfScope p(EPI == EPI_SWIGLU ? K_GATE_UP : K_DOWN, s);
+  grouped_gemm_kernel<EPI><<<grid, THREADS, DYN_SMEM, s>>>(a, a_sh, b0, b1, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const void* x,
+                                const int32_t* seg, const int32_t* sorted_pair,
+                                const float* topk_w, const void* w_gate, const void* w_up,
+                                const void* w_down, void* h, void* y_perm, int* status,
+                                cudaStream_t s) {
+  const long long P = (long long)c.T * c.top_k;
+  const int E = c.n_experts + c.n_shared;
+  const long long R = P + (long long)c.n_shared * c.T;  // rows of H and y_perm
+  if (R == 0) return cudaSuccess;
+  // Upper bound of M tiles: every segment may end in a partial tile.
+  const long long mt_bound = (P + BM - 1) / BM + c.n_experts +
+                             (long long)c.n_shared * ((c.T + BM - 1) / BM);
+
+  CUtensorMap m_xp, m_x, m_wg, m_wu, m_h, m_wd;
+  const bool ok =
+      make_map(&m_xp, P > 0 ? x_perm : x, P > 0 ? P : c.T, c.d_model) &&
+      make_map(&m_x, c.n_shared > 0 ? x : (P > 0 ? x_perm : x), c.n_shared > 0 ? c.T : (P > 0 ? P : c.T),
+               c.d_model) &&
+      make_map(&m_wg, w_gate, (long long)E * c.d_ff, c.d_model) &&
+      make_map(&m_wu, w_up, (long long)E * c.d_ff, c.d_model) &&
+      make_map(&m_h, h, R, c.d_ff) &&
+      make_map(&m_wd, w_down, (long long)E * c.d_model, c.d_ff);
+  if (!ok) return cudaErrorInvalidValue;
+
+  GemmArgs g;
+  g.seg = seg;
+  g.sorted_pair = sorted_pair;
+  g.topk_w = nullptr;
+  g.out = h;
+  g.status = status;
+  g.ldo = c.d_ff;
+  g.n_routed = c.n_experts;
+  g.n_pairs = (int)P;
+  g.K = c.d_model;
+  g.n_out = c.d_ff;
+  g.NT = (c.d_ff + 127) / 128;
+  g.b_rows = c.d_ff;
+  cudaError_t e = launch_gemm<EPI_SWIGLU>(m_xp, m_x, m_wg, m_wu, g, (int)(mt_bound * g.NT), s);
+  if (e != cudaSuccess) return e;
+
+  GemmArgs d = g;
+  d.topk_w = topk_w;
+  d.out = y_perm;
+  d.ldo = c.d_model;
+  d.K = c.d_ff;
+  d.n_out = c.d_model;
+  d.NT = (c.d_model + 255) / 256;
+  d.b_rows = c.d_model;
+  return launch_gemm<EPI_DOWN>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s);
+}
+
+}  // namespace moe

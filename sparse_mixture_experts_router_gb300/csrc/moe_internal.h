@@ -1,0 +1,111 @@
+// Internal declarations shared by the CUDA translation units of libmoe.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Limits of this build (checked on the host before any launch).
+constexpr int kMaxExperts = 256;     // router keeps a [tokens x N] score tile in smem
+constexpr int kMaxTopK = 8;
+constexpr int kMaxShared = 4;
+
+// Router tiling: tokens per block (256 threads, 8 warps, 4 tokens a warp).
+constexpr int kRouterTokens = 32;
+// Permutation chunk: pairs handled by one block (8 warps x 8 rounds x 32).
+constexpr int kPermuteChunk = 2048;
+
+// Grouped GEMM tiling (bf16, tcgen05). A tile is 128 rows of one expert
+// segment times 128 SwiGLU columns (gate and up side by side in one
+// 128x256 accumulator) or times 256 output columns of the down projection.
+constexpr int kTileM = 128;
+constexpr int kSwigluTileN = 128;
+constexpr int kDownTileN = 256;
+
+// Device status word codes (stored as the negative status values).
+__host__ __device__ constexpr int status_timeout() { return MOE_ERR_TIMEOUT; }
+__host__ __device__ constexpr int status_check() { return MOE_ERR_DEVICE_CHECK; }
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+inline size_t elem_bytes(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
+
+// Segment table of the grouped GEMM, in device memory (int32 words):
+//   [0] E = number of segments (N routed + n_shared)
+//   [1] total M tiles
+//   [2 .. 2+E]        mt_start[e]: first M tile of segment e (E+1 entries)
+//   [3+E  .. 3+2E)    rows[e]
+//   [3+2E .. 3+3E)    a_row0[e]: first input row (x_perm row, or 0 in x)
+//   [3+3E .. 3+4E)    out_row0[e]: first output row in H / y_perm
+inline size_t seg_table_words(int E) { return 3 + 4 * (size_t)E + 1; }
+
+// ---- launchers (enqueue only; return cudaError_t of the launch) -----------
+cudaError_t launch_router(const moe_config& c, const void* x, const void* w_router,
+                          const float* logit_bias, const float* sel_bias,
+                          const float* logits_in, float* logits_out,
+                          int32_t* topk_idx, float* topk_w, int32_t* counts,
+                          float* prob_sum, float* partials, int* status,
+                          cudaStream_t s);
+size_t router_partials_bytes(const moe_config& c);
+
+cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
+                           int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos,
+                           void* x_perm, int32_t* chunk_hist, int* status,
+                           cudaStream_t s);
+size_t permute_scratch_bytes(const moe_config& c);
+
+cudaError_t launch_seg_table(const moe_config& c, const int32_t* offsets, int32_t* seg,
+                             int* status, cudaStream_t s);
+
+// bf16 tcgen05 path: gate/up (SwiGLU epilogue into h) then down (gate
+// weight epilogue into y_perm).
+cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const void* x,
+                                const int32_t* seg, const int32_t* sorted_pair,
+                                const float* topk_w, const void* w_gate, const void* w_up,
+                                const void* w_down, void* h, void* y_perm, int* status,
+                                cudaStream_t s);
+// fp32 CUDA-core path.
+cudaError_t launch_grouped_f32(const moe_config& c, const void* x_perm, const void* x,
+                               const int32_t* seg, const int32_t* sorted_pair,
+                               const float* topk_w, const void* w_gate, const void* w_up,
+                               const void* w_down, void* h, void* y_perm, int* status,
+                               cudaStream_t s);
+
+cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_t* inv_pos,
+                           const float* topk_w, void* y, cudaStream_t s);
+
+cudaError_t launch_balance_stats(int N, int T, int k, const int32_t* counts,
+                                 const float* prob_sum, float alpha, float* f, float* P,
+                                 float* aux, cudaStream_t s);
+
+// ---- profiling hooks (abi.cu) ----------------------------------------------
+enum KernelId {
+  K_ROUTER = 0,
+  K_ROUTER_REDUCE,
+  K_PERMUTE_HIST,
+  K_PERMUTE_SCAN,
+  K_PERMUTE_RANK,
+  K_PERMUTE_GATHER,
+  K_SEG_TABLE,
+  K_GATE_UP,
+  K_DOWN,
+  K_COMBINE,
+  K_BALANCE,
+  K_NUM
+};
+void prof_begin(int id, cudaStream_t s);
+void prof_end(int id, cudaStream_t s);
+void count_launch();
+
+struct ProfScope {
+  int id;
+  cudaStream_t s;
+  ProfScope(int i, cudaStream_t st) : id(i), s(st) { prof_begin(id, s); }
+  ~ProfScope() { prof_end(id, s); count_launch(); }
+};
+
+}  // namespace moe

@@ -1,0 +1,127 @@
+"""Helpers of the GPU parity tests: seeded inputs with the top-k margin
+guarantee, calls through the C ABI, host copies for the oracle, and the
+error measures the tolerances are stated in.
+
+Expected values come only from the oracle run on the generated inputs; no
+output of the CUDA library is ever fed to the oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import sparse_mixture_experts_router_gb300 as moe
+from sparse_mixture_experts_router_gb300 import synth
+
+MIN_MARGIN = 1e-3   # top-k selection margin of generated tokens (fp64 keys)
+BF16_TOL = 2e-2     # max |y - y_ref| / max |y_ref|, bf16 weights and activations
+F32_TOL = 1e-5      # same measure, fp32 layers
+
+
+def cfg_of(w: synth.Workload) -> moe.moe_config:
+    return moe.config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k,
+                      d_ff=w.d_ff, n_shared=w.n_shared,
+                      dtype=moe.MOE_BF16 if w.dtype == "bf16" else moe.MOE_F32,
+                      gate_mode=w.gate_mode)
+
+
+def host(t):
+    """numpy copy of a device tensor in the form the oracle reads (bf16 as
+    uint16 bit patterns); None stays None."""
+    if t is None:
+        return None
+    return synth.bf16_bits(t)
+
+
+def margin_inputs(w: synth.Workload, oracle, device="cuda", max_rounds=30):
+    """Workload inputs whose tokens all have a selection margin >= 1e-3
+    (tokens below it are redrawn from fresh N(0,1) draws)."""
+    inp = synth.make_inputs(w, device)
+    W = host(inp["w_router"])
+    lb = None if inp["logit_bias"] is None else inp["logit_bias"].double().cpu().numpy()
+    sb = host(inp["sel_bias"])
+    rows = np.arange(w.T)
+    for rnd in range(max_rounds):
+        xs = host(inp["x"][torch.as_tensor(rows, device=inp["x"].device)])
+        r64, _ = oracle.router_logits(xs, W, lb)
+        m = oracle.selection_margin(r64, w.top_k, sb)
+        bad = rows[m < MIN_MARGIN]
+        if bad.size == 0:
+            return inp
+        synth.redraw_rows(inp["x"], bad.tolist(), w.seed, rnd)
+        rows = bad
+    raise RuntimeError("could not reach the selection margin")
+
+
+def oracle_routing(oracle, w, inp):
+    """Routing of all tokens by the oracle: (r64, topk_idx, topk_w, counts, prob_sum)."""
+    lb = None if inp["logit_bias"] is None else inp["logit_bias"].double().cpu().numpy()
+    r64, r32 = oracle.router_logits(host(inp["x"]), host(inp["w_router"]), lb)
+    idx, tw, counts, ps = oracle.route(r32, w.top_k, w.gate_mode, host(inp["sel_bias"]))
+    return r64, idx, tw, counts, ps
+
+
+def oracle_rows(oracle, w, inp, idx, tw, rows, max_experts=40):
+    """Oracle layer output for the listed tokens, copying to the host only
+    the experts those tokens use, a batch of tokens at a time."""
+    rows = [int(r) for r in rows]
+    xh = host(inp["x"])
+    out = np.empty((len(rows), w.d_model), np.float64)
+    shared = list(range(w.n_experts, w.n_experts + w.n_shared))
+    i = 0
+    while i < len(rows):
+        batch, need = [], set(shared)
+        while i < len(rows):
+            cand = need | set(idx[rows[i]].tolist())
+            if batch and len(cand) > max_experts:
+                break
+            need = cand
+            batch.append(rows[i])
+            i += 1
+        experts = {e: (host(inp["w_gate"][e]), host(inp["w_up"][e]), host(inp["w_down"][e]))
+                   for e in sorted(need)}
+        y = oracle.layer_rows(xh, experts, idx, tw, batch, w.n_experts, w.n_shared)
+        out[i - len(batch):i] = y
+    return out
+
+
+class LayerRun:
+    """Device outputs of one moe_layer_forward call."""
+
+    def __init__(self, w: synth.Workload, inp: dict, device="cuda"):
+        self.cfg = cfg_of(w)
+        T, N, k = w.T, w.n_experts, w.top_k
+        self.y = torch.full((T, w.d_model), float("nan"), dtype=w.torch_dtype, device=device)
+        self.topk_idx = torch.full((T, k), -1, dtype=torch.int32, device=device)
+        self.topk_w = torch.zeros((T, k), dtype=torch.float32, device=device)
+        self.counts = torch.full((N,), -1, dtype=torch.int32, device=device)
+        self.prob_sum = torch.full((N,), float("nan"), dtype=torch.float32, device=device)
+        self.ws = moe.workspace(self.cfg, "layer", device)
+        self.inp = inp
+
+    def __call__(self):
+        i = self.inp
+        moe.moe_layer_forward(self.cfg, i["x"], i["w_router"], i["logit_bias"], i["sel_bias"],
+                              i["w_gate"], i["w_up"], i["w_down"], self.y, self.topk_idx,
+                              self.topk_w, self.counts, self.prob_sum, self.ws)
+        return self
+
+    def status(self):
+        return moe.moe_stream_status(self.ws)
+
+
+def rel_inf(y, ref):
+    """max |y - ref| / max |ref| over all elements."""
+    y = np.asarray(y, np.float64)
+    ref = np.asarray(ref, np.float64)
+    den = np.abs(ref).max()
+    return float(np.abs(y - ref).max() / (den if den > 0 else 1.0))
+
+
+def sample_rows(T, n, seed=0):
+    """n token rows including the first and the last."""
+    if T <= n:
+        return list(range(T))
+    rng = np.random.default_rng(seed)
+    mid = rng.choice(np.arange(1, T - 1), size=n - 2, replace=False)
+    return sorted([0, T - 1] + mid.tolist())

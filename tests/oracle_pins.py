@@ -345,6 +345,19 @@ def pin_shared_expert_always_runs_with_weight_one(o):
     assert (b["counts"] == a["counts"]).all()
 
 
+def pin_selection_margin_small(o):
+    """Worked by hand: keys [3, 1, 2.5, 0] (+ bias [0, 2, 0, 0] -> [3, 3, 2.5,
+    0]); the gap after the k-th largest."""
+    r = np.array([[3.0, 1.0, 2.5, 0.0]])
+    assert np.allclose(o.selection_margin(r, 1), [0.5])
+    assert np.allclose(o.selection_margin(r, 2), [1.5])
+    assert np.allclose(o.selection_margin(r, 3), [1.0])
+    assert np.isinf(o.selection_margin(r, 4)).all()
+    sb = np.array([0.0, 2.0, 0.0, 0.0], np.float32)
+    assert np.allclose(o.selection_margin(r, 1, sb), [0.0])
+    assert np.allclose(o.selection_margin(r, 2, sb), [0.5])
+
+
 def pin_balance_stats_sum_to_one(o):
     rng = _rng(11)
     T, N, k = 64, 8, 2

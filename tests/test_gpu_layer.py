@@ -1,0 +1,83 @@
+"""The whole layer (moe_layer_forward) against the oracle.
+
+* The tiny fp32 layer and reduced-size bf16 layers of each workload family:
+  every token checked; routing, counts bit-exact; y within 1e-5 (fp32) or
+  2e-2 (bf16) of max |y_ref|.
+* The full-size workloads (Mixtral-8x7B prefill and decode, DeepSeek-V3,
+  Zipf-imbalanced) in the configuration the benchmark times: routing of
+  every token bit-exact, statistics within fp32 rounding, y checked on
+  sampled tokens (the oracle computes them one by one).
+"""
+import numpy as np
+import pytest
+import torch
+
+import sparse_mixture_experts_router_gb300 as moe
+from sparse_mixture_experts_router_gb300 import synth
+from gpu_common import (BF16_TOL, F32_TOL, LayerRun, margin_inputs, oracle_routing, oracle_rows,
+                        rel_inf, sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    synth.TINY,
+    synth.Workload("mix_small", T=512, d_model=512, n_experts=8, top_k=2, d_ff=1024, seed=21),
+    synth.Workload("dsv3_small", T=256, d_model=256, n_experts=256, top_k=8, d_ff=256, n_shared=1,
+                   gate_mode=1, sel_bias=True, seed=22),
+    synth.Workload("zipf_small", T=1024, d_model=256, n_experts=128, top_k=8, d_ff=128,
+                   zipf_s=1.2, seed=23),
+    synth.Workload("decode_small", T=3, d_model=512, n_experts=8, top_k=2, d_ff=512, seed=24),
+    synth.Workload("f32_shared", T=100, d_model=48, n_experts=6, top_k=3, d_ff=64, n_shared=2,
+                   dtype="f32", gate_mode=1, sel_bias=True, seed=25),
+]
+
+
+def check_layer(oracle, w, rows=None):
+    inp = margin_inputs(w, oracle)
+    run = LayerRun(w, inp)()
+    assert run.status() == 0
+    r64, idx, tw, counts, ps = oracle_routing(oracle, w, inp)
+    assert np.array_equal(run.topk_idx.cpu().numpy(), idx)
+    assert np.array_equal(run.counts.cpu().numpy(), counts)
+    assert np.abs(run.topk_w.cpu().numpy() - tw).max() <= 1e-5
+    assert np.allclose(run.prob_sum.cpu().numpy(), ps, rtol=1e-4, atol=1e-4)
+    rows = list(range(w.T)) if rows is None else rows
+    ref = oracle_rows(oracle, w, inp, idx, tw, rows)
+    got = run.y.float().cpu().numpy()[rows]
+    assert not np.isnan(got).any()
+    tol = BF16_TOL if w.dtype == "bf16" else F32_TOL
+    err = rel_inf(got, ref)
+    assert err <= tol, err
+    return run, err
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_layer_small(oracle, w):
+    check_layer(oracle, w)
+
+
+def test_layer_is_deterministic(oracle):
+    w = SMALL[2]
+    inp = margin_inputs(w, oracle)
+    a = LayerRun(w, inp)()
+    ya = a.y.clone()
+    a()
+    assert torch.equal(ya.view(torch.int16), a.y.view(torch.int16))
+
+
+def test_layer_empty_batch():
+    w = synth.MIXTRAL_PREFILL.replace(T=0, d_model=64, d_ff=128)
+    inp = synth.make_inputs(w, "cuda")
+    run = LayerRun(w, inp)()
+    assert run.status() == 0
+    assert run.counts.cpu().tolist() == [0] * w.n_experts
+
+
+FULL = [synth.MIXTRAL_PREFILL, *synth.MIXTRAL_DECODE, synth.DEEPSEEK_V3, synth.ZIPF]
+
+
+@pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
+def test_layer_full_size(oracle, w):
+    rows = sample_rows(w.T, 16, seed=w.seed)
+    run, err = check_layer(oracle, w, rows)
+    print(f"{w.name}: rel-inf error on {len(rows)} sampled tokens = {err:.3e}")

@@ -26,7 +26,7 @@ MUTATIONS = [
     ("selection_bias_in_gates", "r[e] = (double)rt[e];", "r[e] = (double)rt[e] + (sel_bias ? (double)sel_bias[e] : 0.0);"),
     ("logit_bias_dropped", "if (logit_bias) acc += logit_bias[e];", ""),
     ("no_renormalisation", "g[s] = p[idx[s]] / z;", "g[s] = p[idx[s]];"),
-    ("shared_expert_dropped", "G[k + s] = 1.0;", "G[k + s] = 0.0;"),
+    ("shared_expert_dropped", "G[q] = 1.0;", "G[q] = 0.0;"),
     ("permute_descending_tokens", "for (int t = 0; t < T; ++t)\n      for (int s = 0; s < k; ++s)\n        if (topk_idx", "for (int t = T - 1; t >= 0; --t)\n      for (int s = 0; s < k; ++s)\n        if (topk_idx"),
     ("balance_loss_without_N", "return alpha * (double)N * s;", "return alpha * s;"),
     ("f_over_tokens_not_assignments", "f[i] = (double)counts[i] / ((double)T * (double)k);", "f[i] = (double)counts[i] / (double)T;"),
