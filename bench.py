@@ -1,0 +1,449 @@
+"""Benchmark of the sparse top-k MoE layer forward on GB300.
+
+One step = one moe_layer_forward (router + top-k, permutation, grouped
+SwiGLU GEMMs, combine) over one batch of seeded synthetic tokens of the
+Mixtral-8x7B-shaped prefill layer (T=4096, d_model=4096, 8 experts, top-2,
+d_ff=14336, bf16). Prints one JSON line; see ``--help``.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain fp64 definition) on the
+host cores on a bounded sample of the same workload instead.
+With N > 1 (torchrun) every rank runs an independent replica on its own
+tokens (the layer is per-token; no collective on the data path); the
+barrier and the max-over-ranks of the elapsed time use a gloo group.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s; grouped-GEMM % bf16 tensor peak; decode % HBM BW"
+UNIT = "tokens/s"
+
+
+# ----------------------------------------------------------------- helpers --
+def world():
+    """(rank, world_size, local_rank) from the torchrun environment."""
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def init_group(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group("gloo")
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(v: float, ws: int) -> float:
+    """Max of a host float over all ranks (gloo)."""
+    if ws == 1:
+        return float(v)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 50 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [s.strip() for s in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        # Samples while the GPU is loaded: the highest-power half of the run.
+        pw = sorted((num(r[3]) or 0.0, i) for i, r in enumerate(rows))
+        loaded = [rows[i] for _, i in pw[len(pw) // 2:]] or rows
+        sm_loaded = [num(r[1]) for r in loaded if num(r[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in loaded:
+            for name, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm_loaded) if sm_loaded else None,
+                "sm_max_mhz": max(num(r[2]) or 0 for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(num(r[3]) or 0 for r in rows)}
+
+
+# ---------------------------------------------------------- work accounting --
+def gemm_flops(w):
+    rows = w.T * w.top_k + w.n_shared * w.T
+    return 4.0 * rows * w.d_model * w.d_ff, 2.0 * rows * w.d_ff * w.d_model
+
+
+def touched_weight_bytes(w, counts):
+    """Expert weight bytes a forward must read: every expert with a row."""
+    eb = 2 if w.dtype == "bf16" else 4
+    per = 3 * w.d_model * w.d_ff * eb
+    active = sum(1 for c in counts if c > 0) + w.n_shared
+    return active * per, active
+
+
+# ----------------------------------------------------------------- our arm --
+def run_ours(args):
+    import torch
+
+    import sparse_mixture_experts_router_gb300 as moe
+    from sparse_mixture_experts_router_gb300 import synth
+
+    rank, ws, local = world()
+    init_group(ws)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pk = peaks()
+    w = synth.MIXTRAL_PREFILL
+    inp = synth.make_inputs(w, dev, seed=w.seed + 1000 * rank)
+    cfg = moe.config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k, d_ff=w.d_ff,
+                     n_shared=w.n_shared, dtype=moe.MOE_BF16, gate_mode=w.gate_mode)
+    y = torch.empty(w.T, w.d_model, dtype=torch.bfloat16, device=dev)
+    idx = torch.empty(w.T, w.top_k, dtype=torch.int32, device=dev)
+    tw = torch.empty(w.T, w.top_k, dtype=torch.float32, device=dev)
+    counts = torch.empty(w.n_experts, dtype=torch.int32, device=dev)
+    ps = torch.empty(w.n_experts, dtype=torch.float32, device=dev)
+    wsp = moe.workspace(cfg, "layer", dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(x):
+        moe.moe_layer_forward(cfg, x, inp["w_router"], inp["logit_bias"], inp["sel_bias"],
+                              inp["w_gate"], inp["w_up"], inp["w_down"], y, idx, tw, counts, ps, wsp,
+                              stream)
+
+    for _ in range(args.warmup):
+        step(inp["x"])
+    torch.cuda.synchronize(dev)
+    st = moe.moe_stream_status(wsp, stream)
+    if st != 0:
+        raise RuntimeError(f"warm-up step failed on the device: {moe.status_string(st)}")
+
+    # ---- device-timed region: inputs resident in HBM -------------------------
+    clocks = ClockSampler(local)
+    clocks.start()
+    moe.profile_enable(True)
+    moe.profile_collect()  # drop anything recorded before
+    launches0 = moe.launch_count()
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    clocks.mark("t0")
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(inp["x"])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark("t1")
+    barrier(ws)
+    launches = moe.launch_count() - launches0
+    kern = moe.profile_collect()
+    moe.profile_enable(False)
+    clk = clocks.stop()
+    ms_local = e0.elapsed_time(e1)
+    ms_total = reduce_max(ms_local, ws)
+    ms_step = ms_total / args.steps
+    value = ws * w.T * args.steps / (ms_total / 1e3)
+
+    # ---- end to end through the C ABI with host buffers ----------------------
+    x_host = inp["x"].cpu().pin_memory()
+    y_host = torch.empty(w.T, w.d_model, dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(inp["x"])
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        step(x_dev)
+        y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        step(x_dev)
+        y_host.copy_(y, non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e2e_ms = reduce_max(f0.elapsed_time(f1), ws)
+    e2e_value = ws * w.T * args.steps / (e2e_ms / 1e3)
+    bytes_io = w.T * w.d_model * 2
+
+    # ---- roofline of the dominant kernel ---------------------------------------
+    f_gu, f_dn = gemm_flops(w)
+    per_kernel = {}
+    for name, (ms, n) in kern.items():
+        per_kernel[name] = {"ms_per_launch": ms / n, "launches": n,
+                            "share": ms / sum(v[0] for v in kern.values())}
+    gu_ms = per_kernel["gate_up"]["ms_per_launch"]
+    dn_ms = per_kernel["down"]["ms_per_launch"]
+    per_kernel["gate_up"]["tflops"] = f_gu / (gu_ms / 1e3) / 1e12
+    per_kernel["down"]["tflops"] = f_dn / (dn_ms / 1e3) / 1e12
+    gemm_tflops = (f_gu + f_dn) / ((gu_ms + dn_ms) / 1e3) / 1e12
+    ach = per_kernel["gate_up"]["tflops"]
+    roofline = {"bound": "tensor", "kernel": "gate_up (grouped SwiGLU gate+up GEMM)",
+                "achieved": round(ach, 1), "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": round(ach / pk["bf16"], 4), "traffic": args.traffic,
+                "peak_source": f"{pk['source']} bf16 burst",
+                "frac_of_sustained": round(ach / pk["bf16_sustained"], 4),
+                "algorithmic_flops_per_launch": f_gu,
+                "grouped_gemm_both_kernels_tflops": round(gemm_tflops, 1),
+                "grouped_gemm_both_kernels_frac": round(gemm_tflops / pk["bf16"], 4)}
+    # HBM-bound kernels of the step against the copy bandwidth
+    P = w.T * w.top_k
+    hb = {"router_topk": w.T * w.d_model * 2 + w.n_experts * w.d_model * 2 + P * 8,
+          "permute_gather": 2 * P * w.d_model * 2 + P * 4,
+          "combine": P * w.d_model * 2 + w.T * w.d_model * 2 + P * 4}
+    for name, b in hb.items():
+        if name in per_kernel:
+            gbs = b / (per_kernel[name]["ms_per_launch"] / 1e3) / 1e9
+            per_kernel[name]["gbs"] = round(gbs, 1)
+            per_kernel[name]["hbm_frac"] = round(gbs / pk["hbm"], 4)
+
+    decode = run_decode(moe, synth, dev, stream, pk, args) if not args.no_decode else None
+
+    if rank == 0:
+        cpu = None if args.no_cpu_baseline else cpu_baseline(inp, w, args)
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) random-init weights)",
+            "config": {"workload": w.name, "T": w.T, "d_model": w.d_model,
+                       "n_experts": w.n_experts, "top_k": w.top_k, "d_ff": w.d_ff,
+                       "n_shared": w.n_shared, "gate": "softmax over the kept top-2 scores",
+                       "parallelism": f"replicas x{ws} (per-token layer, no collective)",
+                       "l2": "inputs larger than L2: 2.82 GB of expert weights read every step"},
+            "tflops_grouped_gemm": round(gemm_tflops, 1),
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": bytes_io,
+                    "d2h_bytes_per_step": bytes_io,
+                    "path": "pinned host x -> H2D -> moe_layer_forward (C ABI) -> D2H y"},
+            "gpu_launches": int(launches),
+            "clocks": clk,
+            "kernels": per_kernel,
+            "decode": decode,
+        }
+        print(json.dumps(line))
+
+
+def run_decode(moe, synth, dev, stream, pk, args):
+    """Decode steps (T = 1, 8, 32, 64) of the same layer: weight streaming,
+    reported as algorithmic bytes / time against the HBM copy bandwidth. L2
+    is flushed (a 256 MB write) before every timed step."""
+    import torch
+    out = {}
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    base = synth.make_inputs(synth.MIXTRAL_DECODE[-1], dev)
+    for w in synth.MIXTRAL_DECODE:
+        x = base["x"][: w.T].contiguous()
+        cfg = moe.config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k,
+                         d_ff=w.d_ff, dtype=moe.MOE_BF16)
+        y = torch.empty(w.T, w.d_model, dtype=torch.bfloat16, device=dev)
+        counts = torch.empty(w.n_experts, dtype=torch.int32, device=dev)
+        wsp = moe.workspace(cfg, "layer", dev)
+
+        def step():
+            moe.moe_layer_forward(cfg, x, base["w_router"], None, None, base["w_gate"],
+                                  base["w_up"], base["w_down"], y, None, None, counts, None, wsp,
+                                  stream)
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize(dev)
+        times = []
+        for _ in range(max(5, min(args.steps, 50))):
+            flush.fill_(1)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+        wbytes, active = touched_weight_bytes(w, counts.cpu().tolist())
+        total = wbytes + w.n_experts * w.d_model * 2 + 2 * w.T * w.d_model * 2
+        gbs = total / (ms / 1e3) / 1e9
+        out[f"T{w.T}"] = {"ms": round(ms, 4), "experts_touched": active,
+                          "algorithmic_bytes": total, "gbs": round(gbs, 1),
+                          "hbm_frac": round(gbs / pk["hbm"], 4),
+                          "tokens_per_s": round(w.T / (ms / 1e3), 1)}
+    return out
+
+
+# ------------------------------------------------------------- CPU oracle ----
+def _oracle_sample(o, inp_host, w, rows):
+    """Oracle forward: routing of every token, layer output of `rows`."""
+    x, Wr, wg, wu, wd = inp_host
+    _, r32 = o.router_logits(x, Wr, None)
+    idx, tw, _, _ = o.route(r32, w.top_k, w.gate_mode, None)
+    need = sorted(set(idx[rows].ravel().tolist()))
+    experts = {e: (wg[e], wu[e], wd[e]) for e in need}
+    return o.layer_rows(x, experts, idx, tw, rows, w.n_experts, w.n_shared)
+
+
+def _host_inputs(inp):
+    from sparse_mixture_experts_router_gb300 import synth
+    return tuple(synth.bf16_bits(inp[k]) for k in ("x", "w_router", "w_gate", "w_up", "w_down"))
+
+
+def cpu_baseline(inp, w, args):
+    """The oracle as it stands, on this host's cores, on a bounded sample:
+    routing of all T tokens plus the layer output of n sampled tokens, timed
+    and scaled to tokens/s (tokens are independent, so per-token time
+    extrapolates)."""
+    import oracle
+    o = oracle.Oracle()
+    host = _host_inputs(inp)
+    n = args.cpu_tokens
+    rows = list(range(0, w.T, max(1, w.T // n)))[:n]
+    t0 = time.perf_counter()
+    _oracle_sample(o, host, w, rows)
+    dt = time.perf_counter() - t0
+    return {"value": round(len(rows) / dt, 3), "unit": UNIT, "cores": o.num_threads(),
+            "kind": "oracle",
+            "sample": f"routing of all {w.T} tokens + layer output of {len(rows)} of {w.T} tokens "
+                      f"(fp64 C oracle, OpenMP), {dt:.1f} s; tokens/s = {len(rows)} / time"}
+
+
+def run_reference(args):
+    """The CPU oracle timed on the host cores (rank 0 only)."""
+    rank, ws, local = world()
+    if rank != 0:
+        return
+    import torch
+
+    import oracle
+    from sparse_mixture_experts_router_gb300 import synth
+    w = synth.MIXTRAL_PREFILL
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    inp = synth.make_inputs(w, dev)
+    host = _host_inputs(inp)
+    del inp
+    o = oracle.Oracle()
+    n = args.ref_tokens
+    times = []
+    for i in range(args.warmup + args.steps):
+        rows = [((i * 997) + j * (w.T // n)) % w.T for j in range(n)]
+        t0 = time.perf_counter()
+        _oracle_sample(o, host, w, rows)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = n * len(times) / total
+    sample = (f"per step: routing of all {w.T} tokens + layer output of {n} of {w.T} tokens "
+              f"(fp64 C oracle, OpenMP); tokens/s = sampled tokens / time")
+    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * total / len(times), 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "d_model": w.d_model, "n_experts": w.n_experts,
+                       "top_k": w.top_k, "d_ff": w.d_ff},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "kind": "oracle",
+                             "cores": o.num_threads(), "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-tokens", type=int, default=48,
+                    help="sampled tokens of the CPU-oracle baseline")
+    ap.add_argument("--ref-tokens", type=int, default=4,
+                    help="sampled tokens per step of --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per gate_up launch from an ncu capture of this build")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
