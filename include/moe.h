@@ -143,6 +143,31 @@ MOE_API int moe_router_topk(const moe_config* cfg, const void* x, const void* w_
                     moe_stream_t stream);
 
 /*
+ * moe_router_topk for callers that cannot allocate: no workspace argument,
+ * and the library allocates nothing. The pages have no counterpart; this
+ * is an interface for callers whose device memory is all assigned in
+ * advance (a runtime's memory planner, or a plugin slot that passes an
+ * operator only its inputs and outputs), so they can neither call
+ * cudaMalloc nor hand over the scratch moe_router_topk takes.
+ * Arguments and results are those of moe_router_topk without ws/ws_bytes.
+ * The scratch (a status word and per-block probability partials) lives in
+ * a fixed 1 MiB array of the library's own device memory on every GPU that
+ * loads the library, held until the process exits:
+ *  - a call needs 256 + 4 * ceil(T / 32) * N bytes of it (for N = 256,
+ *    T <= 32736); a larger call returns MOE_ERR_WORKSPACE, launching nothing;
+ *  - the first call made with a device current looks up the array's device
+ *    address for that device; make that first call before any stream capture;
+ *  - all calls share the array: calls whose work overlaps on the GPU race
+ *    on it and give undefined results; order them on one stream;
+ *  - MOE_ERR_CUDA here leaves the CUDA error to cudaGetLastError.
+ */
+MOE_API int moe_router_topk_noalloc(const moe_config* cfg, const void* x,
+                    const void* w_router, const float* logit_bias,
+                    const float* sel_bias, const float* logits_in,
+                    float* logits_out, int32_t* topk_idx, float* topk_w,
+                    int32_t* counts, float* prob_sum, moe_stream_t stream);
+
+/*
  * Groups the T*k (token, slot) pairs by expert and gathers their token rows.
  * Pair p = t*k + slot. Rows are expert-major; inside one expert, ascending
  * pair id (a token cannot pick an expert twice, so ascending token). This

@@ -64,6 +64,7 @@ _SIGS = {
     "moe_grouped_workspace_size": (_SZ, [_CFG]),
     "moe_workspace_size": (_SZ, [_CFG]),
     "moe_router_topk": (_I, [_CFG] + [_P] * 10 + [_P, _SZ, _P]),
+    "moe_router_topk_noalloc": (_I, [_CFG] + [_P] * 10 + [_P]),
     "moe_permute": (_I, [_CFG] + [_P] * 6 + [_P, _SZ, _P]),
     "moe_grouped_swiglu": (_I, [_CFG] + [_P] * 9 + [_P, _SZ, _P]),
     "moe_combine": (_I, [_CFG, _P, _P, _P, _P, _P]),
@@ -152,6 +153,14 @@ def moe_router_topk(cfg, x, w_router, logit_bias, sel_bias, logits_in, logits_ou
         ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(sel_bias),
         _ptr(logits_in), _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _ptr(counts),
         _ptr(prob_sum), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def moe_router_topk_noalloc(cfg, x, w_router, logit_bias, sel_bias, logits_in, logits_out,
+                            topk_idx, topk_w, counts, prob_sum, stream=None):
+    _check("moe_router_topk_noalloc", lib().moe_router_topk_noalloc(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(sel_bias),
+        _ptr(logits_in), _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _ptr(counts),
+        _ptr(prob_sum), _stream(stream)))
 
 
 def moe_permute(cfg, x, topk_idx, expert_offsets, sorted_pair, inv_pos, x_perm, ws, stream=None):

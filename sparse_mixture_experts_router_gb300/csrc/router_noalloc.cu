@@ -1,0 +1,95 @@
+// moe_router_topk_noalloc: the router entry point for callers that cannot
+// allocate device memory and cannot hand the library a workspace.
+//
+// Some callers own every byte of device memory up front: an inference
+// runtime whose memory planner assigns all buffers before the first step,
+// or a plugin interface that gives an operator only its inputs and outputs
+// and has no workspace slot. They can neither call cudaMalloc nor pass the
+// scratch that moe_router_topk takes. This entry point runs the same router
+// kernels, with their scratch (one status word and the per-block
+// probability partials) in a fixed array of this library's own device
+// memory instead of a caller workspace.
+//
+// Limits and rules (also stated in include/moe.h):
+//  - The array is kNoallocScratchBytes (1 MiB) per GPU that loads the
+//    library, held until the process exits. A call needs
+//    256 + 4 * ceil(T / 32) * N bytes of it; a larger call returns
+//    MOE_ERR_WORKSPACE and launches nothing.
+//  - The array's device address is looked up once per device, by the first
+//    call made while that device is current; make that first call before
+//    any stream capture.
+//  - Every call shares the one array and it keeps the last call's contents.
+//    The status word is cleared at the start of every call; the partials are
+//    fully rewritten before they are read. Calls whose work overlaps on the
+//    GPU (different streams, or different host threads without ordering)
+//    race on the array and give undefined results.
+//  - Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+#include <mutex>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr size_t kNoallocScratchBytes = 1u << 20;  // 1 MiB
+constexpr size_t kStatusBytes = 256;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_router_scratch[kNoallocScratchBytes];
+
+std::mutex g_setup_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_router_scratch for the current device (looked up once
+// per device). Returns a cudaError_t.
+cudaError_t scratch_for_current_device(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> g(g_setup_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_router_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_router_topk_noalloc(const moe_config* cfg, const void* x, const void* w_router,
+                                       const float* logit_bias, const float* sel_bias,
+                                       const float* logits_in, float* logits_out,
+                                       int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                       float* prob_sum, moe_stream_t stream) {
+  int rc = moe_check_config(cfg);
+  if (rc != MOE_OK) return rc;
+  const moe_config& c = *cfg;
+  if (!counts || !prob_sum) return MOE_ERR_INVALID_ARG;
+  if (c.T > 0 && (!topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
+  if (c.T > 0 && !logits_in && (!x || !w_router)) return MOE_ERR_INVALID_ARG;
+  if (logits_in && logit_bias) return MOE_ERR_INVALID_ARG;
+  for (const void* p : {x, w_router, (const void*)logit_bias, (const void*)sel_bias,
+                        (const void*)logits_in, (const void*)logits_out, (const void*)topk_idx,
+                        (const void*)topk_w, (const void*)counts, (const void*)prob_sum})
+    if (p && ((uintptr_t)p % 16)) return MOE_ERR_MISALIGNED;
+  if (kStatusBytes + router_partials_bytes(c) > kNoallocScratchBytes) return MOE_ERR_WORKSPACE;
+
+  void* scratch = nullptr;
+  cudaError_t e = scratch_for_current_device(&scratch);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  int* status = static_cast<int*>(scratch);
+  float* partials = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + kStatusBytes);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  e = cudaMemsetAsync(status, 0, sizeof(int), s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_router(c, x, w_router, logit_bias, sel_bias, logits_in, logits_out, topk_idx, topk_w,
+                    counts, prob_sum, partials, status, s);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
