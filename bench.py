@@ -64,6 +64,33 @@ def reduce_max(v: float, ws: int) -> float:
     return float(t.item())
 
 
+def recorded_traffic():
+    """DRAM bytes per gate/up launch from the committed ncu summary, or None
+    when the kernel sources changed since that capture."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "grouped_gemm_mixtral_8x7b_prefill.md")
+    csrc = os.path.join(ROOT, "sparse_mixture_experts_router_gb300", "csrc")
+    try:
+        text = open(prof).read()
+        h = hashlib.sha256()
+        for f in ("grouped_sm103.cu", "sm103_ptx.cuh"):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().split(":")[0] in ("gate_up_dram_bytes_per_launch",
+                                                          "kernel_source_sha256"):
+            k, v = line.strip().split(":", 1)
+            vals[k] = v.strip()
+    if vals.get("kernel_source_sha256") != h.hexdigest()[:16]:
+        return None
+    try:
+        return float(vals["gate_up_dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -257,7 +284,8 @@ def run_ours(args):
     ach = per_kernel["gate_up"]["tflops"]
     roofline = {"bound": "tensor", "kernel": "gate_up (grouped SwiGLU gate+up GEMM)",
                 "achieved": round(ach, 1), "peak": pk["bf16"], "unit": "TFLOP/s",
-                "frac": round(ach / pk["bf16"], 4), "traffic": args.traffic,
+                "frac": round(ach / pk["bf16"], 4),
+                "traffic": args.traffic if args.traffic is not None else recorded_traffic(),
                 "peak_source": f"{pk['source']} bf16 burst",
                 "frac_of_sustained": round(ach / pk["bf16_sustained"], 4),
                 "algorithmic_flops_per_launch": f_gu,
