@@ -29,6 +29,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer tokens/s; grouped-GEMM % bf16 tensor peak; decode % HBM BW"
+# fp32 FMA peak from unit counts and the maximum clock: 152 SMs x 128 lanes x 2 flop x 2.07 GHz
+FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 UNIT = "tokens/s"
 
 
@@ -195,7 +197,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pk = peaks()
-    w = synth.MIXTRAL_PREFILL
+    w = WORKLOADS[args.workload](synth)
     inp = synth.make_inputs(w, dev, seed=w.seed + 1000 * rank)
     cfg = moe.config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k, d_ff=w.d_ff,
                      n_shared=w.n_shared, dtype=moe.MOE_BF16, gate_mode=w.gate_mode)
@@ -212,6 +214,7 @@ def run_ours(args):
                               inp["w_gate"], inp["w_up"], inp["w_down"], y, idx, tw, counts, ps, wsp,
                               stream)
 
+    default = args.workload == DEFAULT_WORKLOAD
     for _ in range(args.warmup):
         step(inp["x"])
     torch.cuda.synchronize(dev)
@@ -295,17 +298,26 @@ def run_ours(args):
     P = w.T * w.top_k
     hb = {"router_topk": w.T * w.d_model * 2 + w.n_experts * w.d_model * 2 + P * 8,
           "permute_gather": 2 * P * w.d_model * 2 + P * 4,
-          "combine": P * w.d_model * 2 + w.T * w.d_model * 2 + P * 4}
+          "combine": (P + w.n_shared * w.T) * w.d_model * 2 + w.T * w.d_model * 2 + P * 4}
+    if "router_topk" in per_kernel:  # fp32 FMA work of the router scores
+        fl = 2.0 * w.T * w.n_experts * w.d_model
+        tf = fl / (per_kernel["router_topk"]["ms_per_launch"] / 1e3) / 1e12
+        per_kernel["router_topk"]["fp32_tflops"] = round(tf, 2)
+        per_kernel["router_topk"]["fp32_alu_frac"] = round(tf / FP32_ALU_PEAK_TFLOPS, 4)
     for name, b in hb.items():
         if name in per_kernel:
             gbs = b / (per_kernel[name]["ms_per_launch"] / 1e3) / 1e9
             per_kernel[name]["gbs"] = round(gbs, 1)
             per_kernel[name]["hbm_frac"] = round(gbs / pk["hbm"], 4)
 
-    decode = run_decode(moe, synth, dev, stream, pk, args) if not args.no_decode else None
+    decode = run_decode(moe, synth, dev, stream, pk, args) if default and not args.no_decode else None
+    E = w.n_experts + w.n_shared
+    wb = 3 * E * w.d_model * w.d_ff * 2
+    routing = {"max_over_mean_expert_load": round(float(counts.max()) / max(1e-9, float(counts.float().mean())), 3),
+               "experts_with_tokens": int((counts > 0).sum())}
 
     if rank == 0:
-        cpu = None if args.no_cpu_baseline else cpu_baseline(inp, w, args)
+        cpu = None if (args.no_cpu_baseline or not default) else cpu_baseline(inp, w, args)
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -313,9 +325,13 @@ def run_ours(args):
             "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) random-init weights)",
             "config": {"workload": w.name, "T": w.T, "d_model": w.d_model,
                        "n_experts": w.n_experts, "top_k": w.top_k, "d_ff": w.d_ff,
-                       "n_shared": w.n_shared, "gate": "softmax over the kept top-2 scores",
+                       "n_shared": w.n_shared,
+                       "gate": ["softmax over the kept top-k scores",
+                                "softmax over all scores, kept ones renormalised"][w.gate_mode],
+                       "selection_bias": w.sel_bias, "zipf_offset_s": w.zipf_s or None,
                        "parallelism": f"replicas x{ws} (per-token layer, no collective)",
-                       "l2": "inputs larger than L2: 2.82 GB of expert weights read every step"},
+                       "l2": f"inputs larger than L2: {wb / 1e9:.2f} GB of expert weights read every step"},
+            "routing": routing,
             "tflops_grouped_gemm": round(gemm_tflops, 1),
             "roofline": roofline,
             "cpu_baseline": cpu,
@@ -451,12 +467,22 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+DEFAULT_WORKLOAD = "mixtral_8x7b_prefill"
+WORKLOADS = {
+    "mixtral_8x7b_prefill": lambda synth: synth.MIXTRAL_PREFILL,
+    "deepseek_v3_moe": lambda synth: synth.DEEPSEEK_V3,
+    "zipf_imbalanced": lambda synth: synth.ZIPF,
+}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD,
+                    help="layer shape to time (the default is the one the metric is quoted on)")
     ap.add_argument("--cpu-tokens", type=int, default=48,
                     help="sampled tokens of the CPU-oracle baseline")
     ap.add_argument("--ref-tokens", type=int, default=4,

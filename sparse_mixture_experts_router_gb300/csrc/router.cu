@@ -8,14 +8,24 @@
 // "The bare mechanism" (affinity softmax over all experts, renormalised
 // top-k weights, a routing bias that only moves the choice).
 //
-// One block scores 32 tokens against all N experts on the CUDA cores (fp32
-// FMA over d_model, operands staged through shared memory), keeps the
-// [32 x N] score tile in shared memory, then each warp selects the top k of
-// four tokens with warp shuffles: k rounds of a (key desc, index asc)
-// argmax, so equal keys go to the lower index. Counts use shared-memory
-// integer atomics (order-free, so exact); the per-expert probability sums
-// are added in a fixed order (tokens of a warp, warps of a block, then
-// blocks in a separate pass), so results are bitwise reproducible.
+// Scores are fp32 dot products on the CUDA cores, in one of two kernels:
+//  - few experts (N <= 32, W_r fits in shared memory): the whole of W_r is
+//    staged in shared memory once per block; each warp streams the rows of
+//    1-4 tokens once from HBM with 16-byte loads, accumulates all N dot
+//    products per lane and reduces them across the warp. Bound by HBM
+//    (reading x once).
+//  - many experts: a register-tiled block GEMM. A block scores 64 tokens
+//    against all N (<= 256) experts; each thread owns a TM x 8 tile
+//    (tokens x consecutive experts); 32-wide K slices of x and W_r are
+//    staged transposed in shared memory with the next slice prefetched into
+//    registers. Bound by fp32 FMA throughput.
+// Both hand every token to the same warp-level selection: lane l holds the
+// scores of experts l, l+32, ...; k rounds of a (key desc, index asc) warp
+// argmax choose the top k (equal keys go to the lower index); the gates and
+// the full softmax come from the unbiased scores. Counts use shared-memory
+// integer atomics (order-free, exact); the per-expert probability sums are
+// added in a fixed order (tokens of a warp, warps of a block, then blocks in
+// a separate pass), so the results are bitwise reproducible.
 #include <float.h>
 
 #include "device_util.cuh"
@@ -26,9 +36,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kTok = kRouterTokens;          // 32 tokens per block
-constexpr int kTokPerWarp = kTok / kWarps;   // 4
-constexpr int kKC = 32;                      // d_model chunk staged in smem
+constexpr int kTileTokens = 64;              // tokens per block, tiled kernel
+constexpr int kKC = 32;                      // K slice of the tiled kernel
+constexpr size_t kSmallSmemLimit = 200 * 1024;
 
 struct RouterArgs {
   const void* x;
@@ -45,210 +55,376 @@ struct RouterArgs {
   int T, d, N, k, gate_mode;
 };
 
-// Four consecutive elements of a row as fp32 (index must be a multiple of 4).
-__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
-  float4 q = *reinterpret_cast<const float4*>(p);
-  v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-}
-__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
-  uint2 q = *reinterpret_cast<const uint2*>(p);
-  bf16x2_to_f32(q.x, v[0], v[1]);
-  bf16x2_to_f32(q.y, v[2], v[3]);
-}
+// Eight (bf16) or four (fp32) elements of a 16-byte vector as fp32.
+template <typename TX> struct V16;
+template <> struct V16<__nv_bfloat16> {
+  static constexpr int n = 8;
+  __device__ static void cvt(const uint4& q, float* f) {
+    bf16x2_to_f32(q.x, f[0], f[1]);
+    bf16x2_to_f32(q.y, f[2], f[3]);
+    bf16x2_to_f32(q.z, f[4], f[5]);
+    bf16x2_to_f32(q.w, f[6], f[7]);
+  }
+};
+template <> struct V16<float> {
+  static constexpr int n = 4;
+  __device__ static void cvt(const uint4& q, float* f) {
+    f[0] = __uint_as_float(q.x); f[1] = __uint_as_float(q.y);
+    f[2] = __uint_as_float(q.z); f[3] = __uint_as_float(q.w);
+  }
+};
 
-// (key, index) ordering of the top-k: larger key first, then lower index.
+// (key, index) order of the top-k: larger key first, then lower index.
 __device__ __forceinline__ bool better(float ka, int ia, float kb, int ib) {
   return ka > kb || (ka == kb && ia < ib);
 }
 
-// EJ = experts handled per lane (N <= 32 * EJ).
-template <typename TX, int EJ>
-__global__ void __launch_bounds__(kThreads) router_topk_kernel(const RouterArgs a) {
-  extern __shared__ float smem[];
+// Selection, gates and statistics of one token, by one full warp. r[j] is
+// the unbiased score of expert lane + 32*j (any value where that index is
+// >= N). Adds softmax(r) to psum and the kept experts to bcount; lane 0
+// writes topk_idx / topk_w.
+template <int EJ>
+__device__ __forceinline__ void select_token(const float (&r)[EJ], int lane, long long t,
+                                             const RouterArgs& a, float (&psum)[EJ],
+                                             int* bcount) {
   const int N = a.N;
-  const int NP = 32 * EJ;                       // padded expert count
-  float* xs = smem;                             // [kTok][kKC]
-  float* wsm = xs + kTok * kKC;                 // [NP][kKC + 1]
-  float* lt = wsm + NP * (kKC + 1);             // [kTok][NP] scores
-  float* wprob = lt + kTok * NP;                // [kWarps][NP]
-  int* bcount = reinterpret_cast<int*>(wprob + kWarps * NP);  // [NP]
+  float key[EJ];
+#pragma unroll
+  for (int j = 0; j < EJ; ++j) {
+    const int e = lane + 32 * j;
+    key[j] = (e < N && a.sel_bias) ? __fadd_rn(r[j], a.sel_bias[e]) : r[j];
+  }
+  // Full softmax over the N unbiased scores (the affinity probabilities).
+  float m = -FLT_MAX;
+#pragma unroll
+  for (int j = 0; j < EJ; ++j)
+    if (lane + 32 * j < N) m = fmaxf(m, r[j]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float p[EJ];
+  float z = 0.f;
+#pragma unroll
+  for (int j = 0; j < EJ; ++j) {
+    p[j] = (lane + 32 * j < N) ? expf(r[j] - m) : 0.f;
+    z += p[j];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+#pragma unroll
+  for (int j = 0; j < EJ; ++j) psum[j] += p[j] / z;
 
-  const int tid = threadIdx.x;
-  const int warp = tid / 32;
-  const int lane = tid % 32;
-  const int t0 = blockIdx.x * kTok;
+  // k rounds of warp argmax over (key, index).
+  uint32_t taken = 0;
+  int sel[kMaxTopK];
+  float rsel[kMaxTopK];
+  for (int s = 0; s < a.k; ++s) {
+    float bk = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < EJ; ++j) {
+      const int e = lane + 32 * j;
+      if (e < N && !(taken & (1u << j)) && better(key[j], e, bk, bi)) {
+        bk = key[j];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (better(ok, oi, bk, bi)) {
+        bk = ok;
+        bi = oi;
+      }
+    }
+    sel[s] = bi;
+    float mine = 0.f;
+#pragma unroll
+    for (int j = 0; j < EJ; ++j)
+      if (j == (bi >> 5)) mine = r[j];
+    rsel[s] = __shfl_sync(0xffffffffu, mine, bi & 31);
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+  }
+  if (lane == 0) {
+    float g[kMaxTopK];
+    if (a.gate_mode == MOE_GATE_TOPK_SOFTMAX) {
+      float mk = rsel[0];
+      for (int s = 1; s < a.k; ++s) mk = fmaxf(mk, rsel[s]);
+      float zs = 0.f;
+      for (int s = 0; s < a.k; ++s) {
+        g[s] = expf(rsel[s] - mk);
+        zs += g[s];
+      }
+      for (int s = 0; s < a.k; ++s) g[s] = g[s] / zs;
+    } else {
+      float zs = 0.f;
+      for (int s = 0; s < a.k; ++s) {
+        g[s] = expf(rsel[s] - m) / z;
+        zs += g[s];
+      }
+      for (int s = 0; s < a.k; ++s) g[s] = g[s] / zs;
+    }
+    for (int s = 0; s < a.k; ++s) {
+      a.topk_idx[t * a.k + s] = sel[s];
+      a.topk_w[t * a.k + s] = g[s];
+      atomicAdd(&bcount[sel[s]], 1);
+    }
+  }
+}
 
-  for (int e = tid; e < NP; e += kThreads) bcount[e] = 0;
+// Per-block probability partial (warps summed in order) and counts.
+template <int EJ>
+__device__ __forceinline__ void finish_block(const float (&psum)[EJ], float* wprob, int* bcount,
+                                             const RouterArgs& a) {
+  const int NP = 32 * EJ;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+#pragma unroll
+  for (int j = 0; j < EJ; ++j) wprob[warp * NP + lane + 32 * j] = psum[j];
+  __syncthreads();
+  for (int e = threadIdx.x; e < a.N; e += kThreads) {
+    float s = 0.f;
+    for (int w = 0; w < kWarps; ++w) s += wprob[w * NP + e];
+    a.partials[(size_t)blockIdx.x * a.N + e] = s;
+    if (bcount[e]) atomicAdd(&a.counts[e], bcount[e]);
+  }
+}
 
-  // ---- scores -------------------------------------------------------------
+// ---------------------------------------------------------------------------
+// Few experts: W_r in shared memory, x streamed once. NP = padded N (8, 16
+// or 32), TPW tokens per warp at a time (NP * TPW = 32 accumulators).
+template <typename TX, int NP, int TPW>
+__global__ void __launch_bounds__(kThreads) router_small_kernel(const RouterArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  constexpr int EPV = V16<TX>::n;
+  constexpr int U = 4;  // 16-byte vectors per lane in flight per token
+  const int N = a.N;
+  const int vec = a.d / EPV;  // 16-byte vectors per row
+  uint4* wsm = reinterpret_cast<uint4*>(smem_raw);
+  float* wprob = reinterpret_cast<float*>(wsm + (size_t)N * vec);
+  int* bcount = reinterpret_cast<int*>(wprob + kWarps * 32);
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+
+  const uint4* wg = static_cast<const uint4*>(a.w);
+  for (int i = tid; i < N * vec; i += kThreads) wsm[i] = __ldg(wg + i);
+  if (tid < 32) bcount[tid] = 0;
+  __syncthreads();
+
+  const uint4* x = static_cast<const uint4*>(a.x);
+  float psum[1] = {0.f};
+  const int gw = blockIdx.x * kWarps + warp, nw = gridDim.x * kWarps;
+  for (long long t0 = (long long)gw * TPW; t0 < a.T; t0 += (long long)nw * TPW) {
+    float acc[TPW][NP];
+#pragma unroll
+    for (int q = 0; q < TPW; ++q)
+#pragma unroll
+      for (int e = 0; e < NP; ++e) acc[q][e] = 0.f;
+    for (int v0 = 0; v0 < vec; v0 += 32 * U) {
+      uint4 xv[TPW][U];
+#pragma unroll
+      for (int q = 0; q < TPW; ++q)
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + u * 32 + lane;
+          xv[q][u] = (t0 + q < a.T && v < vec) ? __ldg(x + (t0 + q) * vec + v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v >= vec) break;
+        float xf[TPW][EPV];
+#pragma unroll
+        for (int q = 0; q < TPW; ++q) V16<TX>::cvt(xv[q][u], xf[q]);
+#pragma unroll
+        for (int e = 0; e < NP; ++e) {
+          if (e >= N) break;
+          float wf[EPV];
+          V16<TX>::cvt(wsm[e * vec + v], wf);
+#pragma unroll
+          for (int q = 0; q < TPW; ++q)
+#pragma unroll
+            for (int i = 0; i < EPV; ++i) acc[q][e] = fmaf(xf[q][i], wf[i], acc[q][e]);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < TPW; ++q) {
+      if (t0 + q >= a.T) break;  // warp-uniform
+#pragma unroll
+      for (int e = 0; e < NP; ++e)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[q][e] += __shfl_xor_sync(0xffffffffu, acc[q][e], o);
+      float r[1] = {0.f};
+#pragma unroll
+      for (int e = 0; e < NP; ++e)
+        if (e == lane) r[0] = acc[q][e];
+      if (lane < N && a.logit_bias) r[0] = __fadd_rn(r[0], a.logit_bias[lane]);
+      if (a.logits_out && lane < N) a.logits_out[(t0 + q) * N + lane] = r[0];
+      select_token<1>(r, lane, t0 + q, a, psum, bcount);
+    }
+  }
+  finish_block<1>(psum, wprob, bcount, a);
+}
+
+// ---------------------------------------------------------------------------
+// Many experts: 64 tokens x (32*EJ) experts per block, register tiles.
+template <typename TX, int EJ>
+__global__ void __launch_bounds__(kThreads) router_tiled_kernel(const RouterArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  constexpr int BN = 32 * EJ;            // padded experts
+  constexpr int BM = kTileTokens;        // 64 tokens
+  constexpr int NEG = BN / 8;            // expert groups of 8
+  constexpr int TM = BN / 32;            // tokens per thread (BM = 256/NEG * TM)
+  constexpr int XV = (BM * kKC) / (8 * kThreads);   // 8-element vectors of x per thread (1)
+  constexpr int WVEC = BN * kKC / 8;                  // 8-element vectors of a W slice
+  constexpr int WV = (WVEC + kThreads - 1) / kThreads;
+  constexpr int REGION = (BM * BN > kKC * (BM + BN)) ? BM * BN : kKC * (BM + BN);
+  static_assert(BM == (kThreads / NEG) * TM, "tile shape");
+  static_assert(XV == 1, "x slice: one 8-element vector per thread");
+
+  float* xs = reinterpret_cast<float*>(smem_raw);          // [kKC][BM]
+  float* wsm = xs + kKC * BM;                              // [kKC][BN]
+  float* lt = reinterpret_cast<float*>(smem_raw);          // [BM][BN], reuses xs/wsm
+  float* wprob = lt + REGION;                              // [kWarps][BN]
+  int* bcount = reinterpret_cast<int*>(wprob + kWarps * BN);
+
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int eg = tid % NEG, tg = tid / NEG;
+  const long long t0 = (long long)blockIdx.x * BM;
+  const int N = a.N;
+  for (int e = tid; e < BN; e += kThreads) bcount[e] = 0;
+
   if (a.logits_in == nullptr) {
     const TX* x = static_cast<const TX*>(a.x);
     const TX* w = static_cast<const TX*>(a.w);
-    float acc[kTokPerWarp][EJ];
+    // global -> register mapping of one K slice
+    const int xt = tid % BM, xk = (tid / BM) * 8;
+    int we[WV], wk[WV];
+    bool wact[WV];
 #pragma unroll
-    for (int i = 0; i < kTokPerWarp; ++i)
+    for (int i = 0; i < WV; ++i) {
+      const int idx = tid + kThreads * i;
+      wact[i] = idx < WVEC;
+      we[i] = idx % BN;
+      wk[i] = (idx / BN) * 8;
+    }
+    float xr[8], wr[WV][8];
+    auto load_slice = [&](int k0) {
+      const long long t = t0 + xt;
+      float f[8];
+      if (t < a.T && k0 + xk < a.d) {
+        if (sizeof(TX) == 2) {
+          V16<TX>::cvt(__ldg(reinterpret_cast<const uint4*>(x + t * a.d + k0 + xk)), f);
+        } else {
+          V16<TX>::cvt(__ldg(reinterpret_cast<const uint4*>(x + t * a.d + k0 + xk)), f);
+          V16<TX>::cvt(__ldg(reinterpret_cast<const uint4*>(x + t * a.d + k0 + xk + 4)), f + 4);
+        }
+      } else {
 #pragma unroll
-      for (int j = 0; j < EJ; ++j) acc[i][j] = 0.f;
+        for (int q = 0; q < 8; ++q) f[q] = 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) xr[q] = f[q];
+#pragma unroll
+      for (int i = 0; i < WV; ++i) {
+        if (wact[i] && we[i] < N && k0 + wk[i] < a.d) {
+          const TX* src = w + (size_t)we[i] * a.d + k0 + wk[i];
+          if (sizeof(TX) == 2) {
+            V16<TX>::cvt(__ldg(reinterpret_cast<const uint4*>(src)), wr[i]);
+          } else {
+            V16<TX>::cvt(__ldg(reinterpret_cast<const uint4*>(src)), wr[i]);
+            V16<TX>::cvt(__ldg(reinterpret_cast<const uint4*>(src + 4)), wr[i] + 4);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) wr[i][q] = 0.f;
+        }
+      }
+    };
+    float acc[TM][8];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
+    load_slice(0);
     for (int k0 = 0; k0 < a.d; k0 += kKC) {
-      // x chunk: 32 tokens x 32 columns, 4 columns per thread.
-      {
-        const int r = tid / 8, c = (tid % 8) * 4;
-        const int t = t0 + r;
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (t < a.T && k0 + c < a.d) load4(x + (size_t)t * a.d + k0 + c, v);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) xs[r * kKC + c + q] = v[q];
-      }
-      // router weight chunk: N rows x 32 columns.
-      for (int i = tid; i < NP * 8; i += kThreads) {
-        const int r = i / 8, c = (i % 8) * 4;
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (r < N && k0 + c < a.d) load4(w + (size_t)r * a.d + k0 + c, v);
+      for (int q = 0; q < 8; ++q) xs[(xk + q) * BM + xt] = xr[q];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) wsm[r * (kKC + 1) + c + q] = v[q];
-      }
+      for (int i = 0; i < WV; ++i)
+        if (wact[i])
+#pragma unroll
+          for (int q = 0; q < 8; ++q) wsm[(wk[i] + q) * BN + we[i]] = wr[i][q];
       __syncthreads();
-#pragma unroll 8
+      if (k0 + kKC < a.d) load_slice(k0 + kKC);
+#pragma unroll 4
       for (int kk = 0; kk < kKC; ++kk) {
-        float xv[kTokPerWarp], wv[EJ];
+        float av[TM], bv[8];
+        if (TM >= 4) {
 #pragma unroll
-        for (int i = 0; i < kTokPerWarp; ++i) xv[i] = xs[(warp * kTokPerWarp + i) * kKC + kk];
+          for (int i = 0; i < TM; i += 4) {
+            const float4 q4 = *reinterpret_cast<const float4*>(xs + kk * BM + tg * TM + i);
+            av[i] = q4.x; av[i + 1] = q4.y; av[i + 2] = q4.z; av[i + 3] = q4.w;
+          }
+        } else {
 #pragma unroll
-        for (int j = 0; j < EJ; ++j) wv[j] = wsm[(lane + 32 * j) * (kKC + 1) + kk];
+          for (int i = 0; i < TM; ++i) av[i] = xs[kk * BM + tg * TM + i];
+        }
+        const float4 b0 = *reinterpret_cast<const float4*>(wsm + kk * BN + eg * 8);
+        const float4 b1 = *reinterpret_cast<const float4*>(wsm + kk * BN + eg * 8 + 4);
+        bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
+        bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
 #pragma unroll
-        for (int i = 0; i < kTokPerWarp; ++i)
+        for (int i = 0; i < TM; ++i)
 #pragma unroll
-          for (int j = 0; j < EJ; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
+          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
       }
       __syncthreads();
     }
+    // scores (+ logit bias) into the [BM][BN] tile
 #pragma unroll
-    for (int i = 0; i < kTokPerWarp; ++i)
+    for (int i = 0; i < TM; ++i) {
+      float o[8];
 #pragma unroll
-      for (int j = 0; j < EJ; ++j) {
-        const int e = lane + 32 * j;
-        float r = acc[i][j];
-        if (e < N && a.logit_bias) r = __fadd_rn(r, a.logit_bias[e]);
-        lt[(warp * kTokPerWarp + i) * NP + e] = r;
+      for (int j = 0; j < 8; ++j) {
+        const int e = eg * 8 + j;
+        o[j] = (e < N && a.logit_bias) ? __fadd_rn(acc[i][j], a.logit_bias[e]) : acc[i][j];
       }
+      float* dst = lt + (size_t)(tg * TM + i) * BN + eg * 8;
+      *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<float4*>(dst + 4) = make_float4(o[4], o[5], o[6], o[7]);
+    }
   } else {
-    for (int i = tid; i < kTok * NP; i += kThreads) {
-      const int r = i / NP, e = i % NP;
-      const int t = t0 + r;
-      lt[i] = (t < a.T && e < N) ? a.logits_in[(size_t)t * N + e] : 0.f;
+    for (int i = tid; i < BM * BN; i += kThreads) {
+      const int r = i / BN, e = i % BN;
+      const long long t = t0 + r;
+      lt[i] = (t < a.T && e < N) ? a.logits_in[t * N + e] : 0.f;
     }
   }
   __syncthreads();
 
   if (a.logits_out) {
-    for (int i = tid; i < kTok * N; i += kThreads) {
+    for (int i = tid; i < BM * N; i += kThreads) {
       const int r = i / N, e = i % N;
-      if (t0 + r < a.T) a.logits_out[(size_t)(t0 + r) * N + e] = lt[r * NP + e];
+      if (t0 + r < a.T) a.logits_out[(t0 + r) * N + e] = lt[r * BN + e];
     }
   }
 
-  // ---- top-k, gates, statistics: one warp per 4 tokens -----------------------
   float psum[EJ];
 #pragma unroll
   for (int j = 0; j < EJ; ++j) psum[j] = 0.f;
-
-  for (int i = 0; i < kTokPerWarp; ++i) {
-    const int tl = warp * kTokPerWarp + i;
-    const int t = t0 + tl;
+  constexpr int TPW_SEL = BM / kWarps;  // 8 tokens per warp
+  for (int i = 0; i < TPW_SEL; ++i) {
+    const int tl = warp * TPW_SEL + i;
+    const long long t = t0 + tl;
     if (t >= a.T) break;  // warp-uniform
-    float r[EJ], key[EJ];
+    float r[EJ];
 #pragma unroll
-    for (int j = 0; j < EJ; ++j) {
-      const int e = lane + 32 * j;
-      r[j] = (e < N) ? lt[tl * NP + e] : -FLT_MAX;
-      key[j] = (e < N && a.sel_bias) ? __fadd_rn(r[j], a.sel_bias[e]) : r[j];
-    }
-    // Full softmax over the N unbiased scores (the affinity probabilities).
-    float m = -FLT_MAX;
-#pragma unroll
-    for (int j = 0; j < EJ; ++j)
-      if (lane + 32 * j < N) m = fmaxf(m, r[j]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float p[EJ];
-    float z = 0.f;
-#pragma unroll
-    for (int j = 0; j < EJ; ++j) {
-      p[j] = (lane + 32 * j < N) ? expf(r[j] - m) : 0.f;
-      z += p[j];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-#pragma unroll
-    for (int j = 0; j < EJ; ++j) {
-      p[j] = p[j] / z;
-      psum[j] += p[j];
-    }
-
-    // k rounds of warp argmax over (key, index).
-    uint32_t taken = 0;
-    int sel[kMaxTopK];
-    float rsel[kMaxTopK];
-    for (int s = 0; s < a.k; ++s) {
-      float bk = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int j = 0; j < EJ; ++j) {
-        const int e = lane + 32 * j;
-        if (e < N && !(taken & (1u << j)) && better(key[j], e, bk, bi)) {
-          bk = key[j];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (better(ok, oi, bk, bi)) {
-          bk = ok;
-          bi = oi;
-        }
-      }
-      sel[s] = bi;
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      rsel[s] = lt[tl * NP + bi];
-    }
-    if (lane == 0) {
-      float g[kMaxTopK];
-      if (a.gate_mode == MOE_GATE_TOPK_SOFTMAX) {
-        float mk = rsel[0];
-        for (int s = 1; s < a.k; ++s) mk = fmaxf(mk, rsel[s]);
-        float zs = 0.f;
-        for (int s = 0; s < a.k; ++s) {
-          g[s] = expf(rsel[s] - mk);
-          zs += g[s];
-        }
-        for (int s = 0; s < a.k; ++s) g[s] = g[s] / zs;
-      } else {
-        float zs = 0.f;
-        for (int s = 0; s < a.k; ++s) {
-          g[s] = expf(rsel[s] - m) / z;
-          zs += g[s];
-        }
-        for (int s = 0; s < a.k; ++s) g[s] = g[s] / zs;
-      }
-      for (int s = 0; s < a.k; ++s) {
-        a.topk_idx[(size_t)t * a.k + s] = sel[s];
-        a.topk_w[(size_t)t * a.k + s] = g[s];
-        atomicAdd(&bcount[sel[s]], 1);
-      }
-    }
+    for (int j = 0; j < EJ; ++j) r[j] = lt[tl * BN + lane + 32 * j];
+    select_token<EJ>(r, lane, t, a, psum, bcount);
   }
-#pragma unroll
-  for (int j = 0; j < EJ; ++j) wprob[warp * NP + lane + 32 * j] = psum[j];
-  __syncthreads();
-  for (int e = tid; e < N; e += kThreads) {
-    float s = 0.f;
-    for (int w = 0; w < kWarps; ++w) s += wprob[w * NP + e];
-    a.partials[(size_t)blockIdx.x * N + e] = s;
-    if (bcount[e]) atomicAdd(&a.counts[e], bcount[e]);
-  }
+  __syncthreads();  // lt is read above; wprob does not alias it, bcount does not either
+  finish_block<EJ>(psum, wprob, bcount, a);
 }
 
 // prob_sum[e] = sum over blocks, in block order.
@@ -260,32 +436,65 @@ __global__ void router_reduce_kernel(const float* partials, int nblk, int N, flo
   prob_sum[e] = s;
 }
 
-template <typename TX, int EJ>
-cudaError_t launch_t(const RouterArgs& a, int nblk, cudaStream_t s) {
-  const int NP = 32 * EJ;
-  const size_t smem = sizeof(float) * ((size_t)kTok * kKC + (size_t)NP * (kKC + 1) +
-                                       (size_t)kTok * NP + (size_t)kWarps * NP) +
-                      sizeof(int) * NP;
-  cudaError_t e = cudaFuncSetAttribute(router_topk_kernel<TX, EJ>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+template <typename K>
+cudaError_t launch_k(K kernel, const RouterArgs& a, int grid, size_t smem, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   ProfScope p(K_ROUTER, s);
-  router_topk_kernel<TX, EJ><<<nblk, kThreads, smem, s>>>(a);
+  kernel<<<grid, kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
+size_t small_smem(const moe_config& c) {
+  return (size_t)c.n_experts * c.d_model * elem_bytes(c.dtype) + sizeof(float) * kWarps * 32 +
+         sizeof(int) * 32;
+}
+
+bool use_small(const moe_config& c, const float* logits_in) {
+  return logits_in == nullptr && c.n_experts <= 32 && small_smem(c) <= kSmallSmemLimit;
+}
+
+int router_grid(const moe_config& c, const float* logits_in) {
+  if (use_small(c, logits_in)) {
+    // never more blocks than ceil(T/32): the partials buffer is sized for that
+    const int per_sm = (int)((227 * 1024) / small_smem(c));
+    const int cap = num_sms() * (per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm));
+    const int g = ceil_div(c.T, kRouterTokens);
+    return g < cap ? g : cap;
+  }
+  return ceil_div(c.T, kTileTokens);
+}
+
 template <typename TX>
-cudaError_t launch_dtype(const RouterArgs& a, int nblk, cudaStream_t s) {
-  if (a.N <= 32) return launch_t<TX, 1>(a, nblk, s);
-  if (a.N <= 64) return launch_t<TX, 2>(a, nblk, s);
-  if (a.N <= 128) return launch_t<TX, 4>(a, nblk, s);
-  return launch_t<TX, 8>(a, nblk, s);
+cudaError_t launch_dtype(const moe_config& c, const RouterArgs& a, int grid, cudaStream_t s) {
+  if (use_small(c, a.logits_in)) {
+    const size_t sm = small_smem(c);
+    if (c.n_experts <= 8) return launch_k(router_small_kernel<TX, 8, 4>, a, grid, sm, s);
+    if (c.n_experts <= 16) return launch_k(router_small_kernel<TX, 16, 2>, a, grid, sm, s);
+    return launch_k(router_small_kernel<TX, 32, 1>, a, grid, sm, s);
+  }
+  auto smem = [](int BN) {  // must match the layout in router_tiled_kernel
+    const size_t tile = sizeof(float) * (size_t)kTileTokens * BN;
+    const size_t slices = sizeof(float) * (size_t)kKC * (kTileTokens + BN);
+    return (tile > slices ? tile : slices) + sizeof(float) * kWarps * BN + sizeof(int) * BN;
+  };
+  if (c.n_experts <= 32) return launch_k(router_tiled_kernel<TX, 1>, a, grid, smem(32), s);
+  if (c.n_experts <= 64) return launch_k(router_tiled_kernel<TX, 2>, a, grid, smem(64), s);
+  if (c.n_experts <= 128) return launch_k(router_tiled_kernel<TX, 4>, a, grid, smem(128), s);
+  return launch_k(router_tiled_kernel<TX, 8>, a, grid, smem(256), s);
 }
 
 }  // namespace
 
 size_t router_partials_bytes(const moe_config& c) {
-  return sizeof(float) * (size_t)ceil_div(c.T, kTok) * (size_t)c.n_experts;
+  return sizeof(float) * (size_t)ceil_div(c.T, kRouterTokens) * (size_t)c.n_experts;
 }
 
 cudaError_t launch_router(const moe_config& c, const void* x, const void* w_router,
@@ -301,12 +510,12 @@ cudaError_t launch_router(const moe_config& c, const void* x, const void* w_rout
   a.logits_in = logits_in; a.logits_out = logits_out; a.topk_idx = topk_idx;
   a.topk_w = topk_w; a.counts = counts; a.partials = partials; a.status = status;
   a.T = c.T; a.d = c.d_model; a.N = c.n_experts; a.k = c.top_k; a.gate_mode = c.gate_mode;
-  const int nblk = ceil_div(c.T, kTok);
-  e = (c.dtype == MOE_BF16) ? launch_dtype<__nv_bfloat16>(a, nblk, s) : launch_dtype<float>(a, nblk, s);
+  const int grid = router_grid(c, logits_in);
+  e = (c.dtype == MOE_BF16) ? launch_dtype<__nv_bfloat16>(c, a, grid, s) : launch_dtype<float>(c, a, grid, s);
   if (e != cudaSuccess) return e;
   {
     ProfScope p(K_ROUTER_REDUCE, s);
-    router_reduce_kernel<<<ceil_div(c.n_experts, 256), 256, 0, s>>>(partials, nblk, c.n_experts, prob_sum);
+    router_reduce_kernel<<<ceil_div(c.n_experts, 256), 256, 0, s>>>(partials, grid, c.n_experts, prob_sum);
   }
   return cudaGetLastError();
 }
