@@ -370,7 +370,8 @@ def run_decode(moe, synth, dev, stream, pk, args):
             step()
         torch.cuda.synchronize(dev)
         times = []
-        for _ in range(max(5, min(args.steps, 50))):
+        reps = max(5, min(args.steps, 50))
+        for _ in range(reps):
             flush.fill_(1)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
@@ -379,6 +380,14 @@ def run_decode(moe, synth, dev, stream, pk, args):
             b.record(stream)
             torch.cuda.synchronize(dev)
             times.append(a.elapsed_time(b))
+        # per-kernel breakdown in separate steps (the events add a little time)
+        moe.profile_enable(True)
+        moe.profile_collect()
+        for _ in range(5):
+            flush.fill_(1)
+            step()
+        kern = moe.profile_collect()
+        moe.profile_enable(False)
         ms = statistics.median(times)
         wbytes, active = touched_weight_bytes(w, counts.cpu().tolist())
         total = wbytes + w.n_experts * w.d_model * 2 + 2 * w.T * w.d_model * 2
@@ -386,7 +395,8 @@ def run_decode(moe, synth, dev, stream, pk, args):
         out[f"T{w.T}"] = {"ms": round(ms, 4), "experts_touched": active,
                           "algorithmic_bytes": total, "gbs": round(gbs, 1),
                           "hbm_frac": round(gbs / pk["hbm"], 4),
-                          "tokens_per_s": round(w.T / (ms / 1e3), 1)}
+                          "tokens_per_s": round(w.T / (ms / 1e3), 1),
+                          "kernel_us": {k: round(1e3 * v[0] / v[1], 1) for k, v in kern.items()}}
     return out
 
 
@@ -472,6 +482,8 @@ WORKLOADS = {
     "mixtral_8x7b_prefill": lambda synth: synth.MIXTRAL_PREFILL,
     "deepseek_v3_moe": lambda synth: synth.DEEPSEEK_V3,
     "zipf_imbalanced": lambda synth: synth.ZIPF,
+    **{f"mixtral_8x7b_decode_T{t}": (lambda t_: lambda synth: [w for w in synth.MIXTRAL_DECODE if w.T == t_][0])(t)
+       for t in (1, 8, 32, 64)},
 }
 
 

@@ -64,12 +64,15 @@ struct GroupedWs {
   int* status;
   int32_t* seg;
   void* h;
+  float* partial;
 };
 GroupedWs carve_grouped(Carver& cv, const moe_config& c) {
   GroupedWs w;
+  const SplitKPlan plan = splitk_plan(c);
   w.status = cv.take<int>(256);
   w.seg = cv.take<int32_t>(sizeof(int32_t) * seg_table_words(c.n_experts + c.n_shared));
-  w.h = cv.take<void>((size_t)rows_total(c) * c.d_ff * elem_bytes(c.dtype));
+  w.h = cv.take<void>((size_t)padded_rows(rows_total(c)) * c.d_ff * elem_bytes(c.dtype));
+  w.partial = cv.take<float>(plan.partial_bytes);
   return w;
 }
 struct LayerWs {
@@ -87,6 +90,7 @@ struct LayerWs {
   int32_t* hist;
   int32_t* seg;
   void* h;
+  float* partial;
 };
 LayerWs carve_layer(Carver& cv, const moe_config& c) {
   LayerWs w;
@@ -99,12 +103,14 @@ LayerWs carve_layer(Carver& cv, const moe_config& c) {
   w.offsets = cv.take<int32_t>(sizeof(int32_t) * (N + 1));
   w.sorted_pair = cv.take<int32_t>(sizeof(int32_t) * P);
   w.inv_pos = cv.take<int32_t>(sizeof(int32_t) * P);
-  w.x_perm = cv.take<void>(P * c.d_model * eb);
+  w.x_perm = cv.take<void>((size_t)padded_rows((long long)P) * c.d_model * eb);
   w.y_perm = cv.take<void>((size_t)rows_total(c) * c.d_model * eb);
   w.partials = cv.take<float>(router_partials_bytes(c));
   w.hist = cv.take<int32_t>(permute_scratch_bytes(c));
   w.seg = cv.take<int32_t>(sizeof(int32_t) * seg_table_words(c.n_experts + c.n_shared));
-  w.h = cv.take<void>((size_t)rows_total(c) * c.d_ff * eb);
+  w.h = cv.take<void>((size_t)padded_rows(rows_total(c)) * c.d_ff * eb);
+  const SplitKPlan plan = splitk_plan(c);
+  w.partial = cv.take<float>(plan.partial_bytes);
   return w;
 }
 
@@ -139,15 +145,16 @@ int check_device(const moe_config& c) {
   return (major == 10 && minor == 3) ? MOE_OK : MOE_ERR_UNSUPPORTED;
 }
 
-int grouped_impl(const moe_config& c, const void* x_perm, const void* x, const int32_t* offsets,
-                 const int32_t* sorted_pair, const float* topk_w, const void* wg, const void* wu,
-                 const void* wd, void* y_perm, int32_t* seg, void* h, int* status,
-                 cudaStream_t s) {
+int grouped_impl(const moe_config& c, const void* x_perm, long long xp_rows, const void* x,
+                 const int32_t* offsets, const int32_t* sorted_pair, const float* topk_w,
+                 const void* wg, const void* wu, const void* wd, void* y_perm, int32_t* seg,
+                 void* h, float* partial, int* status, cudaStream_t s) {
   if (rows_total(c) == 0) return MOE_OK;
   cudaError_t e = launch_seg_table(c, offsets, seg, status, s);
   if (e != cudaSuccess) return fail_cuda(e);
   e = (c.dtype == MOE_BF16)
-          ? launch_grouped_bf16(c, x_perm, x, seg, sorted_pair, topk_w, wg, wu, wd, h, y_perm, status, s)
+          ? launch_grouped_bf16(c, x_perm, x, seg, sorted_pair, topk_w, wg, wu, wd, h, y_perm, partial,
+                                xp_rows, padded_rows(rows_total(c)), status, s)
           : launch_grouped_f32(c, x_perm, x, seg, sorted_pair, topk_w, wg, wu, wd, h, y_perm, status, s);
   return e == cudaSuccess ? MOE_OK : fail_cuda(e);
 }
@@ -156,7 +163,7 @@ int grouped_impl(const moe_config& c, const void* x_perm, const void* x, const i
 const char* kKernelNames[K_NUM] = {"router_topk",    "router_reduce", "permute_hist",
                                    "permute_scan",   "permute_rank",  "permute_gather",
                                    "seg_table",      "gate_up",       "down",
-                                   "combine",        "balance_stats"};
+                                   "splitk_reduce",  "combine",       "balance_stats"};
 struct Prof {
   std::mutex mu;
   bool on = false;
@@ -335,8 +342,8 @@ int moe_grouped_swiglu(const moe_config* cfg, const void* x_perm, const void* x,
   GroupedWs w = carve_grouped(cv, c);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
-  return grouped_impl(c, x_perm, x, expert_offsets, sorted_pair, topk_w, w_gate, w_up, w_down,
-                      y_perm, w.seg, w.h, w.status, s);
+  return grouped_impl(c, x_perm, pairs(c), x, expert_offsets, sorted_pair, topk_w, w_gate, w_up,
+                      w_down, y_perm, w.seg, w.h, w.partial, w.status, s);
 }
 
 int moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* inv_pos,
@@ -378,8 +385,8 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* w_router
   if (c.T == 0) return MOE_OK;
   e = launch_permute(c, x, idx, w.offsets, w.sorted_pair, w.inv_pos, w.x_perm, w.hist, w.status, s);
   if (e != cudaSuccess) return fail_cuda(e);
-  rc = grouped_impl(c, w.x_perm, x, w.offsets, w.sorted_pair, tw, w_gate, w_up, w_down, w.y_perm,
-                    w.seg, w.h, w.status, s);
+  rc = grouped_impl(c, w.x_perm, padded_rows(pairs(c)), x, w.offsets, w.sorted_pair, tw, w_gate,
+                    w_up, w_down, w.y_perm, w.seg, w.h, w.partial, w.status, s);
   if (rc != MOE_OK) return rc;
   e = launch_combine(c, w.y_perm, w.inv_pos, nullptr, y, s);
   return e == cudaSuccess ? MOE_OK : fail_cuda(e);

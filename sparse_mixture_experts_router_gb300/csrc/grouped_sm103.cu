@@ -39,6 +39,8 @@
 //    its own TMA copies in flight, the MMA thread for its own MMAs, and TMEM
 //    is freed before the CTA exits.
 #include <cuda.h>
+
+#include <algorithm>
 #include <mutex>
 
 #include "device_util.cuh"
@@ -81,6 +83,11 @@ struct GemmArgs {
   int n_out;                   // valid output columns
   int NT;                      // N tiles per segment
   int b_rows;                  // rows of one expert's weight matrix
+  // split-K (few tiles, e.g. decode): fp32 partial rows of every split
+  float* partial;              // [s_max][R][pc] fp32, or null when s_max == 1
+  int s_max;                   // largest split factor the partial buffer holds
+  int pc;                      // partial columns (2*d_ff for gate/up, d for down)
+  long long R;                 // output rows
 };
 
 struct __align__(8) SharedState {
@@ -139,6 +146,37 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
+// Split factor of every tile when there are fewer tiles than CTAs: the S in
+// [1, s_max] (at least kMinKbPerSplit K blocks per split) that best fills
+// whole waves of the grid, the smallest on ties. Every CTA computes the same.
+constexpr int kMinKbPerSplit = 8;
+__device__ __forceinline__ int choose_splits(int tiles, int grid, int KB, int s_max) {
+  if (s_max <= 1 || tiles <= 0 || tiles >= 2 * grid) return 1;
+  int best = 1;
+  long long best_num = tiles, best_den = grid;  // efficiency = num / den
+  for (int S = 2; S <= s_max && KB / S >= kMinKbPerSplit; ++S) {
+    const long long units = (long long)tiles * S;
+    const long long den = (units + grid - 1) / grid * grid;
+    if (units * best_den > best_num * den) {
+      best = S;
+      best_num = units;
+      best_den = den;
+    }
+  }
+  return best;
+}
+__device__ __forceinline__ int kb_begin(int split, int S, int KB) {
+  return (int)(((long long)split * KB) / S);
+}
+
+// Gate weight of an output row of the down projection (1 for shared rows
+// and when no weights are given; 0 for a pair id out of range).
+__device__ __forceinline__ float row_scale(const GemmArgs& a, int seg_id, long long orow) {
+  if (seg_id >= a.n_routed || !a.topk_w) return 1.0f;
+  const int pair = __ldg(a.sorted_pair + orow);
+  return (pair >= 0 && pair < a.n_pairs) ? __ldg(a.topk_w + pair) : 0.0f;
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
@@ -154,8 +192,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int32_t* seg = args.seg;
   const int E = __ldg(seg);
-  const int total = __ldg(seg + 1) * args.NT;
+  const int tiles = __ldg(seg + 1) * args.NT;
   const int KB = (args.K + BK - 1) / BK;
+  const int S = choose_splits(tiles, gridDim.x, KB, args.s_max);
+  const int total = tiles * S;  // work units: (tile, split), splits of a tile adjacent
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -193,8 +233,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode_tile(seg, E, args.NT, tile);
+      for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x) {
+        const int split = unit % S;
+        const Tile t = decode_tile(seg, E, args.NT, unit / S);
         const CUtensorMap* am = &map_a;
         int a_row;
         if (EPI == EPI_SWIGLU) {
@@ -204,7 +245,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           a_row = __ldg(seg + 3 + 3 * E + t.s) + t.m * BM;
         }
         const int b_row = t.s * args.b_rows + t.n * (EPI == EPI_SWIGLU ? 128 : 256);
-        for (int kb = 0; kb < KB; ++kb) {
+        const int kb1 = kb_begin(split + 1, S, KB);
+        for (int kb = kb_begin(split, S, KB); kb < kb1; ++kb) {
           if (!wait_phase(ptx::smem_addr(&st.empty[stage]), phase ^ 1u, abort_flag, args.status)) {
             ok = false;
             break;
@@ -245,7 +287,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x) {
         if (!wait_phase(ptx::smem_addr(&st.acc_empty[acc]), acc_phase ^ 1u, abort_flag,
                         args.status)) {
           ok = false;
@@ -253,7 +295,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < KB; ++kb) {
+        const int split = unit % S;
+        const int kb0 = kb_begin(split, S, KB), kb1 = kb_begin(split + 1, S, KB);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_phase(ptx::smem_addr(&st.full[stage]), phase, abort_flag, args.status)) {
             ok = false;
             break;
@@ -265,7 +309,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
             // +32 bytes of K per step = +2 in the descriptor's address field
-            ptx::mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
+            ptx::mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           ptx::mma_commit(ptx::smem_addr(&st.empty[stage]));
           if (++stage == STAGES) {
@@ -292,69 +336,102 @@ __global__ void __launch_bounds__(THREADS, 1)
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const Tile t = decode_tile(seg, E, args.NT, tile);
+    for (int unit = blockIdx.x; unit < total; unit += gridDim.x) {
+      const int split = unit % S;
+      const Tile t = decode_tile(seg, E, args.NT, unit / S);
       bool ok = wait_phase(ptx::smem_addr(&st.acc_full[acc]), acc_phase, abort_flag, args.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
       const int rows = __ldg(seg + 3 + E + t.s);
+      const int row0 = __ldg(seg + 3 + 3 * E + t.s);
       const int r = t.m * BM + row_in_tile;
       const bool valid = r < rows;
-      const long long orow = (long long)__ldg(seg + 3 + 3 * E + t.s) + r;
+      const long long orow = (long long)row0 + r;
       const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * BN);
-      if (EPI == EPI_SWIGLU) {
+      if (S == 1) {
+        if (EPI == EPI_SWIGLU) {
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t g[32], u[32];
-          ptx::tmem_ld32(tbase + c * 32, g);
-          ptx::tmem_ld32(tbase + 128 + c * 32, u);
-          ptx::tmem_ld_wait();
-          const int col0 = t.n * 128 + c * 32;
-          if (valid) {
-            uint32_t pk[16];
+          for (int c = 0; c < 4; ++c) {
+            uint32_t g[32], u[32];
+            ptx::tmem_ld32(tbase + c * 32, g);
+            ptx::tmem_ld32(tbase + 128 + c * 32, u);
+            ptx::tmem_ld_wait();
+            const int col0 = t.n * 128 + c * 32;
+            if (valid) {
+              uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float h0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
-              const float h1 = silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
-              pk[j] = f32x2_to_bf16x2(h0, h1);
+              for (int j = 0; j < 16; ++j) {
+                const float h0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+                const float h1 = silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+                pk[j] = f32x2_to_bf16x2(h0, h1);
+              }
+              __nv_bfloat16* dst = out + orow * args.ldo + col0;
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                if (col0 + q * 8 < args.n_out)
+                  *reinterpret_cast<uint4*>(dst + q * 8) =
+                      make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
             }
-            __nv_bfloat16* dst = out + orow * args.ldo + col0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (col0 + q * 8 < args.n_out)
-                *reinterpret_cast<uint4*>(dst + q * 8) =
-                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
           }
-        }
-      } else {
-        float scale = 1.0f;
-        if (valid && t.s < args.n_routed && args.topk_w) {
-          const int pair = __ldg(args.sorted_pair + orow);
-          scale = (pair >= 0 && pair < args.n_pairs) ? __ldg(args.topk_w + pair) : 0.0f;
-        }
+        } else {
+          const float scale = valid ? row_scale(args, t.s, orow) : 0.0f;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t v[32];
-          ptx::tmem_ld32(tbase + c * 32, v);
-          ptx::tmem_ld_wait();
-          const int col0 = t.n * 256 + c * 32;
-          if (valid) {
-            uint32_t pk[16];
+          for (int c = 0; c < 8; ++c) {
+            uint32_t v[32];
+            ptx::tmem_ld32(tbase + c * 32, v);
+            ptx::tmem_ld_wait();
+            const int col0 = t.n * 256 + c * 32;
+            if (valid) {
+              uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              pk[j] = f32x2_to_bf16x2(scale * __uint_as_float(v[2 * j]),
-                                      scale * __uint_as_float(v[2 * j + 1]));
-            __nv_bfloat16* dst = out + orow * args.ldo + col0;
+              for (int j = 0; j < 16; ++j)
+                pk[j] = f32x2_to_bf16x2(scale * __uint_as_float(v[2 * j]),
+                                        scale * __uint_as_float(v[2 * j + 1]));
+              __nv_bfloat16* dst = out + orow * args.ldo + col0;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (col0 + q * 8 < args.n_out)
-                *reinterpret_cast<uint4*>(dst + q * 8) =
-                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+              for (int q = 0; q < 4; ++q)
+                if (col0 + q * 8 < args.n_out)
+                  *reinterpret_cast<uint4*>(dst + q * 8) =
+                      make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
           }
         }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ptx::smem_addr(&st.acc_empty[acc]));
+      } else {
+        // Split-K unit: this split's fp32 partial rows; splitk_reduce_kernel
+        // sums the splits in order and applies the epilogue.
+        float* prow = args.partial + ((long long)split * args.R + orow) * args.pc;
+        constexpr int CHUNKS = (EPI == EPI_SWIGLU) ? 4 : 8;
+#pragma unroll 1
+        for (int c = 0; c < CHUNKS; ++c) {
+          uint32_t v[32], u[32];
+          ptx::tmem_ld32(tbase + c * 32, v);
+          if (EPI == EPI_SWIGLU) ptx::tmem_ld32(tbase + 128 + c * 32, u);
+          ptx::tmem_ld_wait();
+          const int col0 = t.n * (EPI == EPI_SWIGLU ? 128 : 256) + c * 32;
+          if (valid) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (col0 + q * 8 >= args.n_out) continue;
+              float4* d0 = reinterpret_cast<float4*>(prow + col0 + q * 8);
+              d0[0] = make_float4(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1]),
+                                  __uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+              d0[1] = make_float4(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]),
+                                  __uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+              if (EPI == EPI_SWIGLU) {
+                float4* d1 = reinterpret_cast<float4*>(prow + args.n_out + col0 + q * 8);
+                d1[0] = make_float4(__uint_as_float(u[8 * q]), __uint_as_float(u[8 * q + 1]),
+                                    __uint_as_float(u[8 * q + 2]), __uint_as_float(u[8 * q + 3]));
+                d1[1] = make_float4(__uint_as_float(u[8 * q + 4]), __uint_as_float(u[8 * q + 5]),
+                                    __uint_as_float(u[8 * q + 6]), __uint_as_float(u[8 * q + 7]));
+              }
+            }
+          }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ptx::smem_addr(&st.acc_empty[acc]));
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(ptx::smem_addr(&st.acc_empty[acc]));
       if (++acc == NUM_ACC) {
         acc = 0;
         acc_phase ^= 1u;
@@ -370,6 +447,52 @@ __global__ void __launch_bounds__(THREADS, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, TMEM_COLS);
   }
+}
+
+// Split-K epilogue: every output element from the partials of all S splits,
+// summed in split order, then the same epilogue as the fused path. One
+// thread per 8 output columns of one row; the whole grid shares the work.
+template <int EPI>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmArgs a, int gemm_grid) {
+  const int tiles = __ldg(a.seg + 1) * a.NT;
+  const int S = choose_splits(tiles, gemm_grid, (a.K + BK - 1) / BK, a.s_max);
+  if (S == 1) return;  // the GEMM finished its tiles itself
+  const int groups = a.n_out / 8;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.R * groups) return;
+  const long long orow = i / groups;
+  const int col = (int)(i % groups) * 8;
+  float v[8], u[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) v[q] = u[q] = 0.f;
+#pragma unroll 4
+  for (int sp = 0; sp < S; ++sp) {
+    const float* src = a.partial + ((long long)sp * a.R + orow) * a.pc + col;
+    const float4 p0 = __ldcg(reinterpret_cast<const float4*>(src));
+    const float4 p1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
+    v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
+    v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
+    if (EPI == EPI_SWIGLU) {
+      const float4 q0 = __ldcg(reinterpret_cast<const float4*>(src + a.n_out));
+      const float4 q1 = __ldcg(reinterpret_cast<const float4*>(src + a.n_out + 4));
+      u[0] += q0.x; u[1] += q0.y; u[2] += q0.z; u[3] += q0.w;
+      u[4] += q1.x; u[5] += q1.y; u[6] += q1.z; u[7] += q1.w;
+    }
+  }
+  float h[8];
+  if (EPI == EPI_SWIGLU) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) h[q] = silu(v[q]) * u[q];
+  } else {
+    // the row's segment: routed rows are [0, n_pairs), shared rows follow
+    const float sc = (orow < a.n_pairs) ? row_scale(a, 0, orow) : 1.0f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) h[q] = sc * v[q];
+  }
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + orow * a.ldo + col;
+  *reinterpret_cast<uint4*>(dst) =
+      make_uint4(f32x2_to_bf16x2(h[0], h[1]), f32x2_to_bf16x2(h[2], h[3]),
+                 f32x2_to_bf16x2(h[4], h[5]), f32x2_to_bf16x2(h[6], h[7]));
 }
 
 // ---------------------------------------------------------------- host side --
@@ -427,36 +550,68 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_sh, const CUt
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  const int grid = max_tiles < num_sms() ? max_tiles : num_sms();
+  // With split-K possible every SM takes part; otherwise no more CTAs than tiles.
+  const int grid = (args.s_max > 1 || max_tiles >= num_sms()) ? num_sms() : max_tiles;
   if (grid <= 0) return cudaSuccess;
-  ProfScope p(EPI == EPI_SWIGLU ? K_GATE_UP : K_DOWN, s);
-  grouped_gemm_kernel<EPI><<<grid, THREADS, DYN_SMEM, s>>>(a, a_sh, b0, b1, args);
+  {
+    ProfScope p(EPI == EPI_SWIGLU ? K_GATE_UP : K_DOWN, s);
+    grouped_gemm_kernel<EPI><<<grid, THREADS, DYN_SMEM, s>>>(a, a_sh, b0, b1, args);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || args.s_max <= 1) return e;
+  const long long n = args.R * (args.n_out / 8);
+  ProfScope p(K_SPLITK_REDUCE, s);
+  splitk_reduce_kernel<EPI><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(args, grid);
   return cudaGetLastError();
+}
+
+long long mt_bound_of(const moe_config& c) {
+  // Upper bound of M tiles: every segment may end in a partial tile.
+  const long long P = (long long)c.T * c.top_k;
+  return (P + BM - 1) / BM + c.n_experts + (long long)c.n_shared * ((c.T + BM - 1) / BM);
 }
 
 }  // namespace
 
+SplitKPlan splitk_plan(const moe_config& c) {
+  SplitKPlan p{1, 1, 0};
+  if (c.dtype != MOE_BF16) return p;
+  const long long R = (long long)c.T * (c.top_k + c.n_shared);
+  if (R == 0) return p;
+  const size_t per_gu = (size_t)R * 2 * c.d_ff * sizeof(float);
+  const size_t per_dn = (size_t)R * c.d_model * sizeof(float);
+  auto smax = [](size_t per) {
+    const size_t s = kSplitKBudget / per;
+    return s >= 2 ? (int)(s < (size_t)kMaxSplitK ? s : (size_t)kMaxSplitK) : 1;
+  };
+  p.s_max_gu = smax(per_gu);
+  p.s_max_dn = smax(per_dn);
+  const size_t b_gu = p.s_max_gu > 1 ? p.s_max_gu * per_gu : 0;
+  const size_t b_dn = p.s_max_dn > 1 ? p.s_max_dn * per_dn : 0;
+  p.partial_bytes = b_gu > b_dn ? b_gu : b_dn;
+  return p;
+}
+
 cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const void* x,
                                 const int32_t* seg, const int32_t* sorted_pair,
                                 const float* topk_w, const void* w_gate, const void* w_up,
-                                const void* w_down, void* h, void* y_perm, int* status,
-                                cudaStream_t s) {
+                                const void* w_down, void* h, void* y_perm, float* partial,
+                                long long xp_rows, long long h_rows, int* status, cudaStream_t s) {
   const long long P = (long long)c.T * c.top_k;
   const int E = c.n_experts + c.n_shared;
   const long long R = P + (long long)c.n_shared * c.T;  // rows of H and y_perm
   if (R == 0) return cudaSuccess;
-  // Upper bound of M tiles: every segment may end in a partial tile.
-  const long long mt_bound = (P + BM - 1) / BM + c.n_experts +
-                             (long long)c.n_shared * ((c.T + BM - 1) / BM);
+  const long long mt_bound = mt_bound_of(c);
+  const SplitKPlan plan = splitk_plan(c);
 
   CUtensorMap m_xp, m_x, m_wg, m_wu, m_h, m_wd;
   const bool ok =
-      make_map(&m_xp, P > 0 ? x_perm : x, P > 0 ? P : c.T, c.d_model) &&
+      make_map(&m_xp, P > 0 ? x_perm : x, P > 0 ? std::max(P, xp_rows) : c.T, c.d_model) &&
       make_map(&m_x, c.n_shared > 0 ? x : (P > 0 ? x_perm : x), c.n_shared > 0 ? c.T : (P > 0 ? P : c.T),
                c.d_model) &&
       make_map(&m_wg, w_gate, (long long)E * c.d_ff, c.d_model) &&
       make_map(&m_wu, w_up, (long long)E * c.d_ff, c.d_model) &&
-      make_map(&m_h, h, R, c.d_ff) &&
+      make_map(&m_h, h, std::max(R, h_rows), c.d_ff) &&
       make_map(&m_wd, w_down, (long long)E * c.d_model, c.d_ff);
   if (!ok) return cudaErrorInvalidValue;
 
@@ -473,6 +628,10 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
   g.n_out = c.d_ff;
   g.NT = (c.d_ff + 127) / 128;
   g.b_rows = c.d_ff;
+  g.partial = partial;
+  g.s_max = plan.s_max_gu;
+  g.pc = 2 * c.d_ff;
+  g.R = R;
   cudaError_t e = launch_gemm<EPI_SWIGLU>(m_xp, m_x, m_wg, m_wu, g, (int)(mt_bound * g.NT), s);
   if (e != cudaSuccess) return e;
 
@@ -484,6 +643,8 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
   d.n_out = c.d_model;
   d.NT = (c.d_model + 255) / 256;
   d.b_rows = c.d_model;
+  d.s_max = plan.s_max_dn;
+  d.pc = c.d_model;
   return launch_gemm<EPI_DOWN>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s);
 }
 

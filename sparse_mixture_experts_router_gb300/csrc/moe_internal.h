@@ -62,12 +62,27 @@ cudaError_t launch_seg_table(const moe_config& c, const int32_t* offsets, int32_
                              int* status, cudaStream_t s);
 
 // bf16 tcgen05 path: gate/up (SwiGLU epilogue into h) then down (gate
-// weight epilogue into y_perm).
+// weight epilogue into y_perm). When a GEMM has fewer tiles than two waves
+// of the grid (small batches), each tile may be split along K; the splits
+// write fp32 partial rows into `partial` and a reduce kernel sums them in
+// split order and applies the epilogue.
+constexpr size_t kSplitKBudget = 64ull << 20;  // bytes of partial rows at most
+constexpr int kMaxSplitK = 16;
+struct SplitKPlan {
+  int s_max_gu, s_max_dn;  // largest split factor per GEMM (1: never split)
+  size_t partial_bytes;    // fp32 partial rows buffer
+};
+SplitKPlan splitk_plan(const moe_config& c);
 cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const void* x,
                                 const int32_t* seg, const int32_t* sorted_pair,
                                 const float* topk_w, const void* w_gate, const void* w_up,
-                                const void* w_down, void* h, void* y_perm, int* status,
+                                const void* w_down, void* h, void* y_perm, float* partial,
+                                long long xp_rows, long long h_rows, int* status,
                                 cudaStream_t s);
+// Rows allocated for library-owned x_perm / H: at least one 128-row tile, so
+// that a small batch's tiles read allocated (masked) rows rather than the
+// tensor map's out-of-bounds fill.
+inline long long padded_rows(long long rows) { return rows < kTileM ? kTileM : rows; }
 // fp32 CUDA-core path.
 cudaError_t launch_grouped_f32(const moe_config& c, const void* x_perm, const void* x,
                                const int32_t* seg, const int32_t* sorted_pair,
@@ -93,6 +108,7 @@ enum KernelId {
   K_SEG_TABLE,
   K_GATE_UP,
   K_DOWN,
+  K_SPLITK_REDUCE,
   K_COMBINE,
   K_BALANCE,
   K_NUM

@@ -9,11 +9,10 @@
 // top-k weights, a routing bias that only moves the choice).
 //
 // Scores are fp32 dot products on the CUDA cores, in one of two kernels:
-//  - few experts (N <= 32, W_r fits in shared memory): the whole of W_r is
-//    staged in shared memory once per block; each warp streams the rows of
-//    1-4 tokens once from HBM with 16-byte loads, accumulates all N dot
-//    products per lane and reduces them across the warp. Bound by HBM
-//    (reading x once).
+//  - few experts (N <= 32): the 8 warps of a block split d_model and score a
+//    group of 2-8 tokens against all N experts together, reading x once
+//    from HBM and W_r from L2 with 16-byte loads. Bound by HBM (reading x
+//    once) for large T, by latency for decode-sized T.
 //  - many experts: a register-tiled block GEMM. A block scores 64 tokens
 //    against all N (<= 256) experts; each thread owns a TM x 8 tile
 //    (tokens x consecutive experts); 32-wide K slices of x and W_r are
@@ -38,7 +37,6 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTileTokens = 64;              // tokens per block, tiled kernel
 constexpr int kKC = 32;                      // K slice of the tiled kernel
-constexpr size_t kSmallSmemLimit = 200 * 1024;
 
 struct RouterArgs {
   const void* x;
@@ -190,77 +188,84 @@ __device__ __forceinline__ void finish_block(const float (&psum)[EJ], float* wpr
 }
 
 // ---------------------------------------------------------------------------
-// Few experts: W_r in shared memory, x streamed once. NP = padded N (8, 16
-// or 32), TPW tokens per warp at a time (NP * TPW = 32 accumulators).
-template <typename TX, int NP, int TPW>
+// Few experts (N <= 32): a block scores TB tokens at a time; each of its 8
+// warps covers 1/8 of d_model for all TB tokens and all N experts (x and
+// W_r read once per token group with 16-byte loads; W_r comes from L2). A
+// lane accumulates TB*NP = 64 partial dot products; a 5-step butterfly
+// reduce-scatter leaves each lane 2 of them summed over the warp, the 8
+// warps' sums are added in warp order through shared memory, and warp q
+// then selects for token q of the group.
+template <typename TX, int NP, int TB>
 __global__ void __launch_bounds__(kThreads) router_small_kernel(const RouterArgs a) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
   constexpr int EPV = V16<TX>::n;
-  constexpr int U = 4;  // 16-byte vectors per lane in flight per token
+  constexpr int NV = NP * TB;  // 64 accumulators
+  static_assert(NV == 64, "reduce-scatter below assumes 64 values over 32 lanes");
+  __shared__ float red[kWarps][NV];
+  __shared__ float wprob[kWarps * 32];
+  __shared__ int bcount[32];
   const int N = a.N;
-  const int vec = a.d / EPV;  // 16-byte vectors per row
-  uint4* wsm = reinterpret_cast<uint4*>(smem_raw);
-  float* wprob = reinterpret_cast<float*>(wsm + (size_t)N * vec);
-  int* bcount = reinterpret_cast<int*>(wprob + kWarps * 32);
+  const int vec = a.d / EPV;                       // 16-byte vectors per row
+  const int vpw = (vec + kWarps - 1) / kWarps;     // vectors per warp
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-
-  const uint4* wg = static_cast<const uint4*>(a.w);
-  for (int i = tid; i < N * vec; i += kThreads) wsm[i] = __ldg(wg + i);
-  if (tid < 32) bcount[tid] = 0;
-  __syncthreads();
-
+  const int v_lo = warp * vpw, v_hi = min(vec, v_lo + vpw);
   const uint4* x = static_cast<const uint4*>(a.x);
+  const uint4* w = static_cast<const uint4*>(a.w);
+  if (tid < 32) bcount[tid] = 0;
+  // index of this lane's two reduced values: 2 * bit-reversed lane
+  const int base = ((lane & 16) ? 32 : 0) + ((lane & 8) ? 16 : 0) + ((lane & 4) ? 8 : 0) +
+                   ((lane & 2) ? 4 : 0) + ((lane & 1) ? 2 : 0);
   float psum[1] = {0.f};
-  const int gw = blockIdx.x * kWarps + warp, nw = gridDim.x * kWarps;
-  for (long long t0 = (long long)gw * TPW; t0 < a.T; t0 += (long long)nw * TPW) {
-    float acc[TPW][NP];
+
+  for (long long t0 = (long long)blockIdx.x * TB; t0 < a.T; t0 += (long long)gridDim.x * TB) {
+    float v[NV];
 #pragma unroll
-    for (int q = 0; q < TPW; ++q)
+    for (int i = 0; i < NV; ++i) v[i] = 0.f;
+    for (int vv = v_lo + lane; vv < v_hi; vv += 32) {
+      uint4 xq[TB];
 #pragma unroll
-      for (int e = 0; e < NP; ++e) acc[q][e] = 0.f;
-    for (int v0 = 0; v0 < vec; v0 += 32 * U) {
-      uint4 xv[TPW][U];
+      for (int q = 0; q < TB; ++q)
+        xq[q] = (t0 + q < a.T) ? __ldg(x + (t0 + q) * vec + vv) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int q = 0; q < TPW; ++q)
+      for (int e = 0; e < NP; ++e) {
+        if (e >= N) break;
+        float wf[EPV];
+        V16<TX>::cvt(__ldg(w + (size_t)e * vec + vv), wf);
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int v = v0 + u * 32 + lane;
-          xv[q][u] = (t0 + q < a.T && v < vec) ? __ldg(x + (t0 + q) * vec + v) : make_uint4(0, 0, 0, 0);
-        }
+        for (int q = 0; q < TB; ++q) {
+          float xf[EPV];
+          V16<TX>::cvt(xq[q], xf);
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int v = v0 + u * 32 + lane;
-        if (v >= vec) break;
-        float xf[TPW][EPV];
-#pragma unroll
-        for (int q = 0; q < TPW; ++q) V16<TX>::cvt(xv[q][u], xf[q]);
-#pragma unroll
-        for (int e = 0; e < NP; ++e) {
-          if (e >= N) break;
-          float wf[EPV];
-          V16<TX>::cvt(wsm[e * vec + v], wf);
-#pragma unroll
-          for (int q = 0; q < TPW; ++q)
-#pragma unroll
-            for (int i = 0; i < EPV; ++i) acc[q][e] = fmaf(xf[q][i], wf[i], acc[q][e]);
+          for (int i = 0; i < EPV; ++i) v[q * NP + e] = fmaf(xf[i], wf[i], v[q * NP + e]);
         }
       }
     }
+    // reduce-scatter: after the step with offset o a lane keeps half of its
+    // values (the upper half when lane & o), each summed with its partner's.
 #pragma unroll
-    for (int q = 0; q < TPW; ++q) {
-      if (t0 + q >= a.T) break;  // warp-uniform
+    for (int o = 16, L = NV; o > 0; o >>= 1, L >>= 1) {
+      const bool upper = (lane & o) != 0;
 #pragma unroll
-      for (int e = 0; e < NP; ++e)
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[q][e] += __shfl_xor_sync(0xffffffffu, acc[q][e], o);
-      float r[1] = {0.f};
-#pragma unroll
-      for (int e = 0; e < NP; ++e)
-        if (e == lane) r[0] = acc[q][e];
-      if (lane < N && a.logit_bias) r[0] = __fadd_rn(r[0], a.logit_bias[lane]);
-      if (a.logits_out && lane < N) a.logits_out[(t0 + q) * N + lane] = r[0];
-      select_token<1>(r, lane, t0 + q, a, psum, bcount);
+      for (int i = 0; i < L / 2; ++i) {
+        const float send = upper ? v[i] : v[i + L / 2];
+        const float keep = upper ? v[i + L / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
     }
+    red[warp][base] = v[0];
+    red[warp][base + 1] = v[1];
+    __syncthreads();
+    if (warp < TB && t0 + warp < a.T) {
+      const long long t = t0 + warp;
+      float r[1] = {0.f};
+      if (lane < N) {
+        float sum = 0.f;
+        for (int ww = 0; ww < kWarps; ++ww) sum += red[ww][warp * NP + lane];
+        r[0] = a.logit_bias ? __fadd_rn(sum, a.logit_bias[lane]) : sum;
+        if (a.logits_out) a.logits_out[t * N + lane] = r[0];
+      }
+      select_token<1>(r, lane, t, a, psum, bcount);
+    }
+    __syncthreads();
   }
   finish_block<1>(psum, wprob, bcount, a);
 }
@@ -452,33 +457,22 @@ cudaError_t launch_k(K kernel, const RouterArgs& a, int grid, size_t smem, cudaS
   return cudaGetLastError();
 }
 
-size_t small_smem(const moe_config& c) {
-  return (size_t)c.n_experts * c.d_model * elem_bytes(c.dtype) + sizeof(float) * kWarps * 32 +
-         sizeof(int) * 32;
-}
-
 bool use_small(const moe_config& c, const float* logits_in) {
-  return logits_in == nullptr && c.n_experts <= 32 && small_smem(c) <= kSmallSmemLimit;
+  return logits_in == nullptr && c.n_experts <= 32;
 }
 
 int router_grid(const moe_config& c, const float* logits_in) {
-  if (use_small(c, logits_in)) {
-    // never more blocks than ceil(T/32): the partials buffer is sized for that
-    const int per_sm = (int)((227 * 1024) / small_smem(c));
-    const int cap = num_sms() * (per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm));
-    const int g = ceil_div(c.T, kRouterTokens);
-    return g < cap ? g : cap;
-  }
+  // never more blocks than ceil(T/32): the partials buffer is sized for that
+  if (use_small(c, logits_in)) return ceil_div(c.T, kRouterTokens);
   return ceil_div(c.T, kTileTokens);
 }
 
 template <typename TX>
 cudaError_t launch_dtype(const moe_config& c, const RouterArgs& a, int grid, cudaStream_t s) {
   if (use_small(c, a.logits_in)) {
-    const size_t sm = small_smem(c);
-    if (c.n_experts <= 8) return launch_k(router_small_kernel<TX, 8, 4>, a, grid, sm, s);
-    if (c.n_experts <= 16) return launch_k(router_small_kernel<TX, 16, 2>, a, grid, sm, s);
-    return launch_k(router_small_kernel<TX, 32, 1>, a, grid, sm, s);
+    if (c.n_experts <= 8) return launch_k(router_small_kernel<TX, 8, 8>, a, grid, 0, s);
+    if (c.n_experts <= 16) return launch_k(router_small_kernel<TX, 16, 4>, a, grid, 0, s);
+    return launch_k(router_small_kernel<TX, 32, 2>, a, grid, 0, s);
   }
   auto smem = [](int BN) {  // must match the layout in router_tiled_kernel
     const size_t tile = sizeof(float) * (size_t)kTileTokens * BN;

@@ -3,7 +3,8 @@ segment, gate-weighted, against the oracle's expert on the same rows.
 
 Shapes span several 128-row tiles, ragged segment ends, empty experts, a
 K not a multiple of the 64-wide K block, an output width not a multiple of
-the tile width, and a shared expert. The oracle's own grouping (rows in
+the tile width, a shared expert, and batches small enough that tiles are
+split along K (decode). The oracle's own grouping (rows in
 expert order) decides which pair each output row belongs to."""
 import numpy as np
 import pytest
@@ -24,6 +25,10 @@ CASES = [
     ("k_n_tails", 130, 200, 3, 2, 136, 1, "bf16", 0.0),
     ("hot_expert", 1000, 256, 4, 1, 128, 0, "bf16", 6.0),
     ("many_experts", 600, 128, 64, 4, 128, 2, "bf16", 1.2),
+    # few tiles: the K dimension is split across CTAs and the partials summed
+    ("splitk_decode_T1", 1, 4096, 8, 2, 14336, 0, "bf16", 0.0),
+    ("splitk_T5_shared", 5, 1024, 8, 2, 2048, 1, "bf16", 0.0),
+    ("splitk_ragged_k", 20, 1000, 16, 4, 520, 0, "bf16", 0.0),
     ("f32", 64, 64, 4, 2, 128, 0, "f32", 0.0),
     ("f32_shared", 90, 40, 5, 2, 48, 1, "f32", 0.0),
 ]
