@@ -150,7 +150,8 @@ int grouped_impl(const moe_config& c, const void* x_perm, long long xp_rows, con
                  const void* wg, const void* wu, const void* wd, void* y_perm, int32_t* seg,
                  void* h, float* partial, int* status, cudaStream_t s) {
   if (rows_total(c) == 0) return MOE_OK;
-  cudaError_t e = launch_seg_table(c, offsets, seg, status, s);
+  cudaError_t e = launch_seg_table(c, offsets, seg, c.dtype == MOE_BF16 ? seg_tile_m(c) : kTileM,
+                                   status, s);
   if (e != cudaSuccess) return fail_cuda(e);
   e = (c.dtype == MOE_BF16)
           ? launch_grouped_bf16(c, x_perm, x, seg, sorted_pair, topk_w, wg, wu, wd, h, y_perm, partial,

@@ -177,6 +177,62 @@ __device__ __forceinline__ float row_scale(const GemmArgs& a, int seg_id, long l
   return (pair >= 0 && pair < a.n_pairs) ? __ldg(a.topk_w + pair) : 0.0f;
 }
 
+// The fused epilogue of one 128-row accumulator: each thread drains its
+// TMEM lane (row) 32 columns at a time and stores bf16 (SwiGLU of the paired
+// gate/up columns, or the gate-weighted down projection). Rows past the
+// segment's end (valid = false) are loaded but not stored.
+template <int EPI>
+__device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tbase, const Tile& t,
+                                               bool valid, long long orow, __nv_bfloat16* out) {
+  if (EPI == EPI_SWIGLU) {
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t g[32], u[32];
+      ptx::tmem_ld32(tbase + c * 32, g);
+      ptx::tmem_ld32(tbase + 128 + c * 32, u);
+      ptx::tmem_ld_wait();
+      const int col0 = t.n * 128 + c * 32;
+      if (valid) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float h0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+          const float h1 = silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+          pk[j] = f32x2_to_bf16x2(h0, h1);
+        }
+        __nv_bfloat16* dst = out + orow * args.ldo + col0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (col0 + q * 8 < args.n_out)
+            *reinterpret_cast<uint4*>(dst + q * 8) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
+    }
+  } else {
+    const float scale = valid ? row_scale(args, t.s, orow) : 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      uint32_t v[32];
+      ptx::tmem_ld32(tbase + c * 32, v);
+      ptx::tmem_ld_wait();
+      const int col0 = t.n * 256 + c * 32;
+      if (valid) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          pk[j] = f32x2_to_bf16x2(scale * __uint_as_float(v[2 * j]),
+                                  scale * __uint_as_float(v[2 * j + 1]));
+        __nv_bfloat16* dst = out + orow * args.ldo + col0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (col0 + q * 8 < args.n_out)
+            *reinterpret_cast<uint4*>(dst + q * 8) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
+    }
+  }
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
@@ -349,53 +405,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const long long orow = (long long)row0 + r;
       const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * BN);
       if (S == 1) {
-        if (EPI == EPI_SWIGLU) {
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t g[32], u[32];
-            ptx::tmem_ld32(tbase + c * 32, g);
-            ptx::tmem_ld32(tbase + 128 + c * 32, u);
-            ptx::tmem_ld_wait();
-            const int col0 = t.n * 128 + c * 32;
-            if (valid) {
-              uint32_t pk[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const float h0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
-                const float h1 = silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
-                pk[j] = f32x2_to_bf16x2(h0, h1);
-              }
-              __nv_bfloat16* dst = out + orow * args.ldo + col0;
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                if (col0 + q * 8 < args.n_out)
-                  *reinterpret_cast<uint4*>(dst + q * 8) =
-                      make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            }
-          }
-        } else {
-          const float scale = valid ? row_scale(args, t.s, orow) : 0.0f;
-#pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
-            uint32_t v[32];
-            ptx::tmem_ld32(tbase + c * 32, v);
-            ptx::tmem_ld_wait();
-            const int col0 = t.n * 256 + c * 32;
-            if (valid) {
-              uint32_t pk[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                pk[j] = f32x2_to_bf16x2(scale * __uint_as_float(v[2 * j]),
-                                        scale * __uint_as_float(v[2 * j + 1]));
-              __nv_bfloat16* dst = out + orow * args.ldo + col0;
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                if (col0 + q * 8 < args.n_out)
-                  *reinterpret_cast<uint4*>(dst + q * 8) =
-                      make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            }
-          }
-        }
+        epilogue_fused<EPI>(args, tbase, t, valid, orow, out);
         ptx::tc_fence_before();
         ptx::mbar_arrive(ptx::smem_addr(&st.acc_empty[acc]));
       } else {
@@ -446,6 +456,216 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The same grouped GEMM on CTA pairs (clusters of 2, tcgen05 cta_group::2):
+// a pair computes a 256-row x 256-column tile with one 256x256x16 MMA per K
+// step, issued by the even CTA. Each CTA stages its own 128 A rows and half
+// of B (the gate rows in the even CTA and the up rows in the odd one, or
+// output features 0-127 / 128-255 for down) and holds its 128 accumulator
+// rows in its own TMEM. Per SM this halves the B bytes per MMA cycle and
+// leaves room for a 6-stage ring (32 KB a stage). Used for large segments
+// only: a 256-row tile wastes up to 255 rows at a segment's end.
+constexpr int PSTAGES = 6;
+constexpr int P_STAGE_BYTES = A_BYTES + B_HALF_BYTES;               // 32 KB per CTA
+constexpr size_t DYN_SMEM_PAIR = (size_t)PSTAGES * P_STAGE_BYTES + 1024;
+constexpr uint32_t IDESC_PAIR = ptx::idesc_bf16_f32(2 * BM, BN);
+constexpr int PAIR_TILE_M = 2 * BM;
+
+struct __align__(8) PairState {
+  uint64_t full[PSTAGES];
+  uint64_t empty[PSTAGES];
+  uint64_t acc_full[NUM_ACC];
+  uint64_t acc_empty[NUM_ACC];  // in the even CTA: arrivals of both CTAs' epilogues
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a,
+                             const __grid_constant__ CUtensorMap map_a_shared,
+                             const __grid_constant__ CUtensorMap map_b0,
+                             const __grid_constant__ CUtensorMap map_b1, const GemmArgs args) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ PairState st;
+
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x / 32), 0);
+  const int lane = threadIdx.x % 32;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const uint32_t ring = (ptx::smem_addr(dyn_smem) + 1023u) & ~1023u;
+
+  const int32_t* seg = args.seg;  // built with 256-row tiles
+  const int E = __ldg(seg);
+  const int tiles = __ldg(seg + 1) * args.NT;
+  const int KB = (args.K + BK - 1) / BK;
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < PSTAGES; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&st.full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&st.empty[i]), 1);
+    }
+    for (int i = 0; i < NUM_ACC; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&st.acc_full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&st.acc_empty[i]), 2 * EPI_THREADS);
+    }
+    ptx::mbar_init(ptx::smem_addr(&st.drain), 1);
+    st.abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&map_a);
+    ptx::prefetch_tmap(&map_a_shared);
+    ptx::prefetch_tmap(&map_b0);
+    ptx::prefetch_tmap(&map_b1);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_addr(&st.tmem_base), TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers initialised before any remote use
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = st.tmem_base;
+  volatile int* abort_flag = &st.abort;
+
+  if (warp == 0) {
+    // ----------------------------------------------- TMA producer (both CTAs) --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
+        const Tile t = decode_tile(seg, E, args.NT, tile);
+        const CUtensorMap* am = &map_a;
+        const CUtensorMap* bm = &map_b0;
+        int a_row, b_row;
+        if (EPI == EPI_SWIGLU) {
+          a_row = __ldg(seg + 3 + 2 * E + t.s) + t.m * PAIR_TILE_M + (int)rank * BM;
+          if (t.s >= args.n_routed) am = &map_a_shared;
+          if (rank == 1) bm = &map_b1;  // up rows in the odd CTA
+          b_row = t.s * args.b_rows + t.n * 128;
+        } else {
+          a_row = __ldg(seg + 3 + 3 * E + t.s) + t.m * PAIR_TILE_M + (int)rank * BM;
+          b_row = t.s * args.b_rows + t.n * 256 + (int)rank * 128;
+        }
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait_phase(ptx::smem_addr(&st.empty[stage]), phase ^ 1u, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_local = ptx::smem_addr(&st.full[stage]);
+          const uint32_t full_leader = ptx::mapa_shared(full_local, 0);
+          const uint32_t a_dst = ring + stage * P_STAGE_BYTES;
+          if (leader) ptx::mbar_arrive_expect_tx(full_local, 2 * P_STAGE_BYTES);
+          ptx::tma_load_2d_pair(a_dst, am, full_leader, kb * BK, a_row);
+          ptx::tma_load_2d_pair(a_dst + A_BYTES, bm, full_leader, kb * BK, b_row);
+          ++issued;
+          if (++stage == PSTAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {
+        const long long n = issued < PSTAGES ? issued : PSTAGES;
+        for (long long i = 1; i <= n; ++i) {
+          const long long q = issued - i;
+          drain_wait(ptx::smem_addr(&st.full[q % PSTAGES]), (uint32_t)((q / PSTAGES) & 1));
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------- MMA issuer (even CTA only) --
+    if (lane == 0 && leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
+        if (!wait_phase(ptx::smem_addr(&st.acc_empty[acc]), acc_phase ^ 1u, abort_flag,
+                        args.status)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait_phase(ptx::smem_addr(&st.full[stage]), phase, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_src = ring + stage * P_STAGE_BYTES;
+          const uint64_t adesc = ptx::sdesc_k128(a_src);
+          const uint64_t bdesc = ptx::sdesc_k128(a_src + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k)
+            ptx::mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC_PAIR, (kb | k) != 0);
+          ptx::mma_commit_pair(ptx::smem_addr(&st.empty[stage]), 0x3);
+          if (++stage == PSTAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair(ptx::smem_addr(&st.acc_full[acc]), 0x3);
+        if (++acc == NUM_ACC) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        ptx::mma_commit_pair(ptx::smem_addr(&st.drain), 0x1);
+        drain_wait(ptx::smem_addr(&st.drain), 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue (both CTAs) --
+    const int sub = warp & 3;
+    const int row_in_tile = sub * 32 + lane;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
+    const uint32_t acc_empty_leader[NUM_ACC] = {
+        ptx::mapa_shared(ptx::smem_addr(&st.acc_empty[0]), 0),
+        ptx::mapa_shared(ptx::smem_addr(&st.acc_empty[1]), 0)};
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = cluster; tile < tiles; tile += nclusters) {
+      const Tile t = decode_tile(seg, E, args.NT, tile);
+      bool ok = wait_phase(ptx::smem_addr(&st.acc_full[acc]), acc_phase, abort_flag, args.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      ptx::tc_fence_after();
+      const int rows = __ldg(seg + 3 + E + t.s);
+      const int r = t.m * PAIR_TILE_M + (int)rank * BM + row_in_tile;
+      const bool valid = r < rows;
+      const long long orow = (long long)__ldg(seg + 3 + 3 * E + t.s) + r;
+      const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * BN);
+      epilogue_fused<EPI>(args, tbase, t, valid, orow, out);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive_cluster(acc_empty_leader[acc]);
+      if (++acc == NUM_ACC) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------- teardown --
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // no CTA leaves while its peer may still use its smem
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -565,13 +785,96 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_sh, const CUt
   return cudaGetLastError();
 }
 
-long long mt_bound_of(const moe_config& c) {
+long long mt_bound_of(const moe_config& c, int tile_m) {
   // Upper bound of M tiles: every segment may end in a partial tile.
   const long long P = (long long)c.T * c.top_k;
-  return (P + BM - 1) / BM + c.n_experts + (long long)c.n_shared * ((c.T + BM - 1) / BM);
+  return (P + tile_m - 1) / tile_m + c.n_experts +
+         (long long)c.n_shared * ((c.T + tile_m - 1) / tile_m);
 }
 
+cudaError_t configure_pair_kernels() {
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device == dev) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI_SWIGLU>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DYN_SMEM_PAIR);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI_DOWN>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DYN_SMEM_PAIR);
+  if (e == cudaSuccess) configured_device = dev;
+  return e;
+}
+
+// Clusters of 2 that can be resident at once with one CTA per SM (0 if the
+// pair kernels cannot be configured on this device).
+int max_pair_clusters() {
+  static thread_local int cached_dev = -1, cached = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (cached_dev == dev) return cached;
+  if (configure_pair_kernels() != cudaSuccess) {
+    cudaGetLastError();
+    cached_dev = dev;
+    cached = 0;
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (num_sms() / 2));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = DYN_SMEM_PAIR;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<EPI_SWIGLU>, &cfg) != cudaSuccess)
+    n = 0;
+  cudaGetLastError();  // clear a failed query
+  cached_dev = dev;
+  cached = n;
+  return n;
+}
+
+template <int EPI>
+cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a_sh, const CUtensorMap& b0,
+                        const CUtensorMap& b1, const GemmArgs& args, int max_tiles,
+                        cudaStream_t s) {
+  const int clusters = std::min(max_tiles, max_pair_clusters());
+  if (clusters <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = DYN_SMEM_PAIR;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  ProfScope p(EPI == EPI_SWIGLU ? K_GATE_UP : K_DOWN, s);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<EPI>, a, a_sh, b0, b1, args);
+}
+
+
 }  // namespace
+
+bool use_pair_tiles(const moe_config& c) {
+  // Large segments only (on average at least 1.5 pair tiles of rows per
+  // routed expert), and never when a projection could be split along K.
+  if (c.dtype != MOE_BF16 || c.n_experts <= 0) return false;
+  const long long P = (long long)c.T * c.top_k;
+  const SplitKPlan plan = splitk_plan(c);
+  return plan.s_max_gu == 1 && plan.s_max_dn == 1 && P >= 384LL * c.n_experts &&
+         max_pair_clusters() > 0;
+}
+
+int seg_tile_m(const moe_config& c) { return use_pair_tiles(c) ? PAIR_TILE_M : BM; }
 
 SplitKPlan splitk_plan(const moe_config& c) {
   SplitKPlan p{1, 1, 0};
@@ -601,8 +904,13 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
   const int E = c.n_experts + c.n_shared;
   const long long R = P + (long long)c.n_shared * c.T;  // rows of H and y_perm
   if (R == 0) return cudaSuccess;
-  const long long mt_bound = mt_bound_of(c);
+  const bool pair = use_pair_tiles(c);
+  const long long mt_bound = mt_bound_of(c, pair ? PAIR_TILE_M : BM);
   const SplitKPlan plan = splitk_plan(c);
+  if (pair) {
+    cudaError_t e = configure_pair_kernels();
+    if (e != cudaSuccess) return e;
+  }
 
   CUtensorMap m_xp, m_x, m_wg, m_wu, m_h, m_wd;
   const bool ok =
@@ -632,7 +940,8 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
   g.s_max = plan.s_max_gu;
   g.pc = 2 * c.d_ff;
   g.R = R;
-  cudaError_t e = launch_gemm<EPI_SWIGLU>(m_xp, m_x, m_wg, m_wu, g, (int)(mt_bound * g.NT), s);
+  cudaError_t e = pair ? launch_pair<EPI_SWIGLU>(m_xp, m_x, m_wg, m_wu, g, (int)(mt_bound * g.NT), s)
+                       : launch_gemm<EPI_SWIGLU>(m_xp, m_x, m_wg, m_wu, g, (int)(mt_bound * g.NT), s);
   if (e != cudaSuccess) return e;
 
   GemmArgs d = g;
@@ -645,7 +954,8 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
   d.b_rows = c.d_model;
   d.s_max = plan.s_max_dn;
   d.pc = c.d_model;
-  return launch_gemm<EPI_DOWN>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s);
+  return pair ? launch_pair<EPI_DOWN>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s)
+              : launch_gemm<EPI_DOWN>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s);
 }
 
 }  // namespace moe

@@ -59,7 +59,12 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
 size_t permute_scratch_bytes(const moe_config& c);
 
 cudaError_t launch_seg_table(const moe_config& c, const int32_t* offsets, int32_t* seg,
-                             int* status, cudaStream_t s);
+                             int tile_m, int* status, cudaStream_t s);
+// The bf16 grouped GEMM runs on CTA pairs with 256-row tiles for large
+// segments (see grouped_sm103.cu); the segment table must then be built
+// with that tile height.
+bool use_pair_tiles(const moe_config& c);
+int seg_tile_m(const moe_config& c);
 
 // bf16 tcgen05 path: gate/up (SwiGLU epilogue into h) then down (gate
 // weight epilogue into y_perm). When a GEMM has fewer tiles than two waves

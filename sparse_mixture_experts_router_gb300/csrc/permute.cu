@@ -235,9 +235,9 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
 }
 
 cudaError_t launch_seg_table(const moe_config& c, const int32_t* offsets, int32_t* seg,
-                             int* status, cudaStream_t s) {
+                             int tile_m, int* status, cudaStream_t s) {
   ProfScope p(K_SEG_TABLE, s);
-  seg_table_kernel<<<1, 256, 0, s>>>(offsets, c.n_experts, c.n_shared, c.T, c.T * c.top_k, kTileM,
+  seg_table_kernel<<<1, 256, 0, s>>>(offsets, c.n_experts, c.n_shared, c.T, c.T * c.top_k, tile_m,
                                      seg, status);
   return cudaGetLastError();
 }

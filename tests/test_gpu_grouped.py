@@ -29,6 +29,10 @@ CASES = [
     ("splitk_decode_T1", 1, 4096, 8, 2, 14336, 0, "bf16", 0.0),
     ("splitk_T5_shared", 5, 1024, 8, 2, 2048, 1, "bf16", 0.0),
     ("splitk_ragged_k", 20, 1000, 16, 4, 520, 0, "bf16", 0.0),
+    # large segments (>= 384 rows per expert on average): 256-row tiles on CTA pairs
+    ("pair_tiles", 2000, 256, 4, 2, 384, 0, "bf16", 0.0),
+    ("pair_ragged_shared", 1500, 200, 3, 2, 136, 1, "bf16", 0.0),
+    ("pair_skewed", 3000, 128, 8, 2, 256, 0, "bf16", 1.5),
     ("f32", 64, 64, 4, 2, 128, 0, "f32", 0.0),
     ("f32_shared", 90, 40, 5, 2, 48, 1, "f32", 0.0),
 ]
