@@ -348,8 +348,9 @@ def run_ours(args):
 
 def run_decode(moe, synth, dev, stream, pk, args):
     """Decode steps (T = 1, 8, 32, 64) of the same layer: weight streaming,
-    reported as algorithmic bytes / time against the HBM copy bandwidth. L2
-    is flushed (a 256 MB write) before every timed step."""
+    reported as algorithmic bytes / time against the HBM copy bandwidth, for
+    plain launches and for the same call replayed from a CUDA graph. L2 is
+    flushed (a 256 MB write) before every timed step."""
     import torch
     out = {}
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -362,24 +363,43 @@ def run_decode(moe, synth, dev, stream, pk, args):
         counts = torch.empty(w.n_experts, dtype=torch.int32, device=dev)
         wsp = moe.workspace(cfg, "layer", dev)
 
-        def step():
+        def step(st=None):
             moe.moe_layer_forward(cfg, x, base["w_router"], None, None, base["w_gate"],
                                   base["w_up"], base["w_down"], y, None, None, counts, None, wsp,
-                                  stream)
+                                  st if st is not None else torch.cuda.current_stream(dev))
         for _ in range(3):
             step()
         torch.cuda.synchronize(dev)
-        times = []
         reps = max(5, min(args.steps, 50))
-        for _ in range(reps):
-            flush.fill_(1)
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            step()
-            b.record(stream)
-            torch.cuda.synchronize(dev)
-            times.append(a.elapsed_time(b))
+
+        def timed(fn):
+            out = []
+            for _ in range(reps):
+                flush.fill_(1)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                torch.cuda.synchronize(dev)
+                out.append(a.elapsed_time(b))
+            return statistics.median(out)
+
+        ms = timed(step)
+        # The same forward captured once in a CUDA graph and replayed (what a
+        # serving loop does for decode-sized steps): no launch gaps.
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cap):
+            step(cap)  # warm the capture stream
+        torch.cuda.current_stream(dev).wait_stream(cap)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(graph, stream=cap):
+            step(cap)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        ms_graph = timed(graph.replay)
         # per-kernel breakdown in separate steps (the events add a little time)
         moe.profile_enable(True)
         moe.profile_collect()
@@ -388,14 +408,16 @@ def run_decode(moe, synth, dev, stream, pk, args):
             step()
         kern = moe.profile_collect()
         moe.profile_enable(False)
-        ms = statistics.median(times)
         wbytes, active = touched_weight_bytes(w, counts.cpu().tolist())
         total = wbytes + w.n_experts * w.d_model * 2 + 2 * w.T * w.d_model * 2
         gbs = total / (ms / 1e3) / 1e9
+        gbs_g = total / (ms_graph / 1e3) / 1e9
         out[f"T{w.T}"] = {"ms": round(ms, 4), "experts_touched": active,
                           "algorithmic_bytes": total, "gbs": round(gbs, 1),
                           "hbm_frac": round(gbs / pk["hbm"], 4),
                           "tokens_per_s": round(w.T / (ms / 1e3), 1),
+                          "graph_ms": round(ms_graph, 4), "graph_gbs": round(gbs_g, 1),
+                          "graph_hbm_frac": round(gbs_g / pk["hbm"], 4),
                           "kernel_us": {k: round(1e3 * v[0] / v[1], 1) for k, v in kern.items()}}
     return out
 

@@ -146,24 +146,25 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
-// Split factor of every tile when there are fewer tiles than CTAs: the S in
-// [1, s_max] (at least kMinKbPerSplit K blocks per split) that best fills
-// whole waves of the grid, the smallest on ties. Every CTA computes the same.
+// Split factor of every tile when there are fewer tiles than two waves of
+// CTAs: among S in [1, s_max] with at least kMinKbPerSplit K blocks per
+// split, the largest whose wave efficiency (units / whole waves of the grid)
+// is within 3% of the best; more, shorter units keep more weight bytes in
+// flight per SM, which is what decode-sized GEMMs are bound by. Every CTA
+// computes the same value.
 constexpr int kMinKbPerSplit = 8;
 __device__ __forceinline__ int choose_splits(int tiles, int grid, int KB, int s_max) {
   if (s_max <= 1 || tiles <= 0 || tiles >= 2 * grid) return 1;
-  int best = 1;
-  long long best_num = tiles, best_den = grid;  // efficiency = num / den
-  for (int S = 2; S <= s_max && KB / S >= kMinKbPerSplit; ++S) {
+  auto eff = [&](int S) {
     const long long units = (long long)tiles * S;
-    const long long den = (units + grid - 1) / grid * grid;
-    if (units * best_den > best_num * den) {
-      best = S;
-      best_num = units;
-      best_den = den;
-    }
-  }
-  return best;
+    return (float)units / (float)((units + grid - 1) / grid * grid);
+  };
+  float best = eff(1);
+  for (int S = 2; S <= s_max && KB / S >= kMinKbPerSplit; ++S) best = fmaxf(best, eff(S));
+  int pick = 1;
+  for (int S = 2; S <= s_max && KB / S >= kMinKbPerSplit; ++S)
+    if (eff(S) >= best - 0.03f) pick = S;
+  return pick;
 }
 __device__ __forceinline__ int kb_begin(int split, int S, int KB) {
   return (int)(((long long)split * KB) / S);

@@ -81,3 +81,33 @@ def test_layer_full_size(oracle, w):
     rows = sample_rows(w.T, 16, seed=w.seed)
     run, err = check_layer(oracle, w, rows)
     print(f"{w.name}: rel-inf error on {len(rows)} sampled tokens = {err:.3e}")
+
+
+def test_layer_replays_from_a_cuda_graph(oracle):
+    """moe_layer_forward only enqueues stream-ordered work (no host syncs or
+    allocations), so it can be captured in a CUDA graph; replays must give
+    the eager result bit for bit, for a prefill-sized (CTA-pair GEMMs) and a
+    decode-sized (split-K) batch."""
+    for w in (synth.Workload("graph_prefill", T=2048, d_model=512, n_experts=4, top_k=2,
+                             d_ff=512, seed=41),
+              synth.Workload("graph_decode", T=2, d_model=1024, n_experts=8, top_k=2,
+                             d_ff=2048, seed=42)):
+        inp = margin_inputs(w, oracle)
+        run = LayerRun(w, inp)()
+        torch.cuda.synchronize()
+        eager = run.y.clone()
+        run.y.fill_(float("nan"))
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=cap):
+            i = inp
+            moe.moe_layer_forward(run.cfg, i["x"], i["w_router"], i["logit_bias"], i["sel_bias"],
+                                  i["w_gate"], i["w_up"], i["w_down"], run.y, run.topk_idx,
+                                  run.topk_w, run.counts, run.prob_sum, run.ws, cap)
+        for _ in range(2):
+            run.y.fill_(float("nan"))
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(run.y.view(torch.int16), eager.view(torch.int16)), w.name
