@@ -153,8 +153,9 @@ MOE_API int moe_router_topk(const moe_config* cfg, const void* x, const void* w_
  * The scratch (a status word and per-block probability partials) lives in
  * a fixed 1 MiB array of the library's own device memory on every GPU that
  * loads the library, held until the process exits:
- *  - a call needs 256 + 4 * ceil(T / 32) * N bytes of it (for N = 256,
- *    T <= 32736); a larger call returns MOE_ERR_WORKSPACE, launching nothing;
+ *  - a call needs 256 + 4 * B * N bytes of it, B = ceil(T / 8) when N <= 32
+ *    and ceil(T / 64) otherwise (for N = 256: T <= 65472); a larger call
+ *    returns MOE_ERR_WORKSPACE, launching nothing;
  *  - the first call made with a device current looks up the array's device
  *    address for that device; make that first call before any stream capture;
  *  - all calls share the array: calls whose work overlaps on the GPU race

@@ -129,8 +129,10 @@ bool all_aligned(std::initializer_list<const void*> ps) {
   return true;
 }
 
+// Zeroes the workspace header words: [0] device status, [1] the router's
+// finished-block counter.
 int reset_status(int* status, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
+  cudaError_t e = cudaMemsetAsync(status, 0, 2 * sizeof(int), s);
   return e == cudaSuccess ? MOE_OK : fail_cuda(e);
 }
 
@@ -145,14 +147,19 @@ int check_device(const moe_config& c) {
   return (major == 10 && minor == 3) ? MOE_OK : MOE_ERR_UNSUPPORTED;
 }
 
+int seg_tile(const moe_config& c) { return c.dtype == MOE_BF16 ? seg_tile_m(c) : kTileM; }
+
+// seg_ready: the segment table was already built (by the permutation).
 int grouped_impl(const moe_config& c, const void* x_perm, long long xp_rows, const void* x,
                  const int32_t* offsets, const int32_t* sorted_pair, const float* topk_w,
                  const void* wg, const void* wu, const void* wd, void* y_perm, int32_t* seg,
-                 void* h, float* partial, int* status, cudaStream_t s) {
+                 bool seg_ready, void* h, float* partial, int* status, cudaStream_t s) {
   if (rows_total(c) == 0) return MOE_OK;
-  cudaError_t e = launch_seg_table(c, offsets, seg, c.dtype == MOE_BF16 ? seg_tile_m(c) : kTileM,
-                                   status, s);
-  if (e != cudaSuccess) return fail_cuda(e);
+  cudaError_t e = cudaSuccess;
+  if (!seg_ready) {
+    e = launch_seg_table(c, offsets, seg, seg_tile(c), status, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
   e = (c.dtype == MOE_BF16)
           ? launch_grouped_bf16(c, x_perm, x, seg, sorted_pair, topk_w, wg, wu, wd, h, y_perm, partial,
                                 xp_rows, padded_rows(rows_total(c)), status, s)
@@ -161,10 +168,11 @@ int grouped_impl(const moe_config& c, const void* x_perm, long long xp_rows, con
 }
 
 // ---- profiler ---------------------------------------------------------------
-const char* kKernelNames[K_NUM] = {"router_topk",    "router_reduce", "permute_hist",
-                                   "permute_scan",   "permute_rank",  "permute_gather",
-                                   "seg_table",      "gate_up",       "down",
-                                   "splitk_reduce",  "combine",       "balance_stats"};
+const char* kKernelNames[K_NUM] = {"router_topk",   "router_reduce",  "permute_hist",
+                                   "permute_scan",  "permute_rank",   "permute_gather",
+                                   "permute_small", "seg_table",      "gate_up",
+                                   "down",          "splitk_reduce",  "combine",
+                                   "balance_stats"};
 struct Prof {
   std::mutex mu;
   bool on = false;
@@ -317,7 +325,7 @@ int moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
   cudaError_t e = launch_permute(c, x, topk_idx, expert_offsets, sorted_pair, inv_pos, x_perm,
-                                 w.hist, w.status, s);
+                                 w.hist, w.status, nullptr, 0, s);
   return e == cudaSuccess ? MOE_OK : fail_cuda(e);
 }
 
@@ -344,7 +352,7 @@ int moe_grouped_swiglu(const moe_config* cfg, const void* x_perm, const void* x,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
   return grouped_impl(c, x_perm, pairs(c), x, expert_offsets, sorted_pair, topk_w, w_gate, w_up,
-                      w_down, y_perm, w.seg, w.h, w.partial, w.status, s);
+                      w_down, y_perm, w.seg, false, w.h, w.partial, w.status, s);
 }
 
 int moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* inv_pos,
@@ -384,10 +392,11 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* w_router
                                 cnt, ps, w.partials, w.status, s);
   if (e != cudaSuccess) return fail_cuda(e);
   if (c.T == 0) return MOE_OK;
-  e = launch_permute(c, x, idx, w.offsets, w.sorted_pair, w.inv_pos, w.x_perm, w.hist, w.status, s);
+  e = launch_permute(c, x, idx, w.offsets, w.sorted_pair, w.inv_pos, w.x_perm, w.hist, w.status,
+                     w.seg, seg_tile(c), s);
   if (e != cudaSuccess) return fail_cuda(e);
   rc = grouped_impl(c, w.x_perm, padded_rows(pairs(c)), x, w.offsets, w.sorted_pair, tw, w_gate,
-                    w_up, w_down, w.y_perm, w.seg, w.h, w.partial, w.status, s);
+                    w_up, w_down, w.y_perm, w.seg, true, w.h, w.partial, w.status, s);
   if (rc != MOE_OK) return rc;
   e = launch_combine(c, w.y_perm, w.inv_pos, nullptr, y, s);
   return e == cudaSuccess ? MOE_OK : fail_cuda(e);

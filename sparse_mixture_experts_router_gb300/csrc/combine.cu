@@ -3,10 +3,10 @@
 // y[t] = sum_slot w * y_perm[inv_pos[t*k+slot]] + sum_shared y_perm[T*k+s*T+t]
 // ("Mixture of experts and speculative decoding", step 4 and the layer
 // equation; "Mixture of Experts and Guided Decoding", the three-expert gated
-// sum). One warp per token; each lane accumulates 16-byte vectors of the
-// k + n_shared rows in fp32 in a fixed order (slots, then shared experts)
-// and writes each output element exactly once, so there are no atomics and
-// the result is reproducible.
+// sum). One block per token; each output vector accumulates the k + n_shared
+// rows' vectors in fp32 in a fixed order (slots, then shared experts) and is
+// written exactly once, so there are no atomics and the result is
+// reproducible.
 #include "device_util.cuh"
 #include "moe_internal.h"
 
@@ -14,16 +14,15 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
 
 template <typename TE>
 struct Vec;
 template <>
 struct Vec<float> {
   static constexpr int n = 4;
-  __device__ static void load(const float* p, float (&v)[4]) {
-    const float4 q = __ldg(reinterpret_cast<const float4*>(p));
-    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+  __device__ static void unpack(const uint4& q, float (&v)[4]) {
+    v[0] = __uint_as_float(q.x); v[1] = __uint_as_float(q.y);
+    v[2] = __uint_as_float(q.z); v[3] = __uint_as_float(q.w);
   }
   __device__ static void store(float* p, const float (&v)[4]) {
     *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
@@ -32,8 +31,7 @@ struct Vec<float> {
 template <>
 struct Vec<__nv_bfloat16> {
   static constexpr int n = 8;
-  __device__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
-    const uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
+  __device__ static void unpack(const uint4& q, float (&v)[8]) {
     bf16x2_to_f32(q.x, v[0], v[1]);
     bf16x2_to_f32(q.y, v[2], v[3]);
     bf16x2_to_f32(q.z, v[4], v[5]);
@@ -45,6 +43,10 @@ struct Vec<__nv_bfloat16> {
   }
 };
 
+// One block per token: the token's k slot rows and weights are read once into
+// shared memory, then each thread sums whole 16-byte vectors of the output
+// row, loading all k + n_shared terms of a vector before adding them in fp32
+// in slot order then shared order, and stores once.
 template <typename TE>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const TE* __restrict__ yp,
                                                            const int32_t* __restrict__ inv_pos,
@@ -52,35 +54,45 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const TE* __restrict_
                                                            TE* __restrict__ y, int T, int d, int k,
                                                            int n_shared) {
   constexpr int V = Vec<TE>::n;
-  const int t = blockIdx.x * kWarps + threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-  if (t >= T) return;
+  constexpr int TERMS = kMaxTopK + kMaxShared;
+  __shared__ long long s_row[TERMS];
+  __shared__ float s_w[TERMS];
+  const int t = blockIdx.x;
   const long long P = (long long)T * k;
-  long long src[kMaxTopK + kMaxShared];
-  float w[kMaxTopK + kMaxShared];
-  int n = 0;
-  for (int s = 0; s < k; ++s) {
-    const int pos = __ldg(inv_pos + (size_t)t * k + s);
-    if (pos < 0 || pos >= P) continue;  // contributes zero
-    src[n] = (long long)pos * d;
-    w[n] = topk_w ? __ldg(topk_w + (size_t)t * k + s) : 1.0f;
-    ++n;
+  if (threadIdx.x < TERMS) {
+    const int j = threadIdx.x;
+    long long row = -1;
+    float w = 1.0f;
+    if (j < kMaxTopK) {
+      if (j < k) {
+        const int pos = inv_pos[(size_t)t * k + j];
+        if (pos >= 0 && pos < P) row = pos;  // out of range: contributes zero
+        if (topk_w) w = topk_w[(size_t)t * k + j];
+      }
+    } else if (j - kMaxTopK < n_shared) {
+      row = P + (long long)(j - kMaxTopK) * T + t;
+    }
+    s_row[j] = row;
+    s_w[j] = w;
   }
-  for (int s = 0; s < n_shared; ++s) {
-    src[n] = (P + (long long)s * T + t) * d;
-    w[n] = 1.0f;
-    ++n;
-  }
+  __syncthreads();
   const int nvec = d / V;
-  for (int v = lane; v < nvec; v += 32) {
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    uint4 raw[TERMS];
+#pragma unroll
+    for (int j = 0; j < TERMS; ++j)
+      raw[j] = s_row[j] >= 0 ? __ldg(reinterpret_cast<const uint4*>(yp + s_row[j] * d) + v)
+                             : make_uint4(0, 0, 0, 0);
     float acc[V];
 #pragma unroll
     for (int q = 0; q < V; ++q) acc[q] = 0.f;
-    for (int j = 0; j < n; ++j) {
-      float val[V];
-      Vec<TE>::load(yp + src[j] + (long long)v * V, val);
 #pragma unroll
-      for (int q = 0; q < V; ++q) acc[q] = fmaf(w[j], val[q], acc[q]);
+    for (int j = 0; j < TERMS; ++j) {
+      if (s_row[j] < 0) continue;
+      float val[V];
+      Vec<TE>::unpack(raw[j], val);
+#pragma unroll
+      for (int q = 0; q < V; ++q) acc[q] = fmaf(s_w[j], val[q], acc[q]);
     }
     Vec<TE>::store(y + (size_t)t * d + (size_t)v * V, acc);
   }
@@ -109,14 +121,17 @@ __global__ void balance_stats_kernel(const int32_t* counts, const float* prob_su
 cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_t* inv_pos,
                            const float* topk_w, void* y, cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
-  const int grid = ceil_div(c.T, kWarps);
+  // one block per token, at most one thread per 16-byte vector of the row
+  const int nvec = c.d_model / (c.dtype == MOE_BF16 ? 8 : 4);
+  const int threads = nvec >= kThreads ? kThreads : ((nvec + 31) / 32) * 32;
+  const int grid = c.T;
   ProfScope p(K_COMBINE, s);
   if (c.dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(
+    combine_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(
         static_cast<const __nv_bfloat16*>(y_perm), inv_pos, topk_w, static_cast<__nv_bfloat16*>(y),
         c.T, c.d_model, c.top_k, c.n_shared);
   else
-    combine_kernel<float><<<grid, kThreads, 0, s>>>(static_cast<const float*>(y_perm), inv_pos,
+    combine_kernel<float><<<grid, threads, 0, s>>>(static_cast<const float*>(y_perm), inv_pos,
                                                     topk_w, static_cast<float*>(y), c.T, c.d_model,
                                                     c.top_k, c.n_shared);
   return cudaGetLastError();

@@ -672,48 +672,49 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // Split-K epilogue: every output element from the partials of all S splits,
 // summed in split order, then the same epilogue as the fused path. One
-// thread per 8 output columns of one row; the whole grid shares the work.
+// thread per 4 output columns of one row; its (up to kMaxSplitK) partial
+// loads are issued together before any is summed.
 template <int EPI>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmArgs a, int gemm_grid) {
   const int tiles = __ldg(a.seg + 1) * a.NT;
   const int S = choose_splits(tiles, gemm_grid, (a.K + BK - 1) / BK, a.s_max);
   if (S == 1) return;  // the GEMM finished its tiles itself
-  const int groups = a.n_out / 8;
+  const int groups = a.n_out / 4;
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= a.R * groups) return;
   const long long orow = i / groups;
-  const int col = (int)(i % groups) * 8;
-  float v[8], u[8];
+  const int col = (int)(i % groups) * 4;
+  float4 pv[kMaxSplitK], pu[kMaxSplitK];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) v[q] = u[q] = 0.f;
-#pragma unroll 4
-  for (int sp = 0; sp < S; ++sp) {
-    const float* src = a.partial + ((long long)sp * a.R + orow) * a.pc + col;
-    const float4 p0 = __ldcg(reinterpret_cast<const float4*>(src));
-    const float4 p1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
-    v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
-    v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
-    if (EPI == EPI_SWIGLU) {
-      const float4 q0 = __ldcg(reinterpret_cast<const float4*>(src + a.n_out));
-      const float4 q1 = __ldcg(reinterpret_cast<const float4*>(src + a.n_out + 4));
-      u[0] += q0.x; u[1] += q0.y; u[2] += q0.z; u[3] += q0.w;
-      u[4] += q1.x; u[5] += q1.y; u[6] += q1.z; u[7] += q1.w;
+  for (int sp = 0; sp < kMaxSplitK; ++sp) {
+    if (sp < S) {
+      const float* src = a.partial + ((long long)sp * a.R + orow) * a.pc + col;
+      pv[sp] = __ldcg(reinterpret_cast<const float4*>(src));
+      if (EPI == EPI_SWIGLU) pu[sp] = __ldcg(reinterpret_cast<const float4*>(src + a.n_out));
     }
   }
-  float h[8];
+  float v[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int sp = 0; sp < kMaxSplitK; ++sp) {
+    if (sp < S) {
+      v[0] += pv[sp].x; v[1] += pv[sp].y; v[2] += pv[sp].z; v[3] += pv[sp].w;
+      if (EPI == EPI_SWIGLU) {
+        u[0] += pu[sp].x; u[1] += pu[sp].y; u[2] += pu[sp].z; u[3] += pu[sp].w;
+      }
+    }
+  }
+  float h[4];
   if (EPI == EPI_SWIGLU) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) h[q] = silu(v[q]) * u[q];
+    for (int q = 0; q < 4; ++q) h[q] = silu(v[q]) * u[q];
   } else {
     // the row's segment: routed rows are [0, n_pairs), shared rows follow
     const float sc = (orow < a.n_pairs) ? row_scale(a, 0, orow) : 1.0f;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) h[q] = sc * v[q];
+    for (int q = 0; q < 4; ++q) h[q] = sc * v[q];
   }
   __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + orow * a.ldo + col;
-  *reinterpret_cast<uint4*>(dst) =
-      make_uint4(f32x2_to_bf16x2(h[0], h[1]), f32x2_to_bf16x2(h[2], h[3]),
-                 f32x2_to_bf16x2(h[4], h[5]), f32x2_to_bf16x2(h[6], h[7]));
+  *reinterpret_cast<uint2*>(dst) = make_uint2(f32x2_to_bf16x2(h[0], h[1]), f32x2_to_bf16x2(h[2], h[3]));
 }
 
 // ---------------------------------------------------------------- host side --
@@ -780,7 +781,7 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_sh, const CUt
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || args.s_max <= 1) return e;
-  const long long n = args.R * (args.n_out / 8);
+  const long long n = args.R * (args.n_out / 4);
   ProfScope p(K_SPLITK_REDUCE, s);
   splitk_reduce_kernel<EPI><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(args, grid);
   return cudaGetLastError();

@@ -14,8 +14,6 @@ constexpr int kMaxExperts = 256;     // router keeps a [tokens x N] score tile i
 constexpr int kMaxTopK = 8;
 constexpr int kMaxShared = 4;
 
-// Router tiling: tokens per block (256 threads, 8 warps, 4 tokens a warp).
-constexpr int kRouterTokens = 32;
 // Permutation chunk: pairs handled by one block (8 warps x 8 rounds x 32).
 constexpr int kPermuteChunk = 2048;
 
@@ -52,10 +50,12 @@ cudaError_t launch_router(const moe_config& c, const void* x, const void* w_rout
                           cudaStream_t s);
 size_t router_partials_bytes(const moe_config& c);
 
+// With seg != null it also builds the grouped GEMM's segment table (tile
+// height tile_m) from the offsets it computes.
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
                            int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos,
-                           void* x_perm, int32_t* chunk_hist, int* status,
-                           cudaStream_t s);
+                           void* x_perm, int32_t* chunk_hist, int* status, int32_t* seg,
+                           int tile_m, cudaStream_t s);
 size_t permute_scratch_bytes(const moe_config& c);
 
 cudaError_t launch_seg_table(const moe_config& c, const int32_t* offsets, int32_t* seg,
@@ -110,6 +110,7 @@ enum KernelId {
   K_PERMUTE_SCAN,
   K_PERMUTE_RANK,
   K_PERMUTE_GATHER,
+  K_PERMUTE_SMALL,
   K_SEG_TABLE,
   K_GATE_UP,
   K_DOWN,

@@ -6,7 +6,7 @@
 // every pair that chose expert e lands in e's contiguous row segment, in
 // ascending pair order, so the result is unique and bit-exact.
 //
-// Four launches:
+// Four launches (one single-block kernel when all pairs fit one chunk):
 //  hist   - one block per chunk of 2048 pairs counts pairs per expert with
 //           warp-aggregated shared-memory atomics (one atomic per distinct
 //           expert in a warp, found with __match_any_sync).
@@ -154,6 +154,108 @@ __global__ void __launch_bounds__(kThreads) permute_gather_kernel(const uint4* _
   for (int i = lane; i < vec_per_row; i += 32) dst[i] = __ldg(src + i);
 }
 
+// The counting, scans and stable ranks of the permutation (and optionally
+// the grouped GEMM's segment table) in one block when the T*k pairs fit one
+// chunk (decode-sized batches): two launches (this and the row gather)
+// instead of five. Same results as the multi-block path.
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallWarps = kSmallThreads / 32;
+__global__ void __launch_bounds__(kSmallThreads) permute_small_kernel(
+    const int32_t* __restrict__ idx, int P, int N, int k, const uint4* __restrict__ x,
+    int vec_per_row, uint4* __restrict__ x_perm, int32_t* offsets, int32_t* sorted_pair,
+    int32_t* inv_pos, int* status, int32_t* seg, int n_shared, int T, int tile_m) {
+  (void)x; (void)vec_per_row; (void)x_perm; (void)k;
+  extern __shared__ int sh[];
+  int* wh = sh;                        // [kSmallWarps][N] counts, then row bases
+  int* soff = sh + kSmallWarps * N;    // [N+1] offsets
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int i = threadIdx.x; i < kSmallWarps * N; i += kSmallThreads) wh[i] = 0;
+  __syncthreads();
+  const int per_warp = (P + kSmallWarps - 1) / kSmallWarps;
+  const int p0 = warp * per_warp, p1 = min(P, p0 + per_warp);
+  int* mine = wh + warp * N;
+  for (int b = p0; b < p1; b += 32) {
+    const int p = b + lane;
+    int e = -1;
+    if (p < p1) {
+      e = idx[p];
+      if (e < 0 || e >= N) {
+        set_status(status, MOE_ERR_DEVICE_CHECK);
+        e = -1;
+      }
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < N; e += kSmallThreads) {
+    int tot = 0;
+    for (int w = 0; w < kSmallWarps; ++w) tot += wh[w * N + e];
+    soff[e] = tot;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int e = 0; e < N; ++e) {
+      const int v = soff[e];
+      soff[e] = run;
+      offsets[e] = run;
+      run += v;
+    }
+    soff[N] = run;
+    offsets[N] = run;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < N; e += kSmallThreads) {
+    int base = soff[e];
+    for (int w = 0; w < kSmallWarps; ++w) {
+      const int v = wh[w * N + e];
+      wh[w * N + e] = base;
+      base += v;
+    }
+  }
+  __syncthreads();
+  const uint32_t lt = lanemask_lt();
+  for (int b = p0; b < p1; b += 32) {
+    const int p = b + lane;
+    int e = (p < p1) ? idx[p] : -1;
+    if (e >= N) e = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0) {
+      const int pos = mine[e] + __popc(peers & lt);
+      sorted_pair[pos] = p;
+      inv_pos[p] = pos;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    __syncwarp();
+  }
+  if (seg != nullptr) {  // segment table of the grouped GEMM (as seg_table_kernel)
+    const int E = N + n_shared;
+    int32_t* mt_start = seg + 2;
+    int32_t* rows = seg + 3 + E;
+    int32_t* a_row0 = seg + 3 + 2 * E;
+    int32_t* out_row0 = seg + 3 + 3 * E;
+    for (int e = threadIdx.x; e < E; e += kSmallThreads) {
+      rows[e] = e < N ? soff[e + 1] - soff[e] : T;
+      a_row0[e] = e < N ? soff[e] : 0;
+      out_row0[e] = e < N ? soff[e] : P + (e - N) * T;
+    }
+    if (threadIdx.x == 0) {
+      int run = 0;
+      for (int e = 0; e < E; ++e) {
+        mt_start[e] = run;
+        const int r = e < N ? soff[e + 1] - soff[e] : T;
+        run += (r + tile_m - 1) / tile_m;
+      }
+      mt_start[E] = run;
+      seg[0] = E;
+      seg[1] = run;
+    }
+  }
+}
+
 // Segment table of the grouped GEMM from the expert offsets (one block).
 // The offsets come from the caller when moe_grouped_swiglu is called on its
 // own, so they are checked first: they must start at 0, never decrease and
@@ -207,10 +309,25 @@ size_t permute_scratch_bytes(const moe_config& c) {
 
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
                            int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos,
-                           void* x_perm, int32_t* chunk_hist, int* status, cudaStream_t s) {
+                           void* x_perm, int32_t* chunk_hist, int* status, int32_t* seg,
+                           int tile_m, cudaStream_t s) {
   const int N = c.n_experts;
   const int P = c.T * c.top_k;
   if (P == 0) return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (N + 1), s);
+  if (P <= kChunk) {
+    const int vec = (int)(c.d_model * elem_bytes(c.dtype) / 16);
+    const size_t smem = sizeof(int) * ((size_t)kSmallWarps * N + N + 1);
+    {
+      ProfScope p(K_PERMUTE_SMALL, s);
+      permute_small_kernel<<<1, kSmallThreads, smem, s>>>(
+          topk_idx, P, N, c.top_k, static_cast<const uint4*>(x), vec, static_cast<uint4*>(x_perm),
+          offsets, sorted_pair, inv_pos, status, seg, c.n_shared, c.T, tile_m);
+    }
+    ProfScope p(K_PERMUTE_GATHER, s);
+    permute_gather_kernel<<<ceil_div(P, kWarps), kThreads, 0, s>>>(
+        static_cast<const uint4*>(x), sorted_pair, P, c.top_k, vec, static_cast<uint4*>(x_perm));
+    return cudaGetLastError();
+  }
   const int nch = ceil_div(P, kChunk);
   {
     ProfScope p(K_PERMUTE_HIST, s);
@@ -231,7 +348,9 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
     permute_gather_kernel<<<ceil_div(P, kWarps), kThreads, 0, s>>>(
         static_cast<const uint4*>(x), sorted_pair, P, c.top_k, vec, static_cast<uint4*>(x_perm));
   }
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || seg == nullptr) return e;
+  return launch_seg_table(c, offsets, seg, tile_m, status, s);
 }
 
 cudaError_t launch_seg_table(const moe_config& c, const int32_t* offsets, int32_t* seg,

@@ -37,6 +37,8 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTileTokens = 64;              // tokens per block, tiled kernel
 constexpr int kKC = 32;                      // K slice of the tiled kernel
+constexpr int kFusedSumMaxBlocks = 32;       // up to this grid the last block sums prob_sum
+constexpr int kSmallTokensPerBlock = 8;      // few-expert kernel: one token group a block
 
 struct RouterArgs {
   const void* x;
@@ -50,6 +52,10 @@ struct RouterArgs {
   int32_t* counts;
   float* partials;  // [gridDim.x][N]
   int* status;
+  // When set (small grids), the last block to finish sums the partials into
+  // prob_sum itself; `done` counts finished blocks and is zero at launch.
+  float* prob_sum;
+  int* done;
   int T, d, N, k, gate_mode;
 };
 
@@ -185,6 +191,21 @@ __device__ __forceinline__ void finish_block(const float (&psum)[EJ], float* wpr
     a.partials[(size_t)blockIdx.x * a.N + e] = s;
     if (bcount[e]) atomicAdd(&a.counts[e], bcount[e]);
   }
+  if (a.done == nullptr) return;
+  // Last block: prob_sum[e] = sum over blocks in block order (same order as
+  // router_reduce_kernel).
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(a.done, 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int e = threadIdx.x; e < a.N; e += kThreads) {
+    float s = 0.f;
+    for (int b = 0; b < (int)gridDim.x; ++b) s += __ldcg(a.partials + (size_t)b * a.N + e);
+    a.prob_sum[e] = s;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -225,11 +246,14 @@ __global__ void __launch_bounds__(kThreads) router_small_kernel(const RouterArgs
 #pragma unroll
       for (int q = 0; q < TB; ++q)
         xq[q] = (t0 + q < a.T) ? __ldg(x + (t0 + q) * vec + vv) : make_uint4(0, 0, 0, 0);
+      uint4 wq[NP];  // all expert rows' vectors issued before any is used
+#pragma unroll
+      for (int e = 0; e < NP; ++e)
+        wq[e] = (e < N) ? __ldg(w + (size_t)e * vec + vv) : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int e = 0; e < NP; ++e) {
-        if (e >= N) break;
         float wf[EPV];
-        V16<TX>::cvt(__ldg(w + (size_t)e * vec + vv), wf);
+        V16<TX>::cvt(wq[e], wf);
 #pragma unroll
         for (int q = 0; q < TB; ++q) {
           float xf[EPV];
@@ -461,9 +485,10 @@ bool use_small(const moe_config& c, const float* logits_in) {
   return logits_in == nullptr && c.n_experts <= 32;
 }
 
+// Blocks of the router launch; router_partials_bytes() sizes the partials
+// buffer for the larger of the two choices.
 int router_grid(const moe_config& c, const float* logits_in) {
-  // never more blocks than ceil(T/32): the partials buffer is sized for that
-  if (use_small(c, logits_in)) return ceil_div(c.T, kRouterTokens);
+  if (use_small(c, logits_in)) return ceil_div(c.T, kSmallTokensPerBlock);
   return ceil_div(c.T, kTileTokens);
 }
 
@@ -488,7 +513,9 @@ cudaError_t launch_dtype(const moe_config& c, const RouterArgs& a, int grid, cud
 }  // namespace
 
 size_t router_partials_bytes(const moe_config& c) {
-  return sizeof(float) * (size_t)ceil_div(c.T, kRouterTokens) * (size_t)c.n_experts;
+  const int blocks = c.n_experts <= 32 ? ceil_div(c.T, kSmallTokensPerBlock)
+                                       : ceil_div(c.T, kTileTokens);
+  return sizeof(float) * (size_t)blocks * (size_t)c.n_experts;
 }
 
 cudaError_t launch_router(const moe_config& c, const void* x, const void* w_router,
@@ -496,6 +523,8 @@ cudaError_t launch_router(const moe_config& c, const void* x, const void* w_rout
                           const float* logits_in, float* logits_out, int32_t* topk_idx,
                           float* topk_w, int32_t* counts, float* prob_sum, float* partials,
                           int* status, cudaStream_t s) {
+  // status[1] counts finished router blocks for the fused final sum; the
+  // caller zeroes status[0..1] before each call.
   cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.n_experts, s);
   if (e != cudaSuccess) return e;
   if (c.T == 0) return cudaMemsetAsync(prob_sum, 0, sizeof(float) * c.n_experts, s);
@@ -505,8 +534,11 @@ cudaError_t launch_router(const moe_config& c, const void* x, const void* w_rout
   a.topk_w = topk_w; a.counts = counts; a.partials = partials; a.status = status;
   a.T = c.T; a.d = c.d_model; a.N = c.n_experts; a.k = c.top_k; a.gate_mode = c.gate_mode;
   const int grid = router_grid(c, logits_in);
+  const bool fused_sum = grid <= kFusedSumMaxBlocks;
+  a.prob_sum = prob_sum;
+  a.done = fused_sum ? status + 1 : nullptr;
   e = (c.dtype == MOE_BF16) ? launch_dtype<__nv_bfloat16>(c, a, grid, s) : launch_dtype<float>(c, a, grid, s);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || fused_sum) return e;
   {
     ProfScope p(K_ROUTER_REDUCE, s);
     router_reduce_kernel<<<ceil_div(c.n_experts, 256), 256, 0, s>>>(partials, grid, c.n_experts, prob_sum);

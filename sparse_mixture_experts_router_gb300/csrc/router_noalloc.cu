@@ -12,15 +12,17 @@
 //
 // Limits and rules (also stated in include/moe.h):
 //  - The array is kNoallocScratchBytes (1 MiB) per GPU that loads the
-//    library, held until the process exits. A call needs
-//    256 + 4 * ceil(T / 32) * N bytes of it; a larger call returns
-//    MOE_ERR_WORKSPACE and launches nothing.
+//    library, held until the process exits. A call needs 256 + 4 * B * N
+//    bytes of it, B = ceil(T / 8) when N <= 32 and ceil(T / 64) otherwise
+//    (the router's block count); a larger call returns MOE_ERR_WORKSPACE
+//    and launches nothing.
 //  - The array's device address is looked up once per device, by the first
 //    call made while that device is current; make that first call before
 //    any stream capture.
 //  - Every call shares the one array and it keeps the last call's contents.
-//    The status word is cleared at the start of every call; the partials are
-//    fully rewritten before they are read. Calls whose work overlaps on the
+//    The status word and the router's finished-block counter are cleared at
+//    the start of every call; the partials are fully rewritten before they
+//    are read. Calls whose work overlaps on the
 //    GPU (different streams, or different host threads without ordering)
 //    race on the array and give undefined results.
 //  - Nothing here calls cudaMalloc, cudaFree or any allocating routine.
@@ -87,7 +89,7 @@ extern "C" int moe_router_topk_noalloc(const moe_config* cfg, const void* x, con
   int* status = static_cast<int*>(scratch);
   float* partials = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + kStatusBytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  e = cudaMemsetAsync(status, 0, sizeof(int), s);
+  e = cudaMemsetAsync(status, 0, 2 * sizeof(int), s);  // status, router block counter
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   e = launch_router(c, x, w_router, logit_bias, sel_bias, logits_in, logits_out, topk_idx, topk_w,
                     counts, prob_sum, partials, status, s);
