@@ -250,26 +250,50 @@ def run_ours(args):
     value = ws * w.T * args.steps / (ms_total / 1e3)
 
     # ---- end to end through the C ABI with host buffers ----------------------
+    # Every step copies its tokens from pinned host memory to the device, runs
+    # moe_layer_forward and copies y back to pinned host memory. The copies of
+    # step i+1 / i-1 overlap the forward of step i (separate copy streams,
+    # two device buffers each, ordered with events), as a serving loop does.
     x_host = inp["x"].cpu().pin_memory()
-    y_host = torch.empty(w.T, w.d_model, dtype=torch.bfloat16).pin_memory()
-    x_dev = torch.empty_like(inp["x"])
-    for _ in range(2):
-        x_dev.copy_(x_host, non_blocking=True)
-        step(x_dev)
-        y_host.copy_(y, non_blocking=True)
+    y_host = [torch.empty(w.T, w.d_model, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(inp["x"]) for _ in range(2)]
+    y_dev = [torch.empty_like(y) for _ in range(2)]
+    h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    x_ready, x_free = [ev(), ev()], [ev(), ev()]
+    y_ready, y_free = [ev(), ev()], [ev(), ev()]
+    for e_ in x_free + y_free:
+        e_.record(stream)
+
+    def e2e_step(i):
+        b = i % 2
+        h2d.wait_event(x_free[b])
+        with torch.cuda.stream(h2d):
+            x_dev[b].copy_(x_host, non_blocking=True)
+        x_ready[b].record(h2d)
+        stream.wait_event(x_ready[b])
+        stream.wait_event(y_free[b])
+        moe.moe_layer_forward(cfg, x_dev[b], inp["w_router"], inp["logit_bias"], inp["sel_bias"],
+                              inp["w_gate"], inp["w_up"], inp["w_down"], y_dev[b], idx, tw, counts,
+                              ps, wsp, stream)
+        x_free[b].record(stream)
+        y_ready[b].record(stream)
+        d2h.wait_event(y_ready[b])
+        with torch.cuda.stream(d2h):
+            y_host[b].copy_(y_dev[b], non_blocking=True)
+        y_free[b].record(d2h)
+
+    for i in range(4):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     barrier(ws)
-    f0 = torch.cuda.Event(enable_timing=True)
-    f1 = torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for _ in range(args.steps):
-        x_dev.copy_(x_host, non_blocking=True)
-        step(x_dev)
-        y_host.copy_(y, non_blocking=True)
-    f1.record(stream)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
+    e2e_s = time.perf_counter() - t0
     barrier(ws)
-    e2e_ms = reduce_max(f0.elapsed_time(f1), ws)
+    e2e_ms = reduce_max(e2e_s * 1e3, ws)
     e2e_value = ws * w.T * args.steps / (e2e_ms / 1e3)
     bytes_io = w.T * w.d_model * 2
 
@@ -337,7 +361,9 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": bytes_io,
                     "d2h_bytes_per_step": bytes_io,
-                    "path": "pinned host x -> H2D -> moe_layer_forward (C ABI) -> D2H y"},
+                    "path": "per step: pinned host x -> H2D (copy stream) -> moe_layer_forward "
+                            "(C ABI, compute stream) -> D2H y (copy stream) -> pinned host; "
+                            "copies overlap neighbouring steps' forwards; host wall clock"},
             "gpu_launches": int(launches),
             "clocks": clk,
             "kernels": per_kernel,
