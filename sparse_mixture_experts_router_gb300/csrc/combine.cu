@@ -59,6 +59,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const TE* __restrict_
   __shared__ float s_w[TERMS];
   const int t = blockIdx.x;
   const long long P = (long long)T * k;
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x < TERMS) {
     const int j = threadIdx.x;
     long long row = -1;
@@ -101,6 +103,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const TE* __restrict_
 __global__ void balance_stats_kernel(const int32_t* counts, const float* prob_sum, int N, int T,
                                      int k, float alpha, float* f, float* P, float* aux) {
   __shared__ float fp[kMaxExperts];
+  pdl_wait();
+  pdl_trigger();
   for (int e = threadIdx.x; e < N; e += blockDim.x) {
     const float fe = T > 0 ? (float)counts[e] / ((float)T * (float)k) : 0.f;
     const float pe = T > 0 ? prob_sum[e] / (float)T : 0.f;
@@ -127,21 +131,19 @@ cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_
   const int grid = c.T;
   ProfScope p(K_COMBINE, s);
   if (c.dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(y_perm), inv_pos, topk_w, static_cast<__nv_bfloat16*>(y),
-        c.T, c.d_model, c.top_k, c.n_shared);
-  else
-    combine_kernel<float><<<grid, threads, 0, s>>>(static_cast<const float*>(y_perm), inv_pos,
-                                                    topk_w, static_cast<float*>(y), c.T, c.d_model,
-                                                    c.top_k, c.n_shared);
-  return cudaGetLastError();
+    return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(grid), dim3(threads), 0, s, 1,
+                      static_cast<const __nv_bfloat16*>(y_perm), inv_pos, topk_w,
+                      static_cast<__nv_bfloat16*>(y), c.T, c.d_model, c.top_k, c.n_shared);
+  return launch_pdl(combine_kernel<float>, dim3(grid), dim3(threads), 0, s, 1,
+                    static_cast<const float*>(y_perm), inv_pos, topk_w, static_cast<float*>(y),
+                    c.T, c.d_model, c.top_k, c.n_shared);
 }
 
 cudaError_t launch_balance_stats(int N, int T, int k, const int32_t* counts, const float* prob_sum,
                                  float alpha, float* f, float* P, float* aux, cudaStream_t s) {
   ProfScope p(K_BALANCE, s);
-  balance_stats_kernel<<<1, 256, 0, s>>>(counts, prob_sum, N, T, k, alpha, f, P, aux);
-  return cudaGetLastError();
+  return launch_pdl(balance_stats_kernel, dim3(1), dim3(256), 0, s, 1, counts, prob_sum, N, T, k,
+                    alpha, f, P, aux);
 }
 
 }  // namespace moe

@@ -32,6 +32,19 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Programmatic dependent launch. Every kernel of the library is launched
+// with programmatic stream serialization, so it may start while the previous
+// kernel on the stream is still running: pdl_wait() blocks until all
+// previous grids have completed and their memory is visible, and must come
+// before the kernel's first global-memory access (read or write) of data
+// another kernel touches. pdl_trigger() lets the next kernel launch; it is
+// issued right after pdl_wait(). Without the launch attribute both are
+// no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // bf16 pairs packed in 32-bit words <-> fp32.
 __device__ __forceinline__ void bf16x2_to_f32(uint32_t u, float& lo, float& hi) {
   lo = __uint_as_float(u << 16);

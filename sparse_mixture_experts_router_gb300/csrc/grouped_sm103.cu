@@ -248,11 +248,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t ring = (ptx::smem_addr(dyn_smem) + 1023u) & ~1023u;
 
   const int32_t* seg = args.seg;
-  const int E = __ldg(seg);
-  const int tiles = __ldg(seg + 1) * args.NT;
   const int KB = (args.K + BK - 1) / BK;
-  const int S = choose_splits(tiles, gridDim.x, KB, args.s_max);
-  const int total = tiles * S;  // work units: (tile, split), splits of a tile adjacent
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -282,6 +278,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = st.tmem_base;
   volatile int* abort_flag = &st.abort;
+  pdl_wait();  // the segment table and the operands come from earlier kernels
+  pdl_trigger();
+  const int E = __ldg(seg);
+  const int tiles = __ldg(seg + 1) * args.NT;
+  const int S = choose_splits(tiles, gridDim.x, KB, args.s_max);
+  const int total = tiles * S;  // work units: (tile, split), splits of a tile adjacent
 
   if (warp == 0) {
     // ------------------------------------------------------- TMA producer --
@@ -501,8 +503,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t ring = (ptx::smem_addr(dyn_smem) + 1023u) & ~1023u;
 
   const int32_t* seg = args.seg;  // built with 256-row tiles
-  const int E = __ldg(seg);
-  const int tiles = __ldg(seg + 1) * args.NT;
   const int KB = (args.K + BK - 1) / BK;
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
 
@@ -535,6 +535,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = st.tmem_base;
   volatile int* abort_flag = &st.abort;
+  pdl_wait();  // the segment table and the operands come from earlier kernels
+  pdl_trigger();
+  const int E = __ldg(seg);
+  const int tiles = __ldg(seg + 1) * args.NT;
 
   if (warp == 0) {
     // ----------------------------------------------- TMA producer (both CTAs) --
@@ -670,12 +674,271 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Decode-sized batches (T <= 64, so every expert segment has at most 64
+// rows): swap A and B. The expert weights are the MMA's M side (128 output
+// features of one expert per tile) and the segment's few token rows the N
+// side (16-64), so a stage holds only bytes the product needs: for gate/up
+// a 128x64 tile of W_gate and of W_up and Ntok x 64 of the tokens, for down
+// a 128x64 tile of W_down and Ntok x 64 of H. Gate and up accumulate in two
+// TMEM column ranges of one 256-column buffer; the epilogue thread of TMEM
+// lane j owns output feature j of the tile for every token of the segment.
+// The ring has as many stages as fit in shared memory (5 for gate/up, 8+
+// for down), so more weight bytes are in flight per SM than with 128-row
+// token tiles. Tiles, splits and the partial-row layout are those of
+// grouped_gemm_kernel, so splitk_reduce_kernel finishes split tiles.
+constexpr int kDecodeMaxRows = 64;
+constexpr int TOK_BOX = 16;                       // token rows per TMA box
+constexpr int TOK_BOX_BYTES = TOK_BOX * BK * 2;   // 2 KB
+constexpr size_t DYN_SMEM_DECODE = 200 * 1024 + 1024;
+constexpr int kDecodeMaxStages = 16;
+
+struct __align__(8) DecodeState {
+  uint64_t full[kDecodeMaxStages];
+  uint64_t empty[kDecodeMaxStages];
+  uint64_t acc_full[NUM_ACC];
+  uint64_t acc_empty[NUM_ACC];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct DecodeShape {
+  int stages;       // ring depth
+  int stage_bytes;  // multiple of 1024
+  int a_bytes;      // weight bytes a stage (16 or 32 KB)
+};
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_decode_kernel(const __grid_constant__ CUtensorMap map_w0,
+                          const __grid_constant__ CUtensorMap map_w1,
+                          const __grid_constant__ CUtensorMap map_tok,
+                          const __grid_constant__ CUtensorMap map_tok_shared, const GemmArgs args,
+                          const DecodeShape shape) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ DecodeState st;
+
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x / 32), 0);
+  const int lane = threadIdx.x % 32;
+  const uint32_t ring = (ptx::smem_addr(dyn_smem) + 1023u) & ~1023u;
+  const int STG = shape.stages;
+
+  const int32_t* seg = args.seg;
+  const int KB = (args.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STG; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&st.full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&st.empty[i]), 1);
+    }
+    for (int i = 0; i < NUM_ACC; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&st.acc_full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&st.acc_empty[i]), EPI_THREADS);
+    }
+    ptx::mbar_init(ptx::smem_addr(&st.drain), 1);
+    st.abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&map_w0);
+    ptx::prefetch_tmap(&map_w1);
+    ptx::prefetch_tmap(&map_tok);
+    ptx::prefetch_tmap(&map_tok_shared);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(&st.tmem_base), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = st.tmem_base;
+  volatile int* abort_flag = &st.abort;
+  pdl_wait();  // the segment table and the operands come from earlier kernels
+  pdl_trigger();
+  const int E = __ldg(seg);
+  const int tiles = __ldg(seg + 1) * args.NT;
+  const int S = choose_splits(tiles, gridDim.x, KB, args.s_max);
+  const int total = tiles * S;
+
+  if (warp == 0) {
+    // ------------------------------------------------------- TMA producer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x) {
+        const int split = unit % S;
+        const Tile t = decode_tile(seg, E, args.NT, unit / S);
+        const int rows = __ldg(seg + 3 + E + t.s);
+        const int nbox = (rows + TOK_BOX - 1) / TOK_BOX;
+        const int w_row = t.s * args.b_rows + t.n * BM;
+        int tok_row;
+        const CUtensorMap* tm = &map_tok;
+        if (EPI == EPI_SWIGLU) {
+          tok_row = __ldg(seg + 3 + 2 * E + t.s);
+          if (t.s >= args.n_routed) tm = &map_tok_shared;
+        } else {
+          tok_row = __ldg(seg + 3 + 3 * E + t.s);
+        }
+        const uint32_t tx = (uint32_t)shape.a_bytes + (uint32_t)(nbox * TOK_BOX_BYTES);
+        const int kb1 = kb_begin(split + 1, S, KB);
+        for (int kb = kb_begin(split, S, KB); kb < kb1; ++kb) {
+          if (!wait_phase(ptx::smem_addr(&st.empty[stage]), phase ^ 1u, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = ptx::smem_addr(&st.full[stage]);
+          const uint32_t dst = ring + stage * shape.stage_bytes;
+          ptx::mbar_arrive_expect_tx(fb, tx);
+          ptx::tma_load_2d(dst, &map_w0, fb, kb * BK, w_row);
+          if (EPI == EPI_SWIGLU) ptx::tma_load_2d(dst + A_BYTES, &map_w1, fb, kb * BK, w_row);
+          for (int b = 0; b < nbox; ++b)
+            ptx::tma_load_2d(dst + shape.a_bytes + b * TOK_BOX_BYTES, tm, fb, kb * BK,
+                             tok_row + b * TOK_BOX);
+          ++issued;
+          if (++stage == STG) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        const long long n = issued < STG ? issued : STG;
+        for (long long i = 1; i <= n; ++i) {
+          const long long q = issued - i;
+          drain_wait(ptx::smem_addr(&st.full[q % STG]), (uint32_t)((q / STG) & 1));
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x) {
+        const Tile t = decode_tile(seg, E, args.NT, unit / S);
+        const int rows = __ldg(seg + 3 + E + t.s);
+        const int ntok = ((rows + TOK_BOX - 1) / TOK_BOX) * TOK_BOX;
+        const uint32_t idesc = ptx::idesc_bf16_f32(BM, ntok);
+        if (!wait_phase(ptx::smem_addr(&st.acc_empty[acc]), acc_phase ^ 1u, abort_flag,
+                        args.status)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        const int split = unit % S;
+        const int kb0 = kb_begin(split, S, KB), kb1 = kb_begin(split + 1, S, KB);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_phase(ptx::smem_addr(&st.full[stage]), phase, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t src = ring + stage * shape.stage_bytes;
+          const uint64_t w0 = ptx::sdesc_k128(src);
+          const uint64_t w1 = ptx::sdesc_k128(src + A_BYTES);
+          const uint64_t tk = ptx::sdesc_k128(src + shape.a_bytes);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
+            ptx::mma_bf16(d_tmem, w0 + 2 * k, tk + 2 * k, idesc, accum);
+            if (EPI == EPI_SWIGLU) ptx::mma_bf16(d_tmem + 128, w1 + 2 * k, tk + 2 * k, idesc, accum);
+          }
+          ptx::mma_commit(ptx::smem_addr(&st.empty[stage]));
+          if (++stage == STG) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(ptx::smem_addr(&st.acc_full[acc]));
+        if (++acc == NUM_ACC) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        ptx::mma_commit(ptx::smem_addr(&st.drain));
+        drain_wait(ptx::smem_addr(&st.drain), 0);
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- epilogue --
+    const int sub = warp & 3;
+    const int j = sub * 32 + lane;  // TMEM lane = output feature within the tile
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int unit = blockIdx.x; unit < total; unit += gridDim.x) {
+      const int split = unit % S;
+      const Tile t = decode_tile(seg, E, args.NT, unit / S);
+      bool ok = wait_phase(ptx::smem_addr(&st.acc_full[acc]), acc_phase, abort_flag, args.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      ptx::tc_fence_after();
+      const int rows = __ldg(seg + 3 + E + t.s);
+      const long long row0 = __ldg(seg + 3 + 3 * E + t.s);
+      const int f = t.n * BM + j;
+      const bool fvalid = f < args.n_out;
+      const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * BN);
+      for (int c0 = 0; c0 < rows; c0 += 32) {
+        uint32_t a[32], b[32];
+        ptx::tmem_ld32(tbase + c0, a);
+        if (EPI == EPI_SWIGLU) ptx::tmem_ld32(tbase + 128 + c0, b);
+        ptx::tmem_ld_wait();
+        const int cn = min(32, rows - c0);
+        if (fvalid) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            if (c >= cn) break;
+            const long long orow = row0 + c0 + c;
+            const float av = __uint_as_float(a[c]);
+            if (S == 1) {
+              float h;
+              if (EPI == EPI_SWIGLU) h = silu(av) * __uint_as_float(b[c]);
+              else h = row_scale(args, t.s, orow) * av;
+              out[orow * args.ldo + f] = __float2bfloat16_rn(h);
+            } else {
+              float* prow = args.partial + ((long long)split * args.R + orow) * args.pc;
+              prow[f] = av;
+              if (EPI == EPI_SWIGLU) prow[args.n_out + f] = __uint_as_float(b[c]);
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_addr(&st.acc_empty[acc]));
+      if (++acc == NUM_ACC) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------- teardown --
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
 // Split-K epilogue: every output element from the partials of all S splits,
 // summed in split order, then the same epilogue as the fused path. One
 // thread per 4 output columns of one row; its (up to kMaxSplitK) partial
 // loads are issued together before any is summed.
 template <int EPI>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmArgs a, int gemm_grid) {
+  pdl_wait();
+  pdl_trigger();
   const int tiles = __ldg(a.seg + 1) * a.NT;
   const int S = choose_splits(tiles, gemm_grid, (a.K + BK - 1) / BK, a.s_max);
   if (S == 1) return;  // the GEMM finished its tiles itself
@@ -737,14 +1000,15 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix [rows][cols] read in boxes of 128 rows x 64 columns
-// with the 128-byte swizzle; out-of-range elements read as zero.
-bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols) {
+// Row-major bf16 matrix [rows][cols] read in boxes of box_rows rows x 64
+// columns with the 128-byte swizzle; out-of-range elements read as zero.
+bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols,
+              unsigned box_rows = 128u) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)BK, 128u};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1u, 1u};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -775,16 +1039,50 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_sh, const CUt
   // With split-K possible every SM takes part; otherwise no more CTAs than tiles.
   const int grid = (args.s_max > 1 || max_tiles >= num_sms()) ? num_sms() : max_tiles;
   if (grid <= 0) return cudaSuccess;
+  cudaError_t e;
   {
     ProfScope p(EPI == EPI_SWIGLU ? K_GATE_UP : K_DOWN, s);
-    grouped_gemm_kernel<EPI><<<grid, THREADS, DYN_SMEM, s>>>(a, a_sh, b0, b1, args);
+    e = launch_pdl(grouped_gemm_kernel<EPI>, dim3(grid), dim3(THREADS), DYN_SMEM, s, 1, a, a_sh, b0,
+                   b1, args);
   }
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || args.s_max <= 1) return e;
   const long long n = args.R * (args.n_out / 4);
   ProfScope p(K_SPLITK_REDUCE, s);
-  splitk_reduce_kernel<EPI><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(args, grid);
-  return cudaGetLastError();
+  return launch_pdl(splitk_reduce_kernel<EPI>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, 1,
+                    args, grid);
+}
+
+template <int EPI>
+cudaError_t launch_decode(const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap& tok,
+                          const CUtensorMap& tok_sh, const GemmArgs& args, int max_rows,
+                          cudaStream_t s) {
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_decode_kernel<EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)DYN_SMEM_DECODE);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  DecodeShape sh;
+  sh.a_bytes = (EPI == EPI_SWIGLU) ? 2 * A_BYTES : A_BYTES;
+  const int tok_bytes = ((max_rows + TOK_BOX - 1) / TOK_BOX) * TOK_BOX_BYTES;
+  sh.stage_bytes = (sh.a_bytes + tok_bytes + 1023) / 1024 * 1024;
+  sh.stages = std::min(kDecodeMaxStages, (int)((DYN_SMEM_DECODE - 1024) / sh.stage_bytes));
+  const int grid = num_sms();
+  cudaError_t e;
+  {
+    ProfScope p(EPI == EPI_SWIGLU ? K_GATE_UP : K_DOWN, s);
+    e = launch_pdl(grouped_decode_kernel<EPI>, dim3(grid), dim3(THREADS), DYN_SMEM_DECODE, s, 1, w0,
+                   w1, tok, tok_sh, args, sh);
+  }
+  if (e != cudaSuccess || args.s_max <= 1) return e;
+  const long long n = args.R * (args.n_out / 4);
+  ProfScope p(K_SPLITK_REDUCE, s);
+  return launch_pdl(splitk_reduce_kernel<EPI>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, 1,
+                    args, grid);
 }
 
 long long mt_bound_of(const moe_config& c, int tile_m) {
@@ -847,20 +1145,9 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a_sh, const CUt
                         cudaStream_t s) {
   const int clusters = std::min(max_tiles, max_pair_clusters());
   if (clusters <= 0) return cudaSuccess;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * clusters);
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = DYN_SMEM_PAIR;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   ProfScope p(EPI == EPI_SWIGLU ? K_GATE_UP : K_DOWN, s);
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<EPI>, a, a_sh, b0, b1, args);
+  return launch_pdl(grouped_gemm_pair_kernel<EPI>, dim3(2 * clusters), dim3(THREADS), DYN_SMEM_PAIR,
+                    s, 2, a, a_sh, b0, b1, args);
 }
 
 
@@ -907,6 +1194,7 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
   const long long R = P + (long long)c.n_shared * c.T;  // rows of H and y_perm
   if (R == 0) return cudaSuccess;
   const bool pair = use_pair_tiles(c);
+  const bool decode = !pair && c.T <= kDecodeMaxRows;  // every segment has <= 64 rows
   const long long mt_bound = mt_bound_of(c, pair ? PAIR_TILE_M : BM);
   const SplitKPlan plan = splitk_plan(c);
   if (pair) {
@@ -942,6 +1230,31 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
   g.s_max = plan.s_max_gu;
   g.pc = 2 * c.d_ff;
   g.R = R;
+  if (decode) {
+    // token tiles of 16 rows over x_perm / x (gate/up) and H (down)
+    CUtensorMap t_xp, t_x, t_h;
+    const bool ok2 = make_map(&t_xp, P > 0 ? x_perm : x, P > 0 ? std::max(P, xp_rows) : c.T,
+                              c.d_model, TOK_BOX) &&
+                     make_map(&t_x, c.n_shared > 0 ? x : (P > 0 ? x_perm : x),
+                              c.n_shared > 0 ? c.T : (P > 0 ? P : c.T), c.d_model, TOK_BOX) &&
+                     make_map(&t_h, h, std::max(R, h_rows), c.d_ff, TOK_BOX);
+    if (!ok2) return cudaErrorInvalidValue;
+    const int max_rows = c.T;  // a segment holds at most T rows
+    cudaError_t e = launch_decode<EPI_SWIGLU>(m_wg, m_wu, t_xp, t_x, g, max_rows, s);
+    if (e != cudaSuccess) return e;
+    GemmArgs d = g;
+    d.topk_w = topk_w;
+    d.out = y_perm;
+    d.ldo = c.d_model;
+    d.K = c.d_ff;
+    d.n_out = c.d_model;
+    d.NT = (c.d_model + BM - 1) / BM;
+    d.b_rows = c.d_model;
+    d.s_max = plan.s_max_dn;
+    d.pc = c.d_model;
+    return launch_decode<EPI_DOWN>(m_wd, m_wd, t_h, t_h, d, max_rows, s);
+  }
+
   cudaError_t e = pair ? launch_pair<EPI_SWIGLU>(m_xp, m_x, m_wg, m_wu, g, (int)(mt_bound * g.NT), s)
                        : launch_gemm<EPI_SWIGLU>(m_xp, m_x, m_wg, m_wu, g, (int)(mt_bound * g.NT), s);
   if (e != cudaSuccess) return e;

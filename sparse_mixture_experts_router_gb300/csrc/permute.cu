@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(kThreads) permute_hist_kernel(const int32_t* _
                                                                 int P, int N, int32_t* hist,
                                                                 int* status) {
   extern __shared__ int sh[];
+  pdl_wait();
+  pdl_trigger();
   for (int e = threadIdx.x; e < N; e += kThreads) sh[e] = 0;
   __syncthreads();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -59,6 +61,8 @@ __global__ void __launch_bounds__(kThreads) permute_hist_kernel(const int32_t* _
 __global__ void __launch_bounds__(kThreads) permute_scan_kernel(int32_t* hist, int nchunks, int N,
                                                                 int32_t* offsets) {
   extern __shared__ int tot[];
+  pdl_wait();
+  pdl_trigger();
   for (int e = threadIdx.x; e < N; e += kThreads) {
     int run = 0;
     for (int c = 0; c < nchunks; ++c) {
@@ -90,6 +94,8 @@ __global__ void __launch_bounds__(kThreads) permute_rank_kernel(const int32_t* _
                                                                 int32_t* sorted_pair,
                                                                 int32_t* inv_pos) {
   extern __shared__ int wh[];  // [kWarps][N]
+  pdl_wait();
+  pdl_trigger();
   for (int i = threadIdx.x; i < kWarps * N; i += kThreads) wh[i] = 0;
   __syncthreads();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -141,6 +147,8 @@ __global__ void __launch_bounds__(kThreads) permute_gather_kernel(const uint4* _
                                                                   uint4* __restrict__ x_perm) {
   const int row = blockIdx.x * kWarps + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  pdl_wait();
+  pdl_trigger();
   if (row >= P) return;
   // Rows past the last valid pair stay unwritten when some expert index was
   // out of range (already reported in the status word); never read through
@@ -169,6 +177,8 @@ __global__ void __launch_bounds__(kSmallThreads) permute_small_kernel(
   int* wh = sh;                        // [kSmallWarps][N] counts, then row bases
   int* soff = sh + kSmallWarps * N;    // [N+1] offsets
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  pdl_wait();
+  pdl_trigger();
   for (int i = threadIdx.x; i < kSmallWarps * N; i += kSmallThreads) wh[i] = 0;
   __syncthreads();
   const int per_warp = (P + kSmallWarps - 1) / kSmallWarps;
@@ -265,6 +275,8 @@ __global__ void seg_table_kernel(const int32_t* __restrict__ offsets, int N, int
                                  int P, int tile_m, int32_t* seg, int* status) {
   __shared__ int ok;
   const int E = N + n_shared;
+  pdl_wait();
+  pdl_trigger();
   int32_t* mt_start = seg + 2;
   int32_t* rows = seg + 3 + E;
   int32_t* a_row0 = seg + 3 + 2 * E;
@@ -319,36 +331,44 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
     const size_t smem = sizeof(int) * ((size_t)kSmallWarps * N + N + 1);
     {
       ProfScope p(K_PERMUTE_SMALL, s);
-      permute_small_kernel<<<1, kSmallThreads, smem, s>>>(
-          topk_idx, P, N, c.top_k, static_cast<const uint4*>(x), vec, static_cast<uint4*>(x_perm),
-          offsets, sorted_pair, inv_pos, status, seg, c.n_shared, c.T, tile_m);
+      cudaError_t e = launch_pdl(permute_small_kernel, dim3(1), dim3(kSmallThreads), smem, s, 1,
+                                 topk_idx, P, N, c.top_k, static_cast<const uint4*>(x), vec,
+                                 static_cast<uint4*>(x_perm), offsets, sorted_pair, inv_pos, status,
+                                 seg, c.n_shared, c.T, tile_m);
+      if (e != cudaSuccess) return e;
     }
     ProfScope p(K_PERMUTE_GATHER, s);
-    permute_gather_kernel<<<ceil_div(P, kWarps), kThreads, 0, s>>>(
-        static_cast<const uint4*>(x), sorted_pair, P, c.top_k, vec, static_cast<uint4*>(x_perm));
-    return cudaGetLastError();
+    return launch_pdl(permute_gather_kernel, dim3(ceil_div(P, kWarps)), dim3(kThreads), 0, s, 1,
+                      static_cast<const uint4*>(x), sorted_pair, P, c.top_k, vec,
+                      static_cast<uint4*>(x_perm));
   }
   const int nch = ceil_div(P, kChunk);
+  cudaError_t e;
   {
     ProfScope p(K_PERMUTE_HIST, s);
-    permute_hist_kernel<<<nch, kThreads, sizeof(int) * N, s>>>(topk_idx, P, N, chunk_hist, status);
+    e = launch_pdl(permute_hist_kernel, dim3(nch), dim3(kThreads), sizeof(int) * N, s, 1, topk_idx,
+                   P, N, chunk_hist, status);
+    if (e != cudaSuccess) return e;
   }
   {
     ProfScope p(K_PERMUTE_SCAN, s);
-    permute_scan_kernel<<<1, kThreads, sizeof(int) * N, s>>>(chunk_hist, nch, N, offsets);
+    e = launch_pdl(permute_scan_kernel, dim3(1), dim3(kThreads), sizeof(int) * N, s, 1, chunk_hist,
+                   nch, N, offsets);
+    if (e != cudaSuccess) return e;
   }
   {
     ProfScope p(K_PERMUTE_RANK, s);
-    permute_rank_kernel<<<nch, kThreads, sizeof(int) * kWarps * N, s>>>(topk_idx, P, N, chunk_hist,
-                                                                       sorted_pair, inv_pos);
+    e = launch_pdl(permute_rank_kernel, dim3(nch), dim3(kThreads), sizeof(int) * kWarps * N, s, 1,
+                   topk_idx, P, N, (const int32_t*)chunk_hist, sorted_pair, inv_pos);
+    if (e != cudaSuccess) return e;
   }
   {
     const int vec = (int)(c.d_model * elem_bytes(c.dtype) / 16);
     ProfScope p(K_PERMUTE_GATHER, s);
-    permute_gather_kernel<<<ceil_div(P, kWarps), kThreads, 0, s>>>(
-        static_cast<const uint4*>(x), sorted_pair, P, c.top_k, vec, static_cast<uint4*>(x_perm));
+    e = launch_pdl(permute_gather_kernel, dim3(ceil_div(P, kWarps)), dim3(kThreads), 0, s, 1,
+                   static_cast<const uint4*>(x), (const int32_t*)sorted_pair, P, c.top_k, vec,
+                   static_cast<uint4*>(x_perm));
   }
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || seg == nullptr) return e;
   return launch_seg_table(c, offsets, seg, tile_m, status, s);
 }
@@ -356,9 +376,8 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
 cudaError_t launch_seg_table(const moe_config& c, const int32_t* offsets, int32_t* seg,
                              int tile_m, int* status, cudaStream_t s) {
   ProfScope p(K_SEG_TABLE, s);
-  seg_table_kernel<<<1, 256, 0, s>>>(offsets, c.n_experts, c.n_shared, c.T, c.T * c.top_k, tile_m,
-                                     seg, status);
-  return cudaGetLastError();
+  return launch_pdl(seg_table_kernel, dim3(1), dim3(256), 0, s, 1, offsets, c.n_experts, c.n_shared,
+                    c.T, c.T * c.top_k, tile_m, seg, status);
 }
 
 }  // namespace moe

@@ -229,6 +229,8 @@ __global__ void __launch_bounds__(kThreads) router_small_kernel(const RouterArgs
   const int vpw = (vec + kWarps - 1) / kWarps;     // vectors per warp
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int v_lo = warp * vpw, v_hi = min(vec, v_lo + vpw);
+  pdl_wait();
+  pdl_trigger();
   const uint4* x = static_cast<const uint4*>(a.x);
   const uint4* w = static_cast<const uint4*>(a.w);
   if (tid < 32) bcount[tid] = 0;
@@ -320,6 +322,8 @@ __global__ void __launch_bounds__(kThreads) router_tiled_kernel(const RouterArgs
   const int eg = tid % NEG, tg = tid / NEG;
   const long long t0 = (long long)blockIdx.x * BM;
   const int N = a.N;
+  pdl_wait();
+  pdl_trigger();
   for (int e = tid; e < BN; e += kThreads) bcount[e] = 0;
 
   if (a.logits_in == nullptr) {
@@ -459,17 +463,12 @@ __global__ void __launch_bounds__(kThreads) router_tiled_kernel(const RouterArgs
 // prob_sum[e] = sum over blocks, in block order.
 __global__ void router_reduce_kernel(const float* partials, int nblk, int N, float* prob_sum) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (e >= N) return;
   float s = 0.f;
   for (int b = 0; b < nblk; ++b) s += partials[(size_t)b * N + e];
   prob_sum[e] = s;
-}
-
-int num_sms() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
 }
 
 template <typename K>
@@ -477,8 +476,7 @@ cudaError_t launch_k(K kernel, const RouterArgs& a, int grid, size_t smem, cudaS
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   ProfScope p(K_ROUTER, s);
-  kernel<<<grid, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(grid), dim3(kThreads), smem, s, 1, a);
 }
 
 bool use_small(const moe_config& c, const float* logits_in) {
@@ -539,11 +537,9 @@ cudaError_t launch_router(const moe_config& c, const void* x, const void* w_rout
   a.done = fused_sum ? status + 1 : nullptr;
   e = (c.dtype == MOE_BF16) ? launch_dtype<__nv_bfloat16>(c, a, grid, s) : launch_dtype<float>(c, a, grid, s);
   if (e != cudaSuccess || fused_sum) return e;
-  {
-    ProfScope p(K_ROUTER_REDUCE, s);
-    router_reduce_kernel<<<ceil_div(c.n_experts, 256), 256, 0, s>>>(partials, grid, c.n_experts, prob_sum);
-  }
-  return cudaGetLastError();
+  ProfScope p(K_ROUTER_REDUCE, s);
+  return launch_pdl(router_reduce_kernel, dim3(ceil_div(c.n_experts, 256)), dim3(256), 0, s, 1,
+                    (const float*)partials, grid, c.n_experts, prob_sum);
 }
 
 }  // namespace moe

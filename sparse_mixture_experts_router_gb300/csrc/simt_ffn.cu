@@ -49,6 +49,8 @@ __device__ __forceinline__ int seg_of_row(const int32_t* seg, int E, int row) {
 
 __global__ void __launch_bounds__(64) simt_ffn_kernel(const FfnArgs a) {
   __shared__ float As[TM][TK + 1];
+  pdl_wait();
+  pdl_trigger();
   const int E = a.seg[0];
   const int32_t* rows_of = a.seg + 3 + E;
   const int32_t* a_row0 = a.seg + 3 + 2 * E;
@@ -169,10 +171,9 @@ cudaError_t launch_grouped_f32(const moe_config& c, const void* x_perm, const vo
   {
     dim3 grid(ceil_div(c.d_ff, TN), ceil_div(R, TM));
     ProfScope p(K_GATE_UP, s);
-    simt_ffn_kernel<<<grid, 64, 0, s>>>(a);
+    cudaError_t e = launch_pdl(simt_ffn_kernel, grid, dim3(64), 0, s, 1, a);
+    if (e != cudaSuccess) return e;
   }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   // Stage 2 reads H rows in output order: input row == output row.
   FfnArgs b = a;
   b.a_routed = static_cast<const float*>(h);
@@ -188,9 +189,8 @@ cudaError_t launch_grouped_f32(const moe_config& c, const void* x_perm, const vo
   {
     dim3 grid(ceil_div(c.d_model, TN), ceil_div(R, TM));
     ProfScope p(K_DOWN, s);
-    simt_ffn_kernel<<<grid, 64, 0, s>>>(b);
+    return launch_pdl(simt_ffn_kernel, grid, dim3(64), 0, s, 1, b);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace moe
