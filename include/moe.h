@@ -127,7 +127,9 @@ MOE_API size_t moe_workspace_size(const moe_config* cfg); /* moe_layer_forward *
  *             r verbatim (no GEMM; logit_bias must then be NULL).
  *  logits_out [device] [T][N] fp32 or NULL: receives r.
  *  topk_idx   [device] [T][k] int32 out: experts by descending key, equal
- *             keys ordered by lower index.
+ *             keys ordered by lower index. A NaN key ranks below every
+ *             number (as -inf), so the indices stay valid and distinct
+ *             whatever the scores hold.
  *  topk_w     [device] [T][k] fp32 out: gate weights (cfg->gate_mode).
  *  counts     [device] [N] int32 out: tokens routed to each expert.
  *  prob_sum   [device] [N] fp32 out: sum over tokens of softmax(r) over all
@@ -150,6 +152,8 @@ MOE_API int moe_router_topk(const moe_config* cfg, const void* x, const void* w_
  * operator only its inputs and outputs), so they can neither call
  * cudaMalloc nor hand over the scratch moe_router_topk takes.
  * Arguments and results are those of moe_router_topk without ws/ws_bytes.
+ * For bf16 with more than 32 experts the scores are computed on the tensor
+ * cores in 128-token tiles, which needs fewer partials than B below.
  * The scratch (a status word and per-block probability partials) lives in
  * a fixed 1 MiB array of the library's own device memory on every GPU that
  * loads the library, held until the process exits:

@@ -67,6 +67,7 @@ def _declare(lib):
     lib.oracle_balance_stats.argtypes = [_I, _I, _I, _P, _P, ctypes.c_double,
                                          _P, _P]
     lib.oracle_selection_margin.argtypes = [_I, _I, _I, _P, _P, _P]
+    lib.oracle_order_margin.argtypes = [_I, _I, _I, _P, _P, _P]
     return lib
 
 
@@ -229,6 +230,16 @@ class Oracle:
         sb = None if sel_bias is None else _c(sel_bias, np.float32)
         m = np.empty(T, np.float64)
         self.lib.oracle_selection_margin(T, N, k, _ptr(r64), _ptr(sb), _ptr(m))
+        return m
+
+    def order_margin(self, r64, k, sel_bias=None):
+        """Per-token smallest gap between neighbours among the k+1 largest
+        fp64 keys (all N keys when k = N)."""
+        r64 = _c(r64, np.float64)
+        T, N = r64.shape
+        sb = None if sel_bias is None else _c(sel_bias, np.float32)
+        m = np.empty(T, np.float64)
+        self.lib.oracle_order_margin(T, N, k, _ptr(r64), _ptr(sb), _ptr(m))
         return m
 
     def balance_loss(self, f, P, alpha=0.01):

@@ -358,3 +358,31 @@ void oracle_selection_margin(int T, int N, int k, const double* r64,
   }
   free(key);
 }
+
+/* Order margin of each token: the smallest gap between neighbours among the
+ * min(k + 1, N) largest fp64 keys, sorted (infinity when N = 1). It bounds
+ * both the selection margin and the gaps between kept experts, so inputs
+ * whose order margin is at least 1e-3 fix the top-k set and its order
+ * (topk_idx is sorted by key) against any fp32 rounding of the scores. */
+void oracle_order_margin(int T, int N, int k, const double* r64,
+                         const float* sel_bias, double* margin) {
+  double* key = (double*)malloc(sizeof(double) * (size_t)N);
+  const int m = k < N ? k + 1 : N;
+  for (int t = 0; t < T; ++t) {
+    for (int e = 0; e < N; ++e)
+      key[e] = r64[(size_t)t * N + e] + (sel_bias ? (double)sel_bias[e] : 0.0);
+    for (int s = 0; s < m; ++s) {
+      int best = s;
+      for (int i = s + 1; i < N; ++i)
+        if (key[i] > key[best]) best = i;
+      double tmp = key[s];
+      key[s] = key[best];
+      key[best] = tmp;
+    }
+    double g = INFINITY;
+    for (int s = 0; s + 1 < m; ++s)
+      if (key[s] - key[s + 1] < g) g = key[s] - key[s + 1];
+    margin[t] = g;
+  }
+  free(key);
+}

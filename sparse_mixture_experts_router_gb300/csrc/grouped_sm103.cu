@@ -46,6 +46,7 @@
 #include "device_util.cuh"
 #include "moe_internal.h"
 #include "sm103_ptx.cuh"
+#include "sm103_wait.cuh"
 
 namespace moe {
 namespace {
@@ -65,8 +66,6 @@ constexpr int THREADS = 192;
 constexpr int EPI_THREADS = 128;
 constexpr size_t DYN_SMEM = (size_t)STAGES * STAGE_BYTES + 1024;  // + 1 KB alignment slack
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
-constexpr uint64_t kDrainLimitNs = 50000000ull;    // 50 ms
 
 enum { EPI_SWIGLU = 0, EPI_DOWN = 1 };
 
@@ -118,30 +117,6 @@ __device__ __forceinline__ Tile decode_tile(const int32_t* __restrict__ seg, int
   const int mt = __ldg(mts + lo + 1) - m0;
   const int local = tile - m0 * NT;
   return Tile{lo, local % mt, local / mt};
-}
-
-// Bounded wait on one mbarrier phase. Returns false if the wait ran out (and
-// then records the timeout and raises the abort flag) or if another role
-// already aborted.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                           int* status) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      *abort_flag = 1;
-      set_status(status, MOE_ERR_TIMEOUT);
-      return false;
-    }
-  }
-}
-// Short bounded wait used only while draining after an abort.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!ptx::mbar_try_wait(bar, parity))
-    if (globaltimer_ns() - t0 > kDrainLimitNs) return;
 }
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
@@ -981,41 +956,6 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmArgs a, in
 }
 
 // ---------------------------------------------------------------- host side --
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-// Row-major bf16 matrix [rows][cols] read in boxes of box_rows rows x 64
-// columns with the 128-byte swizzle; out-of-range elements read as zero.
-bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols,
-              unsigned box_rows = 128u) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1u, 1u};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int num_sms() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);

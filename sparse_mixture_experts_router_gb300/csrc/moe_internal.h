@@ -1,6 +1,7 @@
 // Internal declarations shared by the CUDA translation units of libmoe.so.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -51,6 +52,14 @@ cudaError_t launch_router(const moe_config& c, const void* x, const void* w_rout
                           float* prob_sum, float* partials, int* status,
                           cudaStream_t s);
 size_t router_partials_bytes(const moe_config& c);
+// Tensor-core router (router_tc.cu): bf16, 32 < N <= 256, scores computed
+// (not given). Sets *fused_sum when its last block also sums prob_sum.
+bool router_tc_applies(const moe_config& c, const float* logits_in);
+cudaError_t launch_router_tc(const moe_config& c, const void* x, const void* w_router,
+                             const float* logit_bias, const float* sel_bias, float* logits_out,
+                             int32_t* topk_idx, float* topk_w, int32_t* counts, float* prob_sum,
+                             float* partials, int* status, bool* fused_sum, cudaStream_t s);
+int router_tc_grid(const moe_config& c);
 
 // With seg != null it also builds the grouped GEMM's segment table (tile
 // height tile_m) from the offsets it computes.
@@ -103,6 +112,11 @@ cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_
 cudaError_t launch_balance_stats(int N, int T, int k, const int32_t* counts,
                                  const float* prob_sum, float alpha, float* f, float* P,
                                  float* aux, cudaStream_t s);
+
+// 2-D TMA tensor map of a row-major bf16 matrix [rows][cols], boxes of
+// box_rows x 64 columns with the 128-byte swizzle (tma_maps.cu).
+bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols,
+              unsigned box_rows = 128u);
 
 // ---- profiling hooks (abi.cu) ----------------------------------------------
 enum KernelId {

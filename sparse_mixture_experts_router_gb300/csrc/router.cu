@@ -97,6 +97,7 @@ __device__ __forceinline__ void select_token(const float (&r)[EJ], int lane, lon
   for (int j = 0; j < EJ; ++j) {
     const int e = lane + 32 * j;
     key[j] = (e < N && a.sel_bias) ? __fadd_rn(r[j], a.sel_bias[e]) : r[j];
+    if (key[j] != key[j]) key[j] = -INFINITY;  // a NaN key ranks below every number
   }
   // Full softmax over the N unbiased scores (the affinity probabilities).
   float m = -FLT_MAX;
@@ -531,6 +532,15 @@ cudaError_t launch_router(const moe_config& c, const void* x, const void* w_rout
   a.logits_in = logits_in; a.logits_out = logits_out; a.topk_idx = topk_idx;
   a.topk_w = topk_w; a.counts = counts; a.partials = partials; a.status = status;
   a.T = c.T; a.d = c.d_model; a.N = c.n_experts; a.k = c.top_k; a.gate_mode = c.gate_mode;
+  if (router_tc_applies(c, logits_in)) {
+    bool fused = false;
+    e = launch_router_tc(c, x, w_router, logit_bias, sel_bias, logits_out, topk_idx, topk_w, counts,
+                         prob_sum, partials, status, &fused, s);
+    if (e != cudaSuccess || fused) return e;
+    ProfScope p(K_ROUTER_REDUCE, s);
+    return launch_pdl(router_reduce_kernel, dim3(ceil_div(c.n_experts, 256)), dim3(256), 0, s, 1,
+                      (const float*)partials, router_tc_grid(c), c.n_experts, prob_sum);
+  }
   const int grid = router_grid(c, logits_in);
   const bool fused_sum = grid <= kFusedSumMaxBlocks;
   a.prob_sum = prob_sum;

@@ -358,6 +358,38 @@ def pin_selection_margin_small(o):
     assert np.allclose(o.selection_margin(r, 2, sb), [0.5])
 
 
+def pin_order_margin_small(o):
+    """Worked by hand: keys [10, 0, 7, 6.9, 3] sort to 10, 7, 6.9, 3, 0 with
+    neighbour gaps 3, 0.1, 3.9, 3. The selection margin at k = 3 is 3.9, but
+    the kept experts 7 and 6.9 are only 0.1 apart."""
+    r = np.array([[10.0, 0.0, 7.0, 6.9, 3.0]])
+    assert np.allclose(o.order_margin(r, 1), [3.0])
+    for k in (2, 3, 4, 5):
+        assert np.allclose(o.order_margin(r, k), [0.1])
+    assert np.allclose(o.selection_margin(r, 3), [3.9])
+    sb = np.array([0.0, 0.0, 0.0, 0.0, 7.0], np.float32)   # 3 + 7 ties with 10
+    assert np.allclose(o.order_margin(r, 1, sb), [0.0])
+    assert np.isinf(o.order_margin(np.array([[1.5]]), 1)).all()
+
+
+def pin_order_margin_is_min_pairwise_distance(o):
+    """Brute force: the smallest neighbour gap of a sorted set is the
+    smallest distance over all pairs of the set; the set is the k+1 largest
+    keys (all N when k = N), found here with numpy's argsort."""
+    rng = _rng(12)
+    for T, N in ((40, 6), (30, 9)):
+        r = rng.normal(0, 1, (T, N))
+        sb = rng.uniform(-0.3, 0.3, N).astype(np.float32)
+        for k in range(1, N + 1):
+            got = o.order_margin(r, k, sb)
+            key = r + sb.astype(np.float64)
+            m = min(k + 1, N)
+            for t in range(T):
+                top = key[t][np.argsort(-key[t], kind="stable")[:m]]
+                best = min(abs(a - b) for i, a in enumerate(top) for b in top[i + 1:])
+                assert abs(got[t] - best) <= 1e-15, (T, N, k, t)
+
+
 def pin_balance_stats_sum_to_one(o):
     rng = _rng(11)
     T, N, k = 64, 8, 2

@@ -5,7 +5,7 @@ oracle, through the C ABI.
   indices and counts bit-exact, weights and probability sums within fp32
   rounding.
 * From x and W_r (the fused router GEMM): indices bit-exact on inputs with
-  a selection margin >= 1e-3; scores within fp32 accumulation error.
+  an order margin >= 1e-3; scores within fp32 accumulation error.
 """
 import numpy as np
 import pytest
@@ -13,7 +13,7 @@ import torch
 
 import sparse_mixture_experts_router_gb300 as moe
 from sparse_mixture_experts_router_gb300 import synth
-from gpu_common import cfg_of, host, margin_inputs, oracle_routing
+from gpu_common import GATE_TOL, SCORE_TOL, cfg_of, host, margin_inputs, oracle_routing
 
 pytestmark = pytest.mark.gpu
 
@@ -85,6 +85,16 @@ GEMM_CASES = [
                    sel_bias=True, seed=13),
     synth.Workload("r_zipf", T=257, d_model=1024, n_experts=128, top_k=8, d_ff=8, zipf_s=1.2, seed=14),
     synth.Workload("r_n40", T=65, d_model=136, n_experts=40, top_k=5, d_ff=8, dtype="f32", seed=15),
+    # bf16 with more than 32 experts: the tensor-core router. Ragged expert
+    # count, K not a multiple of the 64-wide K block, partial token tiles,
+    # one token, and more than 32 token tiles (block sums reduced separately).
+    synth.Workload("r_tc_n33", T=130, d_model=136, n_experts=33, top_k=3, d_ff=8, sel_bias=True,
+                   seed=16),
+    synth.Workload("r_tc_one_token", T=1, d_model=64, n_experts=129, top_k=8, d_ff=8, gate_mode=1,
+                   seed=17),
+    synth.Workload("r_tc_n200_many_tiles", T=4500, d_model=200, n_experts=200, top_k=6, d_ff=8,
+                   zipf_s=1.2, seed=18),
+    synth.DEEPSEEK_V3.replace(name="r_dsv3_full_size", d_ff=8),   # d_model = 7168
 ]
 
 
@@ -96,8 +106,34 @@ def test_router_gemm_routes_like_the_oracle(oracle, w):
     r64, idx, tw, counts, ps = oracle_routing(oracle, w, inp)
     assert np.array_equal(got["idx"].numpy(), idx)
     assert np.array_equal(got["counts"].numpy(), counts)
-    assert np.abs(got["logits"].numpy() - r64).max() <= 1e-4
-    assert np.abs(got["w"].numpy() - tw).max() <= 1e-5
+    assert np.abs(got["logits"].numpy() - r64).max() <= SCORE_TOL
+    assert np.abs(got["w"].numpy() - tw).max() <= GATE_TOL
+    assert np.allclose(got["prob_sum"].numpy(), ps, rtol=1e-4, atol=1e-4)
+
+
+@pytest.mark.parametrize("N,k,mode", [(64, 8, 1), (256, 8, 0), (48, 5, 0)])
+def test_router_gemm_breaks_exact_ties_by_index(oracle, N, k, mode):
+    """Small-integer x and W_r make every product and sum exact in fp32, so
+    the scores computed on the tensor cores equal the oracle's bit for bit
+    and tie often (many experts share a score); duplicated router rows and a
+    selection bias on a 1/4 grid add exact key ties. Selection must keep the
+    lower expert index on every tie, as the oracle does."""
+    T, d = 300, 256
+    g = torch.Generator().manual_seed(N * 31 + k)
+    x = torch.randint(-2, 3, (T, d), generator=g).to(torch.bfloat16)
+    base = torch.randint(-1, 2, (N // 4, d), generator=g)
+    W = base.repeat(4, 1)[torch.randperm(N, generator=g)].to(torch.bfloat16)
+    sb = (torch.randint(-2, 3, (N,), generator=g).float() * 0.25)
+    sb[::2] = 0.0
+    cfg = moe.config(T=T, d_model=d, n_experts=N, top_k=k, d_ff=8, dtype=moe.MOE_BF16,
+                     gate_mode=mode)
+    got = run_router(cfg, x.cuda(), W.cuda(), None, sb.cuda())
+    r64, r32 = oracle.router_logits(host(x), host(W), None)
+    assert np.array_equal(got["logits"].numpy(), r32)
+    idx, tw, counts, ps = oracle.route(r32, k, mode, sb.numpy())
+    assert np.array_equal(got["idx"].numpy(), idx)
+    assert np.array_equal(got["counts"].numpy(), counts)
+    assert np.abs(got["w"].numpy() - tw).max() <= 2e-6
     assert np.allclose(got["prob_sum"].numpy(), ps, rtol=1e-4, atol=1e-4)
 
 
@@ -127,3 +163,27 @@ def test_balance_stats_match_oracle(oracle):
     assert np.allclose(f.cpu().numpy(), fr, rtol=1e-6)
     assert np.allclose(P.cpu().numpy(), Pr, rtol=1e-4)
     assert abs(aux.item() - auxr) <= 1e-4 * auxr
+
+
+def test_nan_scores_keep_indices_valid(oracle):
+    """A NaN score ranks below every number: indices stay in range and
+    distinct, and tokens without NaN route exactly as the oracle does."""
+    T, N, k = 200, 64, 6
+    logits = synth.random_logits(T, N, seed=9, ties=False)
+    nan_rows = [3, 50, 51, 199]
+    logits[3, :] = float("nan")          # a token with no number at all
+    logits[50, ::2] = float("nan")
+    logits[51, 5] = float("nan")
+    logits[199, 60:] = float("nan")
+    cfg = moe.config(T=T, d_model=8, n_experts=N, top_k=k, d_ff=8)
+    got = run_router(cfg, logits_in=logits.cuda())
+    idx = got["idx"].numpy()
+    assert ((idx >= 0) & (idx < N)).all()
+    assert all(len(set(row)) == k for row in idx.tolist())
+    assert idx[3].tolist() == list(range(k))       # all -inf: lowest indices
+    assert not np.isnan(logits[50, idx[50]].numpy()).any()
+    ok = [t for t in range(T) if t not in nan_rows]
+    ref_idx, ref_w, _, _ = oracle.route(logits.numpy()[ok], k)
+    assert np.array_equal(idx[ok], ref_idx)
+    assert np.abs(got["w"].numpy()[ok] - ref_w).max() <= 2e-6
+    assert int(got["counts"].numpy().sum()) == T * k

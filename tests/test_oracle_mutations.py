@@ -33,6 +33,7 @@ MUTATIONS = [
     ("gated_sum_transposed", "acc += G[i] * E[(size_t)i * dim + c];", "acc += G[i] * E[(size_t)c * n_terms + i];"),
     ("prob_sum_from_gates", "for (int e = 0; e < N; ++e) prob_sum[e] += p[e];", "for (int s = 0; s < k; ++s) prob_sum[it[s]] += topk_w[(size_t)t * k + s];"),
     ("bf16_widen_wrong_half", "uint32_t u = (uint32_t)((const uint16_t*)base)[i] << 16;", "uint32_t u = (uint32_t)((const uint16_t*)base)[i];"),
+    ("order_margin_skips_last_gap", "for (int s = 0; s + 1 < m; ++s)", "for (int s = 0; s + 2 < m; ++s)"),
     ("selection_ignores_bias", "key[e] = sel_bias ? (float)((double)rt[e] + (double)sel_bias[e]) : rt[e];", "key[e] = rt[e];"),
 ]
 
