@@ -323,11 +323,15 @@ def run_ours(args):
     hb = {"router_topk": w.T * w.d_model * 2 + w.n_experts * w.d_model * 2 + P * 8,
           "permute_gather": 2 * P * w.d_model * 2 + P * 4,
           "combine": (P + w.n_shared * w.T) * w.d_model * 2 + w.T * w.d_model * 2 + P * 4}
-    if "router_topk" in per_kernel:  # fp32 FMA work of the router scores
+    if "router_topk" in per_kernel:  # the router's score contraction
         fl = 2.0 * w.T * w.n_experts * w.d_model
         tf = fl / (per_kernel["router_topk"]["ms_per_launch"] / 1e3) / 1e12
-        per_kernel["router_topk"]["fp32_tflops"] = round(tf, 2)
-        per_kernel["router_topk"]["fp32_alu_frac"] = round(tf / FP32_ALU_PEAK_TFLOPS, 4)
+        if w.dtype == "bf16" and w.n_experts > 32:  # tcgen05 router kernel
+            per_kernel["router_topk"]["tensor_tflops"] = round(tf, 2)
+            per_kernel["router_topk"]["tensor_frac"] = round(tf / pk["bf16"], 4)
+        else:  # CUDA-core FMA router kernels
+            per_kernel["router_topk"]["fp32_tflops"] = round(tf, 2)
+            per_kernel["router_topk"]["fp32_alu_frac"] = round(tf / FP32_ALU_PEAK_TFLOPS, 4)
     for name, b in hb.items():
         if name in per_kernel:
             gbs = b / (per_kernel[name]["ms_per_launch"] / 1e3) / 1e9
