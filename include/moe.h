@@ -153,12 +153,12 @@ MOE_API int moe_router_topk(const moe_config* cfg, const void* x, const void* w_
  * cudaMalloc nor hand over the scratch moe_router_topk takes.
  * Arguments and results are those of moe_router_topk without ws/ws_bytes.
  * For bf16 with more than 32 experts the scores are computed on the tensor
- * cores in 128-token tiles, which needs fewer partials than B below.
- * The scratch (a status word and per-block probability partials) lives in
+ * cores in 128-token tiles, which use half the partials B below allows for.
+ * The scratch (a status word and per-block probability sums and counts) lives in
  * a fixed 1 MiB array of the library's own device memory on every GPU that
  * loads the library, held until the process exits:
- *  - a call needs 256 + 4 * B * N bytes of it, B = ceil(T / 8) when N <= 32
- *    and ceil(T / 64) otherwise (for N = 256: T <= 65472); a larger call
+ *  - a call needs 256 + 8 * B * N bytes of it, B = ceil(T / 8) when N <= 32
+ *    and ceil(T / 64) otherwise (for N = 256: T <= 32704); a larger call
  *    returns MOE_ERR_WORKSPACE, launching nothing;
  *  - the first call made with a device current looks up the array's device
  *    address for that device; make that first call before any stream capture;
@@ -295,13 +295,16 @@ MOE_API int moe_balance_stats(int32_t n_experts, int32_t T, int32_t top_k,
  * MOE_ERR_DEVICE_CHECK), or MOE_ERR_CUDA if the stream reports an error. */
 MOE_API int moe_stream_status(const void* ws, moe_stream_t stream);
 
-/* Kernel-level profiling. While enabled, each kernel launch of this library
- * is bracketed by CUDA events recorded on the launching stream (events are
- * created by the library, host-side). moe_profile_collect synchronises on
- * the last event, writes up to `max_kernels` entries of per-kernel total
- * milliseconds and launch counts (names by moe_profile_kernel_name) and
- * clears the record; it returns the number of kernel kinds. */
-MOE_API void moe_profile_enable(int on);
+/* Kernel-level profiling. While enabled, each launch of the selected kernel
+ * kinds is bracketed by CUDA events recorded on the launching stream (events
+ * are created by the library, host-side). `mask` selects the kinds: bit i
+ * for kind i (named by moe_profile_kernel_name(i)), -1 for all, 0 turns
+ * profiling off. Events between launches cost the overlap of programmatic
+ * dependent launch at that boundary, so select only the kernels to time.
+ * moe_profile_collect synchronises on the last event, writes up to
+ * `max_kernels` entries of per-kernel total milliseconds and launch counts
+ * and clears the record; it returns the number of kernel kinds. */
+MOE_API void moe_profile_enable(int mask);
 MOE_API int moe_profile_collect(float* total_ms, int32_t* launches, int max_kernels);
 MOE_API const char* moe_profile_kernel_name(int id);
 

@@ -202,8 +202,29 @@ def moe_stream_status(ws, stream=None) -> int:
     return int(lib().moe_stream_status(_ptr(ws), _stream(stream)))
 
 
-def profile_enable(on: bool = True):
-    lib().moe_profile_enable(1 if on else 0)
+def profile_kernel_names() -> list:
+    out = []
+    for i in range(32):
+        name = lib().moe_profile_kernel_name(i).decode()
+        if not name:
+            break
+        out.append(name)
+    return out
+
+
+def profile_enable(on: bool = True, kernels=None):
+    """Bracket launches with CUDA events: every kernel kind, or only those
+    named in ``kernels`` (names as in profile_collect)."""
+    if not on:
+        mask = 0
+    elif kernels is None:
+        mask = -1
+    else:
+        names = profile_kernel_names()
+        mask = 0
+        for k in kernels:
+            mask |= 1 << names.index(k)
+    lib().moe_profile_enable(mask)
 
 
 def profile_collect() -> dict:

@@ -168,14 +168,14 @@ int grouped_impl(const moe_config& c, const void* x_perm, long long xp_rows, con
 }
 
 // ---- profiler ---------------------------------------------------------------
-const char* kKernelNames[K_NUM] = {"router_topk",   "router_reduce",  "permute_hist",
-                                   "permute_scan",  "permute_rank",   "permute_gather",
-                                   "permute_small", "seg_table",      "gate_up",
+const char* kKernelNames[K_NUM] = {"router_topk",   "permute_hist",   "permute_scan",
+                                   "permute_rank",  "permute_gather", "permute_small",
+                                   "permute_group", "seg_table",      "gate_up",
                                    "down",          "splitk_reduce",  "combine",
                                    "balance_stats"};
 struct Prof {
   std::mutex mu;
-  bool on = false;
+  uint32_t mask = 0;
   std::vector<cudaEvent_t> pool;
   std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> done;
   cudaEvent_t open[K_NUM] = {};
@@ -200,7 +200,7 @@ Prof& prof() {
 void prof_begin(int id, cudaStream_t s) {
   Prof& p = prof();
   std::lock_guard<std::mutex> g(p.mu);
-  if (!p.on) return;
+  if (!((p.mask >> id) & 1u)) return;
   cudaEvent_t e = p.get();
   cudaEventRecord(e, s);
   p.open[id] = e;
@@ -208,7 +208,7 @@ void prof_begin(int id, cudaStream_t s) {
 void prof_end(int id, cudaStream_t s) {
   Prof& p = prof();
   std::lock_guard<std::mutex> g(p.mu);
-  if (!p.on || !p.open[id]) return;
+  if (!((p.mask >> id) & 1u) || !p.open[id]) return;
   cudaEvent_t e = p.get();
   cudaEventRecord(e, s);
   p.done.push_back({id, {p.open[id], e}});
@@ -324,8 +324,8 @@ int moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
   PermuteWs w = carve_permute(cv, c);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
-  cudaError_t e = launch_permute(c, x, topk_idx, expert_offsets, sorted_pair, inv_pos, x_perm,
-                                 w.hist, w.status, nullptr, 0, s);
+  cudaError_t e = launch_permute(c, x, topk_idx, nullptr, expert_offsets, sorted_pair, inv_pos,
+                                 x_perm, w.hist, w.status, nullptr, 0, s);
   return e == cudaSuccess ? MOE_OK : fail_cuda(e);
 }
 
@@ -392,8 +392,8 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* w_router
                                 cnt, ps, w.partials, w.status, s);
   if (e != cudaSuccess) return fail_cuda(e);
   if (c.T == 0) return MOE_OK;
-  e = launch_permute(c, x, idx, w.offsets, w.sorted_pair, w.inv_pos, w.x_perm, w.hist, w.status,
-                     w.seg, seg_tile(c), s);
+  e = launch_permute(c, x, idx, cnt, w.offsets, w.sorted_pair, w.inv_pos, w.x_perm, w.hist,
+                     w.status, w.seg, seg_tile(c), s);
   if (e != cudaSuccess) return fail_cuda(e);
   rc = grouped_impl(c, w.x_perm, padded_rows(pairs(c)), x, w.offsets, w.sorted_pair, tw, w_gate,
                     w_up, w_down, w.y_perm, w.seg, true, w.h, w.partial, w.status, s);
@@ -426,10 +426,12 @@ int moe_stream_status(const void* ws, moe_stream_t stream) {
   return st;
 }
 
-void moe_profile_enable(int on) {
+void moe_profile_enable(int mask) {
   Prof& p = prof();
   std::lock_guard<std::mutex> g(p.mu);
-  p.on = on != 0;
+  p.mask = (uint32_t)mask;
+  for (int i = 0; i < K_NUM; ++i)  // a kind switched off mid-launch leaves no open event
+    if (!((p.mask >> i) & 1u)) p.open[i] = nullptr;
 }
 
 int moe_profile_collect(float* total_ms, int32_t* launches, int max_kernels) {

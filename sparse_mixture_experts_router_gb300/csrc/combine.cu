@@ -3,7 +3,7 @@
 // y[t] = sum_slot w * y_perm[inv_pos[t*k+slot]] + sum_shared y_perm[T*k+s*T+t]
 // ("Mixture of experts and speculative decoding", step 4 and the layer
 // equation; "Mixture of Experts and Guided Decoding", the three-expert gated
-// sum). One block per token; each output vector accumulates the k + n_shared
+// sum). One warp per token; each output vector accumulates the k + n_shared
 // rows' vectors in fp32 in a fixed order (slots, then shared experts) and is
 // written exactly once, so there are no atomics and the result is
 // reproducible.
@@ -43,60 +43,66 @@ struct Vec<__nv_bfloat16> {
   }
 };
 
-// One block per token: the token's k slot rows and weights are read once into
-// shared memory, then each thread sums whole 16-byte vectors of the output
-// row, loading all k + n_shared terms of a vector before adding them in fp32
-// in slot order then shared order, and stores once.
-template <typename TE>
+// WPT warps per token (1, 2 or 4, so that a lane sums about 8 vectors and
+// blocks stay short). Lane j of each of the token's warps fetches term j's
+// row and weight (slot j for j < k, shared expert j - k after them) and
+// shuffles them to the warp; each lane then sums whole 16-byte vectors of
+// the output row, loading all NT terms of a vector before adding them in
+// fp32 in term order (slots, then shared experts), and stores once. NT is
+// k + n_shared rounded up to a template size; terms past the token's own
+// count are skipped.
+constexpr int kWarpsPerBlock = kThreads / 32;
+template <typename TE, int NT, int UNROLL>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const TE* __restrict__ yp,
                                                            const int32_t* __restrict__ inv_pos,
                                                            const float* __restrict__ topk_w,
                                                            TE* __restrict__ y, int T, int d, int k,
-                                                           int n_shared) {
+                                                           int n_shared, int wpt) {
   constexpr int V = Vec<TE>::n;
-  constexpr int TERMS = kMaxTopK + kMaxShared;
-  __shared__ long long s_row[TERMS];
-  __shared__ float s_w[TERMS];
-  const int t = blockIdx.x;
+  const int lane = threadIdx.x % 32;
+  const int warp = threadIdx.x / 32;
+  const long long t = (long long)blockIdx.x * (kWarpsPerBlock / wpt) + warp / wpt;
+  const int part = warp % wpt;
   const long long P = (long long)T * k;
   pdl_wait();
   pdl_trigger();
-  if (threadIdx.x < TERMS) {
-    const int j = threadIdx.x;
-    long long row = -1;
-    float w = 1.0f;
-    if (j < kMaxTopK) {
-      if (j < k) {
-        const int pos = inv_pos[(size_t)t * k + j];
-        if (pos >= 0 && pos < P) row = pos;  // out of range: contributes zero
-        if (topk_w) w = topk_w[(size_t)t * k + j];
-      }
-    } else if (j - kMaxTopK < n_shared) {
-      row = P + (long long)(j - kMaxTopK) * T + t;
-    }
-    s_row[j] = row;
-    s_w[j] = w;
+  if (t >= T) return;
+  long long my_row = -1;
+  float my_w = 1.0f;
+  if (lane < k) {
+    const int pos = inv_pos[t * k + lane];
+    if (pos >= 0 && pos < P) my_row = pos;  // out of range: contributes zero
+    if (topk_w) my_w = topk_w[t * k + lane];
+  } else if (lane < k + n_shared) {
+    my_row = P + (long long)(lane - k) * T + t;
   }
-  __syncthreads();
-  const int nvec = d / V;
-  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-    uint4 raw[TERMS];
+  const uint4* src[NT];
+  float w[NT];
 #pragma unroll
-    for (int j = 0; j < TERMS; ++j)
-      raw[j] = s_row[j] >= 0 ? __ldg(reinterpret_cast<const uint4*>(yp + s_row[j] * d) + v)
-                             : make_uint4(0, 0, 0, 0);
+  for (int j = 0; j < NT; ++j) {
+    const long long r = __shfl_sync(0xffffffffu, my_row, j);
+    w[j] = __shfl_sync(0xffffffffu, my_w, j);
+    src[j] = r >= 0 ? reinterpret_cast<const uint4*>(yp + r * d) : nullptr;
+  }
+  const int nvec = d / V;
+  uint4* dst = reinterpret_cast<uint4*>(y + t * d);
+#pragma unroll UNROLL
+  for (int v = part * 32 + lane; v < nvec; v += 32 * wpt) {
+    uint4 raw[NT];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) raw[j] = src[j] ? __ldg(src[j] + v) : make_uint4(0, 0, 0, 0);
     float acc[V];
 #pragma unroll
     for (int q = 0; q < V; ++q) acc[q] = 0.f;
 #pragma unroll
-    for (int j = 0; j < TERMS; ++j) {
-      if (s_row[j] < 0) continue;
+    for (int j = 0; j < NT; ++j) {
+      if (!src[j]) continue;
       float val[V];
       Vec<TE>::unpack(raw[j], val);
 #pragma unroll
-      for (int q = 0; q < V; ++q) acc[q] = fmaf(s_w[j], val[q], acc[q]);
+      for (int q = 0; q < V; ++q) acc[q] = fmaf(w[j], val[q], acc[q]);
     }
-    Vec<TE>::store(y + (size_t)t * d + (size_t)v * V, acc);
+    Vec<TE>::store(reinterpret_cast<TE*>(dst + v), acc);
   }
 }
 
@@ -122,21 +128,35 @@ __global__ void balance_stats_kernel(const int32_t* counts, const float* prob_su
 
 }  // namespace
 
+template <typename TE, int NT, int UNROLL>
+cudaError_t launch_combine_t(const moe_config& c, const void* y_perm, const int32_t* inv_pos,
+                             const float* topk_w, void* y, cudaStream_t s) {
+  const int nvec = c.d_model / Vec<TE>::n;
+  int wpt = 1;
+  while (wpt < 4 && nvec > 32 * 8 * wpt) wpt *= 2;
+  return launch_pdl(combine_kernel<TE, NT, UNROLL>, dim3(ceil_div(c.T, kWarpsPerBlock / wpt)),
+                    dim3(kThreads), 0, s, 1, static_cast<const TE*>(y_perm), inv_pos, topk_w,
+                    static_cast<TE*>(y), c.T, c.d_model, c.top_k, c.n_shared, wpt);
+}
+
+template <typename TE>
+cudaError_t launch_combine_dt(const moe_config& c, const void* y_perm, const int32_t* inv_pos,
+                              const float* topk_w, void* y, cudaStream_t s) {
+  const int terms = c.top_k + c.n_shared;
+  if (terms <= 2) return launch_combine_t<TE, 2, 4>(c, y_perm, inv_pos, topk_w, y, s);
+  if (terms <= 4) return launch_combine_t<TE, 4, 2>(c, y_perm, inv_pos, topk_w, y, s);
+  if (terms <= 8) return launch_combine_t<TE, 8, 1>(c, y_perm, inv_pos, topk_w, y, s);
+  if (terms == 9) return launch_combine_t<TE, 9, 1>(c, y_perm, inv_pos, topk_w, y, s);
+  return launch_combine_t<TE, kMaxTopK + kMaxShared, 1>(c, y_perm, inv_pos, topk_w, y, s);
+}
+
 cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_t* inv_pos,
                            const float* topk_w, void* y, cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
-  // one block per token, at most one thread per 16-byte vector of the row
-  const int nvec = c.d_model / (c.dtype == MOE_BF16 ? 8 : 4);
-  const int threads = nvec >= kThreads ? kThreads : ((nvec + 31) / 32) * 32;
-  const int grid = c.T;
   ProfScope p(K_COMBINE, s);
   if (c.dtype == MOE_BF16)
-    return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(grid), dim3(threads), 0, s, 1,
-                      static_cast<const __nv_bfloat16*>(y_perm), inv_pos, topk_w,
-                      static_cast<__nv_bfloat16*>(y), c.T, c.d_model, c.top_k, c.n_shared);
-  return launch_pdl(combine_kernel<float>, dim3(grid), dim3(threads), 0, s, 1,
-                    static_cast<const float*>(y_perm), inv_pos, topk_w, static_cast<float*>(y),
-                    c.T, c.d_model, c.top_k, c.n_shared);
+    return launch_combine_dt<__nv_bfloat16>(c, y_perm, inv_pos, topk_w, y, s);
+  return launch_combine_dt<float>(c, y_perm, inv_pos, topk_w, y, s);
 }
 
 cudaError_t launch_balance_stats(int N, int T, int k, const int32_t* counts, const float* prob_sum,

@@ -53,20 +53,23 @@ cudaError_t launch_router(const moe_config& c, const void* x, const void* w_rout
                           cudaStream_t s);
 size_t router_partials_bytes(const moe_config& c);
 // Tensor-core router (router_tc.cu): bf16, 32 < N <= 256, scores computed
-// (not given). Sets *fused_sum when its last block also sums prob_sum.
+// (not given). Its grid never exceeds router_partial_blocks(c).
 bool router_tc_applies(const moe_config& c, const float* logits_in);
 cudaError_t launch_router_tc(const moe_config& c, const void* x, const void* w_router,
                              const float* logit_bias, const float* sel_bias, float* logits_out,
                              int32_t* topk_idx, float* topk_w, int32_t* counts, float* prob_sum,
-                             float* partials, int* status, bool* fused_sum, cudaStream_t s);
-int router_tc_grid(const moe_config& c);
+                             float* partials, int32_t* cpart, int* status, cudaStream_t s);
+// Blocks the router's per-block partials are sized for.
+int router_partial_blocks(const moe_config& c);
 
 // With seg != null it also builds the grouped GEMM's segment table (tile
-// height tile_m) from the offsets it computes.
+// height tile_m) from the offsets it computes. `counts` (pairs per expert,
+// as the router left them) may be null; when given, mid-sized batches take
+// their offsets from it instead of counting the pairs again.
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
-                           int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos,
-                           void* x_perm, int32_t* chunk_hist, int* status, int32_t* seg,
-                           int tile_m, cudaStream_t s);
+                           const int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
+                           int32_t* inv_pos, void* x_perm, int32_t* chunk_hist, int* status,
+                           int32_t* seg, int tile_m, cudaStream_t s);
 size_t permute_scratch_bytes(const moe_config& c);
 
 cudaError_t launch_seg_table(const moe_config& c, const int32_t* offsets, int32_t* seg,
@@ -121,12 +124,12 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols,
 // ---- profiling hooks (abi.cu) ----------------------------------------------
 enum KernelId {
   K_ROUTER = 0,
-  K_ROUTER_REDUCE,
   K_PERMUTE_HIST,
   K_PERMUTE_SCAN,
   K_PERMUTE_RANK,
   K_PERMUTE_GATHER,
   K_PERMUTE_SMALL,
+  K_PERMUTE_GROUP,
   K_SEG_TABLE,
   K_GATE_UP,
   K_DOWN,

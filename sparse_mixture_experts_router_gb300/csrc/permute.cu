@@ -6,19 +6,29 @@
 // every pair that chose expert e lands in e's contiguous row segment, in
 // ascending pair order, so the result is unique and bit-exact.
 //
-// Four launches (one single-block kernel when all pairs fit one chunk):
-//  hist   - one block per chunk of 2048 pairs counts pairs per expert with
-//           warp-aggregated shared-memory atomics (one atomic per distinct
-//           expert in a warp, found with __match_any_sync).
-//  scan   - one block: per expert, exclusive scan of the chunk counts; then
-//           the exclusive scan over experts gives expert_offsets; the chunk
-//           table becomes each chunk's first row per expert.
-//  rank   - one block per chunk: per-warp counts, a scan over the 8 warps,
-//           then each warp walks its 256 pairs in order, 32 at a time; a
-//           pair's row is its warp base + the number of lower lanes with the
-//           same expert (__match_any_sync + popc of the lane mask).
-//  gather - one warp per output row copies the token row with 16-byte loads
-//           and stores.
+// Launch shapes, by the number of pairs P = T*k:
+//  P <= 2048          - one block does everything but the row gather
+//                       (permute_small_kernel), then the gather.
+//  P <= 65536         - one launch per expert group (permute_group_kernel),
+//                       then the gather: each block owns a group of experts,
+//                       takes the per-expert totals (the router's counts, or
+//                       its own histogram), scans them into offsets, and
+//                       ranks its experts' pairs in two ordered passes.
+//  larger             - four launches:
+//    hist   - one block per chunk of 2048 pairs counts pairs per expert with
+//             warp-aggregated shared-memory atomics (one atomic per distinct
+//             expert in a warp, found with __match_any_sync).
+//    scan   - one block: per expert, exclusive scan of the chunk counts; then
+//             the exclusive scan over experts gives expert_offsets; the chunk
+//             table becomes each chunk's first row per expert.
+//    rank   - one block per chunk: per-warp counts, a scan over the 8 warps,
+//             then each warp walks its 256 pairs in order, 32 at a time; a
+//             pair's row is its warp base + the number of lower lanes with
+//             the same expert (__match_any_sync + popc of the lane mask).
+//  gather     - one warp per output row copies the token row with 16-byte
+//               loads and stores.
+// The segment table of the grouped GEMM comes with the first two shapes and
+// from seg_table_kernel after the third.
 #include "device_util.cuh"
 #include "moe_internal.h"
 
@@ -30,6 +40,55 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = kPermuteChunk;            // 2048 pairs
 constexpr int kPerWarp = kChunk / kWarps;        // 256 pairs
 constexpr int kRounds = kPerWarp / 32;           // 8
+
+// Exclusive scan of v[0..n) in place by one warp (32 at a time, carrying the
+// running total); returns the total to every lane.
+__device__ __forceinline__ int warp_exclusive_scan(int* v, int n, int lane) {
+  int run = 0;
+  for (int b = 0; b < n; b += 32) {
+    const int x = (b + lane < n) ? v[b + lane] : 0;
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (b + lane < n) v[b + lane] = run + incl - x;
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return run;
+}
+
+// Segment table of the grouped GEMM, [E, total tiles, mt_start[E+1],
+// rows[E], a_row0[E], out_row0[E]], from the routed experts' offsets
+// off[0..N] (shared experts take T rows of x each). Called by a whole block;
+// `scratch` holds E + 1 ints of shared memory.
+__device__ void write_seg_table(const int* off, int N, int n_shared, int T, int P, int tile_m,
+                                int32_t* seg, int* scratch) {
+  const int E = N + n_shared;
+  int32_t* mt_start = seg + 2;
+  int32_t* rows = seg + 3 + E;
+  int32_t* a_row0 = seg + 3 + 2 * E;
+  int32_t* out_row0 = seg + 3 + 3 * E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int r = e < N ? off[e + 1] - off[e] : T;
+    rows[e] = r;
+    a_row0[e] = e < N ? off[e] : 0;
+    out_row0[e] = e < N ? off[e] : P + (e - N) * T;
+    scratch[e] = (r + tile_m - 1) / tile_m;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int total = warp_exclusive_scan(scratch, E, threadIdx.x);
+    if (threadIdx.x == 0) {
+      scratch[E] = total;
+      seg[0] = E;
+      seg[1] = total;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) mt_start[e] = scratch[e];
+}
 
 __global__ void __launch_bounds__(kThreads) permute_hist_kernel(const int32_t* __restrict__ idx,
                                                                 int P, int N, int32_t* hist,
@@ -205,18 +264,12 @@ __global__ void __launch_bounds__(kSmallThreads) permute_small_kernel(
     soff[e] = tot;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int e = 0; e < N; ++e) {
-      const int v = soff[e];
-      soff[e] = run;
-      offsets[e] = run;
-      run += v;
-    }
-    soff[N] = run;
-    offsets[N] = run;
+  if (warp == 0) {
+    const int total = warp_exclusive_scan(soff, N, lane);
+    if (lane == 0) soff[N] = total;
   }
   __syncthreads();
+  for (int e = threadIdx.x; e <= N; e += kSmallThreads) offsets[e] = soff[e];
   for (int e = threadIdx.x; e < N; e += kSmallThreads) {
     int base = soff[e];
     for (int w = 0; w < kSmallWarps; ++w) {
@@ -241,27 +294,128 @@ __global__ void __launch_bounds__(kSmallThreads) permute_small_kernel(
     if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
     __syncwarp();
   }
-  if (seg != nullptr) {  // segment table of the grouped GEMM (as seg_table_kernel)
-    const int E = N + n_shared;
-    int32_t* mt_start = seg + 2;
-    int32_t* rows = seg + 3 + E;
-    int32_t* a_row0 = seg + 3 + 2 * E;
-    int32_t* out_row0 = seg + 3 + 3 * E;
-    for (int e = threadIdx.x; e < E; e += kSmallThreads) {
-      rows[e] = e < N ? soff[e + 1] - soff[e] : T;
-      a_row0[e] = e < N ? soff[e] : 0;
-      out_row0[e] = e < N ? soff[e] : P + (e - N) * T;
-    }
-    if (threadIdx.x == 0) {
-      int run = 0;
-      for (int e = 0; e < E; ++e) {
-        mt_start[e] = run;
-        const int r = e < N ? soff[e + 1] - soff[e] : T;
-        run += (r + tile_m - 1) / tile_m;
+  if (seg != nullptr) {  // segment table of the grouped GEMM
+    __syncthreads();
+    write_seg_table(soff, N, n_shared, T, P, tile_m, seg, wh);  // wh is free again
+  }
+}
+
+// Mid-sized batches: block g owns experts [g*epb, min(N, (g+1)*epb)).
+// Every block forms all N offsets (from `counts` when given, else from its
+// own histogram of the pairs) so no block waits for another; block 0 writes
+// expert_offsets and the segment table. Each of the 32 warps covers one
+// contiguous range of pairs: a first pass counts the block's experts per
+// warp, a scan over the warps turns the counts into row bases, and a second
+// pass assigns rows in pair order (lower lanes with the same expert first).
+constexpr int kGroupThreads = 1024;
+constexpr int kGroupWarps = kGroupThreads / 32;
+constexpr int kGroupMaxPairs = 1 << 16;  // above this the chunked path is faster
+constexpr int kGroupBlocks = 16;
+constexpr int kGroupBatch = 8;  // rounds of 32 pairs loaded ahead
+__global__ void __launch_bounds__(kGroupThreads) permute_group_kernel(
+    const int32_t* __restrict__ idx, const int32_t* __restrict__ counts, int P, int N, int epb,
+    int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos, int* status, int32_t* seg,
+    int n_shared, int T, int tile_m) {
+  extern __shared__ int sh[];
+  int* s_off = sh;                      // [N + 1] totals, then offsets
+  int* s_wc = sh + N + 1;               // [kGroupWarps][epb] counts, then row bases
+  int* s_seg = s_wc + kGroupWarps * epb;  // [N + n_shared + 1] (block 0)
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int e_lo = blockIdx.x * epb, e_hi = min(N, e_lo + epb);
+  pdl_wait();
+  pdl_trigger();
+  for (int e = threadIdx.x; e < N; e += kGroupThreads) s_off[e] = counts ? counts[e] : 0;
+  for (int i = threadIdx.x; i < kGroupWarps * epb; i += kGroupThreads) s_wc[i] = 0;
+  __syncthreads();
+  const int per_warp = ((P + kGroupWarps - 1) / kGroupWarps + 31) / 32 * 32;
+  const int p0 = warp * per_warp, p1 = min(P, p0 + per_warp);
+  // The passes below walk the warp's range kGroupBatch rounds at a time,
+  // loading a batch's expert indices before using any of them.
+  if (counts == nullptr) {
+    for (int b0 = p0; b0 < p1; b0 += 32 * kGroupBatch) {
+      int ev[kGroupBatch];
+#pragma unroll
+      for (int r = 0; r < kGroupBatch; ++r) {
+        const int p = b0 + 32 * r + lane;
+        ev[r] = p < p1 ? idx[p] : -1;
       }
-      mt_start[E] = run;
-      seg[0] = E;
-      seg[1] = run;
+#pragma unroll
+      for (int r = 0; r < kGroupBatch; ++r) {
+        const int p = b0 + 32 * r + lane;
+        int e = ev[r];
+        if (p < p1 && (e < 0 || e >= N)) {
+          set_status(status, MOE_ERR_DEVICE_CHECK);
+          e = -1;
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_off[e], __popc(peers));
+      }
+    }
+    __syncthreads();
+  }
+  if (warp == 0) {
+    const int total = warp_exclusive_scan(s_off, N, lane);
+    if (lane == 0) {
+      s_off[N] = total;
+      if (counts != nullptr && total != P) set_status(status, MOE_ERR_DEVICE_CHECK);
+    }
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e <= N; e += kGroupThreads) offsets[e] = s_off[e];
+    if (seg != nullptr) write_seg_table(s_off, N, n_shared, T, P, tile_m, seg, s_seg);
+  }
+  // pass 1: per-warp counts of this block's experts
+  int* mine = s_wc + warp * epb;  // mine[e - e_lo] for e in [e_lo, e_hi)
+  for (int b0 = p0; b0 < p1; b0 += 32 * kGroupBatch) {
+    int ev[kGroupBatch];
+#pragma unroll
+    for (int r = 0; r < kGroupBatch; ++r) {
+      const int p = b0 + 32 * r + lane;
+      ev[r] = p < p1 ? idx[p] : -1;
+    }
+#pragma unroll
+    for (int r = 0; r < kGroupBatch; ++r) {
+      const int e = ev[r];
+      const bool own = e >= e_lo && e < e_hi;
+      const uint32_t peers = __match_any_sync(0xffffffffu, own ? e : -1);
+      if (own && lane == __ffs(peers) - 1) mine[e - e_lo] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < e_hi - e_lo; j += kGroupThreads) {
+    int acc = s_off[e_lo + j];
+    for (int w = 0; w < kGroupWarps; ++w) {
+      const int v = s_wc[w * epb + j];
+      s_wc[w * epb + j] = acc;
+      acc += v;
+    }
+  }
+  __syncthreads();
+  // pass 2: rows in pair order
+  const uint32_t lt = lanemask_lt();
+  for (int b0 = p0; b0 < p1; b0 += 32 * kGroupBatch) {
+    int ev[kGroupBatch];
+#pragma unroll
+    for (int r = 0; r < kGroupBatch; ++r) {
+      const int p = b0 + 32 * r + lane;
+      ev[r] = p < p1 ? idx[p] : -1;
+    }
+#pragma unroll
+    for (int r = 0; r < kGroupBatch; ++r) {
+      const int p = b0 + 32 * r + lane;
+      const int e = ev[r];
+      const bool own = e >= e_lo && e < e_hi;
+      const uint32_t peers = __match_any_sync(0xffffffffu, own ? e : -1);
+      if (own) {
+        const int pos = mine[e - e_lo] + __popc(peers & lt);
+        sorted_pair[pos] = p;
+        inv_pos[p] = pos;
+      }
+      __syncwarp();
+      if (own && lane == __ffs(peers) - 1) mine[e - e_lo] += __popc(peers);
+      __syncwarp();
     }
   }
 }
@@ -271,45 +425,31 @@ __global__ void __launch_bounds__(kSmallThreads) permute_small_kernel(
 // own, so they are checked first: they must start at 0, never decrease and
 // end at most at T*k. Otherwise the status word gets MOE_ERR_DEVICE_CHECK
 // and the table holds zero tiles, so the GEMMs do no work.
-__global__ void seg_table_kernel(const int32_t* __restrict__ offsets, int N, int n_shared, int T,
-                                 int P, int tile_m, int32_t* seg, int* status) {
-  __shared__ int ok;
-  const int E = N + n_shared;
+constexpr int kSegThreads = 256;
+__global__ void __launch_bounds__(kSegThreads) seg_table_kernel(
+    const int32_t* __restrict__ offsets, int N, int n_shared, int T, int P, int tile_m,
+    int32_t* seg, int* status) {
+  extern __shared__ int sh[];
+  int* off = sh;             // [N + 1]
+  int* scratch = sh + N + 1; // [N + n_shared + 1]
   pdl_wait();
   pdl_trigger();
-  int32_t* mt_start = seg + 2;
-  int32_t* rows = seg + 3 + E;
-  int32_t* a_row0 = seg + 3 + 2 * E;
-  int32_t* out_row0 = seg + 3 + 3 * E;
-  if (threadIdx.x == 0) {
-    int good = offsets[0] == 0 && offsets[N] <= P;
-    for (int e = 0; e < N && good; ++e) good = offsets[e + 1] >= offsets[e];
-    ok = good;
-    if (!good) set_status(status, MOE_ERR_DEVICE_CHECK);
+  int good = 1;
+  for (int e = threadIdx.x; e <= N; e += kSegThreads) {
+    off[e] = offsets[e];
+    if (e == 0 && off[0] != 0) good = 0;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    if (e < N) {
-      rows[e] = ok ? offsets[e + 1] - offsets[e] : 0;
-      a_row0[e] = ok ? offsets[e] : 0;
-      out_row0[e] = ok ? offsets[e] : 0;
-    } else {
-      rows[e] = ok ? T : 0;
-      a_row0[e] = 0;
-      out_row0[e] = P + (e - N) * T;
-    }
+  for (int e = threadIdx.x; e < N; e += kSegThreads)
+    if (off[e + 1] < off[e]) good = 0;
+  if (threadIdx.x == 0 && off[N] > P) good = 0;
+  const bool ok = __syncthreads_and(good) != 0;
+  if (!ok) {
+    if (threadIdx.x == 0) set_status(status, MOE_ERR_DEVICE_CHECK);
+    for (int e = threadIdx.x; e <= N; e += kSegThreads) off[e] = 0;  // no routed rows
+    __syncthreads();
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int e = 0; e < E; ++e) {
-      mt_start[e] = run;
-      run += (rows[e] + tile_m - 1) / tile_m;
-    }
-    mt_start[E] = run;
-    seg[0] = E;
-    seg[1] = run;
-  }
+  write_seg_table(off, N, n_shared, ok ? T : 0, P, tile_m, seg, scratch);
 }
 
 }  // namespace
@@ -320,9 +460,9 @@ size_t permute_scratch_bytes(const moe_config& c) {
 }
 
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
-                           int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos,
-                           void* x_perm, int32_t* chunk_hist, int* status, int32_t* seg,
-                           int tile_m, cudaStream_t s) {
+                           const int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
+                           int32_t* inv_pos, void* x_perm, int32_t* chunk_hist, int* status,
+                           int32_t* seg, int tile_m, cudaStream_t s) {
   const int N = c.n_experts;
   const int P = c.T * c.top_k;
   if (P == 0) return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (N + 1), s);
@@ -340,6 +480,24 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
     ProfScope p(K_PERMUTE_GATHER, s);
     return launch_pdl(permute_gather_kernel, dim3(ceil_div(P, kWarps)), dim3(kThreads), 0, s, 1,
                       static_cast<const uint4*>(x), sorted_pair, P, c.top_k, vec,
+                      static_cast<uint4*>(x_perm));
+  }
+  const int vec = (int)(c.d_model * elem_bytes(c.dtype) / 16);
+  if (P <= kGroupMaxPairs) {
+    const int groups = N < kGroupBlocks ? N : kGroupBlocks;
+    const int epb = ceil_div(N, groups);
+    const size_t smem =
+        sizeof(int) * ((size_t)N + 1 + (size_t)kGroupWarps * epb + N + c.n_shared + 1);
+    {
+      ProfScope p(K_PERMUTE_GROUP, s);
+      cudaError_t e = launch_pdl(permute_group_kernel, dim3(ceil_div(N, epb)), dim3(kGroupThreads),
+                                 smem, s, 1, topk_idx, counts, P, N, epb, offsets, sorted_pair,
+                                 inv_pos, status, seg, c.n_shared, c.T, tile_m);
+      if (e != cudaSuccess) return e;
+    }
+    ProfScope p(K_PERMUTE_GATHER, s);
+    return launch_pdl(permute_gather_kernel, dim3(ceil_div(P, kWarps)), dim3(kThreads), 0, s, 1,
+                      static_cast<const uint4*>(x), (const int32_t*)sorted_pair, P, c.top_k, vec,
                       static_cast<uint4*>(x_perm));
   }
   const int nch = ceil_div(P, kChunk);
@@ -363,7 +521,6 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
     if (e != cudaSuccess) return e;
   }
   {
-    const int vec = (int)(c.d_model * elem_bytes(c.dtype) / 16);
     ProfScope p(K_PERMUTE_GATHER, s);
     e = launch_pdl(permute_gather_kernel, dim3(ceil_div(P, kWarps)), dim3(kThreads), 0, s, 1,
                    static_cast<const uint4*>(x), (const int32_t*)sorted_pair, P, c.top_k, vec,
@@ -376,8 +533,9 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
 cudaError_t launch_seg_table(const moe_config& c, const int32_t* offsets, int32_t* seg,
                              int tile_m, int* status, cudaStream_t s) {
   ProfScope p(K_SEG_TABLE, s);
-  return launch_pdl(seg_table_kernel, dim3(1), dim3(256), 0, s, 1, offsets, c.n_experts, c.n_shared,
-                    c.T, c.T * c.top_k, tile_m, seg, status);
+  const size_t smem = sizeof(int) * ((size_t)2 * c.n_experts + c.n_shared + 2);
+  return launch_pdl(seg_table_kernel, dim3(1), dim3(kSegThreads), smem, s, 1, offsets, c.n_experts,
+                    c.n_shared, c.T, c.T * c.top_k, tile_m, seg, status);
 }
 
 }  // namespace moe

@@ -29,6 +29,7 @@
 
 #include "device_util.cuh"
 #include "moe_internal.h"
+#include "router_finish.cuh"
 
 namespace moe {
 namespace {
@@ -37,8 +38,8 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTileTokens = 64;              // tokens per block, tiled kernel
 constexpr int kKC = 32;                      // K slice of the tiled kernel
-constexpr int kFusedSumMaxBlocks = 32;       // up to this grid the last block sums prob_sum
-constexpr int kSmallTokensPerBlock = 8;      // few-expert kernel: one token group a block
+constexpr int kSmallTokensPerBlock = 8;      // few-expert kernel: partials sized for T/8 blocks
+constexpr int kSmallMaxBlocks = 4 * 152;     // few-expert kernel: grid-stride beyond this
 
 struct RouterArgs {
   const void* x;
@@ -50,10 +51,11 @@ struct RouterArgs {
   int32_t* topk_idx;
   float* topk_w;
   int32_t* counts;
-  float* partials;  // [gridDim.x][N]
+  float* partials;  // [gridDim.x][N] probability sums of each block
+  int32_t* cpart;   // [gridDim.x][N] counts of each block
   int* status;
-  // When set (small grids), the last block to finish sums the partials into
-  // prob_sum itself; `done` counts finished blocks and is zero at launch.
+  // The last block to finish sums the partials into prob_sum and counts;
+  // `done` counts finished blocks and is zero at launch.
   float* prob_sum;
   int* done;
   int T, d, N, k, gate_mode;
@@ -177,7 +179,8 @@ __device__ __forceinline__ void select_token(const float (&r)[EJ], int lane, lon
   }
 }
 
-// Per-block probability partial (warps summed in order) and counts.
+// Per-block probability partial (warps summed in order) and counts, then the
+// last block's fixed-order total.
 template <int EJ>
 __device__ __forceinline__ void finish_block(const float (&psum)[EJ], float* wprob, int* bcount,
                                              const RouterArgs& a) {
@@ -190,110 +193,111 @@ __device__ __forceinline__ void finish_block(const float (&psum)[EJ], float* wpr
     float s = 0.f;
     for (int w = 0; w < kWarps; ++w) s += wprob[w * NP + e];
     a.partials[(size_t)blockIdx.x * a.N + e] = s;
-    if (bcount[e]) atomicAdd(&a.counts[e], bcount[e]);
+    a.cpart[(size_t)blockIdx.x * a.N + e] = bcount[e];
   }
-  if (a.done == nullptr) return;
-  // Last block: prob_sum[e] = sum over blocks in block order (same order as
-  // router_reduce_kernel).
-  __shared__ int last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(a.done, 1) == (int)gridDim.x - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  for (int e = threadIdx.x; e < a.N; e += kThreads) {
-    float s = 0.f;
-    for (int b = 0; b < (int)gridDim.x; ++b) s += __ldcg(a.partials + (size_t)b * a.N + e);
-    a.prob_sum[e] = s;
-  }
+  router_finish<kThreads>(a.partials, a.cpart, a.N, a.prob_sum, a.counts, a.done);
 }
 
 // ---------------------------------------------------------------------------
-// Few experts (N <= 32): a block scores TB tokens at a time; each of its 8
-// warps covers 1/8 of d_model for all TB tokens and all N experts (x and
-// W_r read once per token group with 16-byte loads; W_r comes from L2). A
-// lane accumulates TB*NP = 64 partial dot products; a 5-step butterfly
-// reduce-scatter leaves each lane 2 of them summed over the warp, the 8
-// warps' sums are added in warp order through shared memory, and warp q
-// then selects for token q of the group.
-template <typename TX, int NP, int TB>
-__global__ void __launch_bounds__(kThreads) router_small_kernel(const RouterArgs a) {
+// Few experts (N <= 32): each warp scores TPW tokens at a time over all of
+// d_model (grid-stride over token groups, no block barrier inside the loop).
+// A lane takes every 32nd 16-byte vector of the tokens' rows and keeps
+// NV = NP*TPW partial dot products (NP = N rounded up to 8, 16 or 32); x
+// vectors are loaded 32/NP per token at a time, all in flight before the
+// first is used, and the router rows come through L1 (NP of them per x
+// vector, which is where the larger NP find their memory parallelism). A butterfly reduce-scatter then leaves lane (i * 32/NV) with
+// value i summed over the warp, one shuffle hands expert e's score of token
+// q to lane e, and the warp selects for each of its tokens in turn.
+template <typename TX, int NP, int TPW>
+__global__ void __launch_bounds__(kThreads, 2) router_small_kernel(const RouterArgs a) {
   constexpr int EPV = V16<TX>::n;
-  constexpr int NV = NP * TB;  // 64 accumulators
-  static_assert(NV == 64, "reduce-scatter below assumes 64 values over 32 lanes");
-  __shared__ float red[kWarps][NV];
+  constexpr int NV = NP * TPW;
+  static_assert(NV == 16 || NV == 32, "reduce-scatter below assumes 16 or 32 values");
+  constexpr int SPREAD = 32 / NV;
+  constexpr int kSmallBatch = 32 / NP;  // x vectors per token in flight: 4, 2 or 1
   __shared__ float wprob[kWarps * 32];
   __shared__ int bcount[32];
   const int N = a.N;
-  const int vec = a.d / EPV;                       // 16-byte vectors per row
-  const int vpw = (vec + kWarps - 1) / kWarps;     // vectors per warp
-  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int v_lo = warp * vpw, v_hi = min(vec, v_lo + vpw);
+  const int vec = a.d / EPV;  // 16-byte vectors per row
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   pdl_wait();
   pdl_trigger();
+  if (threadIdx.x < 32) bcount[threadIdx.x] = 0;
+  __syncthreads();
   const uint4* x = static_cast<const uint4*>(a.x);
   const uint4* w = static_cast<const uint4*>(a.w);
-  if (tid < 32) bcount[tid] = 0;
-  // index of this lane's two reduced values: 2 * bit-reversed lane
-  const int base = ((lane & 16) ? 32 : 0) + ((lane & 8) ? 16 : 0) + ((lane & 4) ? 8 : 0) +
-                   ((lane & 2) ? 4 : 0) + ((lane & 1) ? 2 : 0);
   float psum[1] = {0.f};
-
-  for (long long t0 = (long long)blockIdx.x * TB; t0 < a.T; t0 += (long long)gridDim.x * TB) {
+  const long long groups = (a.T + TPW - 1) / TPW;
+  for (long long g = (long long)blockIdx.x * kWarps + warp; g < groups;
+       g += (long long)gridDim.x * kWarps) {
+    const long long t0 = g * TPW;
     float v[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) v[i] = 0.f;
-    for (int vv = v_lo + lane; vv < v_hi; vv += 32) {
-      uint4 xq[TB];
+    const uint4* xr[TPW];
 #pragma unroll
-      for (int q = 0; q < TB; ++q)
-        xq[q] = (t0 + q < a.T) ? __ldg(x + (t0 + q) * vec + vv) : make_uint4(0, 0, 0, 0);
-      uint4 wq[NP];  // all expert rows' vectors issued before any is used
+    for (int q = 0; q < TPW; ++q) xr[q] = (t0 + q < a.T) ? x + (t0 + q) * vec : nullptr;
+    for (int vb = lane; vb < vec; vb += 32 * kSmallBatch) {
+      uint4 xq[kSmallBatch][TPW];  // a batch of x vectors in flight before any is used
 #pragma unroll
-      for (int e = 0; e < NP; ++e)
-        wq[e] = (e < N) ? __ldg(w + (size_t)e * vec + vv) : make_uint4(0, 0, 0, 0);
+      for (int b = 0; b < kSmallBatch; ++b)
 #pragma unroll
-      for (int e = 0; e < NP; ++e) {
-        float wf[EPV];
-        V16<TX>::cvt(wq[e], wf);
+        for (int q = 0; q < TPW; ++q) {
+          const int vv = vb + 32 * b;
+          xq[b][q] = (xr[q] && vv < vec) ? __ldg(xr[q] + vv) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-        for (int q = 0; q < TB; ++q) {
-          float xf[EPV];
-          V16<TX>::cvt(xq[q], xf);
+      for (int b = 0; b < kSmallBatch; ++b) {
+        const int vv = vb + 32 * b;
+        if (vv >= vec) break;
+        float xf[TPW][EPV];
 #pragma unroll
-          for (int i = 0; i < EPV; ++i) v[q * NP + e] = fmaf(xf[i], wf[i], v[q * NP + e]);
+        for (int q = 0; q < TPW; ++q) V16<TX>::cvt(xq[b][q], xf[q]);
+#pragma unroll
+        for (int e = 0; e < NP; ++e) {
+          const uint4 wq = (e < N) ? __ldg(w + (size_t)e * vec + vv) : make_uint4(0, 0, 0, 0);
+          float wf[EPV];
+          V16<TX>::cvt(wq, wf);
+#pragma unroll
+          for (int q = 0; q < TPW; ++q)
+#pragma unroll
+            for (int i = 0; i < EPV; ++i) v[q * NP + e] = fmaf(xf[q][i], wf[i], v[q * NP + e]);
         }
       }
     }
     // reduce-scatter: after the step with offset o a lane keeps half of its
-    // values (the upper half when lane & o), each summed with its partner's.
+    // values (the upper half when lane & o), each summed with its partner's;
+    // lanes that end up holding the same value then add their halves.
 #pragma unroll
     for (int o = 16, L = NV; o > 0; o >>= 1, L >>= 1) {
-      const bool upper = (lane & o) != 0;
+      if (L > 1) {
+        const bool upper = (lane & o) != 0;
 #pragma unroll
-      for (int i = 0; i < L / 2; ++i) {
-        const float send = upper ? v[i] : v[i + L / 2];
-        const float keep = upper ? v[i + L / 2] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        for (int i = 0; i < L / 2; ++i) {
+          const float send = upper ? v[i] : v[i + L / 2];
+          const float keep = upper ? v[i + L / 2] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      } else {
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
       }
     }
-    red[warp][base] = v[0];
-    red[warp][base + 1] = v[1];
-    __syncthreads();
-    if (warp < TB && t0 + warp < a.T) {
-      const long long t = t0 + warp;
-      float r[1] = {0.f};
-      if (lane < N) {
-        float sum = 0.f;
-        for (int ww = 0; ww < kWarps; ++ww) sum += red[ww][warp * NP + lane];
-        r[0] = a.logit_bias ? __fadd_rn(sum, a.logit_bias[lane]) : sum;
-        if (a.logits_out) a.logits_out[t * N + lane] = r[0];
+#pragma unroll
+    for (int q = 0; q < TPW; ++q) {
+      const long long t = t0 + q;
+      const int src = ((q * NP + (lane < NP ? lane : 0)) % NV) * SPREAD;
+      const float sum = __shfl_sync(0xffffffffu, v[0], src);
+      if (t < a.T) {  // warp-uniform
+        float r[1] = {0.f};
+        if (lane < N) {
+          r[0] = a.logit_bias ? __fadd_rn(sum, a.logit_bias[lane]) : sum;
+          if (a.logits_out) a.logits_out[t * N + lane] = r[0];
+        }
+        select_token<1>(r, lane, t, a, psum, bcount);
       }
-      select_token<1>(r, lane, t, a, psum, bcount);
     }
-    __syncthreads();
   }
+  __syncthreads();
   finish_block<1>(psum, wprob, bcount, a);
 }
 
@@ -462,15 +466,6 @@ __global__ void __launch_bounds__(kThreads) router_tiled_kernel(const RouterArgs
 }
 
 // prob_sum[e] = sum over blocks, in block order.
-__global__ void router_reduce_kernel(const float* partials, int nblk, int N, float* prob_sum) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  pdl_wait();
-  pdl_trigger();
-  if (e >= N) return;
-  float s = 0.f;
-  for (int b = 0; b < nblk; ++b) s += partials[(size_t)b * N + e];
-  prob_sum[e] = s;
-}
 
 template <typename K>
 cudaError_t launch_k(K kernel, const RouterArgs& a, int grid, size_t smem, cudaStream_t s) {
@@ -487,16 +482,21 @@ bool use_small(const moe_config& c, const float* logits_in) {
 // Blocks of the router launch; router_partials_bytes() sizes the partials
 // buffer for the larger of the two choices.
 int router_grid(const moe_config& c, const float* logits_in) {
-  if (use_small(c, logits_in)) return ceil_div(c.T, kSmallTokensPerBlock);
+  if (use_small(c, logits_in)) {
+    // one token group (2 tokens for N <= 8, else 1) per warp, at most 4 blocks per SM
+    const int tpw = c.n_experts <= 8 ? 2 : 1;
+    const int blocks = ceil_div(ceil_div(c.T, tpw), kWarps);
+    return blocks < kSmallMaxBlocks ? blocks : kSmallMaxBlocks;
+  }
   return ceil_div(c.T, kTileTokens);
 }
 
 template <typename TX>
 cudaError_t launch_dtype(const moe_config& c, const RouterArgs& a, int grid, cudaStream_t s) {
   if (use_small(c, a.logits_in)) {
-    if (c.n_experts <= 8) return launch_k(router_small_kernel<TX, 8, 8>, a, grid, 0, s);
-    if (c.n_experts <= 16) return launch_k(router_small_kernel<TX, 16, 4>, a, grid, 0, s);
-    return launch_k(router_small_kernel<TX, 32, 2>, a, grid, 0, s);
+    if (c.n_experts <= 8) return launch_k(router_small_kernel<TX, 8, 2>, a, grid, 0, s);
+    if (c.n_experts <= 16) return launch_k(router_small_kernel<TX, 16, 1>, a, grid, 0, s);
+    return launch_k(router_small_kernel<TX, 32, 1>, a, grid, 0, s);
   }
   auto smem = [](int BN) {  // must match the layout in router_tiled_kernel
     const size_t tile = sizeof(float) * (size_t)kTileTokens * BN;
@@ -511,10 +511,13 @@ cudaError_t launch_dtype(const moe_config& c, const RouterArgs& a, int grid, cud
 
 }  // namespace
 
+int router_partial_blocks(const moe_config& c) {
+  return c.n_experts <= 32 ? ceil_div(c.T, kSmallTokensPerBlock) : ceil_div(c.T, kTileTokens);
+}
+
 size_t router_partials_bytes(const moe_config& c) {
-  const int blocks = c.n_experts <= 32 ? ceil_div(c.T, kSmallTokensPerBlock)
-                                       : ceil_div(c.T, kTileTokens);
-  return sizeof(float) * (size_t)blocks * (size_t)c.n_experts;
+  // probability sums (float) then counts (int32), [blocks][N] each
+  return 2 * sizeof(float) * (size_t)router_partial_blocks(c) * (size_t)c.n_experts;
 }
 
 cudaError_t launch_router(const moe_config& c, const void* x, const void* w_router,
@@ -522,34 +525,27 @@ cudaError_t launch_router(const moe_config& c, const void* x, const void* w_rout
                           const float* logits_in, float* logits_out, int32_t* topk_idx,
                           float* topk_w, int32_t* counts, float* prob_sum, float* partials,
                           int* status, cudaStream_t s) {
-  // status[1] counts finished router blocks for the fused final sum; the
-  // caller zeroes status[0..1] before each call.
-  cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.n_experts, s);
-  if (e != cudaSuccess) return e;
-  if (c.T == 0) return cudaMemsetAsync(prob_sum, 0, sizeof(float) * c.n_experts, s);
+  // status[1] counts finished router blocks for the final sum in the last
+  // block; the caller zeroes status[0..1] before each call.
+  if (c.T == 0) {
+    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.n_experts, s);
+    if (e != cudaSuccess) return e;
+    return cudaMemsetAsync(prob_sum, 0, sizeof(float) * c.n_experts, s);
+  }
+  int32_t* cpart = reinterpret_cast<int32_t*>(partials) +
+                   (size_t)router_partial_blocks(c) * (size_t)c.n_experts;
+  if (router_tc_applies(c, logits_in))
+    return launch_router_tc(c, x, w_router, logit_bias, sel_bias, logits_out, topk_idx, topk_w,
+                            counts, prob_sum, partials, cpart, status, s);
   RouterArgs a;
   a.x = x; a.w = w_router; a.logit_bias = logit_bias; a.sel_bias = sel_bias;
   a.logits_in = logits_in; a.logits_out = logits_out; a.topk_idx = topk_idx;
-  a.topk_w = topk_w; a.counts = counts; a.partials = partials; a.status = status;
+  a.topk_w = topk_w; a.counts = counts; a.partials = partials; a.cpart = cpart;
+  a.status = status; a.prob_sum = prob_sum; a.done = status + 1;
   a.T = c.T; a.d = c.d_model; a.N = c.n_experts; a.k = c.top_k; a.gate_mode = c.gate_mode;
-  if (router_tc_applies(c, logits_in)) {
-    bool fused = false;
-    e = launch_router_tc(c, x, w_router, logit_bias, sel_bias, logits_out, topk_idx, topk_w, counts,
-                         prob_sum, partials, status, &fused, s);
-    if (e != cudaSuccess || fused) return e;
-    ProfScope p(K_ROUTER_REDUCE, s);
-    return launch_pdl(router_reduce_kernel, dim3(ceil_div(c.n_experts, 256)), dim3(256), 0, s, 1,
-                      (const float*)partials, router_tc_grid(c), c.n_experts, prob_sum);
-  }
   const int grid = router_grid(c, logits_in);
-  const bool fused_sum = grid <= kFusedSumMaxBlocks;
-  a.prob_sum = prob_sum;
-  a.done = fused_sum ? status + 1 : nullptr;
-  e = (c.dtype == MOE_BF16) ? launch_dtype<__nv_bfloat16>(c, a, grid, s) : launch_dtype<float>(c, a, grid, s);
-  if (e != cudaSuccess || fused_sum) return e;
-  ProfScope p(K_ROUTER_REDUCE, s);
-  return launch_pdl(router_reduce_kernel, dim3(ceil_div(c.n_experts, 256)), dim3(256), 0, s, 1,
-                    (const float*)partials, grid, c.n_experts, prob_sum);
+  return (c.dtype == MOE_BF16) ? launch_dtype<__nv_bfloat16>(c, a, grid, s)
+                               : launch_dtype<float>(c, a, grid, s);
 }
 
 }  // namespace moe

@@ -7,22 +7,23 @@
 // and has no workspace slot. They can neither call cudaMalloc nor pass the
 // scratch that moe_router_topk takes. This entry point runs the same router
 // kernels, with their scratch (one status word and the per-block
-// probability partials) in a fixed array of this library's own device
+// probability sums and counts) in a fixed array of this library's own device
 // memory instead of a caller workspace.
 //
 // Limits and rules (also stated in include/moe.h):
 //  - The array is kNoallocScratchBytes (1 MiB) per GPU that loads the
-//    library, held until the process exits. A call needs 256 + 4 * B * N
-//    bytes of it, B = ceil(T / 8) when N <= 32 and ceil(T / 64) otherwise
-//    (the router's block count); a larger call returns MOE_ERR_WORKSPACE
+//    library, held until the process exits. A call needs 256 + 8 * B * N
+//    bytes of it (a float sum and an int count per block and expert), with
+//    B = ceil(T / 8) when N <= 32 and ceil(T / 64) otherwise (the most
+//    blocks a router kernel runs); a larger call returns MOE_ERR_WORKSPACE
 //    and launches nothing.
 //  - The array's device address is looked up once per device, by the first
 //    call made while that device is current; make that first call before
 //    any stream capture.
 //  - Every call shares the one array and it keeps the last call's contents.
 //    The status word and the router's finished-block counter are cleared at
-//    the start of every call; the partials are fully rewritten before they
-//    are read. Calls whose work overlaps on the
+//    the start of every call; the per-block sums and counts are fully
+//    rewritten before they are read. Calls whose work overlaps on the
 //    GPU (different streams, or different host threads without ordering)
 //    race on the array and give undefined results.
 //  - Nothing here calls cudaMalloc, cudaFree or any allocating routine.

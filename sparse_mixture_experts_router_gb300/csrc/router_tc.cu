@@ -29,6 +29,7 @@
 #include "device_util.cuh"
 #include "moe_internal.h"
 #include "sm103_ptx.cuh"
+#include "router_finish.cuh"
 #include "sm103_wait.cuh"
 
 namespace moe {
@@ -51,7 +52,6 @@ constexpr int RT_LSTRIDE = 9;                   // padded quarter list
 constexpr int RT_TMEM_COLS = 256;
 constexpr int RT_NMAX = 256;
 constexpr uint32_t RT_IDESC = ptx::idesc_bf16_f32(RT_BM, RT_NMAX);
-constexpr int kFusedSumMaxBlocks = 32;
 
 struct RouterTcArgs {
   const float* logit_bias;
@@ -60,9 +60,10 @@ struct RouterTcArgs {
   int32_t* topk_idx;
   float* topk_w;
   int32_t* counts;
-  float* partials;  // [gridDim.x][N]
+  float* partials;  // [gridDim.x][N] probability sums of each block
+  int32_t* cpart;   // [gridDim.x][N] counts of each block
   float* prob_sum;
-  int* done;        // finished-block counter for the fused final sum, or null
+  int* done;        // finished-block counter for the final sum, zero at launch
   int* status;
   int T, d, N, k, gate_mode;
 };
@@ -147,7 +148,6 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   __shared__ float s_lb[RT_NMAX], s_sb[RT_NMAX];
   __shared__ float s_psum[4][RT_NMAX];  // [TMEM lane group][expert]
   __shared__ int s_cnt[RT_NMAX];
-  __shared__ int s_last;
 
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x / 32), 0);
   const int lane = threadIdx.x % 32;
@@ -416,25 +416,12 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
-  // block partial of the probability sums (epilogue warps in order) and counts
+  // block partial of the probability sums (lane groups in order) and counts
   for (int e = threadIdx.x; e < N; e += RT_THREADS) {
     a.partials[(size_t)blockIdx.x * N + e] = ((s_psum[0][e] + s_psum[1][e]) + s_psum[2][e]) + s_psum[3][e];
-    if (s_cnt[e]) atomicAdd(&a.counts[e], s_cnt[e]);
+    a.cpart[(size_t)blockIdx.x * N + e] = s_cnt[e];
   }
-  if (a.done != nullptr) {  // small grids: the last block sums the partials in block order
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(a.done, 1) == (int)gridDim.x - 1;
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      for (int e = threadIdx.x; e < N; e += RT_THREADS) {
-        float s = 0.f;
-        for (int b = 0; b < (int)gridDim.x; ++b) s += __ldcg(a.partials + (size_t)b * N + e);
-        a.prob_sum[e] = s;
-      }
-    }
-  }
+  router_finish<RT_THREADS>(a.partials, a.cpart, N, a.prob_sum, a.counts, a.done);
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();
@@ -449,12 +436,10 @@ bool router_tc_applies(const moe_config& c, const float* logits_in) {
          c.n_experts <= RT_NMAX;
 }
 
-int router_tc_grid(const moe_config& c) { return ceil_div(c.T, RT_BM); }
-
 cudaError_t launch_router_tc(const moe_config& c, const void* x, const void* w_router,
                              const float* logit_bias, const float* sel_bias, float* logits_out,
                              int32_t* topk_idx, float* topk_w, int32_t* counts, float* prob_sum,
-                             float* partials, int* status, bool* fused_sum, cudaStream_t s) {
+                             float* partials, int32_t* cpart, int* status, cudaStream_t s) {
   CUtensorMap mx, mw;
   if (!make_map(&mx, x, c.T, c.d_model) || !make_map(&mw, w_router, c.n_experts, c.d_model))
     return cudaErrorInvalidValue;
@@ -467,7 +452,7 @@ cudaError_t launch_router_tc(const moe_config& c, const void* x, const void* w_r
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  const int grid = router_tc_grid(c);
+  const int grid = ceil_div(c.T, RT_BM);
   RouterTcArgs a;
   a.logit_bias = logit_bias;
   a.sel_bias = sel_bias;
@@ -476,9 +461,9 @@ cudaError_t launch_router_tc(const moe_config& c, const void* x, const void* w_r
   a.topk_w = topk_w;
   a.counts = counts;
   a.partials = partials;
+  a.cpart = cpart;
   a.prob_sum = prob_sum;
-  *fused_sum = grid <= kFusedSumMaxBlocks;
-  a.done = *fused_sum ? status + 1 : nullptr;
+  a.done = status + 1;
   a.status = status;
   a.T = c.T;
   a.d = c.d_model;

@@ -40,6 +40,7 @@ CASES = [
     (3000, 128, 8, 64, moe.MOE_BF16, 1.2),     # Zipf-skewed
     (2048, 4, 4, 16, moe.MOE_F32, 0.0),        # k = N
     (777, 33, 3, 40, moe.MOE_BF16, 2.0),
+    (9000, 64, 8, 16, moe.MOE_BF16, 0.5),     # 72000 pairs: the chunked four-launch path
 ]
 
 
@@ -81,10 +82,12 @@ def test_empty_batch():
     assert st == 0 and off.cpu().tolist() == [0] * 6
 
 
-def test_out_of_range_expert_is_reported():
-    """An index outside [0, N) is caught by the kernel's own bounds check:
-    the status word reports it and nothing is written out of bounds."""
-    T, N, k, d = 100, 8, 2, 32
+@pytest.mark.parametrize("T,k", [(100, 2), (1500, 2), (9000, 8)])
+def test_out_of_range_expert_is_reported(T, k):
+    """An index outside [0, N) is caught by the kernel's own bounds check
+    (single-block, expert-group and chunked paths): the status word reports
+    it and nothing is written out of bounds."""
+    N, d = 8, 32
     idx = random_idx(T, N, k, seed=1)
     idx[17, 1] = N + 3
     idx[40, 0] = -2

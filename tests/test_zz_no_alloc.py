@@ -72,7 +72,7 @@ def test_noalloc_router_matches_workspace_router_twice():
 
 def test_noalloc_router_rejects_calls_beyond_its_scratch():
     N, k = 256, 8
-    T = 66 * 1024  # needs 256 + 4 * ceil(T / 64) * 256 bytes > 1 MiB
+    T = 33 * 1024  # needs 256 + 8 * ceil(T / 64) * 256 bytes > 1 MiB
     cfg = moe.config(T=T, d_model=64, n_experts=N, top_k=k, d_ff=8)
     o = _outputs(1, N, k)
     before = moe.launch_count()
