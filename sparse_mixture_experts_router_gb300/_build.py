@@ -63,7 +63,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, sources()))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp, "-ldl", "-lpthread", "-lrt"]
+    cmd = [cc, *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp, "-ldl", "-lpthread", "-lrt",
+           "-Xlinker", "--no-undefined"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -7,6 +7,7 @@
 #include <utility>
 #include <vector>
 
+#include "device_util.cuh"
 #include "moe_internal.h"
 
 namespace moe {
@@ -129,10 +130,8 @@ bool all_aligned(std::initializer_list<const void*> ps) {
   return true;
 }
 
-// Zeroes the workspace header words: [0] device status, [1] the router's
-// finished-block counter.
 int reset_status(int* status, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(status, 0, 2 * sizeof(int), s);
+  cudaError_t e = launch_reset_status(status, s);
   return e == cudaSuccess ? MOE_OK : fail_cuda(e);
 }
 
@@ -168,11 +167,11 @@ int grouped_impl(const moe_config& c, const void* x_perm, long long xp_rows, con
 }
 
 // ---- profiler ---------------------------------------------------------------
-const char* kKernelNames[K_NUM] = {"router_topk",   "permute_hist",   "permute_scan",
-                                   "permute_rank",  "permute_gather", "permute_small",
-                                   "permute_group", "seg_table",      "gate_up",
-                                   "down",          "splitk_reduce",  "combine",
-                                   "balance_stats"};
+const char* kKernelNames[K_NUM] = {"reset_status",  "router_topk",    "permute_hist",
+                                   "permute_scan",  "permute_rank",   "permute_gather",
+                                   "permute_small", "permute_group",  "seg_table",
+                                   "gate_up",       "down",           "splitk_reduce",
+                                   "combine",       "balance_stats"};
 struct Prof {
   std::mutex mu;
   uint32_t mask = 0;
@@ -196,6 +195,26 @@ Prof& prof() {
 }
 
 }  // namespace
+
+// Zeroes the workspace header words, [0] device status and [1] the router's
+// finished-block counter, after the previous grid on the stream has
+// finished (so a late error of the previous call is not wiped out). A
+// kernel rather than a memset: it stays in the chain of programmatic
+// dependent launches, where a memset node breaks it.
+namespace {
+__global__ void reset_status_kernel(int* status) {
+  pdl_wait();
+  if (threadIdx.x < 2) status[threadIdx.x] = 0;
+  __syncwarp();
+  pdl_trigger();
+}
+}  // namespace
+
+cudaError_t launch_reset_status(int* status, cudaStream_t s) {
+  ProfScope p(K_RESET, s);
+  return launch_pdl(reset_status_kernel, dim3(1), dim3(32), 0, s, 1, status);
+}
+
 
 void prof_begin(int id, cudaStream_t s) {
   Prof& p = prof();

@@ -956,13 +956,6 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmArgs a, in
 }
 
 // ---------------------------------------------------------------- host side --
-int num_sms() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
-}
-
 template <int EPI>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_sh, const CUtensorMap& b0,
                         const CUtensorMap& b1, const GemmArgs& args, int max_tiles,

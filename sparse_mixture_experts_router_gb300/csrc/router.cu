@@ -195,7 +195,7 @@ __device__ __forceinline__ void finish_block(const float (&psum)[EJ], float* wpr
     a.partials[(size_t)blockIdx.x * a.N + e] = s;
     a.cpart[(size_t)blockIdx.x * a.N + e] = bcount[e];
   }
-  router_finish<kThreads>(a.partials, a.cpart, a.N, a.prob_sum, a.counts, a.done);
+  router_finish<kThreads>(a.partials, a.cpart, a.N, (int)gridDim.x, a.prob_sum, a.counts, a.done);
 }
 
 // ---------------------------------------------------------------------------
@@ -534,6 +534,9 @@ cudaError_t launch_router(const moe_config& c, const void* x, const void* w_rout
   }
   int32_t* cpart = reinterpret_cast<int32_t*>(partials) +
                    (size_t)router_partial_blocks(c) * (size_t)c.n_experts;
+  if (logits_in == nullptr && c.dtype == MOE_BF16 && c.n_experts <= 32)
+    return launch_router_tc32(c, x, w_router, logit_bias, sel_bias, logits_out, topk_idx, topk_w,
+                              counts, prob_sum, partials, cpart, status, s);
   if (router_tc_applies(c, logits_in))
     return launch_router_tc(c, x, w_router, logit_bias, sel_bias, logits_out, topk_idx, topk_w,
                             counts, prob_sum, partials, cpart, status, s);

@@ -13,21 +13,21 @@
 
 namespace moe {
 
-// Call from all NT threads of every block, after the block has written
-// partials[blockIdx.x][0..N) and cpart[blockIdx.x][0..N). `done` counts
-// finished blocks and must be zero at launch.
+// Call from all NT threads of each of the nblk blocks that hold partials,
+// after the block has written its row b of partials[nblk][N] and
+// cpart[nblk][N]. `done` counts finished blocks and must be zero at launch.
 template <int NT>
 __device__ __forceinline__ void router_finish(const float* partials, const int32_t* cpart, int N,
-                                              float* prob_sum, int32_t* counts, int* done) {
+                                              int nblk, float* prob_sum, int32_t* counts,
+                                              int* done) {
   static_assert(NT % 32 == 0, "whole warps");
   __shared__ int last;
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(done, 1) == (int)gridDim.x - 1;
+  if (threadIdx.x == 0) last = atomicAdd(done, 1) == nblk - 1;
   __syncthreads();
   if (!last) return;
   __threadfence();
-  const int nblk = (int)gridDim.x;
   // G threads per expert: a power of two up to 32 with G * N <= NT when possible
   int G = 1;
   while (G < 32 && 2 * G * N <= NT) G *= 2;

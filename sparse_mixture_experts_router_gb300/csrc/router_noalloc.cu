@@ -90,7 +90,7 @@ extern "C" int moe_router_topk_noalloc(const moe_config* cfg, const void* x, con
   int* status = static_cast<int*>(scratch);
   float* partials = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + kStatusBytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  e = cudaMemsetAsync(status, 0, 2 * sizeof(int), s);  // status, router block counter
+  e = launch_reset_status(status, s);  // status, router block counter
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   e = launch_router(c, x, w_router, logit_bias, sel_bias, logits_in, logits_out, topk_idx, topk_w,
                     counts, prob_sum, partials, status, s);

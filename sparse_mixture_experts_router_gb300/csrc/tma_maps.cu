@@ -1,5 +1,6 @@
-// Host-side TMA tensor maps (cuTensorMapEncodeTiled, looked up through the
-// runtime so the library does not link the driver library).
+// Host-side helpers of the tcgen05 kernels: TMA tensor maps
+// (cuTensorMapEncodeTiled, looked up through the runtime so the library does
+// not link the driver library) and the device's SM count.
 #include <cuda.h>
 
 #include <mutex>
@@ -44,6 +45,13 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
 }
 
 }  // namespace moe
