@@ -152,14 +152,13 @@ MOE_API int moe_router_topk(const moe_config* cfg, const void* x, const void* w_
  * operator only its inputs and outputs), so they can neither call
  * cudaMalloc nor hand over the scratch moe_router_topk takes.
  * Arguments and results are those of moe_router_topk without ws/ws_bytes.
- * For bf16 with more than 32 experts the scores are computed on the tensor
- * cores in 128-token tiles, which use half the partials B below allows for.
  * The scratch (a status word and per-block probability sums and counts) lives in
  * a fixed 1 MiB array of the library's own device memory on every GPU that
  * loads the library, held until the process exits:
- *  - a call needs 256 + 8 * B * N bytes of it, B = ceil(T / 8) when N <= 32
- *    and ceil(T / 64) otherwise (for N = 256: T <= 32704); a larger call
- *    returns MOE_ERR_WORKSPACE, launching nothing;
+ *  - a call needs 256 + 8 * B * N bytes of it, B = ceil(T / 64), or
+ *    max(ceil(T / 64), min(T, 608)) when N <= 32 (for N = 8: T <= 1048320;
+ *    N = 32: T <= 262080; N = 256: T <= 32704); a larger call returns
+ *    MOE_ERR_WORKSPACE, launching nothing;
  *  - the first call made with a device current looks up the array's device
  *    address for that device; make that first call before any stream capture;
  *  - all calls share the array: calls whose work overlaps on the GPU race

@@ -38,8 +38,9 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTileTokens = 64;              // tokens per block, tiled kernel
 constexpr int kKC = 32;                      // K slice of the tiled kernel
-constexpr int kSmallTokensPerBlock = 8;      // few-expert kernel: partials sized for T/8 blocks
 constexpr int kSmallMaxBlocks = 4 * 152;     // few-expert kernel: grid-stride beyond this
+constexpr int kTc32MinTokens = 2048;         // bf16, N <= 32: tensor-core router from here
+constexpr int kSmallTargetWarps = 2 * 152 * kWarps;  // few-expert kernel: warps to keep busy
 
 struct RouterArgs {
   const void* x;
@@ -199,17 +200,21 @@ __device__ __forceinline__ void finish_block(const float (&psum)[EJ], float* wpr
 }
 
 // ---------------------------------------------------------------------------
-// Few experts (N <= 32): each warp scores TPW tokens at a time over all of
-// d_model (grid-stride over token groups, no block barrier inside the loop).
-// A lane takes every 32nd 16-byte vector of the tokens' rows and keeps
-// NV = NP*TPW partial dot products (NP = N rounded up to 8, 16 or 32); x
-// vectors are loaded 32/NP per token at a time, all in flight before the
-// first is used, and the router rows come through L1 (NP of them per x
-// vector, which is where the larger NP find their memory parallelism). A butterfly reduce-scatter then leaves lane (i * 32/NV) with
-// value i summed over the warp, one shuffle hands expert e's score of token
-// q to lane e, and the warp selects for each of its tokens in turn.
+// Few experts (N <= 32): a group of TPW tokens is scored by `wsplit` warps
+// of one block (1 for large batches, up to 8 when there are few tokens, so
+// a decode step still spreads its row over a whole block). A warp takes
+// every (32*wsplit)-th 16-byte vector of the group's rows, starting at its
+// own 32-vector slice, and keeps NV = NP*TPW partial dot products (NP = N
+// rounded up to 8, 16 or 32); x vectors are loaded 32/NP per token at a
+// time, all in flight before the first is used, and the router rows come
+// through L1 (NP of them per x vector, which is where the larger NP find
+// their memory parallelism). A butterfly reduce-scatter then leaves lane
+// (i * 32/NV) with value i summed over the warp; the group's warps add
+// their sums in warp order through shared memory, one shuffle hands expert
+// e's score of token q to lane e of the group's first warp, and that warp
+// selects for each of the group's tokens in turn.
 template <typename TX, int NP, int TPW>
-__global__ void __launch_bounds__(kThreads, 2) router_small_kernel(const RouterArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) router_small_kernel(const RouterArgs a, int wsplit) {
   constexpr int EPV = V16<TX>::n;
   constexpr int NV = NP * TPW;
   static_assert(NV == 16 || NV == 32, "reduce-scatter below assumes 16 or 32 values");
@@ -217,9 +222,12 @@ __global__ void __launch_bounds__(kThreads, 2) router_small_kernel(const RouterA
   constexpr int kSmallBatch = 32 / NP;  // x vectors per token in flight: 4, 2 or 1
   __shared__ float wprob[kWarps * 32];
   __shared__ int bcount[32];
+  __shared__ float red[kWarps][32];
   const int N = a.N;
   const int vec = a.d / EPV;  // 16-byte vectors per row
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int gpb = kWarps / wsplit;  // token groups per block and round
+  const int wi = warp % wsplit;     // this warp's slice of the group's vectors
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x < 32) bcount[threadIdx.x] = 0;
@@ -228,8 +236,9 @@ __global__ void __launch_bounds__(kThreads, 2) router_small_kernel(const RouterA
   const uint4* w = static_cast<const uint4*>(a.w);
   float psum[1] = {0.f};
   const long long groups = (a.T + TPW - 1) / TPW;
-  for (long long g = (long long)blockIdx.x * kWarps + warp; g < groups;
-       g += (long long)gridDim.x * kWarps) {
+  const long long rounds = (groups + gpb - 1) / gpb;
+  for (long long rd = blockIdx.x; rd < rounds; rd += gridDim.x) {  // block-uniform
+    const long long g = rd * gpb + warp / wsplit;
     const long long t0 = g * TPW;
     float v[NV];
 #pragma unroll
@@ -237,18 +246,19 @@ __global__ void __launch_bounds__(kThreads, 2) router_small_kernel(const RouterA
     const uint4* xr[TPW];
 #pragma unroll
     for (int q = 0; q < TPW; ++q) xr[q] = (t0 + q < a.T) ? x + (t0 + q) * vec : nullptr;
-    for (int vb = lane; vb < vec; vb += 32 * kSmallBatch) {
+    const int stride = 32 * wsplit;
+    for (int vb = 32 * wi + lane; vb < vec; vb += stride * kSmallBatch) {
       uint4 xq[kSmallBatch][TPW];  // a batch of x vectors in flight before any is used
 #pragma unroll
       for (int b = 0; b < kSmallBatch; ++b)
 #pragma unroll
         for (int q = 0; q < TPW; ++q) {
-          const int vv = vb + 32 * b;
+          const int vv = vb + stride * b;
           xq[b][q] = (xr[q] && vv < vec) ? __ldg(xr[q] + vv) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
       for (int b = 0; b < kSmallBatch; ++b) {
-        const int vv = vb + 32 * b;
+        const int vv = vb + stride * b;
         if (vv >= vec) break;
         float xf[TPW][EPV];
 #pragma unroll
@@ -282,18 +292,27 @@ __global__ void __launch_bounds__(kThreads, 2) router_small_kernel(const RouterA
         v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
       }
     }
+    if (wsplit > 1) {  // the group's warps, added in warp order
+      red[warp][lane] = v[0];
+      __syncthreads();
+      if (wi == 0)
+        for (int j = 1; j < wsplit; ++j) v[0] += red[warp + j][lane];
+      __syncthreads();
+    }
+    if (wi == 0) {
 #pragma unroll
-    for (int q = 0; q < TPW; ++q) {
-      const long long t = t0 + q;
-      const int src = ((q * NP + (lane < NP ? lane : 0)) % NV) * SPREAD;
-      const float sum = __shfl_sync(0xffffffffu, v[0], src);
-      if (t < a.T) {  // warp-uniform
-        float r[1] = {0.f};
-        if (lane < N) {
-          r[0] = a.logit_bias ? __fadd_rn(sum, a.logit_bias[lane]) : sum;
-          if (a.logits_out) a.logits_out[t * N + lane] = r[0];
+      for (int q = 0; q < TPW; ++q) {
+        const long long t = t0 + q;
+        const int src = ((q * NP + (lane < NP ? lane : 0)) % NV) * SPREAD;
+        const float sum = __shfl_sync(0xffffffffu, v[0], src);
+        if (t < a.T) {  // warp-uniform
+          float r[1] = {0.f};
+          if (lane < N) {
+            r[0] = a.logit_bias ? __fadd_rn(sum, a.logit_bias[lane]) : sum;
+            if (a.logits_out) a.logits_out[t * N + lane] = r[0];
+          }
+          select_token<1>(r, lane, t, a, psum, bcount);
         }
-        select_token<1>(r, lane, t, a, psum, bcount);
       }
     }
   }
@@ -481,11 +500,22 @@ bool use_small(const moe_config& c, const float* logits_in) {
 
 // Blocks of the router launch; router_partials_bytes() sizes the partials
 // buffer for the larger of the two choices.
+// Few-expert kernel: warps per token group (2 tokens for N <= 8, else 1),
+// so that about kSmallTargetWarps warps have work.
+int router_small_wsplit(const moe_config& c) {
+  const int tpw = c.n_experts <= 8 ? 2 : 1;
+  const long long groups = ceil_div(c.T, tpw);
+  int ws = 1;
+  while (ws < kWarps && groups * ws * 2 <= kSmallTargetWarps) ws *= 2;
+  return ws;
+}
+
 int router_grid(const moe_config& c, const float* logits_in) {
   if (use_small(c, logits_in)) {
-    // one token group (2 tokens for N <= 8, else 1) per warp, at most 4 blocks per SM
+    // one round of kWarps / wsplit token groups per block, at most 4 blocks per SM
     const int tpw = c.n_experts <= 8 ? 2 : 1;
-    const int blocks = ceil_div(ceil_div(c.T, tpw), kWarps);
+    const int gpb = kWarps / router_small_wsplit(c);
+    const int blocks = ceil_div(ceil_div(c.T, tpw), gpb);
     return blocks < kSmallMaxBlocks ? blocks : kSmallMaxBlocks;
   }
   return ceil_div(c.T, kTileTokens);
@@ -494,9 +524,13 @@ int router_grid(const moe_config& c, const float* logits_in) {
 template <typename TX>
 cudaError_t launch_dtype(const moe_config& c, const RouterArgs& a, int grid, cudaStream_t s) {
   if (use_small(c, a.logits_in)) {
-    if (c.n_experts <= 8) return launch_k(router_small_kernel<TX, 8, 2>, a, grid, 0, s);
-    if (c.n_experts <= 16) return launch_k(router_small_kernel<TX, 16, 1>, a, grid, 0, s);
-    return launch_k(router_small_kernel<TX, 32, 1>, a, grid, 0, s);
+    const int ws = router_small_wsplit(c);
+    ProfScope p(K_ROUTER, s);
+    if (c.n_experts <= 8)
+      return launch_pdl(router_small_kernel<TX, 8, 2>, dim3(grid), dim3(kThreads), 0, s, 1, a, ws);
+    if (c.n_experts <= 16)
+      return launch_pdl(router_small_kernel<TX, 16, 1>, dim3(grid), dim3(kThreads), 0, s, 1, a, ws);
+    return launch_pdl(router_small_kernel<TX, 32, 1>, dim3(grid), dim3(kThreads), 0, s, 1, a, ws);
   }
   auto smem = [](int BN) {  // must match the layout in router_tiled_kernel
     const size_t tile = sizeof(float) * (size_t)kTileTokens * BN;
@@ -511,8 +545,15 @@ cudaError_t launch_dtype(const moe_config& c, const RouterArgs& a, int grid, cud
 
 }  // namespace
 
+// The most blocks any router kernel for this configuration launches: the
+// tiled kernel (given scores, or N > 32 in fp32) takes one per 64 tokens,
+// the tensor-core kernels one per 128, and for up to 32 experts the warp
+// kernel at most min(T, kSmallMaxBlocks).
 int router_partial_blocks(const moe_config& c) {
-  return c.n_experts <= 32 ? ceil_div(c.T, kSmallTokensPerBlock) : ceil_div(c.T, kTileTokens);
+  const int tiled = ceil_div(c.T, kTileTokens);
+  if (c.n_experts > 32) return tiled;
+  const int warp_blocks = c.T < kSmallMaxBlocks ? c.T : kSmallMaxBlocks;
+  return warp_blocks > tiled ? warp_blocks : tiled;
 }
 
 size_t router_partials_bytes(const moe_config& c) {
@@ -534,7 +575,9 @@ cudaError_t launch_router(const moe_config& c, const void* x, const void* w_rout
   }
   int32_t* cpart = reinterpret_cast<int32_t*>(partials) +
                    (size_t)router_partial_blocks(c) * (size_t)c.n_experts;
-  if (logits_in == nullptr && c.dtype == MOE_BF16 && c.n_experts <= 32)
+  // Up to 32 experts the warp kernel has the lower fixed cost; from 2048
+  // tokens the tensor-core kernel streams x faster (measured crossover).
+  if (logits_in == nullptr && c.dtype == MOE_BF16 && c.n_experts <= 32 && c.T >= kTc32MinTokens)
     return launch_router_tc32(c, x, w_router, logit_bias, sel_bias, logits_out, topk_idx, topk_w,
                               counts, prob_sum, partials, cpart, status, s);
   if (router_tc_applies(c, logits_in))

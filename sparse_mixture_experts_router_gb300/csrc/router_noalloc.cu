@@ -14,9 +14,9 @@
 //  - The array is kNoallocScratchBytes (1 MiB) per GPU that loads the
 //    library, held until the process exits. A call needs 256 + 8 * B * N
 //    bytes of it (a float sum and an int count per block and expert), with
-//    B = ceil(T / 8) when N <= 32 and ceil(T / 64) otherwise (the most
-//    blocks a router kernel runs); a larger call returns MOE_ERR_WORKSPACE
-//    and launches nothing.
+//    B = ceil(T / 64), or max(ceil(T / 64), min(T, 608)) when N <= 32 (the
+//    most blocks a router kernel runs); a larger call returns
+//    MOE_ERR_WORKSPACE and launches nothing.
 //  - The array's device address is looked up once per device, by the first
 //    call made while that device is current; make that first call before
 //    any stream capture.

@@ -97,13 +97,16 @@ GEMM_CASES = [
     synth.DEEPSEEK_V3.replace(name="r_dsv3_full_size", d_ff=8),   # d_model = 7168
     # bf16 with up to 32 experts: the tensor-core router split along d_model
     # over a cluster of 4, 2 or 1 CTAs (partial scores added in rank order).
-    synth.Workload("r_tc32_cluster4", T=1000, d_model=4096, n_experts=8, top_k=2, d_ff=8, seed=19),
-    synth.Workload("r_tc32_n20_ragged", T=129, d_model=520, n_experts=20, top_k=5, d_ff=8,
+    # (from 2048 tokens; fewer tokens take the warp kernel).
+    synth.Workload("r_tc32_cluster4", T=4000, d_model=4096, n_experts=8, top_k=2, d_ff=8, seed=19),
+    synth.Workload("r_tc32_n20_ragged", T=2049, d_model=520, n_experts=20, top_k=5, d_ff=8,
                    gate_mode=1, sel_bias=True, zipf_s=1.2, seed=20),
-    synth.Workload("r_tc32_one_expert", T=77, d_model=256, n_experts=1, top_k=1, d_ff=8, seed=21),
-    synth.Workload("r_tc32_n32_many_tiles", T=4500, d_model=192, n_experts=32, top_k=8, d_ff=8,
-                   seed=22),
-    synth.Workload("r_tc32_decode", T=1, d_model=4096, n_experts=8, top_k=2, d_ff=8, seed=23),
+    synth.Workload("r_tc32_one_expert", T=2100, d_model=256, n_experts=1, top_k=1, d_ff=8, seed=21),
+    synth.Workload("r_tc32_cluster2", T=9000, d_model=256, n_experts=32, top_k=8, d_ff=8, seed=22),
+    synth.Workload("r_tc32_cluster1", T=19500, d_model=128, n_experts=16, top_k=4, d_ff=8, seed=23),
+    synth.Workload("r_warp_decode", T=1, d_model=4096, n_experts=8, top_k=2, d_ff=8, seed=24),
+    synth.Workload("r_warp_n20", T=129, d_model=520, n_experts=20, top_k=5, d_ff=8,
+                   gate_mode=1, sel_bias=True, zipf_s=1.2, seed=25),
 ]
 
 
@@ -120,14 +123,15 @@ def test_router_gemm_routes_like_the_oracle(oracle, w):
     assert np.allclose(got["prob_sum"].numpy(), ps, rtol=1e-4, atol=1e-4)
 
 
-@pytest.mark.parametrize("N,k,mode", [(64, 8, 1), (256, 8, 0), (48, 5, 0), (8, 2, 0), (32, 6, 1)])
-def test_router_gemm_breaks_exact_ties_by_index(oracle, N, k, mode):
+@pytest.mark.parametrize("N,k,mode,T", [(64, 8, 1, 300), (256, 8, 0, 300), (48, 5, 0, 300),
+                                        (8, 2, 0, 300), (8, 2, 0, 2500), (32, 6, 1, 2500)])
+def test_router_gemm_breaks_exact_ties_by_index(oracle, N, k, mode, T):
     """Small-integer x and W_r make every product and sum exact in fp32, so
     the scores computed on the tensor cores equal the oracle's bit for bit
     and tie often (many experts share a score); duplicated router rows and a
     selection bias on a 1/4 grid add exact key ties. Selection must keep the
     lower expert index on every tie, as the oracle does."""
-    T, d = 300, 256
+    d = 256
     g = torch.Generator().manual_seed(N * 31 + k)
     x = torch.randint(-2, 3, (T, d), generator=g).to(torch.bfloat16)
     base = torch.randint(-1, 2, (max(N // 4, 1), d), generator=g)

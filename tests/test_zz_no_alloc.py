@@ -81,3 +81,26 @@ def test_noalloc_router_rejects_calls_beyond_its_scratch():
         _p(o["w"]), _p(o["counts"]), _p(o["prob_sum"]), None)
     assert rc == moe.MOE_ERR_WORKSPACE
     assert moe.launch_count() == before
+
+
+@pytest.mark.parametrize("N,k,T_max", [(8, 2, 1048320), (32, 4, 262080), (256, 8, 32704)])
+def test_noalloc_router_limit_is_exact(N, k, T_max):
+    """The largest accepted batch matches the documented bound (256 + 8*B*N
+    bytes of the 1 MiB array): T_max runs, T_max + 1 is refused unlaunched.
+    Scores are given (logits_in), the path whose block count sets B."""
+    stream = torch.cuda.current_stream()
+    logits = torch.zeros((T_max + 1, N), device="cuda")
+    o = _outputs(T_max + 1, N, k)
+    for T, ok in ((T_max, True), (T_max + 1, False)):
+        cfg = moe.config(T=T, d_model=64, n_experts=N, top_k=k, d_ff=8)
+        before = moe.launch_count()
+        rc = moe.lib().moe_router_topk_noalloc(
+            ctypes.byref(cfg), None, None, None, None, _p(logits), None, _p(o["idx"]), _p(o["w"]),
+            _p(o["counts"]), _p(o["prob_sum"]), ctypes.c_void_p(stream.cuda_stream))
+        if ok:
+            assert rc == moe.MOE_OK
+            torch.cuda.synchronize()
+            assert int(o["counts"].sum().item()) == T * k
+        else:
+            assert rc == moe.MOE_ERR_WORKSPACE
+            assert moe.launch_count() == before
