@@ -12,8 +12,8 @@
 // with A = x_perm for routed experts and A = x for shared experts, w_row the
 // row's gate weight (1 for shared rows). This is the layer's main dense
 // contraction ("Mixture of experts and speculative decoding": an expert
-// costs about 2 flops per parameter); the router's score contraction is the
-// only other one (router_tc.cu, router_tc32.cu).
+// costs about 2 flops per parameter); the router's score contraction for
+// many experts is the only other one (router_tc.cu).
 //
 // Design (sm_103a, one CTA per SM, persistent):
 //  - Tiles: 128 rows of one segment x 256 accumulator columns. For gate/up

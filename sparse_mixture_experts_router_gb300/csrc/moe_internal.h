@@ -59,13 +59,6 @@ cudaError_t launch_router_tc(const moe_config& c, const void* x, const void* w_r
                              const float* logit_bias, const float* sel_bias, float* logits_out,
                              int32_t* topk_idx, float* topk_w, int32_t* counts, float* prob_sum,
                              float* partials, int32_t* cpart, int* status, cudaStream_t s);
-// Tensor-core router for 1 <= N <= 32 (router_tc32.cu): bf16, scores
-// computed; a cluster of router_tc32_cluster(c) CTAs per 128-token tile.
-cudaError_t launch_router_tc32(const moe_config& c, const void* x, const void* w_router,
-                               const float* logit_bias, const float* sel_bias, float* logits_out,
-                               int32_t* topk_idx, float* topk_w, int32_t* counts, float* prob_sum,
-                               float* partials, int32_t* cpart, int* status, cudaStream_t s);
-int router_tc32_cluster(const moe_config& c);
 // Zeroes the status word and the router's block counter (a kernel, so it
 // keeps the chain of programmatic dependent launches).
 cudaError_t launch_reset_status(int* status, cudaStream_t s);

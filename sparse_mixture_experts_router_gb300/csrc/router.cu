@@ -39,7 +39,6 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kTileTokens = 64;              // tokens per block, tiled kernel
 constexpr int kKC = 32;                      // K slice of the tiled kernel
 constexpr int kSmallMaxBlocks = 4 * 152;     // few-expert kernel: grid-stride beyond this
-constexpr int kTc32MinTokens = 2048;         // bf16, N <= 32: tensor-core router from here
 constexpr int kSmallTargetWarps = 2 * 152 * kWarps;  // few-expert kernel: warps to keep busy
 
 struct RouterArgs {
@@ -547,7 +546,7 @@ cudaError_t launch_dtype(const moe_config& c, const RouterArgs& a, int grid, cud
 
 // The most blocks any router kernel for this configuration launches: the
 // tiled kernel (given scores, or N > 32 in fp32) takes one per 64 tokens,
-// the tensor-core kernels one per 128, and for up to 32 experts the warp
+// the tensor-core kernel one per 128, and for up to 32 experts the warp
 // kernel at most min(T, kSmallMaxBlocks).
 int router_partial_blocks(const moe_config& c) {
   const int tiled = ceil_div(c.T, kTileTokens);
@@ -575,11 +574,6 @@ cudaError_t launch_router(const moe_config& c, const void* x, const void* w_rout
   }
   int32_t* cpart = reinterpret_cast<int32_t*>(partials) +
                    (size_t)router_partial_blocks(c) * (size_t)c.n_experts;
-  // Up to 32 experts the warp kernel has the lower fixed cost; from 2048
-  // tokens the tensor-core kernel streams x faster (measured crossover).
-  if (logits_in == nullptr && c.dtype == MOE_BF16 && c.n_experts <= 32 && c.T >= kTc32MinTokens)
-    return launch_router_tc32(c, x, w_router, logit_bias, sel_bias, logits_out, topk_idx, topk_w,
-                              counts, prob_sum, partials, cpart, status, s);
   if (router_tc_applies(c, logits_in))
     return launch_router_tc(c, x, w_router, logit_bias, sel_bias, logits_out, topk_idx, topk_w,
                             counts, prob_sum, partials, cpart, status, s);

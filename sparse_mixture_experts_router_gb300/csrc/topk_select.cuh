@@ -1,5 +1,4 @@
-// Top-k selection on packed 64-bit keys, shared by the tensor-core router
-// kernels: a key and its expert index become one word that orders by key
+// Top-k selection on packed 64-bit keys for the tensor-core router: a key and its expert index become one word that orders by key
 // and then by lower index, so a plain unsigned comparison decides both, and
 // small comparator networks keep the 8 largest words of a thread's scores.
 #pragma once

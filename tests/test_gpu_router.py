@@ -95,15 +95,13 @@ GEMM_CASES = [
     synth.Workload("r_tc_n200_many_tiles", T=4500, d_model=200, n_experts=200, top_k=6, d_ff=8,
                    zipf_s=1.2, seed=18),
     synth.DEEPSEEK_V3.replace(name="r_dsv3_full_size", d_ff=8),   # d_model = 7168
-    # bf16 with up to 32 experts: the tensor-core router split along d_model
-    # over a cluster of 4, 2 or 1 CTAs (partial scores added in rank order).
-    # (from 2048 tokens; fewer tokens take the warp kernel).
-    synth.Workload("r_tc32_cluster4", T=4000, d_model=4096, n_experts=8, top_k=2, d_ff=8, seed=19),
-    synth.Workload("r_tc32_n20_ragged", T=2049, d_model=520, n_experts=20, top_k=5, d_ff=8,
-                   gate_mode=1, sel_bias=True, zipf_s=1.2, seed=20),
-    synth.Workload("r_tc32_one_expert", T=2100, d_model=256, n_experts=1, top_k=1, d_ff=8, seed=21),
-    synth.Workload("r_tc32_cluster2", T=9000, d_model=256, n_experts=32, top_k=8, d_ff=8, seed=22),
-    synth.Workload("r_tc32_cluster1", T=19500, d_model=128, n_experts=16, top_k=4, d_ff=8, seed=23),
+    # bf16 with up to 32 experts: the warp kernel, one to eight warps per token group.
+    synth.Workload("r_warp_many_groups", T=4000, d_model=4096, n_experts=8, top_k=2, d_ff=8,
+                   seed=19),
+    synth.Workload("r_warp_one_expert", T=2100, d_model=256, n_experts=1, top_k=1, d_ff=8, seed=21),
+    synth.Workload("r_warp_n32", T=9000, d_model=256, n_experts=32, top_k=8, d_ff=8, seed=22),
+    synth.Workload("r_warp_n16_grid_stride", T=19500, d_model=128, n_experts=16, top_k=4, d_ff=8,
+                   seed=23),
     synth.Workload("r_warp_decode", T=1, d_model=4096, n_experts=8, top_k=2, d_ff=8, seed=24),
     synth.Workload("r_warp_n20", T=129, d_model=520, n_experts=20, top_k=5, d_ff=8,
                    gate_mode=1, sel_bias=True, zipf_s=1.2, seed=25),
