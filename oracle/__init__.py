@@ -55,12 +55,13 @@ def _declare(lib):
     lib.oracle_gates.argtypes = [_I, _I, _I, _P, _P, _P]
     lib.oracle_router_logits.argtypes = [_I, _I, _I, _I, _P, _I, _P, _P, _P, _P]
     lib.oracle_route.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P]
-    lib.oracle_permute.argtypes = [_I, _I, _I, _P, _P, _P, _P]
+    lib.oracle_capacity_keep.argtypes = [_I, _I, _I, _P, _I, _P]
+    lib.oracle_permute.argtypes = [_I, _I, _I, _P, _I, _P, _P, _P]
     lib.oracle_expert_swiglu.argtypes = [_I, _I, _I, _P, _P, _P, _P, _P]
     lib.oracle_gated_sum.argtypes = [_I, _I, _P, _P, _P]
     lib.oracle_layer_rows.restype = _I
     lib.oracle_layer_rows.argtypes = [_I, _I, _I, _I, _I, _I, _I, _P, _I,
-                                      _P, _P, _P, _P, _P, _I, _P, _P]
+                                      _P, _P, _P, _P, _P, _P, _I, _P, _P]
     lib.oracle_balance_loss.restype = ctypes.c_double
     lib.oracle_balance_loss.argtypes = [_I, _P, _P, ctypes.c_double]
     lib.oracle_balance_stats.restype = ctypes.c_double
@@ -163,15 +164,25 @@ class Oracle:
                               _ptr(w), _ptr(counts), _ptr(prob_sum))
         return idx, w, counts, prob_sum
 
-    def permute(self, topk_idx, N):
-        """(offsets [N+1], sorted_pair [T*k], inv_pos [T*k]) int32."""
+    def capacity_keep(self, topk_idx, N, capacity):
+        """keep [T*k] uint8: 1 for a pair its expert keeps under the capacity."""
+        topk_idx = _c(topk_idx, np.int32)
+        T, k = topk_idx.shape
+        keep = np.empty(T * k, np.uint8)
+        self.lib.oracle_capacity_keep(T, k, N, _ptr(topk_idx), int(capacity), _ptr(keep))
+        return keep
+
+    def permute(self, topk_idx, N, capacity=0):
+        """(offsets [N+1], sorted_pair [rows], inv_pos [T*k]) int32; rows =
+        offsets[N] kept pairs, inv_pos -1 for a dropped pair."""
         topk_idx = _c(topk_idx, np.int32)
         T, k = topk_idx.shape
         offsets = np.empty(N + 1, np.int32)
         sp = np.empty(T * k, np.int32)
         inv = np.empty(T * k, np.int32)
-        self.lib.oracle_permute(T, k, N, _ptr(topk_idx), _ptr(offsets), _ptr(sp), _ptr(inv))
-        return offsets, sp, inv
+        self.lib.oracle_permute(T, k, N, _ptr(topk_idx), int(capacity), _ptr(offsets), _ptr(sp),
+                                _ptr(inv))
+        return offsets, sp[:offsets[N]], inv
 
     def expert_swiglu(self, x_row, wg, wu, wd):
         wdt, wg = _stored(wg)
@@ -192,10 +203,12 @@ class Oracle:
         self.lib.oracle_gated_sum(G.size, E.shape[1], _ptr(G), _ptr(E), _ptr(y))
         return y
 
-    def layer_rows(self, x, experts, topk_idx, topk_w, rows, N, n_shared=0):
+    def layer_rows(self, x, experts, topk_idx, topk_w, rows, N, n_shared=0, keep=None):
         """y [len(rows), d] fp64 for the listed tokens. ``experts`` maps an
         expert index (0..N+n_shared-1; shared ones last) to its (wg, wu, wd)
-        stored arrays; experts no listed token uses may be absent."""
+        stored arrays; experts no listed token uses may be absent. ``keep``
+        ([T*k] uint8, from capacity_keep) marks the pairs that run; a dropped
+        pair adds nothing."""
         xd, x = _stored(x)
         T, d = x.shape
         topk_idx = _c(topk_idx, np.int32)
@@ -203,7 +216,7 @@ class Oracle:
         k = topk_idx.shape[1]
         rows = _c(rows, np.int32)
         E = N + n_shared
-        keep = []
+        refs = []  # the stored arrays, alive until the call returns
         tabs = [(_P * E)(), (_P * E)(), (_P * E)()]
         wdt = None
         d_ff = None
@@ -212,13 +225,14 @@ class Oracle:
                 dt, m = _stored(m)
                 wdt = dt if wdt is None else wdt
                 assert dt == wdt
-                keep.append(m)
+                refs.append(m)
                 tabs[j][e] = m.ctypes.data
             d_ff = mats[0].shape[0]
         y = np.empty((rows.size, d), np.float64)
+        keep = None if keep is None else _c(keep, np.uint8)
         rc = self.lib.oracle_layer_rows(T, d, d_ff, N, k, n_shared, xd, _ptr(x), wdt,
                                         tabs[0], tabs[1], tabs[2], _ptr(topk_idx),
-                                        _ptr(topk_w), rows.size, _ptr(rows), _ptr(y))
+                                        _ptr(topk_w), _ptr(keep), rows.size, _ptr(rows), _ptr(y))
         if rc != 0:
             raise ValueError("oracle_layer_rows: a token needs an expert that was not supplied")
         return y
@@ -260,20 +274,22 @@ class Oracle:
 
     # ---- composition: the full layer for a token subset ---------------------
     def layer(self, x, w_router, wg, wu, wd, k, gate_mode=GATE_TOPK_SOFTMAX,
-              logit_bias=None, sel_bias=None, n_shared=0, rows=None):
+              logit_bias=None, sel_bias=None, n_shared=0, rows=None, capacity=0):
         """Full forward: router scores for all tokens, routing for all tokens,
-        expert outputs for ``rows`` (all tokens when None). wg/wu/wd are the
-        stacked [N+n_shared, ...] stored arrays (or dicts expert -> array).
-        Returns a dict with r32, topk_idx, topk_w, counts, prob_sum, y."""
+        expert outputs for ``rows`` (all tokens when None), with an expert
+        capacity (0 = none). wg/wu/wd are the stacked [N+n_shared, ...]
+        stored arrays (or dicts expert -> array). Returns a dict with r32,
+        topk_idx, topk_w, counts, prob_sum, keep, y."""
         _, r32 = self.router_logits(x, w_router, logit_bias)
         idx, w, counts, prob_sum = self.route(r32, k, gate_mode, sel_bias)
         N = r32.shape[1]
         T = r32.shape[0]
+        keep = self.capacity_keep(idx, N, capacity)
         if rows is None:
             rows = np.arange(T, dtype=np.int32)
         rows = np.asarray(rows, np.int32)
         need = sorted(set(idx[rows].ravel().tolist()) | set(range(N, N + n_shared)))
         experts = {e: (wg[e], wu[e], wd[e]) for e in need}
-        y = self.layer_rows(x, experts, idx, w, rows, N, n_shared)
+        y = self.layer_rows(x, experts, idx, w, rows, N, n_shared, keep)
         return dict(r32=r32, topk_idx=idx, topk_w=w, counts=counts,
-                    prob_sum=prob_sum, y=y, rows=rows)
+                    prob_sum=prob_sum, keep=keep, y=y, rows=rows)

@@ -197,8 +197,33 @@ void oracle_route(int T, int N, int k, int gate_mode, const float* r32,
  * This is the data layout of the toy layer's per-expert dispatch loop
  * ([P1] "A toy MoE layer in PyTorch"; [P2] sparse MoE code): every token
  * that chose expert e, and only those, is processed by e. */
-void oracle_permute(int T, int k, int N, const int32_t* topk_idx,
+/* Expert capacity. [P1] "Keeping the experts busy": a system may cap the
+ * tokens one expert takes from a batch, and the extras are dropped. Reading:
+ * with capacity C > 0, expert e keeps the first C of the pairs that chose it
+ * in ascending pair order (token, then slot) and drops the rest; C = 0 sets
+ * no cap. keep[p] = 1 for a kept pair, 0 for a dropped one. */
+void oracle_capacity_keep(int T, int k, int N, const int32_t* topk_idx, int capacity,
+                          uint8_t* keep) {
+  for (int e = 0; e < N; ++e) {
+    int taken = 0;
+    for (int t = 0; t < T; ++t)
+      for (int s = 0; s < k; ++s)
+        if (topk_idx[(size_t)t * k + s] == e) {
+          keep[(size_t)t * k + s] = (capacity == 0 || taken < capacity) ? 1 : 0;
+          ++taken;
+        }
+  }
+}
+
+/* Rows grouped by expert, kept pairs only (capacity as in
+ * oracle_capacity_keep; 0 = none): offsets[e] is the first row of expert e,
+ * sorted_pair[row] the pair id t*k+s, inv_pos[pair] its row, or -1 for a
+ * dropped pair. [P1] "A toy MoE layer in PyTorch": each expert processes
+ * the tokens routed to it. */
+void oracle_permute(int T, int k, int N, const int32_t* topk_idx, int capacity,
                     int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos) {
+  uint8_t* keep = (uint8_t*)malloc((size_t)T * k + 1);
+  oracle_capacity_keep(T, k, N, topk_idx, capacity, keep);
   int32_t row = 0;
   for (int e = 0; e < N; ++e) {
     offsets[e] = row;
@@ -206,12 +231,17 @@ void oracle_permute(int T, int k, int N, const int32_t* topk_idx,
       for (int s = 0; s < k; ++s)
         if (topk_idx[(size_t)t * k + s] == e) {
           int32_t pair = t * k + s;
-          sorted_pair[row] = pair;
-          inv_pos[pair] = row;
-          ++row;
+          if (keep[pair]) {
+            sorted_pair[row] = pair;
+            inv_pos[pair] = row;
+            ++row;
+          } else {
+            inv_pos[pair] = -1;
+          }
         }
   }
   offsets[N] = row;
+  free(keep);
 }
 
 /* SiLU(z) = z / (1 + e^-z). */
@@ -267,14 +297,15 @@ int oracle_layer_rows(int T, int d, int d_ff, int N, int k, int n_shared,
                       int xdtype, const void* x, int wdtype,
                       const void* const* wg, const void* const* wu,
                       const void* const* wd, const int32_t* topk_idx,
-                      const double* topk_w, int n_rows, const int32_t* rows,
-                      double* y) {
+                      const double* topk_w, const uint8_t* keep, int n_rows,
+                      const int32_t* rows, double* y) {
   int bad = 0;
   for (int r = 0; r < n_rows; ++r) {
     int t = rows[r];
     if (t < 0 || t >= T) return -1;
     for (int s = 0; s < k; ++s) {
       int e = topk_idx[(size_t)t * k + s];
+      if (keep && !keep[(size_t)t * k + s]) continue;  /* dropped: not evaluated */
       if (e < 0 || e >= N || !wg[e] || !wu[e] || !wd[e]) bad = 1;
     }
   }
@@ -301,7 +332,13 @@ int oracle_layer_rows(int T, int d, int d_ff, int N, int k, int n_shared,
       e = N + (s - k);
       G[q] = 1.0;
     }
-    oracle_expert_swiglu(d, d_ff, wdtype, wg[e], wu[e], wd[e], xt, E + (size_t)q * d);
+    if (s < k && keep && !keep[(size_t)t * k + s]) {
+      /* a dropped pair contributes nothing ([P1] "Keeping the experts busy") */
+      G[q] = 0.0;
+      for (int c = 0; c < d; ++c) E[(size_t)q * d + c] = 0.0;
+    } else {
+      oracle_expert_swiglu(d, d_ff, wdtype, wg[e], wu[e], wd[e], xt, E + (size_t)q * d);
+    }
     free(xt);
   }
   for (int r = 0; r < n_rows; ++r)

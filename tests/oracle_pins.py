@@ -390,6 +390,56 @@ def pin_order_margin_is_min_pairwise_distance(o):
                 assert abs(got[t] - best) <= 1e-15, (T, N, k, t)
 
 
+def pin_capacity_hand_worked(o):
+    """Worked by hand, capacity 1 ("Keeping the experts busy": the extras
+    are dropped; the earlier tokens are kept). Pairs in order: p0 (token 0,
+    expert 0), p1 (0, 1), p2 (1, 1), p3 (1, 0), p4 (2, 0), p5 (2, 2). Expert
+    0 keeps p0 and drops p3, p4; expert 1 keeps p1 and drops p2; expert 2
+    keeps p5."""
+    idx = np.array([[0, 1], [1, 0], [0, 2]])
+    assert o.capacity_keep(idx, 3, 1).tolist() == [1, 1, 0, 0, 0, 1]
+    off, sp, inv = o.permute(idx, 3, capacity=1)
+    assert off.tolist() == [0, 1, 2, 3]
+    assert sp.tolist() == [0, 1, 5]
+    assert inv.tolist() == [0, 1, -1, -1, -1, 2]
+    # capacity 2: expert 0 keeps p0, p3 and drops p4
+    assert o.capacity_keep(idx, 3, 2).tolist() == [1, 1, 1, 1, 0, 1]
+    off, sp, inv = o.permute(idx, 3, capacity=2)
+    assert off.tolist() == [0, 2, 4, 5] and sp.tolist() == [0, 3, 1, 2, 5]
+    # 0 means no cap; a cap at the largest count drops nothing either
+    for cap in (0, 3):
+        assert o.capacity_keep(idx, 3, cap).all()
+
+
+def pin_capacity_layer_is_dense_with_dropped_gates_zeroed(o):
+    """Brute force: with a capacity, the layer equals the dense evaluation
+    of every expert on every token with the gate of each unselected or
+    dropped pair set to zero; with no capacity (or one no expert exceeds)
+    it equals the uncapped layer."""
+    rng = _rng(13)
+    T, d, dff, N, k = 9, 8, 6, 3, 2
+    x = rng.normal(0, 1, (T, d))
+    Wr = rng.normal(0, 1, (N, d))
+    wg = rng.normal(0, 0.5, (N, dff, d))
+    wu = rng.normal(0, 0.5, (N, dff, d))
+    wd = rng.normal(0, 0.5, (N, d, dff))
+    base = o.layer(x, Wr, wg, wu, wd, k)
+    for cap in (1, 2, 4):
+        out = o.layer(x, Wr, wg, wu, wd, k, capacity=cap)
+        keep = out["keep"].reshape(T, k)
+        for t in range(T):
+            ref = np.zeros(d)
+            for s in range(k):
+                if keep[t, s]:
+                    e = out["topk_idx"][t, s]
+                    ref += out["topk_w"][t, s] * _torch_swiglu(x[t:t + 1], wg[e], wu[e], wd[e]).numpy()[0]
+            assert np.allclose(out["y"][t], ref, atol=1e-12)
+        counts = np.bincount(out["topk_idx"].ravel(), minlength=N)
+        assert int(keep.sum()) == int(np.minimum(counts, cap).sum())
+    full = o.layer(x, Wr, wg, wu, wd, k, capacity=T)
+    assert np.array_equal(full["y"], base["y"])
+
+
 def pin_balance_stats_sum_to_one(o):
     rng = _rng(11)
     T, N, k = 64, 8, 2

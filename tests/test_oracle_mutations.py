@@ -27,7 +27,10 @@ MUTATIONS = [
     ("logit_bias_dropped", "if (logit_bias) acc += logit_bias[e];", ""),
     ("no_renormalisation", "g[s] = p[idx[s]] / z;", "g[s] = p[idx[s]];"),
     ("shared_expert_dropped", "G[q] = 1.0;", "G[q] = 0.0;"),
-    ("permute_descending_tokens", "for (int t = 0; t < T; ++t)\n      for (int s = 0; s < k; ++s)\n        if (topk_idx", "for (int t = T - 1; t >= 0; --t)\n      for (int s = 0; s < k; ++s)\n        if (topk_idx"),
+    ("permute_descending_tokens", "for (int t = 0; t < T; ++t)\n      for (int s = 0; s < k; ++s)\n        if (topk_idx[(size_t)t * k + s] == e) {\n          int32_t pair", "for (int t = T - 1; t >= 0; --t)\n      for (int s = 0; s < k; ++s)\n        if (topk_idx[(size_t)t * k + s] == e) {\n          int32_t pair"),
+    ("capacity_keeps_the_last_pairs", "for (int t = 0; t < T; ++t)\n      for (int s = 0; s < k; ++s)\n        if (topk_idx[(size_t)t * k + s] == e) {\n          keep", "for (int t = T - 1; t >= 0; --t)\n      for (int s = 0; s < k; ++s)\n        if (topk_idx[(size_t)t * k + s] == e) {\n          keep"),
+    ("capacity_off_by_one", "(capacity == 0 || taken < capacity)", "(capacity == 0 || taken <= capacity)"),
+    ("dropped_pair_still_runs", "if (s < k && keep && !keep[(size_t)t * k + s]) {", "if (0) {"),
     ("balance_loss_without_N", "return alpha * (double)N * s;", "return alpha * s;"),
     ("f_over_tokens_not_assignments", "f[i] = (double)counts[i] / ((double)T * (double)k);", "f[i] = (double)counts[i] / (double)T;"),
     ("gated_sum_transposed", "acc += G[i] * E[(size_t)i * dim + c];", "acc += G[i] * E[(size_t)c * n_terms + i];"),
