@@ -172,8 +172,21 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------- work accounting --
-def gemm_flops(w):
-    rows = w.T * w.top_k + w.n_shared * w.T
+def capacity_of(w):
+    if w.capacity_factor <= 0:
+        return 0
+    return max(1, math.ceil(w.capacity_factor * w.T * w.top_k / w.n_experts))
+
+
+def gemm_flops(w, counts=None):
+    """Algorithmic flops of the two grouped GEMMs: 4·d·d_ff and 2·d·d_ff per
+    row that runs (routed pairs kept by the capacity, plus T shared rows per
+    shared expert)."""
+    routed = w.T * w.top_k
+    cap = capacity_of(w)
+    if cap and counts is not None:
+        routed = sum(min(int(c), cap) for c in counts)
+    rows = routed + w.n_shared * w.T
     return 4.0 * rows * w.d_model * w.d_ff, 2.0 * rows * w.d_ff * w.d_model
 
 
@@ -200,7 +213,8 @@ def run_ours(args):
     w = WORKLOADS[args.workload](synth)
     inp = synth.make_inputs(w, dev, seed=w.seed + 1000 * rank)
     cfg = moe.config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k, d_ff=w.d_ff,
-                     n_shared=w.n_shared, dtype=moe.MOE_BF16, gate_mode=w.gate_mode)
+                     n_shared=w.n_shared, dtype=moe.MOE_BF16, gate_mode=w.gate_mode,
+                     capacity=capacity_of(w))
     y = torch.empty(w.T, w.d_model, dtype=torch.bfloat16, device=dev)
     idx = torch.empty(w.T, w.top_k, dtype=torch.int32, device=dev)
     tw = torch.empty(w.T, w.top_k, dtype=torch.float32, device=dev)
@@ -310,7 +324,7 @@ def run_ours(args):
     moe.profile_enable(False)
 
     # ---- roofline of the dominant kernel ---------------------------------------
-    f_gu, f_dn = gemm_flops(w)
+    f_gu, f_dn = gemm_flops(w, counts.cpu().tolist())
     per_kernel = {}
     for name, (ms, n) in kern.items():
         per_kernel[name] = {"ms_per_launch": ms / n, "launches": n,
@@ -357,6 +371,9 @@ def run_ours(args):
     wb = 3 * E * w.d_model * w.d_ff * 2
     routing = {"max_over_mean_expert_load": round(float(counts.max()) / max(1e-9, float(counts.float().mean())), 3),
                "experts_with_tokens": int((counts > 0).sum())}
+    if capacity_of(w):
+        routing["pairs_dropped_by_capacity"] = int(sum(max(0, int(c) - capacity_of(w))
+                                                       for c in counts.cpu().tolist()))
 
     if rank == 0:
         cpu = None if (args.no_cpu_baseline or not default) else cpu_baseline(inp, w, args)
@@ -371,6 +388,7 @@ def run_ours(args):
                        "gate": ["softmax over the kept top-k scores",
                                 "softmax over all scores, kept ones renormalised"][w.gate_mode],
                        "selection_bias": w.sel_bias, "zipf_offset_s": w.zipf_s or None,
+                       "capacity": capacity_of(w) or None,
                        "parallelism": f"replicas x{ws} (per-token layer, no collective)",
                        "l2": f"inputs larger than L2: {wb / 1e9:.2f} GB of expert weights read every step"},
             "routing": routing,
@@ -548,6 +566,7 @@ WORKLOADS = {
     "mixtral_8x7b_prefill": lambda synth: synth.MIXTRAL_PREFILL,
     "deepseek_v3_moe": lambda synth: synth.DEEPSEEK_V3,
     "zipf_imbalanced": lambda synth: synth.ZIPF,
+    "zipf_imbalanced_capacity": lambda synth: synth.ZIPF_CAPACITY,
     **{f"mixtral_8x7b_decode_T{t}": (lambda t_: lambda synth: [w for w in synth.MIXTRAL_DECODE if w.T == t_][0])(t)
        for t in (1, 8, 32, 64)},
 }

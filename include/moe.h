@@ -88,6 +88,14 @@ typedef struct moe_config {
   int32_t d_ff;      /* expert hidden width, >= 8, multiple of 8              */
   int32_t dtype;     /* moe_dtype                                             */
   int32_t gate_mode; /* moe_gate_mode                                         */
+  int32_t capacity;  /* expert capacity C, >= 0; 0 = no cap. With C > 0 each
+                      * routed expert runs at most the first C of its (token,
+                      * slot) pairs in ascending token order; the others are
+                      * dropped and add nothing to y ("Mixture of experts and
+                      * speculative decoding", "Keeping the experts busy": the
+                      * extras are dropped). Routing, counts and the balance
+                      * statistics are those before the cap; shared experts
+                      * are never capped.                                    */
 } moe_config;
 
 /* Library version (major*10000 + minor*100 + patch). */
@@ -185,11 +193,14 @@ MOE_API int moe_router_topk_noalloc(const moe_config* cfg, const void* x,
  *                 range sets MOE_ERR_DEVICE_CHECK in the workspace status;
  *                 that pair is then left out and the outputs are undefined.
  *  expert_offsets [device] [N+1] int32 out: exclusive prefix sum of the
- *                 per-expert pair counts; expert_offsets[N] = T*k.
- *  sorted_pair    [device] [T*k] int32 out: pair id stored at each row.
- *  inv_pos        [device] [T*k] int32 out: row of each pair id.
+ *                 per-expert rows, min(count, cfg->capacity) with a cap,
+ *                 else count; expert_offsets[N] = rows kept (T*k uncapped).
+ *  sorted_pair    [device] [T*k] int32 out: pair id stored at each row
+ *                 (rows past expert_offsets[N] are left as they were).
+ *  inv_pos        [device] [T*k] int32 out: row of each pair id, -1 for a
+ *                 pair dropped by the capacity.
  *  x_perm         [device] [T*k][d_model] cfg->dtype out: x_perm[row] =
- *                 x[sorted_pair[row] / k], byte for byte.
+ *                 x[sorted_pair[row] / k], byte for byte, for the kept rows.
  *  ws             [device] moe_permute_workspace_size(cfg) bytes.
  */
 MOE_API int moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,

@@ -39,15 +39,23 @@ class MoeError(RuntimeError):
 class moe_config(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d_model", ctypes.c_int32), ("n_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("d_ff", ctypes.c_int32),
-                ("dtype", ctypes.c_int32), ("gate_mode", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("gate_mode", ctypes.c_int32),
+                ("capacity", ctypes.c_int32)]
 
     def __repr__(self):
         return "moe_config(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
 
 
 def config(T, d_model, n_experts, top_k, d_ff, n_shared=0, dtype=MOE_BF16,
-           gate_mode=MOE_GATE_TOPK_SOFTMAX) -> moe_config:
-    return moe_config(T, d_model, n_experts, top_k, n_shared, d_ff, dtype, gate_mode)
+           gate_mode=MOE_GATE_TOPK_SOFTMAX, capacity=0) -> moe_config:
+    return moe_config(T, d_model, n_experts, top_k, n_shared, d_ff, dtype, gate_mode, capacity)
+
+
+def capacity_for(factor: float, T: int, top_k: int, n_experts: int) -> int:
+    """Expert capacity from a capacity factor: ceil(factor * T * k / N), the
+    even share of the T*k pairs times the factor (at least 1)."""
+    import math
+    return max(1, math.ceil(factor * T * top_k / n_experts))
 
 
 _P = ctypes.c_void_p

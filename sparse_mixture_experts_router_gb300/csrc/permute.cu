@@ -117,9 +117,12 @@ __global__ void __launch_bounds__(kThreads) permute_hist_kernel(const int32_t* _
   for (int e = threadIdx.x; e < N; e += kThreads) hist[(size_t)blockIdx.x * N + e] = sh[e];
 }
 
+// Per expert, the chunk counts become each chunk's first rank inside the
+// expert (exclusive scan over chunks); the experts' kept rows (count, or
+// min(count, capacity)) scanned over experts give expert_offsets.
 __global__ void __launch_bounds__(kThreads) permute_scan_kernel(int32_t* hist, int nchunks, int N,
-                                                                int32_t* offsets) {
-  extern __shared__ int tot[];
+                                                                int capacity, int32_t* offsets) {
+  extern __shared__ int tot[];  // [N + 1]
   pdl_wait();
   pdl_trigger();
   for (int e = threadIdx.x; e < N; e += kThreads) {
@@ -129,27 +132,21 @@ __global__ void __launch_bounds__(kThreads) permute_scan_kernel(int32_t* hist, i
       hist[(size_t)c * N + e] = run;
       run += v;
     }
-    tot[e] = run;
+    tot[e] = (capacity > 0 && run > capacity) ? capacity : run;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int e = 0; e < N; ++e) {
-      const int v = tot[e];
-      tot[e] = run;
-      offsets[e] = run;
-      run += v;
-    }
-    offsets[N] = run;
+  if (threadIdx.x < 32) {
+    const int total = warp_exclusive_scan(tot, N, threadIdx.x);
+    if (threadIdx.x == 0) tot[N] = total;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < N; e += kThreads)
-    for (int c = 0; c < nchunks; ++c) hist[(size_t)c * N + e] += tot[e];
+  for (int e = threadIdx.x; e <= N; e += kThreads) offsets[e] = tot[e];
 }
 
 __global__ void __launch_bounds__(kThreads) permute_rank_kernel(const int32_t* __restrict__ idx,
-                                                                int P, int N,
+                                                                int P, int N, int capacity,
                                                                 const int32_t* __restrict__ chunk_base,
+                                                                const int32_t* __restrict__ offsets,
                                                                 int32_t* sorted_pair,
                                                                 int32_t* inv_pos) {
   extern __shared__ int wh[];  // [kWarps][N]
@@ -189,9 +186,14 @@ __global__ void __launch_bounds__(kThreads) permute_rank_kernel(const int32_t* _
     const int e = ev[r];
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     if (e >= 0) {
-      const int pos = mine[e] + __popc(peers & lt);
-      sorted_pair[pos] = p;
-      inv_pos[p] = pos;
+      const int rank = mine[e] + __popc(peers & lt);  // among expert e's pairs
+      if (capacity == 0 || rank < capacity) {
+        const int pos = offsets[e] + rank;
+        sorted_pair[pos] = p;
+        inv_pos[p] = pos;
+      } else {
+        inv_pos[p] = -1;  // dropped by the capacity
+      }
     }
     __syncwarp();
     if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
@@ -202,13 +204,14 @@ __global__ void __launch_bounds__(kThreads) permute_rank_kernel(const int32_t* _
 // One warp per output row: x_perm[row] = x[sorted_pair[row] / k].
 __global__ void __launch_bounds__(kThreads) permute_gather_kernel(const uint4* __restrict__ x,
                                                                   const int32_t* __restrict__ sorted_pair,
-                                                                  int P, int k, int vec_per_row,
+                                                                  const int32_t* __restrict__ offsets,
+                                                                  int N, int P, int k, int vec_per_row,
                                                                   uint4* __restrict__ x_perm) {
   const int row = blockIdx.x * kWarps + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   pdl_wait();
   pdl_trigger();
-  if (row >= P) return;
+  if (row >= P || row >= offsets[N]) return;  // rows past the kept ones stay unwritten
   // Rows past the last valid pair stay unwritten when some expert index was
   // out of range (already reported in the status word); never read through
   // such a row.
@@ -228,12 +231,11 @@ __global__ void __launch_bounds__(kThreads) permute_gather_kernel(const uint4* _
 constexpr int kSmallThreads = 1024;
 constexpr int kSmallWarps = kSmallThreads / 32;
 __global__ void __launch_bounds__(kSmallThreads) permute_small_kernel(
-    const int32_t* __restrict__ idx, int P, int N, int k, const uint4* __restrict__ x,
-    int vec_per_row, uint4* __restrict__ x_perm, int32_t* offsets, int32_t* sorted_pair,
-    int32_t* inv_pos, int* status, int32_t* seg, int n_shared, int T, int tile_m) {
-  (void)x; (void)vec_per_row; (void)x_perm; (void)k;
+    const int32_t* __restrict__ idx, int P, int N, int capacity, int32_t* offsets,
+    int32_t* sorted_pair, int32_t* inv_pos, int* status, int32_t* seg, int n_shared, int T,
+    int tile_m) {
   extern __shared__ int sh[];
-  int* wh = sh;                        // [kSmallWarps][N] counts, then row bases
+  int* wh = sh;                        // [kSmallWarps][N] counts, then rank bases
   int* soff = sh + kSmallWarps * N;    // [N+1] offsets
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   pdl_wait();
@@ -261,7 +263,7 @@ __global__ void __launch_bounds__(kSmallThreads) permute_small_kernel(
   for (int e = threadIdx.x; e < N; e += kSmallThreads) {
     int tot = 0;
     for (int w = 0; w < kSmallWarps; ++w) tot += wh[w * N + e];
-    soff[e] = tot;
+    soff[e] = (capacity > 0 && tot > capacity) ? capacity : tot;  // rows kept
   }
   __syncthreads();
   if (warp == 0) {
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(kSmallThreads) permute_small_kernel(
   __syncthreads();
   for (int e = threadIdx.x; e <= N; e += kSmallThreads) offsets[e] = soff[e];
   for (int e = threadIdx.x; e < N; e += kSmallThreads) {
-    int base = soff[e];
+    int base = 0;
     for (int w = 0; w < kSmallWarps; ++w) {
       const int v = wh[w * N + e];
       wh[w * N + e] = base;
@@ -286,9 +288,14 @@ __global__ void __launch_bounds__(kSmallThreads) permute_small_kernel(
     if (e >= N) e = -1;
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     if (e >= 0) {
-      const int pos = mine[e] + __popc(peers & lt);
-      sorted_pair[pos] = p;
-      inv_pos[p] = pos;
+      const int rank = mine[e] + __popc(peers & lt);  // among expert e's pairs
+      if (capacity == 0 || rank < capacity) {
+        const int pos = soff[e] + rank;
+        sorted_pair[pos] = p;
+        inv_pos[p] = pos;
+      } else {
+        inv_pos[p] = -1;  // dropped by the capacity
+      }
     }
     __syncwarp();
     if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
@@ -314,7 +321,8 @@ constexpr int kGroupBlocks = 16;
 constexpr int kGroupBatch = 8;  // rounds of 32 pairs loaded ahead
 __global__ void __launch_bounds__(kGroupThreads) permute_group_kernel(
     const int32_t* __restrict__ idx, const int32_t* __restrict__ counts, int P, int N, int epb,
-    int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos, int* status, int32_t* seg,
+    int capacity, int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos, int* status,
+    int32_t* seg,
     int n_shared, int T, int tile_m) {
   extern __shared__ int sh[];
   int* s_off = sh;                      // [N + 1] totals, then offsets
@@ -354,10 +362,19 @@ __global__ void __launch_bounds__(kGroupThreads) permute_group_kernel(
     __syncthreads();
   }
   if (warp == 0) {
+    // the routed pairs must add up to T*k; then each expert keeps at most
+    // `capacity` rows
+    int routed = 0;
+    for (int e = lane; e < N; e += 32) {
+      routed += s_off[e];
+      if (capacity > 0 && s_off[e] > capacity) s_off[e] = capacity;
+    }
+    for (int o = 16; o > 0; o >>= 1) routed += __shfl_xor_sync(0xffffffffu, routed, o);
+    __syncwarp();
     const int total = warp_exclusive_scan(s_off, N, lane);
     if (lane == 0) {
       s_off[N] = total;
-      if (counts != nullptr && total != P) set_status(status, MOE_ERR_DEVICE_CHECK);
+      if (counts != nullptr && routed != P) set_status(status, MOE_ERR_DEVICE_CHECK);
     }
   }
   __syncthreads();
@@ -385,7 +402,7 @@ __global__ void __launch_bounds__(kGroupThreads) permute_group_kernel(
   }
   __syncthreads();
   for (int j = threadIdx.x; j < e_hi - e_lo; j += kGroupThreads) {
-    int acc = s_off[e_lo + j];
+    int acc = 0;  // rank bases inside the expert
     for (int w = 0; w < kGroupWarps; ++w) {
       const int v = s_wc[w * epb + j];
       s_wc[w * epb + j] = acc;
@@ -409,9 +426,14 @@ __global__ void __launch_bounds__(kGroupThreads) permute_group_kernel(
       const bool own = e >= e_lo && e < e_hi;
       const uint32_t peers = __match_any_sync(0xffffffffu, own ? e : -1);
       if (own) {
-        const int pos = mine[e - e_lo] + __popc(peers & lt);
-        sorted_pair[pos] = p;
-        inv_pos[p] = pos;
+        const int rank = mine[e - e_lo] + __popc(peers & lt);  // among expert e's pairs
+        if (capacity == 0 || rank < capacity) {
+          const int pos = s_off[e] + rank;
+          sorted_pair[pos] = p;
+          inv_pos[p] = pos;
+        } else {
+          inv_pos[p] = -1;  // dropped by the capacity
+        }
       }
       __syncwarp();
       if (own && lane == __ffs(peers) - 1) mine[e - e_lo] += __popc(peers);
@@ -465,24 +487,26 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
                            int32_t* seg, int tile_m, cudaStream_t s) {
   const int N = c.n_experts;
   const int P = c.T * c.top_k;
+  const int cap = c.capacity;
   if (P == 0) return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (N + 1), s);
+  const int vec = (int)(c.d_model * elem_bytes(c.dtype) / 16);
+  auto gather = [&]() {
+    ProfScope p(K_PERMUTE_GATHER, s);
+    return launch_pdl(permute_gather_kernel, dim3(ceil_div(P, kWarps)), dim3(kThreads), 0, s, 1,
+                      static_cast<const uint4*>(x), (const int32_t*)sorted_pair,
+                      (const int32_t*)offsets, N, P, c.top_k, vec, static_cast<uint4*>(x_perm));
+  };
   if (P <= kChunk) {
-    const int vec = (int)(c.d_model * elem_bytes(c.dtype) / 16);
     const size_t smem = sizeof(int) * ((size_t)kSmallWarps * N + N + 1);
     {
       ProfScope p(K_PERMUTE_SMALL, s);
       cudaError_t e = launch_pdl(permute_small_kernel, dim3(1), dim3(kSmallThreads), smem, s, 1,
-                                 topk_idx, P, N, c.top_k, static_cast<const uint4*>(x), vec,
-                                 static_cast<uint4*>(x_perm), offsets, sorted_pair, inv_pos, status,
-                                 seg, c.n_shared, c.T, tile_m);
+                                 topk_idx, P, N, cap, offsets, sorted_pair, inv_pos, status, seg,
+                                 c.n_shared, c.T, tile_m);
       if (e != cudaSuccess) return e;
     }
-    ProfScope p(K_PERMUTE_GATHER, s);
-    return launch_pdl(permute_gather_kernel, dim3(ceil_div(P, kWarps)), dim3(kThreads), 0, s, 1,
-                      static_cast<const uint4*>(x), sorted_pair, P, c.top_k, vec,
-                      static_cast<uint4*>(x_perm));
+    return gather();
   }
-  const int vec = (int)(c.d_model * elem_bytes(c.dtype) / 16);
   if (P <= kGroupMaxPairs) {
     const int groups = N < kGroupBlocks ? N : kGroupBlocks;
     const int epb = ceil_div(N, groups);
@@ -491,14 +515,11 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
     {
       ProfScope p(K_PERMUTE_GROUP, s);
       cudaError_t e = launch_pdl(permute_group_kernel, dim3(ceil_div(N, epb)), dim3(kGroupThreads),
-                                 smem, s, 1, topk_idx, counts, P, N, epb, offsets, sorted_pair,
+                                 smem, s, 1, topk_idx, counts, P, N, epb, cap, offsets, sorted_pair,
                                  inv_pos, status, seg, c.n_shared, c.T, tile_m);
       if (e != cudaSuccess) return e;
     }
-    ProfScope p(K_PERMUTE_GATHER, s);
-    return launch_pdl(permute_gather_kernel, dim3(ceil_div(P, kWarps)), dim3(kThreads), 0, s, 1,
-                      static_cast<const uint4*>(x), (const int32_t*)sorted_pair, P, c.top_k, vec,
-                      static_cast<uint4*>(x_perm));
+    return gather();
   }
   const int nch = ceil_div(P, kChunk);
   cudaError_t e;
@@ -510,22 +531,18 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
   }
   {
     ProfScope p(K_PERMUTE_SCAN, s);
-    e = launch_pdl(permute_scan_kernel, dim3(1), dim3(kThreads), sizeof(int) * N, s, 1, chunk_hist,
-                   nch, N, offsets);
+    e = launch_pdl(permute_scan_kernel, dim3(1), dim3(kThreads), sizeof(int) * (N + 1), s, 1,
+                   chunk_hist, nch, N, cap, offsets);
     if (e != cudaSuccess) return e;
   }
   {
     ProfScope p(K_PERMUTE_RANK, s);
     e = launch_pdl(permute_rank_kernel, dim3(nch), dim3(kThreads), sizeof(int) * kWarps * N, s, 1,
-                   topk_idx, P, N, (const int32_t*)chunk_hist, sorted_pair, inv_pos);
+                   topk_idx, P, N, cap, (const int32_t*)chunk_hist, (const int32_t*)offsets,
+                   sorted_pair, inv_pos);
     if (e != cudaSuccess) return e;
   }
-  {
-    ProfScope p(K_PERMUTE_GATHER, s);
-    e = launch_pdl(permute_gather_kernel, dim3(ceil_div(P, kWarps)), dim3(kThreads), 0, s, 1,
-                   static_cast<const uint4*>(x), (const int32_t*)sorted_pair, P, c.top_k, vec,
-                   static_cast<uint4*>(x_perm));
-  }
+  e = gather();
   if (e != cudaSuccess || seg == nullptr) return e;
   return launch_seg_table(c, offsets, seg, tile_m, status, s);
 }

@@ -32,6 +32,7 @@ class Workload:
     sel_bias: bool = False         # per-expert selection bias ~ U(-0.1, 0.1)
     zipf_s: float = 0.0            # > 0: per-expert Zipf score offset
     seed: int = 0
+    capacity_factor: float = 0.0   # > 0: expert capacity ceil(factor * T * k / N)
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -55,7 +56,10 @@ DEEPSEEK_V3 = Workload("deepseek_v3_moe", T=8192, d_model=7168, n_experts=256, t
                        n_shared=1, gate_mode=1, sel_bias=True, seed=3)
 ZIPF = Workload("zipf_imbalanced", T=16384, d_model=4096, n_experts=128, top_k=8, d_ff=1536,
                 zipf_s=1.2, seed=4)
-ALL = [TINY, MIXTRAL_PREFILL, *MIXTRAL_DECODE, DEEPSEEK_V3, ZIPF]
+# The imbalanced layer with an expert capacity of 1.25x the even share: the
+# hot experts keep their first 1280 pairs and drop the rest.
+ZIPF_CAPACITY = ZIPF.replace(name="zipf_imbalanced_capacity_1.25", capacity_factor=1.25)
+ALL = [TINY, MIXTRAL_PREFILL, *MIXTRAL_DECODE, DEEPSEEK_V3, ZIPF, ZIPF_CAPACITY]
 
 
 def _gen(device, seed):

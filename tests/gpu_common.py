@@ -27,11 +27,16 @@ SCORE_TOL = 1e-4
 GATE_TOL = SCORE_TOL / 2
 
 
+def capacity_of(w: synth.Workload) -> int:
+    return moe.capacity_for(w.capacity_factor, w.T, w.top_k, w.n_experts) \
+        if w.capacity_factor > 0 else 0
+
+
 def cfg_of(w: synth.Workload) -> moe.moe_config:
     return moe.config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k,
                       d_ff=w.d_ff, n_shared=w.n_shared,
                       dtype=moe.MOE_BF16 if w.dtype == "bf16" else moe.MOE_F32,
-                      gate_mode=w.gate_mode)
+                      gate_mode=w.gate_mode, capacity=capacity_of(w))
 
 
 def host(t):
@@ -77,6 +82,7 @@ def oracle_rows(oracle, w, inp, idx, tw, rows, max_experts=40):
     the experts those tokens use, a batch of tokens at a time."""
     rows = [int(r) for r in rows]
     xh = host(inp["x"])
+    keep = oracle.capacity_keep(idx, w.n_experts, capacity_of(w))
     out = np.empty((len(rows), w.d_model), np.float64)
     shared = list(range(w.n_experts, w.n_experts + w.n_shared))
     i = 0
@@ -91,7 +97,7 @@ def oracle_rows(oracle, w, inp, idx, tw, rows, max_experts=40):
             i += 1
         experts = {e: (host(inp["w_gate"][e]), host(inp["w_up"][e]), host(inp["w_down"][e]))
                    for e in sorted(need)}
-        y = oracle.layer_rows(xh, experts, idx, tw, batch, w.n_experts, w.n_shared)
+        y = oracle.layer_rows(xh, experts, idx, tw, batch, w.n_experts, w.n_shared, keep)
         out[i - len(batch):i] = y
     return out
 

@@ -61,6 +61,8 @@ def cfg(**kw):
     ({"d_model": 60}, moe.MOE_ERR_UNSUPPORTED),
     ({"d_ff": 100}, moe.MOE_ERR_UNSUPPORTED),
     ({"T": 1 << 28, "top_k": 4}, moe.MOE_ERR_UNSUPPORTED),
+    ({"capacity": 1}, moe.MOE_OK),
+    ({"capacity": -1}, moe.MOE_ERR_INVALID_ARG),
 ])
 def test_check_config(lib, kw, rc):
     assert moe.check_config(cfg(**kw)) == rc
@@ -149,3 +151,10 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(moe, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         moe.lib()
+
+
+def test_capacity_for():
+    """ceil(factor * T * k / N), at least 1."""
+    assert moe.capacity_for(1.25, 16384, 8, 128) == 1280
+    assert moe.capacity_for(1.0, 10, 1, 3) == 4
+    assert moe.capacity_for(0.01, 4, 1, 8) == 1

@@ -29,6 +29,16 @@ SMALL = [
     synth.Workload("decode_small", T=3, d_model=512, n_experts=8, top_k=2, d_ff=512, seed=24),
     synth.Workload("f32_shared", T=100, d_model=48, n_experts=6, top_k=3, d_ff=64, n_shared=2,
                    dtype="f32", gate_mode=1, sel_bias=True, seed=25),
+    # expert capacity: hot experts drop their later pairs
+    synth.Workload("zipf_small_capacity", T=1024, d_model=256, n_experts=128, top_k=8, d_ff=128,
+                   zipf_s=1.2, capacity_factor=1.0, seed=26),
+    synth.Workload("mix_small_capacity", T=512, d_model=512, n_experts=8, top_k=2, d_ff=1024,
+                   capacity_factor=0.75, seed=27),
+    synth.Workload("dsv3_small_capacity_shared", T=256, d_model=256, n_experts=64, top_k=8,
+                   d_ff=256, n_shared=1, gate_mode=1, sel_bias=True, capacity_factor=0.5,
+                   seed=28),
+    synth.Workload("f32_capacity", T=100, d_model=48, n_experts=6, top_k=3, d_ff=64, n_shared=1,
+                   dtype="f32", capacity_factor=0.6, seed=29),
 ]
 
 
@@ -73,7 +83,8 @@ def test_layer_empty_batch():
     assert run.counts.cpu().tolist() == [0] * w.n_experts
 
 
-FULL = [synth.MIXTRAL_PREFILL, *synth.MIXTRAL_DECODE, synth.DEEPSEEK_V3, synth.ZIPF]
+FULL = [synth.MIXTRAL_PREFILL, *synth.MIXTRAL_DECODE, synth.DEEPSEEK_V3, synth.ZIPF,
+        synth.ZIPF_CAPACITY]
 
 
 @pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)

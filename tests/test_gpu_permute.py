@@ -18,7 +18,7 @@ def random_idx(T, N, k, seed, skew=0.0):
         if T else np.zeros((0, k), np.int32)
 
 
-def run_permute(cfg, x, idx):
+def run_permute(cfg, x, idx):  # noqa: D103
     T, k, d = cfg.T, cfg.top_k, cfg.d_model
     P = T * k
     dev = "cuda"
@@ -61,6 +61,35 @@ def test_permute_is_bit_exact(oracle, T, N, k, d, dtype, skew):
     ref_rows = x[torch.from_numpy(r_sp // k).long().cuda()]
     assert torch.equal(xp.view(torch.int16) if tdt == torch.bfloat16 else xp.view(torch.int32),
                        ref_rows.view(torch.int16) if tdt == torch.bfloat16 else ref_rows.view(torch.int32))
+
+
+CAPACITY_CASES = [
+    # T, N, k, capacity, skew: one case per launch shape (one block, expert
+    # groups, chunks); the skew makes hot experts overflow
+    (100, 8, 2, 10, 1.5),
+    (3000, 128, 8, 150, 1.2),
+    (9000, 64, 8, 900, 0.8),
+    (500, 4, 2, 1, 0.0),       # one row per expert
+]
+
+
+@pytest.mark.parametrize("T,N,k,cap,skew", CAPACITY_CASES)
+def test_permute_with_capacity_is_bit_exact(oracle, T, N, k, cap, skew):
+    """Each expert keeps its first `cap` pairs in ascending token order; the
+    rest get inv_pos = -1 and no row."""
+    idx = random_idx(T, N, k, seed=T + N + cap, skew=skew)
+    x = torch.randn(T, 32, device="cuda").to(torch.bfloat16)
+    cfg = moe.config(T=T, d_model=32, n_experts=N, top_k=k, d_ff=8, capacity=cap)
+    off, sp, inv, xp, st = run_permute(cfg, x, torch.from_numpy(idx).cuda())
+    assert st == 0
+    r_off, r_sp, r_inv = oracle.permute(idx, N, capacity=cap)
+    assert np.array_equal(off.cpu().numpy(), r_off)
+    rows = int(r_off[-1])
+    assert rows < T * k  # something was dropped
+    assert np.array_equal(sp.cpu().numpy()[:rows], r_sp)
+    assert np.array_equal(inv.cpu().numpy(), r_inv)
+    assert torch.equal(xp[:rows].view(torch.int16),
+                       x[torch.from_numpy(r_sp // k).long().cuda()].view(torch.int16))
 
 
 def test_all_tokens_to_one_expert(oracle):
