@@ -61,7 +61,14 @@ def _declare(lib):
     lib.oracle_gated_sum.argtypes = [_I, _I, _P, _P, _P]
     lib.oracle_layer_rows.restype = _I
     lib.oracle_layer_rows.argtypes = [_I, _I, _I, _I, _I, _I, _I, _P, _I,
-                                      _P, _P, _P, _P, _P, _P, _I, _P, _P]
+                                      _P, _P, _P, _P, _P, _P, _I, _I, _P, _P]
+    lib.oracle_e4m3_decode.restype = ctypes.c_double
+    lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.oracle_e4m3_encode_scan.restype = ctypes.c_uint8
+    lib.oracle_e4m3_encode_scan.argtypes = [ctypes.c_float]
+    lib.oracle_quantize_rows_e4m3.argtypes = [_I, _I, _I, _P, _P, _P]
     lib.oracle_balance_loss.restype = ctypes.c_double
     lib.oracle_balance_loss.argtypes = [_I, _P, _P, ctypes.c_double]
     lib.oracle_balance_stats.restype = ctypes.c_double
@@ -203,12 +210,31 @@ class Oracle:
         self.lib.oracle_gated_sum(G.size, E.shape[1], _ptr(G), _ptr(E), _ptr(y))
         return y
 
-    def layer_rows(self, x, experts, topk_idx, topk_w, rows, N, n_shared=0, keep=None):
+    def e4m3_decode(self, code):
+        return float(self.lib.oracle_e4m3_decode(int(code)))
+
+    def e4m3_encode(self, v, scan=False):
+        f = self.lib.oracle_e4m3_encode_scan if scan else self.lib.oracle_e4m3_encode
+        return int(f(float(v)))
+
+    def quantize_rows_e4m3(self, m):
+        """(codes [rows, cols] uint8, scales [rows] fp32) of a stored matrix:
+        one scale fp32(amax/448) per row, codes E4M3(fp32(v/scale))."""
+        dt, m = _stored(m)
+        rows, cols = m.shape
+        q = np.empty((rows, cols), np.uint8)
+        sc = np.empty(rows, np.float32)
+        self.lib.oracle_quantize_rows_e4m3(rows, cols, dt, _ptr(m), _ptr(q), _ptr(sc))
+        return q, sc
+
+    def layer_rows(self, x, experts, topk_idx, topk_w, rows, N, n_shared=0, keep=None,
+                   fp8=False):
         """y [len(rows), d] fp64 for the listed tokens. ``experts`` maps an
         expert index (0..N+n_shared-1; shared ones last) to its (wg, wu, wd)
         stored arrays; experts no listed token uses may be absent. ``keep``
         ([T*k] uint8, from capacity_keep) marks the pairs that run; a dropped
-        pair adds nothing."""
+        pair adds nothing. ``fp8`` evaluates the experts in E4M3 with row
+        scales (tokens, weight output channels and H rows quantized)."""
         xd, x = _stored(x)
         T, d = x.shape
         topk_idx = _c(topk_idx, np.int32)
@@ -232,7 +258,8 @@ class Oracle:
         keep = None if keep is None else _c(keep, np.uint8)
         rc = self.lib.oracle_layer_rows(T, d, d_ff, N, k, n_shared, xd, _ptr(x), wdt,
                                         tabs[0], tabs[1], tabs[2], _ptr(topk_idx),
-                                        _ptr(topk_w), _ptr(keep), rows.size, _ptr(rows), _ptr(y))
+                                        _ptr(topk_w), _ptr(keep), int(bool(fp8)), rows.size,
+                                        _ptr(rows), _ptr(y))
         if rc != 0:
             raise ValueError("oracle_layer_rows: a token needs an expert that was not supplied")
         return y
@@ -274,7 +301,7 @@ class Oracle:
 
     # ---- composition: the full layer for a token subset ---------------------
     def layer(self, x, w_router, wg, wu, wd, k, gate_mode=GATE_TOPK_SOFTMAX,
-              logit_bias=None, sel_bias=None, n_shared=0, rows=None, capacity=0):
+              logit_bias=None, sel_bias=None, n_shared=0, rows=None, capacity=0, fp8=False):
         """Full forward: router scores for all tokens, routing for all tokens,
         expert outputs for ``rows`` (all tokens when None), with an expert
         capacity (0 = none). wg/wu/wd are the stacked [N+n_shared, ...]
@@ -290,6 +317,6 @@ class Oracle:
         rows = np.asarray(rows, np.int32)
         need = sorted(set(idx[rows].ravel().tolist()) | set(range(N, N + n_shared)))
         experts = {e: (wg[e], wu[e], wd[e]) for e in need}
-        y = self.layer_rows(x, experts, idx, w, rows, N, n_shared, keep)
+        y = self.layer_rows(x, experts, idx, w, rows, N, n_shared, keep, fp8)
         return dict(r32=r32, topk_idx=idx, topk_w=w, counts=counts,
                     prob_sum=prob_sum, keep=keep, y=y, rows=rows)

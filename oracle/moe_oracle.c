@@ -26,7 +26,9 @@
  *       auxiliary-loss formula with its balanced / collapsed example.
  *  [P3] "MoE inference: the call centre with 256 specialists and 8 taking
  *       each call": "The bare mechanism" (router, top-k, normalised weights,
- *       SwiGLU experts, shared experts, bias-adjusted routing).
+ *       SwiGLU experts, shared experts, bias-adjusted routing); "The maths
+ *       that matters" and "DeepEP, EPLB and Wide-EP" (experts stored and
+ *       tokens dispatched in FP8).
  *
  * Readings taken where the pages are silent or garbled:
  *  - The SwiGLU expert is down( SiLU(gate(x)) * up(x) ) without biases; the
@@ -65,6 +67,92 @@ static double widen(int dtype, const void* base, size_t i) {
   float f;
   memcpy(&f, &u, sizeof f);
   return (double)f;
+}
+
+/* ---------------------------------------------------------------- FP8 ----
+ * [P3] "The maths that matters" and "DeepEP, EPLB and Wide-EP": deployed
+ * experts are stored, and tokens dispatched, in FP8. The 8-bit format is
+ * E4M3: sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0
+ * holds the subnormals m * 2^-9; the largest finite value is 448 (field 15,
+ * mantissa 6); field 15 with mantissa 7 is NaN; there is no infinity.
+ * Reading (the pages give no scaling rule): each row (a token's activations,
+ * or one output channel of a weight matrix) carries one fp32 scale
+ * s = fp32(amax / 448) and codes q_i = E4M3(fp32(v_i / s)), rounded to
+ * nearest even and saturated at +-448; a row of zeros has s = 0 and codes 0.
+ * The value of a code is decode(q) * s. */
+double oracle_e4m3_decode(uint8_t c) {
+  const int e = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m, -9);
+  else
+    v = ldexp(1.0 + m / 8.0, e - 7);
+  return (c & 0x80) ? -v : v;
+}
+
+/* Definition form of the encoder: the finite code nearest to v, ties to the
+ * even code (mantissa bit 0 clear), |v| past 448 saturated to 448. Slow
+ * (scans the 127 magnitudes); used to pin the direct encoder below. */
+uint8_t oracle_e4m3_encode_scan(float v) {
+  if (isnan(v)) return 0x7F;
+  const uint8_t sign = signbit(v) ? 0x80 : 0;
+  const double a = fabs((double)v);
+  int best = 0;
+  double bd = INFINITY;
+  for (int c = 0; c <= 0x7E; ++c) {
+    const double d = fabs(a - oracle_e4m3_decode((uint8_t)c));
+    if (d < bd || (d == bd && (c & 1) == 0)) {
+      bd = d;
+      best = c;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+/* Direct encoder, the same function: split |v| into exponent and mantissa
+ * and round the 3-bit mantissa (or the subnormal step count) to nearest
+ * even with rint (default rounding mode); a mantissa that rounds up to 8
+ * carries into the exponent. */
+uint8_t oracle_e4m3_encode(float v) {
+  if (isnan(v)) return 0x7F;
+  const uint8_t sign = signbit(v) ? 0x80 : 0;
+  const double a = fabs((double)v);
+  if (a >= 448.0) return sign | 0x7E;
+  if (a < ldexp(1.0, -6)) {                 /* subnormal range: steps of 2^-9 */
+    const int m = (int)rint(ldexp(a, 9));   /* 0..8; 8 is the smallest normal */
+    return (uint8_t)(sign | m);
+  }
+  int x;
+  const double f = frexp(a, &x);            /* a = f * 2^x, f in [0.5, 1) */
+  int E = x - 1;                            /* a = (2f) * 2^E, 2f in [1, 2) */
+  int m = (int)rint((2.0 * f - 1.0) * 8.0);
+  if (m == 8) {
+    m = 0;
+    ++E;
+  }
+  if (E + 7 > 15 || (E + 7 == 15 && m == 7)) return sign | 0x7E;
+  return (uint8_t)(sign | ((E + 7) << 3) | m);
+}
+
+/* Row-wise quantization of a rows x cols matrix of stored values (see the
+ * FP8 note above): scale[r] = fp32(amax_r / 448), q = E4M3(fp32(v / scale)). */
+void oracle_quantize_rows_e4m3(int rows, int cols, int dtype, const void* src, uint8_t* q,
+                               float* scale) {
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < rows; ++r) {
+    float amax = 0.0f;
+    for (int c = 0; c < cols; ++c) {
+      const float v = (float)widen(dtype, src, (size_t)r * cols + c);
+      if (fabsf(v) > amax) amax = fabsf(v);
+    }
+    const float s = amax / 448.0f;
+    scale[r] = s;
+    for (int c = 0; c < cols; ++c) {
+      const float v = (float)widen(dtype, src, (size_t)r * cols + c);
+      q[(size_t)r * cols + c] = s == 0.0f ? 0 : oracle_e4m3_encode(v / s);
+    }
+  }
 }
 
 int oracle_num_threads(void) {
@@ -247,6 +335,51 @@ void oracle_permute(int T, int k, int N, const int32_t* topk_idx, int capacity,
 /* SiLU(z) = z / (1 + e^-z). */
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
+/* fp32 value rounded to bf16 (nearest even), as the GPU stores H. */
+static float round_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7F800000u) != 0x7F800000u) u = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* An expert's three weight matrices in E4M3, one scale per output row. */
+typedef struct {
+  uint8_t *gq, *uq, *dq;
+  float *gs, *us, *ds;
+} QExpert;
+
+/* One SwiGLU expert on one token row in FP8 (see the FP8 note): x is the
+ * token's dequantized row; every weight is dequantized from its code and its
+ * row scale; H is rounded to bf16, quantized as one row, and dequantized
+ * before the down projection. */
+static void expert_swiglu_fp8(int d, int d_ff, const QExpert* q, const double* x, double* out) {
+  float* h = (float*)malloc(sizeof(float) * (size_t)d_ff);
+  for (int j = 0; j < d_ff; ++j) {
+    double a = 0.0, b = 0.0;
+    for (int i = 0; i < d; ++i) {
+      a += oracle_e4m3_decode(q->gq[(size_t)j * d + i]) * x[i];
+      b += oracle_e4m3_decode(q->uq[(size_t)j * d + i]) * x[i];
+    }
+    a *= (double)q->gs[j];
+    b *= (double)q->us[j];
+    h[j] = round_bf16((float)(silu(a) * b));
+  }
+  uint8_t* hq = (uint8_t*)malloc((size_t)d_ff);
+  float hs;
+  oracle_quantize_rows_e4m3(1, d_ff, ORACLE_F32, h, hq, &hs);
+  for (int c = 0; c < d; ++c) {
+    double acc = 0.0;
+    for (int j = 0; j < d_ff; ++j)
+      acc += oracle_e4m3_decode(q->dq[(size_t)c * d_ff + j]) *
+             (oracle_e4m3_decode(hq[j]) * (double)hs);
+    out[c] = acc * (double)q->ds[c];
+  }
+  free(hq);
+  free(h);
+}
+
 /* One SwiGLU expert on one token row x[d] (fp64):
  *   out[c] = sum_j Wd[c][j] * SiLU(sum_i Wg[j][i] x[i]) * (sum_i Wu[j][i] x[i])
  * Wg and Wu are stored [d_ff][d], Wd is stored [d][d_ff] (linear-layer
@@ -297,7 +430,7 @@ int oracle_layer_rows(int T, int d, int d_ff, int N, int k, int n_shared,
                       int xdtype, const void* x, int wdtype,
                       const void* const* wg, const void* const* wu,
                       const void* const* wd, const int32_t* topk_idx,
-                      const double* topk_w, const uint8_t* keep, int n_rows,
+                      const double* topk_w, const uint8_t* keep, int fp8, int n_rows,
                       const int32_t* rows, double* y) {
   int bad = 0;
   for (int r = 0; r < n_rows; ++r) {
@@ -313,6 +446,25 @@ int oracle_layer_rows(int T, int d, int d_ff, int N, int k, int n_shared,
     if (!wg[N + s] || !wu[N + s] || !wd[N + s]) bad = 1;
   if (bad) return -1;
 
+  /* FP8: quantize every supplied expert's weights once, row by row. */
+  const int E_all = N + n_shared;
+  QExpert* qe = NULL;
+  if (fp8) {
+    qe = (QExpert*)calloc((size_t)E_all, sizeof(QExpert));
+    for (int e = 0; e < E_all; ++e) {
+      if (!wg[e] || !wu[e] || !wd[e]) continue;
+      qe[e].gq = (uint8_t*)malloc((size_t)d_ff * d);
+      qe[e].uq = (uint8_t*)malloc((size_t)d_ff * d);
+      qe[e].dq = (uint8_t*)malloc((size_t)d * d_ff);
+      qe[e].gs = (float*)malloc(sizeof(float) * (size_t)d_ff);
+      qe[e].us = (float*)malloc(sizeof(float) * (size_t)d_ff);
+      qe[e].ds = (float*)malloc(sizeof(float) * (size_t)d);
+      oracle_quantize_rows_e4m3(d_ff, d, wdtype, wg[e], qe[e].gq, qe[e].gs);
+      oracle_quantize_rows_e4m3(d_ff, d, wdtype, wu[e], qe[e].uq, qe[e].us);
+      oracle_quantize_rows_e4m3(d, d_ff, wdtype, wd[e], qe[e].dq, qe[e].ds);
+    }
+  }
+
   /* Every (row, term) expert evaluation is independent: evaluate them all
    * (in parallel), then form each row's gated sum in term order. */
   const int terms = k + n_shared;
@@ -323,7 +475,15 @@ int oracle_layer_rows(int T, int d, int d_ff, int N, int k, int n_shared,
     const int r = (int)(q / terms), s = (int)(q % terms);
     const int t = rows[r];
     double* xt = (double*)malloc(sizeof(double) * (size_t)d);
-    for (int i = 0; i < d; ++i) xt[i] = widen(xdtype, x, (size_t)t * d + i);
+    if (fp8) {  /* the token's row, quantized as one row and dequantized */
+      uint8_t* xq = (uint8_t*)malloc((size_t)d);
+      float xs;
+      oracle_quantize_rows_e4m3(1, d, xdtype, (const char*)x + (size_t)t * d * (xdtype == ORACLE_BF16 ? 2 : xdtype == ORACLE_F32 ? 4 : 8), xq, &xs);
+      for (int i = 0; i < d; ++i) xt[i] = oracle_e4m3_decode(xq[i]) * (double)xs;
+      free(xq);
+    } else {
+      for (int i = 0; i < d; ++i) xt[i] = widen(xdtype, x, (size_t)t * d + i);
+    }
     int e;
     if (s < k) {
       e = topk_idx[(size_t)t * k + s];
@@ -336,6 +496,8 @@ int oracle_layer_rows(int T, int d, int d_ff, int N, int k, int n_shared,
       /* a dropped pair contributes nothing ([P1] "Keeping the experts busy") */
       G[q] = 0.0;
       for (int c = 0; c < d; ++c) E[(size_t)q * d + c] = 0.0;
+    } else if (fp8) {
+      expert_swiglu_fp8(d, d_ff, &qe[e], xt, E + (size_t)q * d);
     } else {
       oracle_expert_swiglu(d, d_ff, wdtype, wg[e], wu[e], wd[e], xt, E + (size_t)q * d);
     }
@@ -346,6 +508,13 @@ int oracle_layer_rows(int T, int d, int d_ff, int N, int k, int n_shared,
                      y + (size_t)r * d);
   free(E);
   free(G);
+  if (qe) {
+    for (int e = 0; e < E_all; ++e) {
+      free(qe[e].gq); free(qe[e].uq); free(qe[e].dq);
+      free(qe[e].gs); free(qe[e].us); free(qe[e].ds);
+    }
+    free(qe);
+  }
   return 0;
 }
 

@@ -440,6 +440,94 @@ def pin_capacity_layer_is_dense_with_dropped_gates_zeroed(o):
     assert np.array_equal(full["y"], base["y"])
 
 
+# ------------------------------------------------------------------- FP8 ---
+def pin_e4m3_fixed_points(o):
+    """E4M3 from its definition (bias 7, 3 mantissa bits, subnormals m*2^-9,
+    largest finite 448, field 15 / mantissa 7 = NaN): known codes."""
+    assert o.e4m3_decode(0x00) == 0.0
+    assert o.e4m3_decode(0x01) == 2.0 ** -9          # smallest subnormal
+    assert o.e4m3_decode(0x07) == 7 * 2.0 ** -9      # largest subnormal
+    assert o.e4m3_decode(0x08) == 2.0 ** -6          # smallest normal
+    assert o.e4m3_decode(0x38) == 1.0
+    assert o.e4m3_decode(0x3C) == 1.5
+    assert o.e4m3_decode(0x40) == 2.0
+    assert o.e4m3_decode(0x7E) == 448.0              # largest finite
+    assert np.isnan(o.e4m3_decode(0x7F)) and np.isnan(o.e4m3_decode(0xFF))
+    assert o.e4m3_decode(0xFE) == -448.0 and o.e4m3_decode(0xB8) == -1.0
+    finite = [o.e4m3_decode(c) for c in range(0x7F)]
+    assert all(a < b for a, b in zip(finite, finite[1:]))  # strictly increasing magnitudes
+    for c in list(range(0x7F)) + list(range(0x80, 0xFF)):
+        assert o.e4m3_encode(o.e4m3_decode(c)) == (c if c != 0x80 else 0x80)
+
+
+def pin_e4m3_encoder_matches_definition(o):
+    """The direct encoder equals the definition form (nearest finite code,
+    ties to the even code, saturation at 448) on every code, every midpoint
+    between neighbours (the ties), both signs, and random values."""
+    finite = [o.e4m3_decode(c) for c in range(0x7F)]
+    probes = list(finite)
+    probes += [(a + b) / 2 for a, b in zip(finite, finite[1:])]
+    probes += [448.0, 460.0, 464.0, 500.0, 1e6, 2.0 ** -10, 2.0 ** -11, 3 * 2.0 ** -11]
+    rng = _rng(14)
+    probes += rng.uniform(0, 480, 2000).tolist() + (2.0 ** rng.uniform(-12, 9, 2000)).tolist()
+    for v in probes:
+        for sv in (v, -v):
+            assert o.e4m3_encode(sv) == o.e4m3_encode(sv, scan=True), sv
+    # the tie between 1.0 (0x38) and 1.125 (0x39) goes to the even code
+    assert o.e4m3_encode(1.0625) == 0x38 and o.e4m3_encode(1.1875) == 0x3A
+
+
+def pin_quantize_rows_hand_worked(o):
+    """Row [3.5, -7, 0, 1]: amax 7, scale 7/448 = 2^-6; v/scale = [224, -448,
+    0, 64], codes 0x76, 0xFE, 0x00, 0x68. A row of zeros has scale 0."""
+    q, sc = o.quantize_rows_e4m3(np.array([[3.5, -7.0, 0.0, 1.0], [0.0, 0.0, 0.0, 0.0]],
+                                          np.float32))
+    assert sc.tolist() == [2.0 ** -6, 0.0]
+    assert q[0].tolist() == [0x76, 0xFE, 0x00, 0x68] and q[1].tolist() == [0, 0, 0, 0]
+
+
+def pin_fp8_layer_hand_worked(o):
+    """One expert, d = 1, d_ff = 2, worked by hand. Every weight row and x
+    quantize back to themselves except W_u row 1 (1.84375 -> 448 * fp32(
+    1.84375/448) = 1.84375006): g = 1.75 * [56, 28] = [98, 49], SiLU leaves
+    both unchanged in fp64, u = 1.75 * [1.75, 1.84375006], h = [300.125,
+    158.10157] -> bf16 [300, 158]. The H row: scale s = fp32(300/448) =
+    0.66964287, 158/s = 235.94 rounds to the E4M3 value 240, so H becomes
+    [448 s, 240 s] = [300.0000038, 160.7142878]. W_d = [[1, 1]] quantizes to
+    448 * fp32(1/448) = 1.0000000447 each: y = 460.7143122 (458.0000205
+    without the H quantization)."""
+    x = np.array([[1.75]], np.float32)
+    Wr = np.array([[1.0]], np.float32)
+    wg = np.array([[[56.0], [28.0]]], np.float32)
+    wu = np.array([[[1.75], [1.84375]]], np.float32)
+    wd = np.array([[[1.0, 1.0]]], np.float32)
+    out = o.layer(x, Wr, wg, wu, wd, 1, fp8=True)
+    assert abs(out["y"][0, 0] - 460.714312168105) < 1e-9, out["y"]
+
+
+def pin_fp8_weight_row_scaling_is_exact(o):
+    """Scaling one output row of W_d by 2^j leaves its codes unchanged and
+    multiplies its scale (so that output column) by exactly 2^j, and no other
+    column changes."""
+    rng = _rng(15)
+    T, d, dff, N, k = 5, 16, 12, 3, 2
+    x = rng.normal(0, 1, (T, d)).astype(np.float32)
+    Wr = rng.normal(0, 1, (N, d)).astype(np.float32)
+    wg = rng.normal(0, 0.3, (N, dff, d)).astype(np.float32)
+    wu = rng.normal(0, 0.3, (N, dff, d)).astype(np.float32)
+    wd = rng.normal(0, 0.3, (N, d, dff)).astype(np.float32)
+    a = o.layer(x, Wr, wg, wu, wd, k, fp8=True)
+    wd2 = wd.copy()
+    wd2[:, 5, :] *= 8.0
+    b = o.layer(x, Wr, wg, wu, wd2, k, fp8=True)
+    assert np.array_equal(b["y"][:, 5], 8.0 * a["y"][:, 5])
+    other = [c for c in range(d) if c != 5]
+    assert np.array_equal(b["y"][:, other], a["y"][:, other])
+    # and FP8 stays within a few E4M3 steps (2^-4 relative) of the exact layer
+    ref = o.layer(x, Wr, wg, wu, wd, k)
+    assert np.abs(a["y"] - ref["y"]).max() <= 0.1 * np.abs(ref["y"]).max()
+
+
 def pin_balance_stats_sum_to_one(o):
     rng = _rng(11)
     T, N, k = 64, 8, 2

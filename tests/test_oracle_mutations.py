@@ -37,6 +37,12 @@ MUTATIONS = [
     ("prob_sum_from_gates", "for (int e = 0; e < N; ++e) prob_sum[e] += p[e];", "for (int s = 0; s < k; ++s) prob_sum[it[s]] += topk_w[(size_t)t * k + s];"),
     ("bf16_widen_wrong_half", "uint32_t u = (uint32_t)((const uint16_t*)base)[i] << 16;", "uint32_t u = (uint32_t)((const uint16_t*)base)[i];"),
     ("order_margin_skips_last_gap", "for (int s = 0; s + 1 < m; ++s)", "for (int s = 0; s + 2 < m; ++s)"),
+    ("e4m3_exponent_bias", "v = ldexp(1.0 + m / 8.0, e - 7);", "v = ldexp(1.0 + m / 8.0, e - 8);"),
+    ("e4m3_ties_away_from_even", "if (d < bd || (d == bd && (c & 1) == 0)) {", "if (d <= bd) {"),
+    ("e4m3_direct_no_carry", "  if (m == 8) {\n    m = 0;\n    ++E;\n  }", ""),
+    ("fp8_scale_over_240", "const float s = amax / 448.0f;", "const float s = amax / 240.0f;"),
+    ("fp8_h_not_quantized", "(oracle_e4m3_decode(hq[j]) * (double)hs);", "(double)h[j];"),
+    ("fp8_wrong_weight_row_scale", "out[c] = acc * (double)q->ds[c];", "out[c] = acc * (double)q->ds[d - 1 - c];"),
     ("selection_ignores_bias", "key[e] = sel_bias ? (float)((double)rt[e] + (double)sel_bias[e]) : rt[e];", "key[e] = rt[e];"),
 ]
 
