@@ -77,9 +77,11 @@ static double widen(int dtype, const void* base, size_t i) {
  * mantissa 6); field 15 with mantissa 7 is NaN; there is no infinity.
  * Reading (the pages give no scaling rule): each row (a token's activations,
  * or one output channel of a weight matrix) carries one fp32 scale
- * s = fp32(amax / 448) and codes q_i = E4M3(fp32(v_i / s)), rounded to
- * nearest even and saturated at +-448; a row of zeros has s = 0 and codes 0.
- * The value of a code is decode(q) * s. */
+ * s = fp32(amax / 448) and codes q_i = E4M3(fp32(v_i * inv)) with
+ * inv = fp32(448 / amax), rounded to nearest even and saturated at +-448 (a
+ * product rather than v_i / s, so that a kernel quantizes at memory speed);
+ * a row of zeros has s = 0 and codes 0. The value of a code is
+ * decode(q) * s. */
 double oracle_e4m3_decode(uint8_t c) {
   const int e = (c >> 3) & 15, m = c & 7;
   double v;
@@ -136,7 +138,8 @@ uint8_t oracle_e4m3_encode(float v) {
 }
 
 /* Row-wise quantization of a rows x cols matrix of stored values (see the
- * FP8 note above): scale[r] = fp32(amax_r / 448), q = E4M3(fp32(v / scale)). */
+ * FP8 note above): scale[r] = fp32(amax_r / 448),
+ * q = E4M3(fp32(v * fp32(448 / amax_r))). */
 void oracle_quantize_rows_e4m3(int rows, int cols, int dtype, const void* src, uint8_t* q,
                                float* scale) {
 #pragma omp parallel for schedule(static)
@@ -147,10 +150,11 @@ void oracle_quantize_rows_e4m3(int rows, int cols, int dtype, const void* src, u
       if (fabsf(v) > amax) amax = fabsf(v);
     }
     const float s = amax / 448.0f;
+    const float inv = amax > 0.0f ? 448.0f / amax : 0.0f;
     scale[r] = s;
     for (int c = 0; c < cols; ++c) {
       const float v = (float)widen(dtype, src, (size_t)r * cols + c);
-      q[(size_t)r * cols + c] = s == 0.0f ? 0 : oracle_e4m3_encode(v / s);
+      q[(size_t)r * cols + c] = amax == 0.0f ? 0 : oracle_e4m3_encode(v * inv);
     }
   }
 }

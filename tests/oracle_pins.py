@@ -478,12 +478,16 @@ def pin_e4m3_encoder_matches_definition(o):
 
 
 def pin_quantize_rows_hand_worked(o):
-    """Row [3.5, -7, 0, 1]: amax 7, scale 7/448 = 2^-6; v/scale = [224, -448,
-    0, 64], codes 0x76, 0xFE, 0x00, 0x68. A row of zeros has scale 0."""
+    """Row [3.5, -7, 0, 1]: amax 7, scale 7/448 = 2^-6, 448/amax = 64;
+    v * 64 = [224, -448, 0, 64], codes 0x76, 0xFE, 0x00, 0x68. A row of zeros
+    has scale 0. Row [1.84375]: 448/1.84375 rounds to fp32 242.98305, and
+    1.84375 times that rounds to 448.00000 in fp32: code 0x7E."""
     q, sc = o.quantize_rows_e4m3(np.array([[3.5, -7.0, 0.0, 1.0], [0.0, 0.0, 0.0, 0.0]],
                                           np.float32))
     assert sc.tolist() == [2.0 ** -6, 0.0]
     assert q[0].tolist() == [0x76, 0xFE, 0x00, 0x68] and q[1].tolist() == [0, 0, 0, 0]
+    q2, _ = o.quantize_rows_e4m3(np.array([[1.84375]], np.float32))
+    assert q2.tolist() == [[0x7E]]
 
 
 def pin_fp8_layer_hand_worked(o):

@@ -41,6 +41,7 @@ MUTATIONS = [
     ("e4m3_ties_away_from_even", "if (d < bd || (d == bd && (c & 1) == 0)) {", "if (d <= bd) {"),
     ("e4m3_direct_no_carry", "  if (m == 8) {\n    m = 0;\n    ++E;\n  }", ""),
     ("fp8_scale_over_240", "const float s = amax / 448.0f;", "const float s = amax / 240.0f;"),
+    ("fp8_codes_over_240", "const float inv = amax > 0.0f ? 448.0f / amax : 0.0f;", "const float inv = amax > 0.0f ? 240.0f / amax : 0.0f;"),
     ("fp8_h_not_quantized", "(oracle_e4m3_decode(hq[j]) * (double)hs);", "(double)h[j];"),
     ("fp8_wrong_weight_row_scale", "out[c] = acc * (double)q->ds[c];", "out[c] = acc * (double)q->ds[d - 1 - c];"),
     ("selection_ignores_bias", "key[e] = sel_bias ? (float)((double)rt[e] + (double)sel_bias[e]) : rt[e];", "key[e] = rt[e];"),
