@@ -190,12 +190,47 @@ def gemm_flops(w, counts=None):
     return 4.0 * rows * w.d_model * w.d_ff, 2.0 * rows * w.d_ff * w.d_model
 
 
-def touched_weight_bytes(w, counts):
-    """Expert weight bytes a forward must read: every expert with a row."""
-    eb = 2 if w.dtype == "bf16" else 4
-    per = 3 * w.d_model * w.d_ff * eb
+def touched_weight_bytes(w, counts, fp8=False):
+    """Expert weight bytes a forward must read: every expert with a row (E4M3:
+    one byte a weight plus an fp32 scale per output channel)."""
+    if fp8:
+        per = 3 * w.d_model * w.d_ff + 4 * (2 * w.d_ff + w.d_model)
+    else:
+        per = 3 * w.d_model * w.d_ff * (2 if w.dtype == "bf16" else 4)
     active = sum(1 for c in counts if c > 0) + w.n_shared
     return active * per, active
+
+
+class Forward:
+    """One layer forward through the C ABI: moe_layer_forward, or with
+    --fp8 moe_layer_forward_fp8 on weights quantized once by moe_quantize_fp8."""
+
+    def __init__(self, moe, cfg, inp, fp8, dev, q=None):
+        import torch
+        self.moe, self.cfg, self.inp, self.fp8 = moe, cfg, inp, fp8
+        self.ws = moe.workspace(cfg, "layer_fp8" if fp8 else "layer", dev)
+        self.q = q if q is not None else []
+        if fp8 and not self.q:
+            for n in ("w_gate", "w_up", "w_down"):
+                t = inp[n]
+                rows, cols = t.shape[0] * t.shape[1], t.shape[2]
+                q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+                sc = torch.empty(rows, dtype=torch.float32, device=dev)
+                moe.moe_quantize_fp8(t.reshape(rows, cols), q, sc)
+                self.q.append((q, sc))
+            torch.cuda.synchronize(dev)
+
+    def __call__(self, x, y, idx, tw, counts, ps, stream):
+        i = self.inp
+        if self.fp8:
+            (gq, gs), (uq, us), (dq, ds) = self.q
+            self.moe.moe_layer_forward_fp8(self.cfg, x, i["w_router"], i["logit_bias"],
+                                           i["sel_bias"], gq, gs, uq, us, dq, ds, y, idx, tw,
+                                           counts, ps, self.ws, stream)
+        else:
+            self.moe.moe_layer_forward(self.cfg, x, i["w_router"], i["logit_bias"], i["sel_bias"],
+                                       i["w_gate"], i["w_up"], i["w_down"], y, idx, tw, counts,
+                                       ps, self.ws, stream)
 
 
 # ----------------------------------------------------------------- our arm --
@@ -220,13 +255,12 @@ def run_ours(args):
     tw = torch.empty(w.T, w.top_k, dtype=torch.float32, device=dev)
     counts = torch.empty(w.n_experts, dtype=torch.int32, device=dev)
     ps = torch.empty(w.n_experts, dtype=torch.float32, device=dev)
-    wsp = moe.workspace(cfg, "layer", dev)
+    fwd = Forward(moe, cfg, inp, args.fp8, dev)
+    wsp = fwd.ws
     stream = torch.cuda.current_stream(dev)
 
     def step(x):
-        moe.moe_layer_forward(cfg, x, inp["w_router"], inp["logit_bias"], inp["sel_bias"],
-                              inp["w_gate"], inp["w_up"], inp["w_down"], y, idx, tw, counts, ps, wsp,
-                              stream)
+        fwd(x, y, idx, tw, counts, ps, stream)
 
     default = args.workload == DEFAULT_WORKLOAD
     for _ in range(args.warmup):
@@ -289,9 +323,7 @@ def run_ours(args):
         x_ready[b].record(h2d)
         stream.wait_event(x_ready[b])
         stream.wait_event(y_free[b])
-        moe.moe_layer_forward(cfg, x_dev[b], inp["w_router"], inp["logit_bias"], inp["sel_bias"],
-                              inp["w_gate"], inp["w_up"], inp["w_down"], y_dev[b], idx, tw, counts,
-                              ps, wsp, stream)
+        fwd(x_dev[b], y_dev[b], idx, tw, counts, ps, stream)
         x_free[b].record(stream)
         y_ready[b].record(stream)
         d2h.wait_event(y_ready[b])
@@ -337,15 +369,20 @@ def run_ours(args):
     per_kernel["down"]["tflops"] = f_dn / (dn_ms / 1e3) / 1e12
     gemm_tflops = (f_gu + f_dn) / ((gu_ms + dn_ms) / 1e3) / 1e12
     ach = per_kernel["gate_up"]["tflops"]
+    # E4M3: the measured bf16 peaks times the nominal fp8/bf16 ratio (4.5 / 2.25)
+    tpk = pk["bf16"] * (2.0 if args.fp8 else 1.0)
+    tpk_s = pk["bf16_sustained"] * (2.0 if args.fp8 else 1.0)
     roofline = {"bound": "tensor", "kernel": "gate_up (grouped SwiGLU gate+up GEMM)",
-                "achieved": round(ach, 1), "peak": pk["bf16"], "unit": "TFLOP/s",
-                "frac": round(ach / pk["bf16"], 4),
-                "traffic": args.traffic if args.traffic is not None else recorded_traffic(),
-                "peak_source": f"{pk['source']} bf16 burst",
-                "frac_of_sustained": round(ach / pk["bf16_sustained"], 4),
+                "achieved": round(ach, 1), "peak": round(tpk, 1), "unit": "TFLOP/s",
+                "frac": round(ach / tpk, 4),
+                "traffic": (args.traffic if args.traffic is not None
+                            else (None if args.fp8 else recorded_traffic())),
+                "peak_source": (f"{pk['source']} bf16 burst x 2 (nominal fp8/bf16 ratio)"
+                                if args.fp8 else f"{pk['source']} bf16 burst"),
+                "frac_of_sustained": round(ach / tpk_s, 4),
                 "algorithmic_flops_per_launch": f_gu,
                 "grouped_gemm_both_kernels_tflops": round(gemm_tflops, 1),
-                "grouped_gemm_both_kernels_frac": round(gemm_tflops / pk["bf16"], 4)}
+                "grouped_gemm_both_kernels_frac": round(gemm_tflops / tpk, 4)}
     # HBM-bound kernels of the step against the copy bandwidth
     P = w.T * w.top_k
     hb = {"router_topk": w.T * w.d_model * 2 + w.n_experts * w.d_model * 2 + P * 8,
@@ -380,7 +417,8 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 experts (row scales), bf16 tokens and router" if args.fp8 else "bf16",
             "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) random-init weights)",
             "config": {"workload": w.name, "T": w.T, "d_model": w.d_model,
                        "n_experts": w.n_experts, "top_k": w.top_k, "d_ff": w.d_ff,
@@ -397,7 +435,8 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": bytes_io,
                     "d2h_bytes_per_step": bytes_io,
-                    "path": "per step: pinned host x -> H2D (copy stream) -> moe_layer_forward "
+                    "path": "per step: pinned host x -> H2D (copy stream) -> moe_layer_forward"
+                            + ("_fp8 " if args.fp8 else " ") +
                             "(C ABI, compute stream) -> D2H y (copy stream) -> pinned host; "
                             "copies overlap neighbouring steps' forwards; host wall clock"},
             "gpu_launches": int(launches),
@@ -417,18 +456,19 @@ def run_decode(moe, synth, dev, stream, pk, args):
     out = {}
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     base = synth.make_inputs(synth.MIXTRAL_DECODE[-1], dev)
+    qcache = None
     for w in synth.MIXTRAL_DECODE:
         x = base["x"][: w.T].contiguous()
         cfg = moe.config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k,
                          d_ff=w.d_ff, dtype=moe.MOE_BF16)
         y = torch.empty(w.T, w.d_model, dtype=torch.bfloat16, device=dev)
         counts = torch.empty(w.n_experts, dtype=torch.int32, device=dev)
-        wsp = moe.workspace(cfg, "layer", dev)
+        fwd = Forward(moe, cfg, base, args.fp8, dev, qcache)
+        qcache = fwd.q  # the expert weights are quantized once for all batch sizes
 
         def step(st=None):
-            moe.moe_layer_forward(cfg, x, base["w_router"], None, None, base["w_gate"],
-                                  base["w_up"], base["w_down"], y, None, None, counts, None, wsp,
-                                  st if st is not None else torch.cuda.current_stream(dev))
+            fwd(x, y, None, None, counts, None,
+                st if st is not None else torch.cuda.current_stream(dev))
         for _ in range(3):
             step()
         torch.cuda.synchronize(dev)
@@ -470,7 +510,7 @@ def run_decode(moe, synth, dev, stream, pk, args):
             step()
         kern = moe.profile_collect()
         moe.profile_enable(False)
-        wbytes, active = touched_weight_bytes(w, counts.cpu().tolist())
+        wbytes, active = touched_weight_bytes(w, counts.cpu().tolist(), args.fp8)
         total = wbytes + w.n_experts * w.d_model * 2 + 2 * w.T * w.d_model * 2
         gbs = total / (ms / 1e3) / 1e9
         gbs_g = total / (ms_graph / 1e3) / 1e9
@@ -586,6 +626,8 @@ def main(argv=None):
                     help="sampled tokens per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="E4M3 expert weights (moe_layer_forward_fp8); not the headline, which is bf16")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per gate_up launch from an ncu capture of this build")
     args = ap.parse_args(argv)

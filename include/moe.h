@@ -286,6 +286,48 @@ MOE_API int moe_layer_forward(const moe_config* cfg, const void* x,
                       moe_stream_t stream);
 
 /*
+ * FP8 experts. Deployed experts are stored, and tokens dispatched, in FP8
+ * ("MoE inference: the call centre with 256 specialists and 8 taking each
+ * call", "The maths that matters" and "DeepEP, EPLB and Wide-EP"). The
+ * format is E4M3 (4 exponent bits, bias 7, 3 mantissa bits, largest finite
+ * 448, no infinity) with one fp32 scale per row: s = fp32(amax / 448) and
+ * codes q = E4M3(fp32(v * fp32(448 / amax))), rounded to nearest even and
+ * saturated; a row of zeros has s = 0 and codes 0; a code stands for
+ * decode(q) * s. The pages give no scaling rule; this is the library's.
+ *
+ * moe_quantize_fp8: rows x cols bf16 [device] -> q [rows][cols] uint8 and
+ * scale [rows] fp32 [device]. cols a multiple of 8, pointers 16-byte
+ * aligned. Quantize each weight tensor of moe_layer_forward_fp8 with it
+ * (rows = output channels: E*d_ff for gate and up, E*d_model for down).
+ */
+MOE_API int moe_quantize_fp8(int64_t rows, int32_t cols, const void* src, uint8_t* q,
+                    float* scale, moe_stream_t stream);
+
+/*
+ * moe_layer_forward with E4M3 experts: routing as moe_layer_forward (bf16 x
+ * and W_r; cfg->dtype must be MOE_BF16), then every routed token row, x for
+ * the shared experts, and each row of H are quantized as above, and both
+ * expert projections run on the tensor cores in E4M3 (fp32 accumulation),
+ * the row and channel scales applied in the GEMM epilogues. H is stored in
+ * bf16 before its quantization; y is bf16.
+ *
+ *  wg_q, wu_q [device] [N+s][d_ff][d_model] uint8 codes;
+ *  wg_scale, wu_scale [device] [N+s][d_ff] fp32 row scales;
+ *  wd_q [device] [N+s][d_model][d_ff] uint8; wd_scale [N+s][d_model] fp32.
+ *  Other arguments as moe_layer_forward; ws: moe_workspace_size_fp8(cfg).
+ *  d_model and d_ff must be multiples of 16 (MOE_ERR_UNSUPPORTED otherwise).
+ */
+MOE_API size_t moe_workspace_size_fp8(const moe_config* cfg);
+MOE_API int moe_layer_forward_fp8(const moe_config* cfg, const void* x, const void* w_router,
+                    const float* logit_bias, const float* sel_bias,
+                    const uint8_t* wg_q, const float* wg_scale,
+                    const uint8_t* wu_q, const float* wu_scale,
+                    const uint8_t* wd_q, const float* wd_scale, void* y,
+                    int32_t* topk_idx, float* topk_w, int32_t* counts,
+                    float* prob_sum, void* ws, size_t ws_bytes,
+                    moe_stream_t stream);
+
+/*
  * The load-balance statistics on the device: f_i = counts_i / (T*k),
  * P_i = prob_sum_i / T and aux = alpha * N * sum_i f_i P_i (one fixed-order
  * sum). ("Mixture of experts and speculative decoding", "Keeping the

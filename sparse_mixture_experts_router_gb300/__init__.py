@@ -77,6 +77,9 @@ _SIGS = {
     "moe_grouped_swiglu": (_I, [_CFG] + [_P] * 9 + [_P, _SZ, _P]),
     "moe_combine": (_I, [_CFG, _P, _P, _P, _P, _P]),
     "moe_layer_forward": (_I, [_CFG] + [_P] * 12 + [_P, _SZ, _P]),
+    "moe_quantize_fp8": (_I, [ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P]),
+    "moe_workspace_size_fp8": (_SZ, [_CFG]),
+    "moe_layer_forward_fp8": (_I, [_CFG] + [_P] * 15 + [_P, _SZ, _P]),
     "moe_balance_stats": (_I, [ctypes.c_int32] * 3 + [_P, _P, ctypes.c_float, _P, _P, _P, _P]),
     "moe_stream_status": (_I, [_P, _P]),
     "moe_profile_enable": (None, [_I]),
@@ -142,7 +145,8 @@ def check_config(cfg: moe_config) -> int:
 
 def workspace_size(cfg: moe_config, kind: str = "layer") -> int:
     fn = {"layer": "moe_workspace_size", "router": "moe_router_workspace_size",
-          "permute": "moe_permute_workspace_size", "grouped": "moe_grouped_workspace_size"}[kind]
+          "permute": "moe_permute_workspace_size", "grouped": "moe_grouped_workspace_size",
+          "layer_fp8": "moe_workspace_size_fp8"}[kind]
     return int(getattr(lib(), fn)(ctypes.byref(cfg)))
 
 
@@ -189,6 +193,22 @@ def moe_grouped_swiglu(cfg, x_perm, x, expert_offsets, sorted_pair, topk_w, w_ga
 def moe_combine(cfg, y_perm, inv_pos, topk_w, y, stream=None):
     _check("moe_combine", lib().moe_combine(
         ctypes.byref(cfg), _ptr(y_perm), _ptr(inv_pos), _ptr(topk_w), _ptr(y), _stream(stream)))
+
+
+def moe_quantize_fp8(src, q, scale, stream=None):
+    """Row-wise E4M3 codes and fp32 scales of a [rows, cols] bf16 tensor."""
+    rows, cols = src.shape[0], src.numel() // max(1, src.shape[0])
+    _check("moe_quantize_fp8", lib().moe_quantize_fp8(rows, cols, _ptr(src), _ptr(q), _ptr(scale),
+                                                      _stream(stream)))
+
+
+def moe_layer_forward_fp8(cfg, x, w_router, logit_bias, sel_bias, wg_q, wg_scale, wu_q, wu_scale,
+                          wd_q, wd_scale, y, topk_idx, topk_w, counts, prob_sum, ws, stream=None):
+    _check("moe_layer_forward_fp8", lib().moe_layer_forward_fp8(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(sel_bias),
+        _ptr(wg_q), _ptr(wg_scale), _ptr(wu_q), _ptr(wu_scale), _ptr(wd_q), _ptr(wd_scale),
+        _ptr(y), _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(prob_sum), _ptr(ws),
+        ws.numel() if ws is not None else 0, _stream(stream)))
 
 
 def moe_layer_forward(cfg, x, w_router, logit_bias, sel_bias, w_gate, w_up, w_down, y, topk_idx,

@@ -115,6 +115,35 @@ LayerWs carve_layer(Carver& cv, const moe_config& c) {
   return w;
 }
 
+// The FP8 layer: the bf16 layer's routing and output buffers, E4M3 copies
+// of the routed rows and of x (shared experts), H in bf16 with its rows' max
+// |H|, and H in E4M3, each with fp32 row scales.
+struct LayerFp8Ws {
+  LayerWs base;  // x_perm unused
+  uint8_t* xq_perm;
+  float* xp_scale;
+  uint8_t* xq;
+  float* x_scale;
+  unsigned* h_amax;
+  uint8_t* hq;
+  float* h_scale;
+};
+LayerFp8Ws carve_layer_fp8(Carver& cv, const moe_config& c) {
+  LayerFp8Ws w;
+  moe_config b = c;
+  b.dtype = MOE_BF16;
+  w.base = carve_layer(cv, b);
+  const size_t P = (size_t)pairs(c), R = (size_t)rows_total(c);
+  w.xq_perm = cv.take<uint8_t>((size_t)padded_rows((long long)P) * c.d_model);
+  w.xp_scale = cv.take<float>(sizeof(float) * P);
+  w.xq = cv.take<uint8_t>((size_t)padded_rows(c.T) * c.d_model);
+  w.x_scale = cv.take<float>(sizeof(float) * (size_t)c.T);
+  w.h_amax = cv.take<unsigned>(sizeof(unsigned) * R);
+  w.hq = cv.take<uint8_t>((size_t)padded_rows((long long)R) * c.d_ff);
+  w.h_scale = cv.take<float>(sizeof(float) * R);
+  return w;
+}
+
 int check_ws(const moe_config& c, void* ws, size_t ws_bytes, size_t need) {
   (void)c;
   if (!ws) return MOE_ERR_INVALID_ARG;
@@ -171,7 +200,7 @@ const char* kKernelNames[K_NUM] = {"reset_status",  "router_topk",    "permute_h
                                    "permute_scan",  "permute_rank",   "permute_gather",
                                    "permute_small", "permute_group",  "seg_table",
                                    "gate_up",       "down",           "splitk_reduce",
-                                   "combine",       "balance_stats"};
+                                   "combine",       "balance_stats",  "quantize_fp8"};
 struct Prof {
   std::mutex mu;
   uint32_t mask = 0;
@@ -418,6 +447,103 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* w_router
                     w_up, w_down, w.y_perm, w.seg, true, w.h, w.partial, w.status, s);
   if (rc != MOE_OK) return rc;
   e = launch_combine(c, w.y_perm, w.inv_pos, nullptr, y, s);
+  return e == cudaSuccess ? MOE_OK : fail_cuda(e);
+}
+
+size_t moe_workspace_size_fp8(const moe_config* c) {
+  if (moe_check_config(c) != MOE_OK || c->dtype != MOE_BF16) return 0;
+  if (c->d_model % 16 != 0 || c->d_ff % 16 != 0) return 0;
+  Carver cv(nullptr);
+  carve_layer_fp8(cv, *c);
+  return align_up(cv.off, 256);
+}
+
+int moe_quantize_fp8(int64_t rows, int32_t cols, const void* src, uint8_t* q, float* scale,
+                     moe_stream_t stream) {
+  if (rows < 0 || cols < 8 || cols % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!src || !q || !scale) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned({src, q, scale})) return MOE_ERR_MISALIGNED;
+  QuantArgs a{};
+  a.src = static_cast<const __nv_bfloat16*>(src);
+  a.rows = rows;
+  a.cols = cols;
+  a.q = q;
+  a.scale = scale;
+  cudaError_t e = launch_quantize_rows(a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : fail_cuda(e);
+}
+
+int moe_layer_forward_fp8(const moe_config* cfg, const void* x, const void* w_router,
+                          const float* logit_bias, const float* sel_bias, const uint8_t* wg_q,
+                          const float* wg_scale, const uint8_t* wu_q, const float* wu_scale,
+                          const uint8_t* wd_q, const float* wd_scale, void* y, int32_t* topk_idx,
+                          float* topk_w, int32_t* counts, float* prob_sum, void* ws,
+                          size_t ws_bytes, moe_stream_t stream) {
+  int rc = moe_check_config(cfg);
+  if (rc != MOE_OK) return rc;
+  const moe_config& c = *cfg;
+  if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;  // bf16 tokens, E4M3 experts
+  // E4M3 rows are read by TMA, whose row pitch must be a multiple of 16 bytes
+  if (c.d_model % 16 != 0 || c.d_ff % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  if (c.T > 0 && (!x || !w_router || !wg_q || !wg_scale || !wu_q || !wu_scale || !wd_q ||
+                  !wd_scale || !y))
+    return MOE_ERR_INVALID_ARG;
+  if (!all_aligned({x, w_router, logit_bias, sel_bias, wg_q, wg_scale, wu_q, wu_scale, wd_q,
+                    wd_scale, y, topk_idx, topk_w, counts, prob_sum}))
+    return MOE_ERR_MISALIGNED;
+  if ((rc = check_ws(c, ws, ws_bytes, moe_workspace_size_fp8(cfg))) != MOE_OK) return rc;
+  if ((rc = check_device(c)) != MOE_OK) return rc;
+  Carver cv(ws);
+  LayerFp8Ws w8 = carve_layer_fp8(cv, c);
+  LayerWs& w = w8.base;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
+  int32_t* idx = topk_idx ? topk_idx : w.topk_idx;
+  float* tw = topk_w ? topk_w : w.topk_w;
+  int32_t* cnt = counts ? counts : w.counts;
+  float* ps = prob_sum ? prob_sum : w.prob_sum;
+  cudaError_t e = launch_router(c, x, w_router, logit_bias, sel_bias, nullptr, nullptr, idx, tw,
+                                cnt, ps, w.partials, w.status, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (c.T == 0) return MOE_OK;
+  const long long P = pairs(c);
+  e = launch_permute(c, x, idx, cnt, w.offsets, w.sorted_pair, w.inv_pos, nullptr, w.hist,
+                     w.status, w.seg, kTileM, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  // routed rows: gathered and quantized in one pass; their H maxima cleared
+  QuantArgs qa{};
+  qa.src = static_cast<const __nv_bfloat16*>(x);
+  qa.rows = P;
+  qa.cols = c.d_model;
+  qa.gather = w.sorted_pair;
+  qa.k = c.top_k;
+  qa.src_rows = c.T;
+  qa.rows_dev = w.offsets + c.n_experts;
+  qa.q = w8.xq_perm;
+  qa.scale = w8.xp_scale;
+  qa.clear = w8.h_amax;
+  qa.clear_n = 1;
+  e = launch_quantize_rows(qa, s);
+  if (e == cudaSuccess && c.n_shared > 0) {  // x for the shared experts
+    QuantArgs qs{};
+    qs.src = static_cast<const __nv_bfloat16*>(x);
+    qs.rows = c.T;
+    qs.cols = c.d_model;
+    qs.q = w8.xq;
+    qs.scale = w8.x_scale;
+    qs.clear = w8.h_amax;
+    qs.clear_base = P;
+    qs.clear_stride = c.T;
+    qs.clear_n = c.n_shared;
+    e = launch_quantize_rows(qs, s);
+  }
+  if (e == cudaSuccess)
+    e = launch_grouped_e4m3(c, w8.xq_perm, w8.xp_scale, w8.xq, w8.x_scale, w.seg, w.sorted_pair, tw,
+                            wg_q, wg_scale, wu_q, wu_scale, wd_q, wd_scale, w.h, w8.h_amax, w8.hq,
+                            w8.h_scale, w.y_perm, w.partial, padded_rows(P),
+                            padded_rows(rows_total(c)), w.status, s);
+  if (e == cudaSuccess) e = launch_combine(c, w.y_perm, w.inv_pos, nullptr, y, s);
   return e == cudaSuccess ? MOE_OK : fail_cuda(e);
 }
 

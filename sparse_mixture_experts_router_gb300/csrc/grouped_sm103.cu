@@ -66,9 +66,31 @@ constexpr int TMEM_COLS = BN * NUM_ACC;        // 512
 constexpr int THREADS = 192;
 constexpr int EPI_THREADS = 128;
 constexpr size_t DYN_SMEM = (size_t)STAGES * STAGE_BYTES + 1024;  // + 1 KB alignment slack
-constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
 
 enum { EPI_SWIGLU = 0, EPI_DOWN = 1 };
+
+// Operand types. A stage row is 128 bytes either way: 64 bf16 or 128 E4M3
+// elements of K, and one MMA takes 32 bytes of K (16 bf16 with kind::f16,
+// 32 E4M3 with kind::f8f6f4), so rings, descriptors and K steps are shared;
+// only the K extent of a block, the instruction and the epilogue scales
+// (E4M3: one fp32 scale per A row and per weight output channel) differ.
+enum { OP_BF16 = 0, OP_E4M3 = 1 };
+template <int OP>
+struct Op {
+  static constexpr int EPK = OP == OP_BF16 ? 64 : 128;  // K elements per 128-byte block
+};
+template <int OP>
+__host__ __device__ constexpr uint32_t idesc_op(int M, int N) {
+  return OP == OP_BF16 ? ptx::idesc_bf16_f32(M, N) : ptx::idesc_e4m3_f32(M, N);
+}
+template <int OP>
+__device__ __forceinline__ void mma_op(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+  if constexpr (OP == OP_BF16)
+    ptx::mma_bf16(d, a, b, idesc, accumulate);
+  else
+    ptx::mma_e4m3(d, a, b, idesc, accumulate);
+}
 
 struct GemmArgs {
   const int32_t* seg;          // segment table (moe_internal.h)
@@ -88,6 +110,15 @@ struct GemmArgs {
   int s_max;                   // largest split factor the partial buffer holds
   int pc;                      // partial columns (2*d_ff for gate/up, d for down)
   long long R;                 // output rows
+  // E4M3 operands only (null otherwise): the fp32 scale of every A row
+  // (routed rows; the shared experts' token rows), of every weight output
+  // channel [E][b_rows] (gate or down; up), and, for gate/up, the running
+  // max |H| of every output row (fp32 bits, for the H quantization).
+  const float* a_scale;
+  const float* a_scale_shared;
+  const float* b_scale0;
+  const float* b_scale1;
+  unsigned* h_amax;
 };
 
 struct __align__(8) SharedState {
@@ -157,11 +188,15 @@ __device__ __forceinline__ float row_scale(const GemmArgs& a, int seg_id, long l
 // The fused epilogue of one 128-row accumulator: each thread drains its
 // TMEM lane (row) 32 columns at a time and stores bf16 (SwiGLU of the paired
 // gate/up columns, or the gate-weighted down projection). Rows past the
-// segment's end (valid = false) are loaded but not stored.
-template <int EPI>
+// segment's end (valid = false) are loaded but not stored. E4M3 operands:
+// sa is the row's A scale and sb0/sb1 point at the tile's first weight
+// channel scale (gate, up; or down); gate/up also records the row's max |H|.
+template <int EPI, int OP>
 __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tbase, const Tile& t,
-                                               bool valid, long long orow, __nv_bfloat16* out) {
+                                               bool valid, long long orow, __nv_bfloat16* out,
+                                               float sa, const float* sb0, const float* sb1) {
   if (EPI == EPI_SWIGLU) {
+    float hmax = 0.f;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       uint32_t g[32], u[32];
@@ -173,9 +208,22 @@ __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tb
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const float h0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
-          const float h1 = silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
-          pk[j] = f32x2_to_bf16x2(h0, h1);
+          float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+          float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
+          if constexpr (OP == OP_E4M3) {
+            const int cc = c * 32 + 2 * j;
+            const bool in0 = col0 + 2 * j < args.n_out, in1 = col0 + 2 * j + 1 < args.n_out;
+            g0 *= sa * (in0 ? __ldg(sb0 + cc) : 0.f);
+            u0 *= sa * (in0 ? __ldg(sb1 + cc) : 0.f);
+            g1 *= sa * (in1 ? __ldg(sb0 + cc + 1) : 0.f);
+            u1 *= sa * (in1 ? __ldg(sb1 + cc + 1) : 0.f);
+          }
+          pk[j] = f32x2_to_bf16x2(silu(g0) * u0, silu(g1) * u1);
+          if constexpr (OP == OP_E4M3) {
+            float h0, h1;
+            bf16x2_to_f32(pk[j], h0, h1);
+            hmax = fmaxf(hmax, fmaxf(fabsf(h0), fabsf(h1)));
+          }
         }
         __nv_bfloat16* dst = out + orow * args.ldo + col0;
 #pragma unroll
@@ -185,8 +233,10 @@ __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tb
                 make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
       }
     }
+    if constexpr (OP == OP_E4M3)
+      if (valid && hmax > 0.f) atomicMax(args.h_amax + orow, __float_as_uint(hmax));
   } else {
-    const float scale = valid ? row_scale(args, t.s, orow) : 0.0f;
+    const float scale = valid ? row_scale(args, t.s, orow) * sa : 0.0f;
 #pragma unroll 1
     for (int c = 0; c < 8; ++c) {
       uint32_t v[32];
@@ -196,9 +246,15 @@ __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tb
       if (valid) {
         uint32_t pk[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          pk[j] = f32x2_to_bf16x2(scale * __uint_as_float(v[2 * j]),
-                                  scale * __uint_as_float(v[2 * j + 1]));
+        for (int j = 0; j < 16; ++j) {
+          float y0 = scale * __uint_as_float(v[2 * j]), y1 = scale * __uint_as_float(v[2 * j + 1]);
+          if constexpr (OP == OP_E4M3) {
+            const int cc = c * 32 + 2 * j;
+            y0 *= col0 + 2 * j < args.n_out ? __ldg(sb0 + cc) : 0.f;
+            y1 *= col0 + 2 * j + 1 < args.n_out ? __ldg(sb0 + cc + 1) : 0.f;
+          }
+          pk[j] = f32x2_to_bf16x2(y0, y1);
+        }
         __nv_bfloat16* dst = out + orow * args.ldo + col0;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
@@ -210,7 +266,7 @@ __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tb
   }
 }
 
-template <int EPI>
+template <int EPI, int OP>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_a_shared,
@@ -224,7 +280,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t ring = (ptx::smem_addr(dyn_smem) + 1023u) & ~1023u;
 
   const int32_t* seg = args.seg;
-  const int KB = (args.K + BK - 1) / BK;
+  const int KB = (args.K + Op<OP>::EPK - 1) / Op<OP>::EPK;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -290,13 +346,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t a_dst = ring + stage * STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_BYTES;
           ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          ptx::tma_load_2d(a_dst, am, fb, kb * BK, a_row);
+          ptx::tma_load_2d(a_dst, am, fb, kb * Op<OP>::EPK, a_row);
           if (EPI == EPI_SWIGLU) {
-            ptx::tma_load_2d(b_dst, &map_b0, fb, kb * BK, b_row);
-            ptx::tma_load_2d(b_dst + B_HALF_BYTES, &map_b1, fb, kb * BK, b_row);
+            ptx::tma_load_2d(b_dst, &map_b0, fb, kb * Op<OP>::EPK, b_row);
+            ptx::tma_load_2d(b_dst + B_HALF_BYTES, &map_b1, fb, kb * Op<OP>::EPK, b_row);
           } else {
-            ptx::tma_load_2d(b_dst, &map_b0, fb, kb * BK, b_row);
-            ptx::tma_load_2d(b_dst + B_HALF_BYTES, &map_b0, fb, kb * BK, b_row + 128);
+            ptx::tma_load_2d(b_dst, &map_b0, fb, kb * Op<OP>::EPK, b_row);
+            ptx::tma_load_2d(b_dst + B_HALF_BYTES, &map_b0, fb, kb * Op<OP>::EPK, b_row + 128);
           }
           ++issued;
           if (++stage == STAGES) {
@@ -344,7 +400,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
             // +32 bytes of K per step = +2 in the descriptor's address field
-            ptx::mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+            mma_op<OP>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_op<OP>(BM, BN),
+                       (kb > kb0 || k > 0) ? 1u : 0u);
           }
           ptx::mma_commit(ptx::smem_addr(&st.empty[stage]));
           if (++stage == STAGES) {
@@ -383,8 +440,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool valid = r < rows;
       const long long orow = (long long)row0 + r;
       const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * BN);
+      // E4M3 scales of this row and of the tile's weight channels
+      float sa = 1.f;
+      const float* sb0 = nullptr;
+      const float* sb1 = nullptr;
+      if constexpr (OP == OP_E4M3) {
+        const long long wbase = (long long)t.s * args.b_rows + t.n * (EPI == EPI_SWIGLU ? 128 : 256);
+        sb0 = args.b_scale0 + wbase;
+        if (EPI == EPI_SWIGLU) {
+          sb1 = args.b_scale1 + wbase;
+          const long long arow = __ldg(seg + 3 + 2 * E + t.s) + r;  // x_perm row, or token
+          if (valid)
+            sa = __ldg((t.s >= args.n_routed ? args.a_scale_shared : args.a_scale) + arow);
+        } else if (valid) {
+          sa = __ldg(args.a_scale + orow);  // H row
+        }
+      }
       if (S == 1) {
-        epilogue_fused<EPI>(args, tbase, t, valid, orow, out);
+        epilogue_fused<EPI, OP>(args, tbase, t, valid, orow, out, sa, sb0, sb1);
         ptx::tc_fence_before();
         ptx::mbar_arrive(ptx::smem_addr(&st.acc_empty[acc]));
       } else {
@@ -399,6 +472,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (EPI == EPI_SWIGLU) ptx::tmem_ld32(tbase + 128 + c * 32, u);
           ptx::tmem_ld_wait();
           const int col0 = t.n * (EPI == EPI_SWIGLU ? 128 : 256) + c * 32;
+          if constexpr (OP == OP_E4M3) {  // partials carry their scales (sums are linear)
+            const int cb = c * 32;
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              const bool in = col0 + jj < args.n_out;
+              v[jj] = __float_as_uint(__uint_as_float(v[jj]) * sa * (in ? __ldg(sb0 + cb + jj) : 0.f));
+              if (EPI == EPI_SWIGLU)
+                u[jj] = __float_as_uint(__uint_as_float(u[jj]) * sa * (in ? __ldg(sb1 + cb + jj) : 0.f));
+            }
+          }
           if (valid) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -629,7 +712,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool valid = r < rows;
       const long long orow = (long long)__ldg(seg + 3 + 3 * E + t.s) + r;
       const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * BN);
-      epilogue_fused<EPI>(args, tbase, t, valid, orow, out);
+      epilogue_fused<EPI, OP_BF16>(args, tbase, t, valid, orow, out, 1.f, nullptr, nullptr);
       ptx::tc_fence_before();
       ptx::mbar_arrive_cluster(acc_empty_leader[acc]);
       if (++acc == NUM_ACC) {
@@ -685,7 +768,7 @@ struct DecodeShape {
   int a_bytes;      // weight bytes a stage (16 or 32 KB)
 };
 
-template <int EPI>
+template <int EPI, int OP>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_decode_kernel(const __grid_constant__ CUtensorMap map_w0,
                           const __grid_constant__ CUtensorMap map_w1,
@@ -701,7 +784,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int STG = shape.stages;
 
   const int32_t* seg = args.seg;
-  const int KB = (args.K + BK - 1) / BK;
+  const int KB = (args.K + Op<OP>::EPK - 1) / Op<OP>::EPK;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STG; ++i) {
@@ -769,10 +852,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t fb = ptx::smem_addr(&st.full[stage]);
           const uint32_t dst = ring + stage * shape.stage_bytes;
           ptx::mbar_arrive_expect_tx(fb, tx);
-          ptx::tma_load_2d(dst, &map_w0, fb, kb * BK, w_row);
-          if (EPI == EPI_SWIGLU) ptx::tma_load_2d(dst + A_BYTES, &map_w1, fb, kb * BK, w_row);
+          ptx::tma_load_2d(dst, &map_w0, fb, kb * Op<OP>::EPK, w_row);
+          if (EPI == EPI_SWIGLU) ptx::tma_load_2d(dst + A_BYTES, &map_w1, fb, kb * Op<OP>::EPK, w_row);
           for (int b = 0; b < nbox; ++b)
-            ptx::tma_load_2d(dst + shape.a_bytes + b * TOK_BOX_BYTES, tm, fb, kb * BK,
+            ptx::tma_load_2d(dst + shape.a_bytes + b * TOK_BOX_BYTES, tm, fb, kb * Op<OP>::EPK,
                              tok_row + b * TOK_BOX);
           ++issued;
           if (++stage == STG) {
@@ -801,7 +884,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const Tile t = decode_tile(seg, E, args.NT, unit / S);
         const int rows = __ldg(seg + 3 + E + t.s);
         const int ntok = ((rows + TOK_BOX - 1) / TOK_BOX) * TOK_BOX;
-        const uint32_t idesc = ptx::idesc_bf16_f32(BM, ntok);
+        const uint32_t idesc = idesc_op<OP>(BM, ntok);
         if (!wait_phase(ptx::smem_addr(&st.acc_empty[acc]), acc_phase ^ 1u, abort_flag,
                         args.status)) {
           ok = false;
@@ -824,8 +907,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
             const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
-            ptx::mma_bf16(d_tmem, w0 + 2 * k, tk + 2 * k, idesc, accum);
-            if (EPI == EPI_SWIGLU) ptx::mma_bf16(d_tmem + 128, w1 + 2 * k, tk + 2 * k, idesc, accum);
+            mma_op<OP>(d_tmem, w0 + 2 * k, tk + 2 * k, idesc, accum);
+            if (EPI == EPI_SWIGLU) mma_op<OP>(d_tmem + 128, w1 + 2 * k, tk + 2 * k, idesc, accum);
           }
           ptx::mma_commit(ptx::smem_addr(&st.empty[stage]));
           if (++stage == STG) {
@@ -863,28 +946,55 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int f = t.n * BM + j;
       const bool fvalid = f < args.n_out;
       const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * BN);
+      // E4M3: the feature's weight-channel scales and the tokens' row scales
+      float sw0 = 1.f, sw1 = 1.f;
+      const float* tok_scale = nullptr;
+      long long tok_row0 = 0;
+      if constexpr (OP == OP_E4M3) {
+        const long long wrow = (long long)t.s * args.b_rows + f;
+        sw0 = fvalid ? __ldg(args.b_scale0 + wrow) : 0.f;
+        if (EPI == EPI_SWIGLU) {
+          sw1 = fvalid ? __ldg(args.b_scale1 + wrow) : 0.f;
+          tok_row0 = __ldg(seg + 3 + 2 * E + t.s);
+          tok_scale = t.s >= args.n_routed ? args.a_scale_shared : args.a_scale;
+        } else {
+          tok_row0 = row0;
+          tok_scale = args.a_scale;
+        }
+      }
       for (int c0 = 0; c0 < rows; c0 += 32) {
         uint32_t a[32], b[32];
         ptx::tmem_ld32(tbase + c0, a);
         if (EPI == EPI_SWIGLU) ptx::tmem_ld32(tbase + 128 + c0, b);
         ptx::tmem_ld_wait();
         const int cn = min(32, rows - c0);
-        if (fvalid) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            if (c >= cn) break;
-            const long long orow = row0 + c0 + c;
-            const float av = __uint_as_float(a[c]);
-            if (S == 1) {
-              float h;
-              if (EPI == EPI_SWIGLU) h = silu(av) * __uint_as_float(b[c]);
-              else h = row_scale(args, t.s, orow) * av;
-              out[orow * args.ldo + f] = __float2bfloat16_rn(h);
-            } else {
-              float* prow = args.partial + ((long long)split * args.R + orow) * args.pc;
-              prow[f] = av;
-              if (EPI == EPI_SWIGLU) prow[args.n_out + f] = __uint_as_float(b[c]);
+        for (int c = 0; c < 32; ++c) {
+          if (c >= cn) break;  // cn is the same for the whole warp
+          const long long orow = row0 + c0 + c;
+          float av = __uint_as_float(a[c]);
+          float bv = EPI == EPI_SWIGLU ? __uint_as_float(b[c]) : 0.f;
+          if constexpr (OP == OP_E4M3) {
+            const float st = __ldg(tok_scale + tok_row0 + c0 + c);
+            av *= sw0 * st;
+            bv *= sw1 * st;
+          }
+          if (S == 1) {
+            __nv_bfloat16 hb;
+            if (EPI == EPI_SWIGLU) hb = __float2bfloat16_rn(silu(av) * bv);
+            else hb = __float2bfloat16_rn(row_scale(args, t.s, orow) * av);
+            if (fvalid) out[orow * args.ldo + f] = hb;
+            if constexpr (OP == OP_E4M3 && EPI == EPI_SWIGLU) {
+              // the H row's max |H| over this warp's 32 features, one atomic
+              float m = fvalid ? fabsf(__bfloat162float(hb)) : 0.f;
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+              if (lane == 0 && m > 0.f) atomicMax(args.h_amax + orow, __float_as_uint(m));
             }
+          } else if (fvalid) {
+            float* prow = args.partial + ((long long)split * args.R + orow) * args.pc;
+            prow[f] = av;
+            if (EPI == EPI_SWIGLU) prow[args.n_out + f] = bv;
           }
         }
       }
@@ -910,54 +1020,78 @@ __global__ void __launch_bounds__(THREADS, 1)
 // Split-K epilogue: every output element from the partials of all S splits,
 // summed in split order, then the same epilogue as the fused path. One
 // thread per 4 output columns of one row; its (up to kMaxSplitK) partial
-// loads are issued together before any is summed.
-template <int EPI>
+// loads are issued together before any is summed. E4M3 partials already
+// carry their scales; for gate/up the rows' max |H| is gathered per block in
+// shared memory (a block spans at most 256 rows) and sent with one atomic
+// per row.
+template <int EPI, int OP>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmArgs a, int gemm_grid) {
+  __shared__ unsigned s_max[256];
   pdl_wait();
   pdl_trigger();
   const int tiles = __ldg(a.seg + 1) * a.NT;
-  const int S = choose_splits(tiles, gemm_grid, (a.K + BK - 1) / BK, a.s_max);
+  const int S = choose_splits(tiles, gemm_grid, (a.K + Op<OP>::EPK - 1) / Op<OP>::EPK, a.s_max);
   if (S == 1) return;  // the GEMM finished its tiles itself
   const int groups = a.n_out / 4;
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= a.R * groups) return;
-  const long long orow = i / groups;
-  const int col = (int)(i % groups) * 4;
-  float4 pv[kMaxSplitK], pu[kMaxSplitK];
-#pragma unroll
-  for (int sp = 0; sp < kMaxSplitK; ++sp) {
-    if (sp < S) {
-      const float* src = a.partial + ((long long)sp * a.R + orow) * a.pc + col;
-      pv[sp] = __ldcg(reinterpret_cast<const float4*>(src));
-      if (EPI == EPI_SWIGLU) pu[sp] = __ldcg(reinterpret_cast<const float4*>(src + a.n_out));
-    }
+  const long long first_row = ((long long)blockIdx.x * blockDim.x) / groups;
+  constexpr bool kAmax = OP == OP_E4M3 && EPI == EPI_SWIGLU;
+  if (kAmax) {
+    s_max[threadIdx.x] = 0u;
+    __syncthreads();
   }
-  float v[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+  if (i < a.R * groups) {
+    const long long orow = i / groups;
+    const int col = (int)(i % groups) * 4;
+    float4 pv[kMaxSplitK], pu[kMaxSplitK];
 #pragma unroll
-  for (int sp = 0; sp < kMaxSplitK; ++sp) {
-    if (sp < S) {
-      v[0] += pv[sp].x; v[1] += pv[sp].y; v[2] += pv[sp].z; v[3] += pv[sp].w;
-      if (EPI == EPI_SWIGLU) {
-        u[0] += pu[sp].x; u[1] += pu[sp].y; u[2] += pu[sp].z; u[3] += pu[sp].w;
+    for (int sp = 0; sp < kMaxSplitK; ++sp) {
+      if (sp < S) {
+        const float* src = a.partial + ((long long)sp * a.R + orow) * a.pc + col;
+        pv[sp] = __ldcg(reinterpret_cast<const float4*>(src));
+        if (EPI == EPI_SWIGLU) pu[sp] = __ldcg(reinterpret_cast<const float4*>(src + a.n_out));
       }
     }
-  }
-  float h[4];
-  if (EPI == EPI_SWIGLU) {
+    float v[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) h[q] = silu(v[q]) * u[q];
-  } else {
-    // the row's segment: routed rows are [0, n_pairs), shared rows follow
-    const float sc = (orow < a.n_pairs) ? row_scale(a, 0, orow) : 1.0f;
+    for (int sp = 0; sp < kMaxSplitK; ++sp) {
+      if (sp < S) {
+        v[0] += pv[sp].x; v[1] += pv[sp].y; v[2] += pv[sp].z; v[3] += pv[sp].w;
+        if (EPI == EPI_SWIGLU) {
+          u[0] += pu[sp].x; u[1] += pu[sp].y; u[2] += pu[sp].z; u[3] += pu[sp].w;
+        }
+      }
+    }
+    float h[4];
+    if (EPI == EPI_SWIGLU) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) h[q] = sc * v[q];
+      for (int q = 0; q < 4; ++q) h[q] = silu(v[q]) * u[q];
+    } else {
+      // the row's segment: routed rows are [0, n_pairs), shared rows follow
+      const float sc = (orow < a.n_pairs) ? row_scale(a, 0, orow) : 1.0f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) h[q] = sc * v[q];
+    }
+    const uint32_t p0 = f32x2_to_bf16x2(h[0], h[1]), p1 = f32x2_to_bf16x2(h[2], h[3]);
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + orow * a.ldo + col;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(p0, p1);
+    if (kAmax) {
+      float r0, r1, r2, r3;
+      bf16x2_to_f32(p0, r0, r1);
+      bf16x2_to_f32(p1, r2, r3);
+      const float m = fmaxf(fmaxf(fabsf(r0), fabsf(r1)), fmaxf(fabsf(r2), fabsf(r3)));
+      atomicMax(&s_max[orow - first_row], __float_as_uint(m));
+    }
   }
-  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + orow * a.ldo + col;
-  *reinterpret_cast<uint2*>(dst) = make_uint2(f32x2_to_bf16x2(h[0], h[1]), f32x2_to_bf16x2(h[2], h[3]));
+  if (kAmax) {
+    __syncthreads();
+    const long long row = first_row + threadIdx.x;
+    if (s_max[threadIdx.x] != 0u && row < a.R) atomicMax(a.h_amax + row, s_max[threadIdx.x]);
+  }
 }
 
 // ---------------------------------------------------------------- host side --
-template <int EPI>
+template <int EPI, int OP>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_sh, const CUtensorMap& b0,
                         const CUtensorMap& b1, const GemmArgs& args, int max_tiles,
                         cudaStream_t s) {
@@ -965,7 +1099,7 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_sh, const CUt
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>,
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, OP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DYN_SMEM);
     if (e != cudaSuccess) return e;
     configured_device = dev;
@@ -976,17 +1110,17 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_sh, const CUt
   cudaError_t e;
   {
     ProfScope p(EPI == EPI_SWIGLU ? K_GATE_UP : K_DOWN, s);
-    e = launch_pdl(grouped_gemm_kernel<EPI>, dim3(grid), dim3(THREADS), DYN_SMEM, s, 1, a, a_sh, b0,
-                   b1, args);
+    e = launch_pdl(grouped_gemm_kernel<EPI, OP>, dim3(grid), dim3(THREADS), DYN_SMEM, s, 1, a,
+                   a_sh, b0, b1, args);
   }
   if (e != cudaSuccess || args.s_max <= 1) return e;
   const long long n = args.R * (args.n_out / 4);
   ProfScope p(K_SPLITK_REDUCE, s);
-  return launch_pdl(splitk_reduce_kernel<EPI>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, 1,
-                    args, grid);
+  return launch_pdl(splitk_reduce_kernel<EPI, OP>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0,
+                    s, 1, args, grid);
 }
 
-template <int EPI>
+template <int EPI, int OP>
 cudaError_t launch_decode(const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap& tok,
                           const CUtensorMap& tok_sh, const GemmArgs& args, int max_rows,
                           cudaStream_t s) {
@@ -994,7 +1128,7 @@ cudaError_t launch_decode(const CUtensorMap& w0, const CUtensorMap& w1, const CU
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_decode_kernel<EPI>,
+    cudaError_t e = cudaFuncSetAttribute(grouped_decode_kernel<EPI, OP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)DYN_SMEM_DECODE);
     if (e != cudaSuccess) return e;
@@ -1009,14 +1143,14 @@ cudaError_t launch_decode(const CUtensorMap& w0, const CUtensorMap& w1, const CU
   cudaError_t e;
   {
     ProfScope p(EPI == EPI_SWIGLU ? K_GATE_UP : K_DOWN, s);
-    e = launch_pdl(grouped_decode_kernel<EPI>, dim3(grid), dim3(THREADS), DYN_SMEM_DECODE, s, 1, w0,
-                   w1, tok, tok_sh, args, sh);
+    e = launch_pdl(grouped_decode_kernel<EPI, OP>, dim3(grid), dim3(THREADS), DYN_SMEM_DECODE, s, 1,
+                   w0, w1, tok, tok_sh, args, sh);
   }
   if (e != cudaSuccess || args.s_max <= 1) return e;
   const long long n = args.R * (args.n_out / 4);
   ProfScope p(K_SPLITK_REDUCE, s);
-  return launch_pdl(splitk_reduce_kernel<EPI>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, 1,
-                    args, grid);
+  return launch_pdl(splitk_reduce_kernel<EPI, OP>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0,
+                    s, 1, args, grid);
 }
 
 long long mt_bound_of(const moe_config& c, int tile_m) {
@@ -1164,6 +1298,8 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
   g.s_max = plan.s_max_gu;
   g.pc = 2 * c.d_ff;
   g.R = R;
+  g.a_scale = g.a_scale_shared = g.b_scale0 = g.b_scale1 = nullptr;
+  g.h_amax = nullptr;
   if (decode) {
     // token tiles of 16 rows over x_perm / x (gate/up) and H (down)
     CUtensorMap t_xp, t_x, t_h;
@@ -1174,7 +1310,7 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
                      make_map(&t_h, h, std::max(R, h_rows), c.d_ff, TOK_BOX);
     if (!ok2) return cudaErrorInvalidValue;
     const int max_rows = c.T;  // a segment holds at most T rows
-    cudaError_t e = launch_decode<EPI_SWIGLU>(m_wg, m_wu, t_xp, t_x, g, max_rows, s);
+    cudaError_t e = launch_decode<EPI_SWIGLU, OP_BF16>(m_wg, m_wu, t_xp, t_x, g, max_rows, s);
     if (e != cudaSuccess) return e;
     GemmArgs d = g;
     d.topk_w = topk_w;
@@ -1186,11 +1322,12 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
     d.b_rows = c.d_model;
     d.s_max = plan.s_max_dn;
     d.pc = c.d_model;
-    return launch_decode<EPI_DOWN>(m_wd, m_wd, t_h, t_h, d, max_rows, s);
+    return launch_decode<EPI_DOWN, OP_BF16>(m_wd, m_wd, t_h, t_h, d, max_rows, s);
   }
 
   cudaError_t e = pair ? launch_pair<EPI_SWIGLU>(m_xp, m_x, m_wg, m_wu, g, (int)(mt_bound * g.NT), s)
-                       : launch_gemm<EPI_SWIGLU>(m_xp, m_x, m_wg, m_wu, g, (int)(mt_bound * g.NT), s);
+                       : launch_gemm<EPI_SWIGLU, OP_BF16>(m_xp, m_x, m_wg, m_wu, g,
+                                                          (int)(mt_bound * g.NT), s);
   if (e != cudaSuccess) return e;
 
   GemmArgs d = g;
@@ -1204,7 +1341,100 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
   d.s_max = plan.s_max_dn;
   d.pc = c.d_model;
   return pair ? launch_pair<EPI_DOWN>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s)
-              : launch_gemm<EPI_DOWN>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s);
+              : launch_gemm<EPI_DOWN, OP_BF16>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s);
+}
+
+cudaError_t launch_grouped_e4m3(const moe_config& c, const uint8_t* xq_perm,
+                                const float* xp_scale, const uint8_t* xq, const float* x_scale,
+                                const int32_t* seg, const int32_t* sorted_pair,
+                                const float* topk_w, const uint8_t* wg_q, const float* wg_s,
+                                const uint8_t* wu_q, const float* wu_s, const uint8_t* wd_q,
+                                const float* wd_s, void* h, unsigned* h_amax, uint8_t* hq,
+                                float* h_scale, void* y_perm, float* partial, long long xp_rows,
+                                long long h_rows, int* status, cudaStream_t s) {
+  const long long P = (long long)c.T * c.top_k;
+  const int E = c.n_experts + c.n_shared;
+  const long long R = P + (long long)c.n_shared * c.T;
+  if (R == 0) return cudaSuccess;
+  const bool decode = c.T <= kDecodeMaxRows;
+  const long long mt_bound = mt_bound_of(c, BM);
+  const SplitKPlan plan = splitk_plan(c);
+  // A tensors: routed token rows (x_perm) and, for shared experts, x itself
+  const void* a_r = P > 0 ? (const void*)xq_perm : (const void*)xq;
+  const long long a_r_rows = P > 0 ? std::max(P, xp_rows) : c.T;
+  const void* a_s = c.n_shared > 0 ? (const void*)xq : a_r;
+  const long long a_s_rows = c.n_shared > 0 ? padded_rows(c.T) : a_r_rows;  // x_q is padded
+
+  GemmArgs g;
+  g.seg = seg;
+  g.sorted_pair = sorted_pair;
+  g.topk_w = nullptr;
+  g.out = h;
+  g.status = status;
+  g.ldo = c.d_ff;
+  g.n_routed = c.n_experts;
+  g.n_pairs = (int)P;
+  g.K = c.d_model;
+  g.n_out = c.d_ff;
+  g.NT = (c.d_ff + 127) / 128;
+  g.b_rows = c.d_ff;
+  g.partial = partial;
+  g.s_max = plan.s_max_gu;
+  g.pc = 2 * c.d_ff;
+  g.R = R;
+  g.a_scale = xp_scale;
+  g.a_scale_shared = x_scale;
+  g.b_scale0 = wg_s;
+  g.b_scale1 = wu_s;
+  g.h_amax = h_amax;
+  GemmArgs d = g;
+  d.topk_w = topk_w;
+  d.out = y_perm;
+  d.ldo = c.d_model;
+  d.K = c.d_ff;
+  d.n_out = c.d_model;
+  d.b_rows = c.d_model;
+  d.s_max = plan.s_max_dn;
+  d.pc = c.d_model;
+  d.a_scale = h_scale;
+  d.a_scale_shared = h_scale;
+  d.b_scale0 = wd_s;
+  d.b_scale1 = wd_s;
+  d.h_amax = nullptr;
+  // H (bf16, with its rows' max |H|) -> E4M3 codes and row scales
+  QuantArgs qh{};
+  qh.src = static_cast<const __nv_bfloat16*>(h);
+  qh.rows = R;
+  qh.cols = c.d_ff;
+  qh.amax_in = h_amax;
+  qh.q = hq;
+  qh.scale = h_scale;
+
+  CUtensorMap m_wg, m_wu, m_wd;
+  if (!make_map_u8(&m_wg, wg_q, (long long)E * c.d_ff, c.d_model) ||
+      !make_map_u8(&m_wu, wu_q, (long long)E * c.d_ff, c.d_model) ||
+      !make_map_u8(&m_wd, wd_q, (long long)E * c.d_model, c.d_ff))
+    return cudaErrorInvalidValue;
+  const unsigned box = decode ? TOK_BOX : (unsigned)BM;
+  CUtensorMap m_xp, m_x, m_h;
+  if (!make_map_u8(&m_xp, a_r, a_r_rows, c.d_model, box) ||
+      !make_map_u8(&m_x, a_s, a_s_rows, c.d_model, box) ||
+      !make_map_u8(&m_h, hq, std::max(R, h_rows), c.d_ff, box))
+    return cudaErrorInvalidValue;
+  cudaError_t e;
+  if (decode) {
+    const int max_rows = c.T;  // a segment holds at most T rows
+    e = launch_decode<EPI_SWIGLU, OP_E4M3>(m_wg, m_wu, m_xp, m_x, g, max_rows, s);
+    if (e == cudaSuccess) e = launch_quantize_rows(qh, s);
+    if (e != cudaSuccess) return e;
+    d.NT = (c.d_model + BM - 1) / BM;
+    return launch_decode<EPI_DOWN, OP_E4M3>(m_wd, m_wd, m_h, m_h, d, max_rows, s);
+  }
+  e = launch_gemm<EPI_SWIGLU, OP_E4M3>(m_xp, m_x, m_wg, m_wu, g, (int)(mt_bound * g.NT), s);
+  if (e == cudaSuccess) e = launch_quantize_rows(qh, s);
+  if (e != cudaSuccess) return e;
+  d.NT = (c.d_model + 255) / 256;
+  return launch_gemm<EPI_DOWN, OP_E4M3>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s);
 }
 
 }  // namespace moe

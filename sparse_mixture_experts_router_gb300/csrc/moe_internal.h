@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -59,6 +60,46 @@ cudaError_t launch_router_tc(const moe_config& c, const void* x, const void* w_r
                              const float* logit_bias, const float* sel_bias, float* logits_out,
                              int32_t* topk_idx, float* topk_w, int32_t* counts, float* prob_sum,
                              float* partials, int32_t* cpart, int* status, cudaStream_t s);
+// Row-wise E4M3 quantization (fp8.cu): output row r of q/scale comes from
+// source row r, or from token gather[r] / k; rows at or past *rows_dev are
+// skipped; amax_in, when set, gives each row's max |v| (fp32 bits); clear,
+// when set, zeroes clear[clear_base + i * clear_stride + r] for i < clear_n.
+struct QuantArgs {
+  const __nv_bfloat16* src;
+  long long rows;
+  int cols;                  // multiple of 8
+  const int32_t* gather;
+  int k;
+  long long src_rows;
+  const int32_t* rows_dev;
+  const unsigned* amax_in;
+  uint8_t* q;
+  float* scale;
+  unsigned* clear;
+  long long clear_base, clear_stride;
+  int clear_n;
+};
+cudaError_t launch_quantize_rows(const QuantArgs& a, cudaStream_t s);
+
+// The grouped SwiGLU GEMMs with E4M3 operands (1-CTA tiles, or swap-AB
+// decode tiles for T <= 64): gate/up from xq_perm / xq (shared experts)
+// writes H in bf16 and each H row's max |H|; H is quantized into hq; down
+// reads hq. Row scales as QuantArgs writes them; weight scales per output
+// channel [E][rows of one expert's matrix]. The segment table must be built
+// with kTileM rows a tile.
+cudaError_t launch_grouped_e4m3(const moe_config& c, const uint8_t* xq_perm,
+                                const float* xp_scale, const uint8_t* xq, const float* x_scale,
+                                const int32_t* seg, const int32_t* sorted_pair,
+                                const float* topk_w, const uint8_t* wg_q, const float* wg_s,
+                                const uint8_t* wu_q, const float* wu_s, const uint8_t* wd_q,
+                                const float* wd_s, void* h, unsigned* h_amax, uint8_t* hq,
+                                float* h_scale, void* y_perm, float* partial, long long xp_rows,
+                                long long h_rows, int* status, cudaStream_t s);
+// Row-major uint8 matrix [rows][cols] read in boxes of box_rows rows x 128
+// bytes with the 128-byte swizzle (the E4M3 operands).
+bool make_map_u8(CUtensorMap* m, const void* base, long long rows, long long cols,
+                 unsigned box_rows = 128u);
+
 // Zeroes the status word and the router's block counter (a kernel, so it
 // keeps the chain of programmatic dependent launches).
 cudaError_t launch_reset_status(int* status, cudaStream_t s);
@@ -68,7 +109,8 @@ int router_partial_blocks(const moe_config& c);
 int num_sms();
 
 // With seg != null it also builds the grouped GEMM's segment table (tile
-// height tile_m) from the offsets it computes. `counts` (pairs per expert,
+// height tile_m) from the offsets it computes; with x_perm == null it skips
+// the row gather. `counts` (pairs per expert,
 // as the router left them) may be null; when given, mid-sized batches take
 // their offsets from it instead of counting the pairs again.
 cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
@@ -142,6 +184,7 @@ enum KernelId {
   K_SPLITK_REDUCE,
   K_COMBINE,
   K_BALANCE,
+  K_QUANTIZE,
   K_NUM
 };
 void prof_begin(int id, cudaStream_t s);

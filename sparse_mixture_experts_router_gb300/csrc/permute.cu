@@ -491,6 +491,7 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
   if (P == 0) return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (N + 1), s);
   const int vec = (int)(c.d_model * elem_bytes(c.dtype) / 16);
   auto gather = [&]() {
+    if (x_perm == nullptr) return cudaSuccess;  // the caller gathers (FP8 layer: with quantization)
     ProfScope p(K_PERMUTE_GATHER, s);
     return launch_pdl(permute_gather_kernel, dim3(ceil_div(P, kWarps)), dim3(kThreads), 0, s, 1,
                       static_cast<const uint4*>(x), (const int32_t*)sorted_pair,
