@@ -509,7 +509,7 @@ int moe_layer_forward_fp8(const moe_config* cfg, const void* x, const void* w_ro
   if (c.T == 0) return MOE_OK;
   const long long P = pairs(c);
   e = launch_permute(c, x, idx, cnt, w.offsets, w.sorted_pair, w.inv_pos, nullptr, w.hist,
-                     w.status, w.seg, kTileM, s);
+                     w.status, w.seg, seg_tile_m(c), s);
   if (e != cudaSuccess) return fail_cuda(e);
   // routed rows: gathered and quantized in one pass; their H maxima cleared
   QuantArgs qa{};

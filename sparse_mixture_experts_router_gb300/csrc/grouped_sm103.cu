@@ -91,6 +91,14 @@ __device__ __forceinline__ void mma_op(uint32_t d, uint64_t a, uint64_t b, uint3
   else
     ptx::mma_e4m3(d, a, b, idesc, accumulate);
 }
+template <int OP>
+__device__ __forceinline__ void mma_op_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+  if constexpr (OP == OP_BF16)
+    ptx::mma_bf16_pair(d, a, b, idesc, accumulate);
+  else
+    ptx::mma_e4m3_pair(d, a, b, idesc, accumulate);
+}
 
 struct GemmArgs {
   const int32_t* seg;          // segment table (moe_internal.h)
@@ -262,6 +270,28 @@ __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tb
             *reinterpret_cast<uint4*>(dst + q * 8) =
                 make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
       }
+    }
+  }
+}
+
+// E4M3 epilogue scales of one accumulator row: the row's A scale (x_perm row
+// or token for gate/up, H row for down) and the tile's first weight-channel
+// scales (gate, up; or down). bf16: 1 and null.
+template <int EPI, int OP>
+__device__ __forceinline__ void row_scales(const GemmArgs& args, const int32_t* seg, int E,
+                                           const Tile& t, int r, bool valid, long long orow,
+                                           float& sa, const float*& sb0, const float*& sb1) {
+  sa = 1.f;
+  sb0 = sb1 = nullptr;
+  if constexpr (OP == OP_E4M3) {
+    const long long wbase = (long long)t.s * args.b_rows + t.n * (EPI == EPI_SWIGLU ? 128 : 256);
+    sb0 = args.b_scale0 + wbase;
+    if (EPI == EPI_SWIGLU) {
+      sb1 = args.b_scale1 + wbase;
+      const long long arow = __ldg(seg + 3 + 2 * E + t.s) + r;
+      if (valid) sa = __ldg((t.s >= args.n_routed ? args.a_scale_shared : args.a_scale) + arow);
+    } else if (valid) {
+      sa = __ldg(args.a_scale + orow);
     }
   }
 }
@@ -440,22 +470,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool valid = r < rows;
       const long long orow = (long long)row0 + r;
       const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * BN);
-      // E4M3 scales of this row and of the tile's weight channels
-      float sa = 1.f;
-      const float* sb0 = nullptr;
-      const float* sb1 = nullptr;
-      if constexpr (OP == OP_E4M3) {
-        const long long wbase = (long long)t.s * args.b_rows + t.n * (EPI == EPI_SWIGLU ? 128 : 256);
-        sb0 = args.b_scale0 + wbase;
-        if (EPI == EPI_SWIGLU) {
-          sb1 = args.b_scale1 + wbase;
-          const long long arow = __ldg(seg + 3 + 2 * E + t.s) + r;  // x_perm row, or token
-          if (valid)
-            sa = __ldg((t.s >= args.n_routed ? args.a_scale_shared : args.a_scale) + arow);
-        } else if (valid) {
-          sa = __ldg(args.a_scale + orow);  // H row
-        }
-      }
+      float sa;
+      const float* sb0;
+      const float* sb1;
+      row_scales<EPI, OP>(args, seg, E, t, r, valid, orow, sa, sb0, sb1);
       if (S == 1) {
         epilogue_fused<EPI, OP>(args, tbase, t, valid, orow, out, sa, sb0, sb1);
         ptx::tc_fence_before();
@@ -533,7 +551,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 constexpr int PSTAGES = 6;
 constexpr int P_STAGE_BYTES = A_BYTES + B_HALF_BYTES;               // 32 KB per CTA
 constexpr size_t DYN_SMEM_PAIR = (size_t)PSTAGES * P_STAGE_BYTES + 1024;
-constexpr uint32_t IDESC_PAIR = ptx::idesc_bf16_f32(2 * BM, BN);
 constexpr int PAIR_TILE_M = 2 * BM;
 
 struct __align__(8) PairState {
@@ -546,7 +563,7 @@ struct __align__(8) PairState {
   int abort;
 };
 
-template <int EPI>
+template <int EPI, int OP>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                              const __grid_constant__ CUtensorMap map_a_shared,
@@ -562,7 +579,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t ring = (ptx::smem_addr(dyn_smem) + 1023u) & ~1023u;
 
   const int32_t* seg = args.seg;  // built with 256-row tiles
-  const int KB = (args.K + BK - 1) / BK;
+  const int KB = (args.K + Op<OP>::EPK - 1) / Op<OP>::EPK;
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
@@ -629,8 +646,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t full_leader = ptx::mapa_shared(full_local, 0);
           const uint32_t a_dst = ring + stage * P_STAGE_BYTES;
           if (leader) ptx::mbar_arrive_expect_tx(full_local, 2 * P_STAGE_BYTES);
-          ptx::tma_load_2d_pair(a_dst, am, full_leader, kb * BK, a_row);
-          ptx::tma_load_2d_pair(a_dst + A_BYTES, bm, full_leader, kb * BK, b_row);
+          ptx::tma_load_2d_pair(a_dst, am, full_leader, kb * Op<OP>::EPK, a_row);
+          ptx::tma_load_2d_pair(a_dst + A_BYTES, bm, full_leader, kb * Op<OP>::EPK, b_row);
           ++issued;
           if (++stage == PSTAGES) {
             stage = 0;
@@ -673,7 +690,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint64_t bdesc = ptx::sdesc_k128(a_src + A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k)
-            ptx::mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC_PAIR, (kb | k) != 0);
+            mma_op_pair<OP>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_op<OP>(2 * BM, BN),
+                            (kb | k) != 0);
           ptx::mma_commit_pair(ptx::smem_addr(&st.empty[stage]), 0x3);
           if (++stage == PSTAGES) {
             stage = 0;
@@ -712,7 +730,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool valid = r < rows;
       const long long orow = (long long)__ldg(seg + 3 + 3 * E + t.s) + r;
       const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * BN);
-      epilogue_fused<EPI, OP_BF16>(args, tbase, t, valid, orow, out, 1.f, nullptr, nullptr);
+      float sa;
+      const float* sb0;
+      const float* sb1;
+      row_scales<EPI, OP>(args, seg, E, t, r, valid, orow, sa, sb0, sb1);
+      epilogue_fused<EPI, OP>(args, tbase, t, valid, orow, out, sa, sb0, sb1);
       ptx::tc_fence_before();
       ptx::mbar_arrive_cluster(acc_empty_leader[acc]);
       if (++acc == NUM_ACC) {
@@ -1165,11 +1187,14 @@ cudaError_t configure_pair_kernels() {
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device == dev) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI_SWIGLU>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DYN_SMEM_PAIR);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI_DOWN>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DYN_SMEM_PAIR);
+  const void* kernels[4] = {(const void*)grouped_gemm_pair_kernel<EPI_SWIGLU, OP_BF16>,
+                            (const void*)grouped_gemm_pair_kernel<EPI_DOWN, OP_BF16>,
+                            (const void*)grouped_gemm_pair_kernel<EPI_SWIGLU, OP_E4M3>,
+                            (const void*)grouped_gemm_pair_kernel<EPI_DOWN, OP_E4M3>};
+  cudaError_t e = cudaSuccess;
+  for (const void* k : kernels)
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DYN_SMEM_PAIR);
   if (e == cudaSuccess) configured_device = dev;
   return e;
 }
@@ -1199,7 +1224,8 @@ int max_pair_clusters() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<EPI_SWIGLU>, &cfg) != cudaSuccess)
+  if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<EPI_SWIGLU, OP_BF16>, &cfg) !=
+      cudaSuccess)
     n = 0;
   cudaGetLastError();  // clear a failed query
   cached_dev = dev;
@@ -1207,15 +1233,15 @@ int max_pair_clusters() {
   return n;
 }
 
-template <int EPI>
+template <int EPI, int OP>
 cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a_sh, const CUtensorMap& b0,
                         const CUtensorMap& b1, const GemmArgs& args, int max_tiles,
                         cudaStream_t s) {
   const int clusters = std::min(max_tiles, max_pair_clusters());
   if (clusters <= 0) return cudaSuccess;
   ProfScope p(EPI == EPI_SWIGLU ? K_GATE_UP : K_DOWN, s);
-  return launch_pdl(grouped_gemm_pair_kernel<EPI>, dim3(2 * clusters), dim3(THREADS), DYN_SMEM_PAIR,
-                    s, 2, a, a_sh, b0, b1, args);
+  return launch_pdl(grouped_gemm_pair_kernel<EPI, OP>, dim3(2 * clusters), dim3(THREADS),
+                    DYN_SMEM_PAIR, s, 2, a, a_sh, b0, b1, args);
 }
 
 
@@ -1325,7 +1351,8 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
     return launch_decode<EPI_DOWN, OP_BF16>(m_wd, m_wd, t_h, t_h, d, max_rows, s);
   }
 
-  cudaError_t e = pair ? launch_pair<EPI_SWIGLU>(m_xp, m_x, m_wg, m_wu, g, (int)(mt_bound * g.NT), s)
+  cudaError_t e = pair ? launch_pair<EPI_SWIGLU, OP_BF16>(m_xp, m_x, m_wg, m_wu, g,
+                                                         (int)(mt_bound * g.NT), s)
                        : launch_gemm<EPI_SWIGLU, OP_BF16>(m_xp, m_x, m_wg, m_wu, g,
                                                           (int)(mt_bound * g.NT), s);
   if (e != cudaSuccess) return e;
@@ -1340,7 +1367,7 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
   d.b_rows = c.d_model;
   d.s_max = plan.s_max_dn;
   d.pc = c.d_model;
-  return pair ? launch_pair<EPI_DOWN>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s)
+  return pair ? launch_pair<EPI_DOWN, OP_BF16>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s)
               : launch_gemm<EPI_DOWN, OP_BF16>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s);
 }
 
@@ -1356,9 +1383,14 @@ cudaError_t launch_grouped_e4m3(const moe_config& c, const uint8_t* xq_perm,
   const int E = c.n_experts + c.n_shared;
   const long long R = P + (long long)c.n_shared * c.T;
   if (R == 0) return cudaSuccess;
-  const bool decode = c.T <= kDecodeMaxRows;
-  const long long mt_bound = mt_bound_of(c, BM);
+  const bool pair = use_pair_tiles(c);
+  const bool decode = !pair && c.T <= kDecodeMaxRows;
+  const long long mt_bound = mt_bound_of(c, pair ? PAIR_TILE_M : BM);
   const SplitKPlan plan = splitk_plan(c);
+  if (pair) {
+    cudaError_t e = configure_pair_kernels();
+    if (e != cudaSuccess) return e;
+  }
   // A tensors: routed token rows (x_perm) and, for shared experts, x itself
   const void* a_r = P > 0 ? (const void*)xq_perm : (const void*)xq;
   const long long a_r_rows = P > 0 ? std::max(P, xp_rows) : c.T;
@@ -1430,11 +1462,13 @@ cudaError_t launch_grouped_e4m3(const moe_config& c, const uint8_t* xq_perm,
     d.NT = (c.d_model + BM - 1) / BM;
     return launch_decode<EPI_DOWN, OP_E4M3>(m_wd, m_wd, m_h, m_h, d, max_rows, s);
   }
-  e = launch_gemm<EPI_SWIGLU, OP_E4M3>(m_xp, m_x, m_wg, m_wu, g, (int)(mt_bound * g.NT), s);
+  e = pair ? launch_pair<EPI_SWIGLU, OP_E4M3>(m_xp, m_x, m_wg, m_wu, g, (int)(mt_bound * g.NT), s)
+           : launch_gemm<EPI_SWIGLU, OP_E4M3>(m_xp, m_x, m_wg, m_wu, g, (int)(mt_bound * g.NT), s);
   if (e == cudaSuccess) e = launch_quantize_rows(qh, s);
   if (e != cudaSuccess) return e;
   d.NT = (c.d_model + 255) / 256;
-  return launch_gemm<EPI_DOWN, OP_E4M3>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s);
+  return pair ? launch_pair<EPI_DOWN, OP_E4M3>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s)
+              : launch_gemm<EPI_DOWN, OP_E4M3>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s);
 }
 
 }  // namespace moe

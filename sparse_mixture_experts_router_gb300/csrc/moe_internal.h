@@ -81,12 +81,12 @@ struct QuantArgs {
 };
 cudaError_t launch_quantize_rows(const QuantArgs& a, cudaStream_t s);
 
-// The grouped SwiGLU GEMMs with E4M3 operands (1-CTA tiles, or swap-AB
-// decode tiles for T <= 64): gate/up from xq_perm / xq (shared experts)
+// The grouped SwiGLU GEMMs with E4M3 operands (CTA-pair, 1-CTA or swap-AB
+// decode tiles, chosen as for bf16): gate/up from xq_perm / xq (shared experts)
 // writes H in bf16 and each H row's max |H|; H is quantized into hq; down
 // reads hq. Row scales as QuantArgs writes them; weight scales per output
 // channel [E][rows of one expert's matrix]. The segment table must be built
-// with kTileM rows a tile.
+// with seg_tile_m(c) rows a tile.
 cudaError_t launch_grouped_e4m3(const moe_config& c, const uint8_t* xq_perm,
                                 const float* xp_scale, const uint8_t* xq, const float* x_scale,
                                 const int32_t* seg, const int32_t* sorted_pair,

@@ -105,7 +105,11 @@ def test_layer_fp8_small(oracle, w):
     check_fp8(oracle, w)
 
 
-FULL = [synth.MIXTRAL_PREFILL, synth.MIXTRAL_DECODE[0], synth.MIXTRAL_DECODE[3], synth.DEEPSEEK_V3]
+FULL = [synth.MIXTRAL_PREFILL, synth.MIXTRAL_DECODE[0], synth.MIXTRAL_DECODE[3], synth.DEEPSEEK_V3,
+        # CTA-pair tiles: >= 384 pairs per expert and no K split possible
+        # (fp32 partial rows of either projection would exceed 64 MB)
+        synth.Workload("fp8_pair_tiles", T=4096, d_model=2176, n_experts=8, top_k=2, d_ff=1024,
+                       n_shared=1, seed=58)]
 
 
 @pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
