@@ -66,11 +66,12 @@ def reduce_max(v: float, ws: int) -> float:
     return float(t.item())
 
 
-def recorded_traffic():
-    """DRAM bytes per gate/up launch from the committed ncu summary, or None
-    when the kernel sources changed since that capture."""
+def recorded_traffic(fp8=False):
+    """DRAM bytes per gate/up launch from the committed ncu summary (bf16 or
+    E4M3 kernel), or None when the kernel sources changed since that capture."""
     import hashlib
-    prof = os.path.join(ROOT, "profiles", "grouped_gemm_mixtral_8x7b_prefill.md")
+    prof = os.path.join(ROOT, "profiles", "grouped_gemm_fp8_mixtral_8x7b_prefill.md" if fp8
+                        else "grouped_gemm_mixtral_8x7b_prefill.md")
     csrc = os.path.join(ROOT, "sparse_mixture_experts_router_gb300", "csrc")
     try:
         text = open(prof).read()
@@ -376,7 +377,7 @@ def run_ours(args):
                 "achieved": round(ach, 1), "peak": round(tpk, 1), "unit": "TFLOP/s",
                 "frac": round(ach / tpk, 4),
                 "traffic": (args.traffic if args.traffic is not None
-                            else (None if args.fp8 else recorded_traffic())),
+                            else recorded_traffic(args.fp8)),
                 "peak_source": (f"{pk['source']} bf16 burst x 2 (nominal fp8/bf16 ratio)"
                                 if args.fp8 else f"{pk['source']} bf16 burst"),
                 "frac_of_sustained": round(ach / tpk_s, 4),
@@ -405,7 +406,7 @@ def run_ours(args):
 
     decode = run_decode(moe, synth, dev, stream, pk, args) if default and not args.no_decode else None
     E = w.n_experts + w.n_shared
-    wb = 3 * E * w.d_model * w.d_ff * 2
+    wb = 3 * E * w.d_model * w.d_ff * (1 if args.fp8 else 2)  # E4M3 codes: 1 byte each
     routing = {"max_over_mean_expert_load": round(float(counts.max()) / max(1e-9, float(counts.float().mean())), 3),
                "experts_with_tokens": int((counts > 0).sum())}
     if capacity_of(w):

@@ -26,14 +26,15 @@
 //    tiles b, b+grid, ...; the list length and segment table live on the
 //    device (no host synchronisation on the routing). Rows of a tile past its
 //    segment's end are computed on whatever rows follow and never stored.
-//  - Warp roles (192 threads): warp 0 issues TMA loads (128-byte swizzle,
+//  - Warp roles (320 threads): warp 0 issues TMA loads (128-byte swizzle,
 //    64-wide K blocks) into a 4-stage shared-memory ring; warp 1 allocates
 //    512 TMEM columns (two 256-column accumulators) and issues tcgen05.mma
 //    from one thread, releasing ring slots and publishing finished
-//    accumulators with tcgen05.commit; warps 2-5 drain an accumulator with
-//    tcgen05.ld (each warp owns the 32 TMEM lanes its index allows), apply
-//    the SwiGLU or gate-weight epilogue and store bf16 rows, while the MMA
-//    warp fills the other accumulator.
+//    accumulators with tcgen05.commit; warps 2-9 drain an accumulator with
+//    tcgen05.ld (each warp owns the 32 TMEM lanes its index allows, two
+//    warps per lane quarter, each taking half the columns), apply the SwiGLU
+//    or gate-weight epilogue and store bf16 rows, while the MMA warp fills
+//    the other accumulator.
 //  - Every wait is bounded (2 s of %globaltimer). A wait that runs out
 //    records MOE_ERR_TIMEOUT in the status word and sets a shared abort flag
 //    that ends the other roles' loops; the producer then waits (bounded) for
@@ -63,8 +64,14 @@ constexpr int B_BYTES = BN * BK * 2;           // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES; // 48 KB
 constexpr int NUM_ACC = 2;
 constexpr int TMEM_COLS = BN * NUM_ACC;        // 512
-constexpr int THREADS = 192;
+constexpr int THREADS = 192;      // decode kernel: producer, MMA, 4 epilogue warps
 constexpr int EPI_THREADS = 128;
+// Grouped and pair kernels: two epilogue warps per TMEM lane quarter, each
+// draining half of the accumulator's columns, so the epilogue keeps up with
+// the MMA at the E4M3 rate.
+constexpr int EPI_WARPS = 8;
+constexpr int G_EPI_THREADS = 32 * EPI_WARPS;  // 256
+constexpr int G_THREADS = 64 + G_EPI_THREADS;  // 320
 constexpr size_t DYN_SMEM = (size_t)STAGES * STAGE_BYTES + 1024;  // + 1 KB alignment slack
 
 enum { EPI_SWIGLU = 0, EPI_DOWN = 1 };
@@ -159,7 +166,28 @@ __device__ __forceinline__ Tile decode_tile(const int32_t* __restrict__ seg, int
   return Tile{lo, local % mt, local / mt};
 }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+// SiLU(g) = g * sigmoid(g). The quotient is the fast reciprocal-multiply
+// (a few ulp in fp32, far below the bf16 rounding of the result); as g goes
+// to -inf the divisor overflows to inf and the result goes to -0, the limit.
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+// Eight consecutive channel scales times a row scale, from two warp-uniform
+// 16-byte loads (p 16-byte aligned); zeros when the group is past the output.
+__device__ __forceinline__ void load_scales8(const float* p, bool in, float row, float (&s)[8]) {
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+  if (in) {
+    a = __ldg(reinterpret_cast<const float4*>(p));
+    b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  }
+  s[0] = row * a.x;
+  s[1] = row * a.y;
+  s[2] = row * a.z;
+  s[3] = row * a.w;
+  s[4] = row * b.x;
+  s[5] = row * b.y;
+  s[6] = row * b.z;
+  s[7] = row * b.w;
+}
 
 // Split factor of every tile when there are fewer tiles than two waves of
 // CTAs: among S in [1, s_max] with at least kMinKbPerSplit K blocks per
@@ -195,36 +223,47 @@ __device__ __forceinline__ float row_scale(const GemmArgs& a, int seg_id, long l
 
 // The fused epilogue of one 128-row accumulator: each thread drains its
 // TMEM lane (row) 32 columns at a time and stores bf16 (SwiGLU of the paired
-// gate/up columns, or the gate-weighted down projection). Rows past the
-// segment's end (valid = false) are loaded but not stored. E4M3 operands:
+// gate/up columns, or the gate-weighted down projection). Two warps share a
+// lane quarter; `half` picks which half of the columns this one drains. Rows
+// past the segment's end (valid = false) are loaded but not stored. E4M3:
 // sa is the row's A scale and sb0/sb1 point at the tile's first weight
 // channel scale (gate, up; or down); gate/up also records the row's max |H|.
 template <int EPI, int OP>
 __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tbase, const Tile& t,
-                                               bool valid, long long orow, __nv_bfloat16* out,
-                                               float sa, const float* sb0, const float* sb1) {
+                                               int half, bool valid, long long orow,
+                                               __nv_bfloat16* out, float sa, const float* sb0,
+                                               const float* sb1) {
   if (EPI == EPI_SWIGLU) {
     float hmax = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 2 * half; c < 2 * half + 2; ++c) {
       uint32_t g[32], u[32];
       ptx::tmem_ld32(tbase + c * 32, g);
       ptx::tmem_ld32(tbase + 128 + c * 32, u);
-      ptx::tmem_ld_wait();
       const int col0 = t.n * 128 + c * 32;
-      if (valid) {
-        uint32_t pk[16];
+      ptx::tmem_ld_wait();
+      uint32_t pk[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+      for (int q = 0; q < 4; ++q) {
+        // E4M3: the 8 gate and 8 up channel scales of this column group, one
+        // warp-uniform 16-byte load each (n_out is a multiple of 16, so a
+        // group is wholly inside or wholly past it)
+        float sg[8], su[8];
+        if constexpr (OP == OP_E4M3) {
+          const bool in = col0 + q * 8 < args.n_out;
+          load_scales8(sb0 + c * 32 + q * 8, in, sa, sg);
+          load_scales8(sb1 + c * 32 + q * 8, in, sa, su);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = 4 * q + jj;
           float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
           float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
           if constexpr (OP == OP_E4M3) {
-            const int cc = c * 32 + 2 * j;
-            const bool in0 = col0 + 2 * j < args.n_out, in1 = col0 + 2 * j + 1 < args.n_out;
-            g0 *= sa * (in0 ? __ldg(sb0 + cc) : 0.f);
-            u0 *= sa * (in0 ? __ldg(sb1 + cc) : 0.f);
-            g1 *= sa * (in1 ? __ldg(sb0 + cc + 1) : 0.f);
-            u1 *= sa * (in1 ? __ldg(sb1 + cc + 1) : 0.f);
+            g0 *= sg[2 * jj];
+            g1 *= sg[2 * jj + 1];
+            u0 *= su[2 * jj];
+            u1 *= su[2 * jj + 1];
           }
           pk[j] = f32x2_to_bf16x2(silu(g0) * u0, silu(g1) * u1);
           if constexpr (OP == OP_E4M3) {
@@ -233,6 +272,8 @@ __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tb
             hmax = fmaxf(hmax, fmaxf(fabsf(h0), fabsf(h1)));
           }
         }
+      }
+      if (valid) {
         __nv_bfloat16* dst = out + orow * args.ldo + col0;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
@@ -246,23 +287,32 @@ __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tb
   } else {
     const float scale = valid ? row_scale(args, t.s, orow) * sa : 0.0f;
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 4 * half; c < 4 * half + 4; ++c) {
       uint32_t v[32];
       ptx::tmem_ld32(tbase + c * 32, v);
-      ptx::tmem_ld_wait();
       const int col0 = t.n * 256 + c * 32;
-      if (valid) {
-        uint32_t pk[16];
+      ptx::tmem_ld_wait();
+      uint32_t pk[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          float y0 = scale * __uint_as_float(v[2 * j]), y1 = scale * __uint_as_float(v[2 * j + 1]);
+      for (int q = 0; q < 4; ++q) {
+        float sd[8];
+        if constexpr (OP == OP_E4M3)
+          load_scales8(sb0 + c * 32 + q * 8, col0 + q * 8 < args.n_out, scale, sd);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = 4 * q + jj;
+          float y0 = __uint_as_float(v[2 * j]), y1 = __uint_as_float(v[2 * j + 1]);
           if constexpr (OP == OP_E4M3) {
-            const int cc = c * 32 + 2 * j;
-            y0 *= col0 + 2 * j < args.n_out ? __ldg(sb0 + cc) : 0.f;
-            y1 *= col0 + 2 * j + 1 < args.n_out ? __ldg(sb0 + cc + 1) : 0.f;
+            y0 *= sd[2 * jj];
+            y1 *= sd[2 * jj + 1];
+          } else {
+            y0 *= scale;
+            y1 *= scale;
           }
           pk[j] = f32x2_to_bf16x2(y0, y1);
         }
+      }
+      if (valid) {
         __nv_bfloat16* dst = out + orow * args.ldo + col0;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
@@ -297,7 +347,7 @@ __device__ __forceinline__ void row_scales(const GemmArgs& args, const int32_t* 
 }
 
 template <int EPI, int OP>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(G_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_a_shared,
                         const __grid_constant__ CUtensorMap map_b0,
@@ -319,7 +369,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int i = 0; i < NUM_ACC; ++i) {
       ptx::mbar_init(ptx::smem_addr(&st.acc_full[i]), 1);
-      ptx::mbar_init(ptx::smem_addr(&st.acc_empty[i]), EPI_THREADS);
+      ptx::mbar_init(ptx::smem_addr(&st.acc_empty[i]), G_EPI_THREADS);
     }
     ptx::mbar_init(ptx::smem_addr(&st.drain), 1);
     st.abort = 0;
@@ -454,6 +504,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ----------------------------------------------------------- epilogue --
     const int sub = warp & 3;  // TMEM lanes [32*sub, 32*sub+32) are this warp's
+    const int half = (warp - 2) >> 2;  // which half of the columns
     const int row_in_tile = sub * 32 + lane;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
     int acc = 0;
@@ -475,29 +526,33 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float* sb1;
       row_scales<EPI, OP>(args, seg, E, t, r, valid, orow, sa, sb0, sb1);
       if (S == 1) {
-        epilogue_fused<EPI, OP>(args, tbase, t, valid, orow, out, sa, sb0, sb1);
+        epilogue_fused<EPI, OP>(args, tbase, t, half, valid, orow, out, sa, sb0, sb1);
         ptx::tc_fence_before();
         ptx::mbar_arrive(ptx::smem_addr(&st.acc_empty[acc]));
       } else {
         // Split-K unit: this split's fp32 partial rows; splitk_reduce_kernel
         // sums the splits in order and applies the epilogue.
         float* prow = args.partial + ((long long)split * args.R + orow) * args.pc;
-        constexpr int CHUNKS = (EPI == EPI_SWIGLU) ? 4 : 8;
+        constexpr int HALF_CHUNKS = (EPI == EPI_SWIGLU) ? 2 : 4;
 #pragma unroll 1
-        for (int c = 0; c < CHUNKS; ++c) {
+        for (int c = half * HALF_CHUNKS; c < (half + 1) * HALF_CHUNKS; ++c) {
           uint32_t v[32], u[32];
           ptx::tmem_ld32(tbase + c * 32, v);
           if (EPI == EPI_SWIGLU) ptx::tmem_ld32(tbase + 128 + c * 32, u);
-          ptx::tmem_ld_wait();
           const int col0 = t.n * (EPI == EPI_SWIGLU ? 128 : 256) + c * 32;
+          float my0 = 0.f, my1 = 0.f;  // E4M3: lane l fetches column l's scales
+          if constexpr (OP == OP_E4M3)
+            if (col0 + (threadIdx.x % 32) < args.n_out) {
+              my0 = __ldg(sb0 + c * 32 + threadIdx.x % 32);
+              if (EPI == EPI_SWIGLU) my1 = __ldg(sb1 + c * 32 + threadIdx.x % 32);
+            }
+          ptx::tmem_ld_wait();
           if constexpr (OP == OP_E4M3) {  // partials carry their scales (sums are linear)
-            const int cb = c * 32;
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
-              const bool in = col0 + jj < args.n_out;
-              v[jj] = __float_as_uint(__uint_as_float(v[jj]) * sa * (in ? __ldg(sb0 + cb + jj) : 0.f));
+              v[jj] = __float_as_uint(__uint_as_float(v[jj]) * sa * __shfl_sync(0xffffffffu, my0, jj));
               if (EPI == EPI_SWIGLU)
-                u[jj] = __float_as_uint(__uint_as_float(u[jj]) * sa * (in ? __ldg(sb1 + cb + jj) : 0.f));
+                u[jj] = __float_as_uint(__uint_as_float(u[jj]) * sa * __shfl_sync(0xffffffffu, my1, jj));
             }
           }
           if (valid) {
@@ -564,7 +619,7 @@ struct __align__(8) PairState {
 };
 
 template <int EPI, int OP>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(G_THREADS, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                              const __grid_constant__ CUtensorMap map_a_shared,
                              const __grid_constant__ CUtensorMap map_b0,
@@ -589,7 +644,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int i = 0; i < NUM_ACC; ++i) {
       ptx::mbar_init(ptx::smem_addr(&st.acc_full[i]), 1);
-      ptx::mbar_init(ptx::smem_addr(&st.acc_empty[i]), 2 * EPI_THREADS);
+      ptx::mbar_init(ptx::smem_addr(&st.acc_empty[i]), 2 * G_EPI_THREADS);
     }
     ptx::mbar_init(ptx::smem_addr(&st.drain), 1);
     st.abort = 0;
@@ -713,11 +768,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ------------------------------------------------ epilogue (both CTAs) --
     const int sub = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row_in_tile = sub * 32 + lane;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
-    const uint32_t acc_empty_leader[NUM_ACC] = {
-        ptx::mapa_shared(ptx::smem_addr(&st.acc_empty[0]), 0),
-        ptx::mapa_shared(ptx::smem_addr(&st.acc_empty[1]), 0)};
+    static_assert(NUM_ACC == 2, "two accumulators");
+    const uint32_t acc_empty_leader0 = ptx::mapa_shared(ptx::smem_addr(&st.acc_empty[0]), 0);
+    const uint32_t acc_empty_leader1 = ptx::mapa_shared(ptx::smem_addr(&st.acc_empty[1]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = cluster; tile < tiles; tile += nclusters) {
@@ -734,9 +790,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float* sb0;
       const float* sb1;
       row_scales<EPI, OP>(args, seg, E, t, r, valid, orow, sa, sb0, sb1);
-      epilogue_fused<EPI, OP>(args, tbase, t, valid, orow, out, sa, sb0, sb1);
+      epilogue_fused<EPI, OP>(args, tbase, t, half, valid, orow, out, sa, sb0, sb1);
       ptx::tc_fence_before();
-      ptx::mbar_arrive_cluster(acc_empty_leader[acc]);
+      ptx::mbar_arrive_cluster(acc ? acc_empty_leader1 : acc_empty_leader0);
       if (++acc == NUM_ACC) {
         acc = 0;
         acc_phase ^= 1u;
@@ -1132,7 +1188,7 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_sh, const CUt
   cudaError_t e;
   {
     ProfScope p(EPI == EPI_SWIGLU ? K_GATE_UP : K_DOWN, s);
-    e = launch_pdl(grouped_gemm_kernel<EPI, OP>, dim3(grid), dim3(THREADS), DYN_SMEM, s, 1, a,
+    e = launch_pdl(grouped_gemm_kernel<EPI, OP>, dim3(grid), dim3(G_THREADS), DYN_SMEM, s, 1, a,
                    a_sh, b0, b1, args);
   }
   if (e != cudaSuccess || args.s_max <= 1) return e;
@@ -1214,7 +1270,7 @@ int max_pair_clusters() {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (num_sms() / 2));
-  cfg.blockDim = dim3(THREADS);
+  cfg.blockDim = dim3(G_THREADS);
   cfg.dynamicSmemBytes = DYN_SMEM_PAIR;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1240,7 +1296,7 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a_sh, const CUt
   const int clusters = std::min(max_tiles, max_pair_clusters());
   if (clusters <= 0) return cudaSuccess;
   ProfScope p(EPI == EPI_SWIGLU ? K_GATE_UP : K_DOWN, s);
-  return launch_pdl(grouped_gemm_pair_kernel<EPI, OP>, dim3(2 * clusters), dim3(THREADS),
+  return launch_pdl(grouped_gemm_pair_kernel<EPI, OP>, dim3(2 * clusters), dim3(G_THREADS),
                     DYN_SMEM_PAIR, s, 2, a, a_sh, b0, b1, args);
 }
 
