@@ -76,6 +76,14 @@ def _declare(lib):
                                          _P, _P]
     lib.oracle_selection_margin.argtypes = [_I, _I, _I, _P, _P, _P]
     lib.oracle_order_margin.argtypes = [_I, _I, _I, _P, _P, _P]
+    _D = ctypes.c_double
+    lib.oracle_layer_backward.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P,
+                                          _P, _P, _P, _P, _P, _D, _D, _P, _P, _P, _P, _P]
+    lib.oracle_layer_backward.restype = None
+    lib.oracle_backward_samples.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P,
+                                            _P, _P, _P, _P, _P, _D, _D, _I, _P, _P, _I, _P, _P,
+                                            _P, _P, _P]
+    lib.oracle_backward_samples.restype = None
     return lib
 
 
@@ -320,3 +328,61 @@ class Oracle:
         y = self.layer_rows(x, experts, idx, w, rows, N, n_shared, keep, fp8)
         return dict(r32=r32, topk_idx=idx, topk_w=w, counts=counts,
                     prob_sum=prob_sum, keep=keep, y=y, rows=rows)
+
+    def _bwd_inputs(self, x, w_router, wg, wu, wd, k, dy, logit_bias, sel_bias):
+        xd, x = _stored(x)
+        wdt, w_router = _stored(w_router)
+        mats = []
+        for m in (wg, wu, wd):
+            dt, m = _stored(m)
+            assert dt == wdt, "weights share one stored type"
+            mats.append(m)
+        T, d = x.shape
+        N = w_router.shape[0]
+        E, d_ff = mats[0].shape[0], mats[0].shape[1]
+        lb = None if logit_bias is None else _c(logit_bias, np.float64)
+        sb = None if sel_bias is None else _c(sel_bias, np.float32)
+        dy = _c(dy, np.float64)
+        assert dy.shape == (T, d)
+        return xd, x, wdt, w_router, mats, T, d, N, E, d_ff, lb, sb, dy
+
+    def layer_backward(self, x, w_router, wg, wu, wd, k, dy, gate_mode=GATE_TOPK_SOFTMAX,
+                       logit_bias=None, sel_bias=None, n_shared=0, capacity=0, alpha=0.01,
+                       aux_grad=1.0):
+        """Gradients of sum(dy * y) + aux_grad * aux for all tokens (routing
+        held fixed): dict of dx [T,d], dw_router [N,d], dw_gate / dw_up
+        [E,d_ff,d], dw_down [E,d,d_ff], fp64. Stacked weight arrays, shared
+        experts last (E = N + n_shared)."""
+        (xd, x, wdt, w_router, mats, T, d, N, E, d_ff, lb, sb,
+         dy) = self._bwd_inputs(x, w_router, wg, wu, wd, k, dy, logit_bias, sel_bias)
+        assert E == N + n_shared
+        out = dict(dx=np.empty((T, d)), dw_router=np.empty((N, d)),
+                   dw_gate=np.empty((E, d_ff, d)), dw_up=np.empty((E, d_ff, d)),
+                   dw_down=np.empty((E, d, d_ff)))
+        self.lib.oracle_layer_backward(
+            T, d, d_ff, N, k, n_shared, gate_mode, capacity, xd, _ptr(x), wdt, _ptr(w_router),
+            _ptr(lb), _ptr(sb), _ptr(mats[0]), _ptr(mats[1]), _ptr(mats[2]), _ptr(dy),
+            float(alpha), float(aux_grad), _ptr(out["dx"]), _ptr(out["dw_router"]),
+            _ptr(out["dw_gate"]), _ptr(out["dw_up"]), _ptr(out["dw_down"]))
+        return out
+
+    def backward_samples(self, x, w_router, wg, wu, wd, k, dy, tokens=(), columns=(),
+                         gate_mode=GATE_TOPK_SOFTMAX, logit_bias=None, sel_bias=None,
+                         n_shared=0, capacity=0, alpha=0.01, aux_grad=1.0):
+        """The same gradients at sampled places: dx rows of ``tokens``; for
+        each (e, j) of ``columns`` the row j of dw_gate[e] and dw_up[e] and
+        the column j of dw_down[e] (each length d)."""
+        (xd, x, wdt, w_router, mats, T, d, N, E, d_ff, lb, sb,
+         dy) = self._bwd_inputs(x, w_router, wg, wu, wd, k, dy, logit_bias, sel_bias)
+        toks = _c(list(tokens), np.int32)
+        cols = np.asarray(list(columns), np.int32).reshape(-1, 2)
+        we, wj = _c(cols[:, 0], np.int32), _c(cols[:, 1], np.int32)
+        out = dict(dx_rows=np.empty((toks.size, d)), dw_gate_rows=np.empty((we.size, d)),
+                   dw_up_rows=np.empty((we.size, d)), dw_down_cols=np.empty((we.size, d)))
+        self.lib.oracle_backward_samples(
+            T, d, d_ff, N, k, n_shared, gate_mode, capacity, xd, _ptr(x), wdt, _ptr(w_router),
+            _ptr(lb), _ptr(sb), _ptr(mats[0]), _ptr(mats[1]), _ptr(mats[2]), _ptr(dy),
+            float(alpha), float(aux_grad), toks.size, _ptr(toks), _ptr(out["dx_rows"]), we.size,
+            _ptr(we), _ptr(wj), _ptr(out["dw_gate_rows"]), _ptr(out["dw_up_rows"]),
+            _ptr(out["dw_down_cols"]))
+        return out

@@ -1,5 +1,6 @@
 /*
- * CPU oracle for the sparse top-k Mixture-of-Experts FFN layer forward.
+ * CPU oracle for the sparse top-k Mixture-of-Experts FFN layer: the forward,
+ * and its gradient (the backward section at the end).
  *
  * TEST INFRASTRUCTURE ONLY. This file is the plain, slow, obviously correct
  * definition that the CUDA library is checked against. Only the test suite,
@@ -595,4 +596,359 @@ void oracle_order_margin(int T, int N, int k, const double* r64,
     margin[t] = g;
   }
   free(key);
+}
+
+/* ------------------------------------------------------------ backward ----
+ * Gradient of the scalar
+ *     L = sum_t sum_c dy[t][c] * y[t][c] + aux_grad * aux,
+ *     aux = alpha * N * sum_i f_i * P_i,
+ * with respect to x, W_r, W_g, W_u and W_d, where y is the layer output
+ * ([P1] the layer equation) and aux the balance term ([P1] "Keeping the
+ * experts busy"; [P2] the auxiliary-loss formula). Readings:
+ *  - The top-k choice, the capacity cut and the counts (so f) are hard
+ *    decisions and stay fixed; the gradient flows through the gate weights g
+ *    and through P ([P2]: f comes from a hard choice and is not
+ *    differentiated, the gradient flows through P).
+ *  - The fp32 rounding of the score only fixes the routing decision and is
+ *    taken as the identity: g and P are differentiated as the functions of
+ *    the score r they are defined as, at the forward's values (the score
+ *    rounded to fp32, as the forward evaluates them).
+ *  - logit_bias and sel_bias are constants.
+ * Everything is the chain rule through the forward's steps, in fp64. The
+ * weights are the stacked [N+n_shared] arrays (shared experts last). */
+
+static size_t elem_size(int dtype) {
+  return dtype == ORACLE_F64 ? 8 : dtype == ORACLE_F32 ? 4 : 2;
+}
+static const void* elem_ptr(int dtype, const void* base, size_t i) {
+  return (const char*)base + i * elem_size(dtype);
+}
+
+/* SiLU'(z) = s * (1 + z * (1 - s)) with s = 1 / (1 + e^-z). */
+static double silu_grad(double z) {
+  const double s = 1.0 / (1.0 + exp(-z));
+  return s * (1.0 + z * (1.0 - s));
+}
+
+/* One expert term of one token and its backward. With a = Wg x, b = Wu x,
+ * h = SiLU(a) * b and o = Wd h (the expert of oracle_expert_swiglu), the term
+ * adds G * o to y, so
+ *   do = G * dy,  dh = Wd^T do,  da = dh * b * SiLU'(a),  db = dh * SiLU(a),
+ *   dx += Wg^T da + Wu^T db,
+ * and dL/dG = <dy, o>, which is returned. h, da, db and do are left for the
+ * weight gradients (dWg += da x^T, dWu += db x^T, dWd += do h^T). */
+static double expert_backward(int d, int d_ff, int wdtype, const void* wg, const void* wu,
+                              const void* wd, const double* xt, const double* dyt, double G,
+                              double* h, double* da, double* db, double* dout, double* dxt) {
+  double* a = (double*)malloc(sizeof(double) * (size_t)d_ff);
+  double* b = (double*)malloc(sizeof(double) * (size_t)d_ff);
+  for (int j = 0; j < d_ff; ++j) {
+    double aj = 0.0, bj = 0.0;
+    for (int i = 0; i < d; ++i) {
+      aj += widen(wdtype, wg, (size_t)j * d + i) * xt[i];
+      bj += widen(wdtype, wu, (size_t)j * d + i) * xt[i];
+    }
+    a[j] = aj;
+    b[j] = bj;
+    h[j] = silu(aj) * bj;
+  }
+  double dG = 0.0;
+  for (int c = 0; c < d; ++c) {
+    double o = 0.0;
+    for (int j = 0; j < d_ff; ++j) o += widen(wdtype, wd, j + (size_t)c * d_ff) * h[j];
+    dG += dyt[c] * o;
+    dout[c] = G * dyt[c];
+  }
+  for (int j = 0; j < d_ff; ++j) {
+    double dh = 0.0;
+    for (int c = 0; c < d; ++c) dh += widen(wdtype, wd, j + (size_t)c * d_ff) * dout[c];
+    da[j] = dh * b[j] * silu_grad(a[j]);
+    db[j] = dh * silu(a[j]);
+  }
+  for (int i = 0; i < d; ++i) {
+    double acc = 0.0;
+    for (int j = 0; j < d_ff; ++j)
+      acc += widen(wdtype, wg, (size_t)j * d + i) * da[j] +
+             widen(wdtype, wu, (size_t)j * d + i) * db[j];
+    dxt[i] = acc;
+  }
+  free(a);
+  free(b);
+  return dG;
+}
+
+/* Score gradient of one token. r: its scores (fp32 values widened), idx:
+ * its k experts, dG[s]: dL/dg_s, f: the balance fractions. Gates, by mode:
+ *  TOPK_SOFTMAX: g = softmax of the k kept scores, so
+ *    dr[idx_s] += g_s * (dG_s - sum_l g_l dG_l);
+ *  ALL_SOFTMAX_RENORM: p = softmax(r) over all N, Z = sum_s p[idx_s],
+ *    g_s = p[idx_s] / Z, so dp[idx_s] = (dG_s - sum_l g_l dG_l) / Z and
+ *    dr_i += p_i * (dp_i - sum_m p_m dp_m).
+ * Balance term: P_i = (1/T) sum_t p_t[i], so
+ *    dr_i += aux_grad * alpha * N / T * p_i * (f_i - sum_m p_m f_m). */
+static void score_backward(int N, int k, int T, int gate_mode, const double* r,
+                           const int32_t* idx, const double* dG, const double* f, double alpha,
+                           double aux_grad, double* dr) {
+  double* g = (double*)malloc(sizeof(double) * (size_t)k);
+  double* p = (double*)malloc(sizeof(double) * (size_t)N);
+  double* dp = (double*)calloc((size_t)N, sizeof(double));
+  for (int i = 0; i < N; ++i) dr[i] = 0.0;
+  oracle_gates(N, k, gate_mode, r, idx, g);
+  oracle_softmax(N, r, p);
+  double gdG = 0.0;
+  for (int s = 0; s < k; ++s) gdG += g[s] * dG[s];
+  if (gate_mode == ORACLE_GATE_TOPK_SOFTMAX) {
+    for (int s = 0; s < k; ++s) dr[idx[s]] += g[s] * (dG[s] - gdG);
+  } else {
+    double Z = 0.0;
+    for (int s = 0; s < k; ++s) Z += p[idx[s]];
+    for (int s = 0; s < k; ++s) dp[idx[s]] = (dG[s] - gdG) / Z;
+    double pdp = 0.0;
+    for (int m = 0; m < N; ++m) pdp += p[m] * dp[m];
+    for (int i = 0; i < N; ++i) dr[i] += p[i] * (dp[i] - pdp);
+  }
+  double pf = 0.0;
+  for (int m = 0; m < N; ++m) pf += p[m] * f[m];
+  const double scale = aux_grad * alpha * (double)N / (double)T;
+  for (int i = 0; i < N; ++i) dr[i] += scale * p[i] * (f[i] - pf);
+  free(g);
+  free(p);
+  free(dp);
+}
+
+/* Forward routing shared by the two backward entry points: fp32 scores,
+ * top-k, gates, counts, kept pairs and f. */
+typedef struct {
+  float* r32;
+  int32_t* idx;
+  double* g;
+  int32_t* counts;
+  uint8_t* keep;
+  double* f;
+} Routing;
+
+static void routing_forward(int T, int d, int N, int k, int gate_mode, int capacity, int xdtype,
+                            const void* x, int wdtype, const void* w_router,
+                            const double* logit_bias, const float* sel_bias, Routing* R) {
+  R->r32 = (float*)malloc(sizeof(float) * (size_t)T * N);
+  R->idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)T * k);
+  R->g = (double*)malloc(sizeof(double) * (size_t)T * k);
+  R->counts = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+  R->keep = (uint8_t*)malloc((size_t)T * k + 1);
+  R->f = (double*)malloc(sizeof(double) * (size_t)N);
+  oracle_router_logits(T, d, N, xdtype, x, wdtype, w_router, logit_bias, NULL, R->r32);
+  oracle_route(T, N, k, gate_mode, R->r32, sel_bias, R->idx, R->g, R->counts, NULL);
+  oracle_capacity_keep(T, k, N, R->idx, capacity, R->keep);
+  for (int i = 0; i < N; ++i) R->f[i] = (double)R->counts[i] / ((double)T * (double)k);
+}
+
+static void routing_free(Routing* R) {
+  free(R->r32);
+  free(R->idx);
+  free(R->g);
+  free(R->counts);
+  free(R->keep);
+  free(R->f);
+}
+
+/* The expert of term s (< k: routed slot, else shared expert N + s - k) of
+ * token t, with its gate (0 for a dropped pair: it is not evaluated). */
+static int term_expert(const Routing* R, int N, int k, int t, int s, double* G) {
+  if (s < k) {
+    const size_t q = (size_t)t * k + s;
+    if (!R->keep[q]) {
+      *G = 0.0;
+      return -1;
+    }
+    *G = R->g[q];
+    return R->idx[q];
+  }
+  *G = 1.0;
+  return N + (s - k);
+}
+
+/* Full backward for all tokens: dx [T][d], dw_router [N][d],
+ * dwg/dwu [N+s][d_ff][d], dwd [N+s][d][d_ff], all fp64. dy is [T][d] fp64.
+ * Weight gradients sum their terms in ascending (token, term) order. */
+void oracle_layer_backward(int T, int d, int d_ff, int N, int k, int n_shared, int gate_mode,
+                           int capacity, int xdtype, const void* x, int wdtype,
+                           const void* w_router, const double* logit_bias,
+                           const float* sel_bias, const void* wg, const void* wu,
+                           const void* wd, const double* dy, double alpha, double aux_grad,
+                           double* dx, double* dw_router, double* dwg, double* dwu,
+                           double* dwd) {
+  const int terms = k + n_shared, E = N + n_shared;
+  Routing R;
+  routing_forward(T, d, N, k, gate_mode, capacity, xdtype, x, wdtype, w_router, logit_bias,
+                  sel_bias, &R);
+  const size_t Q = (size_t)T * terms;
+  double* H = (double*)calloc(Q * d_ff, sizeof(double));
+  double* DA = (double*)calloc(Q * d_ff, sizeof(double));
+  double* DB = (double*)calloc(Q * d_ff, sizeof(double));
+  double* DO = (double*)calloc(Q * d, sizeof(double));
+  double* DXE = (double*)calloc(Q * d, sizeof(double));
+  double* dG = (double*)calloc((size_t)T * k, sizeof(double));
+  int* ex = (int*)malloc(sizeof(int) * Q);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long long q = 0; q < (long long)Q; ++q) {
+    const int t = (int)(q / terms), s = (int)(q % terms);
+    double G;
+    const int e = term_expert(&R, N, k, t, s, &G);
+    ex[q] = e;
+    if (e < 0) continue;  /* dropped pair: no term, dL/dg = 0 */
+    double* xt = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int i = 0; i < d; ++i) xt[i] = widen(xdtype, x, (size_t)t * d + i);
+    const double dGq = expert_backward(
+        d, d_ff, wdtype, elem_ptr(wdtype, wg, (size_t)e * d_ff * d),
+        elem_ptr(wdtype, wu, (size_t)e * d_ff * d), elem_ptr(wdtype, wd, (size_t)e * d * d_ff),
+        xt, dy + (size_t)t * d, G, H + q * d_ff, DA + q * d_ff, DB + q * d_ff, DO + q * d,
+        DXE + q * d);
+    if (s < k) dG[(size_t)t * k + s] = dGq;
+    free(xt);
+  }
+  double* DR = (double*)malloc(sizeof(double) * (size_t)T * N);
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    double* r = (double*)malloc(sizeof(double) * (size_t)N);
+    for (int e = 0; e < N; ++e) r[e] = (double)R.r32[(size_t)t * N + e];
+    score_backward(N, k, T, gate_mode, r, R.idx + (size_t)t * k, dG + (size_t)t * k, R.f, alpha,
+                   aux_grad, DR + (size_t)t * N);
+    for (int i = 0; i < d; ++i) {
+      double acc = 0.0;
+      for (int s = 0; s < terms; ++s) acc += DXE[((size_t)t * terms + s) * d + i];
+      for (int e = 0; e < N; ++e)
+        acc += DR[(size_t)t * N + e] * widen(wdtype, w_router, (size_t)e * d + i);
+      dx[(size_t)t * d + i] = acc;
+    }
+    free(r);
+  }
+#pragma omp parallel for schedule(static)
+  for (int e = 0; e < N; ++e)
+    for (int i = 0; i < d; ++i) {
+      double acc = 0.0;
+      for (int t = 0; t < T; ++t)
+        acc += DR[(size_t)t * N + e] * widen(xdtype, x, (size_t)t * d + i);
+      dw_router[(size_t)e * d + i] = acc;
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long long ej = 0; ej < (long long)E * d_ff; ++ej) {
+    const int e = (int)(ej / d_ff), j = (int)(ej % d_ff);
+    double* rg = dwg + (size_t)ej * d;
+    double* ru = dwu + (size_t)ej * d;
+    for (int i = 0; i < d; ++i) rg[i] = ru[i] = 0.0;
+    for (size_t q = 0; q < Q; ++q) {
+      if (ex[q] != e) continue;
+      const int t = (int)(q / terms);
+      for (int i = 0; i < d; ++i) {
+        const double xi = widen(xdtype, x, (size_t)t * d + i);
+        rg[i] += DA[q * d_ff + j] * xi;
+        ru[i] += DB[q * d_ff + j] * xi;
+      }
+    }
+  }
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long long ec = 0; ec < (long long)E * d; ++ec) {
+    const int e = (int)(ec / d), c = (int)(ec % d);
+    double* rd = dwd + (size_t)ec * d_ff;
+    for (int j = 0; j < d_ff; ++j) rd[j] = 0.0;
+    for (size_t q = 0; q < Q; ++q) {
+      if (ex[q] != e) continue;
+      for (int j = 0; j < d_ff; ++j) rd[j] += DO[q * d + c] * H[q * d_ff + j];
+    }
+  }
+  free(H);
+  free(DA);
+  free(DB);
+  free(DO);
+  free(DXE);
+  free(dG);
+  free(ex);
+  free(DR);
+  routing_free(&R);
+}
+
+/* The same gradients at sampled places, for sizes where the full backward
+ * is too slow: dx rows of the listed tokens, and for each listed (e, j) the
+ * row j of dWg[e] and dWu[e] (length d) and the column j of dWd[e] (length
+ * d). A column j of the weight gradients needs only a_j, b_j and dh_j of
+ * every token the expert takes, so each is one pass over those tokens. */
+void oracle_backward_samples(int T, int d, int d_ff, int N, int k, int n_shared, int gate_mode,
+                             int capacity, int xdtype, const void* x, int wdtype,
+                             const void* w_router, const double* logit_bias,
+                             const float* sel_bias, const void* wg, const void* wu,
+                             const void* wd, const double* dy, double alpha, double aux_grad,
+                             int n_tok, const int32_t* toks, double* dx_rows, int n_w,
+                             const int32_t* w_e, const int32_t* w_j, double* dwg_rows,
+                             double* dwu_rows, double* dwd_cols) {
+  const int terms = k + n_shared;
+  Routing R;
+  routing_forward(T, d, N, k, gate_mode, capacity, xdtype, x, wdtype, w_router, logit_bias,
+                  sel_bias, &R);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int n = 0; n < n_tok; ++n) {
+    const int t = toks[n];
+    double* xt = (double*)malloc(sizeof(double) * (size_t)d);
+    double* h = (double*)malloc(sizeof(double) * (size_t)d_ff);
+    double* da = (double*)malloc(sizeof(double) * (size_t)d_ff);
+    double* db = (double*)malloc(sizeof(double) * (size_t)d_ff);
+    double* dout = (double*)malloc(sizeof(double) * (size_t)d);
+    double* dxe = (double*)malloc(sizeof(double) * (size_t)d);
+    double* dG = (double*)calloc((size_t)k, sizeof(double));
+    double* r = (double*)malloc(sizeof(double) * (size_t)N);
+    double* dr = (double*)malloc(sizeof(double) * (size_t)N);
+    double* out = dx_rows + (size_t)n * d;
+    for (int i = 0; i < d; ++i) {
+      xt[i] = widen(xdtype, x, (size_t)t * d + i);
+      out[i] = 0.0;
+    }
+    for (int s = 0; s < terms; ++s) {
+      double G;
+      const int e = term_expert(&R, N, k, t, s, &G);
+      if (e < 0) continue;
+      const double g = expert_backward(
+          d, d_ff, wdtype, elem_ptr(wdtype, wg, (size_t)e * d_ff * d),
+          elem_ptr(wdtype, wu, (size_t)e * d_ff * d), elem_ptr(wdtype, wd, (size_t)e * d * d_ff),
+          xt, dy + (size_t)t * d, G, h, da, db, dout, dxe);
+      if (s < k) dG[s] = g;
+      for (int i = 0; i < d; ++i) out[i] += dxe[i];
+    }
+    for (int e = 0; e < N; ++e) r[e] = (double)R.r32[(size_t)t * N + e];
+    score_backward(N, k, T, gate_mode, r, R.idx + (size_t)t * k, dG, R.f, alpha, aux_grad, dr);
+    for (int i = 0; i < d; ++i)
+      for (int e = 0; e < N; ++e) out[i] += dr[e] * widen(wdtype, w_router, (size_t)e * d + i);
+    free(xt); free(h); free(da); free(db); free(dout); free(dxe); free(dG); free(r); free(dr);
+  }
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int n = 0; n < n_w; ++n) {
+    const int e = w_e[n], j = w_j[n];
+    double* rg = dwg_rows + (size_t)n * d;
+    double* ru = dwu_rows + (size_t)n * d;
+    double* cd = dwd_cols + (size_t)n * d;
+    for (int i = 0; i < d; ++i) rg[i] = ru[i] = cd[i] = 0.0;
+    const void* g_e = elem_ptr(wdtype, wg, (size_t)e * d_ff * d);
+    const void* u_e = elem_ptr(wdtype, wu, (size_t)e * d_ff * d);
+    const void* d_e = elem_ptr(wdtype, wd, (size_t)e * d * d_ff);
+    for (int t = 0; t < T; ++t)
+      for (int s = 0; s < terms; ++s) {
+        double G;
+        if (term_expert(&R, N, k, t, s, &G) != e) continue;
+        double a = 0.0, b = 0.0, dh = 0.0;
+        for (int i = 0; i < d; ++i) {
+          const double xi = widen(xdtype, x, (size_t)t * d + i);
+          a += widen(wdtype, g_e, (size_t)j * d + i) * xi;
+          b += widen(wdtype, u_e, (size_t)j * d + i) * xi;
+        }
+        for (int c = 0; c < d; ++c)
+          dh += widen(wdtype, d_e, (size_t)c * d_ff + j) * G * dy[(size_t)t * d + c];
+        const double h = silu(a) * b;
+        const double da = dh * b * silu_grad(a), db = dh * silu(a);
+        for (int i = 0; i < d; ++i) {
+          const double xi = widen(xdtype, x, (size_t)t * d + i);
+          rg[i] += da * xi;
+          ru[i] += db * xi;
+        }
+        for (int c = 0; c < d; ++c) cd[c] += G * dy[(size_t)t * d + c] * h;
+      }
+  }
+  routing_free(&R);
 }

@@ -532,6 +532,170 @@ def pin_fp8_weight_row_scaling_is_exact(o):
     assert np.abs(a["y"] - ref["y"]).max() <= 0.1 * np.abs(ref["y"]).max()
 
 
+# -------------------------------------------------------------- backward ---
+def _bwd_case(seed, T=5, d=6, N=4, k=2, dff=7, S=1):
+    rng = _rng(seed)
+    E = N + S
+    return dict(x=rng.normal(0, 1, (T, d)), w_router=rng.normal(0, 1, (N, d)),
+                wg=rng.normal(0, 0.5, (E, dff, d)), wu=rng.normal(0, 0.5, (E, dff, d)),
+                wd=rng.normal(0, 0.5, (E, d, dff)), dy=rng.normal(0, 1, (T, d)), k=k, n_shared=S)
+
+
+def _loss(o, c, gate_mode, alpha, aux_grad, capacity=0, **over):
+    """sum(dy * y) + aux_grad * aux from the oracle's forward (fp64 inputs)."""
+    a = dict(c, **over)
+    out = o.layer(a["x"], a["w_router"], a["wg"], a["wu"], a["wd"], a["k"],
+                  gate_mode=gate_mode, n_shared=a["n_shared"], capacity=capacity)
+    T = a["x"].shape[0]
+    _, _, aux = o.balance_stats(out["counts"], out["prob_sum"], T, a["k"], alpha)
+    return float((a["dy"] * out["y"]).sum() + aux_grad * aux), out["topk_idx"]
+
+
+def _finite_differences(o, c, name, gate_mode, alpha, aux_grad, h, capacity=0):
+    arr = c[name]
+    fd = np.zeros_like(arr)
+    base = _loss(o, c, gate_mode, alpha, aux_grad, capacity)[1]
+    for i in np.ndindex(arr.shape):
+        plus, minus = arr.copy(), arr.copy()
+        plus[i] += h
+        minus[i] -= h
+        lp, ip = _loss(o, c, gate_mode, alpha, aux_grad, capacity, **{name: plus})
+        lm, im = _loss(o, c, gate_mode, alpha, aux_grad, capacity, **{name: minus})
+        assert (ip == base).all() and (im == base).all(), "a step changed the routing"
+        fd[i] = (lp - lm) / (2 * h)
+    return fd
+
+
+_GRAD_OF = dict(x="dx", w_router="dw_router", wg="dw_gate", wu="dw_up", wd="dw_down")
+
+
+def _rel(a, b):
+    return float(np.abs(a - b).max() / max(1e-300, np.abs(b).max()))
+
+
+def pin_backward_matches_finite_differences(o):
+    """Every gradient against central differences of the forward's loss
+    sum(dy * y) + aux_grad * aux, in both gate modes, with a shared expert.
+    The forward rounds scores to fp32 (2^-24 relative) before the softmax,
+    so the router-side differences carry ~6e-8 / h of noise; the expert
+    weights see none."""
+    c = _bwd_case(21)
+    for mode in (0, 1):
+        g = o.layer_backward(c["x"], c["w_router"], c["wg"], c["wu"], c["wd"], c["k"], c["dy"],
+                             gate_mode=mode, n_shared=c["n_shared"], alpha=0.01, aux_grad=3.0)
+        for name in ("x", "w_router", "wg", "wu", "wd"):
+            fd = _finite_differences(o, c, name, mode, 0.01, 3.0, h=1e-3)
+            tol = 1e-3 if name in ("x", "w_router") else 1e-5
+            assert _rel(g[_GRAD_OF[name]], fd) < tol, (mode, name, _rel(g[_GRAD_OF[name]], fd))
+
+
+def pin_backward_balance_term_alone(o):
+    """With dy = 0 only the balance term moves the loss: dx and dW_r against
+    central differences of aux alone, and every expert-weight gradient is
+    exactly zero (f is held fixed, so the experts do not enter aux)."""
+    c = _bwd_case(22, T=6, N=5, k=2, S=0)
+    c["dy"] = np.zeros_like(c["dy"])
+    g = o.layer_backward(c["x"], c["w_router"], c["wg"], c["wu"], c["wd"], c["k"], c["dy"],
+                         alpha=0.01, aux_grad=50.0)
+    for name in ("x", "w_router"):
+        fd = _finite_differences(o, c, name, 0, 0.01, 50.0, h=1e-3)
+        assert _rel(g[_GRAD_OF[name]], fd) < 1e-3, (name, _rel(g[_GRAD_OF[name]], fd))
+    for key in ("dw_gate", "dw_up", "dw_down"):
+        assert not g[key].any(), key
+
+
+def pin_backward_collapsed_example(o):
+    """Mixture of Experts and Guided Decoding, the auxiliary-loss example
+    (N = 4, collapsed routing f = [1, 0, 0, 0], P = [0.7, 0.1, 0.1, 0.1]), as
+    one token with d = 1: x = 1 and router weights [ln 7, 0, 0, 0] give
+    p = P, and top-1 picks expert 0. With dy = 0 the score gradient is the
+    balance term alone, alpha * N / T * p_i * (f_i - sum_m p_m f_m)
+    = alpha * 4 * [0.7 * 0.3, -0.1 * 0.7, -0.1 * 0.7, -0.1 * 0.7]
+    = alpha * [0.84, -0.28, -0.28, -0.28], which is dW_r (x = 1) and sums
+    into dx = sum_e dr_e * W_r[e] = alpha * 0.84 * ln 7."""
+    g0 = golden("balance_loss_n4.json")
+    alpha = g0["alpha"]
+    P = np.array(g0["collapsed"]["P"])
+    wr = np.log(P / P[-1]).reshape(4, 1)       # [ln 7, 0, 0, 0]
+    x = np.ones((1, 1))
+    z = np.zeros((4, 2, 1))
+    g = o.layer_backward(x, wr, z, z, np.zeros((4, 1, 2)), 1, np.zeros((1, 1)), alpha=alpha,
+                         aux_grad=1.0)
+    want = alpha * np.array([0.84, -0.28, -0.28, -0.28])
+    assert np.allclose(g["dw_router"][:, 0], want, rtol=1e-6, atol=0), g["dw_router"]
+    assert abs(g["dx"][0, 0] - alpha * 0.84 * math.log(7.0)) < 1e-8, g["dx"]
+
+
+def pin_backward_gate_modes_agree(o):
+    """A softmax over all scores renormalised over the kept experts equals a
+    softmax over the kept scores, so the two gate modes have the same
+    gradient (with the balance term and a capacity cut too)."""
+    c = _bwd_case(23, T=8, N=5, k=3, S=1)
+    args = (c["x"], c["w_router"], c["wg"], c["wu"], c["wd"], c["k"], c["dy"])
+    a = o.layer_backward(*args, gate_mode=0, n_shared=1, capacity=4, aux_grad=2.0)
+    b = o.layer_backward(*args, gate_mode=1, n_shared=1, capacity=4, aux_grad=2.0)
+    for key in a:
+        assert _rel(a[key], b[key]) < 1e-12, key
+
+
+def pin_backward_matches_autograd(o):
+    """The whole layer written with torch fp64 ops and differentiated by
+    autograd, with the oracle's routing (top-k sets and kept pairs) held
+    fixed: softmax gates over the kept scores, SwiGLU experts
+    (F.silu), a shared expert, a capacity cut, and the balance term with f
+    held constant. The oracle's gates use scores rounded to fp32, so the two
+    agree to ~1e-7 relative."""
+    F = torch.nn.functional
+    c = _bwd_case(24, T=7, d=5, N=4, k=2, dff=6, S=1)
+    cap, alpha, ag = 3, 0.01, 5.0
+    g = o.layer_backward(c["x"], c["w_router"], c["wg"], c["wu"], c["wd"], c["k"], c["dy"],
+                         n_shared=1, capacity=cap, alpha=alpha, aux_grad=ag)
+    fwd = o.layer(c["x"], c["w_router"], c["wg"], c["wu"], c["wd"], c["k"], n_shared=1,
+                  capacity=cap)
+    idx, keep = fwd["topk_idx"], fwd["keep"].reshape(-1, c["k"])
+    T, N, k = c["x"].shape[0], c["w_router"].shape[0], c["k"]
+    f = torch.tensor(np.bincount(idx.ravel(), minlength=N) / (T * k))
+    t = {n: torch.tensor(c[n], requires_grad=True)
+         for n in ("x", "w_router", "wg", "wu", "wd")}
+    r = t["x"] @ t["w_router"].T
+    p = torch.softmax(r, dim=1)
+
+    def expert(e, xt):
+        return t["wd"][e] @ (F.silu(t["wg"][e] @ xt) * (t["wu"][e] @ xt))
+
+    ys = []
+    for tok in range(T):
+        kept = torch.tensor(idx[tok].tolist())
+        gates = torch.softmax(r[tok, kept], dim=0)
+        y = expert(N, t["x"][tok])
+        for s in range(k):
+            if keep[tok, s]:
+                y = y + gates[s] * expert(int(idx[tok, s]), t["x"][tok])
+        ys.append(y)
+    aux = alpha * N * (f * p.mean(dim=0)).sum()
+    loss = (torch.stack(ys) * torch.tensor(c["dy"])).sum() + ag * aux
+    loss.backward()
+    for n in t:
+        assert _rel(g[_GRAD_OF[n]], t[n].grad.numpy()) < 1e-6, (n, _rel(g[_GRAD_OF[n]], t[n].grad.numpy()))
+
+
+def pin_backward_samples_match_full(o):
+    """The sampled gradients (dx rows; rows of dW_g, dW_u and columns of
+    dW_d) equal the same entries of the full backward, shared expert and
+    capacity cut included."""
+    c = _bwd_case(25, T=9, d=6, N=4, k=2, dff=5, S=1)
+    args = (c["x"], c["w_router"], c["wg"], c["wu"], c["wd"], c["k"], c["dy"])
+    kw = dict(n_shared=1, capacity=4, aux_grad=2.0, gate_mode=1)
+    full = o.layer_backward(*args, **kw)
+    cols = [(0, 1), (3, 4), (4, 0), (2, 2)]
+    smp = o.backward_samples(*args, tokens=[0, 4, 8], columns=cols, **kw)
+    assert _rel(smp["dx_rows"], full["dx"][[0, 4, 8]]) < 1e-12
+    for n, (e, j) in enumerate(cols):
+        assert _rel(smp["dw_gate_rows"][n], full["dw_gate"][e, j]) < 1e-12
+        assert _rel(smp["dw_up_rows"][n], full["dw_up"][e, j]) < 1e-12
+        assert _rel(smp["dw_down_cols"][n], full["dw_down"][e, :, j]) < 1e-12
+
+
 def pin_balance_stats_sum_to_one(o):
     rng = _rng(11)
     T, N, k = 64, 8, 2

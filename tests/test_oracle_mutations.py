@@ -45,6 +45,15 @@ MUTATIONS = [
     ("fp8_h_not_quantized", "(oracle_e4m3_decode(hq[j]) * (double)hs);", "(double)h[j];"),
     ("fp8_wrong_weight_row_scale", "out[c] = acc * (double)q->ds[c];", "out[c] = acc * (double)q->ds[d - 1 - c];"),
     ("selection_ignores_bias", "key[e] = sel_bias ? (float)((double)rt[e] + (double)sel_bias[e]) : rt[e];", "key[e] = rt[e];"),
+    ("bwd_silu_grad_missing_term", "return s * (1.0 + z * (1.0 - s));", "return s;"),
+    ("bwd_db_uses_silu_grad", "db[j] = dh * silu(a[j]);", "db[j] = dh * silu_grad(a[j]);"),
+    ("bwd_gate_grad_from_weighted_output", "dG += dyt[c] * o;", "dG += dyt[c] * o * G;"),
+    ("bwd_balance_sign", "for (int i = 0; i < N; ++i) dr[i] += scale * p[i] * (f[i] - pf);", "for (int i = 0; i < N; ++i) dr[i] -= scale * p[i] * (f[i] - pf);"),
+    ("bwd_balance_not_centred", "dr[i] += scale * p[i] * (f[i] - pf);", "dr[i] += scale * p[i] * f[i];"),
+    ("bwd_renorm_not_centred", "dp[idx[s]] = (dG[s] - gdG) / Z;", "dp[idx[s]] = dG[s] / Z;"),
+    ("bwd_dx_without_router_term", "        acc += DR[(size_t)t * N + e] * widen(wdtype, w_router, (size_t)e * d + i);\n      dx[(size_t)t * d + i] = acc;", "      dx[(size_t)t * d + i] = acc;"),
+    ("bwd_down_grad_from_da", "rd[j] += DO[q * d + c] * H[q * d_ff + j];", "rd[j] += DO[q * d + c] * DA[q * d_ff + j];"),
+    ("bwd_gate_grad_transposed", "acc += widen(wdtype, wg, (size_t)j * d + i) * da[j] +", "acc += widen(wdtype, wu, (size_t)j * d + i) * da[j] +"),
 ]
 
 
