@@ -342,6 +342,47 @@ MOE_API int moe_balance_stats(int32_t n_experts, int32_t T, int32_t top_k,
                       float alpha, float* f, float* P, float* aux,
                       moe_stream_t stream);
 
+/*
+ * Backward of moe_layer_forward (bf16): the gradients of the scalar
+ *   L = sum_{t,c} dy[t][c] * y[t][c] + aux_grad * aux,
+ *   aux = alpha * N * sum_i f_i * P_i
+ * (y the layer output, aux the balance loss of moe_balance_stats) with
+ * respect to x, W_r, W_g, W_u and W_d ("Mixture of experts and speculative
+ * decoding", the layer equation and "Keeping the experts busy"; "Mixture of
+ * Experts and Guided Decoding", the auxiliary-loss formula). The top-k
+ * choice, the capacity cut and the counts (so f) are hard decisions and are
+ * held fixed: the gradient flows through the gate weights and through P.
+ * The fp32 rounding of the scores only fixes the routing and counts as the
+ * identity; logit_bias and sel_bias are constants.
+ *
+ * The forward is recomputed inside (router, permutation, both projections),
+ * from the same inputs as the forward call. Rounding: H, the
+ * pre-activations, dO = g * dy, da | db and each expert's input gradient
+ * are bf16 intermediates; every sum accumulates in fp32.
+ *
+ *  x, w_router, logit_bias, sel_bias, w_gate, w_up, w_down: as
+ *                 moe_layer_forward (bf16; cfg->dtype must be MOE_BF16).
+ *  dy             [device] [T][d_model] bf16, dL/dy.
+ *  alpha          the balance-loss coefficient (as moe_balance_stats).
+ *  aux_grad       dL/daux (0 leaves the balance term out).
+ *  dx             [device] [T][d_model] fp32 out.
+ *  dw_router      [device] [N][d_model] fp32 out.
+ *  dw_gate, dw_up [device] [N+s][d_ff][d_model] fp32 out.
+ *  dw_down        [device] [N+s][d_model][d_ff] fp32 out. Experts that take
+ *                 no token get zeros.
+ *  ws             moe_workspace_size_backward(cfg) bytes.
+ * d_ff must be a multiple of 64 (MOE_ERR_UNSUPPORTED otherwise; then
+ * moe_workspace_size_backward returns 0). Every sum runs in a fixed order,
+ * so two calls give the same bits.
+ */
+MOE_API size_t moe_workspace_size_backward(const moe_config* cfg);
+MOE_API int moe_layer_backward(const moe_config* cfg, const void* x, const void* w_router,
+                    const float* logit_bias, const float* sel_bias,
+                    const void* w_gate, const void* w_up, const void* w_down,
+                    const void* dy, float alpha, float aux_grad, float* dx,
+                    float* dw_router, float* dw_gate, float* dw_up, float* dw_down,
+                    void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* Synchronises `stream`, then returns the device-side status recorded in the
  * workspace `ws` by the last call that used it (MOE_OK, MOE_ERR_TIMEOUT or
  * MOE_ERR_DEVICE_CHECK), or MOE_ERR_CUDA if the stream reports an error. */

@@ -83,7 +83,10 @@ def _declare(lib):
     lib.oracle_backward_samples.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P,
                                             _P, _P, _P, _P, _P, _D, _D, _I, _P, _P, _I, _P, _P,
                                             _P, _P, _P]
-    lib.oracle_backward_samples.restype = None
+    lib.oracle_backward_samples.restype = _I
+    lib.oracle_balance_backward.argtypes = [_I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _D, _D,
+                                            _P, _P]
+    lib.oracle_balance_backward.restype = None
     return lib
 
 
@@ -366,23 +369,58 @@ class Oracle:
             _ptr(out["dw_gate"]), _ptr(out["dw_up"]), _ptr(out["dw_down"]))
         return out
 
-    def backward_samples(self, x, w_router, wg, wu, wd, k, dy, tokens=(), columns=(),
+    def backward_samples(self, x, w_router, experts, N, k, dy, tokens=(), columns=(),
                          gate_mode=GATE_TOPK_SOFTMAX, logit_bias=None, sel_bias=None,
                          n_shared=0, capacity=0, alpha=0.01, aux_grad=1.0):
         """The same gradients at sampled places: dx rows of ``tokens``; for
         each (e, j) of ``columns`` the row j of dw_gate[e] and dw_up[e] and
-        the column j of dw_down[e] (each length d)."""
-        (xd, x, wdt, w_router, mats, T, d, N, E, d_ff, lb, sb,
-         dy) = self._bwd_inputs(x, w_router, wg, wu, wd, k, dy, logit_bias, sel_bias)
+        the column j of dw_down[e] (each length d). ``experts`` maps an
+        expert index (shared ones after the N routed) to its stored
+        (wg, wu, wd); experts no sample needs may be absent."""
+        xd, x = _stored(x)
+        wdt, w_router = _stored(w_router)
+        T, d = x.shape
+        E = N + n_shared
+        refs = []
+        tabs = [(_P * E)(), (_P * E)(), (_P * E)()]
+        d_ff = None
+        for e, mats in experts.items():
+            for j, m in enumerate(mats):
+                dt, m = _stored(m)
+                assert dt == wdt, "weights share one stored type"
+                refs.append(m)
+                tabs[j][e] = m.ctypes.data
+            d_ff = mats[0].shape[0]
+        lb = None if logit_bias is None else _c(logit_bias, np.float64)
+        sb = None if sel_bias is None else _c(sel_bias, np.float32)
+        dy = _c(dy, np.float64)
         toks = _c(list(tokens), np.int32)
         cols = np.asarray(list(columns), np.int32).reshape(-1, 2)
         we, wj = _c(cols[:, 0], np.int32), _c(cols[:, 1], np.int32)
         out = dict(dx_rows=np.empty((toks.size, d)), dw_gate_rows=np.empty((we.size, d)),
                    dw_up_rows=np.empty((we.size, d)), dw_down_cols=np.empty((we.size, d)))
-        self.lib.oracle_backward_samples(
+        rc = self.lib.oracle_backward_samples(
             T, d, d_ff, N, k, n_shared, gate_mode, capacity, xd, _ptr(x), wdt, _ptr(w_router),
-            _ptr(lb), _ptr(sb), _ptr(mats[0]), _ptr(mats[1]), _ptr(mats[2]), _ptr(dy),
-            float(alpha), float(aux_grad), toks.size, _ptr(toks), _ptr(out["dx_rows"]), we.size,
-            _ptr(we), _ptr(wj), _ptr(out["dw_gate_rows"]), _ptr(out["dw_up_rows"]),
+            _ptr(lb), _ptr(sb), tabs[0], tabs[1], tabs[2], _ptr(dy), float(alpha),
+            float(aux_grad), toks.size, _ptr(toks), _ptr(out["dx_rows"]), we.size, _ptr(we),
+            _ptr(wj), _ptr(out["dw_gate_rows"]), _ptr(out["dw_up_rows"]),
             _ptr(out["dw_down_cols"]))
+        if rc != 0:
+            raise ValueError("oracle_backward_samples: a sample needs an expert not supplied")
         return out
+
+    def balance_backward(self, x, w_router, k, gate_mode=GATE_TOPK_SOFTMAX, logit_bias=None,
+                         sel_bias=None, alpha=0.01, aux_grad=1.0):
+        """dx [T,d] and dw_router [N,d] when dy = 0 (the balance term alone)."""
+        xd, x = _stored(x)
+        wdt, w_router = _stored(w_router)
+        T, d = x.shape
+        N = w_router.shape[0]
+        lb = None if logit_bias is None else _c(logit_bias, np.float64)
+        sb = None if sel_bias is None else _c(sel_bias, np.float32)
+        dx = np.empty((T, d))
+        dwr = np.empty((N, d))
+        self.lib.oracle_balance_backward(T, d, N, k, gate_mode, xd, _ptr(x), wdt, _ptr(w_router),
+                                         _ptr(lb), _ptr(sb), float(alpha), float(aux_grad),
+                                         _ptr(dx), _ptr(dwr))
+        return dx, dwr

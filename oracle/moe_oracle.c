@@ -871,19 +871,35 @@ void oracle_layer_backward(int T, int d, int d_ff, int N, int k, int n_shared, i
  * is too slow: dx rows of the listed tokens, and for each listed (e, j) the
  * row j of dWg[e] and dWu[e] (length d) and the column j of dWd[e] (length
  * d). A column j of the weight gradients needs only a_j, b_j and dh_j of
- * every token the expert takes, so each is one pass over those tokens. */
-void oracle_backward_samples(int T, int d, int d_ff, int N, int k, int n_shared, int gate_mode,
-                             int capacity, int xdtype, const void* x, int wdtype,
-                             const void* w_router, const double* logit_bias,
-                             const float* sel_bias, const void* wg, const void* wu,
-                             const void* wd, const double* dy, double alpha, double aux_grad,
-                             int n_tok, const int32_t* toks, double* dx_rows, int n_w,
-                             const int32_t* w_e, const int32_t* w_j, double* dwg_rows,
-                             double* dwu_rows, double* dwd_cols) {
+ * every token the expert takes, so each is one pass over those tokens.
+ * wg/wu/wd are per-expert pointer tables (length N + n_shared); an expert
+ * no listed token or column uses may be NULL. Returns -1 (and computes
+ * nothing) when a needed expert is missing. */
+int oracle_backward_samples(int T, int d, int d_ff, int N, int k, int n_shared, int gate_mode,
+                            int capacity, int xdtype, const void* x, int wdtype,
+                            const void* w_router, const double* logit_bias,
+                            const float* sel_bias, const void* const* wg,
+                            const void* const* wu, const void* const* wd, const double* dy,
+                            double alpha, double aux_grad, int n_tok, const int32_t* toks,
+                            double* dx_rows, int n_w, const int32_t* w_e, const int32_t* w_j,
+                            double* dwg_rows, double* dwu_rows, double* dwd_cols) {
   const int terms = k + n_shared;
   Routing R;
   routing_forward(T, d, N, k, gate_mode, capacity, xdtype, x, wdtype, w_router, logit_bias,
                   sel_bias, &R);
+  int bad = 0;
+  for (int n = 0; n < n_tok; ++n)
+    for (int s = 0; s < terms; ++s) {
+      double G;
+      const int e = term_expert(&R, N, k, toks[n], s, &G);
+      if (e >= 0 && (!wg[e] || !wu[e] || !wd[e])) bad = 1;
+    }
+  for (int n = 0; n < n_w; ++n)
+    if (!wg[w_e[n]] || !wu[w_e[n]] || !wd[w_e[n]]) bad = 1;
+  if (bad) {
+    routing_free(&R);
+    return -1;
+  }
 #pragma omp parallel for schedule(dynamic, 1)
   for (int n = 0; n < n_tok; ++n) {
     const int t = toks[n];
@@ -905,10 +921,8 @@ void oracle_backward_samples(int T, int d, int d_ff, int N, int k, int n_shared,
       double G;
       const int e = term_expert(&R, N, k, t, s, &G);
       if (e < 0) continue;
-      const double g = expert_backward(
-          d, d_ff, wdtype, elem_ptr(wdtype, wg, (size_t)e * d_ff * d),
-          elem_ptr(wdtype, wu, (size_t)e * d_ff * d), elem_ptr(wdtype, wd, (size_t)e * d * d_ff),
-          xt, dy + (size_t)t * d, G, h, da, db, dout, dxe);
+      const double g = expert_backward(d, d_ff, wdtype, wg[e], wu[e], wd[e], xt,
+                                       dy + (size_t)t * d, G, h, da, db, dout, dxe);
       if (s < k) dG[s] = g;
       for (int i = 0; i < d; ++i) out[i] += dxe[i];
     }
@@ -925,9 +939,6 @@ void oracle_backward_samples(int T, int d, int d_ff, int N, int k, int n_shared,
     double* ru = dwu_rows + (size_t)n * d;
     double* cd = dwd_cols + (size_t)n * d;
     for (int i = 0; i < d; ++i) rg[i] = ru[i] = cd[i] = 0.0;
-    const void* g_e = elem_ptr(wdtype, wg, (size_t)e * d_ff * d);
-    const void* u_e = elem_ptr(wdtype, wu, (size_t)e * d_ff * d);
-    const void* d_e = elem_ptr(wdtype, wd, (size_t)e * d * d_ff);
     for (int t = 0; t < T; ++t)
       for (int s = 0; s < terms; ++s) {
         double G;
@@ -935,11 +946,11 @@ void oracle_backward_samples(int T, int d, int d_ff, int N, int k, int n_shared,
         double a = 0.0, b = 0.0, dh = 0.0;
         for (int i = 0; i < d; ++i) {
           const double xi = widen(xdtype, x, (size_t)t * d + i);
-          a += widen(wdtype, g_e, (size_t)j * d + i) * xi;
-          b += widen(wdtype, u_e, (size_t)j * d + i) * xi;
+          a += widen(wdtype, wg[e], (size_t)j * d + i) * xi;
+          b += widen(wdtype, wu[e], (size_t)j * d + i) * xi;
         }
         for (int c = 0; c < d; ++c)
-          dh += widen(wdtype, d_e, (size_t)c * d_ff + j) * G * dy[(size_t)t * d + c];
+          dh += widen(wdtype, wd[e], (size_t)c * d_ff + j) * G * dy[(size_t)t * d + c];
         const double h = silu(a) * b;
         const double da = dh * b * silu_grad(a), db = dh * silu(a);
         for (int i = 0; i < d; ++i) {
@@ -950,5 +961,45 @@ void oracle_backward_samples(int T, int d, int d_ff, int N, int k, int n_shared,
         for (int c = 0; c < d; ++c) cd[c] += G * dy[(size_t)t * d + c] * h;
       }
   }
+  routing_free(&R);
+  return 0;
+}
+
+/* The gradient when dy = 0: only the balance term moves the loss, so
+ * dx = dr W_r and dW_r = dr^T x with dr the balance part of score_backward
+ * (the gates' part is zero). Needs no expert. dx [T][d], dw_router [N][d]. */
+void oracle_balance_backward(int T, int d, int N, int k, int gate_mode, int xdtype,
+                             const void* x, int wdtype, const void* w_router,
+                             const double* logit_bias, const float* sel_bias, double alpha,
+                             double aux_grad, double* dx, double* dw_router) {
+  Routing R;
+  routing_forward(T, d, N, k, gate_mode, 0, xdtype, x, wdtype, w_router, logit_bias, sel_bias,
+                  &R);
+  double* DR = (double*)malloc(sizeof(double) * (size_t)T * N);
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    double* r = (double*)malloc(sizeof(double) * (size_t)N);
+    double* dG = (double*)calloc((size_t)k, sizeof(double));
+    for (int e = 0; e < N; ++e) r[e] = (double)R.r32[(size_t)t * N + e];
+    score_backward(N, k, T, gate_mode, r, R.idx + (size_t)t * k, dG, R.f, alpha, aux_grad,
+                   DR + (size_t)t * N);
+    for (int i = 0; i < d; ++i) {
+      double acc = 0.0;
+      for (int e = 0; e < N; ++e)
+        acc += widen(wdtype, w_router, (size_t)e * d + i) * DR[(size_t)t * N + e];
+      dx[(size_t)t * d + i] = acc;
+    }
+    free(r);
+    free(dG);
+  }
+#pragma omp parallel for schedule(static)
+  for (int e = 0; e < N; ++e)
+    for (int i = 0; i < d; ++i) {
+      double acc = 0.0;
+      for (int t = 0; t < T; ++t)
+        acc += DR[(size_t)t * N + e] * widen(xdtype, x, (size_t)t * d + i);
+      dw_router[(size_t)e * d + i] = acc;
+    }
+  free(DR);
   routing_free(&R);
 }

@@ -81,6 +81,9 @@ _SIGS = {
     "moe_workspace_size_fp8": (_SZ, [_CFG]),
     "moe_layer_forward_fp8": (_I, [_CFG] + [_P] * 15 + [_P, _SZ, _P]),
     "moe_balance_stats": (_I, [ctypes.c_int32] * 3 + [_P, _P, ctypes.c_float, _P, _P, _P, _P]),
+    "moe_workspace_size_backward": (_SZ, [_CFG]),
+    "moe_layer_backward": (_I, [_CFG] + [_P] * 8 + [ctypes.c_float, ctypes.c_float] + [_P] * 5
+                           + [_P, _SZ, _P]),
     "moe_stream_status": (_I, [_P, _P]),
     "moe_profile_enable": (None, [_I]),
     "moe_profile_collect": (_I, [_P, _P, _I]),
@@ -146,7 +149,8 @@ def check_config(cfg: moe_config) -> int:
 def workspace_size(cfg: moe_config, kind: str = "layer") -> int:
     fn = {"layer": "moe_workspace_size", "router": "moe_router_workspace_size",
           "permute": "moe_permute_workspace_size", "grouped": "moe_grouped_workspace_size",
-          "layer_fp8": "moe_workspace_size_fp8"}[kind]
+          "layer_fp8": "moe_workspace_size_fp8",
+          "backward": "moe_workspace_size_backward"}[kind]
     return int(getattr(lib(), fn)(ctypes.byref(cfg)))
 
 
@@ -218,6 +222,15 @@ def moe_layer_forward(cfg, x, w_router, logit_bias, sel_bias, w_gate, w_up, w_do
         _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(y), _ptr(topk_idx), _ptr(topk_w),
         _ptr(counts), _ptr(prob_sum), _ptr(ws), ws.numel() if ws is not None else 0,
         _stream(stream)))
+
+
+def moe_layer_backward(cfg, x, w_router, logit_bias, sel_bias, w_gate, w_up, w_down, dy, alpha,
+                       aux_grad, dx, dw_router, dw_gate, dw_up, dw_down, ws, stream=None):
+    _check("moe_layer_backward", lib().moe_layer_backward(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(sel_bias),
+        _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(dy), ctypes.c_float(alpha),
+        ctypes.c_float(aux_grad), _ptr(dx), _ptr(dw_router), _ptr(dw_gate), _ptr(dw_up),
+        _ptr(dw_down), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)))
 
 
 def moe_balance_stats(n_experts, T, top_k, counts, prob_sum, alpha, f, P, aux, stream=None):

@@ -200,7 +200,10 @@ const char* kKernelNames[K_NUM] = {"reset_status",  "router_topk",    "permute_h
                                    "permute_scan",  "permute_rank",   "permute_gather",
                                    "permute_small", "permute_group",  "seg_table",
                                    "gate_up",       "down",           "splitk_reduce",
-                                   "combine",       "balance_stats",  "quantize_fp8"};
+                                   "combine",       "balance_stats",  "quantize_fp8",
+                                   "bwd_gate",      "bwd_score",      "bwd_dh_swiglu",
+                                   "bwd_da",        "bwd_dx",         "bwd_w_router",
+                                   "bwd_wgrad"};
 struct Prof {
   std::mutex mu;
   uint32_t mask = 0;
@@ -447,6 +450,130 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* w_router
                     w_up, w_down, w.y_perm, w.seg, true, w.h, w.partial, w.status, s);
   if (rc != MOE_OK) return rc;
   e = launch_combine(c, w.y_perm, w.inv_pos, nullptr, y, s);
+  return e == cudaSuccess ? MOE_OK : fail_cuda(e);
+}
+
+// ---- backward -----------------------------------------------------------------
+// Workspace of moe_layer_backward: the forward's routing and permutation,
+// the recomputed rows (x_perm, H, a | b, o), and the gradients' rows (dL/dg,
+// dO, dL/dr, da | db, dA). o and dA share one buffer: o is read only by the
+// gate-gradient kernel, before dA is written.
+struct BwdWs {
+  int* status;
+  float* logits;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* counts;
+  float* prob_sum;
+  int32_t* offsets;
+  int32_t* sorted_pair;
+  int32_t* inv_pos;
+  void* x_perm;
+  float* partials;
+  int32_t* hist;
+  int32_t* seg;
+  void* h;
+  void* ab;
+  void* o_dA;
+  float* dg;
+  void* dO;
+  float* dr;
+  void* dab;
+};
+BwdWs carve_bwd(Carver& cv, const moe_config& c) {
+  BwdWs w;
+  const size_t P = (size_t)pairs(c), N = (size_t)c.n_experts, T = (size_t)c.T;
+  const size_t R = (size_t)padded_rows(rows_total(c)), d = c.d_model, f = c.d_ff;
+  w.status = cv.take<int>(256);
+  w.logits = cv.take<float>(sizeof(float) * T * N);
+  w.topk_idx = cv.take<int32_t>(sizeof(int32_t) * P);
+  w.topk_w = cv.take<float>(sizeof(float) * P);
+  w.counts = cv.take<int32_t>(sizeof(int32_t) * N);
+  w.prob_sum = cv.take<float>(sizeof(float) * N);
+  w.offsets = cv.take<int32_t>(sizeof(int32_t) * (N + 1));
+  w.sorted_pair = cv.take<int32_t>(sizeof(int32_t) * P);
+  w.inv_pos = cv.take<int32_t>(sizeof(int32_t) * P);
+  w.x_perm = cv.take<void>((size_t)padded_rows((long long)P) * d * 2);
+  w.partials = cv.take<float>(router_partials_bytes(c));
+  w.hist = cv.take<int32_t>(permute_scratch_bytes(c));
+  w.seg = cv.take<int32_t>(sizeof(int32_t) * seg_table_words(c.n_experts + c.n_shared));
+  w.h = cv.take<void>(R * f * 2);
+  w.ab = cv.take<void>(R * 2 * f * 2);
+  w.o_dA = cv.take<void>(R * d * 2);
+  w.dg = cv.take<float>(sizeof(float) * P);
+  w.dO = cv.take<void>(R * d * 2);
+  w.dr = cv.take<float>(sizeof(float) * T * N);
+  w.dab = cv.take<void>(R * 2 * f * 2);
+  return w;
+}
+
+size_t moe_workspace_size_backward(const moe_config* c) {
+  if (moe_check_config(c) != MOE_OK || c->dtype != MOE_BF16 || c->d_ff % 64 != 0) return 0;
+  Carver cv(nullptr);
+  carve_bwd(cv, *c);
+  return align_up(cv.off, 256);
+}
+
+int moe_layer_backward(const moe_config* cfg, const void* x, const void* w_router,
+                       const float* logit_bias, const float* sel_bias, const void* w_gate,
+                       const void* w_up, const void* w_down, const void* dy, float alpha,
+                       float aux_grad, float* dx, float* dw_router, float* dw_gate,
+                       float* dw_up, float* dw_down, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+  int rc = moe_check_config(cfg);
+  if (rc != MOE_OK) return rc;
+  const moe_config& c = *cfg;
+  if (c.dtype != MOE_BF16 || c.d_ff % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!x || !w_router || !w_gate || !w_up || !w_down || !dy || !dx || !dw_router || !dw_gate ||
+      !dw_up || !dw_down)
+    return MOE_ERR_INVALID_ARG;
+  if (!all_aligned({x, w_router, logit_bias, sel_bias, w_gate, w_up, w_down, dy, dx, dw_router,
+                    dw_gate, dw_up, dw_down}))
+    return MOE_ERR_MISALIGNED;
+  if ((rc = check_ws(c, ws, ws_bytes, moe_workspace_size_backward(cfg))) != MOE_OK) return rc;
+  if ((rc = check_device(c)) != MOE_OK) return rc;
+  Carver cv(ws);
+  BwdWs w = carve_bwd(cv, c);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
+  // forward recompute: routing (with the scores), permutation, H, a | b, o
+  cudaError_t e = launch_router(c, x, w_router, logit_bias, sel_bias, nullptr, w.logits,
+                                w.topk_idx, w.topk_w, w.counts, w.prob_sum, w.partials, w.status,
+                                s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  const long long xp_rows = padded_rows(pairs(c)), r_rows = padded_rows(rows_total(c));
+  if (c.T > 0) {
+    e = launch_permute(c, x, w.topk_idx, w.counts, w.offsets, w.sorted_pair, w.inv_pos, w.x_perm,
+                       w.hist, w.status, w.seg, kTileM, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    e = launch_bwd_recompute(c, w.x_perm, x, w.seg, w_gate, w_up, w_down, w.h, w.ab, w.o_dA,
+                             xp_rows, r_rows, w.status, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    // dL/dg and dO, then dL/dr
+    e = launch_bwd_gate(c, dy, w.o_dA, w.inv_pos, w.topk_w, w.dg, w.dO, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    e = launch_bwd_score(c, w.logits, w.topk_idx, w.topk_w, w.dg, w.counts, alpha, aux_grad, w.dr,
+                         s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    // through the experts: da | db, dA; then dx
+    e = launch_bwd_dgrad(c, w.seg, w.dO, w.ab, w_gate, w_up, w_down, w.dab, w.o_dA, r_rows,
+                         w.status, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    e = launch_bwd_dx(c, w.o_dA, w.inv_pos, w.dr, w_router, dx, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  // weight gradients (zero for experts that took no rows, and for T = 0)
+  e = launch_bwd_wr(c, w.dr, x, dw_router, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (c.T == 0) {
+    const size_t E = (size_t)c.n_experts + c.n_shared;
+    const size_t wbytes = E * c.d_ff * c.d_model * sizeof(float);
+    for (float* p : {dw_gate, dw_up, dw_down})
+      if ((e = cudaMemsetAsync(p, 0, wbytes, s)) != cudaSuccess) return fail_cuda(e);
+    return MOE_OK;
+  }
+  e = launch_bwd_wgrad(c, w.seg, w.x_perm, x, w.dab, w.dO, w.h, dw_gate, dw_up, dw_down, xp_rows,
+                       r_rows, w.status, s);
   return e == cudaSuccess ? MOE_OK : fail_cuda(e);
 }
 

@@ -74,7 +74,24 @@ constexpr int G_EPI_THREADS = 32 * EPI_WARPS;  // 256
 constexpr int G_THREADS = 64 + G_EPI_THREADS;  // 320
 constexpr size_t DYN_SMEM = (size_t)STAGES * STAGE_BYTES + 1024;  // + 1 KB alignment slack
 
-enum { EPI_SWIGLU = 0, EPI_DOWN = 1 };
+// Epilogues. The forward's two, and the backward's (1-CTA kernel only):
+//  EPI_SWIGLU_SAVE  gate/up as EPI_SWIGLU, also storing the pre-activations
+//                   a | b (bf16) in aux [rows][2 * n_out];
+//  EPI_SWIGLU_BWD   dH = dO W_d (B MN-major) and, per element, the SwiGLU
+//                   backward: da = dH * b * SiLU'(a), db = dH * SiLU(a) from
+//                   aux, stored as da | db in out [rows][2 * n_out];
+//  EPI_DGRAD        dA = [da | db] [W_g ; W_u] (B MN-major, K = 2 d_ff,
+//                   W_g rows for the first kb_split K blocks), stored plain.
+enum { EPI_SWIGLU = 0, EPI_DOWN = 1, EPI_SWIGLU_SAVE = 2, EPI_SWIGLU_BWD = 3, EPI_DGRAD = 4 };
+// gate/up layout: B stacks 128 gate rows over 128 up rows; 128 output columns
+__host__ __device__ constexpr bool gu_like(int EPI) {
+  return EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_SAVE;
+}
+// B stored MN-major (K rows of an expert's weight, N columns contiguous)
+__host__ __device__ constexpr bool b_mn(int EPI) {
+  return EPI == EPI_SWIGLU_BWD || EPI == EPI_DGRAD;
+}
+constexpr int B_MN_BOX_BYTES = 64 * 128;  // one TMA box: 64 K rows x 64 bf16 columns
 
 // Operand types. A stage row is 128 bytes either way: 64 bf16 or 128 E4M3
 // elements of K, and one MMA takes 32 bytes of K (16 bf16 with kind::f16,
@@ -134,6 +151,12 @@ struct GemmArgs {
   const float* b_scale0;
   const float* b_scale1;
   unsigned* h_amax;
+  // Backward epilogues: bf16 [rows][2 * n_out] pre-activations a | b
+  // (written by EPI_SWIGLU_SAVE, read by EPI_SWIGLU_BWD), and for MN-major B
+  // the K blocks taken from map_b0 before map_b1 (EPI_DGRAD: d_ff / 64).
+  __nv_bfloat16* aux;
+  long long ld_aux;
+  int kb_split;
 };
 
 struct __align__(8) SharedState {
@@ -170,6 +193,7 @@ __device__ __forceinline__ Tile decode_tile(const int32_t* __restrict__ seg, int
 // (a few ulp in fp32, far below the bf16 rounding of the result); as g goes
 // to -inf the divisor overflows to inf and the result goes to -0, the limit.
 __device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+__device__ __forceinline__ float sigmoid(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 
 // Eight consecutive channel scales times a row scale, from two warp-uniform
 // 16-byte loads (p 16-byte aligned); zeros when the group is past the output.
@@ -233,7 +257,7 @@ __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tb
                                                int half, bool valid, long long orow,
                                                __nv_bfloat16* out, float sa, const float* sb0,
                                                const float* sb1) {
-  if (EPI == EPI_SWIGLU) {
+  if constexpr (gu_like(EPI)) {
     float hmax = 0.f;
 #pragma unroll 1
     for (int c = 2 * half; c < 2 * half + 2; ++c) {
@@ -280,10 +304,73 @@ __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tb
           if (col0 + q * 8 < args.n_out)
             *reinterpret_cast<uint4*>(dst + q * 8) =
                 make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        if constexpr (EPI == EPI_SWIGLU_SAVE) {  // the pre-activations a | b, bf16
+          __nv_bfloat16* pa = args.aux + orow * args.ld_aux + col0;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (col0 + q * 8 >= args.n_out) continue;
+            uint32_t wa[4], wb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int j = 8 * q + 2 * i;
+              wa[i] = f32x2_to_bf16x2(__uint_as_float(g[j]), __uint_as_float(g[j + 1]));
+              wb[i] = f32x2_to_bf16x2(__uint_as_float(u[j]), __uint_as_float(u[j + 1]));
+            }
+            *reinterpret_cast<uint4*>(pa + q * 8) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+            *reinterpret_cast<uint4*>(pa + args.n_out + q * 8) =
+                make_uint4(wb[0], wb[1], wb[2], wb[3]);
+          }
+        }
       }
     }
     if constexpr (OP == OP_E4M3)
       if (valid && hmax > 0.f) atomicMax(args.h_amax + orow, __float_as_uint(hmax));
+  } else if constexpr (EPI == EPI_SWIGLU_BWD) {
+#pragma unroll 1
+    for (int c = 4 * half; c < 4 * half + 4; ++c) {
+      uint32_t v[32];
+      ptx::tmem_ld32(tbase + c * 32, v);
+      const int col0 = t.n * 256 + c * 32;
+      const bool in = valid && col0 < args.n_out;  // n_out is a multiple of 64
+      uint4 av[4], bv[4];
+      if (in) {
+        const __nv_bfloat16* pa = args.aux + orow * args.ld_aux + col0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          av[q] = __ldg(reinterpret_cast<const uint4*>(pa) + q);
+          bv[q] = __ldg(reinterpret_cast<const uint4*>(pa + args.n_out) + q);
+        }
+      }
+      ptx::tmem_ld_wait();
+      if (in) {
+        uint32_t pda[16], pdb[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t aw[4] = {av[q].x, av[q].y, av[q].z, av[q].w};
+          const uint32_t bw[4] = {bv[q].x, bv[q].y, bv[q].z, bv[q].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float a0, a1, b0, b1;
+            bf16x2_to_f32(aw[i], a0, a1);
+            bf16x2_to_f32(bw[i], b0, b1);
+            const float dh0 = __uint_as_float(v[8 * q + 2 * i]);
+            const float dh1 = __uint_as_float(v[8 * q + 2 * i + 1]);
+            const float s0 = sigmoid(a0), s1 = sigmoid(a1);
+            pda[4 * q + i] = f32x2_to_bf16x2(dh0 * b0 * s0 * (1.f + a0 * (1.f - s0)),
+                                             dh1 * b1 * s1 * (1.f + a1 * (1.f - s1)));
+            pdb[4 * q + i] = f32x2_to_bf16x2(dh0 * a0 * s0, dh1 * a1 * s1);
+          }
+        }
+        __nv_bfloat16* dst = out + orow * args.ldo + col0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          *reinterpret_cast<uint4*>(dst + q * 8) =
+              make_uint4(pda[4 * q], pda[4 * q + 1], pda[4 * q + 2], pda[4 * q + 3]);
+          *reinterpret_cast<uint4*>(dst + args.n_out + q * 8) =
+              make_uint4(pdb[4 * q], pdb[4 * q + 1], pdb[4 * q + 2], pdb[4 * q + 3]);
+        }
+      }
+    }
   } else {
     const float scale = valid ? row_scale(args, t.s, orow) * sa : 0.0f;
 #pragma unroll 1
@@ -334,9 +421,9 @@ __device__ __forceinline__ void row_scales(const GemmArgs& args, const int32_t* 
   sa = 1.f;
   sb0 = sb1 = nullptr;
   if constexpr (OP == OP_E4M3) {
-    const long long wbase = (long long)t.s * args.b_rows + t.n * (EPI == EPI_SWIGLU ? 128 : 256);
+    const long long wbase = (long long)t.s * args.b_rows + t.n * (gu_like(EPI) ? 128 : 256);
     sb0 = args.b_scale0 + wbase;
-    if (EPI == EPI_SWIGLU) {
+    if (gu_like(EPI)) {
       sb1 = args.b_scale1 + wbase;
       const long long arow = __ldg(seg + 3 + 2 * E + t.s) + r;
       if (valid) sa = __ldg((t.s >= args.n_routed ? args.a_scale_shared : args.a_scale) + arow);
@@ -409,13 +496,13 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         const Tile t = decode_tile(seg, E, args.NT, unit / S);
         const CUtensorMap* am = &map_a;
         int a_row;
-        if (EPI == EPI_SWIGLU) {
+        if (gu_like(EPI)) {
           a_row = __ldg(seg + 3 + 2 * E + t.s) + t.m * BM;
           if (t.s >= args.n_routed) am = &map_a_shared;
         } else {
           a_row = __ldg(seg + 3 + 3 * E + t.s) + t.m * BM;
         }
-        const int b_row = t.s * args.b_rows + t.n * (EPI == EPI_SWIGLU ? 128 : 256);
+        const int b_row = t.s * args.b_rows + t.n * (gu_like(EPI) ? 128 : 256);
         const int kb1 = kb_begin(split + 1, S, KB);
         for (int kb = kb_begin(split, S, KB); kb < kb1; ++kb) {
           if (!wait_phase(ptx::smem_addr(&st.empty[stage]), phase ^ 1u, abort_flag, args.status)) {
@@ -427,7 +514,16 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           const uint32_t b_dst = a_dst + A_BYTES;
           ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
           ptx::tma_load_2d(a_dst, am, fb, kb * Op<OP>::EPK, a_row);
-          if (EPI == EPI_SWIGLU) {
+          if constexpr (b_mn(EPI)) {
+            // K rows kb*64.. of this expert's B (from map_b1 past kb_split),
+            // as 4 boxes of 64 N columns
+            const bool second = kb >= args.kb_split;
+            const CUtensorMap* bm = second ? &map_b1 : &map_b0;
+            const int krow = t.s * args.b_rows + (second ? kb - args.kb_split : kb) * BK;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              ptx::tma_load_2d(b_dst + q * B_MN_BOX_BYTES, bm, fb, t.n * 256 + q * 64, krow);
+          } else if (gu_like(EPI)) {
             ptx::tma_load_2d(b_dst, &map_b0, fb, kb * Op<OP>::EPK, b_row);
             ptx::tma_load_2d(b_dst + B_HALF_BYTES, &map_b1, fb, kb * Op<OP>::EPK, b_row);
           } else {
@@ -476,12 +572,20 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           ptx::tc_fence_after();
           const uint32_t a_src = ring + stage * STAGE_BYTES;
           const uint64_t adesc = ptx::sdesc_k128(a_src);
-          const uint64_t bdesc = ptx::sdesc_k128(a_src + A_BYTES);
+          if constexpr (b_mn(EPI)) {
+            const uint64_t bdesc = ptx::sdesc_mn128(a_src + A_BYTES, B_MN_BOX_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / UMMA_K; ++k) {
-            // +32 bytes of K per step = +2 in the descriptor's address field
-            mma_op<OP>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_op<OP>(BM, BN),
-                       (kb > kb0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < BK / UMMA_K; ++k)  // B: +2048 bytes (two 8-row K groups) a step
+              ptx::mma_bf16(d_tmem, adesc + 2 * k, bdesc + 128 * k,
+                            ptx::idesc_bf16_f32_mn(BM, BN, false), (kb > kb0 || k > 0) ? 1u : 0u);
+          } else {
+            const uint64_t bdesc = ptx::sdesc_k128(a_src + A_BYTES);
+#pragma unroll
+            for (int k = 0; k < BK / UMMA_K; ++k) {
+              // +32 bytes of K per step = +2 in the descriptor's address field
+              mma_op<OP>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_op<OP>(BM, BN),
+                         (kb > kb0 || k > 0) ? 1u : 0u);
+            }
           }
           ptx::mma_commit(ptx::smem_addr(&st.empty[stage]));
           if (++stage == STAGES) {
@@ -533,7 +637,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         // Split-K unit: this split's fp32 partial rows; splitk_reduce_kernel
         // sums the splits in order and applies the epilogue.
         float* prow = args.partial + ((long long)split * args.R + orow) * args.pc;
-        constexpr int HALF_CHUNKS = (EPI == EPI_SWIGLU) ? 2 : 4;
+        constexpr int HALF_CHUNKS = gu_like(EPI) ? 2 : 4;
 #pragma unroll 1
         for (int c = half * HALF_CHUNKS; c < (half + 1) * HALF_CHUNKS; ++c) {
           uint32_t v[32], u[32];
@@ -1187,7 +1291,11 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_sh, const CUt
   if (grid <= 0) return cudaSuccess;
   cudaError_t e;
   {
-    ProfScope p(EPI == EPI_SWIGLU ? K_GATE_UP : K_DOWN, s);
+    ProfScope p(gu_like(EPI)              ? K_GATE_UP
+                : EPI == EPI_SWIGLU_BWD ? K_BWD_DH
+                : EPI == EPI_DGRAD      ? K_BWD_DA
+                                        : K_DOWN,
+                s);
     e = launch_pdl(grouped_gemm_kernel<EPI, OP>, dim3(grid), dim3(G_THREADS), DYN_SMEM, s, 1, a,
                    a_sh, b0, b1, args);
   }
@@ -1525,6 +1633,107 @@ cudaError_t launch_grouped_e4m3(const moe_config& c, const uint8_t* xq_perm,
   d.NT = (c.d_model + 255) / 256;
   return pair ? launch_pair<EPI_DOWN, OP_E4M3>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s)
               : launch_gemm<EPI_DOWN, OP_E4M3>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s);
+}
+
+// ---- backward -----------------------------------------------------------------
+
+namespace {
+GemmArgs bwd_args(const moe_config& c, const int32_t* seg, int* status, long long R) {
+  GemmArgs g{};
+  g.seg = seg;
+  g.status = status;
+  g.n_routed = c.n_experts;
+  g.n_pairs = (int)((long long)c.T * c.top_k);
+  g.s_max = 1;
+  g.R = R;
+  return g;
+}
+}  // namespace
+
+cudaError_t launch_bwd_recompute(const moe_config& c, const void* x_perm, const void* x,
+                                 const int32_t* seg, const void* w_gate, const void* w_up,
+                                 const void* w_down, void* h, void* ab, void* o, long long xp_rows,
+                                 long long r_rows, int* status, cudaStream_t s) {
+  const long long P = (long long)c.T * c.top_k;
+  const int E = c.n_experts + c.n_shared;
+  const long long R = P + (long long)c.n_shared * c.T;
+  if (R == 0) return cudaSuccess;
+  CUtensorMap m_xp, m_x, m_wg, m_wu, m_h, m_wd;
+  const bool ok = make_map(&m_xp, x_perm, std::max(P, xp_rows), c.d_model) &&
+                  make_map(&m_x, c.n_shared > 0 ? x : x_perm, c.n_shared > 0 ? c.T : P,
+                           c.d_model) &&
+                  make_map(&m_wg, w_gate, (long long)E * c.d_ff, c.d_model) &&
+                  make_map(&m_wu, w_up, (long long)E * c.d_ff, c.d_model) &&
+                  make_map(&m_h, h, std::max(R, r_rows), c.d_ff) &&
+                  make_map(&m_wd, w_down, (long long)E * c.d_model, c.d_ff);
+  if (!ok) return cudaErrorInvalidValue;
+  const long long mt = mt_bound_of(c, BM);
+  GemmArgs g = bwd_args(c, seg, status, R);
+  g.out = h;
+  g.ldo = c.d_ff;
+  g.K = c.d_model;
+  g.n_out = c.d_ff;
+  g.NT = (c.d_ff + 127) / 128;
+  g.b_rows = c.d_ff;
+  g.pc = 2 * c.d_ff;
+  g.aux = static_cast<__nv_bfloat16*>(ab);
+  g.ld_aux = 2LL * c.d_ff;
+  cudaError_t e = launch_gemm<EPI_SWIGLU_SAVE, OP_BF16>(m_xp, m_x, m_wg, m_wu, g, (int)(mt * g.NT), s);
+  if (e != cudaSuccess) return e;
+  GemmArgs d = bwd_args(c, seg, status, R);  // unweighted: topk_w null
+  d.out = o;
+  d.ldo = c.d_model;
+  d.K = c.d_ff;
+  d.n_out = c.d_model;
+  d.NT = (c.d_model + 255) / 256;
+  d.b_rows = c.d_model;
+  d.pc = c.d_model;
+  return launch_gemm<EPI_DOWN, OP_BF16>(m_h, m_h, m_wd, m_wd, d, (int)(mt * d.NT), s);
+}
+
+cudaError_t launch_bwd_dgrad(const moe_config& c, const int32_t* seg, const void* dO,
+                             const void* ab, const void* w_gate, const void* w_up,
+                             const void* w_down, void* dab, void* dA, long long r_rows,
+                             int* status, cudaStream_t s) {
+  const long long P = (long long)c.T * c.top_k;
+  const int E = c.n_experts + c.n_shared;
+  const long long R = P + (long long)c.n_shared * c.T;
+  if (R == 0) return cudaSuccess;
+  const long long rows = std::max(R, r_rows);
+  // A operands K-major (128-row boxes); B MN-major (64 x 64 boxes of the
+  // weights viewed as [E * K][N])
+  CUtensorMap m_do, m_dab, m_wd, m_wg, m_wu;
+  const bool ok = make_map(&m_do, dO, rows, c.d_model) &&
+                  make_map(&m_dab, dab, rows, 2LL * c.d_ff) &&
+                  make_map(&m_wd, w_down, (long long)E * c.d_model, c.d_ff, 64) &&
+                  make_map(&m_wg, w_gate, (long long)E * c.d_ff, c.d_model, 64) &&
+                  make_map(&m_wu, w_up, (long long)E * c.d_ff, c.d_model, 64);
+  if (!ok) return cudaErrorInvalidValue;
+  const long long mt = mt_bound_of(c, BM);
+  // dH = dO W_d, K = d_model; SwiGLU backward into dab
+  GemmArgs g = bwd_args(c, seg, status, R);
+  g.out = dab;
+  g.ldo = 2LL * c.d_ff;
+  g.K = c.d_model;
+  g.n_out = c.d_ff;
+  g.NT = (c.d_ff + 255) / 256;
+  g.b_rows = c.d_model;
+  g.kb_split = (c.d_model + BK - 1) / BK;
+  g.aux = static_cast<__nv_bfloat16*>(const_cast<void*>(ab));
+  g.ld_aux = 2LL * c.d_ff;
+  cudaError_t e =
+      launch_gemm<EPI_SWIGLU_BWD, OP_BF16>(m_do, m_do, m_wd, m_wd, g, (int)(mt * g.NT), s);
+  if (e != cudaSuccess) return e;
+  // dA = da W_g + db W_u, K = 2 d_ff (W_g rows for the first d_ff / 64 blocks)
+  GemmArgs d = bwd_args(c, seg, status, R);
+  d.out = dA;
+  d.ldo = c.d_model;
+  d.K = 2 * c.d_ff;
+  d.n_out = c.d_model;
+  d.NT = (c.d_model + 255) / 256;
+  d.b_rows = c.d_ff;
+  d.kb_split = c.d_ff / BK;
+  return launch_gemm<EPI_DGRAD, OP_BF16>(m_dab, m_dab, m_wg, m_wu, d, (int)(mt * d.NT), s);
 }
 
 }  // namespace moe

@@ -168,6 +168,42 @@ cudaError_t launch_balance_stats(int N, int T, int k, const int32_t* counts,
 bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols,
               unsigned box_rows = 128u);
 
+// ---- backward (bwd.cu, wgrad_sm103.cu, grouped_sm103.cu) -------------------
+// dL/dg of every pair (0 for a dropped one) and dO = g * dy per expert row
+// (dy for shared-expert rows), from the unweighted expert outputs o.
+cudaError_t launch_bwd_gate(const moe_config& c, const void* dy, const void* o,
+                            const int32_t* inv_pos, const float* topk_w, float* dg, void* dO,
+                            cudaStream_t s);
+// dL/dr [T][N] fp32: softmax backward of the gates plus the balance term.
+cudaError_t launch_bwd_score(const moe_config& c, const float* logits, const int32_t* topk_idx,
+                             const float* topk_w, const float* dg, const int32_t* counts,
+                             float alpha, float aux_grad, float* dr, cudaStream_t s);
+// dx [T][d] fp32 = the token's dA rows + dr W_r.
+cudaError_t launch_bwd_dx(const moe_config& c, const void* dA, const int32_t* inv_pos,
+                          const float* dr, const void* w_router, float* dx, cudaStream_t s);
+// dW_r [N][d] fp32 = dr^T x.
+cudaError_t launch_bwd_wr(const moe_config& c, const float* dr, const void* x, float* dw_router,
+                          cudaStream_t s);
+// Forward recompute for the backward (1-CTA tiles; seg built with kTileM):
+// h, the pre-activations ab = a | b [rows][2 d_ff], and the unweighted
+// expert outputs o [rows][d], all bf16.
+cudaError_t launch_bwd_recompute(const moe_config& c, const void* x_perm, const void* x,
+                                 const int32_t* seg, const void* w_gate, const void* w_up,
+                                 const void* w_down, void* h, void* ab, void* o, long long xp_rows,
+                                 long long r_rows, int* status, cudaStream_t s);
+// Activation gradients through the experts: dab = da | db [rows][2 d_ff]
+// from dO and ab, then dA [rows][d] = dab [W_g ; W_u]. d_ff % 64 == 0.
+cudaError_t launch_bwd_dgrad(const moe_config& c, const int32_t* seg, const void* dO,
+                             const void* ab, const void* w_gate, const void* w_up,
+                             const void* w_down, void* dab, void* dA, long long r_rows,
+                             int* status, cudaStream_t s);
+// Weight gradients (fp32): dW_g[e] = da_e^T A_e, dW_u[e] = db_e^T A_e,
+// dW_d[e] = dO_e^T h_e, A = x_perm rows (x for shared experts).
+cudaError_t launch_bwd_wgrad(const moe_config& c, const int32_t* seg, const void* x_perm,
+                             const void* x, const void* dab, const void* dO, const void* h,
+                             float* dw_gate, float* dw_up, float* dw_down, long long xp_rows,
+                             long long r_rows, int* status, cudaStream_t s);
+
 // ---- profiling hooks (abi.cu) ----------------------------------------------
 enum KernelId {
   K_RESET = 0,
@@ -185,6 +221,13 @@ enum KernelId {
   K_COMBINE,
   K_BALANCE,
   K_QUANTIZE,
+  K_BWD_GATE,
+  K_BWD_SCORE,
+  K_BWD_DH,
+  K_BWD_DA,
+  K_BWD_DX,
+  K_BWD_WR,
+  K_WGRAD,
   K_NUM
 };
 void prof_begin(int id, cudaStream_t s);

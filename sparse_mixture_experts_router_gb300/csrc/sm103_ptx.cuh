@@ -152,6 +152,32 @@ __device__ __forceinline__ uint64_t sdesc_k128(uint32_t saddr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// Orders this thread's earlier generic-proxy shared-memory writes before
+// later async-proxy accesses (tcgen05.mma operand reads, TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+
+// Shared-memory matrix descriptor for an MN-major operand with the 128-byte
+// swizzle: the operand is stored as TMA boxes of 64 rows (K) x 64 bf16
+// columns (M or N), each row 128 bytes along M/N. One swizzle atom is 8 K
+// rows of 128 bytes (1024 bytes, the stride between 8-row K groups, SBO);
+// the atoms of the next 64 M/N columns start `mn_stride` bytes on (LBO,
+// the box size). A K = 16 step of the MMA is two K groups: +2048 bytes,
+// +128 in the address field.
+__device__ __forceinline__ uint64_t sdesc_mn128(uint32_t saddr, uint32_t mn_stride) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16 with bf16 A and B and an fp32 D, as
+// idesc_bf16_f32, with B MN-major (bit 16) and optionally A MN-major (bit 15).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int M, int N, bool a_mn) {
+  return idesc_bf16_f32(M, N) | (a_mn ? (1u << 15) : 0u) | (1u << 16);
+}
+
 // ---- tcgen05.ld: 32 lanes x 32 columns of 32-bit, one row per thread --------
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

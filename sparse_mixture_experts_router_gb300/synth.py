@@ -106,6 +106,14 @@ def make_inputs(w: Workload, device="cuda", seed: int | None = None) -> dict:
                 sel_bias=sel_bias, logit_bias=logit_bias)
 
 
+def make_grad_output(w: Workload, device="cuda", seed: int | None = None) -> torch.Tensor:
+    """dL/dy [T, d] for the backward: N(0, 1) in the workload dtype, drawn
+    from a generator of its own (the workload seed + 1000), so the forward
+    inputs are the same with or without it."""
+    g = _gen(device, (w.seed if seed is None else seed) + 1000)
+    return _normal_into(torch.empty(w.T, w.d_model, dtype=w.torch_dtype, device=device), 1.0, g)
+
+
 def redraw_rows(x: torch.Tensor, rows, seed: int, round_: int):
     """Replace the listed token rows with fresh N(0, 1) draws (a separate
     stream per round), in place."""

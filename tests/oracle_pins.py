@@ -688,12 +688,24 @@ def pin_backward_samples_match_full(o):
     kw = dict(n_shared=1, capacity=4, aux_grad=2.0, gate_mode=1)
     full = o.layer_backward(*args, **kw)
     cols = [(0, 1), (3, 4), (4, 0), (2, 2)]
-    smp = o.backward_samples(*args, tokens=[0, 4, 8], columns=cols, **kw)
+    experts = {e: (c["wg"][e], c["wu"][e], c["wd"][e]) for e in range(5)}
+    smp = o.backward_samples(c["x"], c["w_router"], experts, 4, c["k"], c["dy"], tokens=[0, 4, 8],
+                             columns=cols, **kw)
     assert _rel(smp["dx_rows"], full["dx"][[0, 4, 8]]) < 1e-12
     for n, (e, j) in enumerate(cols):
         assert _rel(smp["dw_gate_rows"][n], full["dw_gate"][e, j]) < 1e-12
         assert _rel(smp["dw_up_rows"][n], full["dw_up"][e, j]) < 1e-12
         assert _rel(smp["dw_down_cols"][n], full["dw_down"][e, :, j]) < 1e-12
+
+
+def pin_backward_balance_entry_matches_full(o):
+    """The dy = 0 entry point equals the full backward with dy = 0."""
+    c = _bwd_case(26, T=7, N=5, k=2, S=0)
+    dy0 = np.zeros_like(c["dy"])
+    full = o.layer_backward(c["x"], c["w_router"], c["wg"], c["wu"], c["wd"], c["k"], dy0,
+                            gate_mode=1, aux_grad=4.0)
+    dx, dwr = o.balance_backward(c["x"], c["w_router"], c["k"], gate_mode=1, aux_grad=4.0)
+    assert _rel(dx, full["dx"]) < 1e-12 and _rel(dwr, full["dw_router"]) < 1e-12
 
 
 def pin_balance_stats_sum_to_one(o):

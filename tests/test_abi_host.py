@@ -79,6 +79,10 @@ def test_workspace_sizes(lib):
     c = cfg(T=4096, d_model=4096, n_experts=8, top_k=2, d_ff=14336)
     P = 4096 * 2
     assert moe.workspace_size(c) >= 2 * P * 4096 * 2 + P * 14336 * 2
+    # backward: bf16 with d_ff a multiple of 64 only; it holds H, a | b, da | db
+    assert moe.workspace_size(cfg(dtype=moe.MOE_F32), "backward") == 0
+    assert moe.workspace_size(cfg(d_ff=96), "backward") == 0
+    assert moe.workspace_size(c, "backward") >= 5 * P * 14336 * 2
 
 
 def test_status_strings(lib):
@@ -138,6 +142,21 @@ def test_host_rejections_launch_nothing(lib):
     assert lib.moe_layer_forward(ctypes.byref(c), _P(A), _P(A), None, None, _P(A), _P(A), _P(A),
                                  _P(A + 8), None, None, None, None, _P(A), 1 << 30,
                                  None) == moe.MOE_ERR_MISALIGNED
+    # backward: fp32 and d_ff not a multiple of 64 are not built; null and
+    # misaligned outputs; a short workspace
+    F = ctypes.c_float
+    bw = [_P(A)] * 2 + [None, None] + [_P(A)] * 4
+    outs = [_P(A)] * 5
+    assert lib.moe_layer_backward(ctypes.byref(cfg(dtype=moe.MOE_F32)), *bw, F(0.01), F(1.0),
+                                  *outs, _P(A), 1 << 40, None) == moe.MOE_ERR_UNSUPPORTED
+    assert lib.moe_layer_backward(ctypes.byref(cfg(d_ff=96)), *bw, F(0.01), F(1.0), *outs, _P(A),
+                                  1 << 40, None) == moe.MOE_ERR_UNSUPPORTED
+    assert lib.moe_layer_backward(ctypes.byref(c), *bw, F(0.01), F(1.0), None, *outs[1:], _P(A),
+                                  1 << 40, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_backward(ctypes.byref(c), *bw, F(0.01), F(1.0), _P(A + 4), *outs[1:],
+                                  _P(A), 1 << 40, None) == moe.MOE_ERR_MISALIGNED
+    assert lib.moe_layer_backward(ctypes.byref(c), *bw, F(0.01), F(1.0), *outs, _P(A), 64,
+                                  None) == moe.MOE_ERR_WORKSPACE
     # balance stats: bad sizes
     assert lib.moe_balance_stats(0, 4, 1, _P(A), _P(A), ctypes.c_float(0.01), _P(A), _P(A), _P(A),
                                  None) == moe.MOE_ERR_INVALID_ARG
