@@ -2,6 +2,7 @@
 // layout, the call sequence of the layer, device status, and the optional
 // per-kernel event profiler. Every computation runs in the kernels of the
 // other translation units; nothing here touches tensor data on the host.
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <utility>
@@ -202,7 +203,7 @@ const char* kKernelNames[K_NUM] = {"reset_status",  "router_topk",    "permute_h
                                    "gate_up",       "down",           "splitk_reduce",
                                    "combine",       "balance_stats",  "quantize_fp8",
                                    "bwd_gate",      "bwd_score",      "bwd_dh_swiglu",
-                                   "bwd_da",        "bwd_dx",         "bwd_w_router",
+                                   "bwd_da",        "bwd_dx",         "bwd_router",
                                    "bwd_wgrad"};
 struct Prof {
   std::mutex mu;
@@ -477,9 +478,12 @@ struct BwdWs {
   void* o_dA;
   float* dg;
   void* dO;
-  float* dr;
+  void* dr_bf;   // [T][n_pad] bf16
+  void* drT_bf;  // [n_pad][t_pad] bf16
   void* dab;
 };
+int bwd_n_pad(const moe_config& c) { return (c.n_experts + 7) / 8 * 8; }
+int bwd_t_pad(const moe_config& c) { return (c.T + 7) / 8 * 8; }
 BwdWs carve_bwd(Carver& cv, const moe_config& c) {
   BwdWs w;
   const size_t P = (size_t)pairs(c), N = (size_t)c.n_experts, T = (size_t)c.T;
@@ -502,7 +506,9 @@ BwdWs carve_bwd(Carver& cv, const moe_config& c) {
   w.o_dA = cv.take<void>(R * d * 2);
   w.dg = cv.take<float>(sizeof(float) * P);
   w.dO = cv.take<void>(R * d * 2);
-  w.dr = cv.take<float>(sizeof(float) * T * N);
+  const size_t np = (size_t)bwd_n_pad(c), tp = (size_t)bwd_t_pad(c);
+  w.dr_bf = cv.take<void>(std::max<size_t>(T, 1) * np * 2);
+  w.drT_bf = cv.take<void>(np * std::max<size_t>(tp, 8) * 2);
   w.dab = cv.take<void>(R * 2 * f * 2);
   return w;
 }
@@ -552,19 +558,23 @@ int moe_layer_backward(const moe_config* cfg, const void* x, const void* w_route
     // dL/dg and dO, then dL/dr
     e = launch_bwd_gate(c, dy, w.o_dA, w.inv_pos, w.topk_w, w.dg, w.dO, s);
     if (e != cudaSuccess) return fail_cuda(e);
-    e = launch_bwd_score(c, w.logits, w.topk_idx, w.topk_w, w.dg, w.counts, alpha, aux_grad, w.dr,
-                         s);
+    e = launch_bwd_score(c, w.logits, w.topk_idx, w.topk_w, w.dg, w.counts, alpha, aux_grad,
+                         w.dr_bf, w.drT_bf, bwd_n_pad(c), bwd_t_pad(c), s);
     if (e != cudaSuccess) return fail_cuda(e);
-    // through the experts: da | db, dA; then dx
+  }
+  // dx = dr W_r and dW_r = dr^T x (dW_r = 0 when T = 0)
+  e = launch_bwd_router_grads(c, w.dr_bf, w.drT_bf, bwd_n_pad(c), bwd_t_pad(c), x, w_router, dx,
+                              dw_router, w.status, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (c.T > 0) {
+    // through the experts: da | db, dA; then dx += dA rows
     e = launch_bwd_dgrad(c, w.seg, w.dO, w.ab, w_gate, w_up, w_down, w.dab, w.o_dA, r_rows,
                          w.status, s);
     if (e != cudaSuccess) return fail_cuda(e);
-    e = launch_bwd_dx(c, w.o_dA, w.inv_pos, w.dr, w_router, dx, s);
+    e = launch_bwd_dx(c, w.o_dA, w.inv_pos, dx, s);
     if (e != cudaSuccess) return fail_cuda(e);
   }
-  // weight gradients (zero for experts that took no rows, and for T = 0)
-  e = launch_bwd_wr(c, w.dr, x, dw_router, s);
-  if (e != cudaSuccess) return fail_cuda(e);
+  // expert weight gradients (zero for experts that took no rows, and for T = 0)
   if (c.T == 0) {
     const size_t E = (size_t)c.n_experts + c.n_shared;
     const size_t wbytes = E * c.d_ff * c.d_model * sizeof(float);

@@ -10,10 +10,12 @@
 //                     unweighted expert output, and dO[row] = g * dy[t]
 //                     (dy itself for shared-expert rows);
 //  bwd_score_kernel   dL/dr per token: the gates' softmax backward plus the
-//                     balance term alpha * N / T * p * (f - <p, f>);
-//  bwd_dx_kernel      dx[t] = sum of the token's dA rows (kept slots, then
-//                     shared experts) + sum_e dr[t][e] W_r[e];
-//  bwd_wr_kernel      dW_r[e] = sum_t dr[t][e] x[t], tokens in order.
+//                     balance term alpha * N / T * p * (f - <p, f>), stored in
+//                     bf16 as dr [T][n_pad] and drT [n_pad][t_pad], the
+//                     operands of dx = dr W_r and dW_r = dr^T x (tensor cores,
+//                     wgrad_sm103.cu);
+//  bwd_dx_kernel      dx[t] += the token's dA rows (kept slots, then shared
+//                     experts), on top of dr W_r.
 // Every sum runs in a fixed order, so the results are reproducible.
 #include "device_util.cuh"
 #include "moe_internal.h"
@@ -85,8 +87,9 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads)
     bwd_score_kernel(const float* __restrict__ logits, const int32_t* __restrict__ topk_idx,
                      const float* __restrict__ topk_w, const float* __restrict__ dg,
-                     const int32_t* __restrict__ counts, float* __restrict__ dr, int T, int N,
-                     int k, float balance_scale) {
+                     const int32_t* __restrict__ counts, __nv_bfloat16* __restrict__ dr,
+                     __nv_bfloat16* __restrict__ drT, int T, int N, int k, int n_pad, int t_pad,
+                     float balance_scale) {
   constexpr int EPL = kMaxExperts / 32;
   const int lane = threadIdx.x % 32;
   const long long t = (long long)blockIdx.x * kWarps + threadIdx.x / 32;
@@ -143,7 +146,11 @@ __global__ void __launch_bounds__(kThreads)
     const int e = lane + 32 * i;
     if (e < N) {
       const float f = (float)counts[e] * inv_tk;
-      dr[t * N + e] = acc[i] + balance_scale * r[i] * (f - pf);
+      const __nv_bfloat16 v = __float2bfloat16_rn(acc[i] + balance_scale * r[i] * (f - pf));
+      dr[t * n_pad + e] = v;
+      drT[(long long)e * t_pad + t] = v;
+    } else if (e < n_pad) {
+      dr[t * n_pad + e] = __float2bfloat16_rn(0.0f);
     }
   }
 }
@@ -152,8 +159,7 @@ __global__ void __launch_bounds__(kThreads)
 template <int MAXT>
 __global__ void __launch_bounds__(kThreads)
     bwd_dx_kernel(const __nv_bfloat16* __restrict__ dA, const int32_t* __restrict__ inv_pos,
-                  const float* __restrict__ dr, const __nv_bfloat16* __restrict__ w_router,
-                  float* __restrict__ dx, int T, int d, int N, int k, int n_shared) {
+                  float* __restrict__ dx, int T, int d, int k, int n_shared) {
   const int lane = threadIdx.x % 32;
   const long long t = (long long)blockIdx.x * kWarps + threadIdx.x / 32;
   const long long P = (long long)T * k;
@@ -167,9 +173,10 @@ __global__ void __launch_bounds__(kThreads)
     if (pos >= 0 && pos < P) rows[nt++] = pos;
   }
   for (int q = 0; q < n_shared; ++q) rows[nt++] = P + (long long)q * T + t;
-  const float* drt = dr + t * N;
   for (int v = lane; v < d / 8; v += 32) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float4* out = reinterpret_cast<float4*>(dx + t * d) + 2 * v;
+    const float4 r0 = out[0], r1 = out[1];  // dr W_r
+    float acc[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
     for (int i = 0; i < nt; ++i) {
       const uint4 q = __ldg(reinterpret_cast<const uint4*>(dA + rows[i] * d) + v);
       const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
@@ -181,60 +188,9 @@ __global__ void __launch_bounds__(kThreads)
         acc[2 * j + 1] += a1;
       }
     }
-    for (int e = 0; e < N; ++e) {
-      const float g = __ldg(drt + e);
-      const uint4 q = __ldg(reinterpret_cast<const uint4*>(w_router + (long long)e * d) + v);
-      const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float a0, a1;
-        bf16x2_to_f32(qw[j], a0, a1);
-        acc[2 * j] += g * a0;
-        acc[2 * j + 1] += g * a1;
-      }
-    }
-    float4* out = reinterpret_cast<float4*>(dx + t * d) + 2 * v;
     out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
-}
-
-// Block (column group of 256, expert group of 8): thread c sums dr[t][e] x[t][c]
-// over all tokens in order for its 8 experts; the dr rows are staged in
-// shared memory 64 tokens at a time.
-constexpr int kWrExperts = 8;
-constexpr int kWrTokens = 64;
-__global__ void __launch_bounds__(kThreads)
-    bwd_wr_kernel(const float* __restrict__ dr, const __nv_bfloat16* __restrict__ x,
-                  float* __restrict__ dw_router, int T, int d, int N) {
-  __shared__ float s_dr[kWrTokens][kWrExperts];
-  const int c = blockIdx.x * kThreads + threadIdx.x;
-  const int e0 = blockIdx.y * kWrExperts;
-  pdl_wait();
-  pdl_trigger();
-  float acc[kWrExperts];
-#pragma unroll
-  for (int j = 0; j < kWrExperts; ++j) acc[j] = 0.0f;
-  for (int t0 = 0; t0 < T; t0 += kWrTokens) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < kWrTokens * kWrExperts; i += kThreads) {
-      const int tt = t0 + i / kWrExperts, e = e0 + i % kWrExperts;
-      s_dr[i / kWrExperts][i % kWrExperts] = (tt < T && e < N) ? dr[(long long)tt * N + e] : 0.f;
-    }
-    __syncthreads();
-    if (c < d) {
-      const int tn = min(kWrTokens, T - t0);
-      for (int i = 0; i < tn; ++i) {
-        const float xv = __bfloat162float(x[(long long)(t0 + i) * d + c]);
-#pragma unroll
-        for (int j = 0; j < kWrExperts; ++j) acc[j] += s_dr[i][j] * xv;
-      }
-    }
-  }
-  if (c < d)
-#pragma unroll
-    for (int j = 0; j < kWrExperts; ++j)
-      if (e0 + j < N) dw_router[(long long)(e0 + j) * d + c] = acc[j];
 }
 
 }  // namespace
@@ -253,32 +209,25 @@ cudaError_t launch_bwd_gate(const moe_config& c, const void* dy, const void* o,
 
 cudaError_t launch_bwd_score(const moe_config& c, const float* logits, const int32_t* topk_idx,
                              const float* topk_w, const float* dg, const int32_t* counts,
-                             float alpha, float aux_grad, float* dr, cudaStream_t s) {
+                             float alpha, float aux_grad, void* dr_bf, void* drT_bf, int n_pad,
+                             int t_pad, cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
   ProfScope p(K_BWD_SCORE, s);
   const float scale = aux_grad * alpha * (float)c.n_experts / (float)c.T;
   return launch_pdl(bwd_score_kernel, dim3(ceil_div(c.T, kWarps)), dim3(kThreads), 0, s, 1,
-                    logits, topk_idx, topk_w, dg, counts, dr, c.T, c.n_experts, c.top_k, scale);
+                    logits, topk_idx, topk_w, dg, counts, static_cast<__nv_bfloat16*>(dr_bf),
+                    static_cast<__nv_bfloat16*>(drT_bf), c.T, c.n_experts, c.top_k, n_pad, t_pad,
+                    scale);
 }
 
-cudaError_t launch_bwd_dx(const moe_config& c, const void* dA, const int32_t* inv_pos,
-                          const float* dr, const void* w_router, float* dx, cudaStream_t s) {
+cudaError_t launch_bwd_dx(const moe_config& c, const void* dA, const int32_t* inv_pos, float* dx,
+                          cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
   ProfScope p(K_BWD_DX, s);
   static_assert(kMaxTopK + kMaxShared <= 12, "term table");
   return launch_pdl(bwd_dx_kernel<12>, dim3(ceil_div(c.T, kWarps)), dim3(kThreads), 0, s, 1,
-                    static_cast<const __nv_bfloat16*>(dA), inv_pos, dr,
-                    static_cast<const __nv_bfloat16*>(w_router), dx, c.T, c.d_model,
-                    c.n_experts, c.top_k, c.n_shared);
-}
-
-cudaError_t launch_bwd_wr(const moe_config& c, const float* dr, const void* x, float* dw_router,
-                          cudaStream_t s) {
-  ProfScope p(K_BWD_WR, s);
-  return launch_pdl(bwd_wr_kernel,
-                    dim3(ceil_div(c.d_model, kThreads), ceil_div(c.n_experts, kWrExperts)),
-                    dim3(kThreads), 0, s, 1, dr, static_cast<const __nv_bfloat16*>(x), dw_router,
-                    c.T, c.d_model, c.n_experts);
+                    static_cast<const __nv_bfloat16*>(dA), inv_pos, dx, c.T, c.d_model, c.top_k,
+                    c.n_shared);
 }
 
 }  // namespace moe

@@ -167,6 +167,8 @@ cudaError_t launch_balance_stats(int N, int T, int k, const int32_t* counts,
 // box_rows x 64 columns with the 128-byte swizzle (tma_maps.cu).
 bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols,
               unsigned box_rows = 128u);
+// 3-D TMA map of an fp32 output [E][M][N] stored in 32 x 32 boxes.
+bool make_map_out3d(CUtensorMap* m, void* base, long long E, long long M, long long N);
 
 // ---- backward (bwd.cu, wgrad_sm103.cu, grouped_sm103.cu) -------------------
 // dL/dg of every pair (0 for a dropped one) and dO = g * dy per expert row
@@ -174,16 +176,20 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols,
 cudaError_t launch_bwd_gate(const moe_config& c, const void* dy, const void* o,
                             const int32_t* inv_pos, const float* topk_w, float* dg, void* dO,
                             cudaStream_t s);
-// dL/dr [T][N] fp32: softmax backward of the gates plus the balance term.
+// dL/dr: softmax backward of the gates plus the balance term, in bf16 as
+// dr [T][n_pad] and its transpose drT [n_pad][t_pad] (the operands of the
+// two router gradient products; n_pad, t_pad multiples of 8).
 cudaError_t launch_bwd_score(const moe_config& c, const float* logits, const int32_t* topk_idx,
                              const float* topk_w, const float* dg, const int32_t* counts,
-                             float alpha, float aux_grad, float* dr, cudaStream_t s);
-// dx [T][d] fp32 = the token's dA rows + dr W_r.
-cudaError_t launch_bwd_dx(const moe_config& c, const void* dA, const int32_t* inv_pos,
-                          const float* dr, const void* w_router, float* dx, cudaStream_t s);
-// dW_r [N][d] fp32 = dr^T x.
-cudaError_t launch_bwd_wr(const moe_config& c, const float* dr, const void* x, float* dw_router,
+                             float alpha, float aux_grad, void* dr_bf, void* drT_bf, int n_pad,
+                             int t_pad, cudaStream_t s);
+// dx [T][d] fp32 += the token's dA rows (kept slots, then shared experts).
+cudaError_t launch_bwd_dx(const moe_config& c, const void* dA, const int32_t* inv_pos, float* dx,
                           cudaStream_t s);
+// dx = dr W_r and dW_r = dr^T x on the tensor cores (wgrad kernel, one segment).
+cudaError_t launch_bwd_router_grads(const moe_config& c, const void* dr_bf, const void* drT_bf,
+                                    int n_pad, int t_pad, const void* x, const void* w_router,
+                                    float* dx, float* dw_router, int* status, cudaStream_t s);
 // Forward recompute for the backward (1-CTA tiles; seg built with kTileM):
 // h, the pre-activations ab = a | b [rows][2 d_ff], and the unweighted
 // expert outputs o [rows][d], all bf16.
@@ -226,7 +232,7 @@ enum KernelId {
   K_BWD_DH,
   K_BWD_DA,
   K_BWD_DX,
-  K_BWD_WR,
+  K_BWD_ROUTER,
   K_WGRAD,
   K_NUM
 };

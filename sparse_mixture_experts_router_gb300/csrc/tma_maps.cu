@@ -61,6 +61,23 @@ bool make_map_u8(CUtensorMap* m, const void* base, long long rows, long long col
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [E][M][N] written in boxes of 32 rows x 32 columns (128 bytes) with
+// the 128-byte swizzle; the expert index is a dimension of its own, so a box
+// that runs past row M of one expert is clipped there rather than writing
+// into the next expert's rows.
+bool make_map_out3d(CUtensorMap* m, void* base, long long E, long long M, long long N) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)E};
+  cuuint64_t strides[2] = {(cuuint64_t)N * 4, (cuuint64_t)(M * N) * 4};
+  cuuint32_t box[3] = {32u, 32u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int num_sms() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);

@@ -15,9 +15,13 @@
 // 64 rows x 64 columns with the 128-byte swizzle give the MN-major layout
 // tcgen05 reads directly (no transpose pass). Tiles are 128 x 256 outputs of
 // one expert, persistent CTAs, warp-specialised like the forward GEMM:
-// warp 0 loads (4-stage ring of 48 KB), warp 1 issues tcgen05.mma from one
+// warp 0 loads (3-stage ring of 48 KB), warp 1 issues tcgen05.mma from one
 // thread into one of two 256-column TMEM accumulators, warps 2-9 drain them
-// (two warps per TMEM lane quarter, half the columns each) and store fp32.
+// (two warps per TMEM lane quarter, half the columns each): 32 x 32 fp32
+// blocks go through a swizzled shared-memory buffer (two per warp) to TMA
+// tensor stores, so the output leaves in whole 128-byte lines. The same
+// kernel with one segment of K rows (no segment table) computes the router's
+// two gradient products.
 // A segment's last K block may run past its end into the next segment's
 // rows: warp 1 zeroes those rows of both operands in shared memory (whole
 // 128-byte lines, so the swizzle does not matter) and fences them to the
@@ -41,17 +45,19 @@ constexpr int BOX_BYTES = 64 * 128;            // 64 K rows x 64 bf16
 constexpr int WA_BYTES = 2 * BOX_BYTES;        // M = 128: two boxes
 constexpr int WB_BYTES = 4 * BOX_BYTES;        // N = 256: four boxes
 constexpr int W_STAGE_BYTES = WA_BYTES + WB_BYTES;  // 48 KB
-constexpr int W_STAGES = 4;
+constexpr int W_STAGES = 3;
 constexpr int W_ACC = 2;
 constexpr int W_TMEM_COLS = WN * W_ACC;        // 512
 constexpr int W_EPI_THREADS = 256;
 constexpr int W_THREADS = 64 + W_EPI_THREADS;  // 320
-constexpr size_t W_DYN_SMEM = (size_t)W_STAGES * W_STAGE_BYTES + 1024;
+constexpr int STG_BYTES = 32 * 128;              // one 32 x 32 fp32 block
+constexpr int W_STG_BYTES = 8 * 2 * STG_BYTES;     // two blocks per epilogue warp
+constexpr size_t W_DYN_SMEM = (size_t)W_STAGES * W_STAGE_BYTES + W_STG_BYTES + 1024;
 
 struct WgradArgs {
-  const int32_t* seg;  // segment table (moe_internal.h)
+  const int32_t* seg;  // segment table (moe_internal.h), or null: one segment
+  int rows1;           // of rows1 rows from row 0 of A and B
   int* status;
-  float* out;          // [E][M][N] fp32
   int M, N;            // one expert's gradient
   int MT, NT;          // its tiles
   int a_col0;          // first column of A taken (the up half of da | db: d_ff)
@@ -81,6 +87,11 @@ __device__ __forceinline__ WTile wtile(const WgradArgs& a, int E, int tile) {
   const int r = tile - w.e * per;
   w.n = r / a.MT;
   w.m = r - w.n * a.MT;
+  if (!a.seg) {
+    w.rows = a.rows1;
+    w.a_row = w.b_row = 0;
+    return w;
+  }
   w.rows = __ldg(a.seg + 3 + E + w.e);
   w.a_row = __ldg(a.seg + 3 + 3 * E + w.e);
   w.b_row = a.b_in_rows ? __ldg(a.seg + 3 + 2 * E + w.e) : w.a_row;
@@ -89,7 +100,8 @@ __device__ __forceinline__ WTile wtile(const WgradArgs& a, int E, int tile) {
 
 __global__ void __launch_bounds__(W_THREADS, 1)
     wgrad_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                 const __grid_constant__ CUtensorMap map_b_shared, const WgradArgs args) {
+                 const __grid_constant__ CUtensorMap map_b_shared,
+                 const __grid_constant__ CUtensorMap map_out, const WgradArgs args) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ WState st;
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x / 32), 0);
@@ -113,6 +125,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
     ptx::prefetch_tmap(&map_a);
     ptx::prefetch_tmap(&map_b);
     ptx::prefetch_tmap(&map_b_shared);
+    ptx::prefetch_tmap(&map_out);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_addr(&st.tmem_base), W_TMEM_COLS);
@@ -125,7 +138,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
   volatile int* abort_flag = &st.abort;
   pdl_wait();
   pdl_trigger();
-  const int E = __ldg(args.seg);
+  const int E = args.seg ? __ldg(args.seg) : 1;
   const int tiles = E * args.MT * args.NT;
 
   if (warp == 0) {
@@ -241,47 +254,57 @@ __global__ void __launch_bounds__(W_THREADS, 1)
     // ------------------------------------------------------------ epilogue --
     const int sub = warp & 3;          // TMEM lanes [32 sub, 32 sub + 32)
     const int half = (warp - 2) >> 2;  // columns [128 half, 128 half + 128)
-    const int r_in = sub * 32 + lane;
+    const uint32_t stg = ring + W_STAGES * W_STAGE_BYTES + (warp - 2) * 2 * STG_BYTES;
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t nblk = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
       const WTile w = wtile(args, E, tile);
-      const int r = w.m * WM + r_in;
-      float* orow = args.out + ((long long)w.e * args.M + r) * args.N + w.n * WN;
-      const bool row_ok = r < args.M;
-      if (w.rows == 0) {
-        if (row_ok)
-          for (int c = half * 128; c < half * 128 + 128; c += 4)
-            if (w.n * WN + c < args.N)
-              *reinterpret_cast<float4*>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-        continue;
+      const bool zero = w.rows == 0;  // no rows: a zero gradient, no MMA
+      uint32_t tbase = 0;
+      if (!zero) {
+        const bool ok =
+            wait_phase(ptx::smem_addr(&st.acc_full[acc]), acc_phase, abort_flag, args.status);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        ptx::tc_fence_after();
+        tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * WN);
       }
-      const bool ok =
-          wait_phase(ptx::smem_addr(&st.acc_full[acc]), acc_phase, abort_flag, args.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      ptx::tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * WN);
 #pragma unroll 1
-      for (int c = 4 * half; c < 4 * half + 4; ++c) {
+      for (int c = 4 * half; c < 4 * half + 4; ++c, ++nblk) {
         uint32_t v[32];
-        ptx::tmem_ld32(tbase + c * 32, v);
-        ptx::tmem_ld_wait();
-        if (row_ok) {
+        if (!zero) {
+          ptx::tmem_ld32(tbase + c * 32, v);
+        } else {
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            if (w.n * WN + c * 32 + 4 * q < args.N)
-              *reinterpret_cast<float4*>(orow + c * 32 + 4 * q) =
-                  make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                              __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        // this buffer's store from two blocks ago has read shared memory
+        const uint32_t buf = stg + (nblk & 1u) * STG_BYTES;
+        if (lane == 0) ptx::bulk_wait_read<1>();
+        __syncwarp();
+        if (!zero) ptx::tmem_ld_wait();
+        // row `lane` of the 32 x 32 block, 16-byte chunk q at q ^ (row % 8)
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          ptx::st_shared_v4(buf + lane * 128 + ((q ^ (lane & 7)) << 4), v[4 * q], v[4 * q + 1],
+                            v[4 * q + 2], v[4 * q + 3]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_3d(&map_out, buf, w.n * WN + c * 32, w.m * WM + sub * 32, w.e);
+          ptx::bulk_commit();
         }
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(ptx::smem_addr(&st.acc_empty[acc]));
-      if (++acc == W_ACC) {
-        acc = 0;
-        acc_phase ^= 1u;
+      if (!zero) {
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ptx::smem_addr(&st.acc_empty[acc]));
+        if (++acc == W_ACC) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
     }
+    if (lane == 0) ptx::bulk_wait_all();
   }
 
   ptx::tc_fence_before();
@@ -294,7 +317,8 @@ __global__ void __launch_bounds__(W_THREADS, 1)
 }
 
 cudaError_t launch_wgrad(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b_sh,
-                         const WgradArgs& args, int E, cudaStream_t s) {
+                         const CUtensorMap& out, const WgradArgs& args, int E, int prof_id,
+                         cudaStream_t s) {
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -307,8 +331,9 @@ cudaError_t launch_wgrad(const CUtensorMap& a, const CUtensorMap& b, const CUten
   const long long tiles = (long long)E * args.MT * args.NT;
   if (tiles == 0) return cudaSuccess;
   const int grid = (int)std::min<long long>(tiles, num_sms());
-  ProfScope p(K_WGRAD, s);
-  return launch_pdl(wgrad_kernel, dim3(grid), dim3(W_THREADS), W_DYN_SMEM, s, 1, a, b, b_sh, args);
+  ProfScope p(prof_id, s);
+  return launch_pdl(wgrad_kernel, dim3(grid), dim3(W_THREADS), W_DYN_SMEM, s, 1, a, b, b_sh, out,
+                    args);
 }
 
 }  // namespace
@@ -321,8 +346,11 @@ cudaError_t launch_bwd_wgrad(const moe_config& c, const int32_t* seg, const void
   const long long R = P + (long long)c.n_shared * c.T;
   const int E = c.n_experts + c.n_shared;
   const long long rows = std::max(R, r_rows);
-  CUtensorMap m_dab, m_do, m_h, m_xp, m_x;
-  const bool ok = make_map(&m_dab, dab, rows, 2LL * c.d_ff, 64) &&
+  CUtensorMap m_dab, m_do, m_h, m_xp, m_x, o_g, o_u, o_d;
+  const bool ok = make_map_out3d(&o_g, dw_gate, E, c.d_ff, c.d_model) &&
+                  make_map_out3d(&o_u, dw_up, E, c.d_ff, c.d_model) &&
+                  make_map_out3d(&o_d, dw_down, E, c.d_model, c.d_ff) &&
+                  make_map(&m_dab, dab, rows, 2LL * c.d_ff, 64) &&
                   make_map(&m_do, dO, rows, c.d_model, 64) &&
                   make_map(&m_h, h, rows, c.d_ff, 64) &&
                   make_map(&m_xp, x_perm, std::max(P, xp_rows), c.d_model, 64) &&
@@ -339,13 +367,11 @@ cudaError_t launch_bwd_wgrad(const moe_config& c, const int32_t* seg, const void
   a.MT = ceil_div(c.d_ff, WM);
   a.NT = ceil_div(c.d_model, WN);
   a.b_in_rows = 1;
-  a.out = dw_gate;
   a.a_col0 = 0;
-  cudaError_t e = launch_wgrad(m_dab, m_xp, m_x, a, E, s);
+  cudaError_t e = launch_wgrad(m_dab, m_xp, m_x, o_g, a, E, K_WGRAD, s);
   if (e != cudaSuccess) return e;
-  a.out = dw_up;
   a.a_col0 = c.d_ff;
-  e = launch_wgrad(m_dab, m_xp, m_x, a, E, s);
+  e = launch_wgrad(m_dab, m_xp, m_x, o_u, a, E, K_WGRAD, s);
   if (e != cudaSuccess) return e;
   // dW_d [E][d][d_ff]: A = dO, B = H (both in the output-row space)
   a.M = c.d_model;
@@ -353,9 +379,40 @@ cudaError_t launch_bwd_wgrad(const moe_config& c, const int32_t* seg, const void
   a.MT = ceil_div(c.d_model, WM);
   a.NT = ceil_div(c.d_ff, WN);
   a.b_in_rows = 0;
-  a.out = dw_down;
   a.a_col0 = 0;
-  return launch_wgrad(m_do, m_h, m_h, a, E, s);
+  return launch_wgrad(m_do, m_h, m_h, o_d, a, E, K_WGRAD, s);
+}
+
+cudaError_t launch_bwd_router_grads(const moe_config& c, const void* dr_bf, const void* drT_bf,
+                                    int n_pad, int t_pad, const void* x, const void* w_router,
+                                    float* dx, float* dw_router, int* status, cudaStream_t s) {
+  CUtensorMap m_dr, m_drt, m_x, m_wr, o_dx, o_wr;
+  const bool ok = make_map(&m_dr, dr_bf, std::max(c.T, 1), n_pad, 64) &&
+                  make_map(&m_drt, drT_bf, n_pad, t_pad, 64) &&
+                  make_map(&m_x, x, std::max(c.T, 1), c.d_model, 64) &&
+                  make_map(&m_wr, w_router, c.n_experts, c.d_model, 64) &&
+                  make_map_out3d(&o_dx, dx, 1, std::max(c.T, 1), c.d_model) &&
+                  make_map_out3d(&o_wr, dw_router, 1, c.n_experts, c.d_model);
+  if (!ok) return cudaErrorInvalidValue;
+  WgradArgs a{};
+  a.status = status;
+  a.n_routed = 1;
+  a.N = c.d_model;
+  a.NT = ceil_div(c.d_model, WN);
+  // dx = dr W_r: K = the N experts, A = dr^T [N][T], B = W_r [N][d]
+  cudaError_t e = cudaSuccess;
+  if (c.T > 0) {
+    a.rows1 = c.n_experts;
+    a.M = c.T;
+    a.MT = ceil_div(c.T, WM);
+    e = launch_wgrad(m_drt, m_wr, m_wr, o_dx, a, 1, K_BWD_ROUTER, s);
+    if (e != cudaSuccess) return e;
+  }
+  // dW_r = dr^T x: K = the T tokens, A = dr [T][N], B = x [T][d]
+  a.rows1 = c.T;
+  a.M = c.n_experts;
+  a.MT = ceil_div(c.n_experts, WM);
+  return launch_wgrad(m_dr, m_x, m_x, o_wr, a, 1, K_BWD_ROUTER, s);
 }
 
 }  // namespace moe
