@@ -405,6 +405,8 @@ def run_ours(args):
             per_kernel[name]["hbm_frac"] = round(gbs / pk["hbm"], 4)
 
     decode = run_decode(moe, synth, dev, stream, pk, args) if default and not args.no_decode else None
+    backward = (run_backward(moe, dev, stream, pk, w, inp, cfg, args)
+                if default and not args.fp8 and not args.no_backward else None)
     E = w.n_experts + w.n_shared
     wb = 3 * E * w.d_model * w.d_ff * (1 if args.fp8 else 2)  # E4M3 codes: 1 byte each
     routing = {"max_over_mean_expert_load": round(float(counts.max()) / max(1e-9, float(counts.float().mean())), 3),
@@ -444,8 +446,71 @@ def run_ours(args):
             "clocks": clk,
             "kernels": per_kernel,
             "decode": decode,
+            "backward": backward,
         }
         print(json.dumps(line))
+
+
+def run_backward(moe, dev, stream, pk, w, inp, cfg, args):
+    """The layer's backward (moe_layer_backward: forward recomputed, then the
+    activation and weight gradients) on the same workload, dL/dy ~ N(0, 1):
+    device time per step with CUDA events (operands and gradients far larger
+    than L2), a per-kernel breakdown from a separate profiled step, and the
+    tensor-core work against the bf16 peak. Algorithmic work: the forward's
+    two projections again (6 d d_ff flop per row), the activation gradients
+    dH and dA (6 d d_ff), the weight gradients (6 d d_ff); the router's
+    products (2 x 2 T N d) are counted too."""
+    import torch
+    from sparse_mixture_experts_router_gb300 import synth
+    E = w.n_experts + w.n_shared
+    dy = synth.make_grad_output(w, dev)
+    dx = torch.empty(w.T, w.d_model, device=dev)
+    dwr = torch.empty(w.n_experts, w.d_model, device=dev)
+    dwg = torch.empty(E, w.d_ff, w.d_model, device=dev)
+    dwu = torch.empty_like(dwg)
+    dwd = torch.empty(E, w.d_model, w.d_ff, device=dev)
+    ws = moe.workspace(cfg, "backward", dev)
+
+    def step():
+        moe.moe_layer_backward(cfg, inp["x"], inp["w_router"], inp["logit_bias"], inp["sel_bias"],
+                               inp["w_gate"], inp["w_up"], inp["w_down"], dy, 0.01, 1.0, dx, dwr,
+                               dwg, dwu, dwd, ws, stream)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    if moe.moe_stream_status(ws, stream) != 0:
+        raise RuntimeError("backward warm-up failed on the device")
+    reps = max(3, min(args.steps, 20))
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / reps
+    moe.profile_enable(True)
+    moe.profile_collect()
+    step()
+    kern = moe.profile_collect()
+    moe.profile_enable(False)
+    R = w.T * (w.top_k + w.n_shared)
+    flops = 18.0 * w.d_model * w.d_ff * R + 4.0 * w.T * w.n_experts * w.d_model
+    tf = flops / (ms / 1e3) / 1e12
+    out = {"ms_per_step": round(ms, 4), "steps": reps,
+           "tokens_per_s": round(w.T / (ms / 1e3), 1),
+           "algorithmic_tflop": round(flops / 1e12, 3), "tflops": round(tf, 1),
+           "frac_of_bf16_sustained": round(tf / pk["bf16_sustained"], 4),
+           "kernels": {k: {"ms": round(v[0], 4), "launches": v[1],
+                           "share": round(v[0] / sum(x[0] for x in kern.values()), 4)}
+                       for k, v in kern.items()},
+           "outputs": "fp32 dx, dW_r, dW_g, dW_u, dW_d; dy bf16; alpha 0.01, aux_grad 1"}
+    if "bwd_wgrad" in kern:  # the three expert weight-gradient launches
+        wms = kern["bwd_wgrad"][0] / kern["bwd_wgrad"][1]
+        wfl = 2.0 * w.d_model * w.d_ff * R
+        out["wgrad_tflops"] = round(wfl / (wms / 1e3) / 1e12, 1)
+        out["wgrad_gbs_written"] = round(E * w.d_model * w.d_ff * 4 / (wms / 1e3) / 1e9, 1)
+    return out
 
 
 def run_decode(moe, synth, dev, stream, pk, args):
@@ -627,6 +692,7 @@ def main(argv=None):
                     help="sampled tokens per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--fp8", action="store_true",
                     help="E4M3 expert weights (moe_layer_forward_fp8); not the headline, which is bf16")
     ap.add_argument("--traffic", type=float, default=None,

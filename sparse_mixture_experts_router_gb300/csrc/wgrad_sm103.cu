@@ -15,11 +15,14 @@
 // 64 rows x 64 columns with the 128-byte swizzle give the MN-major layout
 // tcgen05 reads directly (no transpose pass). Tiles are 128 x 256 outputs of
 // one expert, persistent CTAs, warp-specialised like the forward GEMM:
-// warp 0 loads (3-stage ring of 48 KB), warp 1 issues tcgen05.mma from one
+// warp 0 loads (4-stage ring of 48 KB), warp 1 issues tcgen05.mma from one
 // thread into one of two 256-column TMEM accumulators, warps 2-9 drain them
 // (two warps per TMEM lane quarter, half the columns each): 32 x 32 fp32
-// blocks go through a swizzled shared-memory buffer (two per warp) to TMA
-// tensor stores, so the output leaves in whole 128-byte lines. The same
+// blocks go through a swizzled shared-memory buffer (one per warp) to TMA
+// tensor stores, so the output leaves in whole 128-byte lines. (Measured
+// alternatives, slower on these shapes: a 3-stage ring with two buffers a
+// warp; CTA pairs with 256 x 256 tiles; plain coalesced stores after a
+// shared-memory transpose.) The same
 // kernel with one segment of K rows (no segment table) computes the router's
 // two gradient products.
 // A segment's last K block may run past its end into the next segment's
@@ -45,13 +48,13 @@ constexpr int BOX_BYTES = 64 * 128;            // 64 K rows x 64 bf16
 constexpr int WA_BYTES = 2 * BOX_BYTES;        // M = 128: two boxes
 constexpr int WB_BYTES = 4 * BOX_BYTES;        // N = 256: four boxes
 constexpr int W_STAGE_BYTES = WA_BYTES + WB_BYTES;  // 48 KB
-constexpr int W_STAGES = 3;
+constexpr int W_STAGES = 4;
 constexpr int W_ACC = 2;
 constexpr int W_TMEM_COLS = WN * W_ACC;        // 512
 constexpr int W_EPI_THREADS = 256;
 constexpr int W_THREADS = 64 + W_EPI_THREADS;  // 320
 constexpr int STG_BYTES = 32 * 128;              // one 32 x 32 fp32 block
-constexpr int W_STG_BYTES = 8 * 2 * STG_BYTES;     // two blocks per epilogue warp
+constexpr int W_STG_BYTES = 8 * STG_BYTES;         // one block per epilogue warp
 constexpr size_t W_DYN_SMEM = (size_t)W_STAGES * W_STAGE_BYTES + W_STG_BYTES + 1024;
 
 struct WgradArgs {
@@ -254,10 +257,9 @@ __global__ void __launch_bounds__(W_THREADS, 1)
     // ------------------------------------------------------------ epilogue --
     const int sub = warp & 3;          // TMEM lanes [32 sub, 32 sub + 32)
     const int half = (warp - 2) >> 2;  // columns [128 half, 128 half + 128)
-    const uint32_t stg = ring + W_STAGES * W_STAGE_BYTES + (warp - 2) * 2 * STG_BYTES;
+    const uint32_t stg = ring + W_STAGES * W_STAGE_BYTES + (warp - 2) * STG_BYTES;
     int acc = 0;
     uint32_t acc_phase = 0;
-    uint32_t nblk = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
       const WTile w = wtile(args, E, tile);
       const bool zero = w.rows == 0;  // no rows: a zero gradient, no MMA
@@ -270,7 +272,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
         tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * WN);
       }
 #pragma unroll 1
-      for (int c = 4 * half; c < 4 * half + 4; ++c, ++nblk) {
+      for (int c = 4 * half; c < 4 * half + 4; ++c) {
         uint32_t v[32];
         if (!zero) {
           ptx::tmem_ld32(tbase + c * 32, v);
@@ -278,9 +280,9 @@ __global__ void __launch_bounds__(W_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
-        // this buffer's store from two blocks ago has read shared memory
-        const uint32_t buf = stg + (nblk & 1u) * STG_BYTES;
-        if (lane == 0) ptx::bulk_wait_read<1>();
+        // the previous block's store has read the buffer
+        const uint32_t buf = stg;
+        if (lane == 0) ptx::bulk_wait_read<0>();
         __syncwarp();
         if (!zero) ptx::tmem_ld_wait();
         // row `lane` of the 32 x 32 block, 16-byte chunk q at q ^ (row % 8)
