@@ -451,6 +451,27 @@ def run_ours(args):
         print(json.dumps(line))
 
 
+def run_backward_only(args):
+    """The backward alone, on the workload or a smaller case of the same shape
+    (--tokens, --experts): one JSON line with the backward object."""
+    import torch
+
+    import sparse_mixture_experts_router_gb300 as moe
+    from sparse_mixture_experts_router_gb300 import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload](synth)
+    w = w.replace(T=args.tokens or w.T, n_experts=args.experts or w.n_experts,
+                  top_k=min(w.top_k, args.experts or w.n_experts))
+    inp = synth.make_inputs(w, dev)
+    cfg = moe.config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k, d_ff=w.d_ff,
+                     n_shared=w.n_shared, dtype=moe.MOE_BF16, gate_mode=w.gate_mode,
+                     capacity=capacity_of(w))
+    out = run_backward(moe, dev, torch.cuda.current_stream(dev), peaks(), w, inp, cfg, args)
+    print(json.dumps({"workload": w.name, "T": w.T, "n_experts": w.n_experts, "top_k": w.top_k,
+                      "d_model": w.d_model, "d_ff": w.d_ff, "backward": out}))
+
+
 def run_backward(moe, dev, stream, pk, w, inp, cfg, args):
     """The layer's backward (moe_layer_backward: forward recomputed, then the
     activation and weight gradients) on the same workload, dL/dy ~ N(0, 1):
@@ -693,6 +714,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="time only the layer's backward and print its object (for profiling)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="with --backward-only: tokens T instead of the workload's")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="with --backward-only: routed experts N instead of the workload's")
     ap.add_argument("--fp8", action="store_true",
                     help="E4M3 expert weights (moe_layer_forward_fp8); not the headline, which is bf16")
     ap.add_argument("--traffic", type=float, default=None,
@@ -701,6 +728,8 @@ def main(argv=None):
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.backward_only:
+        run_backward_only(args)
     else:
         run_ours(args)
 
