@@ -276,7 +276,7 @@ def run_ours(args):
     clocks.start()
     # Events only around the dominant kernel: an event between two launches
     # costs the programmatic-dependent-launch overlap at that boundary.
-    moe.profile_enable(True, kernels=["gate_up"])
+    moe.profile_enable(True, kernels=["gate_up", "decode_fused"])
     moe.profile_collect()  # drop anything recorded before
     launches0 = moe.launch_count()
     barrier(ws)
@@ -363,27 +363,43 @@ def run_ours(args):
         per_kernel[name] = {"ms_per_launch": ms / n, "launches": n,
                             "share": ms / sum(v[0] for v in kern.values())}
     # the dominant kernel's duration comes from the timed region itself
-    per_kernel["gate_up"]["ms_per_launch"] = kern_timed["gate_up"][0] / kern_timed["gate_up"][1]
-    gu_ms = per_kernel["gate_up"]["ms_per_launch"]
-    dn_ms = per_kernel["down"]["ms_per_launch"]
-    per_kernel["gate_up"]["tflops"] = f_gu / (gu_ms / 1e3) / 1e12
-    per_kernel["down"]["tflops"] = f_dn / (dn_ms / 1e3) / 1e12
-    gemm_tflops = (f_gu + f_dn) / ((gu_ms + dn_ms) / 1e3) / 1e12
-    ach = per_kernel["gate_up"]["tflops"]
     # E4M3: the measured bf16 peaks times the nominal fp8/bf16 ratio (4.5 / 2.25)
     tpk = pk["bf16"] * (2.0 if args.fp8 else 1.0)
     tpk_s = pk["bf16_sustained"] * (2.0 if args.fp8 else 1.0)
-    roofline = {"bound": "tensor", "kernel": "gate_up (grouped SwiGLU gate+up GEMM)",
-                "achieved": round(ach, 1), "peak": round(tpk, 1), "unit": "TFLOP/s",
-                "frac": round(ach / tpk, 4),
-                "traffic": (args.traffic if args.traffic is not None
-                            else recorded_traffic(args.fp8)),
-                "peak_source": (f"{pk['source']} bf16 burst x 2 (nominal fp8/bf16 ratio)"
-                                if args.fp8 else f"{pk['source']} bf16 burst"),
-                "frac_of_sustained": round(ach / tpk_s, 4),
-                "algorithmic_flops_per_launch": f_gu,
-                "grouped_gemm_both_kernels_tflops": round(gemm_tflops, 1),
-                "grouped_gemm_both_kernels_frac": round(gemm_tflops / tpk, 4)}
+    if "gate_up" not in kern_timed:  # a single token: the whole layer is one kernel
+        fused_ms = kern_timed["decode_fused"][0] / kern_timed["decode_fused"][1]
+        per_kernel["decode_fused"]["ms_per_launch"] = fused_ms
+        wbytes, _ = touched_weight_bytes(w, counts.cpu().tolist(), args.fp8)
+        total = wbytes + w.n_experts * w.d_model * 2 + 2 * w.T * w.d_model * 2
+        gbs = total / (fused_ms / 1e3) / 1e9
+        per_kernel["decode_fused"]["gbs"] = round(gbs, 1)
+        gemm_tflops = (f_gu + f_dn) / (fused_ms / 1e3) / 1e12
+        roofline = {"bound": "hbm", "kernel": "decode_fused (routing, both projections and the "
+                                              "gated sum in one kernel)",
+                    "achieved": round(gbs, 1), "peak": round(pk["hbm"], 1), "unit": "GB/s",
+                    "frac": round(gbs / pk["hbm"], 4), "traffic": None,
+                    "peak_source": f"{pk['source']} HBM copy",
+                    "algorithmic_bytes_per_launch": total}
+    else:
+        per_kernel["gate_up"]["ms_per_launch"] = kern_timed["gate_up"][0] / kern_timed["gate_up"][1]
+    gu_ms = per_kernel["gate_up"]["ms_per_launch"] if "gate_up" in kern_timed else None
+    if gu_ms is not None:
+        dn_ms = per_kernel["down"]["ms_per_launch"]
+        per_kernel["gate_up"]["tflops"] = f_gu / (gu_ms / 1e3) / 1e12
+        per_kernel["down"]["tflops"] = f_dn / (dn_ms / 1e3) / 1e12
+        gemm_tflops = (f_gu + f_dn) / ((gu_ms + dn_ms) / 1e3) / 1e12
+        ach = per_kernel["gate_up"]["tflops"]
+        roofline = {"bound": "tensor", "kernel": "gate_up (grouped SwiGLU gate+up GEMM)",
+                    "achieved": round(ach, 1), "peak": round(tpk, 1), "unit": "TFLOP/s",
+                    "frac": round(ach / tpk, 4),
+                    "traffic": (args.traffic if args.traffic is not None
+                                else recorded_traffic(args.fp8)),
+                    "peak_source": (f"{pk['source']} bf16 burst x 2 (nominal fp8/bf16 ratio)"
+                                    if args.fp8 else f"{pk['source']} bf16 burst"),
+                    "frac_of_sustained": round(ach / tpk_s, 4),
+                    "algorithmic_flops_per_launch": f_gu,
+                    "grouped_gemm_both_kernels_tflops": round(gemm_tflops, 1),
+                    "grouped_gemm_both_kernels_frac": round(gemm_tflops / tpk, 4)}
     # HBM-bound kernels of the step against the copy bandwidth
     P = w.T * w.top_k
     hb = {"router_topk": w.T * w.d_model * 2 + w.n_experts * w.d_model * 2 + P * 8,

@@ -93,6 +93,7 @@ struct LayerWs {
   int32_t* seg;
   void* h;
   float* partial;
+  float* dpart;  // the one-kernel decode path's workspace
 };
 LayerWs carve_layer(Carver& cv, const moe_config& c) {
   LayerWs w;
@@ -113,6 +114,7 @@ LayerWs carve_layer(Carver& cv, const moe_config& c) {
   w.h = cv.take<void>((size_t)padded_rows(rows_total(c)) * c.d_ff * eb);
   const SplitKPlan plan = splitk_plan(c);
   w.partial = cv.take<float>(plan.partial_bytes);
+  w.dpart = cv.take<float>(decode_fused_ws_bytes(c));
   return w;
 }
 
@@ -204,7 +206,7 @@ const char* kKernelNames[K_NUM] = {"reset_status",  "router_topk",    "permute_h
                                    "combine",       "balance_stats",  "quantize_fp8",
                                    "bwd_gate",      "bwd_score",      "bwd_dh_swiglu",
                                    "bwd_da",        "bwd_dx",         "bwd_router",
-                                   "bwd_wgrad"};
+                                   "bwd_wgrad",     "decode_fused"};
 struct Prof {
   std::mutex mu;
   uint32_t mask = 0;
@@ -237,7 +239,7 @@ Prof& prof() {
 namespace {
 __global__ void reset_status_kernel(int* status) {
   pdl_wait();
-  if (threadIdx.x < 2) status[threadIdx.x] = 0;
+  if (threadIdx.x < 3) status[threadIdx.x] = 0;
   __syncwarp();
   pdl_trigger();
 }
@@ -440,6 +442,11 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* w_router
   float* tw = topk_w ? topk_w : w.topk_w;
   int32_t* cnt = counts ? counts : w.counts;
   float* ps = prob_sum ? prob_sum : w.prob_sum;
+  if (decode_fused_applies(c)) {  // a decode-sized batch: the whole layer in one kernel
+    cudaError_t e = launch_decode_fused(c, x, w_router, logit_bias, sel_bias, w_gate, w_up, w_down,
+                                        y, idx, tw, cnt, ps, w.dpart, w.status, s);
+    return e == cudaSuccess ? MOE_OK : fail_cuda(e);
+  }
   cudaError_t e = launch_router(c, x, w_router, logit_bias, sel_bias, nullptr, nullptr, idx, tw,
                                 cnt, ps, w.partials, w.status, s);
   if (e != cudaSuccess) return fail_cuda(e);

@@ -100,8 +100,9 @@ cudaError_t launch_grouped_e4m3(const moe_config& c, const uint8_t* xq_perm,
 bool make_map_u8(CUtensorMap* m, const void* base, long long rows, long long cols,
                  unsigned box_rows = 128u);
 
-// Zeroes the status word and the router's block counter (a kernel, so it
-// keeps the chain of programmatic dependent launches).
+// Zeroes the status word, the router's block counter and the decode kernel's
+// grid-barrier counter (a kernel, so it keeps the chain of programmatic
+// dependent launches).
 cudaError_t launch_reset_status(int* status, cudaStream_t s);
 // Blocks the router's per-block partials are sized for.
 int router_partial_blocks(const moe_config& c);
@@ -170,6 +171,23 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols,
 // 3-D TMA map of an fp32 output [E][M][N] stored in 32 x 32 boxes.
 bool make_map_out3d(CUtensorMap* m, void* base, long long E, long long M, long long N);
 
+// ---- decode-sized layers in one kernel (decode_fused.cu) -------------------
+constexpr int kDecodeFusedMaxT = 1;
+// bf16, 1 <= T <= kDecodeFusedMaxT, N <= 32, d_model a multiple of 256,
+// d_ff of 256, x of all tokens (fp32) within the kernel's shared memory.
+bool decode_fused_applies(const moe_config& c);
+// Its workspace: the gate/up pre-activation halves and the down
+// projection's partial sums (0 when it does not apply).
+size_t decode_fused_ws_bytes(const moe_config& c);
+// The whole layer forward (routing, both projections, the gated sum) as one
+// cooperative launch; ws: decode_fused_ws_bytes(c) bytes, 256-byte aligned;
+// status[2] must be zero at launch (launch_reset_status).
+cudaError_t launch_decode_fused(const moe_config& c, const void* x, const void* w_router,
+                                const float* logit_bias, const float* sel_bias,
+                                const void* w_gate, const void* w_up, const void* w_down,
+                                void* y, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                float* prob_sum, void* ws, int* status, cudaStream_t s);
+
 // ---- backward (bwd.cu, wgrad_sm103.cu, grouped_sm103.cu) -------------------
 // dL/dg of every pair (0 for a dropped one) and dO = g * dy per expert row
 // (dy for shared-expert rows), from the unweighted expert outputs o.
@@ -234,6 +252,7 @@ enum KernelId {
   K_BWD_DX,
   K_BWD_ROUTER,
   K_WGRAD,
+  K_DECODE_FUSED,
   K_NUM
 };
 void prof_begin(int id, cudaStream_t s);

@@ -39,6 +39,19 @@ SMALL = [
                    seed=28),
     synth.Workload("f32_capacity", T=100, d_model=48, n_experts=6, top_k=3, d_ff=64, n_shared=1,
                    dtype="f32", capacity_factor=0.6, seed=29),
+    # decode-sized batches: the whole layer in one cooperative kernel
+    synth.Workload("decode_fused_shared_renorm", T=5, d_model=256, n_experts=16, top_k=4,
+                   d_ff=256, n_shared=2, gate_mode=1, sel_bias=True, seed=30),
+    synth.Workload("decode_fused_capacity", T=8, d_model=512, n_experts=4, top_k=2, d_ff=512,
+                   capacity_factor=0.5, seed=31),
+    synth.Workload("decode_fused_32_experts_top8", T=8, d_model=256, n_experts=32, top_k=8,
+                   d_ff=256, seed=32),
+    synth.Workload("decode_fused_zipf_single_token", T=1, d_model=768, n_experts=8, top_k=2,
+                   d_ff=1280, zipf_s=1.2, seed=33),
+    synth.Workload("decode_fused_single_token_shared_renorm", T=1, d_model=512, n_experts=32,
+                   top_k=8, d_ff=768, n_shared=2, gate_mode=1, sel_bias=True, seed=34),
+    synth.Workload("decode_fused_single_token_capacity", T=1, d_model=256, n_experts=4, top_k=2,
+                   d_ff=512, capacity_factor=0.1, seed=35),
 ]
 
 
