@@ -69,6 +69,13 @@ def _declare(lib):
     lib.oracle_e4m3_encode_scan.restype = ctypes.c_uint8
     lib.oracle_e4m3_encode_scan.argtypes = [ctypes.c_float]
     lib.oracle_quantize_rows_e4m3.argtypes = [_I, _I, _I, _P, _P, _P]
+    lib.oracle_e2m1_decode.restype = ctypes.c_double
+    lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+    lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+    lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+    lib.oracle_e2m1_encode_scan.restype = ctypes.c_uint8
+    lib.oracle_e2m1_encode_scan.argtypes = [ctypes.c_float]
+    lib.oracle_quantize_rows_nvfp4.argtypes = [_I, _I, _I, _P, _P, _P, _P]
     lib.oracle_balance_loss.restype = ctypes.c_double
     lib.oracle_balance_loss.argtypes = [_I, _P, _P, ctypes.c_double]
     lib.oracle_balance_stats.restype = ctypes.c_double
@@ -238,14 +245,43 @@ class Oracle:
         self.lib.oracle_quantize_rows_e4m3(rows, cols, dt, _ptr(m), _ptr(q), _ptr(sc))
         return q, sc
 
+    def e2m1_decode(self, code):
+        return float(self.lib.oracle_e2m1_decode(int(code)))
+
+    def e2m1_encode(self, v, scan=False):
+        f = self.lib.oracle_e2m1_encode_scan if scan else self.lib.oracle_e2m1_encode
+        return int(f(float(v)))
+
+    def quantize_rows_nvfp4(self, m):
+        """(codes [rows, cols] uint8 (one E2M1 code per element), block scale
+        codes [rows, cols/16] uint8 (E4M3), row scales [rows] fp32) of a
+        stored matrix whose column count is a multiple of 16."""
+        dt, m = _stored(m)
+        rows, cols = m.shape
+        assert cols % 16 == 0
+        q = np.empty((rows, cols), np.uint8)
+        bs = np.empty((rows, cols // 16), np.uint8)
+        sc = np.empty(rows, np.float32)
+        self.lib.oracle_quantize_rows_nvfp4(rows, cols, dt, _ptr(m), _ptr(q), _ptr(bs), _ptr(sc))
+        return q, bs, sc
+
+    def nvfp4_values(self, q, bs, sc):
+        """fp64 values of an NVFP4 matrix (codes, block scales, row scales)."""
+        e2 = np.array([self.e2m1_decode(c) for c in range(16)])
+        e4 = np.array([self.e4m3_decode(c) for c in range(256)])
+        return e2[q] * np.repeat(e4[bs], 16, axis=1) * sc.astype(np.float64)[:, None]
+
     def layer_rows(self, x, experts, topk_idx, topk_w, rows, N, n_shared=0, keep=None,
-                   fp8=False):
+                   fp8=False, nvfp4=False):
         """y [len(rows), d] fp64 for the listed tokens. ``experts`` maps an
         expert index (0..N+n_shared-1; shared ones last) to its (wg, wu, wd)
         stored arrays; experts no listed token uses may be absent. ``keep``
         ([T*k] uint8, from capacity_keep) marks the pairs that run; a dropped
         pair adds nothing. ``fp8`` evaluates the experts in E4M3 with row
-        scales (tokens, weight output channels and H rows quantized)."""
+        scales (tokens, weight output channels and H rows quantized);
+        ``nvfp4`` in NVFP4 (E2M1 codes, E4M3 scales of 16-element blocks and
+        fp32 row scales, the same rows quantized)."""
+        assert not (fp8 and nvfp4)
         xd, x = _stored(x)
         T, d = x.shape
         topk_idx = _c(topk_idx, np.int32)
@@ -269,7 +305,7 @@ class Oracle:
         keep = None if keep is None else _c(keep, np.uint8)
         rc = self.lib.oracle_layer_rows(T, d, d_ff, N, k, n_shared, xd, _ptr(x), wdt,
                                         tabs[0], tabs[1], tabs[2], _ptr(topk_idx),
-                                        _ptr(topk_w), _ptr(keep), int(bool(fp8)), rows.size,
+                                        _ptr(topk_w), _ptr(keep), 2 if nvfp4 else int(bool(fp8)), rows.size,
                                         _ptr(rows), _ptr(y))
         if rc != 0:
             raise ValueError("oracle_layer_rows: a token needs an expert that was not supplied")
@@ -312,7 +348,8 @@ class Oracle:
 
     # ---- composition: the full layer for a token subset ---------------------
     def layer(self, x, w_router, wg, wu, wd, k, gate_mode=GATE_TOPK_SOFTMAX,
-              logit_bias=None, sel_bias=None, n_shared=0, rows=None, capacity=0, fp8=False):
+              logit_bias=None, sel_bias=None, n_shared=0, rows=None, capacity=0, fp8=False,
+              nvfp4=False):
         """Full forward: router scores for all tokens, routing for all tokens,
         expert outputs for ``rows`` (all tokens when None), with an expert
         capacity (0 = none). wg/wu/wd are the stacked [N+n_shared, ...]
@@ -328,7 +365,7 @@ class Oracle:
         rows = np.asarray(rows, np.int32)
         need = sorted(set(idx[rows].ravel().tolist()) | set(range(N, N + n_shared)))
         experts = {e: (wg[e], wu[e], wd[e]) for e in need}
-        y = self.layer_rows(x, experts, idx, w, rows, N, n_shared, keep, fp8)
+        y = self.layer_rows(x, experts, idx, w, rows, N, n_shared, keep, fp8, nvfp4)
         return dict(r32=r32, topk_idx=idx, topk_w=w, counts=counts,
                     prob_sum=prob_sum, keep=keep, y=y, rows=rows)
 

@@ -29,7 +29,7 @@
  *       each call": "The bare mechanism" (router, top-k, normalised weights,
  *       SwiGLU experts, shared experts, bias-adjusted routing); "The maths
  *       that matters" and "DeepEP, EPLB and Wide-EP" (experts stored and
- *       tokens dispatched in FP8).
+ *       tokens dispatched in FP8; NVFP4 experts in the GB200 deployment).
  *
  * Readings taken where the pages are silent or garbled:
  *  - The SwiGLU expert is down( SiLU(gate(x)) * up(x) ) without biases; the
@@ -158,6 +158,106 @@ void oracle_quantize_rows_e4m3(int rows, int cols, int dtype, const void* src, u
       q[(size_t)r * cols + c] = amax == 0.0f ? 0 : oracle_e4m3_encode(v * inv);
     }
   }
+}
+
+/* -------------------------------------------------------------- NVFP4 ----
+ * [P3] "The maths that matters" and "DeepEP, EPLB and Wide-EP": the GB200
+ * deployment keeps its experts in NVFP4. The pages name the format and no
+ * more; its definition: 4-bit E2M1 elements (sign, 2 exponent bits with
+ * bias 1, 1 mantissa bit; exponent field 0 holds the subnormal 0.5; the
+ * magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4 and 6; no infinity, no NaN) in
+ * blocks of 16 consecutive elements along the contraction, each block with
+ * an unsigned E4M3 scale.
+ * Reading (the pages give no scaling rule): as for the FP8 rows, each row
+ * also carries one fp32 scale, so that the block scales use E4M3's range.
+ * For a row with max |v| = amax > 0:
+ *   scale  = fp32(amax / 2688)                        (2688 = 6 * 448)
+ *   block  b = E4M3(fp32(bmax * fp32(448 / amax)))    (bmax: the block's max |v|)
+ *   code   q = E2M1(fp32(v * fp32(fp32(2688 / amax) / e4m3(b))))
+ * both roundings to nearest even and saturating (at 448 and at 6), the sign
+ * of v kept also when q rounds to zero; a block whose scale decodes to 0
+ * has codes 0, and a row of zeros has scale 0 and all codes 0. The value of
+ * an element is e2m1(q) * e4m3(b) * scale. */
+double oracle_e2m1_decode(uint8_t c) {
+  const int e = (c >> 1) & 3, m = c & 1;
+  const double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return (c & 8) ? -v : v;
+}
+
+/* Definition form: the code whose magnitude is nearest |v|, ties to the even
+ * code (mantissa bit clear); from 6 up, saturated to 6. */
+uint8_t oracle_e2m1_encode_scan(float v) {
+  const uint8_t sign = signbit(v) ? 8 : 0;
+  const double a = fabs((double)v);
+  if (a >= 6.0) return (uint8_t)(sign | 7);
+  int best = 0;
+  double bd = INFINITY;
+  for (int c = 0; c < 8; ++c) {
+    const double d = fabs(a - oracle_e2m1_decode((uint8_t)c));
+    if (d < bd || (d == bd && !(c & 1))) {
+      bd = d;
+      best = c;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+/* Direct form, the same function: the spacing of the magnitudes is 0.5
+ * below 2 (where the code is the step count itself), 1 from 2 to 4 and 2
+ * from 4 to 6; rint rounds the step count to nearest even, and codes past
+ * 7 saturate. */
+uint8_t oracle_e2m1_encode(float v) {
+  const uint8_t sign = signbit(v) ? 8 : 0;
+  const double a = fabs((double)v);
+  int c;
+  if (a < 2.0)
+    c = (int)rint(2.0 * a);
+  else if (a < 4.0)
+    c = 4 + (int)rint(a - 2.0);
+  else
+    c = a >= 6.0 ? 7 : 6 + (int)rint(0.5 * (a - 4.0));
+  return (uint8_t)(sign | c);
+}
+
+/* Row-wise NVFP4 quantization of a rows x cols matrix (cols a multiple of
+ * 16; see the NVFP4 note): q[r][c] one E2M1 code per element, bs[r][c/16]
+ * the E4M3 block scale codes, scale[r] the fp32 row scale. */
+void oracle_quantize_rows_nvfp4(int rows, int cols, int dtype, const void* src, uint8_t* q,
+                                uint8_t* bs, float* scale) {
+  const int nb = cols / 16;
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < rows; ++r) {
+    float amax = 0.0f;
+    for (int c = 0; c < cols; ++c) {
+      const float v = (float)widen(dtype, src, (size_t)r * cols + c);
+      if (fabsf(v) > amax) amax = fabsf(v);
+    }
+    scale[r] = amax / 2688.0f;
+    const float to_block = amax > 0.0f ? 448.0f / amax : 0.0f;
+    const float to_code = amax > 0.0f ? 2688.0f / amax : 0.0f;
+    for (int b = 0; b < nb; ++b) {
+      float bmax = 0.0f;
+      for (int i = 0; i < 16; ++i) {
+        const float v = (float)widen(dtype, src, (size_t)r * cols + 16 * b + i);
+        if (fabsf(v) > bmax) bmax = fabsf(v);
+      }
+      const uint8_t code = amax > 0.0f ? oracle_e4m3_encode(bmax * to_block) : 0;
+      bs[(size_t)r * nb + b] = code;
+      const float bv = (float)oracle_e4m3_decode(code);
+      const float inv = bv > 0.0f ? to_code / bv : 0.0f;
+      for (int i = 0; i < 16; ++i) {
+        const float v = (float)widen(dtype, src, (size_t)r * cols + 16 * b + i);
+        q[(size_t)r * cols + 16 * b + i] = bv > 0.0f ? oracle_e2m1_encode(v * inv) : 0;
+      }
+    }
+  }
+}
+
+/* Value of element (r, c) of an NVFP4 matrix with cols columns. */
+static double nvfp4_value(const uint8_t* q, const uint8_t* bs, const float* scale, int cols,
+                          size_t r, int c) {
+  return oracle_e2m1_decode(q[r * cols + c]) * oracle_e4m3_decode(bs[r * (cols / 16) + c / 16]) *
+         (double)scale[r];
 }
 
 int oracle_num_threads(void) {
@@ -385,6 +485,44 @@ static void expert_swiglu_fp8(int d, int d_ff, const QExpert* q, const double* x
   free(h);
 }
 
+/* An expert's three weight matrices in NVFP4: codes, block scales and row
+ * scales of each. */
+typedef struct {
+  uint8_t *gq, *uq, *dq, *gb, *ub, *db;
+  float *gs, *us, *ds;
+} Q4Expert;
+
+/* One SwiGLU expert on one token row in NVFP4 (see the NVFP4 note): x is
+ * the token's dequantized row, every weight is its NVFP4 value, H is rounded
+ * to bf16, quantized as one NVFP4 row and taken at its NVFP4 value by the
+ * down projection. */
+static void expert_swiglu_nvfp4(int d, int d_ff, const Q4Expert* q, const double* x,
+                                double* out) {
+  float* h = (float*)malloc(sizeof(float) * (size_t)d_ff);
+  for (int j = 0; j < d_ff; ++j) {
+    double a = 0.0, b = 0.0;
+    for (int i = 0; i < d; ++i) {
+      a += nvfp4_value(q->gq, q->gb, q->gs, d, (size_t)j, i) * x[i];
+      b += nvfp4_value(q->uq, q->ub, q->us, d, (size_t)j, i) * x[i];
+    }
+    h[j] = round_bf16((float)(silu(a) * b));
+  }
+  uint8_t* hq = (uint8_t*)malloc((size_t)d_ff);
+  uint8_t* hb = (uint8_t*)malloc((size_t)d_ff / 16);
+  float hs;
+  oracle_quantize_rows_nvfp4(1, d_ff, ORACLE_F32, h, hq, hb, &hs);
+  for (int c = 0; c < d; ++c) {
+    double acc = 0.0;
+    for (int j = 0; j < d_ff; ++j)
+      acc += nvfp4_value(q->dq, q->db, q->ds, d_ff, (size_t)c, j) *
+             nvfp4_value(hq, hb, &hs, d_ff, 0, j);
+    out[c] = acc;
+  }
+  free(hb);
+  free(hq);
+  free(h);
+}
+
 /* One SwiGLU expert on one token row x[d] (fp64):
  *   out[c] = sum_j Wd[c][j] * SiLU(sum_i Wg[j][i] x[i]) * (sum_i Wu[j][i] x[i])
  * Wg and Wu are stored [d_ff][d], Wd is stored [d][d_ff] (linear-layer
@@ -435,7 +573,7 @@ int oracle_layer_rows(int T, int d, int d_ff, int N, int k, int n_shared,
                       int xdtype, const void* x, int wdtype,
                       const void* const* wg, const void* const* wu,
                       const void* const* wd, const int32_t* topk_idx,
-                      const double* topk_w, const uint8_t* keep, int fp8, int n_rows,
+                      const double* topk_w, const uint8_t* keep, int quant, int n_rows,
                       const int32_t* rows, double* y) {
   int bad = 0;
   for (int r = 0; r < n_rows; ++r) {
@@ -451,9 +589,31 @@ int oracle_layer_rows(int T, int d, int d_ff, int N, int k, int n_shared,
     if (!wg[N + s] || !wu[N + s] || !wd[N + s]) bad = 1;
   if (bad) return -1;
 
-  /* FP8: quantize every supplied expert's weights once, row by row. */
+  /* quant = 1 (FP8) or 2 (NVFP4): quantize every supplied expert's weights
+   * once, row by row. */
+  const int fp8 = quant == 1, fp4 = quant == 2;
   const int E_all = N + n_shared;
   QExpert* qe = NULL;
+  Q4Expert* q4 = NULL;
+  if (fp4) {
+    q4 = (Q4Expert*)calloc((size_t)E_all, sizeof(Q4Expert));
+    for (int e = 0; e < E_all; ++e) {
+      if (!wg[e] || !wu[e] || !wd[e]) continue;
+      const size_t n = (size_t)d_ff * d;
+      q4[e].gq = (uint8_t*)malloc(n);
+      q4[e].uq = (uint8_t*)malloc(n);
+      q4[e].dq = (uint8_t*)malloc(n);
+      q4[e].gb = (uint8_t*)malloc(n / 16);
+      q4[e].ub = (uint8_t*)malloc(n / 16);
+      q4[e].db = (uint8_t*)malloc(n / 16);
+      q4[e].gs = (float*)malloc(sizeof(float) * (size_t)d_ff);
+      q4[e].us = (float*)malloc(sizeof(float) * (size_t)d_ff);
+      q4[e].ds = (float*)malloc(sizeof(float) * (size_t)d);
+      oracle_quantize_rows_nvfp4(d_ff, d, wdtype, wg[e], q4[e].gq, q4[e].gb, q4[e].gs);
+      oracle_quantize_rows_nvfp4(d_ff, d, wdtype, wu[e], q4[e].uq, q4[e].ub, q4[e].us);
+      oracle_quantize_rows_nvfp4(d, d_ff, wdtype, wd[e], q4[e].dq, q4[e].db, q4[e].ds);
+    }
+  }
   if (fp8) {
     qe = (QExpert*)calloc((size_t)E_all, sizeof(QExpert));
     for (int e = 0; e < E_all; ++e) {
@@ -486,6 +646,14 @@ int oracle_layer_rows(int T, int d, int d_ff, int N, int k, int n_shared,
       oracle_quantize_rows_e4m3(1, d, xdtype, (const char*)x + (size_t)t * d * (xdtype == ORACLE_BF16 ? 2 : xdtype == ORACLE_F32 ? 4 : 8), xq, &xs);
       for (int i = 0; i < d; ++i) xt[i] = oracle_e4m3_decode(xq[i]) * (double)xs;
       free(xq);
+    } else if (fp4) {  /* the token's row as one NVFP4 row */
+      uint8_t* xq = (uint8_t*)malloc((size_t)d);
+      uint8_t* xb = (uint8_t*)malloc((size_t)d / 16);
+      float xs;
+      oracle_quantize_rows_nvfp4(1, d, xdtype, (const char*)x + (size_t)t * d * (xdtype == ORACLE_BF16 ? 2 : xdtype == ORACLE_F32 ? 4 : 8), xq, xb, &xs);
+      for (int i = 0; i < d; ++i) xt[i] = nvfp4_value(xq, xb, &xs, d, 0, i);
+      free(xb);
+      free(xq);
     } else {
       for (int i = 0; i < d; ++i) xt[i] = widen(xdtype, x, (size_t)t * d + i);
     }
@@ -503,6 +671,8 @@ int oracle_layer_rows(int T, int d, int d_ff, int N, int k, int n_shared,
       for (int c = 0; c < d; ++c) E[(size_t)q * d + c] = 0.0;
     } else if (fp8) {
       expert_swiglu_fp8(d, d_ff, &qe[e], xt, E + (size_t)q * d);
+    } else if (fp4) {
+      expert_swiglu_nvfp4(d, d_ff, &q4[e], xt, E + (size_t)q * d);
     } else {
       oracle_expert_swiglu(d, d_ff, wdtype, wg[e], wu[e], wd[e], xt, E + (size_t)q * d);
     }
@@ -519,6 +689,14 @@ int oracle_layer_rows(int T, int d, int d_ff, int N, int k, int n_shared,
       free(qe[e].gs); free(qe[e].us); free(qe[e].ds);
     }
     free(qe);
+  }
+  if (q4) {
+    for (int e = 0; e < E_all; ++e) {
+      free(q4[e].gq); free(q4[e].uq); free(q4[e].dq);
+      free(q4[e].gb); free(q4[e].ub); free(q4[e].db);
+      free(q4[e].gs); free(q4[e].us); free(q4[e].ds);
+    }
+    free(q4);
   }
   return 0;
 }

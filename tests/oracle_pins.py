@@ -532,6 +532,151 @@ def pin_fp8_weight_row_scaling_is_exact(o):
     assert np.abs(a["y"] - ref["y"]).max() <= 0.1 * np.abs(ref["y"]).max()
 
 
+# ----------------------------------------------------------------- NVFP4 ---
+def pin_e2m1_fixed_points(o):
+    """E2M1 from its definition (sign, 2 exponent bits with bias 1, 1
+    mantissa bit, exponent field 0 = the subnormal 0.5 * m): every code's
+    value as 2^(e-1) * (1 + m/2), and every code encodes back to itself."""
+    want = [0.0, 0.5] + [2.0 ** (e - 1) * (1 + m / 2) for e in (1, 2, 3) for m in (0, 1)]
+    assert want == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for c in range(8):
+        assert o.e2m1_decode(c) == want[c]
+        assert o.e2m1_decode(8 | c) == -want[c]
+        assert o.e2m1_encode(want[c]) == c and o.e2m1_encode(-want[c]) == (8 | c)
+
+
+def pin_e2m1_encoder_matches_definition(o):
+    """The direct encoder equals the definition form (nearest code, ties to
+    the even code, saturation at 6) on every value, every midpoint (the
+    ties), both signs and random values; a few ties by hand."""
+    vals = [o.e2m1_decode(c) for c in range(8)]
+    probes = vals + [(a + b) / 2 for a, b in zip(vals, vals[1:])]
+    probes += [5.9, 6.0, 6.5, 7.0, 100.0, 1e30, 0.1, 0.26, 0.24]
+    probes += _rng(21).uniform(0, 8, 3000).tolist()
+    for v in probes:
+        for sv in (v, -v):
+            assert o.e2m1_encode(sv) == o.e2m1_encode(sv, scan=True), sv
+    # ties: 0.25 -> 0 (code 0), 0.75 -> 1 (code 2), 1.25 -> 1 (code 2),
+    # 1.75 -> 2 (code 4), 2.5 -> 2 (code 4), 3.5 -> 4 (code 6), 5 -> 4 (code 6)
+    assert [o.e2m1_encode(v) for v in (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)] == \
+        [0, 2, 2, 4, 4, 6, 6]
+    assert o.e2m1_encode(-0.1) == 8  # rounds to zero, keeps the sign
+
+
+def pin_quantize_rows_nvfp4_hand_worked(o):
+    """Two blocks of 16. amax = 6: scale = fp32(6/2688) = fp32(1/448),
+    448/amax = 74.666664, 2688/amax = 448.
+    Block 0 [6, -3, 1.5, 0.75, 0 ...]: 6 * 74.666664 rounds to 448 in fp32,
+    block code 0x7E (448); element factor 448/448 = 1; codes 7 (6), 0xD
+    (-3), 3 (1.5), 2 (0.75 ties to the even code, 1.0).
+    Block 1 [0.5, 0.25, -0.125, -0.01, 0 ...]: 0.5 * 74.666664 = 37.333332,
+    nearest E4M3 36 (code 0x61); factor fp32(448/36) = 12.444445; 0.5 ->
+    6.22 saturates to 6 (7), 0.25 -> 3.11 -> 3 (5), -0.125 -> -1.56 -> -1.5
+    (0xB), -0.01 -> -0.124 -> -0 (8)."""
+    row = np.zeros((1, 32), np.float32)
+    row[0, :4] = [6, -3, 1.5, 0.75]
+    row[0, 16:20] = [0.5, 0.25, -0.125, -0.01]
+    q, bs, sc = o.quantize_rows_nvfp4(row)
+    assert sc.tolist() == [np.float32(6) / np.float32(2688)]
+    assert bs.tolist() == [[0x7E, 0x61]]
+    assert q[0, :4].tolist() == [7, 0xD, 3, 2] and q[0, 16:20].tolist() == [7, 5, 0xB, 8]
+    assert not q[0, 4:16].any() and not q[0, 20:].any()
+    q0, bs0, sc0 = o.quantize_rows_nvfp4(np.zeros((1, 16), np.float32))
+    assert sc0.tolist() == [0.0] and not bs0.any() and not q0.any()
+
+
+def pin_nvfp4_error_bounds(o):
+    """On random rows of mixed magnitude, from the format's definition: the
+    row scale is amax/2688; each block scale is the nearest E4M3 value to
+    bmax / (6 * scale) (so within 2^-4 relative, or half a subnormal step);
+    each element is within half an E2M1 spacing of v / (block * scale), or
+    saturated at 6 when past it."""
+    rng = _rng(22)
+    m = rng.normal(0, 1, (40, 128)) * 2.0 ** rng.integers(-12, 12, (40, 1))
+    m *= 2.0 ** rng.integers(-6, 1, (40, 8)).repeat(16, axis=1)  # blocks well below amax
+    m[3, 16:32] = 0.0
+    m = m.astype(np.float32)
+    q, bs, sc = o.quantize_rows_nvfp4(m)
+    e4 = np.array([o.e4m3_decode(c) for c in range(256)])
+    e2 = np.array([o.e2m1_decode(c) for c in range(16)])
+    for r in range(m.shape[0]):
+        amax = np.abs(m[r]).max().astype(np.float64)
+        assert abs(sc[r] - amax / 2688) <= 2.0 ** -23 * amax / 2688
+        for b in range(8):
+            blk = m[r, 16 * b:16 * b + 16].astype(np.float64)
+            bmax = np.abs(blk).max()
+            want = bmax / (6 * float(sc[r]))
+            bv = e4[bs[r, b]]
+            assert abs(bv - want) <= max(2.0 ** -4 * want, 2.0 ** -10) * (1 + 1e-5), (r, b)
+            if bv == 0:
+                assert not (q[r, 16 * b:16 * b + 16] & 7).any()
+                continue
+            u = np.abs(blk) / (bv * float(sc[r]))
+            got = np.abs(e2[q[r, 16 * b:16 * b + 16]])
+            spacing = np.where(u < 2, 0.5, np.where(u < 4, 1.0, 2.0))
+            ok = (np.abs(got - u) <= spacing / 2 * (1 + 1e-5)) | ((u > 6) & (got == 6))
+            assert ok.all(), (r, b)
+            nz = blk != 0
+            assert (np.signbit(e2[q[r, 16 * b:16 * b + 16]][nz]) == np.signbit(blk[nz])).all()
+
+
+def pin_nvfp4_layer_hand_worked(o):
+    """One expert, d = d_ff = 16 (one block each), x = [6, 2.5, 0 ...],
+    W_g rows [0.5, 0 ...], [0, 1, 0 ...], W_u rows [1, 0 ...], [0, 1.5, 0 ...],
+    W_d row 0 = [1, 1, 0 ...], all other entries 0.
+    x: amax 6, block code 448, element factor fp32(448/448) = 1, so 6 -> 6
+    (code 7) and 2.5 ties to 2 (code 4): x becomes [6, 2] times 448 *
+    fp32(6/2688) / 1 = 1 + tiny. A weight row with one nonzero v quantizes to
+    6 * 448 * fp32(v/2688) = v (1 + tiny). a = [3, 2], b = [6, 3], H =
+    SiLU(a) * b = [17.14634, 5.28478] -> bf16 [17.125, 5.28125]. The H row:
+    scale fp32(17.125/2688), block code 448, element factor fp32(fp32(2688 /
+    17.125) / 448) = 0.35036495: 17.125 -> 6 (code 7), 5.28125 -> 1.850 -> 2
+    (code 4), so H becomes [6, 2] * 448 * fp32(17.125/2688). y0 =
+    22.8333334407 (without the H quantization about 22.41; with x unquantized
+    a1 = 2.5 and y0 about 25.7); every other output is 0."""
+    x = np.zeros((1, 16), np.float32)
+    x[0, :2] = [6.0, 2.5]
+    Wr = np.ones((1, 16), np.float32)
+    wg = np.zeros((1, 16, 16), np.float32)
+    wu = np.zeros((1, 16, 16), np.float32)
+    wd = np.zeros((1, 16, 16), np.float32)
+    wg[0, 0, 0], wg[0, 1, 1] = 0.5, 1.0
+    wu[0, 0, 0], wu[0, 1, 1] = 1.0, 1.5
+    wd[0, 0, :2] = 1.0
+    out = o.layer(x, Wr, wg, wu, wd, 1, nvfp4=True)
+    assert abs(out["y"][0, 0] - 22.833333440745864) < 1e-9, out["y"]
+    assert not out["y"][0, 1:].any()
+
+
+def pin_nvfp4_power_of_two_scaling_is_exact(o):
+    """Scaling a row by 2^j leaves its codes and block codes unchanged and
+    multiplies its scale by exactly 2^j; in the layer, scaling one W_d row
+    scales that output column exactly and leaves the others; and NVFP4 stays
+    within a loose bound of the exact layer."""
+    rng = _rng(23)
+    m = rng.normal(0, 1, (6, 64)).astype(np.float32)
+    q, bs, sc = o.quantize_rows_nvfp4(m)
+    q2, bs2, sc2 = o.quantize_rows_nvfp4(m * np.float32(2.0 ** -7))
+    assert np.array_equal(q, q2) and np.array_equal(bs, bs2)
+    assert np.array_equal(sc2, sc * np.float32(2.0 ** -7))
+    T, d, dff, N, k = 5, 32, 16, 3, 2
+    x = rng.normal(0, 1, (T, d)).astype(np.float32)
+    Wr = rng.normal(0, 1, (N, d)).astype(np.float32)
+    wg = rng.normal(0, 0.3, (N, dff, d)).astype(np.float32)
+    wu = rng.normal(0, 0.3, (N, dff, d)).astype(np.float32)
+    wd = rng.normal(0, 0.3, (N, d, dff)).astype(np.float32)
+    a = o.layer(x, Wr, wg, wu, wd, k, nvfp4=True)
+    wd2 = wd.copy()
+    wd2[:, 5, :] *= 16.0
+    b = o.layer(x, Wr, wg, wu, wd2, k, nvfp4=True)
+    assert np.array_equal(b["y"][:, 5], 16.0 * a["y"][:, 5])
+    other = [c for c in range(d) if c != 5]
+    assert np.array_equal(b["y"][:, other], a["y"][:, other])
+    ref = o.layer(x, Wr, wg, wu, wd, k)
+    assert np.abs(a["y"] - ref["y"]).max() <= 0.35 * np.abs(ref["y"]).max()
+    assert np.abs(a["y"] - ref["y"]).max() > 0  # and it is not the exact layer
+
+
 # -------------------------------------------------------------- backward ---
 def _bwd_case(seed, T=5, d=6, N=4, k=2, dff=7, S=1):
     rng = _rng(seed)

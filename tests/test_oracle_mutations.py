@@ -43,6 +43,17 @@ MUTATIONS = [
     ("fp8_scale_over_240", "const float s = amax / 448.0f;", "const float s = amax / 240.0f;"),
     ("fp8_codes_over_240", "const float inv = amax > 0.0f ? 448.0f / amax : 0.0f;", "const float inv = amax > 0.0f ? 240.0f / amax : 0.0f;"),
     ("fp8_h_not_quantized", "(oracle_e4m3_decode(hq[j]) * (double)hs);", "(double)h[j];"),
+    ("e2m1_exponent_bias", "ldexp(1.0 + 0.5 * m, e - 1);", "ldexp(1.0 + 0.5 * m, e - 2);"),
+    ("e2m1_ties_away_from_even", "if (d < bd || (d == bd && !(c & 1))) {", "if (d <= bd) {"),
+    ("e2m1_direct_no_saturation", "c = a >= 6.0 ? 7 : 6 + (int)rint(0.5 * (a - 4.0));", "c = 6 + (int)rint(0.5 * (a - 4.0));"),
+    ("e2m1_direct_truncates", "c = 4 + (int)rint(a - 2.0);", "c = 4 + (int)floor(a - 2.0);"),
+    ("nvfp4_block_scale_from_row_amax", "oracle_e4m3_encode(bmax * to_block) : 0;", "oracle_e4m3_encode(amax * to_block) : 0;"),
+    ("nvfp4_row_scale_over_448", "scale[r] = amax / 2688.0f;", "scale[r] = amax / 448.0f;"),
+    ("nvfp4_codes_over_448", "const float to_code = amax > 0.0f ? 2688.0f / amax : 0.0f;", "const float to_code = amax > 0.0f ? 448.0f / amax : 0.0f;"),
+    ("nvfp4_value_without_block_scale", "return oracle_e2m1_decode(q[r * cols + c]) * oracle_e4m3_decode(bs[r * (cols / 16) + c / 16]) *", "return oracle_e2m1_decode(q[r * cols + c]) *"),
+    ("nvfp4_h_not_quantized", "             nvfp4_value(hq, hb, &hs, d_ff, 0, j);", "             (double)h[j];"),
+    ("nvfp4_token_not_quantized", "for (int i = 0; i < d; ++i) xt[i] = nvfp4_value(xq, xb, &xs, d, 0, i);", "for (int i = 0; i < d; ++i) xt[i] = widen(xdtype, x, (size_t)t * d + i);"),
+    ("nvfp4_sign_dropped", "const uint8_t sign = signbit(v) ? 8 : 0;\n  const double a = fabs((double)v);\n  int c;", "const uint8_t sign = 0;\n  const double a = fabs((double)v);\n  int c;"),
     ("fp8_wrong_weight_row_scale", "out[c] = acc * (double)q->ds[c];", "out[c] = acc * (double)q->ds[d - 1 - c];"),
     ("selection_ignores_bias", "key[e] = sel_bias ? (float)((double)rt[e] + (double)sel_bias[e]) : rt[e];", "key[e] = rt[e];"),
     ("bwd_silu_grad_missing_term", "return s * (1.0 + z * (1.0 - s));", "return s;"),
