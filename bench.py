@@ -32,6 +32,8 @@ METRIC = "MoE layer tokens/s; grouped-GEMM % bf16 tensor peak; decode % HBM BW"
 # fp32 FMA peak from unit counts and the maximum clock: 152 SMs x 128 lanes x 2 flop x 2.07 GHz
 FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 UNIT = "tokens/s"
+# Nominal dense tensor rates relative to bf16 (2.25 PFLOP/s): fp8 4.5, fp4 13.5.
+QUANT_PEAK_RATIO = {None: 1.0, "fp8": 4.5 / 2.25, "nvfp4": 13.5 / 2.25}
 
 
 # ----------------------------------------------------------------- helpers --
@@ -66,12 +68,14 @@ def reduce_max(v: float, ws: int) -> float:
     return float(t.item())
 
 
-def recorded_traffic(fp8=False):
-    """DRAM bytes per gate/up launch from the committed ncu summary (bf16 or
-    E4M3 kernel), or None when the kernel sources changed since that capture."""
+def recorded_traffic(quant=None):
+    """DRAM bytes per gate/up launch from the committed ncu summary (bf16,
+    E4M3 or NVFP4 kernel), or None when the kernel sources changed since that
+    capture."""
     import hashlib
-    prof = os.path.join(ROOT, "profiles", "grouped_gemm_fp8_mixtral_8x7b_prefill.md" if fp8
-                        else "grouped_gemm_mixtral_8x7b_prefill.md")
+    prof = os.path.join(ROOT, "profiles", {None: "grouped_gemm_mixtral_8x7b_prefill.md",
+                                           "fp8": "grouped_gemm_fp8_mixtral_8x7b_prefill.md",
+                                           "nvfp4": "grouped_gemm_nvfp4_mixtral_8x7b_prefill.md"}[quant])
     csrc = os.path.join(ROOT, "sparse_mixture_experts_router_gb300", "csrc")
     try:
         text = open(prof).read()
@@ -191,11 +195,21 @@ def gemm_flops(w, counts=None):
     return 4.0 * rows * w.d_model * w.d_ff, 2.0 * rows * w.d_ff * w.d_model
 
 
-def touched_weight_bytes(w, counts, fp8=False):
+def nvfp4_scale_stride(cols):
+    """Bytes of one row of NVFP4 block scales (cols / 16 rounded up to 16)."""
+    return (cols // 16 + 15) // 16 * 16
+
+
+def touched_weight_bytes(w, counts, quant=None):
     """Expert weight bytes a forward must read: every expert with a row (E4M3:
-    one byte a weight plus an fp32 scale per output channel)."""
-    if fp8:
+    one byte a weight plus an fp32 scale per output channel; NVFP4: half a
+    byte a weight, one E4M3 block scale per 16 weights and an fp32 scale per
+    output channel)."""
+    if quant == "fp8":
         per = 3 * w.d_model * w.d_ff + 4 * (2 * w.d_ff + w.d_model)
+    elif quant == "nvfp4":
+        per = (3 * w.d_model * w.d_ff // 2 + 2 * w.d_ff * nvfp4_scale_stride(w.d_model)
+               + w.d_model * nvfp4_scale_stride(w.d_ff) + 4 * (2 * w.d_ff + w.d_model))
     else:
         per = 3 * w.d_model * w.d_ff * (2 if w.dtype == "bf16" else 4)
     active = sum(1 for c in counts if c > 0) + w.n_shared
@@ -203,31 +217,46 @@ def touched_weight_bytes(w, counts, fp8=False):
 
 
 class Forward:
-    """One layer forward through the C ABI: moe_layer_forward, or with
-    --fp8 moe_layer_forward_fp8 on weights quantized once by moe_quantize_fp8."""
+    """One layer forward through the C ABI: moe_layer_forward, or with --fp8
+    moe_layer_forward_fp8 on weights quantized once by moe_quantize_fp8, or
+    with --nvfp4 moe_layer_forward_nvfp4 on weights quantized once by
+    moe_quantize_nvfp4."""
 
-    def __init__(self, moe, cfg, inp, fp8, dev, q=None):
+    def __init__(self, moe, cfg, inp, quant, dev, q=None):
         import torch
-        self.moe, self.cfg, self.inp, self.fp8 = moe, cfg, inp, fp8
-        self.ws = moe.workspace(cfg, "layer_fp8" if fp8 else "layer", dev)
+        self.moe, self.cfg, self.inp, self.quant = moe, cfg, inp, quant
+        self.ws = moe.workspace(cfg, {None: "layer", "fp8": "layer_fp8",
+                                      "nvfp4": "layer_nvfp4"}[quant], dev)
         self.q = q if q is not None else []
-        if fp8 and not self.q:
+        if quant and not self.q:
             for n in ("w_gate", "w_up", "w_down"):
                 t = inp[n]
                 rows, cols = t.shape[0] * t.shape[1], t.shape[2]
-                q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
                 sc = torch.empty(rows, dtype=torch.float32, device=dev)
-                moe.moe_quantize_fp8(t.reshape(rows, cols), q, sc)
-                self.q.append((q, sc))
+                if quant == "fp8":
+                    q = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+                    moe.moe_quantize_fp8(t.reshape(rows, cols), q, sc)
+                    self.q.append((q, sc))
+                else:
+                    q = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+                    sf = torch.empty((rows, nvfp4_scale_stride(cols)), dtype=torch.uint8,
+                                     device=dev)
+                    moe.moe_quantize_nvfp4(t.reshape(rows, cols), q, sf, sc)
+                    self.q.append((q, sf, sc))
             torch.cuda.synchronize(dev)
 
     def __call__(self, x, y, idx, tw, counts, ps, stream):
         i = self.inp
-        if self.fp8:
+        if self.quant == "fp8":
             (gq, gs), (uq, us), (dq, ds) = self.q
             self.moe.moe_layer_forward_fp8(self.cfg, x, i["w_router"], i["logit_bias"],
                                            i["sel_bias"], gq, gs, uq, us, dq, ds, y, idx, tw,
                                            counts, ps, self.ws, stream)
+        elif self.quant == "nvfp4":
+            (gq, gf, gs), (uq, uf, us), (dq, df, ds) = self.q
+            self.moe.moe_layer_forward_nvfp4(self.cfg, x, i["w_router"], i["logit_bias"],
+                                             i["sel_bias"], gq, gf, gs, uq, uf, us, dq, df, ds,
+                                             y, idx, tw, counts, ps, self.ws, stream)
         else:
             self.moe.moe_layer_forward(self.cfg, x, i["w_router"], i["logit_bias"], i["sel_bias"],
                                        i["w_gate"], i["w_up"], i["w_down"], y, idx, tw, counts,
@@ -256,7 +285,7 @@ def run_ours(args):
     tw = torch.empty(w.T, w.top_k, dtype=torch.float32, device=dev)
     counts = torch.empty(w.n_experts, dtype=torch.int32, device=dev)
     ps = torch.empty(w.n_experts, dtype=torch.float32, device=dev)
-    fwd = Forward(moe, cfg, inp, args.fp8, dev)
+    fwd = Forward(moe, cfg, inp, args.quant, dev)
     wsp = fwd.ws
     stream = torch.cuda.current_stream(dev)
 
@@ -363,13 +392,15 @@ def run_ours(args):
         per_kernel[name] = {"ms_per_launch": ms / n, "launches": n,
                             "share": ms / sum(v[0] for v in kern.values())}
     # the dominant kernel's duration comes from the timed region itself
-    # E4M3: the measured bf16 peaks times the nominal fp8/bf16 ratio (4.5 / 2.25)
-    tpk = pk["bf16"] * (2.0 if args.fp8 else 1.0)
-    tpk_s = pk["bf16_sustained"] * (2.0 if args.fp8 else 1.0)
+    # E4M3 / NVFP4: the measured bf16 peaks times the nominal dense ratio of
+    # the operand type to bf16 (4.5 / 2.25 for fp8, 13.5 / 2.25 for fp4)
+    ratio = QUANT_PEAK_RATIO[args.quant]
+    tpk = pk["bf16"] * ratio
+    tpk_s = pk["bf16_sustained"] * ratio
     if "gate_up" not in kern_timed:  # a single token: the whole layer is one kernel
         fused_ms = kern_timed["decode_fused"][0] / kern_timed["decode_fused"][1]
         per_kernel["decode_fused"]["ms_per_launch"] = fused_ms
-        wbytes, _ = touched_weight_bytes(w, counts.cpu().tolist(), args.fp8)
+        wbytes, _ = touched_weight_bytes(w, counts.cpu().tolist(), args.quant)
         total = wbytes + w.n_experts * w.d_model * 2 + 2 * w.T * w.d_model * 2
         gbs = total / (fused_ms / 1e3) / 1e9
         per_kernel["decode_fused"]["gbs"] = round(gbs, 1)
@@ -393,9 +424,10 @@ def run_ours(args):
                     "achieved": round(ach, 1), "peak": round(tpk, 1), "unit": "TFLOP/s",
                     "frac": round(ach / tpk, 4),
                     "traffic": (args.traffic if args.traffic is not None
-                                else recorded_traffic(args.fp8)),
-                    "peak_source": (f"{pk['source']} bf16 burst x 2 (nominal fp8/bf16 ratio)"
-                                    if args.fp8 else f"{pk['source']} bf16 burst"),
+                                else recorded_traffic(args.quant)),
+                    "peak_source": (f"{pk['source']} bf16 burst x {ratio:g} (nominal "
+                                    f"{args.quant}/bf16 dense ratio)"
+                                    if args.quant else f"{pk['source']} bf16 burst"),
                     "frac_of_sustained": round(ach / tpk_s, 4),
                     "algorithmic_flops_per_launch": f_gu,
                     "grouped_gemm_both_kernels_tflops": round(gemm_tflops, 1),
@@ -422,9 +454,9 @@ def run_ours(args):
 
     decode = run_decode(moe, synth, dev, stream, pk, args) if default and not args.no_decode else None
     backward = (run_backward(moe, dev, stream, pk, w, inp, cfg, args)
-                if default and not args.fp8 and not args.no_backward else None)
+                if default and not args.quant and not args.no_backward else None)
     E = w.n_experts + w.n_shared
-    wb = 3 * E * w.d_model * w.d_ff * (1 if args.fp8 else 2)  # E4M3 codes: 1 byte each
+    wb = touched_weight_bytes(w, [1] * w.n_experts, args.quant)[0]
     routing = {"max_over_mean_expert_load": round(float(counts.max()) / max(1e-9, float(counts.float().mean())), 3),
                "experts_with_tokens": int((counts > 0).sum())}
     if capacity_of(w):
@@ -437,7 +469,9 @@ def run_ours(args):
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3 experts (row scales), bf16 tokens and router" if args.fp8 else "bf16",
+            "dtype": {None: "bf16", "fp8": "e4m3 experts (row scales), bf16 tokens and router",
+                      "nvfp4": "nvfp4 experts (e2m1, e4m3 scales of 16-element blocks, row "
+                               "scales), bf16 tokens and router"}[args.quant],
             "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) random-init weights)",
             "config": {"workload": w.name, "T": w.T, "d_model": w.d_model,
                        "n_experts": w.n_experts, "top_k": w.top_k, "d_ff": w.d_ff,
@@ -455,7 +489,7 @@ def run_ours(args):
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": bytes_io,
                     "d2h_bytes_per_step": bytes_io,
                     "path": "per step: pinned host x -> H2D (copy stream) -> moe_layer_forward"
-                            + ("_fp8 " if args.fp8 else " ") +
+                            + {None: " ", "fp8": "_fp8 ", "nvfp4": "_nvfp4 "}[args.quant] +
                             "(C ABI, compute stream) -> D2H y (copy stream) -> pinned host; "
                             "copies overlap neighbouring steps' forwards; host wall clock"},
             "gpu_launches": int(launches),
@@ -566,7 +600,7 @@ def run_decode(moe, synth, dev, stream, pk, args):
                          d_ff=w.d_ff, dtype=moe.MOE_BF16)
         y = torch.empty(w.T, w.d_model, dtype=torch.bfloat16, device=dev)
         counts = torch.empty(w.n_experts, dtype=torch.int32, device=dev)
-        fwd = Forward(moe, cfg, base, args.fp8, dev, qcache)
+        fwd = Forward(moe, cfg, base, args.quant, dev, qcache)
         qcache = fwd.q  # the expert weights are quantized once for all batch sizes
 
         def step(st=None):
@@ -613,7 +647,7 @@ def run_decode(moe, synth, dev, stream, pk, args):
             step()
         kern = moe.profile_collect()
         moe.profile_enable(False)
-        wbytes, active = touched_weight_bytes(w, counts.cpu().tolist(), args.fp8)
+        wbytes, active = touched_weight_bytes(w, counts.cpu().tolist(), args.quant)
         total = wbytes + w.n_experts * w.d_model * 2 + 2 * w.T * w.d_model * 2
         gbs = total / (ms / 1e3) / 1e9
         gbs_g = total / (ms_graph / 1e3) / 1e9
@@ -738,10 +772,16 @@ def main(argv=None):
                     help="with --backward-only: routed experts N instead of the workload's")
     ap.add_argument("--fp8", action="store_true",
                     help="E4M3 expert weights (moe_layer_forward_fp8); not the headline, which is bf16")
+    ap.add_argument("--nvfp4", action="store_true",
+                    help="NVFP4 expert weights (moe_layer_forward_nvfp4); not the headline, which "
+                         "is bf16")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per gate_up launch from an ncu capture of this build")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.fp8 and args.nvfp4:
+        ap.error("--fp8 and --nvfp4 exclude each other")
+    args.quant = "fp8" if args.fp8 else "nvfp4" if args.nvfp4 else None
     if args.impl == "reference":
         run_reference(args)
     elif args.backward_only:

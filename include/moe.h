@@ -328,6 +328,67 @@ MOE_API int moe_layer_forward_fp8(const moe_config* cfg, const void* x, const vo
                     moe_stream_t stream);
 
 /*
+ * NVFP4 experts. The GB200 deployment keeps its experts in NVFP4 ("MoE
+ * inference: the call centre with 256 specialists and 8 taking each call",
+ * "The maths that matters" and "DeepEP, EPLB and Wide-EP"); the pages name
+ * the format and no scaling rule. Format: E2M1 elements (magnitudes 0, 0.5,
+ * 1, 1.5, 2, 3, 4, 6) in blocks of 16 consecutive elements of a row, each
+ * block with an unsigned E4M3 scale, and, as the library's rule, one fp32
+ * scale per row. For a row with max |v| = amax > 0:
+ *   row scale  s = fp32(amax / 2688)                        (2688 = 6 * 448)
+ *   block      b = E4M3(fp32(bmax * fp32(448 / amax)))     (bmax: block max |v|)
+ *   element    q = E2M1(fp32(v * fp32(fp32(2688 / amax) / e4m3(b))))
+ * rounded to nearest even and saturated (448, 6), the sign kept when q
+ * rounds to zero; a block whose scale is 0 has codes 0; a zero row has s = 0.
+ * An element stands for e2m1(q) * e4m3(b) * s.
+ *
+ * Layout of a rows x cols NVFP4 matrix:
+ *   q     [rows][cols / 2] uint8: two codes a byte, the lower column in the
+ *         low nibble (sign in bit 3 of a nibble);
+ *   sf    [rows][moe_nvfp4_scale_stride(cols)] uint8: E4M3 block scales,
+ *         zero past cols / 16;
+ *   scale [rows] fp32.
+ *
+ * moe_nvfp4_scale_stride: bytes of one row of block scales, cols / 16
+ * rounded up to a multiple of 16 (0 for cols <= 0).
+ * moe_quantize_nvfp4: rows x cols bf16 [device] -> q, sf, scale [device].
+ * cols a multiple of 16; pointers 16-byte aligned. Quantize each weight
+ * tensor of moe_layer_forward_nvfp4 with it (rows = output channels: E*d_ff
+ * for gate and up, E*d_model for down). Returns MOE_ERR_INVALID_ARG for bad
+ * sizes or null pointers, MOE_ERR_MISALIGNED for unaligned ones.
+ */
+MOE_API int32_t moe_nvfp4_scale_stride(int32_t cols);
+MOE_API int moe_quantize_nvfp4(int64_t rows, int32_t cols, const void* src, uint8_t* q,
+                    uint8_t* sf, float* scale, moe_stream_t stream);
+
+/*
+ * moe_layer_forward with NVFP4 experts: routing as moe_layer_forward (bf16
+ * x and W_r; cfg->dtype must be MOE_BF16); every routed token row, x for the
+ * shared experts and each row of H are quantized as above (H stored in bf16
+ * first), and both expert projections run on the tensor cores as block-
+ * scaled E2M1 products (tcgen05.mma kind::mxf4nvf4, the block scales applied
+ * by the MMA, fp32 accumulation), the row scales applied in the GEMM
+ * epilogues. y is bf16.
+ *
+ *  wg_q, wu_q [device] [N+s][d_ff][d_model/2]; wg_sf, wu_sf [N+s][d_ff][stride(d_model)];
+ *  wg_scale, wu_scale [N+s][d_ff] fp32;
+ *  wd_q [device] [N+s][d_model][d_ff/2]; wd_sf [N+s][d_model][stride(d_ff)];
+ *  wd_scale [N+s][d_model] fp32.
+ *  Other arguments as moe_layer_forward; ws: moe_workspace_size_nvfp4(cfg)
+ *  bytes (0 when the shape is unsupported). d_model and d_ff must be
+ *  multiples of 64 and at least 256 (MOE_ERR_UNSUPPORTED otherwise).
+ */
+MOE_API size_t moe_workspace_size_nvfp4(const moe_config* cfg);
+MOE_API int moe_layer_forward_nvfp4(const moe_config* cfg, const void* x, const void* w_router,
+                    const float* logit_bias, const float* sel_bias,
+                    const uint8_t* wg_q, const uint8_t* wg_sf, const float* wg_scale,
+                    const uint8_t* wu_q, const uint8_t* wu_sf, const float* wu_scale,
+                    const uint8_t* wd_q, const uint8_t* wd_sf, const float* wd_scale,
+                    void* y, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                    float* prob_sum, void* ws, size_t ws_bytes,
+                    moe_stream_t stream);
+
+/*
  * The load-balance statistics on the device: f_i = counts_i / (T*k),
  * P_i = prob_sum_i / T and aux = alpha * N * sum_i f_i P_i (one fixed-order
  * sum). ("Mixture of experts and speculative decoding", "Keeping the

@@ -80,6 +80,10 @@ _SIGS = {
     "moe_quantize_fp8": (_I, [ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P]),
     "moe_workspace_size_fp8": (_SZ, [_CFG]),
     "moe_layer_forward_fp8": (_I, [_CFG] + [_P] * 15 + [_P, _SZ, _P]),
+    "moe_nvfp4_scale_stride": (ctypes.c_int32, [ctypes.c_int32]),
+    "moe_quantize_nvfp4": (_I, [ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P, _P]),
+    "moe_workspace_size_nvfp4": (_SZ, [_CFG]),
+    "moe_layer_forward_nvfp4": (_I, [_CFG] + [_P] * 18 + [_P, _SZ, _P]),
     "moe_balance_stats": (_I, [ctypes.c_int32] * 3 + [_P, _P, ctypes.c_float, _P, _P, _P, _P]),
     "moe_workspace_size_backward": (_SZ, [_CFG]),
     "moe_layer_backward": (_I, [_CFG] + [_P] * 8 + [ctypes.c_float, ctypes.c_float] + [_P] * 5
@@ -149,7 +153,7 @@ def check_config(cfg: moe_config) -> int:
 def workspace_size(cfg: moe_config, kind: str = "layer") -> int:
     fn = {"layer": "moe_workspace_size", "router": "moe_router_workspace_size",
           "permute": "moe_permute_workspace_size", "grouped": "moe_grouped_workspace_size",
-          "layer_fp8": "moe_workspace_size_fp8",
+          "layer_fp8": "moe_workspace_size_fp8", "layer_nvfp4": "moe_workspace_size_nvfp4",
           "backward": "moe_workspace_size_backward"}[kind]
     return int(getattr(lib(), fn)(ctypes.byref(cfg)))
 
@@ -213,6 +217,31 @@ def moe_layer_forward_fp8(cfg, x, w_router, logit_bias, sel_bias, wg_q, wg_scale
         _ptr(wg_q), _ptr(wg_scale), _ptr(wu_q), _ptr(wu_scale), _ptr(wd_q), _ptr(wd_scale),
         _ptr(y), _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(prob_sum), _ptr(ws),
         ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def moe_nvfp4_scale_stride(cols):
+    """Bytes of one row of NVFP4 block scales for rows of `cols` elements."""
+    return int(lib().moe_nvfp4_scale_stride(int(cols)))
+
+
+def moe_quantize_nvfp4(src, q, sf, scale, stream=None):
+    """Row-wise NVFP4 of a [rows, cols] bf16 tensor: packed E2M1 codes
+    [rows, cols/2], E4M3 block scales [rows, moe_nvfp4_scale_stride(cols)] and
+    fp32 row scales [rows]."""
+    rows, cols = src.shape[0], src.numel() // max(1, src.shape[0])
+    _check("moe_quantize_nvfp4", lib().moe_quantize_nvfp4(rows, cols, _ptr(src), _ptr(q), _ptr(sf),
+                                                          _ptr(scale), _stream(stream)))
+
+
+def moe_layer_forward_nvfp4(cfg, x, w_router, logit_bias, sel_bias, wg_q, wg_sf, wg_scale, wu_q,
+                            wu_sf, wu_scale, wd_q, wd_sf, wd_scale, y, topk_idx, topk_w, counts,
+                            prob_sum, ws, stream=None):
+    _check("moe_layer_forward_nvfp4", lib().moe_layer_forward_nvfp4(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(sel_bias),
+        _ptr(wg_q), _ptr(wg_sf), _ptr(wg_scale), _ptr(wu_q), _ptr(wu_sf), _ptr(wu_scale),
+        _ptr(wd_q), _ptr(wd_sf), _ptr(wd_scale), _ptr(y), _ptr(topk_idx), _ptr(topk_w),
+        _ptr(counts), _ptr(prob_sum), _ptr(ws), ws.numel() if ws is not None else 0,
+        _stream(stream)))
 
 
 def moe_layer_forward(cfg, x, w_router, logit_bias, sel_bias, w_gate, w_up, w_down, y, topk_idx,

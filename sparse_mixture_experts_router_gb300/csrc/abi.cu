@@ -147,6 +147,41 @@ LayerFp8Ws carve_layer_fp8(Carver& cv, const moe_config& c) {
   return w;
 }
 
+// The NVFP4 layer: the bf16 layer's routing and output buffers, NVFP4 copies
+// (codes, block scales, row scales) of the routed rows and of x (shared
+// experts), H in bf16 with its rows' max |H|, and H in NVFP4.
+struct LayerNvf4Ws {
+  LayerWs base;  // x_perm unused
+  uint8_t *xq_perm, *xp_sf;
+  float* xp_scale;
+  uint8_t *xq, *x_sf;
+  float* x_scale;
+  unsigned* h_amax;
+  uint8_t *hq, *h_sf;
+  float* h_scale;
+};
+LayerNvf4Ws carve_layer_nvf4(Carver& cv, const moe_config& c) {
+  LayerNvf4Ws w;
+  moe_config b = c;
+  b.dtype = MOE_BF16;
+  w.base = carve_layer(cv, b);
+  const size_t P = (size_t)pairs(c), R = (size_t)rows_total(c);
+  const size_t Pp = (size_t)padded_rows((long long)P), Tp = (size_t)padded_rows(c.T),
+               Rp = (size_t)padded_rows((long long)R);
+  const size_t sfd = (size_t)nvf4_sf_stride(c.d_model), sff = (size_t)nvf4_sf_stride(c.d_ff);
+  w.xq_perm = cv.take<uint8_t>(Pp * c.d_model / 2);
+  w.xp_sf = cv.take<uint8_t>(Pp * sfd);
+  w.xp_scale = cv.take<float>(sizeof(float) * P);
+  w.xq = cv.take<uint8_t>(Tp * c.d_model / 2);
+  w.x_sf = cv.take<uint8_t>(Tp * sfd);
+  w.x_scale = cv.take<float>(sizeof(float) * (size_t)c.T);
+  w.h_amax = cv.take<unsigned>(sizeof(unsigned) * R);
+  w.hq = cv.take<uint8_t>(Rp * c.d_ff / 2);
+  w.h_sf = cv.take<uint8_t>(Rp * sff);
+  w.h_scale = cv.take<float>(sizeof(float) * R);
+  return w;
+}
+
 int check_ws(const moe_config& c, void* ws, size_t ws_bytes, size_t need) {
   (void)c;
   if (!ws) return MOE_ERR_INVALID_ARG;
@@ -686,6 +721,121 @@ int moe_layer_forward_fp8(const moe_config* cfg, const void* x, const void* w_ro
     e = launch_grouped_e4m3(c, w8.xq_perm, w8.xp_scale, w8.xq, w8.x_scale, w.seg, w.sorted_pair, tw,
                             wg_q, wg_scale, wu_q, wu_scale, wd_q, wd_scale, w.h, w8.h_amax, w8.hq,
                             w8.h_scale, w.y_perm, w.partial, padded_rows(P),
+                            padded_rows(rows_total(c)), w.status, s);
+  if (e == cudaSuccess) e = launch_combine(c, w.y_perm, w.inv_pos, nullptr, y, s);
+  return e == cudaSuccess ? MOE_OK : fail_cuda(e);
+}
+
+int32_t moe_nvfp4_scale_stride(int32_t cols) { return cols > 0 ? nvf4_sf_stride(cols) : 0; }
+
+namespace {
+// NVFP4 expert GEMMs read each operand row in 128-byte TMA boxes of codes
+// (256 elements) and step K by 64 per MMA.
+bool nvf4_shape_ok(const moe_config& c) {
+  return c.d_model % 64 == 0 && c.d_ff % 64 == 0 && c.d_model >= 256 && c.d_ff >= 256;
+}
+}  // namespace
+
+size_t moe_workspace_size_nvfp4(const moe_config* c) {
+  if (moe_check_config(c) != MOE_OK || c->dtype != MOE_BF16 || !nvf4_shape_ok(*c)) return 0;
+  Carver cv(nullptr);
+  carve_layer_nvf4(cv, *c);
+  return align_up(cv.off, 256);
+}
+
+int moe_quantize_nvfp4(int64_t rows, int32_t cols, const void* src, uint8_t* q, uint8_t* sf,
+                       float* scale, moe_stream_t stream) {
+  if (rows < 0 || cols < 16 || cols % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!src || !q || !sf || !scale) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned({src, q, sf, scale})) return MOE_ERR_MISALIGNED;
+  QuantArgs a{};
+  a.src = static_cast<const __nv_bfloat16*>(src);
+  a.rows = rows;
+  a.cols = cols;
+  a.q = q;
+  a.sf = sf;
+  a.ld_sf = nvf4_sf_stride(cols);
+  a.scale = scale;
+  cudaError_t e = launch_quantize_rows_nvf4(a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : fail_cuda(e);
+}
+
+int moe_layer_forward_nvfp4(const moe_config* cfg, const void* x, const void* w_router,
+                            const float* logit_bias, const float* sel_bias, const uint8_t* wg_q,
+                            const uint8_t* wg_sf, const float* wg_scale, const uint8_t* wu_q,
+                            const uint8_t* wu_sf, const float* wu_scale, const uint8_t* wd_q,
+                            const uint8_t* wd_sf, const float* wd_scale, void* y,
+                            int32_t* topk_idx, float* topk_w, int32_t* counts, float* prob_sum,
+                            void* ws, size_t ws_bytes, moe_stream_t stream) {
+  int rc = moe_check_config(cfg);
+  if (rc != MOE_OK) return rc;
+  const moe_config& c = *cfg;
+  if (c.dtype != MOE_BF16 || !nvf4_shape_ok(c)) return MOE_ERR_UNSUPPORTED;
+  if (c.T > 0 && (!x || !w_router || !wg_q || !wg_sf || !wg_scale || !wu_q || !wu_sf ||
+                  !wu_scale || !wd_q || !wd_sf || !wd_scale || !y))
+    return MOE_ERR_INVALID_ARG;
+  if (!all_aligned({x, w_router, logit_bias, sel_bias, wg_q, wg_sf, wg_scale, wu_q, wu_sf,
+                    wu_scale, wd_q, wd_sf, wd_scale, y, topk_idx, topk_w, counts, prob_sum}))
+    return MOE_ERR_MISALIGNED;
+  if ((rc = check_ws(c, ws, ws_bytes, moe_workspace_size_nvfp4(cfg))) != MOE_OK) return rc;
+  if ((rc = check_device(c)) != MOE_OK) return rc;
+  Carver cv(ws);
+  LayerNvf4Ws w4 = carve_layer_nvf4(cv, c);
+  LayerWs& w = w4.base;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
+  int32_t* idx = topk_idx ? topk_idx : w.topk_idx;
+  float* tw = topk_w ? topk_w : w.topk_w;
+  int32_t* cnt = counts ? counts : w.counts;
+  float* ps = prob_sum ? prob_sum : w.prob_sum;
+  cudaError_t e = launch_router(c, x, w_router, logit_bias, sel_bias, nullptr, nullptr, idx, tw,
+                                cnt, ps, w.partials, w.status, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (c.T == 0) return MOE_OK;
+  const long long P = pairs(c);
+  // the NVFP4 GEMMs run 128-row tiles
+  e = launch_permute(c, x, idx, cnt, w.offsets, w.sorted_pair, w.inv_pos, nullptr, w.hist,
+                     w.status, w.seg, kTileM, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  const int sfd = nvf4_sf_stride(c.d_model);
+  // routed rows: gathered and quantized in one pass; their H maxima cleared
+  QuantArgs qa{};
+  qa.src = static_cast<const __nv_bfloat16*>(x);
+  qa.rows = P;
+  qa.cols = c.d_model;
+  qa.gather = w.sorted_pair;
+  qa.k = c.top_k;
+  qa.src_rows = c.T;
+  qa.rows_dev = w.offsets + c.n_experts;
+  qa.q = w4.xq_perm;
+  qa.sf = w4.xp_sf;
+  qa.ld_sf = sfd;
+  qa.scale = w4.xp_scale;
+  qa.clear = w4.h_amax;
+  qa.clear_n = 1;
+  e = launch_quantize_rows_nvf4(qa, s);
+  if (e == cudaSuccess && c.n_shared > 0) {  // x for the shared experts
+    QuantArgs qs{};
+    qs.src = static_cast<const __nv_bfloat16*>(x);
+    qs.rows = c.T;
+    qs.cols = c.d_model;
+    qs.q = w4.xq;
+    qs.sf = w4.x_sf;
+    qs.ld_sf = sfd;
+    qs.scale = w4.x_scale;
+    qs.clear = w4.h_amax;
+    qs.clear_base = P;
+    qs.clear_stride = c.T;
+    qs.clear_n = c.n_shared;
+    e = launch_quantize_rows_nvf4(qs, s);
+  }
+  if (e == cudaSuccess)
+    e = launch_grouped_nvf4(c, Nvf4Matrix{w4.xq_perm, w4.xp_sf, w4.xp_scale},
+                            Nvf4Matrix{w4.xq, w4.x_sf, w4.x_scale}, w.seg, w.sorted_pair, tw,
+                            Nvf4Matrix{wg_q, wg_sf, wg_scale}, Nvf4Matrix{wu_q, wu_sf, wu_scale},
+                            Nvf4Matrix{wd_q, wd_sf, wd_scale}, w.h, w4.h_amax, w4.hq, w4.h_sf,
+                            w4.h_scale, w.y_perm, w.partial, padded_rows(P), padded_rows(c.T),
                             padded_rows(rows_total(c)), w.status, s);
   if (e == cudaSuccess) e = launch_combine(c, w.y_perm, w.inv_pos, nullptr, y, s);
   return e == cudaSuccess ? MOE_OK : fail_cuda(e);

@@ -72,7 +72,6 @@ constexpr int EPI_THREADS = 128;
 constexpr int EPI_WARPS = 8;
 constexpr int G_EPI_THREADS = 32 * EPI_WARPS;  // 256
 constexpr int G_THREADS = 64 + G_EPI_THREADS;  // 320
-constexpr size_t DYN_SMEM = (size_t)STAGES * STAGE_BYTES + 1024;  // + 1 KB alignment slack
 
 // Epilogues. The forward's two, and the backward's (1-CTA kernel only):
 //  EPI_SWIGLU_SAVE  gate/up as EPI_SWIGLU, also storing the pre-activations
@@ -93,19 +92,39 @@ __host__ __device__ constexpr bool b_mn(int EPI) {
 }
 constexpr int B_MN_BOX_BYTES = 64 * 128;  // one TMA box: 64 K rows x 64 bf16 columns
 
-// Operand types. A stage row is 128 bytes either way: 64 bf16 or 128 E4M3
-// elements of K, and one MMA takes 32 bytes of K (16 bf16 with kind::f16,
-// 32 E4M3 with kind::f8f6f4), so rings, descriptors and K steps are shared;
-// only the K extent of a block, the instruction and the epilogue scales
-// (E4M3: one fp32 scale per A row and per weight output channel) differ.
-enum { OP_BF16 = 0, OP_E4M3 = 1 };
+// Operand types. A stage row is 128 bytes in every case: 64 bf16, 128 E4M3
+// or 256 packed E2M1 (NVFP4) elements of K, and one MMA takes 32 bytes of K
+// (16 bf16 with kind::f16, 32 E4M3 with kind::f8f6f4, 64 E2M1 with
+// kind::mxf4nvf4), so rings, descriptors and K steps are shared; the K
+// extent of a block, the instruction and the epilogue scales (E4M3 and
+// NVFP4: one fp32 scale per A row and per weight output channel) differ.
+// NVFP4 stages also carry the E4M3 block scales of their 256 K elements
+// (16 a row: 2 KB for A, 4 KB for B), which the MMA reads from Tensor
+// Memory; they take TMEM columns, so the NVFP4 kernel keeps a single
+// accumulator (1-CTA tiles only).
+enum { OP_BF16 = 0, OP_E4M3 = 1, OP_NVF4 = 2 };
 template <int OP>
 struct Op {
-  static constexpr int EPK = OP == OP_BF16 ? 64 : 128;  // K elements per 128-byte block
+  static constexpr int EPK = OP == OP_BF16 ? 64 : OP == OP_E4M3 ? 128 : 256;  // K per block
+  static constexpr int KC = OP == OP_BF16 ? 64 : 128;  // TMA inner coordinate step per block
+  static constexpr bool scaled = OP != OP_BF16;        // row and channel scales in the epilogue
+  static constexpr int SF_A = OP == OP_NVF4 ? BM * 16 : 0;
+  static constexpr int SF_B = OP == OP_NVF4 ? BN * 16 : 0;
+  static constexpr int STAGE = STAGE_BYTES + SF_A + SF_B;  // 48 KB, or 54 KB for NVFP4
+  static constexpr int NACC = OP == OP_NVF4 ? 1 : NUM_ACC;
+  static constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024;  // + 1 KB alignment slack
+  // NVFP4 adds a warp (the last) that rearranges each stage's block scales
+  static constexpr int THREADS = G_THREADS + (OP == OP_NVF4 ? 32 : 0);
 };
+// TMEM columns of the NVFP4 block scales: two buffers (alternate K blocks)
+// of 64 columns after the accumulator, A's 16 then B's 32 (4 and 8 a MMA).
+constexpr int SF_TMEM_COL = BN;
+constexpr int SF_TMEM_BUF = 64;
 template <int OP>
 __host__ __device__ constexpr uint32_t idesc_op(int M, int N) {
-  return OP == OP_BF16 ? ptx::idesc_bf16_f32(M, N) : ptx::idesc_e4m3_f32(M, N);
+  return OP == OP_BF16 ? ptx::idesc_bf16_f32(M, N)
+         : OP == OP_E4M3 ? ptx::idesc_e4m3_f32(M, N)
+                         : ptx::idesc_nvf4_f32(M, N);
 }
 template <int OP>
 __device__ __forceinline__ void mma_op(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
@@ -162,6 +181,7 @@ struct GemmArgs {
 struct __align__(8) SharedState {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
+  uint64_t sf_ready[STAGES];  // NVFP4: the stage's block scales are rearranged
   uint64_t acc_full[NUM_ACC];
   uint64_t acc_empty[NUM_ACC];
   uint64_t drain;
@@ -213,6 +233,21 @@ __device__ __forceinline__ void load_scales8(const float* p, bool in, float row,
   s[7] = row * b.w;
 }
 
+// The same from this warp's staged copy of the tile's channel scales in
+// shared memory (zeros past the output already in place).
+__device__ __forceinline__ void staged_scales8(const float* p, float row, float (&s)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  s[0] = row * a.x;
+  s[1] = row * a.y;
+  s[2] = row * a.z;
+  s[3] = row * a.w;
+  s[4] = row * b.x;
+  s[5] = row * b.y;
+  s[6] = row * b.z;
+  s[7] = row * b.w;
+}
+
 // Split factor of every tile when there are fewer tiles than two waves of
 // CTAs: among S in [1, s_max] with at least kMinKbPerSplit K blocks per
 // split, the largest whose wave efficiency (units / whole waves of the grid)
@@ -249,14 +284,18 @@ __device__ __forceinline__ float row_scale(const GemmArgs& a, int seg_id, long l
 // TMEM lane (row) 32 columns at a time and stores bf16 (SwiGLU of the paired
 // gate/up columns, or the gate-weighted down projection). Two warps share a
 // lane quarter; `half` picks which half of the columns this one drains. Rows
-// past the segment's end (valid = false) are loaded but not stored. E4M3:
-// sa is the row's A scale and sb0/sb1 point at the tile's first weight
-// channel scale (gate, up; or down); gate/up also records the row's max |H|.
+// past the segment's end (valid = false) are loaded but not stored. gw is
+// the row's gate weight (down projection). E4M3 and NVFP4: sa is the row's
+// A scale and sb0/sb1 point at the tile's first weight channel scale (gate,
+// up; or down), or, when `ss` is given, the 128 channel scales of this
+// warp's columns are staged there (gate/up: 64 gate then 64 up; down: 128);
+// gate/up also records the row's max |H|.
 template <int EPI, int OP>
 __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tbase, const Tile& t,
                                                int half, bool valid, long long orow,
                                                __nv_bfloat16* out, float sa, const float* sb0,
-                                               const float* sb1) {
+                                               const float* sb1, float gw,
+                                               const float* ss = nullptr) {
   if constexpr (gu_like(EPI)) {
     float hmax = 0.f;
 #pragma unroll 1
@@ -273,24 +312,29 @@ __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tb
         // warp-uniform 16-byte load each (n_out is a multiple of 16, so a
         // group is wholly inside or wholly past it)
         float sg[8], su[8];
-        if constexpr (OP == OP_E4M3) {
-          const bool in = col0 + q * 8 < args.n_out;
-          load_scales8(sb0 + c * 32 + q * 8, in, sa, sg);
-          load_scales8(sb1 + c * 32 + q * 8, in, sa, su);
+        if constexpr (Op<OP>::scaled) {
+          if (ss) {
+            staged_scales8(ss + (c - 2 * half) * 32 + q * 8, sa, sg);
+            staged_scales8(ss + 64 + (c - 2 * half) * 32 + q * 8, sa, su);
+          } else {
+            const bool in = col0 + q * 8 < args.n_out;
+            load_scales8(sb0 + c * 32 + q * 8, in, sa, sg);
+            load_scales8(sb1 + c * 32 + q * 8, in, sa, su);
+          }
         }
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           const int j = 4 * q + jj;
           float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
           float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
-          if constexpr (OP == OP_E4M3) {
+          if constexpr (Op<OP>::scaled) {
             g0 *= sg[2 * jj];
             g1 *= sg[2 * jj + 1];
             u0 *= su[2 * jj];
             u1 *= su[2 * jj + 1];
           }
           pk[j] = f32x2_to_bf16x2(silu(g0) * u0, silu(g1) * u1);
-          if constexpr (OP == OP_E4M3) {
+          if constexpr (Op<OP>::scaled) {
             float h0, h1;
             bf16x2_to_f32(pk[j], h0, h1);
             hmax = fmaxf(hmax, fmaxf(fabsf(h0), fabsf(h1)));
@@ -323,7 +367,7 @@ __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tb
         }
       }
     }
-    if constexpr (OP == OP_E4M3)
+    if constexpr (Op<OP>::scaled)
       if (valid && hmax > 0.f) atomicMax(args.h_amax + orow, __float_as_uint(hmax));
   } else if constexpr (EPI == EPI_SWIGLU_BWD) {
 #pragma unroll 1
@@ -372,7 +416,7 @@ __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tb
       }
     }
   } else {
-    const float scale = valid ? row_scale(args, t.s, orow) * sa : 0.0f;
+    const float scale = valid ? gw * sa : 0.0f;
 #pragma unroll 1
     for (int c = 4 * half; c < 4 * half + 4; ++c) {
       uint32_t v[32];
@@ -383,13 +427,17 @@ __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tb
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         float sd[8];
-        if constexpr (OP == OP_E4M3)
-          load_scales8(sb0 + c * 32 + q * 8, col0 + q * 8 < args.n_out, scale, sd);
+        if constexpr (Op<OP>::scaled) {
+          if (ss)
+            staged_scales8(ss + (c - 4 * half) * 32 + q * 8, scale, sd);
+          else
+            load_scales8(sb0 + c * 32 + q * 8, col0 + q * 8 < args.n_out, scale, sd);
+        }
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           const int j = 4 * q + jj;
           float y0 = __uint_as_float(v[2 * j]), y1 = __uint_as_float(v[2 * j + 1]);
-          if constexpr (OP == OP_E4M3) {
+          if constexpr (Op<OP>::scaled) {
             y0 *= sd[2 * jj];
             y1 *= sd[2 * jj + 1];
           } else {
@@ -420,7 +468,7 @@ __device__ __forceinline__ void row_scales(const GemmArgs& args, const int32_t* 
                                            float& sa, const float*& sb0, const float*& sb1) {
   sa = 1.f;
   sb0 = sb1 = nullptr;
-  if constexpr (OP == OP_E4M3) {
+  if constexpr (Op<OP>::scaled) {
     const long long wbase = (long long)t.s * args.b_rows + t.n * (gu_like(EPI) ? 128 : 256);
     sb0 = args.b_scale0 + wbase;
     if (gu_like(EPI)) {
@@ -433,12 +481,38 @@ __device__ __forceinline__ void row_scales(const GemmArgs& args, const int32_t* 
   }
 }
 
+// NVFP4 block-scale maps (E4M3 bytes [rows][stride], boxes of 128 rows x
+// 16 bytes = the scales of one 256-element K block): A rows, the shared
+// experts' A rows, and the weight rows of B's two halves. Unused otherwise.
+struct SfMaps {
+  CUtensorMap a, a_shared, b0, b1;
+};
+
+// NVFP4: rearranges the block scales of 128 rows, as TMA left them (row r
+// at r*16: its four 32-bit words are the scales of the four MMAs of the
+// block, four 16-element groups each), in place into four 512-byte units,
+// one per MMA, where the 16 bytes of unit row l hold the words of rows l,
+// l+32, l+64 and l+96. That is the layout tcgen05.cp .32x128b.warpx4 turns
+// into the MMA's scale-factor columns (row m at column m/32 of every lane
+// congruent to m mod 32). Executed by a full warp.
+__device__ __forceinline__ void sf_rearrange(uint32_t base, int lane) {
+  uint4 v[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) v[c] = ptx::ld_shared_v4(base + (uint32_t)(lane + 32 * c) * 16u);
+  __syncwarp();
+  ptx::st_shared_v4(base + 0 * 512 + lane * 16, v[0].x, v[1].x, v[2].x, v[3].x);
+  ptx::st_shared_v4(base + 1 * 512 + lane * 16, v[0].y, v[1].y, v[2].y, v[3].y);
+  ptx::st_shared_v4(base + 2 * 512 + lane * 16, v[0].z, v[1].z, v[2].z, v[3].z);
+  ptx::st_shared_v4(base + 3 * 512 + lane * 16, v[0].w, v[1].w, v[2].w, v[3].w);
+}
+
 template <int EPI, int OP>
-__global__ void __launch_bounds__(G_THREADS, 1)
+__global__ void __launch_bounds__(Op<OP>::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_a_shared,
                         const __grid_constant__ CUtensorMap map_b0,
-                        const __grid_constant__ CUtensorMap map_b1, const GemmArgs args) {
+                        const __grid_constant__ CUtensorMap map_b1, const GemmArgs args,
+                        const __grid_constant__ SfMaps sf) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ SharedState st;
 
@@ -453,6 +527,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     for (int i = 0; i < STAGES; ++i) {
       ptx::mbar_init(ptx::smem_addr(&st.full[i]), 1);
       ptx::mbar_init(ptx::smem_addr(&st.empty[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&st.sf_ready[i]), 1);
     }
     for (int i = 0; i < NUM_ACC; ++i) {
       ptx::mbar_init(ptx::smem_addr(&st.acc_full[i]), 1);
@@ -467,6 +542,12 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     ptx::prefetch_tmap(&map_a_shared);
     ptx::prefetch_tmap(&map_b0);
     ptx::prefetch_tmap(&map_b1);
+    if constexpr (OP == OP_NVF4) {
+      ptx::prefetch_tmap(&sf.a);
+      ptx::prefetch_tmap(&sf.a_shared);
+      ptx::prefetch_tmap(&sf.b0);
+      ptx::prefetch_tmap(&sf.b1);
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_addr(&st.tmem_base), TMEM_COLS);
@@ -510,10 +591,21 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             break;
           }
           const uint32_t fb = ptx::smem_addr(&st.full[stage]);
-          const uint32_t a_dst = ring + stage * STAGE_BYTES;
+          const uint32_t a_dst = ring + stage * Op<OP>::STAGE;
           const uint32_t b_dst = a_dst + A_BYTES;
-          ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          ptx::tma_load_2d(a_dst, am, fb, kb * Op<OP>::EPK, a_row);
+          ptx::mbar_arrive_expect_tx(fb, Op<OP>::STAGE);
+          ptx::tma_load_2d(a_dst, am, fb, kb * Op<OP>::KC, a_row);
+          if constexpr (OP == OP_NVF4) {
+            // block scales: A's 128 rows, then B's two 128-row halves
+            const uint32_t sf_dst = a_dst + STAGE_BYTES;
+            const bool sh = gu_like(EPI) && t.s >= args.n_routed;
+            ptx::tma_load_2d(sf_dst, sh ? &sf.a_shared : &sf.a, fb, kb * 16, a_row);
+            ptx::tma_load_2d(sf_dst + 2048, &sf.b0, fb, kb * 16, b_row);
+            if (gu_like(EPI))
+              ptx::tma_load_2d(sf_dst + 4096, &sf.b1, fb, kb * 16, b_row);
+            else
+              ptx::tma_load_2d(sf_dst + 4096, &sf.b0, fb, kb * 16, b_row + 128);
+          }
           if constexpr (b_mn(EPI)) {
             // K rows kb*64.. of this expert's B (from map_b1 past kb_split),
             // as 4 boxes of 64 N columns
@@ -524,11 +616,11 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             for (int q = 0; q < 4; ++q)
               ptx::tma_load_2d(b_dst + q * B_MN_BOX_BYTES, bm, fb, t.n * 256 + q * 64, krow);
           } else if (gu_like(EPI)) {
-            ptx::tma_load_2d(b_dst, &map_b0, fb, kb * Op<OP>::EPK, b_row);
-            ptx::tma_load_2d(b_dst + B_HALF_BYTES, &map_b1, fb, kb * Op<OP>::EPK, b_row);
+            ptx::tma_load_2d(b_dst, &map_b0, fb, kb * Op<OP>::KC, b_row);
+            ptx::tma_load_2d(b_dst + B_HALF_BYTES, &map_b1, fb, kb * Op<OP>::KC, b_row);
           } else {
-            ptx::tma_load_2d(b_dst, &map_b0, fb, kb * Op<OP>::EPK, b_row);
-            ptx::tma_load_2d(b_dst + B_HALF_BYTES, &map_b0, fb, kb * Op<OP>::EPK, b_row + 128);
+            ptx::tma_load_2d(b_dst, &map_b0, fb, kb * Op<OP>::KC, b_row);
+            ptx::tma_load_2d(b_dst + B_HALF_BYTES, &map_b0, fb, kb * Op<OP>::KC, b_row + 128);
           }
           ++issued;
           if (++stage == STAGES) {
@@ -548,7 +640,65 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
+    if constexpr (OP == OP_NVF4) {
+      // Lane 0 waits until a stage's block scales are rearranged (the last
+      // warp, below), copies them into TMEM and issues the block-scaled MMAs.
+      // One accumulator; the scales of consecutive K blocks alternate
+      // between two TMEM buffers.
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0, acc_phase = 0, kcount = 0;
+        bool ok = true;
+        for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x) {
+          if (!wait_phase(ptx::smem_addr(&st.acc_empty[0]), acc_phase ^ 1u, abort_flag,
+                          args.status)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const int split = unit % S;
+          const int kb0 = kb_begin(split, S, KB), kb1 = kb_begin(split + 1, S, KB);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!wait_phase(ptx::smem_addr(&st.sf_ready[stage]), phase, abort_flag,
+                            args.status)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t a_src = ring + stage * Op<OP>::STAGE;
+            const uint32_t sf_src = a_src + STAGE_BYTES;  // A's scales, then B's two halves
+            const uint32_t sfa_t = tmem_base + SF_TMEM_COL + (kcount & 1u) * SF_TMEM_BUF;
+            const uint32_t sfb_t = sfa_t + 16;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              ptx::tmem_cp_32x128b_x4(sfa_t + 4 * k, ptx::sdesc_rows16(sf_src + 512 * k));
+              ptx::tmem_cp_32x128b_x4(sfb_t + 8 * k, ptx::sdesc_rows16(sf_src + 2048 + 512 * k));
+              ptx::tmem_cp_32x128b_x4(sfb_t + 8 * k + 4,
+                                      ptx::sdesc_rows16(sf_src + 4096 + 512 * k));
+            }
+            const uint64_t adesc = ptx::sdesc_k128(a_src);
+            const uint64_t bdesc = ptx::sdesc_k128(a_src + A_BYTES);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)  // +32 bytes (64 E2M1) of K per step
+              ptx::mma_nvf4(tmem_base, adesc + 2 * k, bdesc + 2 * k, idesc_op<OP>(BM, BN),
+                            sfa_t + 4 * k, sfb_t + 8 * k, (kb > kb0 || k > 0) ? 1u : 0u);
+            ptx::mma_commit(ptx::smem_addr(&st.empty[stage]));
+            ++kcount;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          ptx::mma_commit(ptx::smem_addr(&st.acc_full[0]));
+          acc_phase ^= 1u;
+        }
+        if (!ok) {
+          ptx::mma_commit(ptx::smem_addr(&st.drain));
+          drain_wait(ptx::smem_addr(&st.drain), 0);
+        }
+      }
+    } else if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -570,7 +720,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a_src = ring + stage * STAGE_BYTES;
+          const uint32_t a_src = ring + stage * Op<OP>::STAGE;
           const uint64_t adesc = ptx::sdesc_k128(a_src);
           if constexpr (b_mn(EPI)) {
             const uint64_t bdesc = ptx::sdesc_mn128(a_src + A_BYTES, B_MN_BOX_BYTES);
@@ -605,20 +755,53 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         drain_wait(ptx::smem_addr(&st.drain), 0);
       }
     }
+  } else if (OP == OP_NVF4 && warp == G_THREADS / 32) {
+    // ------------------------------------------- NVFP4 block-scale warp --
+    // Waits for each stage, rearranges its block scales for tcgen05.cp
+    // (sf_rearrange) and hands the stage to the MMA thread (sf_ready), so
+    // the MMA issue never waits on this shared-memory work.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x) {
+      const int split = unit % S;
+      const int kb1 = kb_begin(split + 1, S, KB);
+      for (int kb = kb_begin(split, S, KB); kb < kb1; ++kb) {
+        ok = wait_phase(ptx::smem_addr(&st.full[stage]), phase, abort_flag, args.status);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sf_src = ring + stage * Op<OP>::STAGE + STAGE_BYTES;
+        sf_rearrange(sf_src, lane);
+        sf_rearrange(sf_src + 2048, lane);
+        sf_rearrange(sf_src + 4096, lane);
+        ptx::fence_proxy_async_smem();  // generic writes before tcgen05.cp reads them
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&st.sf_ready[stage]));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
   } else {
     // ----------------------------------------------------------- epilogue --
     const int sub = warp & 3;  // TMEM lanes [32*sub, 32*sub+32) are this warp's
     const int half = (warp - 2) >> 2;  // which half of the columns
     const int row_in_tile = sub * 32 + lane;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
+    // E4M3 / NVFP4: each epilogue warp's copy of the channel scales of its
+    // columns of the current tile
+    __shared__ __align__(16) float ch_scales[EPI_WARPS][128];
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int unit = blockIdx.x; unit < total; unit += gridDim.x) {
       const int split = unit % S;
       const Tile t = decode_tile(seg, E, args.NT, unit / S);
-      bool ok = wait_phase(ptx::smem_addr(&st.acc_full[acc]), acc_phase, abort_flag, args.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      ptx::tc_fence_after();
+      // Everything that does not depend on the accumulator is fetched while
+      // the MMAs of this tile still run: the row's place, its scales and
+      // gate weight, and the tile's channel scales.
       const int rows = __ldg(seg + 3 + E + t.s);
       const int row0 = __ldg(seg + 3 + 3 * E + t.s);
       const int r = t.m * BM + row_in_tile;
@@ -629,8 +812,30 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       const float* sb0;
       const float* sb1;
       row_scales<EPI, OP>(args, seg, E, t, r, valid, orow, sa, sb0, sb1);
+      const float gw = (EPI == EPI_DOWN && valid) ? row_scale(args, t.s, orow) : 1.0f;
+      const float* ss = nullptr;
+      if constexpr (Op<OP>::scaled) {
+        if (S == 1) {
+          float* mine = ch_scales[warp - 2];
+          __syncwarp();  // the previous tile's reads of `mine` are done
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int j = lane + 32 * i;
+            const int jj = gu_like(EPI) ? (j & 63) : j;
+            const int col = gu_like(EPI) ? t.n * 128 + 64 * half + jj : t.n * 256 + 128 * half + j;
+            const float* src = gu_like(EPI) ? (j < 64 ? sb0 : sb1) + 64 * half + jj
+                                            : sb0 + 128 * half + j;
+            mine[j] = col < args.n_out ? __ldg(src) : 0.0f;
+          }
+          __syncwarp();
+          ss = mine;
+        }
+      }
+      bool ok = wait_phase(ptx::smem_addr(&st.acc_full[acc]), acc_phase, abort_flag, args.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      ptx::tc_fence_after();
       if (S == 1) {
-        epilogue_fused<EPI, OP>(args, tbase, t, half, valid, orow, out, sa, sb0, sb1);
+        epilogue_fused<EPI, OP>(args, tbase, t, half, valid, orow, out, sa, sb0, sb1, gw, ss);
         ptx::tc_fence_before();
         ptx::mbar_arrive(ptx::smem_addr(&st.acc_empty[acc]));
       } else {
@@ -645,13 +850,13 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           if (EPI == EPI_SWIGLU) ptx::tmem_ld32(tbase + 128 + c * 32, u);
           const int col0 = t.n * (EPI == EPI_SWIGLU ? 128 : 256) + c * 32;
           float my0 = 0.f, my1 = 0.f;  // E4M3: lane l fetches column l's scales
-          if constexpr (OP == OP_E4M3)
+          if constexpr (Op<OP>::scaled)
             if (col0 + (threadIdx.x % 32) < args.n_out) {
               my0 = __ldg(sb0 + c * 32 + threadIdx.x % 32);
               if (EPI == EPI_SWIGLU) my1 = __ldg(sb1 + c * 32 + threadIdx.x % 32);
             }
           ptx::tmem_ld_wait();
-          if constexpr (OP == OP_E4M3) {  // partials carry their scales (sums are linear)
+          if constexpr (Op<OP>::scaled) {  // partials carry their scales (sums are linear)
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
               v[jj] = __float_as_uint(__uint_as_float(v[jj]) * sa * __shfl_sync(0xffffffffu, my0, jj));
@@ -681,7 +886,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         ptx::tc_fence_before();
         ptx::mbar_arrive(ptx::smem_addr(&st.acc_empty[acc]));
       }
-      if (++acc == NUM_ACC) {
+      if (++acc == Op<OP>::NACC) {
         acc = 0;
         acc_phase ^= 1u;
       }
@@ -894,7 +1099,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       const float* sb0;
       const float* sb1;
       row_scales<EPI, OP>(args, seg, E, t, r, valid, orow, sa, sb0, sb1);
-      epilogue_fused<EPI, OP>(args, tbase, t, half, valid, orow, out, sa, sb0, sb1);
+      const float gw = (EPI == EPI_DOWN && valid) ? row_scale(args, t.s, orow) : 1.0f;
+      epilogue_fused<EPI, OP>(args, tbase, t, half, valid, orow, out, sa, sb0, sb1, gw);
       ptx::tc_fence_before();
       ptx::mbar_arrive_cluster(acc ? acc_empty_leader1 : acc_empty_leader0);
       if (++acc == NUM_ACC) {
@@ -1132,7 +1338,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       float sw0 = 1.f, sw1 = 1.f;
       const float* tok_scale = nullptr;
       long long tok_row0 = 0;
-      if constexpr (OP == OP_E4M3) {
+      if constexpr (Op<OP>::scaled) {
         const long long wrow = (long long)t.s * args.b_rows + f;
         sw0 = fvalid ? __ldg(args.b_scale0 + wrow) : 0.f;
         if (EPI == EPI_SWIGLU) {
@@ -1156,7 +1362,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const long long orow = row0 + c0 + c;
           float av = __uint_as_float(a[c]);
           float bv = EPI == EPI_SWIGLU ? __uint_as_float(b[c]) : 0.f;
-          if constexpr (OP == OP_E4M3) {
+          if constexpr (Op<OP>::scaled) {
             const float st = __ldg(tok_scale + tok_row0 + c0 + c);
             av *= sw0 * st;
             bv *= sw1 * st;
@@ -1166,7 +1372,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (EPI == EPI_SWIGLU) hb = __float2bfloat16_rn(silu(av) * bv);
             else hb = __float2bfloat16_rn(row_scale(args, t.s, orow) * av);
             if (fvalid) out[orow * args.ldo + f] = hb;
-            if constexpr (OP == OP_E4M3 && EPI == EPI_SWIGLU) {
+            if constexpr (Op<OP>::scaled && EPI == EPI_SWIGLU) {
               // the H row's max |H| over this warp's 32 features, one atomic
               float m = fvalid ? fabsf(__bfloat162float(hb)) : 0.f;
 #pragma unroll
@@ -1217,7 +1423,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmArgs a, in
   const int groups = a.n_out / 4;
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long first_row = ((long long)blockIdx.x * blockDim.x) / groups;
-  constexpr bool kAmax = OP == OP_E4M3 && EPI == EPI_SWIGLU;
+  constexpr bool kAmax = Op<OP>::scaled && EPI == EPI_SWIGLU;
   if (kAmax) {
     s_max[threadIdx.x] = 0u;
     __syncthreads();
@@ -1276,13 +1482,15 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmArgs a, in
 template <int EPI, int OP>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_sh, const CUtensorMap& b0,
                         const CUtensorMap& b1, const GemmArgs& args, int max_tiles,
-                        cudaStream_t s) {
+                        cudaStream_t s, const SfMaps* sf = nullptr) {
+  static const SfMaps no_sf{};  // never read by the bf16 and E4M3 kernels
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, OP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DYN_SMEM);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Op<OP>::SMEM);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
@@ -1296,8 +1504,8 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_sh, const CUt
                 : EPI == EPI_DGRAD      ? K_BWD_DA
                                         : K_DOWN,
                 s);
-    e = launch_pdl(grouped_gemm_kernel<EPI, OP>, dim3(grid), dim3(G_THREADS), DYN_SMEM, s, 1, a,
-                   a_sh, b0, b1, args);
+    e = launch_pdl(grouped_gemm_kernel<EPI, OP>, dim3(grid), dim3(Op<OP>::THREADS), Op<OP>::SMEM, s, 1, a,
+                   a_sh, b0, b1, args, sf ? *sf : no_sf);
   }
   if (e != cudaSuccess || args.s_max <= 1) return e;
   const long long n = args.R * (args.n_out / 4);
@@ -1633,6 +1841,94 @@ cudaError_t launch_grouped_e4m3(const moe_config& c, const uint8_t* xq_perm,
   d.NT = (c.d_model + 255) / 256;
   return pair ? launch_pair<EPI_DOWN, OP_E4M3>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s)
               : launch_gemm<EPI_DOWN, OP_E4M3>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s);
+}
+
+cudaError_t launch_grouped_nvf4(const moe_config& c, Nvf4Matrix xp, Nvf4Matrix xs,
+                                const int32_t* seg, const int32_t* sorted_pair,
+                                const float* topk_w, Nvf4Matrix wg, Nvf4Matrix wu, Nvf4Matrix wd,
+                                void* h, unsigned* h_amax, uint8_t* hq, uint8_t* h_sf,
+                                float* h_scale, void* y_perm, float* partial, long long xp_rows,
+                                long long xs_rows, long long h_rows, int* status, cudaStream_t s) {
+  const long long P = (long long)c.T * c.top_k;
+  const int E = c.n_experts + c.n_shared;
+  const long long R = P + (long long)c.n_shared * c.T;
+  if (R == 0) return cudaSuccess;
+  const long long mt_bound = mt_bound_of(c, BM);
+  const SplitKPlan plan = splitk_plan(c);
+  // the shared experts' A rows (x); without shared experts the map is unused
+  const Nvf4Matrix as = c.n_shared > 0 ? xs : xp;
+  const long long as_rows = c.n_shared > 0 ? xs_rows : xp_rows;
+  const long long sfd = nvf4_sf_stride(c.d_model), sff = nvf4_sf_stride(c.d_ff);
+
+  GemmArgs g{};
+  g.seg = seg;
+  g.sorted_pair = sorted_pair;
+  g.topk_w = nullptr;
+  g.out = h;
+  g.status = status;
+  g.ldo = c.d_ff;
+  g.n_routed = c.n_experts;
+  g.n_pairs = (int)P;
+  g.K = c.d_model;
+  g.n_out = c.d_ff;
+  g.NT = (c.d_ff + 127) / 128;
+  g.b_rows = c.d_ff;
+  g.partial = partial;
+  g.s_max = plan.s_max_gu;
+  g.pc = 2 * c.d_ff;
+  g.R = R;
+  g.a_scale = xp.scale;
+  g.a_scale_shared = as.scale;
+  g.b_scale0 = wg.scale;
+  g.b_scale1 = wu.scale;
+  g.h_amax = h_amax;
+  GemmArgs d = g;
+  d.topk_w = topk_w;
+  d.out = y_perm;
+  d.ldo = c.d_model;
+  d.K = c.d_ff;
+  d.n_out = c.d_model;
+  d.NT = (c.d_model + 255) / 256;
+  d.b_rows = c.d_model;
+  d.s_max = plan.s_max_dn;
+  d.pc = c.d_model;
+  d.a_scale = h_scale;
+  d.a_scale_shared = h_scale;
+  d.b_scale0 = wd.scale;
+  d.b_scale1 = wd.scale;
+  d.h_amax = nullptr;
+  // H (bf16, with its rows' max |H|) -> NVFP4
+  QuantArgs qh{};
+  qh.src = static_cast<const __nv_bfloat16*>(h);
+  qh.rows = R;
+  qh.cols = c.d_ff;
+  qh.amax_in = h_amax;
+  qh.q = hq;
+  qh.sf = h_sf;
+  qh.ld_sf = (int)sff;
+  qh.scale = h_scale;
+
+  // codes: bytes [rows][K / 2]; block scales: bytes [rows][stride]
+  CUtensorMap m_xp, m_x, m_wg, m_wu, m_h, m_wd;
+  SfMaps sg, sd;
+  const long long wrows_ff = (long long)E * c.d_ff, wrows_d = (long long)E * c.d_model;
+  if (!make_map_u8(&m_xp, xp.q, xp_rows, c.d_model / 2) ||
+      !make_map_u8(&m_x, as.q, as_rows, c.d_model / 2) ||
+      !make_map_u8(&m_wg, wg.q, wrows_ff, c.d_model / 2) ||
+      !make_map_u8(&m_wu, wu.q, wrows_ff, c.d_model / 2) ||
+      !make_map_u8(&m_h, hq, h_rows, c.d_ff / 2) ||
+      !make_map_u8(&m_wd, wd.q, wrows_d, c.d_ff / 2) ||
+      !make_map_sf(&sg.a, xp.sf, xp_rows, sfd) || !make_map_sf(&sg.a_shared, as.sf, as_rows, sfd) ||
+      !make_map_sf(&sg.b0, wg.sf, wrows_ff, sfd) || !make_map_sf(&sg.b1, wu.sf, wrows_ff, sfd) ||
+      !make_map_sf(&sd.a, h_sf, h_rows, sff) || !make_map_sf(&sd.b0, wd.sf, wrows_d, sff))
+    return cudaErrorInvalidValue;
+  sd.a_shared = sd.a;
+  sd.b1 = sd.b0;
+  cudaError_t e = launch_gemm<EPI_SWIGLU, OP_NVF4>(m_xp, m_x, m_wg, m_wu, g,
+                                                   (int)(mt_bound * g.NT), s, &sg);
+  if (e == cudaSuccess) e = launch_quantize_rows_nvf4(qh, s);
+  if (e != cudaSuccess) return e;
+  return launch_gemm<EPI_DOWN, OP_NVF4>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s, &sd);
 }
 
 // ---- backward -----------------------------------------------------------------

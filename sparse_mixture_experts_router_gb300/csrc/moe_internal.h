@@ -78,8 +78,37 @@ struct QuantArgs {
   unsigned* clear;
   long long clear_base, clear_stride;
   int clear_n;
+  // NVFP4 only (nvfp4.cu): q holds packed E2M1 codes [rows][cols / 2] and
+  // sf the E4M3 block scales [rows][ld_sf]; cols a multiple of 64.
+  uint8_t* sf;
+  int ld_sf;
 };
 cudaError_t launch_quantize_rows(const QuantArgs& a, cudaStream_t s);
+// Row-wise NVFP4 quantization (nvfp4.cu): per row one fp32 scale
+// amax / 2688, per 16 elements one E4M3 block scale, per element one E2M1
+// code; other fields as launch_quantize_rows.
+cudaError_t launch_quantize_rows_nvf4(const QuantArgs& a, cudaStream_t s);
+// Bytes of one row of NVFP4 block scales: cols / 16, rounded up to 16.
+inline int nvf4_sf_stride(int cols) { return (cols / 16 + 15) / 16 * 16; }
+
+// An NVFP4 matrix: codes [rows][cols / 2], block scales [rows][stride] and
+// fp32 row scales [rows].
+struct Nvf4Matrix {
+  const uint8_t* q;
+  const uint8_t* sf;
+  const float* scale;
+};
+// The grouped SwiGLU GEMMs with NVFP4 operands (1-CTA tiles; the segment
+// table built with kTileM rows a tile; split-K partials for few tiles):
+// gate/up from xp (routed rows) / xs (the shared experts' token rows)
+// writes H in bf16 and each H row's max |H|; H is quantized into hq (its
+// buffers written, so non-const); down reads hq.
+cudaError_t launch_grouped_nvf4(const moe_config& c, Nvf4Matrix xp, Nvf4Matrix xs,
+                                const int32_t* seg, const int32_t* sorted_pair,
+                                const float* topk_w, Nvf4Matrix wg, Nvf4Matrix wu, Nvf4Matrix wd,
+                                void* h, unsigned* h_amax, uint8_t* hq, uint8_t* h_sf,
+                                float* h_scale, void* y_perm, float* partial, long long xp_rows,
+                                long long xs_rows, long long h_rows, int* status, cudaStream_t s);
 
 // The grouped SwiGLU GEMMs with E4M3 operands (CTA-pair, 1-CTA or swap-AB
 // decode tiles, chosen as for bf16): gate/up from xq_perm / xq (shared experts)
@@ -97,6 +126,9 @@ cudaError_t launch_grouped_e4m3(const moe_config& c, const uint8_t* xq_perm,
                                 long long h_rows, int* status, cudaStream_t s);
 // Row-major uint8 matrix [rows][cols] read in boxes of box_rows rows x 128
 // bytes with the 128-byte swizzle (the E4M3 operands).
+// NVFP4 block scales [rows][stride] bytes, boxes of box_rows rows x 16 bytes.
+bool make_map_sf(CUtensorMap* m, const void* base, long long rows, long long stride,
+                 unsigned box_rows = 128u);
 bool make_map_u8(CUtensorMap* m, const void* base, long long rows, long long cols,
                  unsigned box_rows = 128u);
 

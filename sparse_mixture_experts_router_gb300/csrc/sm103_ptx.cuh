@@ -118,6 +118,47 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint6
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D (+)= (A . SFA) * (B . SFB)^T with NVFP4 operands (kind::mxf4nvf4,
+// block_scale, scale_vec::4X): A and B are packed E2M1 (two elements a
+// byte, the lower K index in the low nibble), K-major; every row of A and of
+// B has one unsigned E4M3 scale per 16 elements of K, read from Tensor
+// Memory at sfa / sfb. One instruction covers 64 elements of K (32 bytes, as
+// the other kinds), so four scales per row; the accumulator is fp32.
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Copies 32 rows of 16 bytes from shared memory (descriptor `sdesc`) into
+// Tensor Memory columns [taddr, taddr + 4) of lanes 0-31, and the same data
+// into lanes 32-63, 64-95 and 96-127 (.warpx4). Ordered before the
+// tcgen05.mma instructions this thread issues after it.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+// Shared-memory descriptor of 32 contiguous rows of 16 bytes without
+// swizzle (the source of tmem_cp_32x128b_x4): 8-row core matrices of 128
+// bytes, the stride between them (128 B) >> 4 in bits 32-45, no leading
+// offset (one 16-byte column), the fixed 0b001 in bits 46-48.
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // Arrives once on `bar` when all tcgen05 operations issued so far by this
 // thread have completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -137,6 +178,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 // (format 0 in bits 7-9 and 10-12), both K-major, N >> 3 and M >> 4 as above.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// Instruction descriptor, kind::mxf4nvf4 (block-scaled; the accumulator is
+// always fp32): scale-factor ids of B (bits 4-5) and A (bits 29-30) 0, A and
+// B E2M1 (format 1 in bits 7-9 and 10-12), both K-major, N >> 3 in bits
+// 17-22, scale type UE4M3 (bit 23 = 0), M >> 4 in bits 24-28, dense K = 64
+// (bit 31 = 0).
+__host__ __device__ constexpr uint32_t idesc_nvf4_f32(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor for a K-major operand stored as rows of

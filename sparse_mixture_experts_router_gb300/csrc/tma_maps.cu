@@ -61,6 +61,22 @@ bool make_map_u8(CUtensorMap* m, const void* base, long long rows, long long col
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// E4M3 block scales of an NVFP4 matrix: bytes [rows][stride] (stride a
+// multiple of 16, padding bytes zero), read in boxes of box_rows rows x 16
+// bytes (the scales of 256 elements of K) without swizzle.
+bool make_map_sf(CUtensorMap* m, const void* base, long long rows, long long stride,
+                 unsigned box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)stride, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)stride};
+  cuuint32_t box[2] = {16u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // fp32 [E][M][N] written in boxes of 32 rows x 32 columns (128 bytes) with
 // the 128-byte swizzle; the expert index is a dimension of its own, so a box
 // that runs past row M of one expert is clipped there rather than writing

@@ -77,7 +77,7 @@ def oracle_routing(oracle, w, inp):
     return r64, idx, tw, counts, ps
 
 
-def oracle_rows(oracle, w, inp, idx, tw, rows, max_experts=40, fp8=False):
+def oracle_rows(oracle, w, inp, idx, tw, rows, max_experts=40, fp8=False, nvfp4=False):
     """Oracle layer output for the listed tokens, copying to the host only
     the experts those tokens use, a batch of tokens at a time."""
     rows = [int(r) for r in rows]
@@ -97,7 +97,8 @@ def oracle_rows(oracle, w, inp, idx, tw, rows, max_experts=40, fp8=False):
             i += 1
         experts = {e: (host(inp["w_gate"][e]), host(inp["w_up"][e]), host(inp["w_down"][e]))
                    for e in sorted(need)}
-        y = oracle.layer_rows(xh, experts, idx, tw, batch, w.n_experts, w.n_shared, keep, fp8)
+        y = oracle.layer_rows(xh, experts, idx, tw, batch, w.n_experts, w.n_shared, keep, fp8,
+                              nvfp4)
         out[i - len(batch):i] = y
     return out
 
