@@ -238,7 +238,7 @@ const char* kKernelNames[K_NUM] = {"reset_status",  "router_topk",    "permute_h
                                    "permute_scan",  "permute_rank",   "permute_gather",
                                    "permute_small", "permute_group",  "seg_table",
                                    "gate_up",       "down",           "splitk_reduce",
-                                   "combine",       "balance_stats",  "quantize_fp8",
+                                   "combine",       "balance_stats",  "quantize",
                                    "bwd_gate",      "bwd_score",      "bwd_dh_swiglu",
                                    "bwd_da",        "bwd_dx",         "bwd_router",
                                    "bwd_wgrad",     "decode_fused"};
