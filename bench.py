@@ -32,6 +32,7 @@ METRIC = "MoE layer tokens/s; grouped-GEMM % bf16 tensor peak; decode % HBM BW"
 # fp32 FMA peak from unit counts and the maximum clock: 152 SMs x 128 lanes x 2 flop x 2.07 GHz
 FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 UNIT = "tokens/s"
+AUX_ALPHA = 0.01  # the balance loss's weight alpha
 # Nominal dense tensor rates relative to bf16 (2.25 PFLOP/s): fp8 4.5, fp4 13.5.
 QUANT_PEAK_RATIO = {None: 1.0, "fp8": 4.5 / 2.25, "nvfp4": 13.5 / 2.25}
 
@@ -193,6 +194,29 @@ def gemm_flops(w, counts=None):
         routed = sum(min(int(c), cap) for c in counts)
     rows = routed + w.n_shared * w.T
     return 4.0 * rows * w.d_model * w.d_ff, 2.0 * rows * w.d_ff * w.d_model
+
+
+def gemm_bytes(w, counts, quant=None):
+    """Algorithmic HBM bytes of the two grouped GEMMs: the weights (and
+    scales) of every expert with a row, the A rows read once and the output
+    rows written once. Operand bytes per element: bf16 2, E4M3 1 (+ an fp32
+    row scale), NVFP4 1/2 (+ an E4M3 scale per 16 and an fp32 row scale); H
+    is written in bf16 by gate/up in every case."""
+    cap = capacity_of(w)
+    routed = sum(min(int(c), cap) if cap else int(c) for c in counts)
+    rows = routed + w.n_shared * w.T
+    active = sum(1 for c in counts if c > 0) + w.n_shared
+    d, f = w.d_model, w.d_ff
+
+    def mat(r, cols):  # bytes of an r x cols operand in the GEMM's format
+        if quant == "fp8":
+            return r * cols + 4 * r
+        if quant == "nvfp4":
+            return r * cols // 2 + r * nvfp4_scale_stride(cols) + 4 * r
+        return r * cols * 2
+    gu = active * 2 * mat(f, d) + mat(rows, d) + rows * f * 2
+    dn = active * mat(d, f) + mat(rows, f) + rows * d * 2
+    return gu, dn
 
 
 def nvfp4_scale_stride(cols):
@@ -418,6 +442,12 @@ def run_ours(args):
         dn_ms = per_kernel["down"]["ms_per_launch"]
         per_kernel["gate_up"]["tflops"] = f_gu / (gu_ms / 1e3) / 1e12
         per_kernel["down"]["tflops"] = f_dn / (dn_ms / 1e3) / 1e12
+        # the same launches against HBM: algorithmic bytes / time
+        b_gu, b_dn = gemm_bytes(w, counts.cpu().tolist(), args.quant)
+        for name, b, ms in (("gate_up", b_gu, gu_ms), ("down", b_dn, dn_ms)):
+            per_kernel[name]["algorithmic_bytes"] = b
+            per_kernel[name]["gbs"] = round(b / (ms / 1e3) / 1e9, 1)
+            per_kernel[name]["hbm_frac"] = round(b / (ms / 1e3) / 1e9 / pk["hbm"], 4)
         gemm_tflops = (f_gu + f_dn) / ((gu_ms + dn_ms) / 1e3) / 1e12
         ach = per_kernel["gate_up"]["tflops"]
         roofline = {"bound": "tensor", "kernel": "gate_up (grouped SwiGLU gate+up GEMM)",
@@ -457,8 +487,19 @@ def run_ours(args):
                 if default and not args.quant and not args.no_backward else None)
     E = w.n_experts + w.n_shared
     wb = touched_weight_bytes(w, [1] * w.n_experts, args.quant)[0]
+    # balance statistics of the last step's routing, by the library's own kernel:
+    # f_i = counts_i / (T*k), P_i = prob_sum_i / T, aux = alpha * N * sum_i f_i P_i
+    bf = torch.empty(w.n_experts, dtype=torch.float32, device=dev)
+    bP = torch.empty(w.n_experts, dtype=torch.float32, device=dev)
+    baux = torch.empty(1, dtype=torch.float32, device=dev)
+    moe.moe_balance_stats(w.n_experts, w.T, w.top_k, counts, ps, AUX_ALPHA, bf, bP, baux, stream)
+    torch.cuda.synchronize(dev)
     routing = {"max_over_mean_expert_load": round(float(counts.max()) / max(1e-9, float(counts.float().mean())), 3),
-               "experts_with_tokens": int((counts > 0).sum())}
+               "experts_with_tokens": int((counts > 0).sum()),
+               "aux_loss": {"alpha": AUX_ALPHA, "value": round(float(baux.item()), 6),
+                            "balanced_value": AUX_ALPHA,
+                            "f": [round(v, 5) for v in bf.cpu().tolist()],
+                            "P": [round(v, 5) for v in bP.cpu().tolist()]}}
     if capacity_of(w):
         routing["pairs_dropped_by_capacity"] = int(sum(max(0, int(c) - capacity_of(w))
                                                        for c in counts.cpu().tolist()))
