@@ -8,7 +8,9 @@
 // "The bare mechanism" (affinity softmax over all experts, renormalised
 // top-k weights, a routing bias that only moves the choice).
 //
-// Scores are fp32 dot products on the CUDA cores, in one of two kernels:
+// Scores are fp32 dot products on the CUDA cores, in one of three kernels:
+//  - few experts and many bf16 tokens (N <= 16, T >= 2048): W_r staged in
+//    shared memory, each warp streaming pairs of whole tokens (below);
 //  - few experts (N <= 32): the 8 warps of a block split d_model and score a
 //    group of 2-8 tokens against all N experts together, reading x once
 //    from HBM and W_r from L2 with 16-byte loads. Bound by HBM (reading x
@@ -198,6 +200,55 @@ __device__ __forceinline__ void finish_block(const float (&psum)[EJ], float* wpr
   router_finish<kThreads>(a.partials, a.cpart, a.N, (int)gridDim.x, a.prob_sum, a.counts, a.done);
 }
 
+// Reduce-scatter of a warp's NV (16 or 32) partial sums: after the step
+// with offset o a lane keeps half of its values (the upper half when
+// lane & o), each summed with its partner's; lanes that end up holding the
+// same value then add their halves. Afterwards value i (summed over the
+// warp) is held by lanes i * 32/NV ... in v[0].
+template <int NV>
+__device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lane) {
+#pragma unroll
+  for (int o = 16, L = NV; o > 0; o >>= 1, L >>= 1) {
+    if (L > 1) {
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < L / 2; ++i) {
+        const float send = upper ? v[i] : v[i + L / 2];
+        const float keep = upper ? v[i + L / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+    }
+  }
+}
+
+// Scores of a group of TPW tokens t0.. after reduce_scatter (value q*NP + e
+// is token t0+q's score for expert e): one shuffle hands expert e's score to
+// lane e, the logit bias is added (and the score written when asked), and
+// the warp selects for each token in turn.
+template <int NP, int TPW>
+__device__ __forceinline__ void select_group(float v0, int lane, long long t0, const RouterArgs& a,
+                                             float (&psum)[1], int* bcount) {
+  constexpr int NV = NP * TPW;
+  constexpr int SPREAD = 32 / NV;
+  const int N = a.N;
+#pragma unroll
+  for (int q = 0; q < TPW; ++q) {
+    const long long t = t0 + q;
+    const int src = ((q * NP + (lane < NP ? lane : 0)) % NV) * SPREAD;
+    const float sum = __shfl_sync(0xffffffffu, v0, src);
+    if (t < a.T) {  // warp-uniform
+      float r[1] = {0.f};
+      if (lane < N) {
+        r[0] = a.logit_bias ? __fadd_rn(sum, a.logit_bias[lane]) : sum;
+        if (a.logits_out) a.logits_out[t * N + lane] = r[0];
+      }
+      select_token<1>(r, lane, t, a, psum, bcount);
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Few experts (N <= 32): a group of TPW tokens is scored by `wsplit` warps
 // of one block (1 for large batches, up to 8 when there are few tokens, so
@@ -217,7 +268,6 @@ __global__ void __launch_bounds__(kThreads, 2) router_small_kernel(const RouterA
   constexpr int EPV = V16<TX>::n;
   constexpr int NV = NP * TPW;
   static_assert(NV == 16 || NV == 32, "reduce-scatter below assumes 16 or 32 values");
-  constexpr int SPREAD = 32 / NV;
   constexpr int kSmallBatch = 32 / NP;  // x vectors per token in flight: 4, 2 or 1
   __shared__ float wprob[kWarps * 32];
   __shared__ int bcount[32];
@@ -274,23 +324,7 @@ __global__ void __launch_bounds__(kThreads, 2) router_small_kernel(const RouterA
         }
       }
     }
-    // reduce-scatter: after the step with offset o a lane keeps half of its
-    // values (the upper half when lane & o), each summed with its partner's;
-    // lanes that end up holding the same value then add their halves.
-#pragma unroll
-    for (int o = 16, L = NV; o > 0; o >>= 1, L >>= 1) {
-      if (L > 1) {
-        const bool upper = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < L / 2; ++i) {
-          const float send = upper ? v[i] : v[i + L / 2];
-          const float keep = upper ? v[i + L / 2] : v[i];
-          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-      } else {
-        v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
-      }
-    }
+    reduce_scatter<NV>(v, lane);
     if (wsplit > 1) {  // the group's warps, added in warp order
       red[warp][lane] = v[0];
       __syncthreads();
@@ -298,22 +332,7 @@ __global__ void __launch_bounds__(kThreads, 2) router_small_kernel(const RouterA
         for (int j = 1; j < wsplit; ++j) v[0] += red[warp + j][lane];
       __syncthreads();
     }
-    if (wi == 0) {
-#pragma unroll
-      for (int q = 0; q < TPW; ++q) {
-        const long long t = t0 + q;
-        const int src = ((q * NP + (lane < NP ? lane : 0)) % NV) * SPREAD;
-        const float sum = __shfl_sync(0xffffffffu, v[0], src);
-        if (t < a.T) {  // warp-uniform
-          float r[1] = {0.f};
-          if (lane < N) {
-            r[0] = a.logit_bias ? __fadd_rn(sum, a.logit_bias[lane]) : sum;
-            if (a.logits_out) a.logits_out[t * N + lane] = r[0];
-          }
-          select_token<1>(r, lane, t, a, psum, bcount);
-        }
-      }
-    }
+    if (wi == 0) select_group<NP, TPW>(v[0], lane, t0, a, psum, bcount);
   }
   __syncthreads();
   finish_block<1>(psum, wprob, bcount, a);
@@ -483,6 +502,113 @@ __global__ void __launch_bounds__(kThreads) router_tiled_kernel(const RouterArgs
   finish_block<EJ>(psum, wprob, bcount, a);
 }
 
+// ---------------------------------------------------------------------------
+// Few experts with bf16 tokens and large batches (N <= 16, T >= 2048, the
+// router rows within kStreamMaxSmem): the block first copies W_r into
+// shared memory with cp.async (NP rows of d bf16, rows past N zero-filled)
+// -- issued before it waits on the kernel ahead of it in the stream, as
+// nothing in the layer writes W_r -- and then each warp streams whole groups
+// of TPW = 2 tokens: lane l takes
+// the 16-byte vectors l, l+32, ... of both rows, loaded kStreamChunk at a
+// time with the next chunk in flight while the current one is used, and
+// dots each against the NP router rows read from shared memory (32 lanes
+// read 512 consecutive bytes: no bank conflicts). Per vector and expert that
+// is one shared load and its conversion for both tokens, against an L1
+// round trip per expert and vector in router_small_kernel. Two tokens a
+// warp and two blocks an SM keep 16 warps' loads in flight; a variant with
+// fp32 router rows, four tokens a warp and packed FMAs issued a third of
+// the instructions but had half the warps and ran 45% longer. The
+// reduction, selection and statistics are router_small_kernel's.
+constexpr int kStreamTPW = 2;
+constexpr int kStreamChunk = 3;
+constexpr size_t kStreamMaxSmem = 160 * 1024;
+// Resident blocks per SM: two with 8 router rows (64 KB at d = 4096), one
+// with 16.
+__host__ __device__ constexpr int stream_blocks_per_sm(int NP) { return NP <= 8 ? 2 : 1; }
+
+template <int NP>
+__global__ void __launch_bounds__(kThreads, stream_blocks_per_sm(NP))
+    router_stream_kernel(const RouterArgs a) {
+  constexpr int TPW = kStreamTPW;
+  constexpr int NV = NP * TPW;
+  constexpr int CH = kStreamChunk;
+  static_assert(NV == 16 || NV == 32, "reduce-scatter assumes 16 or 32 values");
+  extern __shared__ uint4 w_sm[];  // [NP][vec]
+  __shared__ float wprob[kWarps * 32];
+  __shared__ int bcount[32];
+  const int vec = a.d / 8;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  {  // global -> shared copies, all in flight at once; rows past N are zero-filled
+    const uint4* w = static_cast<const uint4*>(a.w);
+    const int nw = a.N * vec;
+    for (int i = threadIdx.x; i < NP * vec; i += kThreads) {
+      const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(w_sm + i));
+      const uint4* src = w + (i < nw ? i : 0);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                   "r"(i < nw ? 16 : 0)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  if (threadIdx.x < 32) bcount[threadIdx.x] = 0;
+  pdl_wait();
+  pdl_trigger();
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+  const uint4* x = static_cast<const uint4*>(a.x);
+  float psum[1] = {0.f};
+  const long long groups = (a.T + TPW - 1) / TPW;
+  for (long long g = (long long)blockIdx.x * kWarps + warp; g < groups;
+       g += (long long)gridDim.x * kWarps) {  // warp-uniform
+    const long long t0 = g * TPW;
+    const uint4* xr[TPW];
+#pragma unroll
+    for (int q = 0; q < TPW; ++q) xr[q] = x + (t0 + q < a.T ? t0 + q : t0) * vec;
+    float v[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = 0.f;
+    auto load = [&](int v0, uint4 (&buf)[CH][TPW]) {
+#pragma unroll
+      for (int c = 0; c < CH; ++c)
+#pragma unroll
+        for (int q = 0; q < TPW; ++q) {
+          const int vv = v0 + 32 * c;
+          buf[c][q] = (vv < vec && t0 + q < a.T) ? __ldg(xr[q] + vv) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    uint4 cur[CH][TPW], nxt[CH][TPW];
+    load(lane, cur);
+    for (int v0 = lane; v0 < vec; v0 += 32 * CH) {
+      load(v0 + 32 * CH, nxt);  // the next chunk in flight while this one is used
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int vv = v0 + 32 * c;
+        if (vv >= vec) break;
+        float xf[TPW][8];
+#pragma unroll
+        for (int q = 0; q < TPW; ++q) V16<__nv_bfloat16>::cvt(cur[c][q], xf[q]);
+#pragma unroll
+        for (int e = 0; e < NP; ++e) {
+          float wf[8];
+          V16<__nv_bfloat16>::cvt(w_sm[e * vec + vv], wf);
+#pragma unroll
+          for (int q = 0; q < TPW; ++q)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[q * NP + e] = fmaf(xf[q][i], wf[i], v[q * NP + e]);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < CH; ++c)
+#pragma unroll
+        for (int q = 0; q < TPW; ++q) cur[c][q] = nxt[c][q];
+    }
+    reduce_scatter<NV>(v, lane);
+    select_group<NP, TPW>(v[0], lane, t0, a, psum, bcount);
+  }
+  __syncthreads();
+  finish_block<1>(psum, wprob, bcount, a);
+}
+
 // prob_sum[e] = sum over blocks, in block order.
 
 template <typename K>
@@ -495,6 +621,27 @@ cudaError_t launch_k(K kernel, const RouterArgs& a, int grid, size_t smem, cudaS
 
 bool use_small(const moe_config& c, const float* logits_in) {
   return logits_in == nullptr && c.n_experts <= 32;
+}
+
+// The streaming kernel: bf16 tokens, up to 16 experts, the router rows in
+// shared memory.
+int stream_np(const moe_config& c) { return c.n_experts <= 8 ? 8 : 16; }
+size_t stream_smem(const moe_config& c) {  // bf16 router rows
+  return (size_t)stream_np(c) * (size_t)c.d_model * 2;
+}
+// Only for batches that give every SM's warps token pairs of their own;
+// decode-sized batches keep router_small_kernel, which spreads a token's
+// row over up to 8 warps.
+constexpr int kStreamMinTokens = 2048;
+bool use_stream(const moe_config& c, const float* logits_in) {
+  return use_small(c, logits_in) && c.dtype == MOE_BF16 && c.n_experts <= 16 &&
+         stream_smem(c) <= kStreamMaxSmem && c.T >= kStreamMinTokens;
+}
+int stream_grid(const moe_config& c) {  // as many blocks as are resident at once
+  const long long groups = ceil_div(c.T, kStreamTPW);
+  const int blocks = ceil_div(groups, kWarps);
+  const int cap = stream_blocks_per_sm(stream_np(c)) * num_sms();
+  return blocks < cap ? blocks : cap;
 }
 
 // Blocks of the router launch; router_partials_bytes() sizes the partials
@@ -510,6 +657,7 @@ int router_small_wsplit(const moe_config& c) {
 }
 
 int router_grid(const moe_config& c, const float* logits_in) {
+  if (use_stream(c, logits_in)) return stream_grid(c);
   if (use_small(c, logits_in)) {
     // one round of kWarps / wsplit token groups per block, at most 4 blocks per SM
     const int tpw = c.n_experts <= 8 ? 2 : 1;
@@ -522,6 +670,21 @@ int router_grid(const moe_config& c, const float* logits_in) {
 
 template <typename TX>
 cudaError_t launch_dtype(const moe_config& c, const RouterArgs& a, int grid, cudaStream_t s) {
+  if (use_stream(c, a.logits_in)) {
+    const size_t smem = stream_smem(c);
+    if (stream_np(c) == 8) {
+      cudaError_t e = cudaFuncSetAttribute(router_stream_kernel<8>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      ProfScope p(K_ROUTER, s);
+      return launch_pdl(router_stream_kernel<8>, dim3(grid), dim3(kThreads), smem, s, 1, a);
+    }
+    cudaError_t e = cudaFuncSetAttribute(router_stream_kernel<16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    ProfScope p(K_ROUTER, s);
+    return launch_pdl(router_stream_kernel<16>, dim3(grid), dim3(kThreads), smem, s, 1, a);
+  }
   if (use_small(c, a.logits_in)) {
     const int ws = router_small_wsplit(c);
     ProfScope p(K_ROUTER, s);
