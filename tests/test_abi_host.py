@@ -164,6 +164,67 @@ def test_host_rejections_launch_nothing(lib):
     assert moe.launch_count() == before
 
 
+def test_quantized_layers_host_rejections(lib):
+    """FP8 and NVFP4 entry points: sizes, shapes, null and misaligned
+    pointers and short workspaces are refused on the host, before any CUDA
+    call (fake addresses are never dereferenced)."""
+    before = moe.launch_count()
+    A = 0x10000
+    ok = cfg(T=64, d_model=256, n_experts=4, top_k=2, d_ff=256)
+    # workspace sizes: zero for what is not supported
+    assert moe.workspace_size(ok, "layer_fp8") > 0
+    assert moe.workspace_size(ok, "layer_nvfp4") > 0
+    assert moe.workspace_size(cfg(dtype=moe.MOE_F32, d_model=256, d_ff=256), "layer_nvfp4") == 0
+    assert moe.workspace_size(cfg(d_model=256, d_ff=320), "layer_nvfp4") > 0
+    for d, f in ((256, 200), (200, 256), (128, 256), (256, 128)):
+        assert moe.workspace_size(cfg(d_model=d, d_ff=f), "layer_nvfp4") == 0, (d, f)
+    # scale stride: cols / 16 rounded up to 16 bytes
+    assert [moe.moe_nvfp4_scale_stride(c) for c in (16, 256, 320, 4096, 14336, 0, -16)] == \
+        [16, 16, 32, 256, 896, 0, 0]
+    # quantizers
+    for fn in (lib.moe_quantize_fp8,):
+        assert fn(4, 12, _P(A), _P(A), _P(A), None) == moe.MOE_ERR_INVALID_ARG      # cols % 8
+        assert fn(4, 16, None, _P(A), _P(A), None) == moe.MOE_ERR_INVALID_ARG
+        assert fn(4, 16, _P(A + 8), _P(A), _P(A), None) == moe.MOE_ERR_MISALIGNED
+        assert fn(0, 16, None, None, None, None) == moe.MOE_OK                      # nothing to do
+    q4 = lib.moe_quantize_nvfp4
+    assert q4(4, 24, _P(A), _P(A), _P(A), _P(A), None) == moe.MOE_ERR_INVALID_ARG   # cols % 16
+    assert q4(-1, 32, _P(A), _P(A), _P(A), _P(A), None) == moe.MOE_ERR_INVALID_ARG
+    assert q4(4, 32, _P(A), _P(A), None, _P(A), None) == moe.MOE_ERR_INVALID_ARG    # no scales
+    assert q4(4, 32, _P(A), _P(A), _P(A + 4), _P(A), None) == moe.MOE_ERR_MISALIGNED
+    assert q4(0, 32, None, None, None, None, None) == moe.MOE_OK
+    # the NVFP4 layer: fp32, unsupported shapes, null weights, short workspace
+    w9 = [_P(A)] * 9
+    tail = [_P(A), None, None, None, None]  # y, topk_idx, topk_w, counts, prob_sum
+    L = lib.moe_layer_forward_nvfp4
+    assert L(ctypes.byref(cfg(dtype=moe.MOE_F32, d_model=256, d_ff=256)), _P(A), _P(A), None, None,
+             *w9, *tail, _P(A), 1 << 40, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L(ctypes.byref(cfg(d_model=256, d_ff=192)), _P(A), _P(A), None, None, *w9, *tail,
+             _P(A), 1 << 40, None) == moe.MOE_ERR_UNSUPPORTED
+    bad = list(w9)
+    bad[4] = None  # wu_sf
+    assert L(ctypes.byref(ok), _P(A), _P(A), None, None, *bad, *tail, _P(A), 1 << 40,
+             None) == moe.MOE_ERR_INVALID_ARG
+    bad = list(w9)
+    bad[7] = _P(A + 8)  # wd_sf
+    assert L(ctypes.byref(ok), _P(A), _P(A), None, None, *bad, *tail, _P(A), 1 << 40,
+             None) == moe.MOE_ERR_MISALIGNED
+    assert L(ctypes.byref(ok), _P(A), _P(A), None, None, *w9, *tail, _P(A), 64,
+             None) == moe.MOE_ERR_WORKSPACE
+    # the FP8 layer
+    w6 = [_P(A)] * 6
+    F8 = lib.moe_layer_forward_fp8
+    assert F8(ctypes.byref(cfg(dtype=moe.MOE_F32, d_model=256, d_ff=256)), _P(A), _P(A), None, None,
+              *w6, *tail, _P(A), 1 << 40, None) == moe.MOE_ERR_UNSUPPORTED
+    bad = list(w6)
+    bad[1] = None
+    assert F8(ctypes.byref(ok), _P(A), _P(A), None, None, *bad, *tail, _P(A), 1 << 40,
+              None) == moe.MOE_ERR_INVALID_ARG
+    assert F8(ctypes.byref(ok), _P(A), _P(A), None, None, *w6, *tail, _P(A), 64,
+              None) == moe.MOE_ERR_WORKSPACE
+    assert moe.launch_count() == before
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     """The product binding has no fallback: a missing library is an error."""
     monkeypatch.setattr(moe, "LIB_PATH", str(tmp_path / "missing.so"))
