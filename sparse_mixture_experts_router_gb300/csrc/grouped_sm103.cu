@@ -114,7 +114,9 @@ struct Op {
   static constexpr int NACC = OP == OP_NVF4 ? 1 : NUM_ACC;
   static constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024;  // + 1 KB alignment slack
   // NVFP4 adds a warp (the last) that rearranges each stage's block scales
-  static constexpr int THREADS = G_THREADS + (OP == OP_NVF4 ? 32 : 0);
+  // NVFP4 adds four warps (the last), one per TMEM lane quarter, that write
+  // each stage's block scales into Tensor Memory
+  static constexpr int THREADS = G_THREADS + (OP == OP_NVF4 ? 128 : 0);
 };
 // TMEM columns of the NVFP4 block scales: two buffers (alternate K blocks)
 // of 64 columns after the accumulator, A's 16 then B's 32 (4 and 8 a MMA).
@@ -181,7 +183,7 @@ struct GemmArgs {
 struct __align__(8) SharedState {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
-  uint64_t sf_ready[STAGES];  // NVFP4: the stage's block scales are rearranged
+  uint64_t sf_ready[STAGES];  // NVFP4: the stage's block scales are in Tensor Memory
   uint64_t acc_full[NUM_ACC];
   uint64_t acc_empty[NUM_ACC];
   uint64_t drain;
@@ -488,22 +490,42 @@ struct SfMaps {
   CUtensorMap a, a_shared, b0, b1;
 };
 
-// NVFP4: rearranges the block scales of 128 rows, as TMA left them (row r
-// at r*16: its four 32-bit words are the scales of the four MMAs of the
-// block, four 16-element groups each), in place into four 512-byte units,
-// one per MMA, where the 16 bytes of unit row l hold the words of rows l,
-// l+32, l+64 and l+96. That is the layout tcgen05.cp .32x128b.warpx4 turns
-// into the MMA's scale-factor columns (row m at column m/32 of every lane
-// congruent to m mod 32). Executed by a full warp.
-__device__ __forceinline__ void sf_rearrange(uint32_t base, int lane) {
-  uint4 v[4];
+// NVFP4: one lane quarter's copy of a stage's block scales in Tensor
+// Memory. The stage holds them as TMA left them: row r of A (128 rows) at
+// sf + r*16 and row r of B (256 rows) at sf + 2048 + r*16, the four 32-bit
+// words of a row being the scales of the block's four MMAs (four
+// 16-element groups each). The block-scaled MMA reads row m's word from
+// column m/32 of the lanes congruent to m mod 32 -- in every lane quarter
+// -- so lane l of the quarter gets, for MMA j, the words of rows l + 32c:
+// A at column sfa + 4j + c (c < 4), B at column sfa + 16 + 8j + c (c < 8).
+// Executed by a full warp; the lane field of sfa_t is the warp's quarter.
+__device__ __forceinline__ void sf_store_quarter(uint32_t sf, uint32_t sfa_t, int lane) {
+  uint32_t va[16], vb[32];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) v[c] = ptx::ld_shared_v4(base + (uint32_t)(lane + 32 * c) * 16u);
-  __syncwarp();
-  ptx::st_shared_v4(base + 0 * 512 + lane * 16, v[0].x, v[1].x, v[2].x, v[3].x);
-  ptx::st_shared_v4(base + 1 * 512 + lane * 16, v[0].y, v[1].y, v[2].y, v[3].y);
-  ptx::st_shared_v4(base + 2 * 512 + lane * 16, v[0].z, v[1].z, v[2].z, v[3].z);
-  ptx::st_shared_v4(base + 3 * 512 + lane * 16, v[0].w, v[1].w, v[2].w, v[3].w);
+  for (int c = 0; c < 4; ++c) {
+    const uint4 w = ptx::ld_shared_v4(sf + (uint32_t)(lane + 32 * c) * 16u);
+    va[c] = w.x;
+    va[4 + c] = w.y;
+    va[8 + c] = w.z;
+    va[12 + c] = w.w;
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 w = ptx::ld_shared_v4(sf + 2048u + (uint32_t)(lane + 32 * c) * 16u);
+    vb[c] = w.x;
+    vb[8 + c] = w.y;
+    vb[16 + c] = w.z;
+    vb[24 + c] = w.w;
+  }
+  uint32_t lo[16], hi[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    lo[i] = vb[i];
+    hi[i] = vb[16 + i];
+  }
+  ptx::tmem_st16(sfa_t, va);
+  ptx::tmem_st16(sfa_t + 16, lo);
+  ptx::tmem_st16(sfa_t + 32, hi);
 }
 
 template <int EPI, int OP>
@@ -527,7 +549,7 @@ __global__ void __launch_bounds__(Op<OP>::THREADS, 1)
     for (int i = 0; i < STAGES; ++i) {
       ptx::mbar_init(ptx::smem_addr(&st.full[i]), 1);
       ptx::mbar_init(ptx::smem_addr(&st.empty[i]), 1);
-      ptx::mbar_init(ptx::smem_addr(&st.sf_ready[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&st.sf_ready[i]), OP == OP_NVF4 ? 4 : 1);
     }
     for (int i = 0; i < NUM_ACC; ++i) {
       ptx::mbar_init(ptx::smem_addr(&st.acc_full[i]), 1);
@@ -641,10 +663,10 @@ __global__ void __launch_bounds__(Op<OP>::THREADS, 1)
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer --
     if constexpr (OP == OP_NVF4) {
-      // Lane 0 waits until a stage's block scales are rearranged (the last
-      // warp, below), copies them into TMEM and issues the block-scaled MMAs.
-      // One accumulator; the scales of consecutive K blocks alternate
-      // between two TMEM buffers.
+      // Lane 0 waits until a stage's operands have landed and its block
+      // scales are in TMEM (the last four warps, below), then issues the
+      // block-scaled MMAs. One accumulator; the scales of consecutive K
+      // blocks alternate between two TMEM buffers.
       if (lane == 0) {
         int stage = 0;
         uint32_t phase = 0, acc_phase = 0, kcount = 0;
@@ -659,23 +681,16 @@ __global__ void __launch_bounds__(Op<OP>::THREADS, 1)
           const int split = unit % S;
           const int kb0 = kb_begin(split, S, KB), kb1 = kb_begin(split + 1, S, KB);
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!wait_phase(ptx::smem_addr(&st.sf_ready[stage]), phase, abort_flag,
+            if (!wait_phase(ptx::smem_addr(&st.full[stage]), phase, abort_flag, args.status) ||
+                !wait_phase(ptx::smem_addr(&st.sf_ready[stage]), phase, abort_flag,
                             args.status)) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
             const uint32_t a_src = ring + stage * Op<OP>::STAGE;
-            const uint32_t sf_src = a_src + STAGE_BYTES;  // A's scales, then B's two halves
             const uint32_t sfa_t = tmem_base + SF_TMEM_COL + (kcount & 1u) * SF_TMEM_BUF;
             const uint32_t sfb_t = sfa_t + 16;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              ptx::tmem_cp_32x128b_x4(sfa_t + 4 * k, ptx::sdesc_rows16(sf_src + 512 * k));
-              ptx::tmem_cp_32x128b_x4(sfb_t + 8 * k, ptx::sdesc_rows16(sf_src + 2048 + 512 * k));
-              ptx::tmem_cp_32x128b_x4(sfb_t + 8 * k + 4,
-                                      ptx::sdesc_rows16(sf_src + 4096 + 512 * k));
-            }
             const uint64_t adesc = ptx::sdesc_k128(a_src);
             const uint64_t bdesc = ptx::sdesc_k128(a_src + A_BYTES);
 #pragma unroll
@@ -755,30 +770,40 @@ __global__ void __launch_bounds__(Op<OP>::THREADS, 1)
         drain_wait(ptx::smem_addr(&st.drain), 0);
       }
     }
-  } else if (OP == OP_NVF4 && warp == G_THREADS / 32) {
-    // ------------------------------------------- NVFP4 block-scale warp --
-    // Waits for each stage, rearranges its block scales for tcgen05.cp
-    // (sf_rearrange) and hands the stage to the MMA thread (sf_ready), so
-    // the MMA issue never waits on this shared-memory work.
+  } else if (OP == OP_NVF4 && warp >= G_THREADS / 32) {
+    // ------------------------------------------ NVFP4 block-scale warps --
+    // One warp per TMEM lane quarter writes each stage's block scales into
+    // its quarter of the stage's scale buffer (sf_store_quarter) and hands
+    // the stage to the MMA thread (sf_ready, four arrivals), so the tensor
+    // pipe only runs MMAs. A buffer is rewritten only after the MMAs of the
+    // K block that last used it -- two blocks back -- have completed (that
+    // block's empty barrier).
+    const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
     int stage = 0;
-    uint32_t phase = 0;
+    uint32_t phase = 0, kcount = 0;
     bool ok = true;
     for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x) {
       const int split = unit % S;
       const int kb1 = kb_begin(split + 1, S, KB);
       for (int kb = kb_begin(split, S, KB); kb < kb1; ++kb) {
         ok = wait_phase(ptx::smem_addr(&st.full[stage]), phase, abort_flag, args.status);
+        if (ok && kcount >= 2) {
+          const uint32_t k2 = kcount - 2;
+          ok = wait_phase(ptx::smem_addr(&st.empty[k2 % STAGES]), (k2 / STAGES) & 1u, abort_flag,
+                          args.status);
+        }
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
-        const uint32_t sf_src = ring + stage * Op<OP>::STAGE + STAGE_BYTES;
-        sf_rearrange(sf_src, lane);
-        sf_rearrange(sf_src + 2048, lane);
-        sf_rearrange(sf_src + 4096, lane);
-        ptx::fence_proxy_async_smem();  // generic writes before tcgen05.cp reads them
+        ptx::tc_fence_after();
+        sf_store_quarter(ring + stage * Op<OP>::STAGE + STAGE_BYTES,
+                         tmem_base + lanes + SF_TMEM_COL + (kcount & 1u) * SF_TMEM_BUF, lane);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&st.sf_ready[stage]));
+        ++kcount;
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
