@@ -33,6 +33,7 @@ METRIC = "MoE layer tokens/s; grouped-GEMM % bf16 tensor peak; decode % HBM BW"
 FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 UNIT = "tokens/s"
 AUX_ALPHA = 0.01  # the balance loss's weight alpha
+L2_BYTES = 129 * 1024 * 1024  # GB300 L2
 # Nominal dense tensor rates relative to bf16 (2.25 PFLOP/s): fp8 4.5, fp4 13.5.
 QUANT_PEAK_RATIO = {None: 1.0, "fp8": 4.5 / 2.25, "nvfp4": 13.5 / 2.25}
 
@@ -213,9 +214,10 @@ def gemm_bytes(w, counts, quant=None):
             return r * cols + 4 * r
         if quant == "nvfp4":
             return r * cols // 2 + r * nvfp4_scale_stride(cols) + 4 * r
-        return r * cols * 2
-    gu = active * 2 * mat(f, d) + mat(rows, d) + rows * f * 2
-    dn = active * mat(d, f) + mat(rows, f) + rows * d * 2
+        return r * cols * eb
+    eb = 4 if w.dtype == "f32" else 2  # activations and unquantized weights
+    gu = active * 2 * mat(f, d) + mat(rows, d) + rows * f * eb
+    dn = active * mat(d, f) + mat(rows, f) + rows * d * eb
     return gu, dn
 
 
@@ -300,11 +302,20 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     pk = peaks()
     w = WORKLOADS[args.workload](synth)
+    if w.dtype == "f32" and args.quant:
+        raise SystemExit("--fp8 / --nvfp4 take bf16 workloads")
     inp = synth.make_inputs(w, dev, seed=w.seed + 1000 * rank)
+    eb = 4 if w.dtype == "f32" else 2
     cfg = moe.config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k, d_ff=w.d_ff,
-                     n_shared=w.n_shared, dtype=moe.MOE_BF16, gate_mode=w.gate_mode,
-                     capacity=capacity_of(w))
-    y = torch.empty(w.T, w.d_model, dtype=torch.bfloat16, device=dev)
+                     n_shared=w.n_shared, dtype=moe.MOE_F32 if w.dtype == "f32" else moe.MOE_BF16,
+                     gate_mode=w.gate_mode, capacity=capacity_of(w))
+    y = torch.empty(w.T, w.d_model, dtype=w.torch_dtype, device=dev)
+    # Inputs that fit in L2 (the tiny fp32 layer) are timed step by step with
+    # L2 flushed (a 256 MB write) before each step; larger ones stream their
+    # weights from HBM every step anyway.
+    in_bytes = sum(t.numel() * t.element_size() for t in inp.values() if t is not None)
+    flush_l2 = in_bytes < 2 * L2_BYTES
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush_l2 else None
     idx = torch.empty(w.T, w.top_k, dtype=torch.int32, device=dev)
     tw = torch.empty(w.T, w.top_k, dtype=torch.float32, device=dev)
     counts = torch.empty(w.n_experts, dtype=torch.int32, device=dev)
@@ -335,20 +346,32 @@ def run_ours(args):
     barrier(ws)
     torch.cuda.synchronize(dev)
     clocks.mark("t0")
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step(inp["x"])
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+    if flush_l2:
+        ms_local = 0.0
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step(inp["x"])
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms_local += e0.elapsed_time(e1)
+    else:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step(inp["x"])
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_local = e0.elapsed_time(e1)
     clocks.mark("t1")
     barrier(ws)
     launches = moe.launch_count() - launches0
     kern_timed = moe.profile_collect()
     moe.profile_enable(False)
     clk = clocks.stop()
-    ms_local = e0.elapsed_time(e1)
     ms_total = reduce_max(ms_local, ws)
     ms_step = ms_total / args.steps
     value = ws * w.T * args.steps / (ms_total / 1e3)
@@ -359,7 +382,7 @@ def run_ours(args):
     # step i+1 / i-1 overlap the forward of step i (separate copy streams,
     # two device buffers each, ordered with events), as a serving loop does.
     x_host = inp["x"].cpu().pin_memory()
-    y_host = [torch.empty(w.T, w.d_model, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    y_host = [torch.empty(w.T, w.d_model, dtype=w.torch_dtype).pin_memory() for _ in range(2)]
     x_dev = [torch.empty_like(inp["x"]) for _ in range(2)]
     y_dev = [torch.empty_like(y) for _ in range(2)]
     h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -397,7 +420,7 @@ def run_ours(args):
     barrier(ws)
     e2e_ms = reduce_max(e2e_s * 1e3, ws)
     e2e_value = ws * w.T * args.steps / (e2e_ms / 1e3)
-    bytes_io = w.T * w.d_model * 2
+    bytes_io = w.T * w.d_model * eb
 
     # ---- every kernel bracketed by events, in a separate pass ------------------
     # (shares and per-kernel rates; the step time above is taken without them)
@@ -450,6 +473,18 @@ def run_ours(args):
             per_kernel[name]["hbm_frac"] = round(b / (ms / 1e3) / 1e9 / pk["hbm"], 4)
         gemm_tflops = (f_gu + f_dn) / ((gu_ms + dn_ms) / 1e3) / 1e12
         ach = per_kernel["gate_up"]["tflops"]
+    if gu_ms is not None and w.dtype == "f32":
+        # fp32 layers run their expert products on the CUDA cores (tcgen05 has
+        # no fp32-operand kind): the peak is the fp32 FMA rate
+        roofline = {"bound": "alu", "kernel": "gate_up (fp32 CUDA-core expert GEMM, stage 1)",
+                    "achieved": round(ach, 3), "peak": round(FP32_ALU_PEAK_TFLOPS, 1),
+                    "unit": "TFLOP/s", "frac": round(ach / FP32_ALU_PEAK_TFLOPS, 5),
+                    "traffic": None,
+                    "peak_source": "152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz",
+                    "algorithmic_flops_per_launch": f_gu,
+                    "note": "a few thousand tokens' worth of work: bound by launch and "
+                            "memory latency, reported for its latency"}
+    elif gu_ms is not None:
         roofline = {"bound": "tensor", "kernel": "gate_up (grouped SwiGLU gate+up GEMM)",
                     "achieved": round(ach, 1), "peak": round(tpk, 1), "unit": "TFLOP/s",
                     "frac": round(ach / tpk, 4),
@@ -464,9 +499,9 @@ def run_ours(args):
                     "grouped_gemm_both_kernels_frac": round(gemm_tflops / tpk, 4)}
     # HBM-bound kernels of the step against the copy bandwidth
     P = w.T * w.top_k
-    hb = {"router_topk": w.T * w.d_model * 2 + w.n_experts * w.d_model * 2 + P * 8,
-          "permute_gather": 2 * P * w.d_model * 2 + P * 4,
-          "combine": (P + w.n_shared * w.T) * w.d_model * 2 + w.T * w.d_model * 2 + P * 4}
+    hb = {"router_topk": w.T * w.d_model * eb + w.n_experts * w.d_model * eb + P * 8,
+          "permute_gather": 2 * P * w.d_model * eb + P * 4,
+          "combine": (P + w.n_shared * w.T) * w.d_model * eb + w.T * w.d_model * eb + P * 4}
     if "router_topk" in per_kernel:  # the router's score contraction
         fl = 2.0 * w.T * w.n_experts * w.d_model
         tf = fl / (per_kernel["router_topk"]["ms_per_launch"] / 1e3) / 1e12
@@ -510,9 +545,10 @@ def run_ours(args):
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": {None: "bf16", "fp8": "e4m3 experts (row scales), bf16 tokens and router",
-                      "nvfp4": "nvfp4 experts (e2m1, e4m3 scales of 16-element blocks, row "
-                               "scales), bf16 tokens and router"}[args.quant],
+            "dtype": ("f32" if w.dtype == "f32" else
+                      {None: "bf16", "fp8": "e4m3 experts (row scales), bf16 tokens and router",
+                       "nvfp4": "nvfp4 experts (e2m1, e4m3 scales of 16-element blocks, row "
+                                "scales), bf16 tokens and router"}[args.quant]),
             "data": "synthetic (seeded N(0,1) tokens, N(0,0.02^2) random-init weights)",
             "config": {"workload": w.name, "T": w.T, "d_model": w.d_model,
                        "n_experts": w.n_experts, "top_k": w.top_k, "d_ff": w.d_ff,
@@ -522,7 +558,11 @@ def run_ours(args):
                        "selection_bias": w.sel_bias, "zipf_offset_s": w.zipf_s or None,
                        "capacity": capacity_of(w) or None,
                        "parallelism": f"replicas x{ws} (per-token layer, no collective)",
-                       "l2": f"inputs larger than L2: {wb / 1e9:.2f} GB of expert weights read every step"},
+                       "l2": (f"inputs ({in_bytes / 1e6:.2f} MB) fit in L2: L2 flushed (256 MB "
+                              "write) before every timed step, each step timed on its own"
+                              if flush_l2 else
+                              f"inputs larger than L2: {wb / 1e9:.2f} GB of expert weights read "
+                              "every step")},
             "routing": routing,
             "tflops_grouped_gemm": round(gemm_tflops, 1),
             "roofline": roofline,
@@ -781,6 +821,7 @@ def run_reference(args):
 
 DEFAULT_WORKLOAD = "mixtral_8x7b_prefill"
 WORKLOADS = {
+    "tiny_fp32": lambda synth: synth.TINY,
     "mixtral_8x7b_prefill": lambda synth: synth.MIXTRAL_PREFILL,
     "deepseek_v3_moe": lambda synth: synth.DEEPSEEK_V3,
     "zipf_imbalanced": lambda synth: synth.ZIPF,
