@@ -70,29 +70,44 @@ def reduce_max(v: float, ws: int) -> float:
     return float(t.item())
 
 
+def kernel_source_key():
+    """First 16 hex digits of the sha256 of the code lines of the grouped GEMM
+    sources (csrc/grouped_sm103.cu then csrc/sm103_ptx.cuh; blank lines and
+    lines that are only a // comment left out, so a comment edit keeps the
+    key). None if the sources cannot be read."""
+    import hashlib
+    csrc = os.path.join(ROOT, "sparse_mixture_experts_router_gb300", "csrc")
+    h = hashlib.sha256()
+    try:
+        for f in ("grouped_sm103.cu", "sm103_ptx.cuh"):
+            for line in open(os.path.join(csrc, f), encoding="utf-8"):
+                t = line.strip()
+                if t and not t.startswith("//"):
+                    h.update((t + "\n").encode())
+    except OSError:
+        return None
+    return h.hexdigest()[:16]
+
+
 def recorded_traffic(quant=None):
     """DRAM bytes per gate/up launch from the committed ncu summary (bf16,
-    E4M3 or NVFP4 kernel), or None when the kernel sources changed since that
-    capture."""
-    import hashlib
+    E4M3 or NVFP4 kernel), or None when the kernel code changed since that
+    capture (kernel_source_key differs from the one recorded there)."""
     prof = os.path.join(ROOT, "profiles", {None: "grouped_gemm_mixtral_8x7b_prefill.md",
                                            "fp8": "grouped_gemm_fp8_mixtral_8x7b_prefill.md",
                                            "nvfp4": "grouped_gemm_nvfp4_mixtral_8x7b_prefill.md"}[quant])
-    csrc = os.path.join(ROOT, "sparse_mixture_experts_router_gb300", "csrc")
     try:
         text = open(prof).read()
-        h = hashlib.sha256()
-        for f in ("grouped_sm103.cu", "sm103_ptx.cuh"):
-            h.update(open(os.path.join(csrc, f), "rb").read())
     except OSError:
         return None
+    key = kernel_source_key()
     vals = {}
     for line in text.splitlines():
         if ":" in line and line.strip().split(":")[0] in ("gate_up_dram_bytes_per_launch",
                                                           "kernel_source_sha256"):
             k, v = line.strip().split(":", 1)
             vals[k] = v.strip()
-    if vals.get("kernel_source_sha256") != h.hexdigest()[:16]:
+    if key is None or vals.get("kernel_source_sha256") != key:
         return None
     try:
         return float(vals["gate_up_dram_bytes_per_launch"])

@@ -35,6 +35,11 @@
 //    warps per lane quarter, each taking half the columns), apply the SwiGLU
 //    or gate-weight epilogue and store bf16 rows, while the MMA warp fills
 //    the other accumulator.
+//  - NVFP4 operands (OP_NVF4, 1-CTA tiles, 448 threads): stages also carry
+//    the E4M3 block scales of their A and B rows; four more warps, one per
+//    TMEM lane quarter, write them into Tensor Memory with tcgen05.st, where
+//    the block-scaled MMA (kind::mxf4nvf4) reads them. The scales take 128
+//    TMEM columns, so this kind has one accumulator.
 //  - Every wait is bounded (2 s of %globaltimer). A wait that runs out
 //    records MOE_ERR_TIMEOUT in the status word and sets a shared abort flag
 //    that ends the other roles' loops; the producer then waits (bounded) for
