@@ -34,6 +34,7 @@ FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 UNIT = "tokens/s"
 AUX_ALPHA = 0.01  # the balance loss's weight alpha
 L2_BYTES = 129 * 1024 * 1024  # GB300 L2
+DECODE_MAX_T = 64  # batches up to this size stream the expert weights (decode)
 # Nominal dense tensor rates relative to bf16 (2.25 PFLOP/s): fp8 4.5, fp4 13.5.
 QUANT_PEAK_RATIO = {None: 1.0, "fp8": 4.5 / 2.25, "nvfp4": 13.5 / 2.25}
 
@@ -89,13 +90,24 @@ def kernel_source_key():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(quant=None):
-    """DRAM bytes per gate/up launch from the committed ncu summary (bf16,
-    E4M3 or NVFP4 kernel), or None when the kernel code changed since that
-    capture (kernel_source_key differs from the one recorded there)."""
-    prof = os.path.join(ROOT, "profiles", {None: "grouped_gemm_mixtral_8x7b_prefill.md",
-                                           "fp8": "grouped_gemm_fp8_mixtral_8x7b_prefill.md",
-                                           "nvfp4": "grouped_gemm_nvfp4_mixtral_8x7b_prefill.md"}[quant])
+# ncu summaries with a gate/up DRAM traffic figure: (operand kind, workload) -> file
+TRAFFIC_PROFILES = {
+    (None, "mixtral_8x7b_prefill"): "grouped_gemm_mixtral_8x7b_prefill.md",
+    ("fp8", "mixtral_8x7b_prefill"): "grouped_gemm_fp8_mixtral_8x7b_prefill.md",
+    ("nvfp4", "mixtral_8x7b_prefill"): "grouped_gemm_nvfp4_mixtral_8x7b_prefill.md",
+    (None, "mixtral_8x7b_decode_T64"): "decode_mixtral_8x7b_T64.md",
+}
+
+
+def recorded_traffic(quant, workload):
+    """DRAM bytes per gate/up launch from the committed ncu summary of this
+    operand kind and workload, or None when there is none or the kernel code
+    changed since that capture (kernel_source_key differs from the one
+    recorded there)."""
+    name = TRAFFIC_PROFILES.get((quant, workload))
+    if name is None:
+        return None
+    prof = os.path.join(ROOT, "profiles", name)
     try:
         text = open(prof).read()
     except OSError:
@@ -499,12 +511,23 @@ def run_ours(args):
                     "algorithmic_flops_per_launch": f_gu,
                     "note": "a few thousand tokens' worth of work: bound by launch and "
                             "memory latency, reported for its latency"}
+    elif gu_ms is not None and w.T <= DECODE_MAX_T:
+        # decode-sized batches stream the weights: the bound is HBM
+        gbs_gu = per_kernel["gate_up"]["gbs"]
+        roofline = {"bound": "hbm", "kernel": "gate_up (grouped SwiGLU gate+up GEMM, decode tiles)",
+                    "achieved": gbs_gu, "peak": round(pk["hbm"], 1), "unit": "GB/s",
+                    "frac": round(gbs_gu / pk["hbm"], 4),
+                    "traffic": (args.traffic if args.traffic is not None
+                                else recorded_traffic(args.quant, w.name)),
+                    "peak_source": f"{pk['source']} HBM copy",
+                    "algorithmic_bytes_per_launch": per_kernel["gate_up"]["algorithmic_bytes"],
+                    "tflops": round(ach, 1)}
     elif gu_ms is not None:
         roofline = {"bound": "tensor", "kernel": "gate_up (grouped SwiGLU gate+up GEMM)",
                     "achieved": round(ach, 1), "peak": round(tpk, 1), "unit": "TFLOP/s",
                     "frac": round(ach / tpk, 4),
                     "traffic": (args.traffic if args.traffic is not None
-                                else recorded_traffic(args.quant)),
+                                else recorded_traffic(args.quant, w.name)),
                     "peak_source": (f"{pk['source']} bf16 burst x {ratio:g} (nominal "
                                     f"{args.quant}/bf16 dense ratio)"
                                     if args.quant else f"{pk['source']} bf16 burst"),
