@@ -9,18 +9,16 @@
 // rounded to nearest even and saturated at +-448 (cvt.rn.satfinite); a row
 // of zeros gets s = 0 and codes 0. A code's value is decode(q) * s.
 //
-// One warp per row: the row's max |v| (or the one the gate/up epilogue
-// recorded for H), then 8 values per lane and step, 16 bytes of bf16 in and
-// 8 bytes of codes out. The same kernel gathers x_perm rows (row r reads
+// One warp per row (one block per row for up to kQBlockRows rows): the
+// row's max |v| (or the one the gate/up epilogue recorded for H), then 8
+// values per thread and step, 16 bytes of bf16 in and 8 bytes of codes out. The same kernel gathers x_perm rows (row r reads
 // token sorted_pair[r] / k) and clears the H maxima of the rows it feeds.
-#include "device_util.cuh"
-#include "moe_internal.h"
+#include "quant_rows.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kQThreads = 256;
-constexpr int kQWarps = kQThreads / 32;
+using namespace quant;
 
 // Two fp32 values to E4M3 codes: `lo` in the low byte, `hi` in the high one
 // (the instruction puts its first source in the upper half).
@@ -30,45 +28,15 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
-__global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(const QuantArgs a) {
-  const long long r = (long long)blockIdx.x * kQWarps + threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-  pdl_wait();
-  pdl_trigger();
-  if (r >= a.rows) return;
-  if (a.rows_dev && r >= (long long)__ldg(a.rows_dev)) return;  // past the rows in use
-  if (a.clear && lane < a.clear_n) a.clear[a.clear_base + lane * a.clear_stride + r] = 0u;
-  long long sr = r;
-  if (a.gather) {
-    const int p = __ldg(a.gather + r);
-    if (p < 0 || (long long)(p / a.k) >= a.src_rows) return;
-    sr = p / a.k;
-  }
-  const uint4* src = reinterpret_cast<const uint4*>(a.src + sr * a.cols);
+// Vectors v0, v0 + step, ... of row r (8 values each): codes, and the row
+// scale from the thread that has v0 = 0.
+__device__ __forceinline__ void quantize_vecs(const QuantArgs& a, long long r, const uint4* src,
+                                              float amax, int v0, int step) {
   const int nvec = a.cols / 8;
-  float amax;
-  if (a.amax_in) {
-    amax = __uint_as_float(__ldg(a.amax_in + r));
-  } else {
-    float m = 0.f;
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 q = __ldg(src + v);
-      float f[8];
-      bf16x2_to_f32(q.x, f[0], f[1]);
-      bf16x2_to_f32(q.y, f[2], f[3]);
-      bf16x2_to_f32(q.z, f[4], f[5]);
-      bf16x2_to_f32(q.w, f[6], f[7]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    amax = m;
-  }
   const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
-  if (lane == 0) a.scale[r] = __fdiv_rn(amax, 448.f);
+  if (v0 == 0) a.scale[r] = __fdiv_rn(amax, 448.f);
   uint2* dst = reinterpret_cast<uint2*>(a.q + r * a.cols);
-  for (int v = lane; v < nvec; v += 32) {
+  for (int v = v0; v < nvec; v += step) {
     if (amax == 0.f) {
       dst[v] = make_uint2(0u, 0u);
       continue;
@@ -86,11 +54,39 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(const QuantArg
   }
 }
 
+// Many rows: one warp a row.
+__global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(const QuantArgs a) {
+  const long long r = (long long)blockIdx.x * kQWarps + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  pdl_wait();
+  pdl_trigger();
+  const long long sr = source_row(a, r, lane);
+  if (sr < 0) return;
+  const uint4* src = reinterpret_cast<const uint4*>(a.src + sr * a.cols);
+  const float amax = a.amax_in ? __uint_as_float(__ldg(a.amax_in + r))
+                               : warp_max(partial_amax(src, lane, a.cols / 8, 32));
+  quantize_vecs(a, r, src, amax, lane, 32);
+}
+
+// Few rows: one block a row.
+__global__ void __launch_bounds__(kQThreads) quantize_row_block_kernel(const QuantArgs a) {
+  const long long r = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  const long long sr = source_row(a, r, threadIdx.x);
+  if (sr < 0) return;  // the same for the whole block
+  const uint4* src = reinterpret_cast<const uint4*>(a.src + sr * a.cols);
+  quantize_vecs(a, r, src, block_row_amax(a, r, src), threadIdx.x, kQThreads);
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_rows(const QuantArgs& a, cudaStream_t s) {
   if (a.rows <= 0) return cudaSuccess;
   ProfScope p(K_QUANTIZE, s);
+  if (a.rows <= kQBlockRows)
+    return launch_pdl(quantize_row_block_kernel, dim3((unsigned)a.rows), dim3(kQThreads), 0, s, 1,
+                      a);
   return launch_pdl(quantize_rows_kernel, dim3((unsigned)((a.rows + kQWarps - 1) / kQWarps)),
                     dim3(kQThreads), 0, s, 1, a);
 }

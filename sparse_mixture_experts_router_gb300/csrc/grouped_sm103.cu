@@ -118,7 +118,6 @@ struct Op {
   static constexpr int STAGE = STAGE_BYTES + SF_A + SF_B;  // 48 KB, or 54 KB for NVFP4
   static constexpr int NACC = OP == OP_NVF4 ? 1 : NUM_ACC;
   static constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024;  // + 1 KB alignment slack
-  // NVFP4 adds a warp (the last) that rearranges each stage's block scales
   // NVFP4 adds four warps (the last), one per TMEM lane quarter, that write
   // each stage's block scales into Tensor Memory
   static constexpr int THREADS = G_THREADS + (OP == OP_NVF4 ? 128 : 0);

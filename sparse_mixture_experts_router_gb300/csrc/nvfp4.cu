@@ -20,22 +20,21 @@
 // [rows][cols / 2]; block scales [rows][ld_sf] bytes with zeros past
 // cols / 16; row scales [rows] fp32.
 //
-// One warp per row: the row's max |v| (or the one the gate/up epilogue
-// recorded for H), then one 16-element block per lane and step: 32 bytes of
-// bf16 in, 8 bytes of codes and one scale byte out. The E2M1 rounding is the
+// One warp per row (one block per row for up to kQBlockRows rows): the
+// row's max |v| (or the one the gate/up epilogue recorded for H), then one
+// 16-element block per thread and step: 32 bytes of bf16 in, 8 bytes of
+// codes and one scale byte out. The E2M1 rounding is the
 // conversion instruction's (round to nearest even, saturating, the sign of a
 // value that rounds to zero kept), checked bit for bit against the oracle's
 // definition of the code. The same kernel gathers
 // x_perm rows (row r reads token sorted_pair[r] / k) and clears the H
 // maxima of the rows it feeds.
-#include "device_util.cuh"
-#include "moe_internal.h"
+#include "quant_rows.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kQThreads = 256;
-constexpr int kQWarps = kQThreads / 32;
+using namespace quant;
 
 // E4M3 code of a non-negative fp32 value, rounded to nearest even and
 // saturated at 448.
@@ -68,47 +67,17 @@ __device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v
   return r;
 }
 
-__global__ void __launch_bounds__(kQThreads) quantize_rows_nvf4_kernel(const QuantArgs a) {
-  const long long r = (long long)blockIdx.x * kQWarps + threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-  pdl_wait();
-  pdl_trigger();
-  if (r >= a.rows) return;
-  if (a.rows_dev && r >= (long long)__ldg(a.rows_dev)) return;  // past the rows in use
-  if (a.clear && lane < a.clear_n) a.clear[a.clear_base + lane * a.clear_stride + r] = 0u;
-  long long sr = r;
-  if (a.gather) {
-    const int p = __ldg(a.gather + r);
-    if (p < 0 || (long long)(p / a.k) >= a.src_rows) return;
-    sr = p / a.k;
-  }
-  const uint4* src = reinterpret_cast<const uint4*>(a.src + sr * a.cols);
+// Blocks b0, b0 + step, ... of row r: codes, block scales, and the zero
+// padding of the block-scale row.
+__device__ __forceinline__ void quantize_blocks(const QuantArgs& a, long long r, const uint4* src,
+                                                float amax, int b0, int step) {
   const int nb = a.cols / 16;  // blocks of 16 = two 16-byte vectors
-  float amax;
-  if (a.amax_in) {
-    amax = __uint_as_float(__ldg(a.amax_in + r));
-  } else {
-    float m = 0.f;
-    for (int v = lane; v < 2 * nb; v += 32) {
-      const uint4 q = __ldg(src + v);
-      float f[8];
-      bf16x2_to_f32(q.x, f[0], f[1]);
-      bf16x2_to_f32(q.y, f[2], f[3]);
-      bf16x2_to_f32(q.z, f[4], f[5]);
-      bf16x2_to_f32(q.w, f[6], f[7]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    amax = m;
-  }
   const float to_block = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
   const float to_code = amax > 0.f ? __fdiv_rn(2688.f, amax) : 0.f;
-  if (lane == 0) a.scale[r] = __fdiv_rn(amax, 2688.f);
+  if (b0 == 0) a.scale[r] = __fdiv_rn(amax, 2688.f);
   uint2* dst = reinterpret_cast<uint2*>(a.q + r * (a.cols / 2));
   uint8_t* sfrow = a.sf + r * a.ld_sf;
-  for (int b = lane; b < nb; b += 32) {
+  for (int b = b0; b < nb; b += step) {
     const uint4 q0 = __ldg(src + 2 * b), q1 = __ldg(src + 2 * b + 1);
     float f[16];
     bf16x2_to_f32(q0.x, f[0], f[1]);
@@ -135,7 +104,32 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_nvf4_kernel(const Qua
     dst[b] = make_uint2(w[0], w[1]);
     sfrow[b] = (uint8_t)bc;
   }
-  for (int b = nb + lane; b < a.ld_sf; b += 32) sfrow[b] = 0;
+  for (int b = nb + b0; b < a.ld_sf; b += step) sfrow[b] = 0;
+}
+
+// Many rows: one warp a row.
+__global__ void __launch_bounds__(kQThreads) quantize_rows_nvf4_kernel(const QuantArgs a) {
+  const long long r = (long long)blockIdx.x * kQWarps + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  pdl_wait();
+  pdl_trigger();
+  const long long sr = source_row(a, r, lane);
+  if (sr < 0) return;
+  const uint4* src = reinterpret_cast<const uint4*>(a.src + sr * a.cols);
+  const float amax = a.amax_in ? __uint_as_float(__ldg(a.amax_in + r))
+                               : warp_max(partial_amax(src, lane, a.cols / 8, 32));
+  quantize_blocks(a, r, src, amax, lane, 32);
+}
+
+// Few rows: one block a row.
+__global__ void __launch_bounds__(kQThreads) quantize_row_block_nvf4_kernel(const QuantArgs a) {
+  const long long r = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  const long long sr = source_row(a, r, threadIdx.x);
+  if (sr < 0) return;  // the same for the whole block
+  const uint4* src = reinterpret_cast<const uint4*>(a.src + sr * a.cols);
+  quantize_blocks(a, r, src, block_row_amax(a, r, src), threadIdx.x, kQThreads);
 }
 
 }  // namespace
@@ -143,6 +137,9 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_nvf4_kernel(const Qua
 cudaError_t launch_quantize_rows_nvf4(const QuantArgs& a, cudaStream_t s) {
   if (a.rows <= 0) return cudaSuccess;
   ProfScope p(K_QUANTIZE, s);
+  if (a.rows <= kQBlockRows)
+    return launch_pdl(quantize_row_block_nvf4_kernel, dim3((unsigned)a.rows), dim3(kQThreads), 0,
+                      s, 1, a);
   return launch_pdl(quantize_rows_nvf4_kernel, dim3((unsigned)((a.rows + kQWarps - 1) / kQWarps)),
                     dim3(kQThreads), 0, s, 1, a);
 }

@@ -31,9 +31,11 @@ def quantize(t):
     return q, sc
 
 
-def test_quantize_fp8_is_bit_exact(oracle):
+# 300 rows take the block-a-row kernel, 1300 the warp-a-row one
+@pytest.mark.parametrize("n_rows", [300, 1300])
+def test_quantize_fp8_is_bit_exact(oracle, n_rows):
     g = torch.Generator(device="cuda").manual_seed(5)
-    m = torch.randn(300, 264, generator=g, device="cuda") * 3
+    m = torch.randn(n_rows, 264, generator=g, device="cuda") * 3
     m[0] = 0.0
     m[1] = -0.0
     m[2, :8] = torch.tensor([448, 464, 1e4, -1e4, 2 ** -9, 2 ** -11, 1.0625, -1.1875])

@@ -12,7 +12,8 @@
   boundary may round the other way when the fp32 and fp64 sums differ,
   which the 2e-2 bar covers. The shapes cover K tails inside a 256-element
   block, partial N tiles, shared experts, capacity drops, the split-K path
-  of decode sizes and the full Mixtral- and DeepSeek-V3-shaped layers.
+  at two batch sizes, decode-sized batches and the full Mixtral- and
+  DeepSeek-V3-shaped layers.
 """
 import numpy as np
 import pytest
@@ -53,9 +54,11 @@ def test_scale_stride():
     assert moe.moe_nvfp4_scale_stride(0) == 0
 
 
-def test_quantize_nvfp4_is_bit_exact(oracle):
+# 300 rows take the block-a-row kernel, 1300 the warp-a-row one
+@pytest.mark.parametrize("n_rows", [300, 1300])
+def test_quantize_nvfp4_is_bit_exact(oracle, n_rows):
     g = torch.Generator(device="cuda").manual_seed(7)
-    m = torch.randn(300, 320, generator=g, device="cuda") * 3
+    m = torch.randn(n_rows, 320, generator=g, device="cuda") * 3
     m[0] = 0.0
     m[1] = -0.0
     # a block of E2M1 ties and saturation against a block max of 6
@@ -137,9 +140,18 @@ SMALL = [
     # and partial N tiles of both projections
     synth.Workload("nvf4_ragged_k", T=300, d_model=320, n_experts=8, top_k=2, d_ff=448, seed=66),
     # split-K: fewer tiles than two waves and 16 K blocks of 256 in both
-    # projections, so both write fp32 partial rows
+    # projections, so both write fp32 partial rows (T = 8 and T = 96)
     synth.Workload("nvf4_split_k", T=8, d_model=4096, n_experts=8, top_k=2, d_ff=4096,
                    n_shared=1, seed=67),
+    synth.Workload("nvf4_split_k_prefill", T=96, d_model=4096, n_experts=8, top_k=2, d_ff=2048,
+                   n_shared=1, seed=73),
+    # decode-sized batches: segments of 1 to 64 rows (a 40-row shared
+    # segment; routed segments of more than 32 rows) with K tails and partial
+    # feature tiles
+    synth.Workload("nvf4_decode_ragged_k", T=40, d_model=320, n_experts=8, top_k=2, d_ff=448,
+                   n_shared=1, seed=74),
+    synth.Workload("nvf4_decode_t64_small", T=64, d_model=512, n_experts=4, top_k=2, d_ff=512,
+                   seed=75),
 ]
 
 
@@ -171,6 +183,8 @@ def test_layer_nvfp4_refuses_unsupported_shapes():
     (synth.Workload("nvf4_block_pattern", T=384, d_model=512, n_experts=8, top_k=2, d_ff=768,
                     n_shared=1, seed=69), None),
     (LARGE.replace(name="nvf4_block_pattern_large", seed=71), 96),
+    (synth.Workload("nvf4_block_pattern_decode", T=48, d_model=512, n_experts=4, top_k=2,
+                    d_ff=768, n_shared=1, seed=72), None),
 ], ids=lambda v: v.name if hasattr(v, "name") else str(v))
 def test_layer_nvfp4_block_scale_pattern(oracle, w, nrows):
     """Expert weights whose 16-element blocks differ by up to 2^8 from one
