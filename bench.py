@@ -96,6 +96,8 @@ TRAFFIC_PROFILES = {
     ("fp8", "mixtral_8x7b_prefill"): "grouped_gemm_fp8_mixtral_8x7b_prefill.md",
     ("nvfp4", "mixtral_8x7b_prefill"): "grouped_gemm_nvfp4_mixtral_8x7b_prefill.md",
     (None, "mixtral_8x7b_decode_T64"): "decode_mixtral_8x7b_T64.md",
+    ("fp8", "mixtral_8x7b_decode_T64"): "decode_mixtral_8x7b_T64_fp8.md",
+    ("nvfp4", "mixtral_8x7b_decode_T64"): "decode_mixtral_8x7b_T64_nvfp4.md",
 }
 
 
