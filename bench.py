@@ -90,42 +90,33 @@ def kernel_source_key():
     return h.hexdigest()[:16]
 
 
-# ncu summaries with a gate/up DRAM traffic figure: (operand kind, workload) -> file
-TRAFFIC_PROFILES = {
-    (None, "mixtral_8x7b_prefill"): "grouped_gemm_mixtral_8x7b_prefill.md",
-    ("fp8", "mixtral_8x7b_prefill"): "grouped_gemm_fp8_mixtral_8x7b_prefill.md",
-    ("nvfp4", "mixtral_8x7b_prefill"): "grouped_gemm_nvfp4_mixtral_8x7b_prefill.md",
-    (None, "mixtral_8x7b_decode_T64"): "decode_mixtral_8x7b_T64.md",
-    ("fp8", "mixtral_8x7b_decode_T64"): "decode_mixtral_8x7b_T64_fp8.md",
-    ("nvfp4", "mixtral_8x7b_decode_T64"): "decode_mixtral_8x7b_T64_nvfp4.md",
-}
+# DRAM bytes per gate/up launch from ncu captures, keyed on the operand kind
+# and workload (profiles/traffic.json; each entry names its summary file)
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def traffic_entries():
+    """The recorded gate/up DRAM figures: {(quant, workload): entry}."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return {}
+    return {(None if e["quant"] == "bf16" else e["quant"], e["workload"]): e
+            for e in d.get("entries", []) if e.get("kernel") == "gate_up"}
 
 
 def recorded_traffic(quant, workload):
-    """DRAM bytes per gate/up launch from the committed ncu summary of this
-    operand kind and workload, or None when there is none or the kernel code
-    changed since that capture (kernel_source_key differs from the one
-    recorded there)."""
-    name = TRAFFIC_PROFILES.get((quant, workload))
-    if name is None:
-        return None
-    prof = os.path.join(ROOT, "profiles", name)
-    try:
-        text = open(prof).read()
-    except OSError:
-        return None
+    """DRAM bytes per gate/up launch recorded for this operand kind and
+    workload, or None when there is none or the kernel code changed since
+    that capture (kernel_source_key differs from the one recorded)."""
+    e = traffic_entries().get((quant, workload))
     key = kernel_source_key()
-    vals = {}
-    for line in text.splitlines():
-        if ":" in line and line.strip().split(":")[0] in ("gate_up_dram_bytes_per_launch",
-                                                          "kernel_source_sha256"):
-            k, v = line.strip().split(":", 1)
-            vals[k] = v.strip()
-    if key is None or vals.get("kernel_source_sha256") != key:
+    if e is None or key is None or e.get("kernel_source_sha256") != key:
         return None
     try:
-        return float(vals["gate_up_dram_bytes_per_launch"])
-    except (KeyError, ValueError):
+        return float(e["dram_bytes_per_launch"])
+    except (KeyError, TypeError, ValueError):
         return None
 
 
@@ -539,8 +530,11 @@ def run_ours(args):
                     "grouped_gemm_both_kernels_frac": round(gemm_tflops / tpk, 4)}
     # HBM-bound kernels of the step against the copy bandwidth
     P = w.T * w.top_k
+    # permute_gather: each token row is read from HBM once (a token's second
+    # and later copies hit L2), every routed row written once, plus the row
+    # indices: the unique bytes, not 2 P d
     hb = {"router_topk": w.T * w.d_model * eb + w.n_experts * w.d_model * eb + P * 8,
-          "permute_gather": 2 * P * w.d_model * eb + P * 4,
+          "permute_gather": (w.T + P) * w.d_model * eb + P * 4,
           "combine": (P + w.n_shared * w.T) * w.d_model * eb + w.T * w.d_model * eb + P * 4}
     if "router_topk" in per_kernel:  # the router's score contraction
         fl = 2.0 * w.T * w.n_experts * w.d_model

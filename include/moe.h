@@ -167,10 +167,17 @@ MOE_API int moe_router_topk(const moe_config* cfg, const void* x, const void* w_
  *    max(ceil(T / 64), min(T, 608)) when N <= 32 (for N = 8: T <= 1048320;
  *    N = 32: T <= 262080; N = 256: T <= 32704); a larger call returns
  *    MOE_ERR_WORKSPACE, launching nothing;
- *  - the first call made with a device current looks up the array's device
- *    address for that device; make that first call before any stream capture;
+ *  - the first call made with a CUDA context current looks up the array's
+ *    device address in that context; make that first call before any stream
+ *    capture. The lookup is keyed on the context's process-unique id, so a
+ *    context made after cudaDeviceReset, or a second context on the same
+ *    device, gets its own lookup on its first call;
  *  - all calls share the array: calls whose work overlaps on the GPU race
  *    on it and give undefined results; order them on one stream;
+ *  - errors found on the device while the router runs (a bounded wait of the
+ *    tensor-core router, N > 32, that ran out: MOE_ERR_TIMEOUT) are recorded
+ *    in the array's status word, which the call clears first; read it with
+ *    moe_router_topk_noalloc_status after the call;
  *  - MOE_ERR_CUDA here leaves the CUDA error to cudaGetLastError.
  */
 MOE_API int moe_router_topk_noalloc(const moe_config* cfg, const void* x,
@@ -178,6 +185,14 @@ MOE_API int moe_router_topk_noalloc(const moe_config* cfg, const void* x,
                     const float* sel_bias, const float* logits_in,
                     float* logits_out, int32_t* topk_idx, float* topk_w,
                     int32_t* counts, float* prob_sum, moe_stream_t stream);
+
+/* Synchronises `stream`, then returns the device-side status that the last
+ * moe_router_topk_noalloc call in the current context recorded in the
+ * library's array (MOE_OK or MOE_ERR_TIMEOUT), or MOE_ERR_CUDA if a CUDA call
+ * failed. Like the array, it is shared by every call: read it after the call
+ * whose status is wanted and before the next one is enqueued. Allocates
+ * nothing. */
+MOE_API int moe_router_topk_noalloc_status(moe_stream_t stream);
 
 /*
  * Groups the T*k (token, slot) pairs by expert and gathers their token rows.
@@ -448,6 +463,20 @@ MOE_API int moe_layer_backward(const moe_config* cfg, const void* x, const void*
  * workspace `ws` by the last call that used it (MOE_OK, MOE_ERR_TIMEOUT or
  * MOE_ERR_DEVICE_CHECK), or MOE_ERR_CUDA if the stream reports an error. */
 MOE_API int moe_stream_status(const void* ws, moe_stream_t stream);
+
+/* Test hook for the failure path of the single-token decode kernel (the
+ * one-launch layer that moe_layer_forward runs for T = 1; bf16, N <= 32).
+ * That kernel has two grid-wide barriers, each a bounded wait: a CTA that
+ * waits longer than the limit records MOE_ERR_TIMEOUT in the workspace
+ * status word and returns, so a missing arrival ends the kernel with an
+ * error that moe_stream_status reports instead of hanging the GPU. With
+ * withhold != 0 the launches enqueued after this call wait for one arrival
+ * more than the grid makes -- an arrival that never comes -- so every wait
+ * runs out after limit_ns nanoseconds, the call's outputs are undefined and
+ * its status is MOE_ERR_TIMEOUT. withhold = 0 with limit_ns = 0 restores
+ * the defaults (no withheld arrival, a 2 s limit). The setting is
+ * process-wide; no other kernel reads it. */
+MOE_API void moe_set_decode_barrier_test(int32_t withhold, uint64_t limit_ns);
 
 /* Kernel-level profiling. While enabled, each launch of the selected kernel
  * kinds is bracketed by CUDA events recorded on the launching stream (events

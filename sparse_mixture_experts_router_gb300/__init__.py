@@ -73,6 +73,7 @@ _SIGS = {
     "moe_workspace_size": (_SZ, [_CFG]),
     "moe_router_topk": (_I, [_CFG] + [_P] * 10 + [_P, _SZ, _P]),
     "moe_router_topk_noalloc": (_I, [_CFG] + [_P] * 10 + [_P]),
+    "moe_router_topk_noalloc_status": (_I, [_P]),
     "moe_permute": (_I, [_CFG] + [_P] * 6 + [_P, _SZ, _P]),
     "moe_grouped_swiglu": (_I, [_CFG] + [_P] * 9 + [_P, _SZ, _P]),
     "moe_combine": (_I, [_CFG, _P, _P, _P, _P, _P]),
@@ -89,6 +90,7 @@ _SIGS = {
     "moe_layer_backward": (_I, [_CFG] + [_P] * 8 + [ctypes.c_float, ctypes.c_float] + [_P] * 5
                            + [_P, _SZ, _P]),
     "moe_stream_status": (_I, [_P, _P]),
+    "moe_set_decode_barrier_test": (None, [ctypes.c_int32, ctypes.c_uint64]),
     "moe_profile_enable": (None, [_I]),
     "moe_profile_collect": (_I, [_P, _P, _I]),
     "moe_profile_kernel_name": (ctypes.c_char_p, [_I]),
@@ -183,6 +185,12 @@ def moe_router_topk_noalloc(cfg, x, w_router, logit_bias, sel_bias, logits_in, l
         _ptr(prob_sum), _stream(stream)))
 
 
+def moe_router_topk_noalloc_status(stream=None):
+    """Synchronises the stream and returns the device-side status of the last
+    moe_router_topk_noalloc call (0, or a negative MOE_ERR_* code)."""
+    return lib().moe_router_topk_noalloc_status(_stream(stream))
+
+
 def moe_permute(cfg, x, topk_idx, expert_offsets, sorted_pair, inv_pos, x_perm, ws, stream=None):
     _check("moe_permute", lib().moe_permute(
         ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(expert_offsets), _ptr(sorted_pair),
@@ -270,6 +278,10 @@ def moe_balance_stats(n_experts, T, top_k, counts, prob_sum, alpha, f, P, aux, s
 
 def moe_stream_status(ws, stream=None) -> int:
     return int(lib().moe_stream_status(_ptr(ws), _stream(stream)))
+
+
+def moe_set_decode_barrier_test(withhold: int, limit_ns: int) -> None:
+    lib().moe_set_decode_barrier_test(int(withhold), int(limit_ns))
 
 
 def profile_kernel_names() -> list:

@@ -32,6 +32,8 @@
 // that bypass L1; H is read at L2 (it was written by other CTAs).
 #include <float.h>
 
+#include <atomic>
+
 #include "device_util.cuh"
 #include "moe_internal.h"
 #include "sm103_wait.cuh"
@@ -65,6 +67,11 @@ struct DecodeArgs {
   int chunk;
   int* status;       // [0] status word, [2] grid-barrier counter (zero at launch)
   int T, d, N, k, s, d_ff, gate_mode, capacity;
+  // Bounded grid-barrier waits: the limit, and arrivals the barriers wait for
+  // beyond the grid's own (0; 1 only under moe_set_decode_barrier_test, an
+  // arrival that never comes, so that every wait runs out).
+  unsigned long long barrier_limit_ns;
+  int barrier_withheld;
 };
 
 struct DfShared {
@@ -107,9 +114,10 @@ __device__ __forceinline__ bool key_better(float ka, int ia, float kb, int ib) {
 
 __device__ __forceinline__ float silu_f(float v) { return v / (1.0f + __expf(-v)); }
 
-// Grid barrier: every CTA adds one to the counter and waits (bounded) until
-// all have. Returns false if the wait ran out (the status word then says so).
-__device__ bool grid_barrier(int* counter, int* status, int target) {
+// Grid barrier: every CTA adds one to the counter and waits (bounded by
+// limit_ns) until all have. Returns false if the wait ran out (the status
+// word then says so).
+__device__ bool grid_barrier(int* counter, int* status, int target, uint64_t limit_ns) {
   __syncthreads();
   __shared__ int ok;
   if (threadIdx.x == 0) {
@@ -118,7 +126,7 @@ __device__ bool grid_barrier(int* counter, int* status, int target) {
     ok = 1;
     const uint64_t t0 = globaltimer_ns();
     while (*reinterpret_cast<volatile int*>(counter) < target) {
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         set_status(status, MOE_ERR_TIMEOUT);
         ok = 0;
         break;
@@ -329,7 +337,8 @@ __global__ void __launch_bounds__(DF_THREADS, MT <= 2 ? 4 : 2) decode_layer_kern
       }
     }
   }
-  if (!grid_barrier(a.status + 2, a.status, gridDim.x)) return;
+  if (!grid_barrier(a.status + 2, a.status, gridDim.x + a.barrier_withheld, a.barrier_limit_ns))
+    return;
 
   // ---- 2. down, in items of (expert, K chunk, 32 output features): the
   // chunk of H (bf16(SiLU(a) * b), a and b the sums of the two halves) of the
@@ -395,7 +404,9 @@ __global__ void __launch_bounds__(DF_THREADS, MT <= 2 ? 4 : 2) decode_layer_kern
       }
     }
   }
-  if (!grid_barrier(a.status + 2, a.status, 2 * gridDim.x)) return;
+  if (!grid_barrier(a.status + 2, a.status, 2 * gridDim.x + a.barrier_withheld,
+                    a.barrier_limit_ns))
+    return;
 
   // ---- 3. y[t][c] = sum over the token's terms (experts ascending, shared
   // last) of g * sum over chunks of part, in that order ---------------------
@@ -418,6 +429,10 @@ __global__ void __launch_bounds__(DF_THREADS, MT <= 2 ? 4 : 2) decode_layer_kern
 }
 
 constexpr size_t DF_MAX_SMEM = 96 * 1024;  // x of all tokens (fp32)
+
+// Grid-barrier settings of the next launches (moe_set_decode_barrier_test).
+std::atomic<unsigned long long> g_barrier_limit_ns{kWaitLimitNs};
+std::atomic<int> g_barrier_withheld{0};
 
 int df_chunk(int d_ff) {
   for (int ch = 2048; ch >= 256; ch /= 2)
@@ -509,6 +524,8 @@ cudaError_t launch_decode_fused(const moe_config& c, const void* x, const void* 
   a.d_ff = c.d_ff;
   a.gate_mode = c.gate_mode;
   a.capacity = c.capacity;
+  a.barrier_limit_ns = g_barrier_limit_ns.load();
+  a.barrier_withheld = g_barrier_withheld.load();
   const size_t smem = df_smem(c);
   ProfScope p(K_DECODE_FUSED, s);
   switch (df_mt(c.T)) {
@@ -520,3 +537,9 @@ cudaError_t launch_decode_fused(const moe_config& c, const void* x, const void* 
 }
 
 }  // namespace moe
+
+extern "C" void moe_set_decode_barrier_test(int32_t withhold, uint64_t limit_ns) {
+  if (withhold == 0 && limit_ns == 0) limit_ns = moe::kWaitLimitNs;
+  moe::g_barrier_withheld.store(withhold != 0 ? 1 : 0);
+  moe::g_barrier_limit_ns.store(limit_ns);
+}

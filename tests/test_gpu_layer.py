@@ -135,3 +135,23 @@ def test_layer_replays_from_a_cuda_graph(oracle):
             g.replay()
             torch.cuda.synchronize()
             assert torch.equal(run.y.view(torch.int16), eager.view(torch.int16)), w.name
+
+
+def test_decode_barrier_timeout_is_reported(oracle):
+    """The single-token layer kernel's grid barriers are bounded waits. With
+    one arrival withheld (an arrival no CTA makes) every wait runs out after
+    1 ms: the kernel records MOE_ERR_TIMEOUT and returns, the host reads it
+    from the status word, and the context stays usable -- the next call with
+    the default setting succeeds and matches the oracle."""
+    w = synth.Workload("barrier_timeout", T=1, d_model=512, n_experts=8, top_k=2, d_ff=1024,
+                       seed=43)
+    inp = margin_inputs(w, oracle)
+    run = LayerRun(w, inp)()
+    assert run.status() == 0
+    moe.moe_set_decode_barrier_test(1, 1_000_000)
+    try:
+        run()
+        assert run.status() == moe.MOE_ERR_TIMEOUT
+    finally:
+        moe.moe_set_decode_barrier_test(0, 0)
+    check_layer(oracle, w)

@@ -2,9 +2,11 @@
 allocate device memory or pass a workspace (a runtime whose memory planner
 assigns all device memory in advance, or a plugin slot that passes only
 inputs and outputs): its scratch is a fixed array of the library's own
-device memory. Checked through the C ABI against moe_router_topk, the
-workspace entry point, on two calls in a row (the second reuses the array
-the first left behind). This file is collected last on purpose."""
+device memory. Checked through the C ABI on two calls in a row (the second
+reuses the array the first left behind): against moe_router_topk, the
+workspace entry point, and against the oracle's routing (indices and counts
+bit-exact on inputs with the top-k order margin), with the array's status
+word read back after each call. This file is collected last on purpose."""
 import ctypes
 
 import numpy as np
@@ -13,6 +15,7 @@ import torch
 
 import sparse_mixture_experts_router_gb300 as moe
 from sparse_mixture_experts_router_gb300 import synth
+from gpu_common import GATE_TOL, margin_inputs, oracle_routing
 
 pytestmark = pytest.mark.gpu
 
@@ -52,14 +55,15 @@ WORKLOADS = [
 ]
 
 
-def test_noalloc_router_matches_workspace_router_twice():
+def test_noalloc_router_matches_workspace_router_twice(oracle):
     stream = torch.cuda.current_stream()
     for w in WORKLOADS:  # two calls in a row on the shared static scratch
-        inp = synth.make_inputs(w, "cuda")
+        inp = margin_inputs(w, oracle)
         cfg = moe.config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k,
                          d_ff=w.d_ff, gate_mode=w.gate_mode)
         a, b = _outputs(w.T, w.n_experts, w.top_k), _outputs(w.T, w.n_experts, w.top_k)
         assert _call_noalloc(cfg, inp, a, stream) == moe.MOE_OK
+        assert moe.moe_router_topk_noalloc_status(stream) == moe.MOE_OK, w.name
         assert _call_ws(cfg, inp, b, stream) == moe.MOE_OK
         torch.cuda.synchronize()
         for key in ("idx", "counts"):
@@ -68,6 +72,12 @@ def test_noalloc_router_matches_workspace_router_twice():
             assert not torch.isnan(a[key]).any()
             assert np.allclose(a[key].cpu().numpy(), b[key].cpu().numpy(), rtol=1e-6, atol=1e-6), \
                 (w.name, key)
+        # the oracle's routing of the same tokens: indices and counts bit-exact
+        _, idx, tw, counts, ps = oracle_routing(oracle, w, inp)
+        assert np.array_equal(a["idx"].cpu().numpy(), idx), w.name
+        assert np.array_equal(a["counts"].cpu().numpy(), counts), w.name
+        assert np.abs(a["w"].cpu().numpy() - tw).max() <= GATE_TOL, w.name
+        assert np.allclose(a["prob_sum"].cpu().numpy(), ps, rtol=1e-4, atol=1e-4), w.name
 
 
 def test_noalloc_router_rejects_calls_beyond_its_scratch():
@@ -99,7 +109,7 @@ def test_noalloc_router_limit_is_exact(N, k, T_max):
             _p(o["counts"]), _p(o["prob_sum"]), ctypes.c_void_p(stream.cuda_stream))
         if ok:
             assert rc == moe.MOE_OK
-            torch.cuda.synchronize()
+            assert moe.moe_router_topk_noalloc_status(stream) == moe.MOE_OK
             assert int(o["counts"].sum().item()) == T * k
         else:
             assert rc == moe.MOE_ERR_WORKSPACE
