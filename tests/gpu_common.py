@@ -77,26 +77,45 @@ def oracle_routing(oracle, w, inp):
     return r64, idx, tw, counts, ps
 
 
+_HOST_WEIGHTS = []  # [(device tensors, host copies)] of the last workload
+
+
+def host_weights(inp):
+    """Host copies (oracle form) of the three expert weight tensors, made
+    once per set of device tensors: one copy each rather than one per
+    expert and batch of tokens. The cache holds the device tensors it was
+    made from, so their memory cannot be reused by other tensors while it
+    is cached."""
+    dev = tuple(inp[n] for n in ("w_gate", "w_up", "w_down"))
+    if not (_HOST_WEIGHTS and all(a is b for a, b in zip(_HOST_WEIGHTS[0][0], dev))):
+        _HOST_WEIGHTS.clear()
+        _HOST_WEIGHTS.append((dev, tuple(host(t) for t in dev)))
+    return _HOST_WEIGHTS[0][1]
+
+
 def oracle_rows(oracle, w, inp, idx, tw, rows, max_experts=40, fp8=False, nvfp4=False):
-    """Oracle layer output for the listed tokens, copying to the host only
-    the experts those tokens use, a batch of tokens at a time."""
+    """Oracle layer output for the listed tokens. The oracle gets only the
+    experts those tokens use, a batch of tokens at a time: FP8 and NVFP4
+    quantize every expert they are given, so a batch is limited to
+    max_experts; bf16 and fp32 take all tokens in one batch."""
     rows = [int(r) for r in rows]
     xh = host(inp["x"])
+    wg, wu, wd = host_weights(inp)
     keep = oracle.capacity_keep(idx, w.n_experts, capacity_of(w))
     out = np.empty((len(rows), w.d_model), np.float64)
     shared = list(range(w.n_experts, w.n_experts + w.n_shared))
+    limit = max_experts if (fp8 or nvfp4) else w.n_experts + w.n_shared
     i = 0
     while i < len(rows):
         batch, need = [], set(shared)
         while i < len(rows):
             cand = need | set(idx[rows[i]].tolist())
-            if batch and len(cand) > max_experts:
+            if batch and len(cand) > limit:
                 break
             need = cand
             batch.append(rows[i])
             i += 1
-        experts = {e: (host(inp["w_gate"][e]), host(inp["w_up"][e]), host(inp["w_down"][e]))
-                   for e in sorted(need)}
+        experts = {e: (wg[e], wu[e], wd[e]) for e in sorted(need)}
         y = oracle.layer_rows(xh, experts, idx, tw, batch, w.n_experts, w.n_shared, keep, fp8,
                               nvfp4)
         out[i - len(batch):i] = y
@@ -143,3 +162,37 @@ def sample_rows(T, n, seed=0):
     rng = np.random.default_rng(seed)
     mid = rng.choice(np.arange(1, T - 1), size=n - 2, replace=False)
     return sorted([0, T - 1] + mid.tolist())
+
+
+def segment_edge_rows(idx, n_experts, capacity=0, n_random=8, seed=0, max_experts=None):
+    """Token rows whose outputs cover both ends of expert segments: the owner
+    of each routed expert's first row and of its last kept row (the row of
+    the segment's last, usually partial, M tile), plus n_random other
+    tokens, first and last token included. Rows inside a segment are in
+    ascending token order, so an expert's first and last rows belong to the
+    smallest and the largest token that chose it (with a capacity C, the
+    C-th smallest). max_experts, when given, takes that many experts evenly
+    spread over [0, N) instead of all of them."""
+    idx = np.asarray(idx)
+    T = idx.shape[0]
+    rows = set(sample_rows(T, max(2, n_random), seed=seed))
+    experts = range(n_experts)
+    if max_experts is not None and max_experts < n_experts:
+        experts = sorted(set(np.linspace(0, n_experts - 1, max_experts).round().astype(int)))
+    for e in experts:
+        toks = np.nonzero((idx == e).any(axis=1))[0]
+        if toks.size == 0:
+            continue
+        last = toks.size - 1 if capacity <= 0 else min(toks.size, capacity) - 1
+        rows.add(int(toks[0]))
+        rows.add(int(toks[last]))
+    return sorted(rows)
+
+
+def grouped_tiles(counts, T, n_shared, d_model, d_ff, tile_m):
+    """Work tiles of the two grouped GEMMs when every segment is cut into
+    tile_m-row tiles: (gate/up tiles of 128 SwiGLU columns, down tiles of
+    256 output columns)."""
+    mt = sum((int(c) + tile_m - 1) // tile_m for c in counts)
+    mt += n_shared * ((T + tile_m - 1) // tile_m)
+    return mt * ((d_ff + 127) // 128), mt * ((d_model + 255) // 256)

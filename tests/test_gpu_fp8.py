@@ -16,8 +16,8 @@ import torch
 
 import sparse_mixture_experts_router_gb300 as moe
 from sparse_mixture_experts_router_gb300 import synth
-from gpu_common import (BF16_TOL, capacity_of, cfg_of, host, margin_inputs, oracle_routing,
-                        oracle_rows, rel_inf, sample_rows)
+from gpu_common import (BF16_TOL, capacity_of, cfg_of, grouped_tiles, host, margin_inputs,
+                        oracle_routing, oracle_rows, rel_inf, segment_edge_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -79,14 +79,14 @@ def check_fp8(oracle, w, rows=None):
     r64, idx, tw, counts, ps = oracle_routing(oracle, w, inp)
     assert np.array_equal(run.idx.cpu().numpy(), idx)
     assert np.array_equal(run.counts.cpu().numpy(), counts)
-    rows = list(range(w.T)) if rows is None else rows
+    rows = list(range(w.T)) if rows is None else rows(idx) if callable(rows) else rows
     ref = oracle_rows(oracle, w, inp, idx, tw, rows, fp8=True)
     got = run.y.float().cpu().numpy()[rows]
     assert not np.isnan(got).any()
     err = rel_inf(got, ref)
     print(f"{w.name}: FP8 rel-inf error {err:.3e}")
     assert err <= BF16_TOL, err
-    return err
+    return err, counts
 
 
 SMALL = [
@@ -116,7 +116,20 @@ FULL = [synth.MIXTRAL_PREFILL, synth.MIXTRAL_DECODE[0], synth.MIXTRAL_DECODE[3],
 
 @pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
 def test_layer_fp8_full_size(oracle, w):
-    check_fp8(oracle, w, sample_rows(w.T, 8, seed=w.seed))
+    check_fp8(oracle, w, lambda idx: segment_edge_rows(idx, w.n_experts, capacity_of(w),
+                                                        n_random=8, seed=w.seed, max_experts=8))
+
+
+def test_layer_fp8_pair_multi_tile_every_row(oracle):
+    """E4M3 on CTA pairs with every pair running >= 3 tiles of each
+    projection (persistent walk, both accumulators); y compared on every
+    token."""
+    w = synth.Workload("fp8_multi_tile_pair", T=16384, d_model=512, n_experts=8, top_k=2,
+                       d_ff=1024, seed=64)
+    _, counts = check_fp8(oracle, w)
+    gu, dn = grouped_tiles(counts, w.T, w.n_shared, w.d_model, w.d_ff, 256)
+    grid = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    assert gu >= 3 * grid and dn >= 3 * grid, (gu, dn, grid)
 
 
 def test_layer_fp8_refuses_unaligned_rows():

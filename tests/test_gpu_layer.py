@@ -14,8 +14,8 @@ import torch
 
 import sparse_mixture_experts_router_gb300 as moe
 from sparse_mixture_experts_router_gb300 import synth
-from gpu_common import (BF16_TOL, F32_TOL, GATE_TOL, LayerRun, margin_inputs, oracle_routing,
-                        oracle_rows, rel_inf, sample_rows)
+from gpu_common import (BF16_TOL, F32_TOL, GATE_TOL, LayerRun, capacity_of, grouped_tiles,
+                        margin_inputs, oracle_routing, oracle_rows, rel_inf, segment_edge_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -64,7 +64,7 @@ def check_layer(oracle, w, rows=None):
     assert np.array_equal(run.counts.cpu().numpy(), counts)
     assert np.abs(run.topk_w.cpu().numpy() - tw).max() <= GATE_TOL
     assert np.allclose(run.prob_sum.cpu().numpy(), ps, rtol=1e-4, atol=1e-4)
-    rows = list(range(w.T)) if rows is None else rows
+    rows = list(range(w.T)) if rows is None else rows(idx) if callable(rows) else rows
     ref = oracle_rows(oracle, w, inp, idx, tw, rows)
     got = run.y.float().cpu().numpy()[rows]
     assert not np.isnan(got).any()
@@ -102,9 +102,47 @@ FULL = [synth.MIXTRAL_PREFILL, *synth.MIXTRAL_DECODE, synth.DEEPSEEK_V3, synth.Z
 
 @pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
 def test_layer_full_size(oracle, w):
-    rows = sample_rows(w.T, 16, seed=w.seed)
-    run, err = check_layer(oracle, w, rows)
-    print(f"{w.name}: rel-inf error on {len(rows)} sampled tokens = {err:.3e}")
+    """Routing of every token bit-exact; y on the owners of the first and the
+    last row of every expert segment (so every segment's last, partial M
+    tile is compared) and on 16 other tokens."""
+    run, err = check_layer(oracle, w, lambda idx: segment_edge_rows(
+        idx, w.n_experts, capacity_of(w), n_random=16, seed=w.seed, max_experts=64))
+    print(f"{w.name}: rel-inf error on segment-edge and sampled tokens = {err:.3e}")
+
+
+# Shapes whose grouped GEMMs give every CTA (or CTA pair) at least three
+# tiles, so the persistent walk, both TMEM accumulators and their phase flips
+# all run; y is compared against the oracle on every token.
+MULTI_TILE = [
+    # CTA pairs, 256-row tiles: ~1024 gate/up and ~256 down tiles
+    (synth.Workload("multi_tile_pair", T=16384, d_model=512, n_experts=8, top_k=2, d_ff=1024,
+                    seed=61), 256),
+    # 1-CTA, 128-row tiles over ~256-row segments, a shared expert, both
+    # DeepSeek-V3 routing options
+    (synth.Workload("multi_tile_1cta_shared", T=4096, d_model=768, n_experts=64, top_k=4,
+                    d_ff=512, n_shared=1, gate_mode=1, sel_bias=True, seed=62), 128),
+]
+
+
+@pytest.mark.parametrize("w,tile_m", MULTI_TILE, ids=lambda v: getattr(v, "name", str(v)))
+def test_layer_multi_tile_every_row(oracle, w, tile_m):
+    run, err = check_layer(oracle, w)
+    counts = run.counts.cpu().tolist()
+    gu, dn = grouped_tiles(counts, w.T, w.n_shared, w.d_model, w.d_ff, tile_m)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    grid = sms // 2 if tile_m == 256 else sms
+    assert gu >= 3 * grid and dn >= 3 * grid, (gu, dn, grid)
+    print(f"{w.name}: {gu} gate/up and {dn} down tiles over {grid} CTAs; rel-inf error {err:.3e}")
+
+
+def test_layer_decode_split_k_every_row(oracle):
+    """T = 64 with d_ff = 4096: swap-AB decode tiles, each projection split
+    along K so that every CTA runs >= 3 (tile, split) units; y compared on
+    every token."""
+    w = synth.Workload("multi_unit_decode_splitk", T=64, d_model=1024, n_experts=8, top_k=2,
+                       d_ff=4096, seed=63)
+    run, err = check_layer(oracle, w)
+    print(f"{w.name}: rel-inf error {err:.3e}")
 
 
 def test_layer_replays_from_a_cuda_graph(oracle):

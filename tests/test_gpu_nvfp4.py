@@ -21,8 +21,8 @@ import torch
 
 import sparse_mixture_experts_router_gb300 as moe
 from sparse_mixture_experts_router_gb300 import synth
-from gpu_common import (BF16_TOL, cfg_of, host, margin_inputs, oracle_routing, oracle_rows,
-                        rel_inf, sample_rows)
+from gpu_common import (BF16_TOL, capacity_of, cfg_of, grouped_tiles, host, margin_inputs,
+                        oracle_routing, oracle_rows, rel_inf, sample_rows, segment_edge_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -115,14 +115,14 @@ def check_nvfp4(oracle, w, rows=None):
     r64, idx, tw, counts, ps = oracle_routing(oracle, w, inp)
     assert np.array_equal(run.idx.cpu().numpy(), idx)
     assert np.array_equal(run.counts.cpu().numpy(), counts)
-    rows = list(range(w.T)) if rows is None else rows
+    rows = list(range(w.T)) if rows is None else rows(idx) if callable(rows) else rows
     ref = oracle_rows(oracle, w, inp, idx, tw, rows, nvfp4=True)
     got = run.y.float().cpu().numpy()[rows]
     assert not np.isnan(got).any()
     err = rel_inf(got, ref)
     print(f"{w.name}: NVFP4 rel-inf error {err:.3e}")
     assert err <= BF16_TOL, err
-    return err
+    return err, counts
 
 
 SMALL = [
@@ -170,7 +170,20 @@ FULL = [synth.MIXTRAL_PREFILL, synth.MIXTRAL_DECODE[0], synth.MIXTRAL_DECODE[3],
 
 @pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
 def test_layer_nvfp4_full_size(oracle, w):
-    check_nvfp4(oracle, w, sample_rows(w.T, 8, seed=w.seed))
+    check_nvfp4(oracle, w, lambda idx: segment_edge_rows(idx, w.n_experts, capacity_of(w),
+                                                          n_random=8, seed=w.seed, max_experts=8))
+
+
+def test_layer_nvfp4_multi_tile_every_row(oracle):
+    """NVFP4 on 1-CTA tiles with every CTA running >= 3 tiles of each
+    projection (persistent walk, the single accumulator's phase flips, the
+    scale buffers' reuse across tiles); y compared on every token."""
+    w = synth.Workload("nvf4_multi_tile", T=8192, d_model=1024, n_experts=8, top_k=2,
+                       d_ff=1024, seed=65)
+    _, counts = check_nvfp4(oracle, w)
+    gu, dn = grouped_tiles(counts, w.T, w.n_shared, w.d_model, w.d_ff, 128)
+    grid = torch.cuda.get_device_properties(0).multi_processor_count
+    assert gu >= 3 * grid and dn >= 3 * grid, (gu, dn, grid)
 
 
 def test_layer_nvfp4_refuses_unsupported_shapes():
