@@ -328,7 +328,7 @@ def run_ours(args):
     eb = 4 if w.dtype == "f32" else 2
     cfg = moe.config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k, d_ff=w.d_ff,
                      n_shared=w.n_shared, dtype=moe.MOE_F32 if w.dtype == "f32" else moe.MOE_BF16,
-                     gate_mode=w.gate_mode, capacity=capacity_of(w))
+                     gate_mode=w.gate_mode, capacity=capacity_of(w), tiles=args.tiles)
     y = torch.empty(w.T, w.d_model, dtype=w.torch_dtype, device=dev)
     # Inputs that fit in L2 (the tiny fp32 layer) are timed step by step with
     # L2 flushed (a 256 MB write) before each step; larger ones stream their
@@ -552,6 +552,14 @@ def run_ours(args):
             per_kernel[name]["hbm_frac"] = round(gbs / pk["hbm"], 4)
 
     decode = run_decode(moe, synth, dev, stream, pk, args) if default and not args.no_decode else None
+    # the other layer shapes and operand types, measured in the same run
+    others = {}
+    if default and not args.quant and not args.no_others:
+        for key, ow, q in (("deepseek_v3_moe", synth.DEEPSEEK_V3, None),
+                           ("zipf_imbalanced", synth.ZIPF, None),
+                           ("mixtral_8x7b_prefill_fp8", synth.MIXTRAL_PREFILL, "fp8"),
+                           ("mixtral_8x7b_prefill_nvfp4", synth.MIXTRAL_PREFILL, "nvfp4")):
+            others[key] = run_layer_summary(moe, synth, dev, stream, pk, ow, q, args)
     backward = (run_backward(moe, dev, stream, pk, w, inp, cfg, args)
                 if default and not args.quant and not args.no_backward else None)
     E = w.n_experts + w.n_shared
@@ -591,6 +599,8 @@ def run_ours(args):
                                 "softmax over all scores, kept ones renormalised"][w.gate_mode],
                        "selection_bias": w.sel_bias, "zipf_offset_s": w.zipf_s or None,
                        "capacity": capacity_of(w) or None,
+                       "tiles": {0: "library's choice", 1: "1-CTA", 2: "256-row CTA pairs",
+                                 3: "weight-stationary CTA pairs"}[args.tiles],
                        "parallelism": f"replicas x{ws} (per-token layer, no collective)",
                        "l2": (f"inputs ({in_bytes / 1e6:.2f} MB) fit in L2: L2 flushed (256 MB "
                               "write) before every timed step, each step timed on its own"
@@ -613,7 +623,95 @@ def run_ours(args):
             "decode": decode,
             "backward": backward,
         }
+        line.update(others)
         print(json.dumps(line))
+
+
+def run_layer_summary(moe, synth, dev, stream, pk, w, quant, args):
+    """A compact measurement of one more workload for the default run: the
+    layer step (device time, CUDA events, inputs resident in HBM; the expert
+    weights exceed L2), tokens/s, and both grouped GEMMs against their
+    rooflines (algorithmic flops against the bf16 burst peak times the
+    operand type's nominal ratio, algorithmic bytes against the measured HBM
+    copy bandwidth), from a second, profiled pass. The tiling is the
+    library's choice."""
+    import torch
+    inp = synth.make_inputs(w, dev)
+    cfg = moe.config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k, d_ff=w.d_ff,
+                     n_shared=w.n_shared, dtype=moe.MOE_BF16, gate_mode=w.gate_mode,
+                     capacity=capacity_of(w))
+    y = torch.empty(w.T, w.d_model, dtype=torch.bfloat16, device=dev)
+    idx = torch.empty(w.T, w.top_k, dtype=torch.int32, device=dev)
+    tw = torch.empty(w.T, w.top_k, dtype=torch.float32, device=dev)
+    counts = torch.empty(w.n_experts, dtype=torch.int32, device=dev)
+    ps = torch.empty(w.n_experts, dtype=torch.float32, device=dev)
+    fwd = Forward(moe, cfg, inp, quant, dev)
+
+    def step():
+        fwd(inp["x"], y, idx, tw, counts, ps, stream)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if moe.moe_stream_status(fwd.ws, stream) != 0:
+        raise RuntimeError(f"{w.name}: warm-up step failed on the device")
+    reps = max(5, min(args.steps, 20))
+    # the dominant kernel's duration inside the timed region, as in the headline
+    moe.profile_enable(True, kernels=["gate_up"])
+    moe.profile_collect()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / reps
+    gu_timed = moe.profile_collect()
+    moe.profile_enable(True)
+    moe.profile_collect()
+    for _ in range(3):
+        step()
+    kern = moe.profile_collect()
+    moe.profile_enable(False)
+    c = counts.cpu().tolist()
+    f_gu, f_dn = gemm_flops(w, c)
+    b_gu, b_dn = gemm_bytes(w, c, quant)
+    ratio = QUANT_PEAK_RATIO[quant]
+    tpk = pk["bf16"] * ratio
+    gu_ms = gu_timed["gate_up"][0] / gu_timed["gate_up"][1]
+    dn_ms = kern["down"][0] / kern["down"][1]
+    out = {"workload": w.name, "T": w.T, "d_model": w.d_model, "n_experts": w.n_experts,
+           "n_shared": w.n_shared, "top_k": w.top_k, "d_ff": w.d_ff,
+           "operands": {None: "bf16", "fp8": "e4m3 experts (row scales)",
+                        "nvfp4": "nvfp4 experts (e2m1, e4m3 16-element block scales, row scales)"}[quant],
+           "ms_per_step": round(ms, 4), "steps": reps,
+           "tokens_per_s": round(w.T / (ms / 1e3), 1),
+           "peak_tflops": round(tpk, 1),
+           "peak_source": (f"{pk['source']} bf16 burst x {ratio:g}" if quant
+                           else f"{pk['source']} bf16 burst")}
+    for name, f, by, t in (("gate_up", f_gu, b_gu, gu_ms), ("down", f_dn, b_dn, dn_ms)):
+        tf = f / (t / 1e3) / 1e12
+        gbs = by / (t / 1e3) / 1e9
+        out[name] = {"ms": round(t, 4), "tflops": round(tf, 1), "tensor_frac": round(tf / tpk, 4),
+                     "algorithmic_bytes": by, "gbs": round(gbs, 1),
+                     "hbm_frac": round(gbs / pk["hbm"], 4),
+                     # the floor is whichever of the tensor and HBM times is larger
+                     "roofline_ms": round(max(f / (tpk * 1e12), by / (pk["hbm"] * 1e9)) * 1e3, 4)}
+    out["kernel_ms"] = {k: round(v[0] / v[1], 4) for k, v in kern.items()}
+    out["experts_with_tokens"] = int(sum(1 for v in c if v > 0))
+    out["max_over_mean_expert_load"] = round(max(c) / max(1e-9, sum(c) / len(c)), 3)
+    if w.zipf_s:
+        bf = torch.empty(w.n_experts, dtype=torch.float32, device=dev)
+        bP = torch.empty(w.n_experts, dtype=torch.float32, device=dev)
+        baux = torch.empty(1, dtype=torch.float32, device=dev)
+        moe.moe_balance_stats(w.n_experts, w.T, w.top_k, counts, ps, AUX_ALPHA, bf, bP, baux,
+                              stream)
+        torch.cuda.synchronize(dev)
+        out["aux_loss"] = {"alpha": AUX_ALPHA, "value": round(float(baux.item()), 6),
+                           "balanced_value": AUX_ALPHA}
+    del inp, fwd
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_backward_only(args):
@@ -880,6 +978,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the DeepSeek-V3, Zipf, FP8 and NVFP4 objects of the default run")
     ap.add_argument("--backward-only", action="store_true",
                     help="time only the layer's backward and print its object (for profiling)")
     ap.add_argument("--tokens", type=int, default=None,
@@ -891,6 +991,9 @@ def main(argv=None):
     ap.add_argument("--nvfp4", action="store_true",
                     help="NVFP4 expert weights (moe_layer_forward_nvfp4); not the headline, which "
                          "is bf16")
+    ap.add_argument("--tiles", type=int, choices=[0, 1, 2, 3], default=0,
+                    help="grouped-GEMM tiling (moe_config.tiles): 0 the library's choice, 1 1-CTA, "
+                         "2 256-row CTA pairs, 3 weight-stationary CTA pairs")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per gate_up launch from an ncu capture of this build")
     args = ap.parse_args(argv)

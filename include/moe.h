@@ -96,7 +96,29 @@ typedef struct moe_config {
                       * extras are dropped). Routing, counts and the balance
                       * statistics are those before the cap; shared experts
                       * are never capped.                                    */
+  int32_t tiles;     /* moe_tiles: how the bf16 and E4M3 expert GEMMs cut
+                      * their work. 0 (MOE_TILES_AUTO) lets the library
+                      * choose; a named tiling changes only speed, never the
+                      * rounding of a result. NVFP4 always runs 1-CTA tiles. */
 } moe_config;
+
+/* Tilings of the grouped expert GEMMs (moe_config.tiles). Every tiling
+ * computes the same sums in the same order per output element. */
+typedef enum {
+  MOE_TILES_AUTO = 0,
+  /* 128 token rows x 256 accumulator columns on one SM, or, for T <= 64,
+   * weight rows x token columns on one SM; either may split K when there
+   * are few tiles. */
+  MOE_TILES_CTA = 1,
+  /* 256 token rows x 256 columns on a pair of SMs (tcgen05 cta_group::2):
+   * suits segments of many hundreds of rows, each ending in a partial
+   * 256-row tile. */
+  MOE_TILES_PAIR = 2,
+  /* 256 weight rows (output features) x up to 256 token rows on a pair of
+   * SMs: a segment's token tiles are cut to multiples of 16 rows, so
+   * segments of a few hundred rows waste little. */
+  MOE_TILES_WEIGHT_PAIR = 3
+} moe_tiles;
 
 /* Library version (major*10000 + minor*100 + patch). */
 MOE_API int moe_version(void);

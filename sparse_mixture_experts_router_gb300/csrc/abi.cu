@@ -338,6 +338,7 @@ int moe_check_config(const moe_config* c) {
   if (c->gate_mode != MOE_GATE_TOPK_SOFTMAX && c->gate_mode != MOE_GATE_ALL_SOFTMAX_RENORM)
     return MOE_ERR_INVALID_ARG;
   if (c->top_k > c->n_experts || c->capacity < 0) return MOE_ERR_INVALID_ARG;
+  if (c->tiles < MOE_TILES_AUTO || c->tiles > MOE_TILES_WEIGHT_PAIR) return MOE_ERR_INVALID_ARG;
   if (c->n_experts > kMaxExperts || c->top_k > kMaxTopK || c->n_shared > kMaxShared)
     return MOE_ERR_UNSUPPORTED;
   if (c->d_model % 8 != 0 || c->d_ff % 8 != 0) return MOE_ERR_UNSUPPORTED;

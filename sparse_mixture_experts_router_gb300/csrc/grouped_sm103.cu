@@ -1151,6 +1151,360 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Weight-stationary CTA pairs ("swap AB") for segments of a few hundred rows
+// (e.g. 256 experts of ~256 rows each): a 256-row token tile would waste up
+// to half its rows at a segment's end, a 128-row 1-CTA tile up to 127 and
+// moves 1.5x the operand bytes per MMA cycle of a pair. Here the MMA's M side
+// is the weights -- 256 output features of one expert, 128 in each CTA -- and
+// its N side the segment's token rows: a segment of R rows is cut into
+// ceil(R / 256) token tiles of equal height h (rounded up to 16) and the MMA
+// takes N = the tile's rows rounded up to 32, each CTA staging N/2 of them,
+// so a tile computes at most 31 rows that are not stored.
+//  - gate/up: two MMAs a K step (gate, then up rows of the same 128 features
+//    of each CTA) into TMEM columns [0, N) and [256, 256 + N), so the
+//    epilogue thread of a feature holds both of its products. That fills
+//    the 512 columns: one accumulator, whose epilogue the next tile's MMAs
+//    wait for. Per CTA a 64-wide K block stages 32 KB of weights and N/2
+//    token rows (<= 16 KB): 4 stages.
+//  - down: one MMA a K step (128 output features a CTA); two accumulators;
+//    a stage is 16 KB of W_d and N/2 rows of H: 6 stages.
+//  - The epilogue thread of TMEM lane j of CTA r owns feature
+//    256 n + 128 r + j for every token (column) of the tile; a warp stores
+//    32 consecutive features (64 bytes) of each token row.
+// Tile order, warp roles, barriers, the bounded waits and teardown are those
+// of grouped_gemm_pair_kernel.
+// A CTA stages its N/2 token rows with a single TMA box: one tensor map per
+// box height 16, 32, ..., 128 (N a multiple of 32). A tile's loads as a sum
+// of power-of-two boxes (N a multiple of 16) were measured up to 1.4x slower
+// in the down projection: one box a stage is what keeps the MMAs fed.
+constexpr int SW_TOK_BOXES = 8;
+struct TokMaps {
+  CUtensorMap box[SW_TOK_BOXES];  // box i: 16 (i + 1) rows
+};
+template <int EPI>
+struct Sw {
+  static constexpr int W_BYTES = (EPI == EPI_SWIGLU ? 2 : 1) * A_BYTES;  // per CTA a stage
+  static constexpr int TOK_MAX_BYTES = 128 * 128;  // 128 token rows (N/2 <= 128) of 128 bytes
+  static constexpr int STAGE = W_BYTES + TOK_MAX_BYTES;
+  static constexpr int STAGES = EPI == EPI_SWIGLU ? 4 : 6;
+  static constexpr int NACC = EPI == EPI_SWIGLU ? 1 : 2;
+  static constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024;
+};
+constexpr int SW_MAX_STAGES = 6;
+
+struct __align__(8) SwapState {
+  uint64_t full[SW_MAX_STAGES];
+  uint64_t empty[SW_MAX_STAGES];
+  uint64_t acc_full[NUM_ACC];
+  uint64_t acc_empty[NUM_ACC];  // in the even CTA: arrivals of both CTAs' epilogues
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Token tile m of a segment of `rows` rows (the segment table counts
+// ceil(rows / 256) tiles): its first row r0 and its rows nr (> 0). The MMA
+// takes N = nr rounded up to 32 (<= 256) columns, N/2 rows in each CTA.
+__device__ __forceinline__ void swap_tile_rows(int rows, int m, int& r0, int& nr) {
+  const int ntt = (rows + PAIR_TILE_M - 1) / PAIR_TILE_M;
+  const int h = (((rows + ntt - 1) / ntt) + 15) & ~15;  // <= 256
+  r0 = m * h;
+  nr = min(h, rows - r0);
+}
+__device__ __forceinline__ int swap_tile_n(int nr) { return (nr + 31) & ~31; }
+
+template <int EPI, int OP>
+__global__ void __launch_bounds__(G_THREADS, 1)
+    grouped_swap_pair_kernel(const __grid_constant__ CUtensorMap map_w0,
+                             const __grid_constant__ CUtensorMap map_w1,
+                             const __grid_constant__ TokMaps tok,
+                             const __grid_constant__ TokMaps tok_sh, const GemmArgs args) {
+  using C = Sw<EPI>;
+  constexpr bool GU = EPI == EPI_SWIGLU;
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ SwapState st;
+
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x / 32), 0);
+  const int lane = threadIdx.x % 32;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const uint32_t ring = (ptx::smem_addr(dyn_smem) + 1023u) & ~1023u;
+
+  const int32_t* seg = args.seg;  // built with 256-row tiles
+  const int KB = (args.K + Op<OP>::EPK - 1) / Op<OP>::EPK;
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::STAGES; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&st.full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&st.empty[i]), 1);
+    }
+    for (int i = 0; i < NUM_ACC; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&st.acc_full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&st.acc_empty[i]), 2 * G_EPI_THREADS);
+    }
+    ptx::mbar_init(ptx::smem_addr(&st.drain), 1);
+    st.abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&map_w0);
+    ptx::prefetch_tmap(&map_w1);
+    for (int i = 0; i < SW_TOK_BOXES; ++i) {
+      ptx::prefetch_tmap(&tok.box[i]);
+      ptx::prefetch_tmap(&tok_sh.box[i]);
+    }
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_addr(&st.tmem_base), TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers initialised before any remote use
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = st.tmem_base;
+  volatile int* abort_flag = &st.abort;
+  pdl_wait();  // the segment table and the operands come from earlier kernels
+  pdl_trigger();
+  const int E = __ldg(seg);
+  const int tiles = __ldg(seg + 1) * args.NT;
+
+  if (warp == 0) {
+    // ----------------------------------------------- TMA producer (both CTAs) --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
+        const Tile t = decode_tile(seg, E, args.NT, tile);
+        int r0, nr;
+        swap_tile_rows(__ldg(seg + 3 + E + t.s), t.m, r0, nr);
+        const int half = swap_tile_n(nr) >> 1;  // token rows this CTA stages (multiple of 16)
+        const TokMaps* tm = (GU && t.s >= args.n_routed) ? &tok_sh : &tok;
+        const int tok_row = __ldg(seg + 3 + (GU ? 2 : 3) * E + t.s) + r0 + (int)rank * half;
+        const int w_row = t.s * args.b_rows + t.n * 256 + (int)rank * 128;
+        const uint32_t bytes = (uint32_t)(C::W_BYTES + half * 128);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait_phase(ptx::smem_addr(&st.empty[stage]), phase ^ 1u, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_local = ptx::smem_addr(&st.full[stage]);
+          const uint32_t full_leader = ptx::mapa_shared(full_local, 0);
+          const uint32_t w_dst = ring + stage * C::STAGE;
+          if (leader) ptx::mbar_arrive_expect_tx(full_local, 2 * bytes);
+          const int kc = kb * Op<OP>::KC;
+          ptx::tma_load_2d_pair(w_dst, &map_w0, full_leader, kc, w_row);
+          if (GU) ptx::tma_load_2d_pair(w_dst + A_BYTES, &map_w1, full_leader, kc, w_row);
+          ptx::tma_load_2d_pair(w_dst + C::W_BYTES, &tm->box[(half >> 4) - 1], full_leader, kc,
+                                tok_row);
+          ++issued;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {
+        const long long n = issued < C::STAGES ? issued : C::STAGES;
+        for (long long i = 1; i <= n; ++i) {
+          const long long q = issued - i;
+          drain_wait(ptx::smem_addr(&st.full[q % C::STAGES]), (uint32_t)((q / C::STAGES) & 1));
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------- MMA issuer (even CTA only) --
+    if (lane == 0 && leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
+        const Tile t = decode_tile(seg, E, args.NT, tile);
+        int r0, nr;
+        swap_tile_rows(__ldg(seg + 3 + E + t.s), t.m, r0, nr);
+        const uint32_t idesc = idesc_op<OP>(2 * BM, swap_tile_n(nr));
+        if (!wait_phase(ptx::smem_addr(&st.acc_empty[acc]), acc_phase ^ 1u, abort_flag,
+                        args.status)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait_phase(ptx::smem_addr(&st.full[stage]), phase, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t w_src = ring + stage * C::STAGE;
+          const uint64_t wdesc0 = ptx::sdesc_k128(w_src);
+          const uint64_t wdesc1 = ptx::sdesc_k128(w_src + A_BYTES);
+          const uint64_t tdesc = ptx::sdesc_k128(w_src + C::W_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            const uint32_t accum = (kb | k) != 0;
+            mma_op_pair<OP>(d_tmem, wdesc0 + 2 * k, tdesc + 2 * k, idesc, accum);
+            if (GU) mma_op_pair<OP>(d_tmem + BN, wdesc1 + 2 * k, tdesc + 2 * k, idesc, accum);
+          }
+          ptx::mma_commit_pair(ptx::smem_addr(&st.empty[stage]), 0x3);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair(ptx::smem_addr(&st.acc_full[acc]), 0x3);
+        if (++acc == C::NACC) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        ptx::mma_commit_pair(ptx::smem_addr(&st.drain), 0x1);
+        drain_wait(ptx::smem_addr(&st.drain), 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue (both CTAs) --
+    // Warps 2-9: the two warps of a TMEM lane quarter take alternate 32-token
+    // chunks of the tile.
+    const int sub = warp & 3;
+    const int hf = (warp - 2) >> 2;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
+    // per epilogue warp: a 32-token x 32-feature bf16 block, so that each
+    // token row's 64 bytes leave as four 16-byte stores
+    __shared__ __align__(16) __nv_bfloat16 stage_out[EPI_WARPS][32 * 32];
+    __nv_bfloat16* stg = stage_out[warp - 2];
+    const uint32_t acc_empty_leader0 = ptx::mapa_shared(ptx::smem_addr(&st.acc_empty[0]), 0);
+    const uint32_t acc_empty_leader1 = ptx::mapa_shared(ptx::smem_addr(&st.acc_empty[1]), 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = cluster; tile < tiles; tile += nclusters) {
+      const Tile t = decode_tile(seg, E, args.NT, tile);
+      int r0, nr;
+      swap_tile_rows(__ldg(seg + 3 + E + t.s), t.m, r0, nr);
+      const long long orow0 = (long long)__ldg(seg + 3 + 3 * E + t.s) + r0;
+      const int fw0 = t.n * 256 + (int)rank * 128 + sub * 32;  // the warp's first feature
+      const int f = fw0 + lane;                                 // this thread's feature
+      const bool fvalid = f < args.n_out;
+      // E4M3: the feature's weight-channel scales, and the tokens' row scales
+      float sw0 = 1.f, sw1 = 1.f;
+      const float* tok_scale = nullptr;
+      long long tok_row0 = orow0;
+      if constexpr (Op<OP>::scaled) {
+        const long long wrow = (long long)t.s * args.b_rows + f;
+        sw0 = fvalid ? __ldg(args.b_scale0 + wrow) : 0.f;
+        if (GU) {
+          sw1 = fvalid ? __ldg(args.b_scale1 + wrow) : 0.f;
+          tok_row0 = (long long)__ldg(seg + 3 + 2 * E + t.s) + r0;
+          tok_scale = t.s >= args.n_routed ? args.a_scale_shared : args.a_scale;
+        } else {
+          tok_scale = args.a_scale;
+        }
+      }
+      // Lane l fetches the row factor of token c0 + l of each of the warp's
+      // (at most 4) chunks -- for down its gate weight, for E4M3 its A row
+      // scale -- before waiting for the accumulator, so the dependent loads
+      // overlap the tile's MMAs.
+      float rfs[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int tkn = hf * 32 + 64 * j + lane;
+        float rf = 1.f;
+        if (tkn < nr) {
+          if (!GU) rf = row_scale(args, t.s, orow0 + tkn);
+          if constexpr (Op<OP>::scaled) rf *= __ldg(tok_scale + tok_row0 + tkn);
+        }
+        rfs[j] = rf;
+      }
+      bool ok = wait_phase(ptx::smem_addr(&st.acc_full[acc]), acc_phase, abort_flag, args.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      ptx::tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c0 = hf * 32 + 64 * j;
+        if (c0 >= nr) break;  // warp-uniform
+        uint32_t a[32], b[32];
+        ptx::tmem_ld32(tbase + c0, a);
+        if (GU) ptx::tmem_ld32(tbase + BN + c0, b);
+        const float rf = rfs[j];
+        ptx::tmem_ld_wait();
+        const int cn = min(32, nr - c0);  // warp-uniform
+        // bf16 results into this warp's 32 x 32 staging block, transposed:
+        // row c (token) holds the warp's 32 features
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          float hv;
+          if constexpr (GU) {
+            float g = __uint_as_float(a[c]), u = __uint_as_float(b[c]);
+            if constexpr (Op<OP>::scaled) {
+              const float r = __shfl_sync(0xffffffffu, rf, c);
+              g *= sw0 * r;
+              u *= sw1 * r;
+            }
+            hv = silu(g) * u;
+          } else {
+            hv = __uint_as_float(a[c]) * __shfl_sync(0xffffffffu, rf, c);
+            if constexpr (Op<OP>::scaled) hv *= sw0;
+          }
+          stg[c * 32 + lane] = __float2bfloat16_rn(hv);
+        }
+        __syncwarp();
+        // 16-byte row pieces: lane l stores piece l % 4 of token rows
+        // l / 4 + 8 i, masked to the tile's rows and the output's columns
+        const int piece = lane & 3;
+        const bool cvalid = fw0 + piece * 8 < args.n_out;  // n_out is a multiple of 8
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = (lane >> 2) + 8 * i;
+          const uint4 v = *reinterpret_cast<const uint4*>(stg + row * 32 + piece * 8);
+          const long long orow = orow0 + c0 + row;
+          if (row < cn && cvalid)
+            *reinterpret_cast<uint4*>(out + orow * args.ldo + fw0 + piece * 8) = v;
+          if constexpr (Op<OP>::scaled && GU) {
+            // the H row's max |H| over this warp's 32 features, one atomic
+            float h0, h1, h2, h3, h4, h5, h6, h7;
+            bf16x2_to_f32(v.x, h0, h1);
+            bf16x2_to_f32(v.y, h2, h3);
+            bf16x2_to_f32(v.z, h4, h5);
+            bf16x2_to_f32(v.w, h6, h7);
+            float m = cvalid ? fmaxf(fmaxf(fmaxf(fabsf(h0), fabsf(h1)), fmaxf(fabsf(h2), fabsf(h3))),
+                                     fmaxf(fmaxf(fabsf(h4), fabsf(h5)), fmaxf(fabsf(h6), fabsf(h7))))
+                             : 0.f;
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            if (piece == 0 && row < cn && m > 0.f) atomicMax(args.h_amax + orow, __float_as_uint(m));
+          }
+        }
+        __syncwarp();  // the block is read before the next chunk rewrites it
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive_cluster(acc ? acc_empty_leader1 : acc_empty_leader0);
+      if (++acc == C::NACC) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------- teardown --
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // no CTA leaves while its peer may still use its smem
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Decode-sized batches (T <= 64, so every expert segment has at most 64
 // rows): swap A and B. The expert weights are the MMA's M side (128 output
 // features of one expert per tile) and the segment's few token rows the N
@@ -1645,18 +1999,68 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a_sh, const CUt
                     DYN_SMEM_PAIR, s, 2, a, a_sh, b0, b1, args);
 }
 
+cudaError_t configure_swap_kernels() {
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device == dev) return cudaSuccess;
+  const void* kernels[4] = {(const void*)grouped_swap_pair_kernel<EPI_SWIGLU, OP_BF16>,
+                            (const void*)grouped_swap_pair_kernel<EPI_DOWN, OP_BF16>,
+                            (const void*)grouped_swap_pair_kernel<EPI_SWIGLU, OP_E4M3>,
+                            (const void*)grouped_swap_pair_kernel<EPI_DOWN, OP_E4M3>};
+  const size_t smem[4] = {Sw<EPI_SWIGLU>::SMEM, Sw<EPI_DOWN>::SMEM, Sw<EPI_SWIGLU>::SMEM,
+                          Sw<EPI_DOWN>::SMEM};
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+    e = cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem[i]);
+  if (e == cudaSuccess) configured_device = dev;
+  return e;
+}
+
+// Token maps of the weight-stationary pair kernel: one per box height.
+bool make_tok_maps(TokMaps* m, const void* base, long long rows, long long cols, bool u8) {
+  for (int i = 0; i < SW_TOK_BOXES; ++i) {
+    const unsigned h = 16u * (unsigned)(i + 1);
+    if (!(u8 ? make_map_u8(&m->box[i], base, rows, cols, h) : make_map(&m->box[i], base, rows, cols, h)))
+      return false;
+  }
+  return true;
+}
+
+template <int EPI, int OP>
+cudaError_t launch_swap_pair(const CUtensorMap& w0, const CUtensorMap& w1, const TokMaps& tok,
+                             const TokMaps& tok_sh, const GemmArgs& args, int max_tiles,
+                             cudaStream_t s) {
+  static_assert(Sw<EPI>::SMEM <= DYN_SMEM_PAIR, "resident like the pair kernel");
+  cudaError_t e = configure_swap_kernels();
+  if (e != cudaSuccess) return e;
+  const int clusters = std::min(max_tiles, max_pair_clusters());
+  if (clusters <= 0) return cudaSuccess;
+  ProfScope p(EPI == EPI_SWIGLU ? K_GATE_UP : K_DOWN, s);
+  return launch_pdl(grouped_swap_pair_kernel<EPI, OP>, dim3(2 * clusters), dim3(G_THREADS),
+                    Sw<EPI>::SMEM, s, 2, w0, w1, tok, tok_sh, args);
+}
 
 }  // namespace
 
-bool use_pair_tiles(const moe_config& c) {
-  // Large segments only (on average at least 1.5 pair tiles of rows per
-  // routed expert), and never when a projection could be split along K.
-  if (c.dtype != MOE_BF16 || c.n_experts <= 0) return false;
-  const long long P = (long long)c.T * c.top_k;
+int gemm_tiles(const moe_config& c) {
+  if (c.dtype != MOE_BF16 || c.n_experts <= 0) return MOE_TILES_CTA;
+  const bool pairs_ok = max_pair_clusters() > 0;
+  if (c.tiles == MOE_TILES_CTA) return MOE_TILES_CTA;
+  if (c.tiles == MOE_TILES_PAIR || c.tiles == MOE_TILES_WEIGHT_PAIR)
+    return pairs_ok ? c.tiles : MOE_TILES_CTA;
+  // Chosen here: a projection that may be split along K (few rows) runs
+  // 1-CTA tiles (or swap-AB decode tiles); every larger batch runs the
+  // weight-stationary pairs, which were as fast as or faster than 256-row
+  // pair tiles on every measured layer (equal on 128 Zipf-skewed experts,
+  // 4% faster on 8 experts of ~1024 rows, 12% faster on 256 experts of
+  // ~256 rows, where 256-row tiles are a third padding).
   const SplitKPlan plan = splitk_plan(c);
-  return plan.s_max_gu == 1 && plan.s_max_dn == 1 && P >= 384LL * c.n_experts &&
-         max_pair_clusters() > 0;
+  if (plan.s_max_gu > 1 || plan.s_max_dn > 1 || !pairs_ok) return MOE_TILES_CTA;
+  return MOE_TILES_WEIGHT_PAIR;
 }
+
+bool use_pair_tiles(const moe_config& c) { return gemm_tiles(c) != MOE_TILES_CTA; }
 
 int seg_tile_m(const moe_config& c) { return use_pair_tiles(c) ? PAIR_TILE_M : BM; }
 
@@ -1688,7 +2092,8 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
   const int E = c.n_experts + c.n_shared;
   const long long R = P + (long long)c.n_shared * c.T;  // rows of H and y_perm
   if (R == 0) return cudaSuccess;
-  const bool pair = use_pair_tiles(c);
+  const int tiles = gemm_tiles(c);
+  const bool pair = tiles != MOE_TILES_CTA;
   const bool decode = !pair && c.T <= kDecodeMaxRows;  // every segment has <= 64 rows
   const long long mt_bound = mt_bound_of(c, pair ? PAIR_TILE_M : BM);
   const SplitKPlan plan = splitk_plan(c);
@@ -1752,12 +2157,6 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
     return launch_decode<EPI_DOWN, OP_BF16>(m_wd, m_wd, t_h, t_h, d, max_rows, s);
   }
 
-  cudaError_t e = pair ? launch_pair<EPI_SWIGLU, OP_BF16>(m_xp, m_x, m_wg, m_wu, g,
-                                                         (int)(mt_bound * g.NT), s)
-                       : launch_gemm<EPI_SWIGLU, OP_BF16>(m_xp, m_x, m_wg, m_wu, g,
-                                                          (int)(mt_bound * g.NT), s);
-  if (e != cudaSuccess) return e;
-
   GemmArgs d = g;
   d.topk_w = topk_w;
   d.out = y_perm;
@@ -1768,6 +2167,28 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
   d.b_rows = c.d_model;
   d.s_max = plan.s_max_dn;
   d.pc = c.d_model;
+  if (tiles == MOE_TILES_WEIGHT_PAIR) {
+    // weights on the MMA's M side, 256 features a pair tile; token boxes
+    // of 128..8 rows over x_perm / x (gate/up) and H (down)
+    TokMaps t_xp, t_x, t_h;
+    if (!make_tok_maps(&t_xp, P > 0 ? x_perm : x, P > 0 ? std::max(P, xp_rows) : c.T, c.d_model,
+                       false) ||
+        !make_tok_maps(&t_x, c.n_shared > 0 ? x : (P > 0 ? x_perm : x),
+                       c.n_shared > 0 ? c.T : (P > 0 ? P : c.T), c.d_model, false) ||
+        !make_tok_maps(&t_h, h, std::max(R, h_rows), c.d_ff, false))
+      return cudaErrorInvalidValue;
+    g.NT = (c.d_ff + 255) / 256;
+    g.s_max = d.s_max = 1;
+    cudaError_t e = launch_swap_pair<EPI_SWIGLU, OP_BF16>(m_wg, m_wu, t_xp, t_x, g,
+                                                          (int)(mt_bound * g.NT), s);
+    if (e != cudaSuccess) return e;
+    return launch_swap_pair<EPI_DOWN, OP_BF16>(m_wd, m_wd, t_h, t_h, d, (int)(mt_bound * d.NT), s);
+  }
+  cudaError_t e = pair ? launch_pair<EPI_SWIGLU, OP_BF16>(m_xp, m_x, m_wg, m_wu, g,
+                                                         (int)(mt_bound * g.NT), s)
+                       : launch_gemm<EPI_SWIGLU, OP_BF16>(m_xp, m_x, m_wg, m_wu, g,
+                                                          (int)(mt_bound * g.NT), s);
+  if (e != cudaSuccess) return e;
   return pair ? launch_pair<EPI_DOWN, OP_BF16>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s)
               : launch_gemm<EPI_DOWN, OP_BF16>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s);
 }
@@ -1784,7 +2205,8 @@ cudaError_t launch_grouped_e4m3(const moe_config& c, const uint8_t* xq_perm,
   const int E = c.n_experts + c.n_shared;
   const long long R = P + (long long)c.n_shared * c.T;
   if (R == 0) return cudaSuccess;
-  const bool pair = use_pair_tiles(c);
+  const int tiles = gemm_tiles(c);
+  const bool pair = tiles != MOE_TILES_CTA;
   const bool decode = !pair && c.T <= kDecodeMaxRows;
   const long long mt_bound = mt_bound_of(c, pair ? PAIR_TILE_M : BM);
   const SplitKPlan plan = splitk_plan(c);
@@ -1863,11 +2285,24 @@ cudaError_t launch_grouped_e4m3(const moe_config& c, const uint8_t* xq_perm,
     d.NT = (c.d_model + BM - 1) / BM;
     return launch_decode<EPI_DOWN, OP_E4M3>(m_wd, m_wd, m_h, m_h, d, max_rows, s);
   }
+  d.NT = (c.d_model + 255) / 256;
+  if (tiles == MOE_TILES_WEIGHT_PAIR) {
+    TokMaps t_xp, t_x, t_h;
+    if (!make_tok_maps(&t_xp, a_r, a_r_rows, c.d_model, true) ||
+        !make_tok_maps(&t_x, a_s, a_s_rows, c.d_model, true) ||
+        !make_tok_maps(&t_h, hq, std::max(R, h_rows), c.d_ff, true))
+      return cudaErrorInvalidValue;
+    g.NT = (c.d_ff + 255) / 256;
+    g.s_max = d.s_max = 1;
+    e = launch_swap_pair<EPI_SWIGLU, OP_E4M3>(m_wg, m_wu, t_xp, t_x, g, (int)(mt_bound * g.NT), s);
+    if (e == cudaSuccess) e = launch_quantize_rows(qh, s);
+    if (e != cudaSuccess) return e;
+    return launch_swap_pair<EPI_DOWN, OP_E4M3>(m_wd, m_wd, t_h, t_h, d, (int)(mt_bound * d.NT), s);
+  }
   e = pair ? launch_pair<EPI_SWIGLU, OP_E4M3>(m_xp, m_x, m_wg, m_wu, g, (int)(mt_bound * g.NT), s)
            : launch_gemm<EPI_SWIGLU, OP_E4M3>(m_xp, m_x, m_wg, m_wu, g, (int)(mt_bound * g.NT), s);
   if (e == cudaSuccess) e = launch_quantize_rows(qh, s);
   if (e != cudaSuccess) return e;
-  d.NT = (c.d_model + 255) / 256;
   return pair ? launch_pair<EPI_DOWN, OP_E4M3>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s)
               : launch_gemm<EPI_DOWN, OP_E4M3>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s);
 }

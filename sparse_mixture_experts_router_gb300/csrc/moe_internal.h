@@ -154,9 +154,11 @@ size_t permute_scratch_bytes(const moe_config& c);
 
 cudaError_t launch_seg_table(const moe_config& c, const int32_t* offsets, int32_t* seg,
                              int tile_m, int* status, cudaStream_t s);
-// The bf16 grouped GEMM runs on CTA pairs with 256-row tiles for large
-// segments (see grouped_sm103.cu); the segment table must then be built
-// with that tile height.
+// Tiling of the bf16 and E4M3 grouped GEMMs (a MOE_TILES_* value other than
+// AUTO): cfg.tiles when it names one that can run, else the library's choice
+// (grouped_sm103.cu). Both CTA-pair tilings cut segments into tiles of at
+// most 256 rows, so the segment table must then be built with that height.
+int gemm_tiles(const moe_config& c);
 bool use_pair_tiles(const moe_config& c);
 int seg_tile_m(const moe_config& c);
 

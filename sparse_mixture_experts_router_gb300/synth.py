@@ -33,6 +33,7 @@ class Workload:
     zipf_s: float = 0.0            # > 0: per-expert Zipf score offset
     seed: int = 0
     capacity_factor: float = 0.0   # > 0: expert capacity ceil(factor * T * k / N)
+    tiles: int = 0                 # grouped-GEMM tiling (moe_config.tiles); 0 = the library's
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)

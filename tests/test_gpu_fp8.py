@@ -111,7 +111,10 @@ FULL = [synth.MIXTRAL_PREFILL, synth.MIXTRAL_DECODE[0], synth.MIXTRAL_DECODE[3],
         # CTA-pair tiles: >= 384 pairs per expert and no K split possible
         # (fp32 partial rows of either projection would exceed 64 MB)
         synth.Workload("fp8_pair_tiles", T=4096, d_model=2176, n_experts=8, top_k=2, d_ff=1024,
-                       n_shared=1, seed=58)]
+                       n_shared=1, seed=58, tiles=2),
+        # weight-stationary CTA pairs: 256 experts of ~200 rows, a K tail
+        synth.Workload("fp8_weight_pair_tiles", T=4096, d_model=1600, n_experts=256, top_k=8,
+                       d_ff=512, n_shared=1, gate_mode=1, sel_bias=True, seed=59, tiles=3)]
 
 
 @pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
@@ -125,7 +128,7 @@ def test_layer_fp8_pair_multi_tile_every_row(oracle):
     projection (persistent walk, both accumulators); y compared on every
     token."""
     w = synth.Workload("fp8_multi_tile_pair", T=16384, d_model=512, n_experts=8, top_k=2,
-                       d_ff=1024, seed=64)
+                       d_ff=1024, seed=64, tiles=2)
     _, counts = check_fp8(oracle, w)
     gu, dn = grouped_tiles(counts, w.T, w.n_shared, w.d_model, w.d_ff, 256)
     grid = torch.cuda.get_device_properties(0).multi_processor_count // 2

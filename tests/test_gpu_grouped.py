@@ -38,15 +38,27 @@ CASES = [
 ]
 
 
+# The same shapes with a named tiling: 256-row CTA pairs, and weight-stationary
+# CTA pairs (token tiles cut to multiples of 16 rows), whatever the library
+# would choose for them.
+FORCED = [c + (t,) for c in CASES if c[7] == "bf16" for t in (2, 3)]
+
+
+@pytest.mark.parametrize("name,T,d,N,k,d_ff,s,dtype,skew,tiles", FORCED,
+                         ids=[f"{c[0]}-tiles{c[-1]}" for c in FORCED])
+def test_grouped_swiglu_tilings_match_oracle(oracle, name, T, d, N, k, d_ff, s, dtype, skew, tiles):
+    test_grouped_swiglu_matches_oracle(oracle, name, T, d, N, k, d_ff, s, dtype, skew, tiles)
+
+
 @pytest.mark.parametrize("name,T,d,N,k,d_ff,s,dtype,skew", CASES, ids=[c[0] for c in CASES])
-def test_grouped_swiglu_matches_oracle(oracle, name, T, d, N, k, d_ff, s, dtype, skew):
+def test_grouped_swiglu_matches_oracle(oracle, name, T, d, N, k, d_ff, s, dtype, skew, tiles=0):
     w = synth.Workload(name, T=T, d_model=d, n_experts=N, top_k=k, d_ff=d_ff, n_shared=s,
                        dtype=dtype, seed=T + d)
     inp = synth.make_inputs(w, "cuda")
     idx = random_idx(T, N, k, seed=T, skew=skew)
     gw = np.random.default_rng(T).uniform(0.05, 1.0, (T, k)).astype(np.float32)
     cfg = moe.config(T=T, d_model=d, n_experts=N, top_k=k, d_ff=d_ff, n_shared=s,
-                     dtype=moe.MOE_BF16 if dtype == "bf16" else moe.MOE_F32)
+                     dtype=moe.MOE_BF16 if dtype == "bf16" else moe.MOE_F32, tiles=tiles)
     P = T * k
     dev = "cuda"
     off = torch.empty(N + 1, dtype=torch.int32, device=dev)

@@ -97,7 +97,12 @@ def test_layer_empty_batch():
 
 
 FULL = [synth.MIXTRAL_PREFILL, *synth.MIXTRAL_DECODE, synth.DEEPSEEK_V3, synth.ZIPF,
-        synth.ZIPF_CAPACITY]
+        synth.ZIPF_CAPACITY,
+        # the large layers on the 256-row CTA-pair tiling, which the library
+        # does not pick for them
+        synth.DEEPSEEK_V3.replace(name="deepseek_v3_moe_pair_tiles", tiles=2),
+        synth.ZIPF.replace(name="zipf_imbalanced_pair_tiles", tiles=2),
+        synth.MIXTRAL_PREFILL.replace(name="mixtral_8x7b_prefill_pair_tiles", tiles=2)]
 
 
 @pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
@@ -116,11 +121,24 @@ def test_layer_full_size(oracle, w):
 MULTI_TILE = [
     # CTA pairs, 256-row tiles: ~1024 gate/up and ~256 down tiles
     (synth.Workload("multi_tile_pair", T=16384, d_model=512, n_experts=8, top_k=2, d_ff=1024,
-                    seed=61), 256),
+                    seed=61, tiles=2), 256),
+    # the same layer on weight-stationary CTA pairs (the library's choice):
+    # ~512 gate/up and ~256 down tiles of 256 features x 256 tokens
+    (synth.Workload("multi_tile_weight_pair", T=16384, d_model=512, n_experts=8, top_k=2,
+                    d_ff=1024, seed=61), 256),
     # 1-CTA, 128-row tiles over ~256-row segments, a shared expert, both
     # DeepSeek-V3 routing options
     (synth.Workload("multi_tile_1cta_shared", T=4096, d_model=768, n_experts=64, top_k=4,
-                    d_ff=512, n_shared=1, gate_mode=1, sel_bias=True, seed=62), 128),
+                    d_ff=512, n_shared=1, gate_mode=1, sel_bias=True, seed=62, tiles=1), 128),
+    # a layer of ~256-row segments on weight-stationary CTA pairs (256
+    # features x <= 256 tokens a tile), and a 256-expert layer of ~128-row
+    # segments on them
+    (synth.Workload("multi_tile_weight_pair_shared", T=4096, d_model=768, n_experts=64,
+                    top_k=4, d_ff=768, n_shared=1, gate_mode=1, sel_bias=True, seed=62,
+                    tiles=3), 256),
+    (synth.Workload("multi_tile_weight_pair_256_experts", T=4096, d_model=1024, n_experts=256,
+                    top_k=8, d_ff=512, n_shared=1, gate_mode=1, sel_bias=True, seed=66,
+                    tiles=3), 256),
 ]
 
 
@@ -129,6 +147,8 @@ def test_layer_multi_tile_every_row(oracle, w, tile_m):
     run, err = check_layer(oracle, w)
     counts = run.counts.cpu().tolist()
     gu, dn = grouped_tiles(counts, w.T, w.n_shared, w.d_model, w.d_ff, tile_m)
+    if w.tiles in (0, 3):  # weight-stationary pairs: 256 features a tile in both projections
+        gu = gu * ((w.d_ff + 255) // 256) // ((w.d_ff + 127) // 128)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     grid = sms // 2 if tile_m == 256 else sms
     assert gu >= 3 * grid and dn >= 3 * grid, (gu, dn, grid)
@@ -148,12 +168,15 @@ def test_layer_decode_split_k_every_row(oracle):
 def test_layer_replays_from_a_cuda_graph(oracle):
     """moe_layer_forward only enqueues stream-ordered work (no host syncs or
     allocations), so it can be captured in a CUDA graph; replays must give
-    the eager result bit for bit, for a prefill-sized (CTA-pair GEMMs) and a
-    decode-sized (split-K) batch."""
+    the eager result bit for bit, for a mid-sized batch (1-CTA tiles with a K
+    split), a decode-sized one (swap-AB decode tiles, split-K) and one on
+    weight-stationary CTA pairs."""
     for w in (synth.Workload("graph_prefill", T=2048, d_model=512, n_experts=4, top_k=2,
                              d_ff=512, seed=41),
               synth.Workload("graph_decode", T=2, d_model=1024, n_experts=8, top_k=2,
-                             d_ff=2048, seed=42)):
+                             d_ff=2048, seed=42),
+              synth.Workload("graph_weight_pair", T=2048, d_model=512, n_experts=4, top_k=2,
+                             d_ff=512, seed=44, tiles=3)):
         inp = margin_inputs(w, oracle)
         run = LayerRun(w, inp)()
         torch.cuda.synchronize()
