@@ -25,8 +25,8 @@
 //             then each warp walks its 256 pairs in order, 32 at a time; a
 //             pair's row is its warp base + the number of lower lanes with
 //             the same expert (__match_any_sync + popc of the lane mask).
-//  gather     - one warp per output row copies the token row with 16-byte
-//               loads and stores.
+//  gather     - one warp per token reads its row once with 16-byte loads
+//               and stores it to the rows of each of its kept pairs.
 // The segment table of the grouped GEMM comes with the first two shapes and
 // from seg_table_kernel after the third.
 #include "device_util.cuh"
@@ -201,27 +201,39 @@ __global__ void __launch_bounds__(kThreads) permute_rank_kernel(const int32_t* _
   }
 }
 
-// One warp per output row: x_perm[row] = x[sorted_pair[row] / k].
+// One warp per token: x_perm[inv_pos[t*k + slot]] = x[t] for every kept
+// slot. The token's row is read from HBM once and written to all of its
+// rows; a row-by-row gather reads a token's row k times, and with x_perm
+// streaming through L2 those repeated reads went back to HBM (DeepSeek-V3
+// shape: about twice the unique bytes). A row is written only when
+// sorted_pair confirms that it holds the pair: a pair dropped by the
+// capacity (-1), or one whose expert index was out of range (reported in the
+// status word; its inv_pos entry is not written), writes nothing.
 __global__ void __launch_bounds__(kThreads) permute_gather_kernel(const uint4* __restrict__ x,
+                                                                  const int32_t* __restrict__ inv_pos,
                                                                   const int32_t* __restrict__ sorted_pair,
-                                                                  const int32_t* __restrict__ offsets,
-                                                                  int N, int P, int k, int vec_per_row,
+                                                                  int T, int P, int k,
+                                                                  int vec_per_row,
                                                                   uint4* __restrict__ x_perm) {
-  const int row = blockIdx.x * kWarps + threadIdx.x / 32;
+  const int t = blockIdx.x * kWarps + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   pdl_wait();
   pdl_trigger();
-  if (row >= P || row >= offsets[N]) return;  // rows past the kept ones stay unwritten
-  // Rows past the last valid pair stay unwritten when some expert index was
-  // out of range (already reported in the status word); never read through
-  // such a row.
-  const int pair = sorted_pair[row];
-  if (pair < 0 || pair >= P) return;
-  const int t = pair / k;
+  if (t >= T) return;
+  const int pair = t * k + lane;
+  int my = lane < k ? __ldg(inv_pos + pair) : -1;
+  if (my < 0 || my >= P || __ldg(sorted_pair + my) != pair) my = -1;
+  int rows[kMaxTopK];
+#pragma unroll
+  for (int s = 0; s < kMaxTopK; ++s) rows[s] = __shfl_sync(0xffffffffu, my, s);
   const uint4* src = x + (size_t)t * vec_per_row;
-  uint4* dst = x_perm + (size_t)row * vec_per_row;
 #pragma unroll 4
-  for (int i = lane; i < vec_per_row; i += 32) dst[i] = __ldg(src + i);
+  for (int i = lane; i < vec_per_row; i += 32) {
+    const uint4 v = __ldg(src + i);
+#pragma unroll
+    for (int s = 0; s < kMaxTopK; ++s)
+      if (s < k && rows[s] >= 0) x_perm[(size_t)rows[s] * vec_per_row + i] = v;
+  }
 }
 
 // The counting, scans and stable ranks of the permutation (and optionally
@@ -493,9 +505,10 @@ cudaError_t launch_permute(const moe_config& c, const void* x, const int32_t* to
   auto gather = [&]() {
     if (x_perm == nullptr) return cudaSuccess;  // the caller gathers (FP8 layer: with quantization)
     ProfScope p(K_PERMUTE_GATHER, s);
-    return launch_pdl(permute_gather_kernel, dim3(ceil_div(P, kWarps)), dim3(kThreads), 0, s, 1,
-                      static_cast<const uint4*>(x), (const int32_t*)sorted_pair,
-                      (const int32_t*)offsets, N, P, c.top_k, vec, static_cast<uint4*>(x_perm));
+    return launch_pdl(permute_gather_kernel, dim3(ceil_div(c.T, kWarps)), dim3(kThreads), 0, s, 1,
+                      static_cast<const uint4*>(x), (const int32_t*)inv_pos,
+                      (const int32_t*)sorted_pair, c.T, P, c.top_k, vec,
+                      static_cast<uint4*>(x_perm));
   };
   if (P <= kChunk) {
     const size_t smem = sizeof(int) * ((size_t)kSmallWarps * N + N + 1);
