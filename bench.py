@@ -328,7 +328,8 @@ def run_ours(args):
     eb = 4 if w.dtype == "f32" else 2
     cfg = moe.config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k, d_ff=w.d_ff,
                      n_shared=w.n_shared, dtype=moe.MOE_F32 if w.dtype == "f32" else moe.MOE_BF16,
-                     gate_mode=w.gate_mode, capacity=capacity_of(w), tiles=args.tiles)
+                     gate_mode=w.gate_mode, capacity=capacity_of(w), tiles=args.tiles,
+                     gather=args.gather)
     y = torch.empty(w.T, w.d_model, dtype=w.torch_dtype, device=dev)
     # Inputs that fit in L2 (the tiny fp32 layer) are timed step by step with
     # L2 flushed (a 256 MB write) before each step; larger ones stream their
@@ -601,6 +602,8 @@ def run_ours(args):
                        "capacity": capacity_of(w) or None,
                        "tiles": {0: "library's choice", 1: "1-CTA", 2: "256-row CTA pairs",
                                  3: "weight-stationary CTA pairs"}[args.tiles],
+                       "gather": {0: "library's choice", 1: "a kernel of its own",
+                                  2: "fused into the gate/up GEMM"}[args.gather],
                        "parallelism": f"replicas x{ws} (per-token layer, no collective)",
                        "l2": (f"inputs ({in_bytes / 1e6:.2f} MB) fit in L2: L2 flushed (256 MB "
                               "write) before every timed step, each step timed on its own"
@@ -994,6 +997,9 @@ def main(argv=None):
     ap.add_argument("--tiles", type=int, choices=[0, 1, 2, 3], default=0,
                     help="grouped-GEMM tiling (moe_config.tiles): 0 the library's choice, 1 1-CTA, "
                          "2 256-row CTA pairs, 3 weight-stationary CTA pairs")
+    ap.add_argument("--gather", type=int, choices=[0, 1, 2], default=0,
+                    help="row gather (moe_config.gather): 0 the library's choice, 1 a kernel of its "
+                         "own, 2 fused into the gate/up GEMM")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per gate_up launch from an ncu capture of this build")
     args = ap.parse_args(argv)

@@ -100,7 +100,25 @@ typedef struct moe_config {
                       * their work. 0 (MOE_TILES_AUTO) lets the library
                       * choose; a named tiling changes only speed, never the
                       * rounding of a result. NVFP4 always runs 1-CTA tiles. */
+  int32_t gather;    /* moe_gather: where moe_layer_forward gathers each
+                      * expert's token rows (bf16). 0 (MOE_GATHER_AUTO) lets
+                      * the library choose; the result is the same bits
+                      * either way. */
 } moe_config;
+
+/* Where the layer's row gather runs (moe_config.gather). */
+typedef enum {
+  MOE_GATHER_AUTO = 0,
+  /* a kernel of its own copies the routed token rows into x_perm, which the
+   * gate/up GEMM reads ("batched kernels" in place of the per-expert loop of
+   * "Mixture of experts and speculative decoding", "A toy MoE layer in
+   * PyTorch") */
+  MOE_GATHER_KERNEL = 1,
+  /* the gate/up GEMM reads the token rows of x itself through the
+   * permutation (no x_perm): only with weight-stationary CTA pairs
+   * (MOE_TILES_WEIGHT_PAIR, bf16); otherwise the kernel above runs */
+  MOE_GATHER_FUSED = 2
+} moe_gather;
 
 /* Tilings of the grouped expert GEMMs (moe_config.tiles). Every tiling
  * computes the same sums in the same order per output element. */

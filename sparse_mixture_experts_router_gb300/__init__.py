@@ -29,6 +29,7 @@ MOE_ERR_DEVICE_CHECK = -7
 MOE_F32, MOE_BF16 = 0, 1
 MOE_GATE_TOPK_SOFTMAX, MOE_GATE_ALL_SOFTMAX_RENORM = 0, 1
 MOE_TILES_AUTO, MOE_TILES_CTA, MOE_TILES_PAIR, MOE_TILES_WEIGHT_PAIR = 0, 1, 2, 3
+MOE_GATHER_AUTO, MOE_GATHER_KERNEL, MOE_GATHER_FUSED = 0, 1, 2
 
 
 class MoeError(RuntimeError):
@@ -41,16 +42,17 @@ class moe_config(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d_model", ctypes.c_int32), ("n_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("gate_mode", ctypes.c_int32),
-                ("capacity", ctypes.c_int32), ("tiles", ctypes.c_int32)]
+                ("capacity", ctypes.c_int32), ("tiles", ctypes.c_int32),
+                ("gather", ctypes.c_int32)]
 
     def __repr__(self):
         return "moe_config(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
 
 
 def config(T, d_model, n_experts, top_k, d_ff, n_shared=0, dtype=MOE_BF16,
-           gate_mode=MOE_GATE_TOPK_SOFTMAX, capacity=0, tiles=0) -> moe_config:
+           gate_mode=MOE_GATE_TOPK_SOFTMAX, capacity=0, tiles=0, gather=0) -> moe_config:
     return moe_config(T, d_model, n_experts, top_k, n_shared, d_ff, dtype, gate_mode, capacity,
-                      tiles)
+                      tiles, gather)
 
 
 def capacity_for(factor: float, T: int, top_k: int, n_experts: int) -> int:

@@ -339,6 +339,7 @@ int moe_check_config(const moe_config* c) {
     return MOE_ERR_INVALID_ARG;
   if (c->top_k > c->n_experts || c->capacity < 0) return MOE_ERR_INVALID_ARG;
   if (c->tiles < MOE_TILES_AUTO || c->tiles > MOE_TILES_WEIGHT_PAIR) return MOE_ERR_INVALID_ARG;
+  if (c->gather < MOE_GATHER_AUTO || c->gather > MOE_GATHER_FUSED) return MOE_ERR_INVALID_ARG;
   if (c->n_experts > kMaxExperts || c->top_k > kMaxTopK || c->n_shared > kMaxShared)
     return MOE_ERR_UNSUPPORTED;
   if (c->d_model % 8 != 0 || c->d_ff % 8 != 0) return MOE_ERR_UNSUPPORTED;
@@ -487,10 +488,13 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* w_router
                                 cnt, ps, w.partials, w.status, s);
   if (e != cudaSuccess) return fail_cuda(e);
   if (c.T == 0) return MOE_OK;
-  e = launch_permute(c, x, idx, cnt, w.offsets, w.sorted_pair, w.inv_pos, w.x_perm, w.hist,
+  // with the gather fused into the gate/up GEMM, x_perm is neither written
+  // nor read
+  void* x_perm = gather_fused(c) ? nullptr : w.x_perm;
+  e = launch_permute(c, x, idx, cnt, w.offsets, w.sorted_pair, w.inv_pos, x_perm, w.hist,
                      w.status, w.seg, seg_tile(c), s);
   if (e != cudaSuccess) return fail_cuda(e);
-  rc = grouped_impl(c, w.x_perm, padded_rows(pairs(c)), x, w.offsets, w.sorted_pair, tw, w_gate,
+  rc = grouped_impl(c, x_perm, padded_rows(pairs(c)), x, w.offsets, w.sorted_pair, tw, w_gate,
                     w_up, w_down, w.y_perm, w.seg, true, w.h, w.partial, w.status, s);
   if (rc != MOE_OK) return rc;
   e = launch_combine(c, w.y_perm, w.inv_pos, nullptr, y, s);

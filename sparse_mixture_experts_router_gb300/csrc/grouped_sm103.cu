@@ -182,6 +182,11 @@ struct GemmArgs {
   __nv_bfloat16* aux;
   long long ld_aux;
   int kb_split;
+  // Gate/up with the row gather fused (weight-stationary pairs, bf16): the
+  // tokens x [T][K] and top-k; the B rows come from x through sorted_pair.
+  const __nv_bfloat16* gx;
+  int gk;
+  int gT;
 };
 
 struct __align__(8) SharedState {
@@ -1195,12 +1200,15 @@ constexpr int SW_MAX_STAGES = 6;
 struct __align__(8) SwapState {
   uint64_t full[SW_MAX_STAGES];
   uint64_t empty[SW_MAX_STAGES];
+  uint64_t gfull[SW_MAX_STAGES];  // fused gather: this CTA's token copies of a stage landed
   uint64_t acc_full[NUM_ACC];
   uint64_t acc_empty[NUM_ACC];  // in the even CTA: arrivals of both CTAs' epilogues
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
+// Warps of the fused gather: one issues the copies, one publishes stages.
+constexpr int SW_GATHER_THREADS = 64;
 
 // Token tile m of a segment of `rows` rows (the segment table counts
 // ceil(rows / 256) tiles): its first row r0 and its rows nr (> 0). The MMA
@@ -1213,14 +1221,15 @@ __device__ __forceinline__ void swap_tile_rows(int rows, int m, int& r0, int& nr
 }
 __device__ __forceinline__ int swap_tile_n(int nr) { return (nr + 31) & ~31; }
 
-template <int EPI, int OP>
-__global__ void __launch_bounds__(G_THREADS, 1)
+template <int EPI, int OP, bool GATHER>
+__global__ void __launch_bounds__(GATHER ? G_THREADS + SW_GATHER_THREADS : G_THREADS, 1)
     grouped_swap_pair_kernel(const __grid_constant__ CUtensorMap map_w0,
                              const __grid_constant__ CUtensorMap map_w1,
                              const __grid_constant__ TokMaps tok,
                              const __grid_constant__ TokMaps tok_sh, const GemmArgs args) {
   using C = Sw<EPI>;
   constexpr bool GU = EPI == EPI_SWIGLU;
+  static_assert(!GATHER || (GU && OP == OP_BF16), "the fused gather is built for bf16 gate/up");
   extern __shared__ uint8_t dyn_smem[];
   __shared__ SwapState st;
 
@@ -1236,8 +1245,11 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::STAGES; ++i) {
-      ptx::mbar_init(ptx::smem_addr(&st.full[i]), 1);
+      // the even CTA's full barrier: the producer's expect-tx arrival, and
+      // with the fused gather one arrival from each CTA's gather warp
+      ptx::mbar_init(ptx::smem_addr(&st.full[i]), GATHER ? 3 : 1);
       ptx::mbar_init(ptx::smem_addr(&st.empty[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&st.gfull[i]), 32);
     }
     for (int i = 0; i < NUM_ACC; ++i) {
       ptx::mbar_init(ptx::smem_addr(&st.acc_full[i]), 1);
@@ -1250,9 +1262,11 @@ __global__ void __launch_bounds__(G_THREADS, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&map_w0);
     ptx::prefetch_tmap(&map_w1);
-    for (int i = 0; i < SW_TOK_BOXES; ++i) {
-      ptx::prefetch_tmap(&tok.box[i]);
-      ptx::prefetch_tmap(&tok_sh.box[i]);
+    if (!GATHER) {
+      for (int i = 0; i < SW_TOK_BOXES; ++i) {
+        ptx::prefetch_tmap(&tok.box[i]);
+        ptx::prefetch_tmap(&tok_sh.box[i]);
+      }
     }
   }
   if (warp == 1) {
@@ -1285,7 +1299,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         const TokMaps* tm = (GU && t.s >= args.n_routed) ? &tok_sh : &tok;
         const int tok_row = __ldg(seg + 3 + (GU ? 2 : 3) * E + t.s) + r0 + (int)rank * half;
         const int w_row = t.s * args.b_rows + t.n * 256 + (int)rank * 128;
-        const uint32_t bytes = (uint32_t)(C::W_BYTES + half * 128);
+        const uint32_t bytes = (uint32_t)(C::W_BYTES + (GATHER ? 0 : half * 128));
         for (int kb = 0; kb < KB; ++kb) {
           if (!wait_phase(ptx::smem_addr(&st.empty[stage]), phase ^ 1u, abort_flag, args.status)) {
             ok = false;
@@ -1298,8 +1312,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           const int kc = kb * Op<OP>::KC;
           ptx::tma_load_2d_pair(w_dst, &map_w0, full_leader, kc, w_row);
           if (GU) ptx::tma_load_2d_pair(w_dst + A_BYTES, &map_w1, full_leader, kc, w_row);
-          ptx::tma_load_2d_pair(w_dst + C::W_BYTES, &tm->box[(half >> 4) - 1], full_leader, kc,
-                                tok_row);
+          if (!GATHER)
+            ptx::tma_load_2d_pair(w_dst + C::W_BYTES, &tm->box[(half >> 4) - 1], full_leader, kc,
+                                  tok_row);
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -1367,6 +1382,96 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       if (!ok) {
         ptx::mma_commit_pair(ptx::smem_addr(&st.drain), 0x1);
         drain_wait(ptx::smem_addr(&st.drain), 0);
+      }
+    }
+  } else if (GATHER && warp == G_THREADS / 32) {
+    // ------------------------------------------ fused row gather (both CTAs) --
+    // The B operand's token rows come straight from x: lane l copies piece
+    // l % 8 (16 bytes) of rows l / 8 + 4 q, q < 32, with cp.async (eight
+    // lanes a 128-byte row, so a warp instruction reads four whole rows)
+    // into the 128-byte-swizzled slot (piece j of row r at j ^ (r % 8)). K
+    // past d_model reads as zero. Each lane keeps its 32 rows' offsets in x
+    // for the whole tile, so a stage is 32 independent copies a lane. The
+    // stage's gfull barrier gets one arrival from each lane when its copies
+    // have landed; the next warp publishes the stage.
+    const __nv_bfloat16* gx = args.gx;
+    const int d = args.K;
+    const int pc = lane & 7;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
+      const Tile t = decode_tile(seg, E, args.NT, tile);
+      const int rows = __ldg(seg + 3 + E + t.s);
+      int r0, nr;
+      swap_tile_rows(rows, t.m, r0, nr);
+      const int half = swap_tile_n(nr) >> 1;
+      const int a_row0 = __ldg(seg + 3 + 2 * E + t.s);
+      // element offset in x of each of this lane's rows, -1 for none
+      long long eoff[32];
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int row = (lane >> 3) + 4 * q;
+        const int r = r0 + (int)rank * half + row;  // row within the segment
+        int tk = -1;
+        if (row < half && r < rows) {
+          if (t.s >= args.n_routed) {
+            tk = r;  // shared experts read x row by row
+          } else {
+            const int pair = __ldg(args.sorted_pair + a_row0 + r);
+            if (pair >= 0 && pair < args.n_pairs) tk = pair / args.gk;
+          }
+        }
+        eoff[q] = tk < 0 ? -1LL : (long long)tk * d;
+      }
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!wait_phase(ptx::smem_addr(&st.empty[stage]), phase ^ 1u, abort_flag, args.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t b_dst = ring + stage * C::STAGE + C::W_BYTES;
+        const int kel = kb * 64 + pc * 8;
+        const uint32_t nbytes = kel < d ? 16u : 0u;  // d_model is a multiple of 8
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          if (eoff[q] < 0) continue;
+          const int row = (lane >> 3) + 4 * q;
+          ptx::cp_async16(b_dst + (uint32_t)(row * 128 + ((pc ^ (row & 7)) << 4)),
+                          nbytes ? (const void*)(gx + eoff[q] + kel) : (const void*)gx, nbytes);
+        }
+        ptx::cp_async_mbar_arrive(ptx::smem_addr(&st.gfull[stage]));
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    ptx::cp_async_wait_all();  // no copy is left in flight when the CTA exits
+  } else if (GATHER && warp == G_THREADS / 32 + 1) {
+    // ------------------------------------- fused gather: publishing a stage --
+    // Waits, stage by stage, until the gather warp's copies have landed,
+    // makes them visible to the tensor cores (a proxy fence; this warp has no
+    // copies of its own in flight, so the fence does not wait for later
+    // stages' copies) and arrives on the even CTA's full barrier.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
+      for (int kb = 0; kb < KB; ++kb) {
+        const bool landed =
+            wait_phase(ptx::smem_addr(&st.gfull[stage]), phase, abort_flag, args.status);
+        if (!__all_sync(0xffffffffu, landed)) {
+          ok = false;
+          break;
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+          ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_addr(&st.full[stage]), 0));
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
     }
   } else {
@@ -2004,14 +2109,15 @@ cudaError_t configure_swap_kernels() {
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device == dev) return cudaSuccess;
-  const void* kernels[4] = {(const void*)grouped_swap_pair_kernel<EPI_SWIGLU, OP_BF16>,
-                            (const void*)grouped_swap_pair_kernel<EPI_DOWN, OP_BF16>,
-                            (const void*)grouped_swap_pair_kernel<EPI_SWIGLU, OP_E4M3>,
-                            (const void*)grouped_swap_pair_kernel<EPI_DOWN, OP_E4M3>};
-  const size_t smem[4] = {Sw<EPI_SWIGLU>::SMEM, Sw<EPI_DOWN>::SMEM, Sw<EPI_SWIGLU>::SMEM,
-                          Sw<EPI_DOWN>::SMEM};
+  const void* kernels[5] = {(const void*)grouped_swap_pair_kernel<EPI_SWIGLU, OP_BF16, false>,
+                            (const void*)grouped_swap_pair_kernel<EPI_DOWN, OP_BF16, false>,
+                            (const void*)grouped_swap_pair_kernel<EPI_SWIGLU, OP_E4M3, false>,
+                            (const void*)grouped_swap_pair_kernel<EPI_DOWN, OP_E4M3, false>,
+                            (const void*)grouped_swap_pair_kernel<EPI_SWIGLU, OP_BF16, true>};
+  const size_t smem[5] = {Sw<EPI_SWIGLU>::SMEM, Sw<EPI_DOWN>::SMEM, Sw<EPI_SWIGLU>::SMEM,
+                          Sw<EPI_DOWN>::SMEM, Sw<EPI_SWIGLU>::SMEM};
   cudaError_t e = cudaSuccess;
-  for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+  for (int i = 0; i < 5 && e == cudaSuccess; ++i)
     e = cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem[i]);
   if (e == cudaSuccess) configured_device = dev;
   return e;
@@ -2027,7 +2133,7 @@ bool make_tok_maps(TokMaps* m, const void* base, long long rows, long long cols,
   return true;
 }
 
-template <int EPI, int OP>
+template <int EPI, int OP, bool GATHER = false>
 cudaError_t launch_swap_pair(const CUtensorMap& w0, const CUtensorMap& w1, const TokMaps& tok,
                              const TokMaps& tok_sh, const GemmArgs& args, int max_tiles,
                              cudaStream_t s) {
@@ -2037,8 +2143,10 @@ cudaError_t launch_swap_pair(const CUtensorMap& w0, const CUtensorMap& w1, const
   const int clusters = std::min(max_tiles, max_pair_clusters());
   if (clusters <= 0) return cudaSuccess;
   ProfScope p(EPI == EPI_SWIGLU ? K_GATE_UP : K_DOWN, s);
-  return launch_pdl(grouped_swap_pair_kernel<EPI, OP>, dim3(2 * clusters), dim3(G_THREADS),
-                    Sw<EPI>::SMEM, s, 2, w0, w1, tok, tok_sh, args);
+  return launch_pdl(grouped_swap_pair_kernel<EPI, OP, GATHER>, dim3(2 * clusters),
+                    dim3(GATHER ? G_THREADS + SW_GATHER_THREADS : G_THREADS), Sw<EPI>::SMEM, s, 2,
+                    w0, w1, tok,
+                    tok_sh, args);
 }
 
 }  // namespace
@@ -2058,6 +2166,11 @@ int gemm_tiles(const moe_config& c) {
   const SplitKPlan plan = splitk_plan(c);
   if (plan.s_max_gu > 1 || plan.s_max_dn > 1 || !pairs_ok) return MOE_TILES_CTA;
   return MOE_TILES_WEIGHT_PAIR;
+}
+
+bool gather_fused(const moe_config& c) {
+  if (c.dtype != MOE_BF16 || gemm_tiles(c) != MOE_TILES_WEIGHT_PAIR) return false;
+  return c.gather == MOE_GATHER_FUSED;
 }
 
 bool use_pair_tiles(const moe_config& c) { return gemm_tiles(c) != MOE_TILES_CTA; }
@@ -2102,10 +2215,15 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
     if (e != cudaSuccess) return e;
   }
 
+  // x_perm is null when the gate/up kernel gathers the rows itself; its maps
+  // then point at x and are not used
+  const bool has_xp = P > 0 && x_perm != nullptr;
+  const void* xp = has_xp ? x_perm : x;
+  const long long xp_n = has_xp ? std::max(P, xp_rows) : c.T;
   CUtensorMap m_xp, m_x, m_wg, m_wu, m_h, m_wd;
   const bool ok =
-      make_map(&m_xp, P > 0 ? x_perm : x, P > 0 ? std::max(P, xp_rows) : c.T, c.d_model) &&
-      make_map(&m_x, c.n_shared > 0 ? x : (P > 0 ? x_perm : x), c.n_shared > 0 ? c.T : (P > 0 ? P : c.T),
+      make_map(&m_xp, xp, xp_n, c.d_model) &&
+      make_map(&m_x, c.n_shared > 0 ? x : xp, c.n_shared > 0 ? c.T : (has_xp ? P : c.T),
                c.d_model) &&
       make_map(&m_wg, w_gate, (long long)E * c.d_ff, c.d_model) &&
       make_map(&m_wu, w_up, (long long)E * c.d_ff, c.d_model) &&
@@ -2113,7 +2231,7 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
       make_map(&m_wd, w_down, (long long)E * c.d_model, c.d_ff);
   if (!ok) return cudaErrorInvalidValue;
 
-  GemmArgs g;
+  GemmArgs g{};
   g.seg = seg;
   g.sorted_pair = sorted_pair;
   g.topk_w = nullptr;
@@ -2135,10 +2253,9 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
   if (decode) {
     // token tiles of 16 rows over x_perm / x (gate/up) and H (down)
     CUtensorMap t_xp, t_x, t_h;
-    const bool ok2 = make_map(&t_xp, P > 0 ? x_perm : x, P > 0 ? std::max(P, xp_rows) : c.T,
-                              c.d_model, TOK_BOX) &&
-                     make_map(&t_x, c.n_shared > 0 ? x : (P > 0 ? x_perm : x),
-                              c.n_shared > 0 ? c.T : (P > 0 ? P : c.T), c.d_model, TOK_BOX) &&
+    const bool ok2 = make_map(&t_xp, xp, xp_n, c.d_model, TOK_BOX) &&
+                     make_map(&t_x, c.n_shared > 0 ? x : xp,
+                              c.n_shared > 0 ? c.T : (has_xp ? P : c.T), c.d_model, TOK_BOX) &&
                      make_map(&t_h, h, std::max(R, h_rows), c.d_ff, TOK_BOX);
     if (!ok2) return cudaErrorInvalidValue;
     const int max_rows = c.T;  // a segment holds at most T rows
@@ -2171,16 +2288,24 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
     // weights on the MMA's M side, 256 features a pair tile; token boxes
     // of 128..8 rows over x_perm / x (gate/up) and H (down)
     TokMaps t_xp, t_x, t_h;
-    if (!make_tok_maps(&t_xp, P > 0 ? x_perm : x, P > 0 ? std::max(P, xp_rows) : c.T, c.d_model,
-                       false) ||
-        !make_tok_maps(&t_x, c.n_shared > 0 ? x : (P > 0 ? x_perm : x),
-                       c.n_shared > 0 ? c.T : (P > 0 ? P : c.T), c.d_model, false) ||
+    if (!make_tok_maps(&t_xp, xp, xp_n, c.d_model, false) ||
+        !make_tok_maps(&t_x, c.n_shared > 0 ? x : xp, c.n_shared > 0 ? c.T : (has_xp ? P : c.T),
+                       c.d_model, false) ||
         !make_tok_maps(&t_h, h, std::max(R, h_rows), c.d_ff, false))
       return cudaErrorInvalidValue;
     g.NT = (c.d_ff + 255) / 256;
     g.s_max = d.s_max = 1;
-    cudaError_t e = launch_swap_pair<EPI_SWIGLU, OP_BF16>(m_wg, m_wu, t_xp, t_x, g,
-                                                          (int)(mt_bound * g.NT), s);
+    cudaError_t e;
+    if (!has_xp && P > 0) {  // the row gather runs inside the gate/up kernel
+      g.gx = static_cast<const __nv_bfloat16*>(x);
+      g.gk = c.top_k;
+      g.gT = c.T;
+      e = launch_swap_pair<EPI_SWIGLU, OP_BF16, true>(m_wg, m_wu, t_xp, t_x, g,
+                                                      (int)(mt_bound * g.NT), s);
+    } else {
+      e = launch_swap_pair<EPI_SWIGLU, OP_BF16>(m_wg, m_wu, t_xp, t_x, g, (int)(mt_bound * g.NT),
+                                                s);
+    }
     if (e != cudaSuccess) return e;
     return launch_swap_pair<EPI_DOWN, OP_BF16>(m_wd, m_wd, t_h, t_h, d, (int)(mt_bound * d.NT), s);
   }
@@ -2220,7 +2345,7 @@ cudaError_t launch_grouped_e4m3(const moe_config& c, const uint8_t* xq_perm,
   const void* a_s = c.n_shared > 0 ? (const void*)xq : a_r;
   const long long a_s_rows = c.n_shared > 0 ? padded_rows(c.T) : a_r_rows;  // x_q is padded
 
-  GemmArgs g;
+  GemmArgs g{};
   g.seg = seg;
   g.sorted_pair = sorted_pair;
   g.topk_w = nullptr;

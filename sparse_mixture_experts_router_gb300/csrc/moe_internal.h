@@ -159,6 +159,9 @@ cudaError_t launch_seg_table(const moe_config& c, const int32_t* offsets, int32_
 // (grouped_sm103.cu). Both CTA-pair tilings cut segments into tiles of at
 // most 256 rows, so the segment table must then be built with that height.
 int gemm_tiles(const moe_config& c);
+// Whether moe_layer_forward fuses the row gather into the gate/up GEMM
+// (bf16, weight-stationary pairs; cfg.gather or the library's choice).
+bool gather_fused(const moe_config& c);
 bool use_pair_tiles(const moe_config& c);
 int seg_tile_m(const moe_config& c);
 

@@ -349,5 +349,22 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask)
       : "memory");
 }
 
+// ---- LSU copies into shared memory (cp.async, 16 bytes a thread) ---------
+// 16 bytes from global to shared memory; with src_bytes = 0 nothing is read
+// and the 16 bytes are zero-filled.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+// The mbarrier at `bar` gets one arrival from this thread once all of its
+// earlier cp.async copies have completed (the barrier's expected count must
+// include it: .noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 }  // namespace ptx
 }  // namespace moe

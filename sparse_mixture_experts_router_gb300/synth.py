@@ -34,6 +34,7 @@ class Workload:
     seed: int = 0
     capacity_factor: float = 0.0   # > 0: expert capacity ceil(factor * T * k / N)
     tiles: int = 0                 # grouped-GEMM tiling (moe_config.tiles); 0 = the library's
+    gather: int = 0                # where the row gather runs (moe_config.gather); 0 = the library's
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)

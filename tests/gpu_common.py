@@ -36,7 +36,8 @@ def cfg_of(w: synth.Workload) -> moe.moe_config:
     return moe.config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k,
                       d_ff=w.d_ff, n_shared=w.n_shared,
                       dtype=moe.MOE_BF16 if w.dtype == "bf16" else moe.MOE_F32,
-                      gate_mode=w.gate_mode, capacity=capacity_of(w), tiles=w.tiles)
+                      gate_mode=w.gate_mode, capacity=capacity_of(w), tiles=w.tiles,
+                      gather=w.gather)
 
 
 def host(t):

@@ -216,3 +216,39 @@ def test_decode_barrier_timeout_is_reported(oracle):
     finally:
         moe.moe_set_decode_barrier_test(0, 0)
     check_layer(oracle, w)
+
+
+# The row gather fused into the gate/up GEMM (weight-stationary pairs): the
+# tensor cores get the same operand values as from x_perm, so y must equal
+# the separate-gather layer's bit for bit, and the oracle within the bar.
+FUSED_GATHER = [
+    synth.Workload("fused_gather_dsv3_small", T=256, d_model=256, n_experts=256, top_k=8,
+                   d_ff=256, n_shared=1, gate_mode=1, sel_bias=True, seed=22, tiles=3),
+    # a K tail (d_model = 200: the last 64-wide K block is part zero-fill),
+    # a shared expert, ragged segments
+    synth.Workload("fused_gather_k_tail_shared", T=700, d_model=200, n_experts=6, top_k=2,
+                   d_ff=136, n_shared=1, seed=45, tiles=3),
+    synth.Workload("fused_gather_capacity", T=1024, d_model=256, n_experts=128, top_k=8,
+                   d_ff=128, zipf_s=1.2, capacity_factor=1.0, seed=26, tiles=3),
+    synth.Workload("fused_gather_multi_tile", T=16384, d_model=512, n_experts=8, top_k=2,
+                   d_ff=1024, seed=61),
+]
+
+
+@pytest.mark.parametrize("w", FUSED_GATHER, ids=lambda w: w.name)
+def test_layer_fused_gather(oracle, w):
+    fused, err = check_layer(oracle, w.replace(gather=2))
+    inp = fused.inp
+    plain = LayerRun(w.replace(gather=1), inp)()
+    assert plain.status() == 0
+    assert torch.equal(fused.y.view(torch.int16), plain.y.view(torch.int16)), w.name
+    print(f"{w.name}: fused gather rel-inf error {err:.3e}, equal to the separate gather")
+
+
+def test_layer_fused_gather_full_size_deepseek(oracle):
+    w = synth.DEEPSEEK_V3.replace(name="deepseek_v3_moe_fused_gather", gather=2)
+    run, err = check_layer(oracle, w, lambda idx: segment_edge_rows(
+        idx, w.n_experts, capacity_of(w), n_random=16, seed=w.seed, max_experts=64))
+    plain = LayerRun(w.replace(gather=1), run.inp)()
+    assert plain.status() == 0
+    assert torch.equal(run.y.view(torch.int16), plain.y.view(torch.int16))
