@@ -321,7 +321,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pk = peaks()
-    w = WORKLOADS[args.workload](synth)
+    w = shaped(WORKLOADS[args.workload](synth), args)
     if w.dtype == "f32" and args.quant:
         raise SystemExit("--fp8 / --nvfp4 take bf16 workloads")
     inp = synth.make_inputs(w, dev, seed=w.seed + 1000 * rank)
@@ -348,7 +348,7 @@ def run_ours(args):
     def step(x):
         fwd(x, y, idx, tw, counts, ps, stream)
 
-    default = args.workload == DEFAULT_WORKLOAD
+    default = args.workload == DEFAULT_WORKLOAD and not reshaped(args)
     for _ in range(args.warmup):
         step(inp["x"])
     torch.cuda.synchronize(dev)
@@ -717,6 +717,21 @@ def run_layer_summary(moe, synth, dev, stream, pk, w, quant, args):
     return out
 
 
+def reshaped(args):
+    return any(v is not None for v in (args.tokens, args.experts, args.d_ff))
+
+
+def shaped(w, args):
+    """The workload with --tokens / --experts / --d-ff applied (a smaller case
+    of the same layer shape, for profiling); its name says so."""
+    if not reshaped(args):
+        return w
+    n = args.experts or w.n_experts
+    w2 = w.replace(T=args.tokens or w.T, n_experts=n, top_k=min(w.top_k, n),
+                   d_ff=args.d_ff or w.d_ff)
+    return w2.replace(name=f"{w.name} (T={w2.T}, {w2.n_experts} experts, d_ff={w2.d_ff})")
+
+
 def run_backward_only(args):
     """The backward alone, on the workload or a smaller case of the same shape
     (--tokens, --experts): one JSON line with the backward object."""
@@ -986,9 +1001,11 @@ def main(argv=None):
     ap.add_argument("--backward-only", action="store_true",
                     help="time only the layer's backward and print its object (for profiling)")
     ap.add_argument("--tokens", type=int, default=None,
-                    help="with --backward-only: tokens T instead of the workload's")
+                    help="tokens T instead of the workload's (a smaller case, for profiling)")
     ap.add_argument("--experts", type=int, default=None,
-                    help="with --backward-only: routed experts N instead of the workload's")
+                    help="routed experts N instead of the workload's (for profiling)")
+    ap.add_argument("--d-ff", type=int, default=None,
+                    help="expert width d_ff instead of the workload's (for profiling)")
     ap.add_argument("--fp8", action="store_true",
                     help="E4M3 expert weights (moe_layer_forward_fp8); not the headline, which is bf16")
     ap.add_argument("--nvfp4", action="store_true",
