@@ -37,6 +37,7 @@ L2_BYTES = 129 * 1024 * 1024  # GB300 L2
 DECODE_MAX_T = 64  # batches up to this size stream the expert weights (decode)
 # Nominal dense tensor rates relative to bf16 (2.25 PFLOP/s): fp8 4.5, fp4 13.5.
 QUANT_PEAK_RATIO = {None: 1.0, "fp8": 4.5 / 2.25, "nvfp4": 13.5 / 2.25}
+SPIN_CYCLES = 200_000  # ~0.1 ms at 2 GHz: covers the host's call latency of a decode step
 
 
 # ----------------------------------------------------------------- helpers --
@@ -371,6 +372,7 @@ def run_ours(args):
         ms_local = 0.0
         for _ in range(args.steps):
             flush.fill_(1)
+            torch.cuda._sleep(SPIN_CYCLES)  # the host's call latency stays outside the events
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -843,9 +845,15 @@ def run_decode(moe, synth, dev, stream, pk, args):
         reps = max(5, min(args.steps, 50))
 
         def timed(fn):
+            # A ~0.1 ms spin kernel after the L2 flush keeps the GPU busy while
+            # the host makes the call (Python marshalling of the step's
+            # arguments takes tens of microseconds, longer than a T = 1 step's
+            # first kernel); the events then bracket the step's own GPU time
+            # and not the host's call latency.
             out = []
             for _ in range(reps):
                 flush.fill_(1)
+                torch.cuda._sleep(SPIN_CYCLES)
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record()

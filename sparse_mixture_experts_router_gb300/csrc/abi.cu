@@ -219,7 +219,8 @@ int seg_tile(const moe_config& c) { return c.dtype == MOE_BF16 ? seg_tile_m(c) :
 int grouped_impl(const moe_config& c, const void* x_perm, long long xp_rows, const void* x,
                  const int32_t* offsets, const int32_t* sorted_pair, const float* topk_w,
                  const void* wg, const void* wu, const void* wd, void* y_perm, int32_t* seg,
-                 bool seg_ready, void* h, float* partial, int* status, cudaStream_t s) {
+                 bool seg_ready, void* h, float* partial, int* status, cudaStream_t s,
+                 const int32_t* inv_pos = nullptr, void* y = nullptr, bool* combined = nullptr) {
   if (rows_total(c) == 0) return MOE_OK;
   cudaError_t e = cudaSuccess;
   if (!seg_ready) {
@@ -228,7 +229,8 @@ int grouped_impl(const moe_config& c, const void* x_perm, long long xp_rows, con
   }
   e = (c.dtype == MOE_BF16)
           ? launch_grouped_bf16(c, x_perm, x, seg, sorted_pair, topk_w, wg, wu, wd, h, y_perm, partial,
-                                xp_rows, padded_rows(rows_total(c)), status, s)
+                                xp_rows, padded_rows(rows_total(c)), status, s, inv_pos, y,
+                                combined)
           : launch_grouped_f32(c, x_perm, x, seg, sorted_pair, topk_w, wg, wu, wd, h, y_perm, status, s);
   return e == cudaSuccess ? MOE_OK : fail_cuda(e);
 }
@@ -494,9 +496,11 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* w_router
   e = launch_permute(c, x, idx, cnt, w.offsets, w.sorted_pair, w.inv_pos, x_perm, w.hist,
                      w.status, w.seg, seg_tile(c), s);
   if (e != cudaSuccess) return fail_cuda(e);
+  bool combined = false;
   rc = grouped_impl(c, x_perm, padded_rows(pairs(c)), x, w.offsets, w.sorted_pair, tw, w_gate,
-                    w_up, w_down, w.y_perm, w.seg, true, w.h, w.partial, w.status, s);
-  if (rc != MOE_OK) return rc;
+                    w_up, w_down, w.y_perm, w.seg, true, w.h, w.partial, w.status, s, w.inv_pos, y,
+                    &combined);
+  if (rc != MOE_OK || combined) return rc;
   e = launch_combine(c, w.y_perm, w.inv_pos, nullptr, y, s);
   return e == cudaSuccess ? MOE_OK : fail_cuda(e);
 }

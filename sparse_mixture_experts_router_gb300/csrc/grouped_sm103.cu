@@ -1976,11 +1976,86 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmArgs a, in
   }
 }
 
+// The down projection's split-K partials reduced straight into y, in place
+// of splitk_reduce_kernel<EPI_DOWN> followed by the combine: for token t,
+//   y[t] = sum over its kept slots, then its shared experts, of
+//          bf16(g * sum over splits of partial[split][row])
+// -- the values the reduction would have written to y_perm, summed in fp32
+// in the combine's order -- so the bits are those of the two kernels. When
+// the GEMM ran unsplit (S = 1, decided on the device as it does) the rows
+// are read from y_perm instead. One thread per token and four output
+// columns; a term's S partial loads are issued together before any is
+// added, as in splitk_reduce_kernel.
+template <int NT>
+__global__ void __launch_bounds__(256) splitk_combine_kernel(const GemmArgs a, int gemm_grid,
+                                                             const int32_t* __restrict__ inv_pos,
+                                                             const float* __restrict__ topk_w,
+                                                             __nv_bfloat16* __restrict__ y, int T,
+                                                             int k, int n_shared) {
+  pdl_wait();
+  pdl_trigger();
+  const int d = a.n_out;
+  const int groups = d / 4;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)T * groups) return;
+  const long long t = i / groups;
+  const int c = (int)(i - t * groups) * 4;
+  const int S = choose_splits(__ldg(a.seg + 1) * a.NT, gemm_grid, (a.K + 63) / 64, a.s_max);
+  const long long P = (long long)T * k;
+  const __nv_bfloat16* yp = static_cast<const __nv_bfloat16*>(a.out);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    if (j >= k + n_shared) break;
+    long long row;
+    float g = 1.0f;
+    if (j < k) {
+      const int pos = __ldg(inv_pos + t * k + j);
+      if (pos < 0 || pos >= P) continue;  // dropped: contributes nothing
+      row = pos;
+      g = __ldg(topk_w + t * k + j);
+    } else {
+      row = P + (long long)(j - k) * T + t;
+    }
+    float v[4];
+    if (S == 1) {
+      const uint2 q = __ldg(reinterpret_cast<const uint2*>(yp + row * a.ldo + c));
+      bf16x2_to_f32(q.x, v[0], v[1]);
+      bf16x2_to_f32(q.y, v[2], v[3]);
+    } else {
+      float4 pv[kMaxSplitK];
+#pragma unroll
+      for (int sp = 0; sp < kMaxSplitK; ++sp)
+        if (sp < S)
+          pv[sp] = __ldcg(
+              reinterpret_cast<const float4*>(a.partial + ((long long)sp * a.R + row) * a.pc + c));
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int sp = 0; sp < kMaxSplitK; ++sp) {
+        if (sp < S) {
+          s4[0] += pv[sp].x;
+          s4[1] += pv[sp].y;
+          s4[2] += pv[sp].z;
+          s4[3] += pv[sp].w;
+        }
+      }
+      const uint32_t p0 = f32x2_to_bf16x2(g * s4[0], g * s4[1]);
+      const uint32_t p1 = f32x2_to_bf16x2(g * s4[2], g * s4[3]);
+      bf16x2_to_f32(p0, v[0], v[1]);
+      bf16x2_to_f32(p1, v[2], v[3]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = fmaf(1.0f, v[q], acc[q]);
+  }
+  *reinterpret_cast<uint2*>(y + t * d + c) =
+      make_uint2(f32x2_to_bf16x2(acc[0], acc[1]), f32x2_to_bf16x2(acc[2], acc[3]));
+}
+
 // ---------------------------------------------------------------- host side --
 template <int EPI, int OP>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_sh, const CUtensorMap& b0,
                         const CUtensorMap& b1, const GemmArgs& args, int max_tiles,
-                        cudaStream_t s, const SfMaps* sf = nullptr) {
+                        cudaStream_t s, const SfMaps* sf = nullptr, bool skip_reduce = false) {
   static const SfMaps no_sf{};  // never read by the bf16 and E4M3 kernels
   static thread_local int configured_device = -1;
   int dev = 0;
@@ -2005,7 +2080,7 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_sh, const CUt
     e = launch_pdl(grouped_gemm_kernel<EPI, OP>, dim3(grid), dim3(Op<OP>::THREADS), Op<OP>::SMEM, s, 1, a,
                    a_sh, b0, b1, args, sf ? *sf : no_sf);
   }
-  if (e != cudaSuccess || args.s_max <= 1) return e;
+  if (e != cudaSuccess || args.s_max <= 1 || skip_reduce) return e;
   const long long n = args.R * (args.n_out / 4);
   ProfScope p(K_SPLITK_REDUCE, s);
   return launch_pdl(splitk_reduce_kernel<EPI, OP>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0,
@@ -2015,7 +2090,7 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a_sh, const CUt
 template <int EPI, int OP>
 cudaError_t launch_decode(const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap& tok,
                           const CUtensorMap& tok_sh, const GemmArgs& args, int max_rows,
-                          cudaStream_t s) {
+                          cudaStream_t s, bool skip_reduce = false) {
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -2038,7 +2113,7 @@ cudaError_t launch_decode(const CUtensorMap& w0, const CUtensorMap& w1, const CU
     e = launch_pdl(grouped_decode_kernel<EPI, OP>, dim3(grid), dim3(THREADS), DYN_SMEM_DECODE, s, 1,
                    w0, w1, tok, tok_sh, args, sh);
   }
-  if (e != cudaSuccess || args.s_max <= 1) return e;
+  if (e != cudaSuccess || args.s_max <= 1 || skip_reduce) return e;
   const long long n = args.R * (args.n_out / 4);
   ProfScope p(K_SPLITK_REDUCE, s);
   return launch_pdl(splitk_reduce_kernel<EPI, OP>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0,
@@ -2112,6 +2187,26 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a_sh, const CUt
   ProfScope p(EPI == EPI_SWIGLU ? K_GATE_UP : K_DOWN, s);
   return launch_pdl(grouped_gemm_pair_kernel<EPI, OP>, dim3(2 * clusters), dim3(G_THREADS),
                     DYN_SMEM_PAIR, s, 2, a, a_sh, b0, b1, args);
+}
+
+cudaError_t launch_splitk_combine(const moe_config& c, const GemmArgs& d, int gemm_grid,
+                                  const int32_t* inv_pos, const float* topk_w, void* y,
+                                  cudaStream_t s) {
+  const int terms = c.top_k + c.n_shared;
+  const dim3 grid((unsigned)ceil_div((long long)c.T * (c.d_model / 4), 256));
+  __nv_bfloat16* yo = static_cast<__nv_bfloat16*>(y);
+  ProfScope p(K_COMBINE, s);
+  if (terms <= 2)
+    return launch_pdl(splitk_combine_kernel<2>, grid, dim3(256), 0, s, 1, d, gemm_grid, inv_pos,
+                      topk_w, yo, c.T, c.top_k, c.n_shared);
+  if (terms <= 4)
+    return launch_pdl(splitk_combine_kernel<4>, grid, dim3(256), 0, s, 1, d, gemm_grid, inv_pos,
+                      topk_w, yo, c.T, c.top_k, c.n_shared);
+  if (terms <= 8)
+    return launch_pdl(splitk_combine_kernel<8>, grid, dim3(256), 0, s, 1, d, gemm_grid, inv_pos,
+                      topk_w, yo, c.T, c.top_k, c.n_shared);
+  return launch_pdl(splitk_combine_kernel<kMaxTopK + kMaxShared>, grid, dim3(256), 0, s, 1, d,
+                    gemm_grid, inv_pos, topk_w, yo, c.T, c.top_k, c.n_shared);
 }
 
 cudaError_t configure_swap_kernels() {
@@ -2210,7 +2305,9 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
                                 const int32_t* seg, const int32_t* sorted_pair,
                                 const float* topk_w, const void* w_gate, const void* w_up,
                                 const void* w_down, void* h, void* y_perm, float* partial,
-                                long long xp_rows, long long h_rows, int* status, cudaStream_t s) {
+                                long long xp_rows, long long h_rows, int* status, cudaStream_t s,
+                                const int32_t* inv_pos, void* y, bool* combined) {
+  if (combined) *combined = false;
   const long long P = (long long)c.T * c.top_k;
   const int E = c.n_experts + c.n_shared;
   const long long R = P + (long long)c.n_shared * c.T;  // rows of H and y_perm
@@ -2281,7 +2378,12 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
     d.b_rows = c.d_model;
     d.s_max = plan.s_max_dn;
     d.pc = c.d_model;
-    return launch_decode<EPI_DOWN, OP_BF16>(m_wd, m_wd, t_h, t_h, d, max_rows, s);
+    // with y given, a split down projection is reduced straight into y
+    const bool fuse = y != nullptr && inv_pos != nullptr && topk_w != nullptr && d.s_max > 1;
+    e = launch_decode<EPI_DOWN, OP_BF16>(m_wd, m_wd, t_h, t_h, d, max_rows, s, fuse);
+    if (e != cudaSuccess || !fuse) return e;
+    *combined = true;
+    return launch_splitk_combine(c, d, num_sms(), inv_pos, topk_w, y, s);
   }
 
   GemmArgs d = g;
@@ -2324,8 +2426,14 @@ cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const v
                        : launch_gemm<EPI_SWIGLU, OP_BF16>(m_xp, m_x, m_wg, m_wu, g,
                                                           (int)(mt_bound * g.NT), s);
   if (e != cudaSuccess) return e;
-  return pair ? launch_pair<EPI_DOWN, OP_BF16>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s)
-              : launch_gemm<EPI_DOWN, OP_BF16>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s);
+  if (pair)
+    return launch_pair<EPI_DOWN, OP_BF16>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s);
+  const bool fuse = y != nullptr && inv_pos != nullptr && topk_w != nullptr && d.s_max > 1;
+  e = launch_gemm<EPI_DOWN, OP_BF16>(m_h, m_h, m_wd, m_wd, d, (int)(mt_bound * d.NT), s, nullptr,
+                                     fuse);
+  if (e != cudaSuccess || !fuse) return e;
+  *combined = true;
+  return launch_splitk_combine(c, d, num_sms(), inv_pos, topk_w, y, s);
 }
 
 cudaError_t launch_grouped_e4m3(const moe_config& c, const uint8_t* xq_perm,

@@ -177,12 +177,16 @@ struct SplitKPlan {
   size_t partial_bytes;    // fp32 partial rows buffer
 };
 SplitKPlan splitk_plan(const moe_config& c);
+// With y and inv_pos given (the layer forward), a down projection that may
+// be split along K is reduced straight into y (the combine fused with the
+// split-K reduction); *combined then says the combine is done.
 cudaError_t launch_grouped_bf16(const moe_config& c, const void* x_perm, const void* x,
                                 const int32_t* seg, const int32_t* sorted_pair,
                                 const float* topk_w, const void* w_gate, const void* w_up,
                                 const void* w_down, void* h, void* y_perm, float* partial,
                                 long long xp_rows, long long h_rows, int* status,
-                                cudaStream_t s);
+                                cudaStream_t s, const int32_t* inv_pos = nullptr,
+                                void* y = nullptr, bool* combined = nullptr);
 // Rows allocated for library-owned x_perm / H: at least one 128-row tile, so
 // that a small batch's tiles read allocated (masked) rows rather than the
 // tensor map's out-of-bounds fill.

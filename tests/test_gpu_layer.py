@@ -252,3 +252,39 @@ def test_layer_fused_gather_full_size_deepseek(oracle):
     plain = LayerRun(w.replace(gather=1), run.inp)()
     assert plain.status() == 0
     assert torch.equal(run.y.view(torch.int16), plain.y.view(torch.int16))
+
+
+@pytest.mark.parametrize("w", [
+    synth.Workload("splitk_combine_decode", T=8, d_model=1024, n_experts=8, top_k=2, d_ff=2048,
+                   seed=46),
+    synth.Workload("splitk_combine_decode_shared", T=40, d_model=512, n_experts=16, top_k=4,
+                   d_ff=1536, n_shared=1, gate_mode=1, sel_bias=True, seed=47),
+    synth.Workload("splitk_combine_1cta", T=300, d_model=768, n_experts=8, top_k=2, d_ff=1024,
+                   capacity_factor=0.8, seed=48),
+], ids=lambda w: w.name)
+def test_layer_split_down_reduced_into_y_matches_separate_kernels(oracle, w):
+    """In the layer forward a down projection split along K is summed
+    straight into y (the split-K reduction and the combine in one kernel).
+    The same routing through the separate entry points (moe_permute,
+    moe_grouped_swiglu with its own reduction, moe_combine) must give y bit
+    for bit, and y must match the oracle."""
+    run, err = check_layer(oracle, w)
+    cfg = run.cfg
+    T, d, N, k = w.T, w.d_model, w.n_experts, w.top_k
+    P = T * k
+    dev = "cuda"
+    inp = run.inp
+    off = torch.empty(N + 1, dtype=torch.int32, device=dev)
+    sp = torch.empty(P, dtype=torch.int32, device=dev)
+    inv = torch.empty(P, dtype=torch.int32, device=dev)
+    xp = torch.empty(max(P, 128), d, dtype=torch.bfloat16, device=dev)
+    wsp = moe.workspace(cfg, "permute")
+    moe.moe_permute(cfg, inp["x"], run.topk_idx, off, sp, inv, xp, wsp)
+    yp = torch.empty(P + w.n_shared * T, d, dtype=torch.bfloat16, device=dev)
+    wsg = moe.workspace(cfg, "grouped")
+    moe.moe_grouped_swiglu(cfg, xp, inp["x"], off, sp, run.topk_w, inp["w_gate"], inp["w_up"],
+                           inp["w_down"], yp, wsg)
+    y2 = torch.empty_like(run.y)
+    moe.moe_combine(cfg, yp, inv, None, y2)
+    assert moe.moe_stream_status(wsg) == 0
+    assert torch.equal(run.y.view(torch.int16), y2.view(torch.int16)), w.name
