@@ -57,6 +57,8 @@ def _declare(lib):
     lib.oracle_route.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P]
     lib.oracle_capacity_keep.argtypes = [_I, _I, _I, _P, _I, _P]
     lib.oracle_permute.argtypes = [_I, _I, _I, _P, _I, _P, _P, _P]
+    lib.oracle_reroute.restype = _I
+    lib.oracle_reroute.argtypes = [_I, _I, _I, _P, _P, _P, _I, _P]
     lib.oracle_expert_swiglu.argtypes = [_I, _I, _I, _P, _P, _P, _P, _P]
     lib.oracle_gated_sum.argtypes = [_I, _I, _P, _P, _P]
     lib.oracle_layer_rows.restype = _I
@@ -209,6 +211,20 @@ class Oracle:
                                 _ptr(inv))
         return offsets, sp[:offsets[N]], inv
 
+    def reroute(self, r32, topk_idx, capacity, sel_bias=None):
+        """(assign [T,k] int32, rounds): the expert each pair runs on when
+        capacity overflow is rerouted in rounds (-1: dropped), and the number
+        of rounds after the capacity cut."""
+        r32 = _c(r32, np.float32)
+        topk_idx = _c(topk_idx, np.int32)
+        T, N = r32.shape
+        k = topk_idx.shape[1]
+        sb = None if sel_bias is None else _c(sel_bias, np.float32)
+        assign = np.empty((T, k), np.int32)
+        rounds = self.lib.oracle_reroute(T, k, N, _ptr(r32), _ptr(sb), _ptr(topk_idx),
+                                         int(capacity), _ptr(assign))
+        return assign, int(rounds)
+
     def expert_swiglu(self, x_row, wg, wu, wd):
         wdt, wg = _stored(wg)
         wdt2, wu = _stored(wu)
@@ -349,25 +365,34 @@ class Oracle:
     # ---- composition: the full layer for a token subset ---------------------
     def layer(self, x, w_router, wg, wu, wd, k, gate_mode=GATE_TOPK_SOFTMAX,
               logit_bias=None, sel_bias=None, n_shared=0, rows=None, capacity=0, fp8=False,
-              nvfp4=False):
+              nvfp4=False, reroute=False):
         """Full forward: router scores for all tokens, routing for all tokens,
         expert outputs for ``rows`` (all tokens when None), with an expert
-        capacity (0 = none). wg/wu/wd are the stacked [N+n_shared, ...]
-        stored arrays (or dicts expert -> array). Returns a dict with r32,
-        topk_idx, topk_w, counts, prob_sum, keep, y."""
+        capacity (0 = none) whose overflow is dropped, or rerouted
+        (``reroute``, see ``reroute``). wg/wu/wd are the stacked
+        [N+n_shared, ...] stored arrays (or dicts expert -> array). Returns a
+        dict with r32, topk_idx, topk_w, counts, prob_sum, keep, assign (the
+        expert each pair runs on, -1 if dropped), rounds, y."""
         _, r32 = self.router_logits(x, w_router, logit_bias)
         idx, w, counts, prob_sum = self.route(r32, k, gate_mode, sel_bias)
         N = r32.shape[1]
         T = r32.shape[0]
-        keep = self.capacity_keep(idx, N, capacity)
+        if reroute:
+            assign, rounds = self.reroute(r32, idx, capacity, sel_bias)
+            keep = (assign.ravel() >= 0).astype(np.uint8)
+        else:
+            keep = self.capacity_keep(idx, N, capacity)
+            assign = np.where(keep.reshape(idx.shape) != 0, idx, -1).astype(np.int32)
+            rounds = 0
         if rows is None:
             rows = np.arange(T, dtype=np.int32)
         rows = np.asarray(rows, np.int32)
-        need = sorted(set(idx[rows].ravel().tolist()) | set(range(N, N + n_shared)))
+        run = np.where(assign >= 0, assign, idx).astype(np.int32)  # dropped: keep says so
+        need = sorted(set(run[rows].ravel().tolist()) | set(range(N, N + n_shared)))
         experts = {e: (wg[e], wu[e], wd[e]) for e in need}
-        y = self.layer_rows(x, experts, idx, w, rows, N, n_shared, keep, fp8, nvfp4)
+        y = self.layer_rows(x, experts, run, w, rows, N, n_shared, keep, fp8, nvfp4)
         return dict(r32=r32, topk_idx=idx, topk_w=w, counts=counts,
-                    prob_sum=prob_sum, keep=keep, y=y, rows=rows)
+                    prob_sum=prob_sum, keep=keep, assign=assign, rounds=rounds, y=y, rows=rows)
 
     def _bwd_inputs(self, x, w_router, wg, wu, wd, k, dy, logit_bias, sel_bias):
         xd, x = _stored(x)

@@ -40,6 +40,9 @@
  *  - Shared experts always run with weight 1 and are not part of f or P.
  *  - f_i = count_i / (T*k) and P_i = mean over tokens of softmax(r)_i over
  *    all N routed experts, so both sum to one as in the pages' example.
+ *  - Capacity overflow is dropped (oracle_capacity_keep), or rerouted in
+ *    rounds to the next-best expert with room (oracle_reroute); the page
+ *    names both without an order.
  *
  * Parity unpinned: the SwiGLU expert at realistic sizes has no printed value
  * on the pages; it is pinned by reduction to library routines (N=1, k=1 is a
@@ -411,12 +414,14 @@ void oracle_capacity_keep(int T, int k, int N, const int32_t* topk_idx, int capa
 /* Rows grouped by expert, kept pairs only (capacity as in
  * oracle_capacity_keep; 0 = none): offsets[e] is the first row of expert e,
  * sorted_pair[row] the pair id t*k+s, inv_pos[pair] its row, or -1 for a
- * dropped pair. [P1] "A toy MoE layer in PyTorch": each expert processes
- * the tokens routed to it. */
+ * dropped pair. An index of -1 marks a pair with no expert (one that
+ * rerouting dropped): it has no row either. [P1] "A toy MoE layer in
+ * PyTorch": each expert processes the tokens routed to it. */
 void oracle_permute(int T, int k, int N, const int32_t* topk_idx, int capacity,
                     int32_t* offsets, int32_t* sorted_pair, int32_t* inv_pos) {
   uint8_t* keep = (uint8_t*)malloc((size_t)T * k + 1);
   oracle_capacity_keep(T, k, N, topk_idx, capacity, keep);
+  for (size_t p = 0; p < (size_t)T * k; ++p) inv_pos[p] = -1;
   int32_t row = 0;
   for (int e = 0; e < N; ++e) {
     offsets[e] = row;
@@ -435,6 +440,105 @@ void oracle_permute(int T, int k, int N, const int32_t* topk_idx, int capacity,
   }
   offsets[N] = row;
   free(keep);
+}
+
+/* Capacity overflow rerouted instead of dropped. [P1] "Keeping the experts
+ * busy": the pairs over an expert's capacity are dropped or rerouted. The
+ * page gives no order; the reading taken here works in rounds:
+ *  round 0  the capacity cut of oracle_capacity_keep. A kept pair stays with
+ *           its expert; the others are pending. room[e] = C - kept at e.
+ *  round r  every pending pair (t, s), in slot order within its token,
+ *           proposes the expert with the highest selection key
+ *           fp32(r + sel_bias) (ties to the lower index) that has room > 0
+ *           at the start of the round, that the token does not hold (its k
+ *           routed experts and those it was rerouted to) and that no lower
+ *           slot of the token proposed to in this round. A pair with no such
+ *           expert is dropped. Each expert then accepts the proposals it got
+ *           in ascending pair id, up to its room; the rest stay pending.
+ * The rounds end when one has no proposal. A rerouted pair keeps its slot's
+ * gate weight. assign[p] is the expert pair p runs on, or -1 if dropped.
+ * A NaN key ranks below every number. capacity = 0 sets no cap (assign =
+ * topk_idx). Returns the number of rounds after round 0. */
+int oracle_reroute(int T, int k, int N, const float* r32, const float* sel_bias,
+                   const int32_t* topk_idx, int capacity, int32_t* assign) {
+  const size_t P = (size_t)T * k;
+  if (capacity == 0) {
+    for (size_t p = 0; p < P; ++p) assign[p] = topk_idx[p];
+    return 0;
+  }
+  enum { PENDING = -2 };
+  uint8_t* keep = (uint8_t*)malloc(P + 1);
+  uint8_t* held = (uint8_t*)calloc((size_t)T * N + 1, 1);
+  uint8_t* tried = (uint8_t*)malloc((size_t)N);
+  int32_t* prop = (int32_t*)malloc(sizeof(int32_t) * (P + 1));
+  int* room = (int*)malloc(sizeof(int) * (size_t)N);
+  int* taken = (int*)malloc(sizeof(int) * (size_t)N);
+  /* round 0: the capacity cut */
+  oracle_capacity_keep(T, k, N, topk_idx, capacity, keep);
+  for (int e = 0; e < N; ++e) room[e] = capacity;
+  for (size_t p = 0; p < P; ++p) {
+    const int e = topk_idx[p];
+    held[(p / k) * N + e] = 1;
+    if (keep[p]) {
+      assign[p] = e;
+      room[e] -= 1;
+    } else {
+      assign[p] = PENDING;
+    }
+  }
+  int rounds = 0;
+  for (;;) {
+    /* proposals */
+    int proposals = 0;
+    for (int t = 0; t < T; ++t) {
+      memset(tried, 0, (size_t)N);
+      for (int s = 0; s < k; ++s) {
+        const size_t p = (size_t)t * k + s;
+        prop[p] = -1;
+        if (assign[p] != PENDING) continue;
+        int best = -1;
+        float best_key = 0.0f;
+        for (int e = 0; e < N; ++e) {
+          if (held[(size_t)t * N + e] || room[e] <= 0 || tried[e]) continue;
+          const float r = r32[(size_t)t * N + e];
+          float key = sel_bias ? (float)((double)r + (double)sel_bias[e]) : r;
+          if (isnan(key)) key = -INFINITY;
+          if (best < 0 || key > best_key) {
+            best = e;
+            best_key = key;
+          }
+        }
+        if (best < 0) {
+          assign[p] = -1;  /* no expert left for it: dropped */
+        } else {
+          prop[p] = best;
+          tried[best] = 1;
+          ++proposals;
+        }
+      }
+    }
+    if (proposals == 0) break;
+    ++rounds;
+    /* each expert accepts in ascending pair id, up to its room */
+    memset(taken, 0, sizeof(int) * (size_t)N);
+    for (size_t p = 0; p < P; ++p) {
+      const int e = prop[p];
+      if (e < 0) continue;
+      if (taken[e] < room[e]) {
+        assign[p] = e;
+        held[(p / k) * N + e] = 1;
+        taken[e] += 1;
+      }
+    }
+    for (int e = 0; e < N; ++e) room[e] -= taken[e];
+  }
+  free(keep);
+  free(held);
+  free(tried);
+  free(prop);
+  free(room);
+  free(taken);
+  return rounds;
 }
 
 /* SiLU(z) = z / (1 + e^-z). */

@@ -440,6 +440,160 @@ def pin_capacity_layer_is_dense_with_dropped_gates_zeroed(o):
     assert np.array_equal(full["y"], base["y"])
 
 
+# ------------------------------------------------------- capacity reroute ---
+# Reading of "Keeping the experts busy" (the extras are dropped or rerouted):
+# after the capacity cut, overflowing pairs re-propose in rounds to their
+# token's best expert (selection key, ties to the lower index) that has room
+# and that the token does not hold; each expert takes proposals in ascending
+# pair id up to its room; a pair with no candidate is dropped.
+
+def _loads(assign, N):
+    a = assign.ravel()
+    return np.bincount(a[a >= 0], minlength=N)
+
+
+def pin_reroute_hand_worked(o):
+    """Worked by hand.
+
+    Case 1 (N=5, k=2, C=1). Scores: t0 [5,4,3,2,1] -> experts 0,1;
+    t1 [5,4,3,3,2] -> 0,1; t2 [4,5,1,3,1] -> 1,0; t3 [5,1,2,0,3] -> 0,4.
+    Pairs p0..p7 = (t0:0,1) (t1:0,1) (t2:1,0) (t3:0,4). The cut: expert 0
+    keeps p0 (p2, p5, p6 pend), expert 1 keeps p1 (p3, p4 pend), expert 4
+    keeps p7. Rooms: e2 = e3 = 1, the rest 0. Round 1: t1's keys for e2 and
+    e3 tie at 3, so p2 proposes e2 (lower index) and p3 e3; t2 prefers e3
+    (3 > 1): p4 -> e3, p5 -> e2; t3 (holds 0 and 4): p6 -> e2 (2 > 0). e2
+    takes p2 (before p5, p6), e3 takes p3 (before p4). Now every expert is
+    full, so p4, p5, p6 are dropped in round 2: one round with proposals.
+
+    Case 2 (N=4, k=1, C=1, all scores 0, selection bias [.1, .4, .3, .2]):
+    every token ranks 1, 2, 3, 0. t0 keeps 1; round 1 gives 2 to t1, round
+    2 gives 3 to t2, round 3 gives 0 to t3, and t4 finds no room: dropped.
+
+    Case 3 (N=4, k=1, C=1, scores [2, NaN, 1, 0] for all three tokens):
+    NaN ranks below every number, so t0 keeps 0, t1 gets 2, t2 gets 3."""
+    r = np.array([[5, 4, 3, 2, 1], [5, 4, 3, 3, 2], [4, 5, 1, 3, 1], [5, 1, 2, 0, 3]], np.float32)
+    idx, _, _, _ = o.route(r, 2)
+    assert idx.tolist() == [[0, 1], [0, 1], [1, 0], [0, 4]]
+    assign, rounds = o.reroute(r, idx, 1)
+    assert assign.tolist() == [[0, 1], [2, 3], [-1, -1], [-1, 4]]
+    assert rounds == 1
+
+    r = np.zeros((5, 4), np.float32)
+    sb = np.array([0.1, 0.4, 0.3, 0.2], np.float32)
+    idx, _, _, _ = o.route(r, 1, sel_bias=sb)
+    assert idx.ravel().tolist() == [1] * 5
+    assign, rounds = o.reroute(r, idx, 1, sel_bias=sb)
+    assert assign.ravel().tolist() == [1, 2, 3, 0, -1]
+    assert rounds == 3
+
+    r = np.array([[2, np.nan, 1, 0]] * 3, np.float32)
+    idx = np.zeros((3, 1), np.int32)
+    assign, rounds = o.reroute(r, idx, 1)
+    assert assign.ravel().tolist() == [0, 2, 3]
+    assert rounds == 2
+
+
+def pin_reroute_identical_rankings_closed_form(o):
+    """When every token has the same scores, the experts rank in one order
+    o_0, o_1, ... (descending key, ties to the lower index). Then each round
+    hands the next k experts of that order to the next C tokens, so token t,
+    slot s runs on o_{k*floor(t/C) + s}, and is dropped when that index
+    reaches N."""
+    rng = _rng(21)
+    for N, k, C, T in [(6, 2, 1, 5), (8, 3, 2, 9), (5, 1, 3, 20), (7, 2, 2, 8), (16, 4, 3, 17)]:
+        row = rng.integers(0, 4, N).astype(np.float32)  # repeated values: ties
+        sb = rng.integers(0, 3, N).astype(np.float32) * 0.5 if N % 2 == 0 else None
+        key = row + (sb if sb is not None else 0)
+        order = sorted(range(N), key=lambda e: (-key[e], e))
+        r = np.tile(row, (T, 1))
+        idx, _, _, _ = o.route(r, k, sel_bias=sb)
+        assign, rounds = o.reroute(r, idx, C, sel_bias=sb)
+        for t in range(T):
+            for s in range(k):
+                j = k * (t // C) + s
+                assert assign[t, s] == (order[j] if j < N else -1), (N, k, C, T, t, s)
+
+
+def pin_reroute_invariants(o):
+    """On random scores (with and without a selection bias, and with ties):
+    no expert runs more than C pairs; a token's experts are distinct; a pair
+    the cut keeps stays on its expert; a rerouted pair runs on an expert
+    outside its token's top k; a pair is dropped only when every expert its
+    token does not hold is full; the rounds stop within N + 1; with C at
+    least the largest count nothing moves."""
+    rng = _rng(22)
+    for T, N, k, C, bias, ties in [(40, 8, 2, 6, False, False), (60, 16, 4, 9, True, False),
+                                   (33, 6, 3, 10, False, True), (50, 12, 1, 2, True, True),
+                                   (80, 32, 8, 15, True, False)]:
+        r = rng.normal(0, 1, (T, N)).astype(np.float32)
+        r += np.linspace(2, 0, N, dtype=np.float32)  # skew: the low experts overflow
+        if ties:
+            r = np.round(r * 2) / 2
+        sb = rng.uniform(-0.5, 0.5, N).astype(np.float32) if bias else None
+        idx, _, counts, _ = o.route(r, k, sel_bias=sb)
+        keep = o.capacity_keep(idx, N, C).reshape(T, k)
+        assign, rounds = o.reroute(r, idx, C, sel_bias=sb)
+        load = _loads(assign, N)
+        assert (load <= C).all()
+        assert 0 <= rounds <= N + 1
+        for t in range(T):
+            got = [e for e in assign[t] if e >= 0]
+            assert len(got) == len(set(got))
+            for s in range(k):
+                if keep[t, s]:
+                    assert assign[t, s] == idx[t, s]
+                elif assign[t, s] >= 0:
+                    assert assign[t, s] not in idx[t]
+                else:
+                    hold = set(idx[t].tolist()) | set(got)
+                    assert all(load[e] == C for e in range(N) if e not in hold), (t, s)
+        assert int((assign >= 0).sum()) >= int(keep.sum())
+        big = int(counts.max())
+        a2, rounds2 = o.reroute(r, idx, big, sel_bias=sb)
+        assert np.array_equal(a2, idx) and rounds2 == 0
+        a0, rounds0 = o.reroute(r, idx, 0, sel_bias=sb)
+        assert np.array_equal(a0, idx) and rounds0 == 0
+
+
+def pin_reroute_without_room_is_dropping(o):
+    """If the cut leaves every expert full, rerouting has nowhere to send the
+    extras: the result is the cut's (kept pairs stay, the rest are -1)."""
+    rng = _rng(23)
+    T, N, k = 64, 8, 2
+    r = rng.normal(0, 1, (T, N)).astype(np.float32)
+    idx, _, counts, _ = o.route(r, k)
+    C = int(counts.min())
+    assert C > 0
+    keep = o.capacity_keep(idx, N, C).reshape(T, k)
+    assign, rounds = o.reroute(r, idx, C)
+    assert np.array_equal(assign, np.where(keep != 0, idx, -1))
+    assert rounds == 0
+
+
+def pin_reroute_layer_is_dense_with_assigned_experts(o):
+    """Brute force: with rerouting, each token's output is the sum over its
+    slots of the slot's gate weight times the FFN of the expert the slot runs
+    on (nothing for a dropped slot), every expert evaluated densely."""
+    rng = _rng(24)
+    T, d, dff, N, k, C = 10, 8, 6, 4, 2, 2
+    x = rng.normal(0, 1, (T, d))
+    Wr = rng.normal(0, 1, (N, d))
+    Wr[0] += 1.5 * x.mean(0)  # expert 0 popular: it overflows
+    wg = rng.normal(0, 0.5, (N, dff, d))
+    wu = rng.normal(0, 0.5, (N, dff, d))
+    wd = rng.normal(0, 0.5, (N, d, dff))
+    out = o.layer(x, Wr, wg, wu, wd, k, capacity=C, reroute=True)
+    assign = out["assign"]
+    assert (assign != out["topk_idx"]).any() and (assign >= 0).any()
+    dense = [_torch_swiglu(x, wg[e], wu[e], wd[e]).numpy() for e in range(N)]
+    for t in range(T):
+        ref = np.zeros(d)
+        for s in range(k):
+            if assign[t, s] >= 0:
+                ref += out["topk_w"][t, s] * dense[assign[t, s]][t]
+        assert np.allclose(out["y"][t], ref, atol=1e-12)
+
+
 # ------------------------------------------------------------------- FP8 ---
 def pin_e4m3_fixed_points(o):
     """E4M3 from its definition (bias 7, 3 mantissa bits, subnormals m*2^-9,

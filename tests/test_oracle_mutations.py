@@ -55,6 +55,16 @@ MUTATIONS = [
     ("nvfp4_token_not_quantized", "for (int i = 0; i < d; ++i) xt[i] = nvfp4_value(xq, xb, &xs, d, 0, i);", "for (int i = 0; i < d; ++i) xt[i] = widen(xdtype, x, (size_t)t * d + i);"),
     ("nvfp4_sign_dropped", "const uint8_t sign = signbit(v) ? 8 : 0;\n  const double a = fabs((double)v);\n  int c;", "const uint8_t sign = 0;\n  const double a = fabs((double)v);\n  int c;"),
     ("fp8_wrong_weight_row_scale", "out[c] = acc * (double)q->ds[c];", "out[c] = acc * (double)q->ds[d - 1 - c];"),
+    ("reroute_tie_to_higher_index", "if (best < 0 || key > best_key) {", "if (best < 0 || key >= best_key) {"),
+    ("reroute_accepts_descending_pairs", "for (size_t p = 0; p < P; ++p) {\n      const int e = prop[p];", "for (size_t p = P; p-- > 0;) {\n      const int e = prop[p];"),
+    ("reroute_ignores_held_experts", "if (held[(size_t)t * N + e] || room[e] <= 0 || tried[e]) continue;", "if (room[e] <= 0 || tried[e]) continue;"),
+    ("reroute_slots_propose_the_same_expert", "if (held[(size_t)t * N + e] || room[e] <= 0 || tried[e]) continue;", "if (held[(size_t)t * N + e] || room[e] <= 0) continue;"),
+    ("reroute_ignores_selection_bias", "float key = sel_bias ? (float)((double)r + (double)sel_bias[e]) : r;", "float key = r;"),
+    ("reroute_nan_not_lowest", "if (isnan(key)) key = -INFINITY;", ""),
+    ("reroute_accepts_up_to_capacity", "if (taken[e] < room[e]) {", "if (taken[e] < capacity) {"),
+    ("reroute_room_not_spent", "for (int e = 0; e < N; ++e) room[e] -= taken[e];", ""),
+    ("reroute_without_cut", "  /* round 0: the capacity cut */\n  oracle_capacity_keep(T, k, N, topk_idx, capacity, keep);", "  /* round 0: the capacity cut */\n  oracle_capacity_keep(T, k, N, topk_idx, 0, keep);"),
+    ("reroute_accepted_expert_not_held", "        held[(p / k) * N + e] = 1;\n        taken[e] += 1;", "        taken[e] += 1;"),
     ("selection_ignores_bias", "key[e] = sel_bias ? (float)((double)rt[e] + (double)sel_bias[e]) : rt[e];", "key[e] = rt[e];"),
     ("bwd_silu_grad_missing_term", "return s * (1.0 + z * (1.0 - s));", "return s;"),
     ("bwd_db_uses_silu_grad", "db[j] = dh * silu(a[j]);", "db[j] = dh * silu_grad(a[j]);"),
