@@ -91,11 +91,12 @@ typedef struct moe_config {
   int32_t capacity;  /* expert capacity C, >= 0; 0 = no cap. With C > 0 each
                       * routed expert runs at most the first C of its (token,
                       * slot) pairs in ascending token order; the others are
-                      * dropped and add nothing to y ("Mixture of experts and
-                      * speculative decoding", "Keeping the experts busy": the
-                      * extras are dropped). Routing, counts and the balance
-                      * statistics are those before the cap; shared experts
-                      * are never capped.                                    */
+                      * dropped and add nothing to y, or rerouted (overflow)
+                      * ("Mixture of experts and speculative decoding",
+                      * "Keeping the experts busy": the extras are dropped or
+                      * rerouted). Routing, counts and the balance statistics
+                      * are those before the cap; shared experts are never
+                      * capped.                                              */
   int32_t tiles;     /* moe_tiles: how the bf16 and E4M3 expert GEMMs cut
                       * their work. 0 (MOE_TILES_AUTO) lets the library
                       * choose; a named tiling changes only speed, never the
@@ -104,7 +105,20 @@ typedef struct moe_config {
                       * expert's token rows (bf16). 0 (MOE_GATHER_AUTO) lets
                       * the library choose; the result is the same bits
                       * either way. */
+  int32_t overflow;  /* moe_overflow: what the layers do with the pairs over
+                      * an expert's capacity (only with capacity > 0) */
 } moe_config;
+
+/* The pairs over an expert's capacity (moe_config.overflow). "Mixture of
+ * experts and speculative decoding", "Keeping the experts busy": the extras
+ * are dropped or rerouted. */
+typedef enum {
+  /* dropped: they add nothing to y (the capacity cut of moe_config.capacity) */
+  MOE_OVERFLOW_DROP = 0,
+  /* rerouted in rounds to the token's next-best expert with room, as
+   * moe_reroute computes; a pair that finds none is dropped */
+  MOE_OVERFLOW_REROUTE = 1
+} moe_overflow;
 
 /* Where the layer's row gather runs (moe_config.gather). */
 typedef enum {
@@ -158,6 +172,7 @@ MOE_API size_t moe_router_workspace_size(const moe_config* cfg);
 MOE_API size_t moe_permute_workspace_size(const moe_config* cfg);
 MOE_API size_t moe_grouped_workspace_size(const moe_config* cfg);
 MOE_API size_t moe_workspace_size(const moe_config* cfg); /* moe_layer_forward */
+MOE_API size_t moe_reroute_workspace_size(const moe_config* cfg);
 
 /*
  * Router scores, top-k selection, gate weights and the per-expert
@@ -244,9 +259,11 @@ MOE_API int moe_router_topk_noalloc_status(moe_stream_t stream);
  * The result is unique, so it is bit-exact and deterministic.
  *
  *  x              [device] [T][d_model] cfg->dtype.
- *  topk_idx       [device] [T][k] int32, each in [0, N). An index out of
- *                 range sets MOE_ERR_DEVICE_CHECK in the workspace status;
- *                 that pair is then left out and the outputs are undefined.
+ *  topk_idx       [device] [T][k] int32, each in [0, N), or -1 for a pair
+ *                 with no expert (one moe_reroute dropped): it gets no row
+ *                 and inv_pos -1. Any other index out of range sets
+ *                 MOE_ERR_DEVICE_CHECK in the workspace status; that pair is
+ *                 then left out and the outputs are undefined.
  *  expert_offsets [device] [N+1] int32 out: exclusive prefix sum of the
  *                 per-expert rows, min(count, cfg->capacity) with a cap,
  *                 else count; expert_offsets[N] = rows kept (T*k uncapped).
@@ -262,6 +279,45 @@ MOE_API int moe_permute(const moe_config* cfg, const void* x, const int32_t* top
                 int32_t* expert_offsets, int32_t* sorted_pair,
                 int32_t* inv_pos, void* x_perm, void* ws, size_t ws_bytes,
                 moe_stream_t stream);
+
+/*
+ * Capacity overflow rerouted instead of dropped ("Mixture of experts and
+ * speculative decoding", "Keeping the experts busy": the pairs over an
+ * expert's capacity are dropped or rerouted; the page gives no order). With
+ * C = cfg->capacity, pair p = t*k + slot:
+ *  - round 0 is the capacity cut: each expert keeps the first C of its pairs
+ *    in ascending pair order; the others are pending;
+ *  - in each later round every pending pair, in slot order within its
+ *    token, proposes the expert with the highest selection key
+ *    fp32(logits + sel_bias) (equal keys: the lower index; NaN below every
+ *    number) that has room left at the start of the round, that the token
+ *    does not hold (its k routed experts and those it was rerouted to) and
+ *    that no lower slot of the token proposed to in this round. A pair with
+ *    no such expert is dropped. Each expert accepts the round's proposals
+ *    in ascending pair id up to its room; the rest stay pending;
+ *  - the rounds end when one has no proposal (at most N + 1 rounds).
+ * The result is unique, so it is bit-exact and deterministic. A rerouted
+ * pair keeps its slot's gate weight. capacity = 0 sets no cap
+ * (assign = topk_idx).
+ *
+ *  logits   [device] [T][N] fp32: the router scores r (moe_router_topk's
+ *           logits_out).
+ *  sel_bias [device] [N] fp32 or NULL: as moe_router_topk.
+ *  topk_idx [device] [T][k] int32: the router's choice. An index outside
+ *           [0, N) sets MOE_ERR_DEVICE_CHECK and that pair is dropped.
+ *  assign   [device] [T][k] int32 out: the expert each pair runs on, -1 for
+ *           a dropped pair; moe_permute takes it in place of topk_idx.
+ *  rounds   [device] int32 out, or NULL: the rounds after the cut.
+ *  ws       [device] moe_reroute_workspace_size(cfg) bytes. Its status word
+ *           records MOE_ERR_TIMEOUT if the kernel's bounded grid barrier
+ *           ran out (outputs then undefined); read it with
+ *           moe_stream_status.
+ * One cooperative launch; its blocks wait on one another, so no other work
+ * may hold the whole GPU while it runs.
+ */
+MOE_API int moe_reroute(const moe_config* cfg, const float* logits, const float* sel_bias,
+                const int32_t* topk_idx, int32_t* assign, int32_t* rounds, void* ws,
+                size_t ws_bytes, moe_stream_t stream);
 
 /*
  * Every expert's SwiGLU FFN over its rows, for all experts in one pass:

@@ -30,6 +30,7 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_GATE_TOPK_SOFTMAX, MOE_GATE_ALL_SOFTMAX_RENORM = 0, 1
 MOE_TILES_AUTO, MOE_TILES_CTA, MOE_TILES_PAIR, MOE_TILES_WEIGHT_PAIR = 0, 1, 2, 3
 MOE_GATHER_AUTO, MOE_GATHER_KERNEL, MOE_GATHER_FUSED = 0, 1, 2
+MOE_OVERFLOW_DROP, MOE_OVERFLOW_REROUTE = 0, 1
 
 
 class MoeError(RuntimeError):
@@ -43,16 +44,17 @@ class moe_config(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("gate_mode", ctypes.c_int32),
                 ("capacity", ctypes.c_int32), ("tiles", ctypes.c_int32),
-                ("gather", ctypes.c_int32)]
+                ("gather", ctypes.c_int32), ("overflow", ctypes.c_int32)]
 
     def __repr__(self):
         return "moe_config(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
 
 
 def config(T, d_model, n_experts, top_k, d_ff, n_shared=0, dtype=MOE_BF16,
-           gate_mode=MOE_GATE_TOPK_SOFTMAX, capacity=0, tiles=0, gather=0) -> moe_config:
+           gate_mode=MOE_GATE_TOPK_SOFTMAX, capacity=0, tiles=0, gather=0,
+           overflow=MOE_OVERFLOW_DROP) -> moe_config:
     return moe_config(T, d_model, n_experts, top_k, n_shared, d_ff, dtype, gate_mode, capacity,
-                      tiles, gather)
+                      tiles, gather, overflow)
 
 
 def capacity_for(factor: float, T: int, top_k: int, n_experts: int) -> int:
@@ -81,6 +83,8 @@ _SIGS = {
     "moe_permute": (_I, [_CFG] + [_P] * 6 + [_P, _SZ, _P]),
     "moe_grouped_swiglu": (_I, [_CFG] + [_P] * 9 + [_P, _SZ, _P]),
     "moe_combine": (_I, [_CFG, _P, _P, _P, _P, _P]),
+    "moe_reroute_workspace_size": (_SZ, [_CFG]),
+    "moe_reroute": (_I, [_CFG] + [_P] * 5 + [_P, _SZ, _P]),
     "moe_layer_forward": (_I, [_CFG] + [_P] * 12 + [_P, _SZ, _P]),
     "moe_quantize_fp8": (_I, [ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P]),
     "moe_workspace_size_fp8": (_SZ, [_CFG]),
@@ -160,7 +164,7 @@ def workspace_size(cfg: moe_config, kind: str = "layer") -> int:
     fn = {"layer": "moe_workspace_size", "router": "moe_router_workspace_size",
           "permute": "moe_permute_workspace_size", "grouped": "moe_grouped_workspace_size",
           "layer_fp8": "moe_workspace_size_fp8", "layer_nvfp4": "moe_workspace_size_nvfp4",
-          "backward": "moe_workspace_size_backward"}[kind]
+          "backward": "moe_workspace_size_backward", "reroute": "moe_reroute_workspace_size"}[kind]
     return int(getattr(lib(), fn)(ctypes.byref(cfg)))
 
 
@@ -193,6 +197,12 @@ def moe_router_topk_noalloc_status(stream=None):
     """Synchronises the stream and returns the device-side status of the last
     moe_router_topk_noalloc call (0, or a negative MOE_ERR_* code)."""
     return lib().moe_router_topk_noalloc_status(_stream(stream))
+
+
+def moe_reroute(cfg, logits, sel_bias, topk_idx, assign, rounds, ws, stream=None):
+    _check("moe_reroute", lib().moe_reroute(
+        ctypes.byref(cfg), _ptr(logits), _ptr(sel_bias), _ptr(topk_idx), _ptr(assign),
+        _ptr(rounds), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)))
 
 
 def moe_permute(cfg, x, topk_idx, expert_offsets, sorted_pair, inv_pos, x_perm, ws, stream=None):

@@ -94,6 +94,11 @@ struct LayerWs {
   void* h;
   float* partial;
   float* dpart;  // the one-kernel decode path's workspace
+  // capacity rerouting only (empty otherwise): the router's scores, the
+  // pairs' experts after the reroute, and the reroute kernel's scratch
+  float* logits;
+  int32_t* assign;
+  void* rr;
 };
 LayerWs carve_layer(Carver& cv, const moe_config& c) {
   LayerWs w;
@@ -115,7 +120,45 @@ LayerWs carve_layer(Carver& cv, const moe_config& c) {
   const SplitKPlan plan = splitk_plan(c);
   w.partial = cv.take<float>(plan.partial_bytes);
   w.dpart = cv.take<float>(decode_fused_ws_bytes(c));
+  const bool rr = reroutes(c);
+  w.logits = cv.take<float>(rr ? sizeof(float) * (size_t)c.T * N : 0);
+  w.assign = cv.take<int32_t>(rr ? sizeof(int32_t) * P : 0);
+  w.rr = cv.take<void>(rr ? reroute_scratch_bytes(c) : 0);
   return w;
+}
+
+// Capacity rerouting without a layer around it.
+struct RerouteWs {
+  int* status;
+  void* rr;
+};
+RerouteWs carve_reroute(Carver& cv, const moe_config& c) {
+  RerouteWs w;
+  w.status = cv.take<int>(256);
+  w.rr = cv.take<void>(reroute_scratch_bytes(c));
+  return w;
+}
+
+// The pairs' experts the permutation groups: the router's choice, or with
+// rerouting on, the reroute kernel's assignment (launched here). Then the
+// cut is already applied and the router's counts no longer hold, so the
+// permutation runs without a cap (*pc) and counts its own pairs.
+struct PermuteIn {
+  const int32_t* idx;
+  const int32_t* counts;
+  moe_config pc;
+};
+cudaError_t overflow_stage(const moe_config& c, const float* sel_bias, const int32_t* idx,
+                           const int32_t* counts, const float* logits, int32_t* assign, void* rr,
+                           int* status, cudaStream_t s, PermuteIn* out) {
+  out->idx = idx;
+  out->counts = counts;
+  out->pc = c;
+  if (!reroutes(c) || c.T == 0) return cudaSuccess;
+  out->idx = assign;
+  out->counts = nullptr;
+  out->pc.capacity = 0;
+  return launch_reroute(c, logits, sel_bias, idx, assign, nullptr, rr, status, s);
 }
 
 // The FP8 layer: the bf16 layer's routing and output buffers, E4M3 copies
@@ -243,7 +286,7 @@ const char* kKernelNames[K_NUM] = {"reset_status",  "router_topk",    "permute_h
                                    "combine",       "balance_stats",  "quantize",
                                    "bwd_gate",      "bwd_score",      "bwd_dh_swiglu",
                                    "bwd_da",        "bwd_dx",         "bwd_router",
-                                   "bwd_wgrad",     "decode_fused"};
+                                   "bwd_wgrad",     "decode_fused",   "reroute"};
 struct Prof {
   std::mutex mu;
   uint32_t mask = 0;
@@ -342,6 +385,8 @@ int moe_check_config(const moe_config* c) {
   if (c->top_k > c->n_experts || c->capacity < 0) return MOE_ERR_INVALID_ARG;
   if (c->tiles < MOE_TILES_AUTO || c->tiles > MOE_TILES_WEIGHT_PAIR) return MOE_ERR_INVALID_ARG;
   if (c->gather < MOE_GATHER_AUTO || c->gather > MOE_GATHER_FUSED) return MOE_ERR_INVALID_ARG;
+  if (c->overflow != MOE_OVERFLOW_DROP && c->overflow != MOE_OVERFLOW_REROUTE)
+    return MOE_ERR_INVALID_ARG;
   if (c->n_experts > kMaxExperts || c->top_k > kMaxTopK || c->n_shared > kMaxShared)
     return MOE_ERR_UNSUPPORTED;
   if (c->d_model % 8 != 0 || c->d_ff % 8 != 0) return MOE_ERR_UNSUPPORTED;
@@ -459,6 +504,30 @@ int moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* inv_po
   return e == cudaSuccess ? MOE_OK : fail_cuda(e);
 }
 
+size_t moe_reroute_workspace_size(const moe_config* c) {
+  if (moe_check_config(c) != MOE_OK) return 0;
+  Carver cv(nullptr);
+  carve_reroute(cv, *c);
+  return align_up(cv.off, 256);
+}
+
+int moe_reroute(const moe_config* cfg, const float* logits, const float* sel_bias,
+                const int32_t* topk_idx, int32_t* assign, int32_t* rounds, void* ws,
+                size_t ws_bytes, moe_stream_t stream) {
+  int rc = moe_check_config(cfg);
+  if (rc != MOE_OK) return rc;
+  const moe_config& c = *cfg;
+  if (c.T > 0 && (!logits || !topk_idx || !assign)) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned({logits, sel_bias, topk_idx, assign, rounds})) return MOE_ERR_MISALIGNED;
+  if ((rc = check_ws(c, ws, ws_bytes, moe_reroute_workspace_size(cfg))) != MOE_OK) return rc;
+  Carver cv(ws);
+  RerouteWs w = carve_reroute(cv, c);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
+  cudaError_t e = launch_reroute(c, logits, sel_bias, topk_idx, assign, rounds, w.rr, w.status, s);
+  return e == cudaSuccess ? MOE_OK : fail_cuda(e);
+}
+
 int moe_layer_forward(const moe_config* cfg, const void* x, const void* w_router,
                       const float* logit_bias, const float* sel_bias, const void* w_gate,
                       const void* w_up, const void* w_down, void* y, int32_t* topk_idx,
@@ -481,20 +550,24 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* w_router
   float* tw = topk_w ? topk_w : w.topk_w;
   int32_t* cnt = counts ? counts : w.counts;
   float* ps = prob_sum ? prob_sum : w.prob_sum;
-  if (decode_fused_applies(c)) {  // a decode-sized batch: the whole layer in one kernel
+  if (decode_fused_applies(c) && !reroutes(c)) {
+    // a decode-sized batch: the whole layer in one kernel
     cudaError_t e = launch_decode_fused(c, x, w_router, logit_bias, sel_bias, w_gate, w_up, w_down,
                                         y, idx, tw, cnt, ps, w.dpart, w.status, s);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e);
   }
-  cudaError_t e = launch_router(c, x, w_router, logit_bias, sel_bias, nullptr, nullptr, idx, tw,
+  cudaError_t e = launch_router(c, x, w_router, logit_bias, sel_bias, nullptr, w.logits, idx, tw,
                                 cnt, ps, w.partials, w.status, s);
   if (e != cudaSuccess) return fail_cuda(e);
   if (c.T == 0) return MOE_OK;
+  PermuteIn pin;
+  if ((e = overflow_stage(c, sel_bias, idx, cnt, w.logits, w.assign, w.rr, w.status, s, &pin)) != cudaSuccess)
+    return fail_cuda(e);
   // with the gather fused into the gate/up GEMM, x_perm is neither written
   // nor read
   void* x_perm = gather_fused(c) ? nullptr : w.x_perm;
-  e = launch_permute(c, x, idx, cnt, w.offsets, w.sorted_pair, w.inv_pos, x_perm, w.hist,
-                     w.status, w.seg, seg_tile(c), s);
+  e = launch_permute(pin.pc, x, pin.idx, pin.counts, w.offsets, w.sorted_pair, w.inv_pos, x_perm,
+                     w.hist, w.status, w.seg, seg_tile(c), s);
   if (e != cudaSuccess) return fail_cuda(e);
   bool combined = false;
   rc = grouped_impl(c, x_perm, padded_rows(pairs(c)), x, w.offsets, w.sorted_pair, tw, w_gate,
@@ -532,6 +605,8 @@ struct BwdWs {
   void* dr_bf;   // [T][n_pad] bf16
   void* drT_bf;  // [n_pad][t_pad] bf16
   void* dab;
+  int32_t* assign;  // capacity rerouting only
+  void* rr;
 };
 int bwd_n_pad(const moe_config& c) { return (c.n_experts + 7) / 8 * 8; }
 int bwd_t_pad(const moe_config& c) { return (c.T + 7) / 8 * 8; }
@@ -561,6 +636,9 @@ BwdWs carve_bwd(Carver& cv, const moe_config& c) {
   w.dr_bf = cv.take<void>(std::max<size_t>(T, 1) * np * 2);
   w.drT_bf = cv.take<void>(np * std::max<size_t>(tp, 8) * 2);
   w.dab = cv.take<void>(R * 2 * f * 2);
+  const bool rr = reroutes(c);
+  w.assign = cv.take<int32_t>(rr ? sizeof(int32_t) * P : 0);
+  w.rr = cv.take<void>(rr ? reroute_scratch_bytes(c) : 0);
   return w;
 }
 
@@ -600,8 +678,12 @@ int moe_layer_backward(const moe_config* cfg, const void* x, const void* w_route
   if (e != cudaSuccess) return fail_cuda(e);
   const long long xp_rows = padded_rows(pairs(c)), r_rows = padded_rows(rows_total(c));
   if (c.T > 0) {
-    e = launch_permute(c, x, w.topk_idx, w.counts, w.offsets, w.sorted_pair, w.inv_pos, w.x_perm,
-                       w.hist, w.status, w.seg, kTileM, s);
+    PermuteIn pin;
+    if ((e = overflow_stage(c, sel_bias, w.topk_idx, w.counts, w.logits, w.assign, w.rr, w.status,
+                            s, &pin)) != cudaSuccess)
+      return fail_cuda(e);
+    e = launch_permute(pin.pc, x, pin.idx, pin.counts, w.offsets, w.sorted_pair, w.inv_pos,
+                       w.x_perm, w.hist, w.status, w.seg, kTileM, s);
     if (e != cudaSuccess) return fail_cuda(e);
     e = launch_bwd_recompute(c, w.x_perm, x, w.seg, w_gate, w_up, w_down, w.h, w.ab, w.o_dA,
                              xp_rows, r_rows, w.status, s);
@@ -691,13 +773,16 @@ int moe_layer_forward_fp8(const moe_config* cfg, const void* x, const void* w_ro
   float* tw = topk_w ? topk_w : w.topk_w;
   int32_t* cnt = counts ? counts : w.counts;
   float* ps = prob_sum ? prob_sum : w.prob_sum;
-  cudaError_t e = launch_router(c, x, w_router, logit_bias, sel_bias, nullptr, nullptr, idx, tw,
+  cudaError_t e = launch_router(c, x, w_router, logit_bias, sel_bias, nullptr, w.logits, idx, tw,
                                 cnt, ps, w.partials, w.status, s);
   if (e != cudaSuccess) return fail_cuda(e);
   if (c.T == 0) return MOE_OK;
   const long long P = pairs(c);
-  e = launch_permute(c, x, idx, cnt, w.offsets, w.sorted_pair, w.inv_pos, nullptr, w.hist,
-                     w.status, w.seg, seg_tile_m(c), s);
+  PermuteIn pin;
+  if ((e = overflow_stage(c, sel_bias, idx, cnt, w.logits, w.assign, w.rr, w.status, s, &pin)) != cudaSuccess)
+    return fail_cuda(e);
+  e = launch_permute(pin.pc, x, pin.idx, pin.counts, w.offsets, w.sorted_pair, w.inv_pos, nullptr,
+                     w.hist, w.status, w.seg, seg_tile_m(c), s);
   if (e != cudaSuccess) return fail_cuda(e);
   // routed rows: gathered and quantized in one pass; their H maxima cleared
   QuantArgs qa{};
@@ -798,14 +883,17 @@ int moe_layer_forward_nvfp4(const moe_config* cfg, const void* x, const void* w_
   float* tw = topk_w ? topk_w : w.topk_w;
   int32_t* cnt = counts ? counts : w.counts;
   float* ps = prob_sum ? prob_sum : w.prob_sum;
-  cudaError_t e = launch_router(c, x, w_router, logit_bias, sel_bias, nullptr, nullptr, idx, tw,
+  cudaError_t e = launch_router(c, x, w_router, logit_bias, sel_bias, nullptr, w.logits, idx, tw,
                                 cnt, ps, w.partials, w.status, s);
   if (e != cudaSuccess) return fail_cuda(e);
   if (c.T == 0) return MOE_OK;
   const long long P = pairs(c);
+  PermuteIn pin;
+  if ((e = overflow_stage(c, sel_bias, idx, cnt, w.logits, w.assign, w.rr, w.status, s, &pin)) != cudaSuccess)
+    return fail_cuda(e);
   // the NVFP4 GEMMs run 128-row tiles
-  e = launch_permute(c, x, idx, cnt, w.offsets, w.sorted_pair, w.inv_pos, nullptr, w.hist,
-                     w.status, w.seg, kTileM, s);
+  e = launch_permute(pin.pc, x, pin.idx, pin.counts, w.offsets, w.sorted_pair, w.inv_pos, nullptr,
+                     w.hist, w.status, w.seg, kTileM, s);
   if (e != cudaSuccess) return fail_cuda(e);
   const int sfd = nvf4_sf_stride(c.d_model);
   // routed rows: gathered and quantized in one pass; their H maxima cleared

@@ -154,6 +154,21 @@ size_t permute_scratch_bytes(const moe_config& c);
 
 cudaError_t launch_seg_table(const moe_config& c, const int32_t* offsets, int32_t* seg,
                              int tile_m, int* status, cudaStream_t s);
+
+// Capacity overflow rerouted in rounds (reroute.cu): assign[p] is the
+// expert pair p runs on, -1 if dropped; *rounds (may be null) the rounds
+// after the capacity cut. One cooperative launch; status[2] must be zero at
+// launch (launch_reset_status). scratch: reroute_scratch_bytes(c) bytes,
+// 256-byte aligned; the optional outputs give its parts' sizes.
+size_t reroute_scratch_bytes(const moe_config& c, size_t* held = nullptr,
+                             size_t* per_pair = nullptr, size_t* pub = nullptr);
+cudaError_t launch_reroute(const moe_config& c, const float* logits, const float* sel_bias,
+                           const int32_t* topk_idx, int32_t* assign, int32_t* rounds,
+                           void* scratch, int* status, cudaStream_t s);
+// Whether a layer reroutes its capacity overflow (cfg.overflow with a cap).
+inline bool reroutes(const moe_config& c) {
+  return c.overflow == MOE_OVERFLOW_REROUTE && c.capacity > 0;
+}
 // Tiling of the bf16 and E4M3 grouped GEMMs (a MOE_TILES_* value other than
 // AUTO): cfg.tiles when it names one that can run, else the library's choice
 // (grouped_sm103.cu). Both CTA-pair tilings cut segments into tiles of at
@@ -294,6 +309,7 @@ enum KernelId {
   K_BWD_ROUTER,
   K_WGRAD,
   K_DECODE_FUSED,
+  K_REROUTE,
   K_NUM
 };
 void prof_begin(int id, cudaStream_t s);

@@ -40,6 +40,10 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = kPermuteChunk;            // 2048 pairs
 constexpr int kPerWarp = kChunk / kWarps;        // 256 pairs
 constexpr int kRounds = kPerWarp / 32;           // 8
+// An expert index of -1 marks a pair with no expert (capacity rerouting
+// dropped it): it gets no row and inv_pos -1, and is not an error.
+constexpr int32_t kNoExpert = -1;
+constexpr int32_t kOutside = -3;  // past the last pair
 
 // Exclusive scan of v[0..n) in place by one warp (32 at a time, carrying the
 // running total); returns the total to every lane.
@@ -106,7 +110,7 @@ __global__ void __launch_bounds__(kThreads) permute_hist_kernel(const int32_t* _
     if (p < P) {
       e = idx[p];
       if (e < 0 || e >= N) {
-        set_status(status, MOE_ERR_DEVICE_CHECK);
+        if (e != kNoExpert) set_status(status, MOE_ERR_DEVICE_CHECK);
         e = -1;
       }
     }
@@ -162,8 +166,9 @@ __global__ void __launch_bounds__(kThreads) permute_rank_kernel(const int32_t* _
 #pragma unroll
   for (int r = 0; r < kRounds; ++r) {
     const int p = base + r * 32 + lane;
-    int e = (p < P) ? idx[p] : -1;
-    if (e >= N) e = -1;
+    int e = (p < P) ? idx[p] : kOutside;
+    if (e == kNoExpert) inv_pos[p] = -1;  // a pair with no expert: no row
+    if (e < 0 || e >= N) e = -1;
     ev[r] = e;
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
@@ -262,8 +267,9 @@ __global__ void __launch_bounds__(kSmallThreads) permute_small_kernel(
     int e = -1;
     if (p < p1) {
       e = idx[p];
+      if (e == kNoExpert) inv_pos[p] = -1;  // a pair with no expert: no row
       if (e < 0 || e >= N) {
-        set_status(status, MOE_ERR_DEVICE_CHECK);
+        if (e != kNoExpert) set_status(status, MOE_ERR_DEVICE_CHECK);
         e = -1;
       }
     }
@@ -297,7 +303,7 @@ __global__ void __launch_bounds__(kSmallThreads) permute_small_kernel(
   for (int b = p0; b < p1; b += 32) {
     const int p = b + lane;
     int e = (p < p1) ? idx[p] : -1;
-    if (e >= N) e = -1;
+    if (e < 0 || e >= N) e = -1;
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     if (e >= 0) {
       const int rank = mine[e] + __popc(peers & lt);  // among expert e's pairs
@@ -364,7 +370,7 @@ __global__ void __launch_bounds__(kGroupThreads) permute_group_kernel(
         const int p = b0 + 32 * r + lane;
         int e = ev[r];
         if (p < p1 && (e < 0 || e >= N)) {
-          set_status(status, MOE_ERR_DEVICE_CHECK);
+          if (e != kNoExpert) set_status(status, MOE_ERR_DEVICE_CHECK);
           e = -1;
         }
         const uint32_t peers = __match_any_sync(0xffffffffu, e);
@@ -435,6 +441,7 @@ __global__ void __launch_bounds__(kGroupThreads) permute_group_kernel(
     for (int r = 0; r < kGroupBatch; ++r) {
       const int p = b0 + 32 * r + lane;
       const int e = ev[r];
+      if (blockIdx.x == 0 && p < p1 && e == kNoExpert) inv_pos[p] = -1;  // no expert: no row
       const bool own = e >= e_lo && e < e_hi;
       const uint32_t peers = __match_any_sync(0xffffffffu, own ? e : -1);
       if (own) {

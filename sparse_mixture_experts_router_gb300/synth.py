@@ -35,6 +35,7 @@ class Workload:
     capacity_factor: float = 0.0   # > 0: expert capacity ceil(factor * T * k / N)
     tiles: int = 0                 # grouped-GEMM tiling (moe_config.tiles); 0 = the library's
     gather: int = 0                # where the row gather runs (moe_config.gather); 0 = the library's
+    overflow: int = 0              # pairs over the capacity (moe_config.overflow): 0 dropped, 1 rerouted
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -61,7 +62,10 @@ ZIPF = Workload("zipf_imbalanced", T=16384, d_model=4096, n_experts=128, top_k=8
 # The imbalanced layer with an expert capacity of 1.25x the even share: the
 # hot experts keep their first 1280 pairs and drop the rest.
 ZIPF_CAPACITY = ZIPF.replace(name="zipf_imbalanced_capacity_1.25", capacity_factor=1.25)
-ALL = [TINY, MIXTRAL_PREFILL, *MIXTRAL_DECODE, DEEPSEEK_V3, ZIPF, ZIPF_CAPACITY]
+# The same cap with the overflow rerouted to each token's next-best expert
+# with room instead of dropped.
+ZIPF_REROUTE = ZIPF_CAPACITY.replace(name="zipf_imbalanced_capacity_1.25_reroute", overflow=1)
+ALL = [TINY, MIXTRAL_PREFILL, *MIXTRAL_DECODE, DEEPSEEK_V3, ZIPF, ZIPF_CAPACITY, ZIPF_REROUTE]
 
 
 def _gen(device, seed):

@@ -37,7 +37,7 @@ def cfg_of(w: synth.Workload) -> moe.moe_config:
                       d_ff=w.d_ff, n_shared=w.n_shared,
                       dtype=moe.MOE_BF16 if w.dtype == "bf16" else moe.MOE_F32,
                       gate_mode=w.gate_mode, capacity=capacity_of(w), tiles=w.tiles,
-                      gather=w.gather)
+                      gather=w.gather, overflow=w.overflow)
 
 
 def host(t):
@@ -48,11 +48,12 @@ def host(t):
     return synth.bf16_bits(t)
 
 
-def margin_inputs(w: synth.Workload, oracle, device="cuda", max_rounds=30):
+def margin_inputs(w: synth.Workload, oracle, device="cuda", max_rounds=30, all_keys=False):
     """Workload inputs whose tokens all have an order margin >= 1e-3: the
-    k+1 largest keys are pairwise at least 1e-3 apart, so the kept set and
-    its order do not depend on how the scores are rounded (tokens below it
-    are redrawn from fresh N(0,1) draws)."""
+    k+1 largest keys (all N with all_keys, which capacity rerouting ranks)
+    are pairwise at least 1e-3 apart, so the kept set and its order do not
+    depend on how the scores are rounded (tokens below it are redrawn from
+    fresh N(0,1) draws)."""
     inp = synth.make_inputs(w, device)
     W = host(inp["w_router"])
     lb = None if inp["logit_bias"] is None else inp["logit_bias"].double().cpu().numpy()
@@ -61,7 +62,7 @@ def margin_inputs(w: synth.Workload, oracle, device="cuda", max_rounds=30):
     for rnd in range(max_rounds):
         xs = host(inp["x"][torch.as_tensor(rows, device=inp["x"].device)])
         r64, _ = oracle.router_logits(xs, W, lb)
-        m = oracle.order_margin(r64, w.top_k, sb)
+        m = oracle.order_margin(r64, w.n_experts - 1 if all_keys else w.top_k, sb)
         bad = rows[m < MIN_MARGIN]
         if bad.size == 0:
             return inp
@@ -94,15 +95,21 @@ def host_weights(inp):
     return _HOST_WEIGHTS[0][1]
 
 
-def oracle_rows(oracle, w, inp, idx, tw, rows, max_experts=40, fp8=False, nvfp4=False):
+def oracle_rows(oracle, w, inp, idx, tw, rows, max_experts=40, fp8=False, nvfp4=False,
+                assign=None):
     """Oracle layer output for the listed tokens. The oracle gets only the
     experts those tokens use, a batch of tokens at a time: FP8 and NVFP4
     quantize every expert they are given, so a batch is limited to
-    max_experts; bf16 and fp32 take all tokens in one batch."""
+    max_experts; bf16 and fp32 take all tokens in one batch. ``assign`` (the
+    oracle's rerouted experts, -1 dropped) replaces the capacity cut."""
     rows = [int(r) for r in rows]
     xh = host(inp["x"])
     wg, wu, wd = host_weights(inp)
-    keep = oracle.capacity_keep(idx, w.n_experts, capacity_of(w))
+    if assign is None:
+        keep = oracle.capacity_keep(idx, w.n_experts, capacity_of(w))
+    else:
+        keep = (np.asarray(assign).ravel() >= 0).astype(np.uint8)
+        idx = np.where(np.asarray(assign) >= 0, assign, idx).astype(np.int32)
     out = np.empty((len(rows), w.d_model), np.float64)
     shared = list(range(w.n_experts, w.n_experts + w.n_shared))
     limit = max_experts if (fp8 or nvfp4) else w.n_experts + w.n_shared

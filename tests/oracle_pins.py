@@ -840,26 +840,29 @@ def _bwd_case(seed, T=5, d=6, N=4, k=2, dff=7, S=1):
                 wd=rng.normal(0, 0.5, (E, d, dff)), dy=rng.normal(0, 1, (T, d)), k=k, n_shared=S)
 
 
-def _loss(o, c, gate_mode, alpha, aux_grad, capacity=0, **over):
-    """sum(dy * y) + aux_grad * aux from the oracle's forward (fp64 inputs)."""
+def _loss(o, c, gate_mode, alpha, aux_grad, capacity=0, reroute=False, **over):
+    """sum(dy * y) + aux_grad * aux from the oracle's forward (fp64 inputs),
+    and the experts the pairs ran on."""
     a = dict(c, **over)
     out = o.layer(a["x"], a["w_router"], a["wg"], a["wu"], a["wd"], a["k"],
-                  gate_mode=gate_mode, n_shared=a["n_shared"], capacity=capacity)
+                  gate_mode=gate_mode, n_shared=a["n_shared"], capacity=capacity,
+                  reroute=reroute)
     T = a["x"].shape[0]
     _, _, aux = o.balance_stats(out["counts"], out["prob_sum"], T, a["k"], alpha)
-    return float((a["dy"] * out["y"]).sum() + aux_grad * aux), out["topk_idx"]
+    ran = np.concatenate([out["topk_idx"], out["assign"]], axis=1)
+    return float((a["dy"] * out["y"]).sum() + aux_grad * aux), ran
 
 
-def _finite_differences(o, c, name, gate_mode, alpha, aux_grad, h, capacity=0):
+def _finite_differences(o, c, name, gate_mode, alpha, aux_grad, h, capacity=0, reroute=False):
     arr = c[name]
     fd = np.zeros_like(arr)
-    base = _loss(o, c, gate_mode, alpha, aux_grad, capacity)[1]
+    base = _loss(o, c, gate_mode, alpha, aux_grad, capacity, reroute)[1]
     for i in np.ndindex(arr.shape):
         plus, minus = arr.copy(), arr.copy()
         plus[i] += h
         minus[i] -= h
-        lp, ip = _loss(o, c, gate_mode, alpha, aux_grad, capacity, **{name: plus})
-        lm, im = _loss(o, c, gate_mode, alpha, aux_grad, capacity, **{name: minus})
+        lp, ip = _loss(o, c, gate_mode, alpha, aux_grad, capacity, reroute, **{name: plus})
+        lm, im = _loss(o, c, gate_mode, alpha, aux_grad, capacity, reroute, **{name: minus})
         assert (ip == base).all() and (im == base).all(), "a step changed the routing"
         fd[i] = (lp - lm) / (2 * h)
     return fd
@@ -886,6 +889,25 @@ def pin_backward_matches_finite_differences(o):
             fd = _finite_differences(o, c, name, mode, 0.01, 3.0, h=1e-3)
             tol = 1e-3 if name in ("x", "w_router") else 1e-5
             assert _rel(g[_GRAD_OF[name]], fd) < tol, (mode, name, _rel(g[_GRAD_OF[name]], fd))
+
+
+def pin_backward_rerouted_matches_finite_differences(o):
+    """With a capacity whose overflow is rerouted, every gradient against
+    central differences of the rerouted forward's loss: a rerouted slot's
+    gate weight multiplies its new expert's output, so the gradient reaches
+    that expert's weights and, through the slot's gate, the router."""
+    c = _bwd_case(26, T=9, N=4, k=2, S=1)
+    c["w_router"][0] += 2.0 * c["x"].mean(0)  # expert 0 popular: it overflows
+    out = o.layer(c["x"], c["w_router"], c["wg"], c["wu"], c["wd"], c["k"], n_shared=1,
+                  capacity=3, reroute=True)
+    moved = (out["assign"] != out["topk_idx"]) & (out["assign"] >= 0)
+    assert moved.any()
+    g = o.layer_backward(c["x"], c["w_router"], c["wg"], c["wu"], c["wd"], c["k"], c["dy"],
+                         n_shared=1, capacity=3, alpha=0.01, aux_grad=2.0, reroute=True)
+    for name in ("x", "w_router", "wg", "wu", "wd"):
+        fd = _finite_differences(o, c, name, 0, 0.01, 2.0, h=1e-3, capacity=3, reroute=True)
+        tol = 1e-3 if name in ("x", "w_router") else 1e-5
+        assert _rel(g[_GRAD_OF[name]], fd) < tol, (name, _rel(g[_GRAD_OF[name]], fd))
 
 
 def pin_backward_balance_term_alone(o):

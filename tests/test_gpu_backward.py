@@ -43,6 +43,8 @@ SMALL = [
                    seed=46),
     synth.Workload("bwd_ragged_dims", T=77, d_model=200, n_experts=4, top_k=2, d_ff=320,
                    n_shared=2, seed=47),
+    synth.Workload("bwd_zipf_reroute", T=300, d_model=128, n_experts=8, top_k=2, d_ff=192,
+                   zipf_s=1.2, capacity_factor=1.0, overflow=1, seed=48),
 ]
 
 
@@ -81,12 +83,13 @@ def oracle_full(oracle, w, inp, dy, aux_grad):
                                  host(inp["w_up"]), host(inp["w_down"]), w.top_k, f64(dy),
                                  gate_mode=w.gate_mode, logit_bias=lb,
                                  sel_bias=host(inp["sel_bias"]), n_shared=w.n_shared,
-                                 capacity=capacity_of(w), alpha=ALPHA, aux_grad=aux_grad)
+                                 capacity=capacity_of(w), alpha=ALPHA, aux_grad=aux_grad,
+                                 reroute=bool(w.overflow))
 
 
 @pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
 def test_backward_small(oracle, w):
-    inp = margin_inputs(w, oracle)
+    inp = margin_inputs(w, oracle, all_keys=bool(w.overflow))
     dy = synth.make_grad_output(w)
     aux_grad = 10.0
     run = BwdRun(w, inp, dy, aux_grad)()

@@ -65,6 +65,7 @@ MUTATIONS = [
     ("reroute_room_not_spent", "for (int e = 0; e < N; ++e) room[e] -= taken[e];", ""),
     ("reroute_without_cut", "  /* round 0: the capacity cut */\n  oracle_capacity_keep(T, k, N, topk_idx, capacity, keep);", "  /* round 0: the capacity cut */\n  oracle_capacity_keep(T, k, N, topk_idx, 0, keep);"),
     ("reroute_accepted_expert_not_held", "        held[(p / k) * N + e] = 1;\n        taken[e] += 1;", "        taken[e] += 1;"),
+    ("bwd_reroute_ignored", "    return R->run[q];", "    return R->idx[q];"),
     ("selection_ignores_bias", "key[e] = sel_bias ? (float)((double)rt[e] + (double)sel_bias[e]) : rt[e];", "key[e] = rt[e];"),
     ("bwd_silu_grad_missing_term", "return s * (1.0 + z * (1.0 - s));", "return s;"),
     ("bwd_db_uses_silu_grad", "db[j] = dh * silu(a[j]);", "db[j] = dh * silu_grad(a[j]);"),
