@@ -86,10 +86,10 @@ def _declare(lib):
     lib.oracle_selection_margin.argtypes = [_I, _I, _I, _P, _P, _P]
     lib.oracle_order_margin.argtypes = [_I, _I, _I, _P, _P, _P]
     _D = ctypes.c_double
-    lib.oracle_layer_backward.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P,
+    lib.oracle_layer_backward.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P,
                                           _P, _P, _P, _P, _P, _D, _D, _P, _P, _P, _P, _P]
     lib.oracle_layer_backward.restype = None
-    lib.oracle_backward_samples.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P,
+    lib.oracle_backward_samples.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P,
                                             _P, _P, _P, _P, _P, _D, _D, _I, _P, _P, _I, _P, _P,
                                             _P, _P, _P]
     lib.oracle_backward_samples.restype = _I
@@ -413,9 +413,9 @@ class Oracle:
 
     def layer_backward(self, x, w_router, wg, wu, wd, k, dy, gate_mode=GATE_TOPK_SOFTMAX,
                        logit_bias=None, sel_bias=None, n_shared=0, capacity=0, alpha=0.01,
-                       aux_grad=1.0):
+                       aux_grad=1.0, reroute=False):
         """Gradients of sum(dy * y) + aux_grad * aux for all tokens (routing
-        held fixed): dict of dx [T,d], dw_router [N,d], dw_gate / dw_up
+        held fixed; capacity overflow dropped, or rerouted with ``reroute``): dict of dx [T,d], dw_router [N,d], dw_gate / dw_up
         [E,d_ff,d], dw_down [E,d,d_ff], fp64. Stacked weight arrays, shared
         experts last (E = N + n_shared)."""
         (xd, x, wdt, w_router, mats, T, d, N, E, d_ff, lb, sb,
@@ -425,15 +425,15 @@ class Oracle:
                    dw_gate=np.empty((E, d_ff, d)), dw_up=np.empty((E, d_ff, d)),
                    dw_down=np.empty((E, d, d_ff)))
         self.lib.oracle_layer_backward(
-            T, d, d_ff, N, k, n_shared, gate_mode, capacity, xd, _ptr(x), wdt, _ptr(w_router),
-            _ptr(lb), _ptr(sb), _ptr(mats[0]), _ptr(mats[1]), _ptr(mats[2]), _ptr(dy),
+            T, d, d_ff, N, k, n_shared, gate_mode, capacity, int(bool(reroute)), xd, _ptr(x), wdt,
+            _ptr(w_router), _ptr(lb), _ptr(sb), _ptr(mats[0]), _ptr(mats[1]), _ptr(mats[2]), _ptr(dy),
             float(alpha), float(aux_grad), _ptr(out["dx"]), _ptr(out["dw_router"]),
             _ptr(out["dw_gate"]), _ptr(out["dw_up"]), _ptr(out["dw_down"]))
         return out
 
     def backward_samples(self, x, w_router, experts, N, k, dy, tokens=(), columns=(),
                          gate_mode=GATE_TOPK_SOFTMAX, logit_bias=None, sel_bias=None,
-                         n_shared=0, capacity=0, alpha=0.01, aux_grad=1.0):
+                         n_shared=0, capacity=0, alpha=0.01, aux_grad=1.0, reroute=False):
         """The same gradients at sampled places: dx rows of ``tokens``; for
         each (e, j) of ``columns`` the row j of dw_gate[e] and dw_up[e] and
         the column j of dw_down[e] (each length d). ``experts`` maps an
@@ -462,8 +462,8 @@ class Oracle:
         out = dict(dx_rows=np.empty((toks.size, d)), dw_gate_rows=np.empty((we.size, d)),
                    dw_up_rows=np.empty((we.size, d)), dw_down_cols=np.empty((we.size, d)))
         rc = self.lib.oracle_backward_samples(
-            T, d, d_ff, N, k, n_shared, gate_mode, capacity, xd, _ptr(x), wdt, _ptr(w_router),
-            _ptr(lb), _ptr(sb), tabs[0], tabs[1], tabs[2], _ptr(dy), float(alpha),
+            T, d, d_ff, N, k, n_shared, gate_mode, capacity, int(bool(reroute)), xd, _ptr(x), wdt,
+            _ptr(w_router), _ptr(lb), _ptr(sb), tabs[0], tabs[1], tabs[2], _ptr(dy), float(alpha),
             float(aux_grad), toks.size, _ptr(toks), _ptr(out["dx_rows"]), we.size, _ptr(we),
             _ptr(wj), _ptr(out["dw_gate_rows"]), _ptr(out["dw_up_rows"]),
             _ptr(out["dw_down_cols"]))

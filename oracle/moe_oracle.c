@@ -1006,21 +1006,29 @@ typedef struct {
   double* g;
   int32_t* counts;
   uint8_t* keep;
+  int32_t* run;  /* the expert each pair runs on, -1 if dropped */
   double* f;
 } Routing;
 
-static void routing_forward(int T, int d, int N, int k, int gate_mode, int capacity, int xdtype,
-                            const void* x, int wdtype, const void* w_router,
-                            const double* logit_bias, const float* sel_bias, Routing* R) {
+static void routing_forward(int T, int d, int N, int k, int gate_mode, int capacity,
+                            int reroute, int xdtype, const void* x, int wdtype,
+                            const void* w_router, const double* logit_bias,
+                            const float* sel_bias, Routing* R) {
   R->r32 = (float*)malloc(sizeof(float) * (size_t)T * N);
   R->idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)T * k);
   R->g = (double*)malloc(sizeof(double) * (size_t)T * k);
   R->counts = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
   R->keep = (uint8_t*)malloc((size_t)T * k + 1);
+  R->run = (int32_t*)malloc(sizeof(int32_t) * ((size_t)T * k + 1));
   R->f = (double*)malloc(sizeof(double) * (size_t)N);
   oracle_router_logits(T, d, N, xdtype, x, wdtype, w_router, logit_bias, NULL, R->r32);
   oracle_route(T, N, k, gate_mode, R->r32, sel_bias, R->idx, R->g, R->counts, NULL);
   oracle_capacity_keep(T, k, N, R->idx, capacity, R->keep);
+  if (reroute) {
+    oracle_reroute(T, k, N, R->r32, sel_bias, R->idx, capacity, R->run);
+  } else {
+    for (size_t q = 0; q < (size_t)T * k; ++q) R->run[q] = R->keep[q] ? R->idx[q] : -1;
+  }
   for (int i = 0; i < N; ++i) R->f[i] = (double)R->counts[i] / ((double)T * (double)k);
 }
 
@@ -1030,20 +1038,22 @@ static void routing_free(Routing* R) {
   free(R->g);
   free(R->counts);
   free(R->keep);
+  free(R->run);
   free(R->f);
 }
 
 /* The expert of term s (< k: routed slot, else shared expert N + s - k) of
- * token t, with its gate (0 for a dropped pair: it is not evaluated). */
+ * token t, with its gate (0 for a dropped pair: it is not evaluated). A
+ * rerouted slot runs on its new expert with the slot's gate. */
 static int term_expert(const Routing* R, int N, int k, int t, int s, double* G) {
   if (s < k) {
     const size_t q = (size_t)t * k + s;
-    if (!R->keep[q]) {
+    if (R->run[q] < 0) {
       *G = 0.0;
       return -1;
     }
     *G = R->g[q];
-    return R->idx[q];
+    return R->run[q];
   }
   *G = 1.0;
   return N + (s - k);
@@ -1053,7 +1063,7 @@ static int term_expert(const Routing* R, int N, int k, int t, int s, double* G) 
  * dwg/dwu [N+s][d_ff][d], dwd [N+s][d][d_ff], all fp64. dy is [T][d] fp64.
  * Weight gradients sum their terms in ascending (token, term) order. */
 void oracle_layer_backward(int T, int d, int d_ff, int N, int k, int n_shared, int gate_mode,
-                           int capacity, int xdtype, const void* x, int wdtype,
+                           int capacity, int reroute, int xdtype, const void* x, int wdtype,
                            const void* w_router, const double* logit_bias,
                            const float* sel_bias, const void* wg, const void* wu,
                            const void* wd, const double* dy, double alpha, double aux_grad,
@@ -1061,8 +1071,8 @@ void oracle_layer_backward(int T, int d, int d_ff, int N, int k, int n_shared, i
                            double* dwd) {
   const int terms = k + n_shared, E = N + n_shared;
   Routing R;
-  routing_forward(T, d, N, k, gate_mode, capacity, xdtype, x, wdtype, w_router, logit_bias,
-                  sel_bias, &R);
+  routing_forward(T, d, N, k, gate_mode, capacity, reroute, xdtype, x, wdtype, w_router,
+                  logit_bias, sel_bias, &R);
   const size_t Q = (size_t)T * terms;
   double* H = (double*)calloc(Q * d_ff, sizeof(double));
   double* DA = (double*)calloc(Q * d_ff, sizeof(double));
@@ -1158,7 +1168,7 @@ void oracle_layer_backward(int T, int d, int d_ff, int N, int k, int n_shared, i
  * no listed token or column uses may be NULL. Returns -1 (and computes
  * nothing) when a needed expert is missing. */
 int oracle_backward_samples(int T, int d, int d_ff, int N, int k, int n_shared, int gate_mode,
-                            int capacity, int xdtype, const void* x, int wdtype,
+                            int capacity, int reroute, int xdtype, const void* x, int wdtype,
                             const void* w_router, const double* logit_bias,
                             const float* sel_bias, const void* const* wg,
                             const void* const* wu, const void* const* wd, const double* dy,
@@ -1167,8 +1177,8 @@ int oracle_backward_samples(int T, int d, int d_ff, int N, int k, int n_shared, 
                             double* dwg_rows, double* dwu_rows, double* dwd_cols) {
   const int terms = k + n_shared;
   Routing R;
-  routing_forward(T, d, N, k, gate_mode, capacity, xdtype, x, wdtype, w_router, logit_bias,
-                  sel_bias, &R);
+  routing_forward(T, d, N, k, gate_mode, capacity, reroute, xdtype, x, wdtype, w_router,
+                  logit_bias, sel_bias, &R);
   int bad = 0;
   for (int n = 0; n < n_tok; ++n)
     for (int s = 0; s < terms; ++s) {
@@ -1255,8 +1265,8 @@ void oracle_balance_backward(int T, int d, int N, int k, int gate_mode, int xdty
                              const double* logit_bias, const float* sel_bias, double alpha,
                              double aux_grad, double* dx, double* dw_router) {
   Routing R;
-  routing_forward(T, d, N, k, gate_mode, 0, xdtype, x, wdtype, w_router, logit_bias, sel_bias,
-                  &R);
+  routing_forward(T, d, N, k, gate_mode, 0, 0, xdtype, x, wdtype, w_router, logit_bias,
+                  sel_bias, &R);
   double* DR = (double*)malloc(sizeof(double) * (size_t)T * N);
 #pragma omp parallel for schedule(static)
   for (int t = 0; t < T; ++t) {
