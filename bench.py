@@ -218,6 +218,41 @@ def gemm_flops(w, counts=None):
     return 4.0 * rows * w.d_model * w.d_ff, 2.0 * rows * w.d_ff * w.d_model
 
 
+def expert_rows(moe, w, cfg, inp, counts, dev, stream):
+    """Rows each routed expert ran in the last step, and a summary of the
+    capacity reroute (None without one). Without a reroute these are the
+    router's counts (gemm_flops and gemm_bytes apply the cut); with one, an
+    untimed pass of the router (scores out) and moe_reroute on the same
+    inputs gives the experts the pairs ran on."""
+    import numpy as np
+    import torch
+    c = counts.cpu().tolist()
+    if not (w.overflow and capacity_of(w)):
+        return c, None
+    T, N, k = w.T, w.n_experts, w.top_k
+    logits = torch.empty(T, N, dtype=torch.float32, device=dev)
+    idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    tw = torch.empty(T, k, dtype=torch.float32, device=dev)
+    cnt = torch.empty(N, dtype=torch.int32, device=dev)
+    ps = torch.empty(N, dtype=torch.float32, device=dev)
+    rws = moe.workspace(cfg, "router", dev)
+    moe.moe_router_topk(cfg, inp["x"], inp["w_router"], inp["logit_bias"], inp["sel_bias"], None,
+                        logits, idx, tw, cnt, ps, rws, stream)
+    assign = torch.empty(T, k, dtype=torch.int32, device=dev)
+    rounds = torch.empty(1, dtype=torch.int32, device=dev)
+    ws = moe.workspace(cfg, "reroute", dev)
+    moe.moe_reroute(cfg, logits, inp["sel_bias"], idx, assign, rounds, ws, stream)
+    if moe.moe_stream_status(ws, stream) != 0:
+        raise RuntimeError(f"{w.name}: moe_reroute failed on the device")
+    a, i0 = assign.cpu().numpy(), idx.cpu().numpy()
+    loads = np.bincount(a[a >= 0], minlength=N).tolist()
+    summary = {"capacity": capacity_of(w), "rounds": int(rounds.item()),
+               "pairs_over_capacity": int(sum(max(0, v - capacity_of(w)) for v in c)),
+               "pairs_rerouted": int(((a != i0) & (a >= 0)).sum()),
+               "pairs_dropped": int((a < 0).sum())}
+    return loads, summary
+
+
 def gemm_bytes(w, counts, quant=None):
     """Algorithmic HBM bytes of the two grouped GEMMs: the weights (and
     scales) of every expert with a row, the A rows read once and the output
@@ -330,7 +365,7 @@ def run_ours(args):
     cfg = moe.config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k, d_ff=w.d_ff,
                      n_shared=w.n_shared, dtype=moe.MOE_F32 if w.dtype == "f32" else moe.MOE_BF16,
                      gate_mode=w.gate_mode, capacity=capacity_of(w), tiles=args.tiles,
-                     gather=args.gather)
+                     gather=args.gather, overflow=w.overflow)
     y = torch.empty(w.T, w.d_model, dtype=w.torch_dtype, device=dev)
     # Inputs that fit in L2 (the tiny fp32 layer) are timed step by step with
     # L2 flushed (a 256 MB write) before each step; larger ones stream their
@@ -461,7 +496,10 @@ def run_ours(args):
     moe.profile_enable(False)
 
     # ---- roofline of the dominant kernel ---------------------------------------
-    f_gu, f_dn = gemm_flops(w, counts.cpu().tolist())
+    # rows each expert ran: the router's counts, cut by the capacity, or
+    # after the capacity reroute
+    loads, rerouted = expert_rows(moe, w, cfg, inp, counts, dev, stream)
+    f_gu, f_dn = gemm_flops(w, loads)
     per_kernel = {}
     for name, (ms, n) in kern.items():
         per_kernel[name] = {"ms_per_launch": ms / n, "launches": n,
@@ -475,7 +513,7 @@ def run_ours(args):
     if "gate_up" not in kern_timed:  # a single token: the whole layer is one kernel
         fused_ms = kern_timed["decode_fused"][0] / kern_timed["decode_fused"][1]
         per_kernel["decode_fused"]["ms_per_launch"] = fused_ms
-        wbytes, _ = touched_weight_bytes(w, counts.cpu().tolist(), args.quant)
+        wbytes, _ = touched_weight_bytes(w, loads, args.quant)
         total = wbytes + w.n_experts * w.d_model * 2 + 2 * w.T * w.d_model * 2
         gbs = total / (fused_ms / 1e3) / 1e9
         per_kernel["decode_fused"]["gbs"] = round(gbs, 1)
@@ -494,7 +532,7 @@ def run_ours(args):
         per_kernel["gate_up"]["tflops"] = f_gu / (gu_ms / 1e3) / 1e12
         per_kernel["down"]["tflops"] = f_dn / (dn_ms / 1e3) / 1e12
         # the same launches against HBM: algorithmic bytes / time
-        b_gu, b_dn = gemm_bytes(w, counts.cpu().tolist(), args.quant)
+        b_gu, b_dn = gemm_bytes(w, loads, args.quant)
         for name, b, ms in (("gate_up", b_gu, gu_ms), ("down", b_dn, dn_ms)):
             per_kernel[name]["algorithmic_bytes"] = b
             per_kernel[name]["gbs"] = round(b / (ms / 1e3) / 1e9, 1)
@@ -564,6 +602,7 @@ def run_ours(args):
     if default and not args.quant and not args.no_others:
         for key, ow, q in (("deepseek_v3_moe", synth.DEEPSEEK_V3, None),
                            ("zipf_imbalanced", synth.ZIPF, None),
+                           ("zipf_imbalanced_capacity_reroute", synth.ZIPF_REROUTE, None),
                            ("mixtral_8x7b_prefill_fp8", synth.MIXTRAL_PREFILL, "fp8"),
                            ("mixtral_8x7b_prefill_nvfp4", synth.MIXTRAL_PREFILL, "nvfp4")):
             others[key] = run_layer_summary(moe, synth, dev, stream, pk, ow, q, args)
@@ -584,7 +623,9 @@ def run_ours(args):
                             "balanced_value": AUX_ALPHA,
                             "f": [round(v, 5) for v in bf.cpu().tolist()],
                             "P": [round(v, 5) for v in bP.cpu().tolist()]}}
-    if capacity_of(w):
+    if rerouted is not None:
+        routing["capacity_reroute"] = rerouted
+    elif capacity_of(w):
         routing["pairs_dropped_by_capacity"] = int(sum(max(0, int(c) - capacity_of(w))
                                                        for c in counts.cpu().tolist()))
 
@@ -606,6 +647,8 @@ def run_ours(args):
                                 "softmax over all scores, kept ones renormalised"][w.gate_mode],
                        "selection_bias": w.sel_bias, "zipf_offset_s": w.zipf_s or None,
                        "capacity": capacity_of(w) or None,
+                       "overflow": (("rerouted" if w.overflow else "dropped")
+                                    if capacity_of(w) else None),
                        "tiles": {0: "library's choice", 1: "1-CTA", 2: "256-row CTA pairs",
                                  3: "weight-stationary CTA pairs"}[args.tiles],
                        "gather": {0: "library's choice", 1: "a kernel of its own",
@@ -648,7 +691,7 @@ def run_layer_summary(moe, synth, dev, stream, pk, w, quant, args):
     inp = synth.make_inputs(w, dev)
     cfg = moe.config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k, d_ff=w.d_ff,
                      n_shared=w.n_shared, dtype=moe.MOE_BF16, gate_mode=w.gate_mode,
-                     capacity=capacity_of(w))
+                     capacity=capacity_of(w), overflow=w.overflow)
     y = torch.empty(w.T, w.d_model, dtype=torch.bfloat16, device=dev)
     idx = torch.empty(w.T, w.top_k, dtype=torch.int32, device=dev)
     tw = torch.empty(w.T, w.top_k, dtype=torch.float32, device=dev)
@@ -682,7 +725,7 @@ def run_layer_summary(moe, synth, dev, stream, pk, w, quant, args):
         step()
     kern = moe.profile_collect()
     moe.profile_enable(False)
-    c = counts.cpu().tolist()
+    c, rerouted = expert_rows(moe, w, cfg, inp, counts, dev, stream)
     f_gu, f_dn = gemm_flops(w, c)
     b_gu, b_dn = gemm_bytes(w, c, quant)
     ratio = QUANT_PEAK_RATIO[quant]
@@ -707,6 +750,8 @@ def run_layer_summary(moe, synth, dev, stream, pk, w, quant, args):
                      # the floor is whichever of the tensor and HBM times is larger
                      "roofline_ms": round(max(f / (tpk * 1e12), by / (pk["hbm"] * 1e9)) * 1e3, 4)}
     out["kernel_ms"] = {k: round(v[0] / v[1], 4) for k, v in kern.items()}
+    if rerouted is not None:
+        out["capacity_reroute"] = rerouted
     out["experts_with_tokens"] = int(sum(1 for v in c if v > 0))
     out["max_over_mean_expert_load"] = round(max(c) / max(1e-9, sum(c) / len(c)), 3)
     if w.zipf_s:
@@ -988,6 +1033,7 @@ WORKLOADS = {
     "deepseek_v3_moe": lambda synth: synth.DEEPSEEK_V3,
     "zipf_imbalanced": lambda synth: synth.ZIPF,
     "zipf_imbalanced_capacity": lambda synth: synth.ZIPF_CAPACITY,
+    "zipf_imbalanced_capacity_reroute": lambda synth: synth.ZIPF_REROUTE,
     **{f"mixtral_8x7b_decode_T{t}": (lambda t_: lambda synth: [w for w in synth.MIXTRAL_DECODE if w.T == t_][0])(t)
        for t in (1, 8, 32, 64)},
 }

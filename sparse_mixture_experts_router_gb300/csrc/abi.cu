@@ -120,10 +120,11 @@ LayerWs carve_layer(Carver& cv, const moe_config& c) {
   const SplitKPlan plan = splitk_plan(c);
   w.partial = cv.take<float>(plan.partial_bytes);
   w.dpart = cv.take<float>(decode_fused_ws_bytes(c));
+  // null unless the layer reroutes: the router then writes no scores
   const bool rr = reroutes(c);
-  w.logits = cv.take<float>(rr ? sizeof(float) * (size_t)c.T * N : 0);
-  w.assign = cv.take<int32_t>(rr ? sizeof(int32_t) * P : 0);
-  w.rr = cv.take<void>(rr ? reroute_scratch_bytes(c) : 0);
+  w.logits = rr ? cv.take<float>(sizeof(float) * (size_t)c.T * N) : nullptr;
+  w.assign = rr ? cv.take<int32_t>(sizeof(int32_t) * P) : nullptr;
+  w.rr = rr ? cv.take<void>(reroute_scratch_bytes(c)) : nullptr;
   return w;
 }
 
@@ -637,8 +638,8 @@ BwdWs carve_bwd(Carver& cv, const moe_config& c) {
   w.drT_bf = cv.take<void>(np * std::max<size_t>(tp, 8) * 2);
   w.dab = cv.take<void>(R * 2 * f * 2);
   const bool rr = reroutes(c);
-  w.assign = cv.take<int32_t>(rr ? sizeof(int32_t) * P : 0);
-  w.rr = cv.take<void>(rr ? reroute_scratch_bytes(c) : 0);
+  w.assign = rr ? cv.take<int32_t>(sizeof(int32_t) * P) : nullptr;
+  w.rr = rr ? cv.take<void>(reroute_scratch_bytes(c)) : nullptr;
   return w;
 }
 
