@@ -52,6 +52,7 @@ constexpr int kRrMaxBlocks = 512;              // bound of the published-count b
 constexpr int kMaxWords = kMaxExperts / 32;    // held-set words per token
 constexpr int32_t kPending = -2;
 constexpr int kNone = INT_MAX;                 // "no candidate" in the argmax
+constexpr int kBatch = 8;                      // published counts loaded at once a thread
 
 struct RerouteArgs {
   const float* logits;      // [T][N] router scores
@@ -105,6 +106,7 @@ __global__ void __launch_bounds__(kRrThreads, 1) reroute_kernel(RerouteArgs a) {
   int* s_cnt = sh;                       // [kRrWarps][N] counts, then bases
   int* s_room = sh + kRrWarps * N;       // [N]
   int* s_tot = s_room + N;               // [N]
+  int* s_base = s_tot + N;               // [N]
   __shared__ int s_any;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int gw = blockIdx.x * kRrWarps + warp;
@@ -207,22 +209,39 @@ __global__ void __launch_bounds__(kRrThreads, 1) reroute_kernel(RerouteArgs a) {
       }
       pub[(size_t)blockIdx.x * N + e] = acc;
     }
+    for (int e = threadIdx.x; e < N; e += kRrThreads) {
+      s_base[e] = 0;
+      s_tot[e] = 0;
+    }
     if (threadIdx.x == 0) s_any = 0;
     if (!rr_grid_barrier(a.status + 2, a.status, (round + 1) * (int)gridDim.x, a.limit_ns)) return;
-    // ---- 3. the block's base and the round's total per expert
-    int any = 0;
-    for (int e = threadIdx.x; e < N; e += kRrThreads) {
-      int base = 0, tot = 0;
-      for (int b = 0; b < (int)gridDim.x; ++b) {
-        const int v = __ldcg(pub + (size_t)b * N + e);
-        base += b < (int)blockIdx.x ? v : 0;
-        tot += v;
+    // ---- 3. the block's base and the round's total per expert: the G x N
+    // published counts are read by all threads at once (kBatch independent
+    // loads in flight each) and summed with shared-memory atomics (integer
+    // sums: the order does not change them)
+    const int total = (int)gridDim.x * N;
+    for (int q0 = threadIdx.x; q0 < total; q0 += kRrThreads * kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int q = q0 + j * kRrThreads;
+        v[j] = q < total ? __ldcg(pub + q) : 0;
       }
-      for (int w = 0; w < kRrWarps; ++w) s_cnt[w * N + e] += base;
-      s_tot[e] = tot;
-      any |= tot;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        if (v[j] != 0) {
+          const int q = q0 + j * kRrThreads;
+          const int b = q / N, e = q - b * N;
+          atomicAdd(&s_tot[e], v[j]);
+          if (b < (int)blockIdx.x) atomicAdd(&s_base[e], v[j]);
+        }
     }
-    if (any) s_any = 1;
+    __syncthreads();
+    for (int e = threadIdx.x; e < N; e += kRrThreads) {
+      const int base = s_base[e];
+      for (int w = 0; w < kRrWarps; ++w) s_cnt[w * N + e] += base;
+      if (s_tot[e] != 0) s_any = 1;
+    }
     __syncthreads();
     if (!s_any) break;  // no proposal in this round: every pair is settled
     for (int t = t_lo; t < t_hi; ++t) {
@@ -287,7 +306,7 @@ cudaError_t launch_reroute(const moe_config& c, const float* logits, const float
   a.W = (c.n_experts + 31) / 32;
   a.capacity = c.capacity;
   a.limit_ns = kWaitLimitNs;
-  const size_t smem = sizeof(int) * ((size_t)kRrWarps * c.n_experts + 2 * c.n_experts);
+  const size_t smem = sizeof(int) * ((size_t)kRrWarps * c.n_experts + 3 * c.n_experts);
   // one block an SM at most (a cooperative grid must be resident at once),
   // and no more blocks than it takes to give every warp a token
   int per_sm = 0;
