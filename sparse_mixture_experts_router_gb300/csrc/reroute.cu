@@ -20,20 +20,28 @@
 //
 // One cooperative kernel runs all rounds. Block b owns a contiguous range of
 // tokens and each of its warps a contiguous sub-range, so (block, warp,
-// token, slot) order is ascending pair order. Per round:
-//  1. propose - each warp walks its tokens; a token's pending slots take, in
-//               slot order, its best eligible experts (a warp argmax over the
-//               token's N keys, one per slot). Each proposal is given its
-//               rank among the warp's proposals to that expert (a per-warp
-//               shared-memory counter; the warp takes its tokens in order).
-//  2. publish - the block's proposal count per expert goes to global memory,
-//               in one of two buffers by round parity; the warp counts become
-//               warp bases inside the block. One grid barrier.
-//  3. accept  - every block sums the published counts of the blocks before it
-//               (its base per expert) and of all blocks (the round's totals).
-//               A proposal is accepted iff block base + warp base + its rank
-//               < room. Every block then takes the totals off its own copy of
-//               room, so all copies agree without a second barrier.
+// token, slot) order is ascending pair order. Round 0's proposals are the
+// routed experts. Then, per round r:
+//  1. publish - the block's count of round-r proposals per expert goes to
+//               global memory, in one of two buffers by round parity; the
+//               per-warp counts become warp bases inside the block. One grid
+//               barrier.
+//  2. totals  - every block sums the published counts of the blocks before it
+//               (its base per expert) and of all blocks (the round's totals),
+//               all threads reading at once. From the totals every block
+//               derives the room left for round r + 1 itself, so all copies
+//               agree without a second barrier. A round without proposals
+//               ends the kernel.
+//  3. walk    - each warp takes its tokens in order, once: a round-r proposal
+//               is accepted iff block base + warp base + its rank among the
+//               warp's proposals to that expert < room; then the token's
+//               still-pending slots take, in slot order, its best eligible
+//               experts for round r + 1 (a warp argmax over the token's N
+//               keys, one per slot), each ranked by a per-warp shared-memory
+//               counter. A token's state, scores and held set are loaded
+//               together, and the next token's loads are issued before the
+//               current one is processed, so a round costs about one memory
+//               round trip per warp plus the barrier.
 // A round's buffer is rewritten two rounds later, after the barrier between,
 // which every block passes only once all blocks have finished reading it.
 #include <limits.h>
@@ -94,128 +102,128 @@ __device__ bool rr_grid_barrier(int* counter, int* status, int target, uint64_t 
   return ok != 0;
 }
 
-// (key, expert) b beats a: a real candidate over none, a larger key, or an
-// equal key with a lower index.
-__device__ __forceinline__ bool beats(float kb, int eb, float ka, int ea) {
-  return eb != kNone && (ea == kNone || kb > ka || (kb == ka && eb < ea));
+// A selection key as an unsigned integer with the same order: the sign bit
+// flipped for positive keys, all bits for negative ones (-0 is made +0 first,
+// as the two compare equal). 0 is below every key, -inf included, and marks
+// "no candidate" in the warp argmax.
+__device__ __forceinline__ uint32_t key_order(float v) {
+  if (v == 0.0f) v = 0.0f;
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The next token a warp walks after t: among its first 32 tokens only those
+// still live, after them every token.
+__device__ __forceinline__ int next_walked(int t, int t_lo, int t_hi, uint32_t live) {
+  const int j = t + 1 - t_lo;
+  if (j < 32) {
+    const uint32_t m = live & (0xffffffffu << j);
+    if (m) return t_lo + __ffs(m) - 1;
+    return min(t_hi, t_lo + 32);
+  }
+  return min(t_hi, t + 1);
+}
+
+// One token's loads for a round's walk: its pairs' state, proposal and
+// rank (lanes < k), its selection keys (expert lane + 32 i in key[i]) and
+// its held-set words (the same in every lane).
+template <int NW>
+struct TokLoad {
+  int st, pr, rk;
+  uint32_t key[NW];  // key_order of the selection keys
+  uint32_t hw[NW];
+};
+
+template <int NW>
+__device__ __forceinline__ void load_token(const RerouteArgs& a, int t, int lane, TokLoad<NW>& L) {
+  const size_t p = (size_t)t * a.k + lane;
+  L.st = lane < a.k ? a.assign[p] : -1;
+  L.pr = lane < a.k ? a.prop[p] : -1;
+  L.rk = lane < a.k ? a.prank[p] : 0;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    const int e = lane + 32 * i;
+    float r = -INFINITY;
+    if (e < a.N) {
+      r = a.logits[(size_t)t * a.N + e];
+      if (a.sel_bias) r = __fadd_rn(r, a.sel_bias[e]);
+      if (isnan(r)) r = -INFINITY;
+    }
+    L.key[i] = key_order(r);
+    L.hw[i] = i < a.W ? a.held[(size_t)t * a.W + i] : 0u;
+  }
+}
+
+template <int NW>
 __global__ void __launch_bounds__(kRrThreads, 1) reroute_kernel(RerouteArgs a) {
   extern __shared__ int sh[];
   const int N = a.N, k = a.k, W = a.W;
-  int* s_cnt = sh;                       // [kRrWarps][N] counts, then bases
-  int* s_room = sh + kRrWarps * N;       // [N]
-  int* s_tot = s_room + N;               // [N]
+  int* s_cnt = sh;                       // [kRrWarps][N] counts of the proposals being made
+  int* s_wbase = sh + kRrWarps * N;      // [kRrWarps][N] bases of the last round's proposals
+  int* s_room = s_wbase + kRrWarps * N;  // [N] room the last round's proposals saw
+  int* s_next = s_room + N;              // [N] room for the proposals being made
+  int* s_tot = s_next + N;               // [N]
   int* s_base = s_tot + N;               // [N]
   __shared__ int s_any;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int gw = blockIdx.x * kRrWarps + warp;
   const int t_lo = min(a.T, gw * a.tokens_per_warp);
   const int t_hi = min(a.T, t_lo + a.tokens_per_warp);
-  const int npl = (N + 31) / 32;  // experts per lane in the argmax
   for (int i = threadIdx.x; i < kRrWarps * N; i += kRrThreads) s_cnt[i] = 0;
   for (int e = threadIdx.x; e < N; e += kRrThreads) s_room[e] = a.capacity > 0 ? a.capacity : INT_MAX;
   __syncthreads();
   int* mine = s_cnt + warp * N;
+  const int* my_base = s_wbase + warp * N;
 
   // round 0: every pair proposes its routed expert; the token holds them all
-  for (int t = t_lo; t < t_hi; ++t) {
-    const size_t p = (size_t)t * k + lane;
-    int e = -1;
-    if (lane < k) {
-      e = a.topk_idx[p];
-      if (e < 0 || e >= N) {
-        set_status(a.status, MOE_ERR_DEVICE_CHECK);
+  {
+    int e_next = (t_lo < t_hi && lane < k) ? a.topk_idx[(size_t)t_lo * k + lane] : -1;
+    for (int t = t_lo; t < t_hi; ++t) {
+      int e = e_next;
+      if (t + 1 < t_hi && lane < k) e_next = a.topk_idx[(size_t)(t + 1) * k + lane];
+      const size_t p = (size_t)t * k + lane;
+      if (lane < k) {
+        if (e < 0 || e >= N) {
+          set_status(a.status, MOE_ERR_DEVICE_CHECK);
+          e = -1;
+        }
+        a.assign[p] = e >= 0 ? kPending : -1;
+        a.prop[p] = e;
+        if (e >= 0) a.prank[p] = atomicAdd(&mine[e], 1);
+      } else {
         e = -1;
       }
-      a.assign[p] = e >= 0 ? kPending : -1;
-      a.prop[p] = e;
-      if (e >= 0) a.prank[p] = atomicAdd(&mine[e], 1);
-    }
-    for (int i = 0; i < W; ++i) {
-      const uint32_t bit = (e >= 0 && (e >> 5) == i) ? (1u << (e & 31)) : 0u;
-      const uint32_t word = __reduce_or_sync(0xffffffffu, bit);
-      if (lane == i) a.held[(size_t)t * W + i] = word;
+      for (int i = 0; i < W; ++i) {
+        const uint32_t bit = (e >= 0 && (e >> 5) == i) ? (1u << (e & 31)) : 0u;
+        const uint32_t word = __reduce_or_sync(0xffffffffu, bit);
+        if (lane == i) a.held[(size_t)t * W + i] = word;
+      }
     }
   }
 
+  // the warp's first 32 tokens that still have a pending pair (bit j: token
+  // t_lo + j); tokens past them are walked every round
+  uint32_t live = t_hi - t_lo >= 32 ? 0xffffffffu : (1u << (t_hi - t_lo)) - 1u;
   int round = 0;
   for (;; ++round) {
-    if (round > 0) {
-      // ---- 1. propose
-      for (int t = t_lo; t < t_hi; ++t) {
-        const size_t p0 = (size_t)t * k;
-        const bool pend = lane < k && a.assign[p0 + lane] == kPending;
-        uint32_t pmask = __ballot_sync(0xffffffffu, pend);
-        if (pmask == 0) continue;
-        float key[kMaxWords];
-        uint32_t elig = 0;  // bit i: expert lane + 32 i can take a proposal
-#pragma unroll
-        for (int i = 0; i < kMaxWords; ++i) {
-          key[i] = -INFINITY;
-          const int e = lane + 32 * i;
-          if (i < npl && e < N) {
-            float r = a.logits[(size_t)t * N + e];
-            if (a.sel_bias) r = __fadd_rn(r, a.sel_bias[e]);
-            key[i] = isnan(r) ? -INFINITY : r;
-            const uint32_t h = a.held[(size_t)t * W + i];
-            if (!((h >> lane) & 1u) && s_room[e] > 0) elig |= 1u << i;
-          }
-        }
-        while (pmask) {
-          const int s = __ffs(pmask) - 1;
-          pmask &= pmask - 1;
-          float bk = -INFINITY;
-          int be = kNone;
-#pragma unroll
-          for (int i = 0; i < kMaxWords; ++i)
-            if ((elig >> i) & 1u) {
-              if (beats(key[i], lane + 32 * i, bk, be)) {
-                bk = key[i];
-                be = lane + 32 * i;
-              }
-            }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const float ok_ = __shfl_xor_sync(0xffffffffu, bk, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (beats(ok_, oe, bk, be)) {
-              bk = ok_;
-              be = oe;
-            }
-          }
-          if (lane == s) {
-            if (be == kNone) {
-              a.assign[p0 + s] = -1;  // no expert left for it: dropped
-            } else {
-              a.prop[p0 + s] = be;
-              a.prank[p0 + s] = mine[be]++;
-            }
-          }
-          if (be != kNone && (be & 31) == lane) elig &= ~(1u << (be >> 5));
-          __syncwarp();
-        }
-      }
-    }
     __syncthreads();
-    // ---- 2. publish the block's counts; warp counts become warp bases
+    // ---- 1. publish this round's counts; warp counts become warp bases
     int32_t* pub = a.pub + (size_t)(round & 1) * gridDim.x * N;
     for (int e = threadIdx.x; e < N; e += kRrThreads) {
       int acc = 0;
       for (int w = 0; w < kRrWarps; ++w) {
         const int v = s_cnt[w * N + e];
-        s_cnt[w * N + e] = acc;
+        s_wbase[w * N + e] = acc;
+        s_cnt[w * N + e] = 0;
         acc += v;
       }
       pub[(size_t)blockIdx.x * N + e] = acc;
-    }
-    for (int e = threadIdx.x; e < N; e += kRrThreads) {
       s_base[e] = 0;
       s_tot[e] = 0;
     }
     if (threadIdx.x == 0) s_any = 0;
     if (!rr_grid_barrier(a.status + 2, a.status, (round + 1) * (int)gridDim.x, a.limit_ns)) return;
-    // ---- 3. the block's base and the round's total per expert: the G x N
+    // ---- 2. the block's base and the round's total per expert: the G x N
     // published counts are read by all threads at once (kBatch independent
     // loads in flight each) and summed with shared-memory atomics (integer
     // sums: the order does not change them)
@@ -238,35 +246,106 @@ __global__ void __launch_bounds__(kRrThreads, 1) reroute_kernel(RerouteArgs a) {
     }
     __syncthreads();
     for (int e = threadIdx.x; e < N; e += kRrThreads) {
-      const int base = s_base[e];
-      for (int w = 0; w < kRrWarps; ++w) s_cnt[w * N + e] += base;
-      if (s_tot[e] != 0) s_any = 1;
+      const int base = s_base[e], tot = s_tot[e];
+      for (int w = 0; w < kRrWarps; ++w) s_wbase[w * N + e] += base;
+      s_next[e] = s_room[e] - min(s_room[e], tot);
+      if (tot != 0) s_any = 1;
     }
     __syncthreads();
     if (!s_any) break;  // no proposal in this round: every pair is settled
-    for (int t = t_lo; t < t_hi; ++t) {
-      const size_t p = (size_t)t * k + lane;
-      if (lane < k && a.assign[p] == kPending) {
-        const int e = a.prop[p];
-        if (e >= 0 && mine[e] + a.prank[p] < s_room[e]) {
-          a.assign[p] = e;
-          atomicOr(&a.held[(size_t)t * W + (e >> 5)], 1u << (e & 31));
-        }
-      }
-      __syncwarp();
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < N; e += kRrThreads) {
-      s_room[e] -= min(s_room[e], s_tot[e]);
-      for (int w = 0; w < kRrWarps; ++w) s_cnt[w * N + e] = 0;
-    }
-    __syncthreads();
-    if (round > N + 1) {  // cannot happen (see above); stop rather than loop
+    if (round > N + 1) {  // cannot happen (a rejecting round fills an expert)
       set_status(a.status, MOE_ERR_DEVICE_CHECK);
       return;
     }
+    // ---- 3. walk: accept this round's proposals, make the next round's
+    TokLoad<NW> cur, nxt;
+    int t = next_walked(t_lo - 1, t_lo, t_hi, live);
+    if (t < t_hi) load_token<NW>(a, t, lane, cur);
+    while (t < t_hi) {
+      const int tn = next_walked(t, t_lo, t_hi, live);
+      if (tn < t_hi) load_token<NW>(a, tn, lane, nxt);
+      const size_t p = (size_t)t * k + lane;
+      int st = cur.st;
+      const bool was_pending = lane < k && st == kPending;
+      bool accepted = false;
+      if (was_pending && cur.pr >= 0 && my_base[cur.pr] + cur.rk < s_room[cur.pr]) {
+        st = cur.pr;
+        accepted = true;
+      }
+      // the held set gains the accepted experts (every lane keeps the words);
+      // round 0's are the routed experts, which it holds already
+      uint32_t amask = round > 0 ? __ballot_sync(0xffffffffu, accepted) : 0u;
+      bool held_changed = amask != 0;
+      while (amask) {
+        const int s = __ffs(amask) - 1;
+        amask &= amask - 1;
+        const int ea = __shfl_sync(0xffffffffu, st, s);
+#pragma unroll
+        for (int i = 0; i < NW; ++i)
+          if ((ea >> 5) == i) cur.hw[i] |= 1u << (ea & 31);
+      }
+      // the slots still pending propose for the next round
+      uint32_t pmask = __ballot_sync(0xffffffffu, lane < k && st == kPending);
+      int new_pr = -1, new_rk = 0;
+      if (pmask) {
+        uint32_t elig = 0;  // bit i: expert lane + 32 i can take a proposal
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+          const int e = lane + 32 * i;
+          if (e < N && !((cur.hw[i] >> lane) & 1u) && s_next[e] > 0) elig |= 1u << i;
+        }
+        while (pmask) {
+          const int s = __ffs(pmask) - 1;
+          pmask &= pmask - 1;
+          // the lane's best eligible key (its experts ascend with i, so the
+          // first of equal keys is the lower index), then the warp's largest
+          // key and the lowest expert that holds it
+          uint32_t bk = 0;
+          int be = kNone;
+#pragma unroll
+          for (int i = 0; i < NW; ++i)
+            if (((elig >> i) & 1u) && cur.key[i] > bk) {
+              bk = cur.key[i];
+              be = lane + 32 * i;
+            }
+          const uint32_t top = __reduce_max_sync(0xffffffffu, bk);
+          be = (int)__reduce_min_sync(0xffffffffu,
+                                      (top != 0 && bk == top) ? (uint32_t)be : (uint32_t)kNone);
+          if (lane == s) {
+            if (be == kNone) {
+              st = -1;  // no expert left for it: dropped
+            } else {
+              new_pr = be;
+              new_rk = mine[be]++;
+            }
+          }
+          if (be != kNone && (be & 31) == lane) elig &= ~(1u << (be >> 5));
+          __syncwarp();
+        }
+      }
+      if (lane < k) {
+        if (st != cur.st) a.assign[p] = st;
+        if (st == kPending) {
+          a.prop[p] = new_pr;
+          a.prank[p] = new_rk;
+        }
+      }
+      if (held_changed && lane < W) {
+#pragma unroll
+        for (int i = 0; i < NW; ++i)
+          if (i == lane) a.held[(size_t)t * W + i] = cur.hw[i];
+      }
+      // a token without a pending pair is done for the remaining rounds
+      if (t - t_lo < 32 && !__any_sync(0xffffffffu, lane < k && st == kPending))
+        live &= ~(1u << (t - t_lo));
+      cur = nxt;
+      t = tn;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < N; e += kRrThreads) s_room[e] = s_next[e];
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0 && a.rounds_out) *a.rounds_out = round - 1;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && a.rounds_out)
+    *a.rounds_out = round > 0 ? round - 1 : 0;
 }
 
 }  // namespace
@@ -306,12 +385,17 @@ cudaError_t launch_reroute(const moe_config& c, const float* logits, const float
   a.W = (c.n_experts + 31) / 32;
   a.capacity = c.capacity;
   a.limit_ns = kWaitLimitNs;
-  const size_t smem = sizeof(int) * ((size_t)kRrWarps * c.n_experts + 3 * c.n_experts);
+  const size_t smem = sizeof(int) * ((size_t)2 * kRrWarps * c.n_experts + 4 * c.n_experts);
+  // keys and held words per lane: one per 32 experts, rounded up to a power of 2
+  void (*kernel)(RerouteArgs) = a.W <= 1   ? reroute_kernel<1>
+                                : a.W <= 2 ? reroute_kernel<2>
+                                : a.W <= 4 ? reroute_kernel<4>
+                                           : reroute_kernel<8>;
   // one block an SM at most (a cooperative grid must be resident at once),
   // and no more blocks than it takes to give every warp a token
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reroute_kernel,
-                                                                kRrThreads, smem);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kRrThreads,
+                                                                smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   int grid = num_sms();
@@ -330,7 +414,7 @@ cudaError_t launch_reroute(const moe_config& c, const float* logits, const float
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   ProfScope p(K_REROUTE, s);
-  return cudaLaunchKernelEx(&cfg, reroute_kernel, a);
+  return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 }  // namespace moe
