@@ -162,6 +162,31 @@ cudaError_t overflow_stage(const moe_config& c, const float* sel_bias, const int
   return launch_reroute(c, logits, sel_bias, idx, assign, nullptr, rr, status, s);
 }
 
+// The quantized layers' routing and permutation (no row gather: their
+// quantizers gather the rows): the single-block decode launch, or the status
+// reset, the router, the overflow stage and the permutation. *rc gets a
+// host-side status; the return value is the CUDA error.
+cudaError_t route_and_permute(const moe_config& c, const void* x, const void* w_router,
+                              const float* logit_bias, const float* sel_bias, int32_t* idx,
+                              float* tw, int32_t* cnt, float* ps, const LayerWs& w, int tile_m,
+                              cudaStream_t s, int* rc) {
+  *rc = MOE_OK;
+  if (decode_front_applies(c))
+    return launch_decode_front(c, x, w_router, logit_bias, sel_bias, idx, tw, cnt, ps, w.offsets,
+                               w.sorted_pair, w.inv_pos, nullptr, w.seg, tile_m, w.status, s);
+  cudaError_t e = launch_reset_status(w.status, s);
+  if (e != cudaSuccess) return e;
+  e = launch_router(c, x, w_router, logit_bias, sel_bias, nullptr, w.logits, idx, tw, cnt, ps,
+                    w.partials, w.status, s);
+  if (e != cudaSuccess || c.T == 0) return e;
+  PermuteIn pin;
+  if ((e = overflow_stage(c, sel_bias, idx, cnt, w.logits, w.assign, w.rr, w.status, s, &pin)) !=
+      cudaSuccess)
+    return e;
+  return launch_permute(pin.pc, x, pin.idx, pin.counts, w.offsets, w.sorted_pair, w.inv_pos,
+                        nullptr, w.hist, w.status, w.seg, tile_m, s);
+}
+
 // The FP8 layer: the bf16 layer's routing and output buffers, E4M3 copies
 // of the routed rows and of x (shared experts), H in bf16 with its rows' max
 // |H|, and H in E4M3, each with fp32 row scales.
@@ -287,7 +312,8 @@ const char* kKernelNames[K_NUM] = {"reset_status",  "router_topk",    "permute_h
                                    "combine",       "balance_stats",  "quantize",
                                    "bwd_gate",      "bwd_score",      "bwd_dh_swiglu",
                                    "bwd_da",        "bwd_dx",         "bwd_router",
-                                   "bwd_wgrad",     "decode_fused",   "reroute"};
+                                   "bwd_wgrad",     "decode_fused",   "reroute",
+                                   "decode_front"};
 struct Prof {
   std::mutex mu;
   uint32_t mask = 0;
@@ -546,30 +572,41 @@ int moe_layer_forward(const moe_config* cfg, const void* x, const void* w_router
   Carver cv(ws);
   LayerWs w = carve_layer(cv, c);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
   int32_t* idx = topk_idx ? topk_idx : w.topk_idx;
   float* tw = topk_w ? topk_w : w.topk_w;
   int32_t* cnt = counts ? counts : w.counts;
   float* ps = prob_sum ? prob_sum : w.prob_sum;
   if (decode_fused_applies(c) && !reroutes(c)) {
-    // a decode-sized batch: the whole layer in one kernel
+    // a single token: the whole layer in one kernel
+    if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
     cudaError_t e = launch_decode_fused(c, x, w_router, logit_bias, sel_bias, w_gate, w_up, w_down,
                                         y, idx, tw, cnt, ps, w.dpart, w.status, s);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e);
   }
-  cudaError_t e = launch_router(c, x, w_router, logit_bias, sel_bias, nullptr, w.logits, idx, tw,
-                                cnt, ps, w.partials, w.status, s);
-  if (e != cudaSuccess) return fail_cuda(e);
-  if (c.T == 0) return MOE_OK;
-  PermuteIn pin;
-  if ((e = overflow_stage(c, sel_bias, idx, cnt, w.logits, w.assign, w.rr, w.status, s, &pin)) != cudaSuccess)
-    return fail_cuda(e);
   // with the gather fused into the gate/up GEMM, x_perm is neither written
   // nor read
   void* x_perm = gather_fused(c) ? nullptr : w.x_perm;
-  e = launch_permute(pin.pc, x, pin.idx, pin.counts, w.offsets, w.sorted_pair, w.inv_pos, x_perm,
-                     w.hist, w.status, w.seg, seg_tile(c), s);
-  if (e != cudaSuccess) return fail_cuda(e);
+  cudaError_t e;
+  if (decode_front_applies(c)) {
+    // a decode-sized batch: routing, permutation and gather in one launch
+    // (which also clears the status words)
+    e = launch_decode_front(c, x, w_router, logit_bias, sel_bias, idx, tw, cnt, ps, w.offsets,
+                            w.sorted_pair, w.inv_pos, x_perm, w.seg, seg_tile(c), w.status, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+  } else {
+    if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
+    e = launch_router(c, x, w_router, logit_bias, sel_bias, nullptr, w.logits, idx, tw, cnt, ps,
+                      w.partials, w.status, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (c.T == 0) return MOE_OK;
+    PermuteIn pin;
+    if ((e = overflow_stage(c, sel_bias, idx, cnt, w.logits, w.assign, w.rr, w.status, s, &pin)) !=
+        cudaSuccess)
+      return fail_cuda(e);
+    e = launch_permute(pin.pc, x, pin.idx, pin.counts, w.offsets, w.sorted_pair, w.inv_pos,
+                       x_perm, w.hist, w.status, w.seg, seg_tile(c), s);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
   bool combined = false;
   rc = grouped_impl(c, x_perm, padded_rows(pairs(c)), x, w.offsets, w.sorted_pair, tw, w_gate,
                     w_up, w_down, w.y_perm, w.seg, true, w.h, w.partial, w.status, s, w.inv_pos, y,
@@ -769,22 +806,15 @@ int moe_layer_forward_fp8(const moe_config* cfg, const void* x, const void* w_ro
   LayerFp8Ws w8 = carve_layer_fp8(cv, c);
   LayerWs& w = w8.base;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
   int32_t* idx = topk_idx ? topk_idx : w.topk_idx;
   float* tw = topk_w ? topk_w : w.topk_w;
   int32_t* cnt = counts ? counts : w.counts;
   float* ps = prob_sum ? prob_sum : w.prob_sum;
-  cudaError_t e = launch_router(c, x, w_router, logit_bias, sel_bias, nullptr, w.logits, idx, tw,
-                                cnt, ps, w.partials, w.status, s);
-  if (e != cudaSuccess) return fail_cuda(e);
-  if (c.T == 0) return MOE_OK;
   const long long P = pairs(c);
-  PermuteIn pin;
-  if ((e = overflow_stage(c, sel_bias, idx, cnt, w.logits, w.assign, w.rr, w.status, s, &pin)) != cudaSuccess)
-    return fail_cuda(e);
-  e = launch_permute(pin.pc, x, pin.idx, pin.counts, w.offsets, w.sorted_pair, w.inv_pos, nullptr,
-                     w.hist, w.status, w.seg, seg_tile_m(c), s);
+  cudaError_t e = route_and_permute(c, x, w_router, logit_bias, sel_bias, idx, tw, cnt, ps, w,
+                                    seg_tile_m(c), s, &rc);
   if (e != cudaSuccess) return fail_cuda(e);
+  if (rc != MOE_OK || c.T == 0) return rc;
   // routed rows: gathered and quantized in one pass; their H maxima cleared
   QuantArgs qa{};
   qa.src = static_cast<const __nv_bfloat16*>(x);
@@ -879,23 +909,16 @@ int moe_layer_forward_nvfp4(const moe_config* cfg, const void* x, const void* w_
   LayerNvf4Ws w4 = carve_layer_nvf4(cv, c);
   LayerWs& w = w4.base;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((rc = reset_status(w.status, s)) != MOE_OK) return rc;
   int32_t* idx = topk_idx ? topk_idx : w.topk_idx;
   float* tw = topk_w ? topk_w : w.topk_w;
   int32_t* cnt = counts ? counts : w.counts;
   float* ps = prob_sum ? prob_sum : w.prob_sum;
-  cudaError_t e = launch_router(c, x, w_router, logit_bias, sel_bias, nullptr, w.logits, idx, tw,
-                                cnt, ps, w.partials, w.status, s);
-  if (e != cudaSuccess) return fail_cuda(e);
-  if (c.T == 0) return MOE_OK;
   const long long P = pairs(c);
-  PermuteIn pin;
-  if ((e = overflow_stage(c, sel_bias, idx, cnt, w.logits, w.assign, w.rr, w.status, s, &pin)) != cudaSuccess)
-    return fail_cuda(e);
   // the NVFP4 GEMMs run 128-row tiles
-  e = launch_permute(pin.pc, x, pin.idx, pin.counts, w.offsets, w.sorted_pair, w.inv_pos, nullptr,
-                     w.hist, w.status, w.seg, kTileM, s);
+  cudaError_t e = route_and_permute(c, x, w_router, logit_bias, sel_bias, idx, tw, cnt, ps, w,
+                                    kTileM, s, &rc);
   if (e != cudaSuccess) return fail_cuda(e);
+  if (rc != MOE_OK || c.T == 0) return rc;
   const int sfd = nvf4_sf_stride(c.d_model);
   // routed rows: gathered and quantized in one pass; their H maxima cleared
   QuantArgs qa{};

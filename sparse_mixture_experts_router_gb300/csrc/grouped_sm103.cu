@@ -268,15 +268,24 @@ __device__ __forceinline__ void staged_scales8(const float* p, float row, float 
 constexpr int kMinKbPerSplit = 8;
 __device__ __forceinline__ int choose_splits(int tiles, int grid, int KB, int s_max) {
   if (s_max <= 1 || tiles <= 0 || tiles >= 2 * grid) return 1;
-  auto eff = [&](int S) {
-    const long long units = (long long)tiles * S;
-    return (float)units / (float)((units + grid - 1) / grid * grid);
-  };
-  float best = eff(1);
-  for (int S = 2; S <= s_max && KB / S >= kMinKbPerSplit; ++S) best = fmaxf(best, eff(S));
+  // tiles < 2 * grid here, so tiles * S stays far inside 32 bits; each split
+  // factor's wave efficiency once (candidates: S <= s_max with at least
+  // kMinKbPerSplit K blocks a split, a condition that holds for a prefix of S)
+  float eff[kMaxSplitK + 1];
+  float best = 0.f;
+#pragma unroll
+  for (int S = 1; S <= kMaxSplitK; ++S) {
+    eff[S] = -1.f;
+    if (S == 1 || (S <= s_max && KB / S >= kMinKbPerSplit)) {
+      const int units = tiles * S;
+      eff[S] = (float)units / (float)((units + grid - 1) / grid * grid);
+      best = fmaxf(best, eff[S]);
+    }
+  }
   int pick = 1;
-  for (int S = 2; S <= s_max && KB / S >= kMinKbPerSplit; ++S)
-    if (eff(S) >= best - 0.03f) pick = S;
+#pragma unroll
+  for (int S = 2; S <= kMaxSplitK; ++S)
+    if (eff[S] >= 0.f && eff[S] >= best - 0.03f) pick = S;
   return pick;
 }
 __device__ __forceinline__ int kb_begin(int split, int S, int KB) {
@@ -1913,10 +1922,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 template <int EPI, int OP>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmArgs a, int gemm_grid) {
   __shared__ unsigned s_max[256];
+  __shared__ int s_splits;
   pdl_wait();
   pdl_trigger();
-  const int tiles = __ldg(a.seg + 1) * a.NT;
-  const int S = choose_splits(tiles, gemm_grid, (a.K + Op<OP>::EPK - 1) / Op<OP>::EPK, a.s_max);
+  if (threadIdx.x == 0)  // once a block: the choice loops over the split factors
+    s_splits = choose_splits(__ldg(a.seg + 1) * a.NT, gemm_grid,
+                             (a.K + Op<OP>::EPK - 1) / Op<OP>::EPK, a.s_max);
+  __syncthreads();
+  const int S = s_splits;
   if (S == 1) return;  // the GEMM finished its tiles itself
   const int groups = a.n_out / 4;
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -1986,40 +1999,52 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmArgs a, in
 // are read from y_perm instead. One thread per token and four output
 // columns; a term's S partial loads are issued together before any is
 // added, as in splitk_reduce_kernel.
+constexpr int kCombineThreads = 128;  // small blocks: a decode step's few rows reach more SMs
 template <int NT>
-__global__ void __launch_bounds__(256) splitk_combine_kernel(const GemmArgs a, int gemm_grid,
-                                                             const int32_t* __restrict__ inv_pos,
-                                                             const float* __restrict__ topk_w,
-                                                             __nv_bfloat16* __restrict__ y, int T,
-                                                             int k, int n_shared) {
+__global__ void __launch_bounds__(kCombineThreads) splitk_combine_kernel(
+    const GemmArgs a, int gemm_grid, const int32_t* __restrict__ inv_pos,
+    const float* __restrict__ topk_w, __nv_bfloat16* __restrict__ y, int T, int k, int n_shared) {
+  __shared__ int s_splits;
   pdl_wait();
   pdl_trigger();
+  if (threadIdx.x == 0)  // once a block: the choice loops over the split factors
+    s_splits = choose_splits(__ldg(a.seg + 1) * a.NT, gemm_grid, (a.K + 63) / 64, a.s_max);
   const int d = a.n_out;
   const int groups = d / 4;
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (long long)T * groups) return;
-  const long long t = i / groups;
-  const int c = (int)(i - t * groups) * 4;
-  const int S = choose_splits(__ldg(a.seg + 1) * a.NT, gemm_grid, (a.K + 63) / 64, a.s_max);
+  const bool in = i < (long long)T * groups;
+  const long long t = in ? i / groups : 0;
+  const int c = in ? (int)(i - t * groups) * 4 : 0;
   const long long P = (long long)T * k;
+  // the terms' rows (-1: dropped) and gate weights, loaded while the split
+  // count is being chosen
+  long long row[NT];
+  float g[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    row[j] = -1;
+    g[j] = 1.0f;
+    if (in && j < k + n_shared) {
+      if (j < k) {
+        const int pos = __ldg(inv_pos + t * k + j);
+        g[j] = __ldg(topk_w + t * k + j);
+        if (pos >= 0 && pos < P) row[j] = pos;
+      } else {
+        row[j] = P + (long long)(j - k) * T + t;
+      }
+    }
+  }
+  __syncthreads();
+  if (!in) return;
+  const int S = s_splits;
   const __nv_bfloat16* yp = static_cast<const __nv_bfloat16*>(a.out);
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
-    if (j >= k + n_shared) break;
-    long long row;
-    float g = 1.0f;
-    if (j < k) {
-      const int pos = __ldg(inv_pos + t * k + j);
-      if (pos < 0 || pos >= P) continue;  // dropped: contributes nothing
-      row = pos;
-      g = __ldg(topk_w + t * k + j);
-    } else {
-      row = P + (long long)(j - k) * T + t;
-    }
+    if (row[j] < 0) continue;  // dropped (or past the terms): contributes nothing
     float v[4];
     if (S == 1) {
-      const uint2 q = __ldg(reinterpret_cast<const uint2*>(yp + row * a.ldo + c));
+      const uint2 q = __ldg(reinterpret_cast<const uint2*>(yp + row[j] * a.ldo + c));
       bf16x2_to_f32(q.x, v[0], v[1]);
       bf16x2_to_f32(q.y, v[2], v[3]);
     } else {
@@ -2027,8 +2052,8 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(const GemmArgs a, i
 #pragma unroll
       for (int sp = 0; sp < kMaxSplitK; ++sp)
         if (sp < S)
-          pv[sp] = __ldcg(
-              reinterpret_cast<const float4*>(a.partial + ((long long)sp * a.R + row) * a.pc + c));
+          pv[sp] = __ldcg(reinterpret_cast<const float4*>(
+              a.partial + ((long long)sp * a.R + row[j]) * a.pc + c));
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int sp = 0; sp < kMaxSplitK; ++sp) {
@@ -2039,8 +2064,8 @@ __global__ void __launch_bounds__(256) splitk_combine_kernel(const GemmArgs a, i
           s4[3] += pv[sp].w;
         }
       }
-      const uint32_t p0 = f32x2_to_bf16x2(g * s4[0], g * s4[1]);
-      const uint32_t p1 = f32x2_to_bf16x2(g * s4[2], g * s4[3]);
+      const uint32_t p0 = f32x2_to_bf16x2(g[j] * s4[0], g[j] * s4[1]);
+      const uint32_t p1 = f32x2_to_bf16x2(g[j] * s4[2], g[j] * s4[3]);
       bf16x2_to_f32(p0, v[0], v[1]);
       bf16x2_to_f32(p1, v[2], v[3]);
     }
@@ -2193,19 +2218,19 @@ cudaError_t launch_splitk_combine(const moe_config& c, const GemmArgs& d, int ge
                                   const int32_t* inv_pos, const float* topk_w, void* y,
                                   cudaStream_t s) {
   const int terms = c.top_k + c.n_shared;
-  const dim3 grid((unsigned)ceil_div((long long)c.T * (c.d_model / 4), 256));
+  const dim3 grid((unsigned)ceil_div((long long)c.T * (c.d_model / 4), kCombineThreads));
   __nv_bfloat16* yo = static_cast<__nv_bfloat16*>(y);
   ProfScope p(K_COMBINE, s);
   if (terms <= 2)
-    return launch_pdl(splitk_combine_kernel<2>, grid, dim3(256), 0, s, 1, d, gemm_grid, inv_pos,
+    return launch_pdl(splitk_combine_kernel<2>, grid, dim3(kCombineThreads), 0, s, 1, d, gemm_grid, inv_pos,
                       topk_w, yo, c.T, c.top_k, c.n_shared);
   if (terms <= 4)
-    return launch_pdl(splitk_combine_kernel<4>, grid, dim3(256), 0, s, 1, d, gemm_grid, inv_pos,
+    return launch_pdl(splitk_combine_kernel<4>, grid, dim3(kCombineThreads), 0, s, 1, d, gemm_grid, inv_pos,
                       topk_w, yo, c.T, c.top_k, c.n_shared);
   if (terms <= 8)
-    return launch_pdl(splitk_combine_kernel<8>, grid, dim3(256), 0, s, 1, d, gemm_grid, inv_pos,
+    return launch_pdl(splitk_combine_kernel<8>, grid, dim3(kCombineThreads), 0, s, 1, d, gemm_grid, inv_pos,
                       topk_w, yo, c.T, c.top_k, c.n_shared);
-  return launch_pdl(splitk_combine_kernel<kMaxTopK + kMaxShared>, grid, dim3(256), 0, s, 1, d,
+  return launch_pdl(splitk_combine_kernel<kMaxTopK + kMaxShared>, grid, dim3(kCombineThreads), 0, s, 1, d,
                     gemm_grid, inv_pos, topk_w, yo, c.T, c.top_k, c.n_shared);
 }
 

@@ -165,6 +165,16 @@ size_t reroute_scratch_bytes(const moe_config& c, size_t* held = nullptr,
 cudaError_t launch_reroute(const moe_config& c, const float* logits, const float* sel_bias,
                            const int32_t* topk_idx, int32_t* assign, int32_t* rounds,
                            void* scratch, int* status, cudaStream_t s);
+// Decode-sized layers (bf16, T <= 64, N <= 32, no reroute): routing,
+// permutation with the capacity cut, segment table (tile height tile_m) and
+// row gather (skipped when x_perm is null) in one single-block launch
+// (router.cu). It also clears status[0..2], so no reset launch precedes it.
+bool decode_front_applies(const moe_config& c);
+cudaError_t launch_decode_front(const moe_config& c, const void* x, const void* w_router,
+                                const float* logit_bias, const float* sel_bias, int32_t* topk_idx,
+                                float* topk_w, int32_t* counts, float* prob_sum, int32_t* offsets,
+                                int32_t* sorted_pair, int32_t* inv_pos, void* x_perm, int32_t* seg,
+                                int tile_m, int* status, cudaStream_t s);
 // Whether a layer reroutes its capacity overflow (cfg.overflow with a cap).
 inline bool reroutes(const moe_config& c) {
   return c.overflow == MOE_OVERFLOW_REROUTE && c.capacity > 0;
@@ -310,6 +320,7 @@ enum KernelId {
   K_WGRAD,
   K_DECODE_FUSED,
   K_REROUTE,
+  K_DECODE_FRONT,
   K_NUM
 };
 void prof_begin(int id, cudaStream_t s);

@@ -32,6 +32,7 @@
 #include "device_util.cuh"
 #include "moe_internal.h"
 #include "router_finish.cuh"
+#include "seg_table.cuh"
 
 namespace moe {
 namespace {
@@ -94,7 +95,7 @@ __device__ __forceinline__ bool better(float ka, int ia, float kb, int ib) {
 template <int EJ>
 __device__ __forceinline__ void select_token(const float (&r)[EJ], int lane, long long t,
                                              const RouterArgs& a, float (&psum)[EJ],
-                                             int* bcount) {
+                                             int* bcount, int* sel_sm = nullptr) {
   const int N = a.N;
   float key[EJ];
 #pragma unroll
@@ -177,6 +178,7 @@ __device__ __forceinline__ void select_token(const float (&r)[EJ], int lane, lon
       a.topk_idx[t * a.k + s] = sel[s];
       a.topk_w[t * a.k + s] = g[s];
       atomicAdd(&bcount[sel[s]], 1);
+      if (sel_sm) sel_sm[t * a.k + s] = sel[s];  // also in shared memory (decode_front_kernel)
     }
   }
 }
@@ -336,6 +338,185 @@ __global__ void __launch_bounds__(kThreads, 2) router_small_kernel(const RouterA
   }
   __syncthreads();
   finish_block<1>(psum, wprob, bcount, a);
+}
+
+// ---------------------------------------------------------------------------
+// Decode-sized batches (bf16, T <= 64, N <= 32): the routing, the
+// permutation (with the capacity cut), the grouped GEMM's segment table and
+// the row gather in one block, in place of the router, the permutation and
+// the gather launches and the status reset (the block clears the call's
+// status words itself once the grids before it have finished). At these
+// sizes each of those launches was latency rather than work: the router's
+// blocks met in a cross-block sum, the permutation and the gather each ran
+// on one block. Results are those of the separate kernels' definitions:
+// the same selection (select_token), probability sums in a fixed order
+// (tokens of a warp, then warps), counts by integer atomics, and each
+// expert's pairs ranked in ascending pair order.
+constexpr int kFrontThreads = 512;
+constexpr int kFrontWarps = kFrontThreads / 32;
+constexpr int kFrontMaxT = 16;
+constexpr size_t kFrontMaxRouterBytes = 128 * 1024;  // router rows staged in shared memory
+constexpr int front_np(int N) { return N <= 8 ? 8 : N <= 16 ? 16 : 32; }
+constexpr int kFrontMaxPairs = kFrontMaxT * kMaxTopK;
+
+struct FrontArgs {
+  RouterArgs r;
+  int capacity, n_shared, tile_m;
+  int32_t* offsets;
+  int32_t* sorted_pair;
+  int32_t* inv_pos;
+  int32_t* seg;
+  uint4* x_perm;  // null: the caller gathers
+};
+
+template <int NP>
+__global__ void __launch_bounds__(kFrontThreads, 1) decode_front_kernel(const FrontArgs f) {
+  constexpr int NV = NP < 16 ? 16 : NP;  // reduce_scatter takes 16 or 32 values
+  extern __shared__ uint4 w_sm[];            // [NP][vec] router rows, rows past N zero
+  __shared__ float sc[kFrontMaxT][32];       // scores
+  __shared__ float red[kFrontWarps][32];     // a token's per-warp partial scores
+  __shared__ float wprob[kFrontWarps][32];   // per-warp probability sums
+  __shared__ int bcount[32];
+  __shared__ int sidx[kFrontMaxPairs];       // expert of each pair
+  __shared__ int srow[kFrontMaxPairs];       // pair of each row
+  __shared__ int soff[33];
+  __shared__ int sscr[32 + kMaxShared + 1];
+  const RouterArgs& a = f.r;
+  const int N = a.N, k = a.k, T = a.T, P = T * k;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int vec = a.d / 8;
+  {  // the router rows into shared memory, all copies in flight at once; they
+     // are inputs of the call, not results of the grid before it, so the
+     // copies start before the wait on that grid
+    const uint4* w = static_cast<const uint4*>(a.w);
+    const int nw = N * vec;
+    for (int i = threadIdx.x; i < NP * vec; i += kFrontThreads) {
+      const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(w_sm + i));
+      const uint4* src = w + (i < nw ? i : 0);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                   "r"(i < nw ? 16 : 0)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x < 3) a.status[threadIdx.x] = 0;
+  if (threadIdx.x < 32) bcount[threadIdx.x] = 0;
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+
+  // 1. scores: `ws` warps per token split its row's 16-byte vectors (x from
+  // global memory, four in flight a lane; the router rows from shared
+  // memory); their partial sums meet in warp order
+  int ws = 1;
+  while (ws < kFrontWarps && 2 * ws * T <= kFrontWarps) ws *= 2;
+  const int gpr = kFrontWarps / ws;  // tokens a round
+  constexpr int kXBatch = 4;
+  const uint4* x = static_cast<const uint4*>(a.x);
+  for (int t0 = 0; t0 < T; t0 += gpr) {
+    const int t = t0 + warp / ws, wi = warp % ws;
+    float v[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = 0.f;
+    if (t < T) {
+      const int stride = 32 * ws;
+      for (int vb0 = wi * 32 + lane; vb0 < vec; vb0 += stride * kXBatch) {
+        uint4 xq[kXBatch];
+#pragma unroll
+        for (int b = 0; b < kXBatch; ++b) {
+          const int vb = vb0 + b * stride;
+          xq[b] = vb < vec ? __ldg(x + (size_t)t * vec + vb) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int b = 0; b < kXBatch; ++b) {
+          const int vb = vb0 + b * stride;
+          if (vb >= vec) break;
+          float xf[8];
+          V16<__nv_bfloat16>::cvt(xq[b], xf);
+#pragma unroll
+          for (int e = 0; e < NP; ++e) {
+            float wf[8];
+            V16<__nv_bfloat16>::cvt(w_sm[e * vec + vb], wf);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[e] = fmaf(xf[i], wf[i], v[e]);
+          }
+        }
+      }
+    }
+    reduce_scatter<NV>(v, lane);  // value e, summed over the warp, at lane e * 32/NV
+    red[warp][lane] = __shfl_sync(0xffffffffu, v[0], (lane < NP ? lane : 0) * (32 / NV));
+    __syncthreads();
+    if (t < T && wi == 0 && lane < N) {
+      float sum = 0.f;
+      for (int j = 0; j < ws; ++j) sum += red[warp + j][lane];
+      sc[t][lane] = a.logit_bias ? __fadd_rn(sum, a.logit_bias[lane]) : sum;
+    }
+    __syncthreads();
+  }
+
+  // 2. selection, gates and statistics: a warp per token
+  float psum[1] = {0.f};
+  for (int t = warp; t < T; t += kFrontWarps) {
+    float r[1] = {lane < N ? sc[t][lane] : 0.f};
+    if (a.logits_out && lane < N) a.logits_out[(size_t)t * N + lane] = r[0];
+    select_token<1>(r, lane, t, a, psum, bcount, sidx);
+  }
+  wprob[warp][lane] = psum[0];
+  __syncthreads();
+  if (threadIdx.x < N) {
+    float s = 0.f;
+    for (int j = 0; j < kFrontWarps; ++j) s += wprob[j][threadIdx.x];
+    a.prob_sum[threadIdx.x] = s;
+    a.counts[threadIdx.x] = bcount[threadIdx.x];
+  }
+  // 3. permutation: kept rows per expert, their offsets, each pair's rank
+  if (warp == 0) {
+    const int kept = lane < N ? (f.capacity > 0 ? min(bcount[lane], f.capacity) : bcount[lane]) : 0;
+    if (lane < N) soff[lane] = kept;
+    __syncwarp();
+    const int total = warp_exclusive_scan(soff, N, lane);
+    if (lane == 0) soff[N] = total;
+  }
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += kFrontThreads) {
+    const int e = sidx[p];
+    int pos = -1;
+    if (e >= 0) {
+      int rank = 0;
+      for (int q = 0; q < p; ++q) rank += sidx[q] == e;
+      if (f.capacity == 0 || rank < f.capacity) pos = soff[e] + rank;
+    }
+    f.inv_pos[p] = pos;
+    if (pos >= 0) {
+      f.sorted_pair[pos] = p;
+      srow[pos] = p;
+    }
+  }
+  for (int e = threadIdx.x; e <= N; e += kFrontThreads) f.offsets[e] = soff[e];
+  __syncthreads();
+  if (f.seg != nullptr) write_seg_table(soff, N, f.n_shared, T, P, f.tile_m, f.seg, sscr);
+  // 4. the gather: row r of x_perm is x[srow[r] / k]
+  if (f.x_perm != nullptr) {  // (x is in L2 from the scores) 8 loads a thread in flight
+    constexpr int kGB = 8;
+    const int total = soff[N] * vec;
+    for (int i0 = threadIdx.x; i0 < total; i0 += kFrontThreads * kGB) {
+      uint4 v[kGB];
+#pragma unroll
+      for (int b = 0; b < kGB; ++b) {
+        const int i = i0 + b * kFrontThreads;
+        if (i < total) {
+          const int row = i / vec, c = i - row * vec;
+          v[b] = __ldg(x + (size_t)(srow[row] / k) * vec + c);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kGB; ++b) {
+        const int i = i0 + b * kFrontThreads;
+        if (i < total) f.x_perm[i] = v[b];
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -706,6 +887,51 @@ cudaError_t launch_dtype(const moe_config& c, const RouterArgs& a, int grid, cud
 }
 
 }  // namespace
+
+bool decode_front_applies(const moe_config& c) {
+  return c.dtype == MOE_BF16 && c.T >= 1 && c.T <= kFrontMaxT && c.n_experts <= 32 &&
+         c.d_model % 8 == 0 && !reroutes(c) &&
+         (size_t)front_np(c.n_experts) * c.d_model * 2 <= kFrontMaxRouterBytes;
+}
+
+cudaError_t launch_decode_front(const moe_config& c, const void* x, const void* w_router,
+                                const float* logit_bias, const float* sel_bias, int32_t* topk_idx,
+                                float* topk_w, int32_t* counts, float* prob_sum, int32_t* offsets,
+                                int32_t* sorted_pair, int32_t* inv_pos, void* x_perm, int32_t* seg,
+                                int tile_m, int* status, cudaStream_t s) {
+  FrontArgs f{};
+  RouterArgs& a = f.r;
+  a.x = x; a.w = w_router; a.logit_bias = logit_bias; a.sel_bias = sel_bias;
+  a.logits_in = nullptr; a.logits_out = nullptr; a.topk_idx = topk_idx; a.topk_w = topk_w;
+  a.counts = counts; a.partials = nullptr; a.cpart = nullptr; a.status = status;
+  a.prob_sum = prob_sum; a.done = nullptr;
+  a.T = c.T; a.d = c.d_model; a.N = c.n_experts; a.k = c.top_k; a.gate_mode = c.gate_mode;
+  f.capacity = c.capacity;
+  f.n_shared = c.n_shared;
+  f.tile_m = tile_m;
+  f.offsets = offsets;
+  f.sorted_pair = sorted_pair;
+  f.inv_pos = inv_pos;
+  f.seg = seg;
+  f.x_perm = static_cast<uint4*>(x_perm);
+  const size_t smem = (size_t)front_np(c.n_experts) * c.d_model * 2;
+  void (*kernel)(FrontArgs) = c.n_experts <= 8    ? decode_front_kernel<8>
+                              : c.n_experts <= 16 ? decode_front_kernel<16>
+                                                  : decode_front_kernel<32>;
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    for (auto kfn : {decode_front_kernel<8>, decode_front_kernel<16>, decode_front_kernel<32>})
+      if ((e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kFrontMaxRouterBytes)) != cudaSuccess)
+        return e;
+    configured_device = dev;
+  }
+  ProfScope p(K_DECODE_FRONT, s);
+  return launch_pdl(kernel, dim3(1), dim3(kFrontThreads), smem, s, 1, f);
+}
 
 // The most blocks any router kernel for this configuration launches: the
 // tiled kernel (given scores, or N > 32 in fp32) takes one per 64 tokens,
