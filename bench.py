@@ -585,7 +585,7 @@ def run_ours(args):
     if "router_topk" in per_kernel:  # the router's score contraction
         fl = 2.0 * w.T * w.n_experts * w.d_model
         tf = fl / (per_kernel["router_topk"]["ms_per_launch"] / 1e3) / 1e12
-        if w.dtype == "bf16" and w.n_experts > 32:  # tcgen05 router kernel
+        if w.dtype == "bf16":  # tensor cores (tcgen05 for N > 32, mma.sync up to 32)
             per_kernel["router_topk"]["tensor_tflops"] = round(tf, 2)
             per_kernel["router_topk"]["tensor_frac"] = round(tf / pk["bf16"], 4)
         else:  # CUDA-core FMA router kernels

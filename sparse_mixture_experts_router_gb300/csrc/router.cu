@@ -8,19 +8,22 @@
 // "The bare mechanism" (affinity softmax over all experts, renormalised
 // top-k weights, a routing bias that only moves the choice).
 //
-// Scores are fp32 dot products on the CUDA cores, in one of three kernels:
-//  - few experts and many bf16 tokens (N <= 16, T >= 2048): W_r staged in
-//    shared memory, each warp streaming pairs of whole tokens (below);
-//  - few experts (N <= 32): the 8 warps of a block split d_model and score a
-//    group of 2-8 tokens against all N experts together, reading x once
-//    from HBM and W_r from L2 with 16-byte loads. Bound by HBM (reading x
-//    once) for large T, by latency for decode-sized T.
-//  - many experts: a register-tiled block GEMM. A block scores 64 tokens
-//    against all N (<= 256) experts; each thread owns a TM x 8 tile
-//    (tokens x consecutive experts); 32-wide K slices of x and W_r are
-//    staged transposed in shared memory with the next slice prefetched into
-//    registers. Bound by fp32 FMA throughput.
-// Both hand every token to the same warp-level selection: lane l holds the
+// Scores are fp32 sums, in one of these kernels (router_tc.cu has the one
+// for bf16 with 32 < N <= 256):
+//  - bf16 with up to 32 experts and T >= 256: mma.sync tensor-core tiles of
+//    16 tokens (router_mma_kernel, below);
+//  - fp32, or bf16 below 256 tokens, with up to 32 experts: the 8 warps of a
+//    block split d_model and
+//    score a group of 2-8 tokens against all N experts together on the CUDA
+//    cores, reading x once from HBM and W_r from L2 with 16-byte loads;
+//  - fp32 with more experts, or scores given: a register-tiled block GEMM.
+//    A block scores 64 tokens against all N (<= 256) experts; each thread
+//    owns a TM x 8 tile (tokens x consecutive experts); 32-wide K slices of
+//    x and W_r are staged transposed in shared memory with the next slice
+//    prefetched into registers. Bound by fp32 FMA throughput.
+//  - decode-sized layers: decode_front_kernel (routing, permutation and
+//    gather in one block).
+// All hand every token to the same warp-level selection: lane l holds the
 // scores of experts l, l+32, ...; k rounds of a (key desc, index asc) warp
 // argmax choose the top k (equal keys go to the lower index); the gates and
 // the full softmax come from the unbiased scores. Counts use shared-memory
@@ -33,6 +36,7 @@
 #include "moe_internal.h"
 #include "router_finish.cuh"
 #include "seg_table.cuh"
+#include "sm103_ptx.cuh"
 
 namespace moe {
 namespace {
@@ -520,6 +524,131 @@ __global__ void __launch_bounds__(kFrontThreads, 1) decode_front_kernel(const Fr
 }
 
 // ---------------------------------------------------------------------------
+// Few experts with bf16 tokens (N <= 32): the scores on the tensor cores,
+// with mma.sync m16n8k16 (bf16 operands, fp32 accumulation). On the CUDA
+// cores each bf16 product also costs a conversion of the router weight,
+// which kept the streaming kernel issue-bound at about a fifth of HBM; here
+// one instruction covers 16 tokens x 8 experts x 16 elements of d_model.
+//
+// A block scores a tile of 16 tokens; its 8 warps split d_model into
+// 32-element chunks (warp w takes the w-th eighth of them). In a chunk, lane
+// (g, c) = (lane / 4, lane % 4) loads one 16-byte vector, elements
+// 8c .. 8c + 7, of x rows g and g + 8 and of router row g of each
+// 8-expert group, and feeds it to two MMAs: elements 0-3 as the fragment's
+// k = 2c, 2c + 1, 2c + 8, 2c + 9 of the first, elements 4-7 as those of the
+// second. Both operands see the same permutation of the chunk's 32 k, so the
+// products summed are exactly the dot product's. The warps' 16 x NP partial
+// tiles meet in shared memory in warp order; each warp then selects for two
+// of the tile's tokens (select_token), and the blocks' statistics meet as in
+// the other kernels. Blocks walk the token tiles grid-stride.
+// Measured on one GB300 (kernel time, L2 flushed): 21 us for the Mixtral
+// prefill shape (T = 4096, N = 8, d = 4096) against 27 us for the CUDA-core
+// streaming kernel this replaced, 25 against 101 us at N = 32, 23 against
+// 35 us at N = 16, d = 7168. A variant that staged each thread's loads in a
+// private cp.async ring (about 170 KB in flight per SM, no registers held)
+// was slower (23, 35 and 21 us): the cost is the per-tile selection and the
+// tiles' latency, not the bytes in flight.
+__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+constexpr int kMmaTile = 16;  // tokens a block tile
+
+template <int NP>
+__global__ void __launch_bounds__(kThreads, 2) router_mma_kernel(const RouterArgs a) {
+  constexpr int NT = NP / 8;             // 8-expert column tiles
+  constexpr int U = NT == 1 ? 4 : 2;     // chunks whose loads are in flight together
+  __shared__ float part[kWarps][kMmaTile][NP + 1];  // warp partial tiles
+  __shared__ float sc[kMmaTile][32];                // the tile's scores
+  __shared__ float wprob[kWarps * 32];
+  __shared__ int bcount[32];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int g = lane / 4, c = lane % 4;
+  const int N = a.N;
+  const int vec = a.d / 8;               // 16-byte vectors a row
+  const int chunks = (vec + 3) / 4;      // 32-element chunks
+  // the warp's chunks are consecutive, so its U loads of a row cover
+  // 64 U contiguous bytes
+  const int per_warp = (chunks + kWarps - 1) / kWarps;
+  const int ch_begin = warp * per_warp, ch_end = min(chunks, ch_begin + per_warp);
+  const uint4* x = static_cast<const uint4*>(a.x);
+  const uint4* w = static_cast<const uint4*>(a.w);
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x < 32) bcount[threadIdx.x] = 0;
+  float psum[1] = {0.f};
+  const long long tiles = (a.T + kMmaTile - 1) / kMmaTile;
+  for (long long tile = blockIdx.x; tile < tiles; tile += gridDim.x) {  // block-uniform
+    const long long t0 = tile * kMmaTile;
+    const long long r0 = t0 + g, r1 = t0 + g + 8;
+    const bool in0 = r0 < a.T, in1 = r1 < a.T;
+    float acc[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[j][q] = 0.f;
+    for (int ch0 = ch_begin; ch0 < ch_end; ch0 += U) {
+      uint4 xa[U], xb[U], wv[U][NT];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int vi = (ch0 + u) * 4 + c;  // this lane's vector of the chunk
+        const bool in = ch0 + u < ch_end && vi < vec;
+        xa[u] = (in && in0) ? __ldg(x + r0 * vec + vi) : zero;
+        xb[u] = (in && in1) ? __ldg(x + r1 * vec + vi) : zero;
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const int e = 8 * j + g;
+          wv[u][j] = (in && e < N) ? __ldg(w + (size_t)e * vec + vi) : zero;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          mma_16816_bf16(acc[j], xa[u].x, xb[u].x, xa[u].y, xb[u].y, wv[u][j].x, wv[u][j].y);
+          mma_16816_bf16(acc[j], xa[u].z, xb[u].z, xa[u].w, xb[u].w, wv[u][j].z, wv[u][j].w);
+        }
+    }
+    // accumulator (row g or g + 8, expert 8j + 2c + {0, 1})
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      part[warp][g][8 * j + 2 * c] = acc[j][0];
+      part[warp][g][8 * j + 2 * c + 1] = acc[j][1];
+      part[warp][g + 8][8 * j + 2 * c] = acc[j][2];
+      part[warp][g + 8][8 * j + 2 * c + 1] = acc[j][3];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kMmaTile * N; i += kThreads) {
+      const int r = i / N, e = i - r * N;
+      float sum = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < kWarps; ++ww) sum += part[ww][r][e];
+      sc[r][e] = a.logit_bias ? __fadd_rn(sum, a.logit_bias[e]) : sum;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kMmaTile / kWarps; ++q) {
+      const int tl = warp * (kMmaTile / kWarps) + q;
+      const long long t = t0 + tl;
+      if (t < a.T) {  // warp-uniform
+        float r[1] = {lane < N ? sc[tl][lane] : 0.f};
+        if (a.logits_out && lane < N) a.logits_out[t * N + lane] = r[0];
+        select_token<1>(r, lane, t, a, psum, bcount);
+      }
+    }
+    __syncthreads();  // part and sc are rewritten by the next tile
+  }
+  finish_block<1>(psum, wprob, bcount, a);
+}
+
+// ---------------------------------------------------------------------------
 // Many experts: 64 tokens x (32*EJ) experts per block, register tiles.
 template <typename TX, int EJ>
 __global__ void __launch_bounds__(kThreads) router_tiled_kernel(const RouterArgs a) {
@@ -683,114 +812,6 @@ __global__ void __launch_bounds__(kThreads) router_tiled_kernel(const RouterArgs
   finish_block<EJ>(psum, wprob, bcount, a);
 }
 
-// ---------------------------------------------------------------------------
-// Few experts with bf16 tokens and large batches (N <= 16, T >= 2048, the
-// router rows within kStreamMaxSmem): the block first copies W_r into
-// shared memory with cp.async (NP rows of d bf16, rows past N zero-filled)
-// -- issued before it waits on the kernel ahead of it in the stream, as
-// nothing in the layer writes W_r -- and then each warp streams whole groups
-// of TPW = 2 tokens: lane l takes
-// the 16-byte vectors l, l+32, ... of both rows, loaded kStreamChunk at a
-// time with the next chunk in flight while the current one is used, and
-// dots each against the NP router rows read from shared memory (32 lanes
-// read 512 consecutive bytes: no bank conflicts). Per vector and expert that
-// is one shared load and its conversion for both tokens, against an L1
-// round trip per expert and vector in router_small_kernel. Two tokens a
-// warp and two blocks an SM keep 16 warps' loads in flight; a variant with
-// fp32 router rows, four tokens a warp and packed FMAs issued a third of
-// the instructions but had half the warps and ran 45% longer. The
-// reduction, selection and statistics are router_small_kernel's.
-constexpr int kStreamTPW = 2;
-constexpr int kStreamChunk = 3;
-constexpr size_t kStreamMaxSmem = 160 * 1024;
-// Resident blocks per SM: two with 8 router rows (64 KB at d = 4096), one
-// with 16.
-__host__ __device__ constexpr int stream_blocks_per_sm(int NP) { return NP <= 8 ? 2 : 1; }
-
-template <int NP>
-__global__ void __launch_bounds__(kThreads, stream_blocks_per_sm(NP))
-    router_stream_kernel(const RouterArgs a) {
-  constexpr int TPW = kStreamTPW;
-  constexpr int NV = NP * TPW;
-  constexpr int CH = kStreamChunk;
-  static_assert(NV == 16 || NV == 32, "reduce-scatter assumes 16 or 32 values");
-  extern __shared__ uint4 w_sm[];  // [NP][vec]
-  __shared__ float wprob[kWarps * 32];
-  __shared__ int bcount[32];
-  const int vec = a.d / 8;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  {  // global -> shared copies, all in flight at once; rows past N are zero-filled
-    const uint4* w = static_cast<const uint4*>(a.w);
-    const int nw = a.N * vec;
-    for (int i = threadIdx.x; i < NP * vec; i += kThreads) {
-      const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(w_sm + i));
-      const uint4* src = w + (i < nw ? i : 0);
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                   "r"(i < nw ? 16 : 0)
-                   : "memory");
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  }
-  if (threadIdx.x < 32) bcount[threadIdx.x] = 0;
-  pdl_wait();
-  pdl_trigger();
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-  __syncthreads();
-  const uint4* x = static_cast<const uint4*>(a.x);
-  float psum[1] = {0.f};
-  const long long groups = (a.T + TPW - 1) / TPW;
-  for (long long g = (long long)blockIdx.x * kWarps + warp; g < groups;
-       g += (long long)gridDim.x * kWarps) {  // warp-uniform
-    const long long t0 = g * TPW;
-    const uint4* xr[TPW];
-#pragma unroll
-    for (int q = 0; q < TPW; ++q) xr[q] = x + (t0 + q < a.T ? t0 + q : t0) * vec;
-    float v[NV];
-#pragma unroll
-    for (int i = 0; i < NV; ++i) v[i] = 0.f;
-    auto load = [&](int v0, uint4 (&buf)[CH][TPW]) {
-#pragma unroll
-      for (int c = 0; c < CH; ++c)
-#pragma unroll
-        for (int q = 0; q < TPW; ++q) {
-          const int vv = v0 + 32 * c;
-          buf[c][q] = (vv < vec && t0 + q < a.T) ? __ldg(xr[q] + vv) : make_uint4(0, 0, 0, 0);
-        }
-    };
-    uint4 cur[CH][TPW], nxt[CH][TPW];
-    load(lane, cur);
-    for (int v0 = lane; v0 < vec; v0 += 32 * CH) {
-      load(v0 + 32 * CH, nxt);  // the next chunk in flight while this one is used
-#pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        const int vv = v0 + 32 * c;
-        if (vv >= vec) break;
-        float xf[TPW][8];
-#pragma unroll
-        for (int q = 0; q < TPW; ++q) V16<__nv_bfloat16>::cvt(cur[c][q], xf[q]);
-#pragma unroll
-        for (int e = 0; e < NP; ++e) {
-          float wf[8];
-          V16<__nv_bfloat16>::cvt(w_sm[e * vec + vv], wf);
-#pragma unroll
-          for (int q = 0; q < TPW; ++q)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[q * NP + e] = fmaf(xf[q][i], wf[i], v[q * NP + e]);
-        }
-      }
-#pragma unroll
-      for (int c = 0; c < CH; ++c)
-#pragma unroll
-        for (int q = 0; q < TPW; ++q) cur[c][q] = nxt[c][q];
-    }
-    reduce_scatter<NV>(v, lane);
-    select_group<NP, TPW>(v[0], lane, t0, a, psum, bcount);
-  }
-  __syncthreads();
-  finish_block<1>(psum, wprob, bcount, a);
-}
-
-// prob_sum[e] = sum over blocks, in block order.
 
 template <typename K>
 cudaError_t launch_k(K kernel, const RouterArgs& a, int grid, size_t smem, cudaStream_t s) {
@@ -802,27 +823,6 @@ cudaError_t launch_k(K kernel, const RouterArgs& a, int grid, size_t smem, cudaS
 
 bool use_small(const moe_config& c, const float* logits_in) {
   return logits_in == nullptr && c.n_experts <= 32;
-}
-
-// The streaming kernel: bf16 tokens, up to 16 experts, the router rows in
-// shared memory.
-int stream_np(const moe_config& c) { return c.n_experts <= 8 ? 8 : 16; }
-size_t stream_smem(const moe_config& c) {  // bf16 router rows
-  return (size_t)stream_np(c) * (size_t)c.d_model * 2;
-}
-// Only for batches that give every SM's warps token pairs of their own;
-// decode-sized batches keep router_small_kernel, which spreads a token's
-// row over up to 8 warps.
-constexpr int kStreamMinTokens = 2048;
-bool use_stream(const moe_config& c, const float* logits_in) {
-  return use_small(c, logits_in) && c.dtype == MOE_BF16 && c.n_experts <= 16 &&
-         stream_smem(c) <= kStreamMaxSmem && c.T >= kStreamMinTokens;
-}
-int stream_grid(const moe_config& c) {  // as many blocks as are resident at once
-  const long long groups = ceil_div(c.T, kStreamTPW);
-  const int blocks = ceil_div(groups, kWarps);
-  const int cap = stream_blocks_per_sm(stream_np(c)) * num_sms();
-  return blocks < cap ? blocks : cap;
 }
 
 // Blocks of the router launch; router_partials_bytes() sizes the partials
@@ -837,8 +837,21 @@ int router_small_wsplit(const moe_config& c) {
   return ws;
 }
 
+// bf16 scores of up to 32 experts for prefill-sized batches: the mma.sync
+// kernel. Below kMmaMinTokens its 16-token tiles leave most SMs idle and
+// the warp kernel, which spreads each token's row over a block, is faster
+// (15 against 17 us at T = 32 and 64, N = 8, d = 4096).
+constexpr int kMmaMinTokens = 256;
+bool use_mma(const moe_config& c, const float* logits_in) {
+  return logits_in == nullptr && c.dtype == MOE_BF16 && c.n_experts <= 32 &&
+         c.d_model % 8 == 0 && c.T >= kMmaMinTokens;
+}
+
 int router_grid(const moe_config& c, const float* logits_in) {
-  if (use_stream(c, logits_in)) return stream_grid(c);
+  if (use_mma(c, logits_in)) {
+    const int tiles = ceil_div(c.T, kMmaTile);
+    return tiles < kSmallMaxBlocks ? tiles : kSmallMaxBlocks;
+  }
   if (use_small(c, logits_in)) {
     // one round of kWarps / wsplit token groups per block, at most 4 blocks per SM
     const int tpw = c.n_experts <= 8 ? 2 : 1;
@@ -851,20 +864,13 @@ int router_grid(const moe_config& c, const float* logits_in) {
 
 template <typename TX>
 cudaError_t launch_dtype(const moe_config& c, const RouterArgs& a, int grid, cudaStream_t s) {
-  if (use_stream(c, a.logits_in)) {
-    const size_t smem = stream_smem(c);
-    if (stream_np(c) == 8) {
-      cudaError_t e = cudaFuncSetAttribute(router_stream_kernel<8>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      ProfScope p(K_ROUTER, s);
-      return launch_pdl(router_stream_kernel<8>, dim3(grid), dim3(kThreads), smem, s, 1, a);
-    }
-    cudaError_t e = cudaFuncSetAttribute(router_stream_kernel<16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+  if (use_mma(c, a.logits_in)) {
     ProfScope p(K_ROUTER, s);
-    return launch_pdl(router_stream_kernel<16>, dim3(grid), dim3(kThreads), smem, s, 1, a);
+    if (c.n_experts <= 8)
+      return launch_pdl(router_mma_kernel<8>, dim3(grid), dim3(kThreads), 0, s, 1, a);
+    if (c.n_experts <= 16)
+      return launch_pdl(router_mma_kernel<16>, dim3(grid), dim3(kThreads), 0, s, 1, a);
+    return launch_pdl(router_mma_kernel<32>, dim3(grid), dim3(kThreads), 0, s, 1, a);
   }
   if (use_small(c, a.logits_in)) {
     const int ws = router_small_wsplit(c);
