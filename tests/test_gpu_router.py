@@ -95,14 +95,13 @@ GEMM_CASES = [
     synth.Workload("r_tc_n200_many_tiles", T=4500, d_model=200, n_experts=200, top_k=6, d_ff=8,
                    zipf_s=1.2, seed=18),
     synth.DEEPSEEK_V3.replace(name="r_dsv3_full_size", d_ff=8),   # d_model = 7168
-    # bf16 with up to 16 experts and at least 2048 tokens: the streaming
-    # kernel (router rows in shared memory, a warp per two tokens); otherwise
-    # with up to 32 experts the warp kernel, one to eight warps per token group.
+    # bf16 with up to 32 experts and at least 256 tokens: the mma.sync kernel
+    # (16-token tiles, the warps splitting d_model); below 256 tokens the
+    # warp kernel, one to eight warps per token group.
     synth.Workload("r_warp_many_groups", T=4000, d_model=4096, n_experts=8, top_k=2, d_ff=8,
                    seed=19),
-    # 16 router rows, four of them past N; 65 vectors a row (a partial lane
-    # round); an odd T (the last group holds one token); T >= 2048 selects
-    # the streaming kernel
+    # two 8-expert column tiles, four of their rows past N; 65 vectors a row
+    # (a partial 32-element chunk); an odd T (the last tile holds 13 tokens)
     synth.Workload("r_stream_n12_ragged_d", T=2301, d_model=520, n_experts=12, top_k=3, d_ff=8,
                    gate_mode=1, sel_bias=True, seed=26),
     synth.Workload("r_warp_one_expert", T=2100, d_model=256, n_experts=1, top_k=1, d_ff=8, seed=21),
