@@ -344,6 +344,20 @@ __global__ void __launch_bounds__(kThreads, 2) router_small_kernel(const RouterA
   finish_block<1>(psum, wprob, bcount, a);
 }
 
+// One m16n8k16 tensor-core MMA, bf16 operands and fp32 accumulation (the
+// fragments as mma.sync defines them: lane (g, c) = (lane / 4, lane % 4)
+// holds A rows g and g + 8, k = 2c, 2c + 1, 2c + 8, 2c + 9, B column g at
+// the same k, and D rows g and g + 8, columns 2c and 2c + 1).
+__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // ---------------------------------------------------------------------------
 // Decode-sized batches (bf16, T <= 64, N <= 32): the routing, the
 // permutation (with the capacity cut), the grouped GEMM's segment table and
@@ -375,10 +389,9 @@ struct FrontArgs {
 
 template <int NP>
 __global__ void __launch_bounds__(kFrontThreads, 1) decode_front_kernel(const FrontArgs f) {
-  constexpr int NV = NP < 16 ? 16 : NP;  // reduce_scatter takes 16 or 32 values
   extern __shared__ uint4 w_sm[];            // [NP][vec] router rows, rows past N zero
   __shared__ float sc[kFrontMaxT][32];       // scores
-  __shared__ float red[kFrontWarps][32];     // a token's per-warp partial scores
+  __shared__ float part[kFrontWarps][16][NP + 1];  // warp partial score tiles
   __shared__ float wprob[kFrontWarps][32];   // per-warp probability sums
   __shared__ int bcount[32];
   __shared__ int sidx[kFrontMaxPairs];       // expert of each pair
@@ -410,51 +423,60 @@ __global__ void __launch_bounds__(kFrontThreads, 1) decode_front_kernel(const Fr
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
 
-  // 1. scores: `ws` warps per token split its row's 16-byte vectors (x from
-  // global memory, four in flight a lane; the router rows from shared
-  // memory); their partial sums meet in warp order
-  int ws = 1;
-  while (ws < kFrontWarps && 2 * ws * T <= kFrontWarps) ws *= 2;
-  const int gpr = kFrontWarps / ws;  // tokens a round
-  constexpr int kXBatch = 4;
   const uint4* x = static_cast<const uint4*>(a.x);
-  for (int t0 = 0; t0 < T; t0 += gpr) {
-    const int t = t0 + warp / ws, wi = warp % ws;
-    float v[NV];
+  // 1. scores on the tensor cores: the T <= 16 tokens are one m16 tile (rows
+  // past T zero); the warps split d_model into 32-element chunks, lane
+  // (g, c) feeding elements 8c .. 8c + 7 of a chunk of x rows g and g + 8 and
+  // of router row g of each 8-expert group to two MMAs (both operands see the
+  // same permutation of the chunk's k); the warps' partial tiles meet in
+  // warp order
+  {
+    constexpr int NT = NP / 8;
+    constexpr int U = 4;
+    const int g = lane / 4, c = lane % 4;
+    const int chunks = (vec + 3) / 4;
+    const int per_warp = (chunks + kFrontWarps - 1) / kFrontWarps;
+    const int ch_end = min(chunks, (warp + 1) * per_warp);
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    float acc[NT][4];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) v[i] = 0.f;
-    if (t < T) {
-      const int stride = 32 * ws;
-      for (int vb0 = wi * 32 + lane; vb0 < vec; vb0 += stride * kXBatch) {
-        uint4 xq[kXBatch];
+    for (int j = 0; j < NT; ++j)
 #pragma unroll
-        for (int b = 0; b < kXBatch; ++b) {
-          const int vb = vb0 + b * stride;
-          xq[b] = vb < vec ? __ldg(x + (size_t)t * vec + vb) : make_uint4(0, 0, 0, 0);
-        }
+      for (int q = 0; q < 4; ++q) acc[j][q] = 0.f;
+    for (int ch0 = warp * per_warp; ch0 < ch_end; ch0 += U) {
+      uint4 xa[U], xb[U];
 #pragma unroll
-        for (int b = 0; b < kXBatch; ++b) {
-          const int vb = vb0 + b * stride;
-          if (vb >= vec) break;
-          float xf[8];
-          V16<__nv_bfloat16>::cvt(xq[b], xf);
+      for (int u = 0; u < U; ++u) {
+        const int vi = (ch0 + u) * 4 + c;
+        const bool in = ch0 + u < ch_end && vi < vec;
+        xa[u] = (in && g < T) ? __ldg(x + (size_t)g * vec + vi) : zero;
+        xb[u] = (in && g + 8 < T) ? __ldg(x + (size_t)(g + 8) * vec + vi) : zero;
+      }
 #pragma unroll
-          for (int e = 0; e < NP; ++e) {
-            float wf[8];
-            V16<__nv_bfloat16>::cvt(w_sm[e * vec + vb], wf);
+      for (int u = 0; u < U; ++u) {
+        const int vi = (ch0 + u) * 4 + c;
+        const bool in = ch0 + u < ch_end && vi < vec;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[e] = fmaf(xf[i], wf[i], v[e]);
-          }
+        for (int j = 0; j < NT; ++j) {  // router rows past N are zero in w_sm
+          const uint4 wv = in ? w_sm[(8 * j + g) * vec + vi] : zero;
+          mma_16816_bf16(acc[j], xa[u].x, xb[u].x, xa[u].y, xb[u].y, wv.x, wv.y);
+          mma_16816_bf16(acc[j], xa[u].z, xb[u].z, xa[u].w, xb[u].w, wv.z, wv.w);
         }
       }
     }
-    reduce_scatter<NV>(v, lane);  // value e, summed over the warp, at lane e * 32/NV
-    red[warp][lane] = __shfl_sync(0xffffffffu, v[0], (lane < NP ? lane : 0) * (32 / NV));
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      part[warp][g][8 * j + 2 * c] = acc[j][0];
+      part[warp][g][8 * j + 2 * c + 1] = acc[j][1];
+      part[warp][g + 8][8 * j + 2 * c] = acc[j][2];
+      part[warp][g + 8][8 * j + 2 * c + 1] = acc[j][3];
+    }
     __syncthreads();
-    if (t < T && wi == 0 && lane < N) {
+    for (int i = threadIdx.x; i < T * N; i += kFrontThreads) {
+      const int r = i / N, e = i - r * N;
       float sum = 0.f;
-      for (int j = 0; j < ws; ++j) sum += red[warp + j][lane];
-      sc[t][lane] = a.logit_bias ? __fadd_rn(sum, a.logit_bias[lane]) : sum;
+      for (int ww = 0; ww < kFrontWarps; ++ww) sum += part[ww][r][e];
+      sc[r][e] = a.logit_bias ? __fadd_rn(sum, a.logit_bias[e]) : sum;
     }
     __syncthreads();
   }
@@ -548,15 +570,6 @@ __global__ void __launch_bounds__(kFrontThreads, 1) decode_front_kernel(const Fr
 // private cp.async ring (about 170 KB in flight per SM, no registers held)
 // was slower (23, 35 and 21 us): the cost is the per-tile selection and the
 // tiles' latency, not the bytes in flight.
-__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1,
-                                               uint32_t a2, uint32_t a3, uint32_t b0,
-                                               uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 
 constexpr int kMmaTile = 16;  // tokens a block tile
 
