@@ -576,7 +576,7 @@ constexpr int kMmaTile = 16;  // tokens a block tile
 template <int NP>
 __global__ void __launch_bounds__(kThreads, 2) router_mma_kernel(const RouterArgs a) {
   constexpr int NT = NP / 8;             // 8-expert column tiles
-  constexpr int U = NT == 1 ? 4 : 2;     // chunks whose loads are in flight together
+  constexpr int U = NT == 1 ? 8 : NT == 2 ? 4 : 2;  // chunks whose loads are in flight together
   __shared__ float part[kWarps][kMmaTile][NP + 1];  // warp partial tiles
   __shared__ float sc[kMmaTile][32];                // the tile's scores
   __shared__ float wprob[kWarps * 32];
