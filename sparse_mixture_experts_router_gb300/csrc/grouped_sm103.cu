@@ -39,7 +39,10 @@
 //    the E4M3 block scales of their A and B rows; four more warps, one per
 //    TMEM lane quarter, write them into Tensor Memory with tcgen05.st, where
 //    the block-scaled MMA (kind::mxf4nvf4) reads them. The scales take 128
-//    TMEM columns, so this kind has one accumulator.
+//    TMEM columns, so two 256-column accumulators do not fit: consecutive
+//    tiles alternate between columns [0, 256) and [128, 384), the epilogue
+//    drains the shared middle 128 columns first and frees them as soon as
+//    its tcgen05.ld has landed, and the next tile's MMAs start then.
 //  - Every wait is bounded (2 s of %globaltimer). A wait that runs out
 //    records MOE_ERR_TIMEOUT in the status word and sets a shared abort flag
 //    that ends the other roles' loops; the producer then waits (bounded) for
@@ -48,6 +51,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <mutex>
 
 #include "device_util.cuh"
@@ -124,8 +128,16 @@ struct Op {
 };
 // TMEM columns of the NVFP4 block scales: two buffers (alternate K blocks)
 // of 64 columns after the accumulator, A's 16 then B's 32 (4 and 8 a MMA).
-constexpr int SF_TMEM_COL = BN;
+// NVFP4 accumulators: three 128-column regions R0-R2 = columns [0, 384);
+// the scale buffers follow. Even work units of a CTA accumulate in R0-R1
+// (columns 0-255), odd ones in R1-R2 (128-383). The epilogue drains R1
+// first and frees each region once its tcgen05.ld has landed, so a unit's
+// MMAs wait only for that first load of the previous unit (the other
+// region was freed a unit earlier).
+constexpr int NVF4_REGION_COLS = 128;
+constexpr int SF_TMEM_COL = 3 * NVF4_REGION_COLS;
 constexpr int SF_TMEM_BUF = 64;
+static_assert(SF_TMEM_COL + 2 * SF_TMEM_BUF == TMEM_COLS, "TMEM columns");
 template <int OP>
 __host__ __device__ constexpr uint32_t idesc_op(int M, int N) {
   return OP == OP_BF16 ? ptx::idesc_bf16_f32(M, N)
@@ -195,6 +207,7 @@ struct __align__(8) SharedState {
   uint64_t sf_ready[STAGES];  // NVFP4: the stage's block scales are in Tensor Memory
   uint64_t acc_full[NUM_ACC];
   uint64_t acc_empty[NUM_ACC];
+  uint64_t slot_empty[3];  // NVFP4: accumulator regions R0-R2 are free
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -479,6 +492,207 @@ __device__ __forceinline__ void epilogue_fused(const GemmArgs& args, uint32_t tb
   }
 }
 
+// NVFP4 epilogue of one work unit, whose accumulator's N halves (B rows
+// 0-127 and 128-255 of the stages) lie in regions r0 and r0+1 (r0 = 0 for
+// an even unit of the CTA, 1 for an odd one). The warp drains the half in
+// R1 first and frees R1 (one arrival a thread) as soon as that load has
+// landed, so the next unit's MMAs can start; the other region is freed
+// after its last load. It scales, applies the SwiGLU or the gate weight and
+// stores bf16, or, for a split-K unit (prow given), stores the scaled fp32
+// partials. Gate/up: N half 0 holds the tile's 128 gate columns and half 1
+// its up columns; the warp takes columns 64*half..64*half+63 of both, keeps
+// the R1 half (up for an even unit, gate for an odd one) in registers and
+// streams the other in 16 columns at a time. Down: N half i holds output
+// columns 128i..128i+127; the warp takes 64 from 64*half. ss: the warp's
+// 128 staged channel scales (gate/up: its 64 gate then 64 up columns; down:
+// its 64 columns of half 0 then of half 1).
+template <int EPI>
+__device__ __forceinline__ void epilogue_nvf4(const GemmArgs& args, uint32_t tq, int r0,
+                                              uint64_t* slot_empty, const Tile& t, int half,
+                                              bool valid, long long orow, __nv_bfloat16* out,
+                                              float sa, const float* sb0, const float* sb1,
+                                              float gw, const float* ss, float* prow) {
+  const int lane = threadIdx.x % 32;
+  if constexpr (gu_like(EPI)) {
+    const int second = r0 == 0 ? 0 : 2;  // the region of the half not in R1
+    const uint32_t tk = tq + (uint32_t)NVF4_REGION_COLS + 64 * half;
+    const uint32_t tw = tq + (uint32_t)(second * NVF4_REGION_COLS) + 64 * half;
+    const int cw = 64 * half;  // the warp's first column of the tile
+    const int col0 = t.n * 128 + cw;
+    auto run = [&](auto up_first) {
+      constexpr bool UF = decltype(up_first)::value;  // the kept half holds the up columns
+      const float* sk = UF ? sb1 : sb0;
+      const float* sw = UF ? sb0 : sb1;
+      uint32_t k[2][32];
+      ptx::tmem_ld32(tk, k[0]);
+      ptx::tmem_ld32(tk + 32, k[1]);
+      if (prow) {
+        // split-K: lane l fetches the scales of column l of each 32
+        float myk[2] = {0.f, 0.f}, myw[2] = {0.f, 0.f};
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+          if (col0 + 32 * cc + lane < args.n_out) {
+            myk[cc] = __ldg(sk + cw + 32 * cc + lane);
+            myw[cc] = __ldg(sw + cw + 32 * cc + lane);
+          }
+        ptx::tmem_ld_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ptx::smem_addr(&slot_empty[1]));
+        float* pk_row = prow + (UF ? args.n_out : 0);
+        float* pw_row = prow + (UF ? 0 : args.n_out);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t w[32];
+          ptx::tmem_ld32(tw + 32 * cc, w);
+          ptx::tmem_ld_wait();
+          if (cc == 1) {
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(ptx::smem_addr(&slot_empty[second]));
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float a[8], b[8];  // every lane takes part in the shuffles
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              a[e] = __uint_as_float(k[cc][8 * q + e]) * sa *
+                     __shfl_sync(0xffffffffu, myk[cc], 8 * q + e);
+              b[e] = __uint_as_float(w[8 * q + e]) * sa *
+                     __shfl_sync(0xffffffffu, myw[cc], 8 * q + e);
+            }
+            const int c = col0 + 32 * cc + 8 * q;
+            if (!valid || c >= args.n_out) continue;
+            float4* dk = reinterpret_cast<float4*>(pk_row + c);
+            float4* dw = reinterpret_cast<float4*>(pw_row + c);
+            dk[0] = make_float4(a[0], a[1], a[2], a[3]);
+            dk[1] = make_float4(a[4], a[5], a[6], a[7]);
+            dw[0] = make_float4(b[0], b[1], b[2], b[3]);
+            dw[1] = make_float4(b[4], b[5], b[6], b[7]);
+          }
+        }
+        return;
+      }
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_addr(&slot_empty[1]));
+      // scale the kept half in place
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float s8[8];
+          staged_scales8(ss + (UF ? 64 : 0) + 32 * cc + 8 * q, sa, s8);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            k[cc][8 * q + e] = __float_as_uint(__uint_as_float(k[cc][8 * q + e]) * s8[e]);
+        }
+      float hmax = 0.f;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {  // 16 columns of the streamed half at a time
+        uint32_t w[16];
+        ptx::tmem_ld16(tw + 16 * p, w);
+        ptx::tmem_ld_wait();
+        if (p == 3) {
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(ptx::smem_addr(&slot_empty[second]));
+        }
+        uint32_t pk[8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float s8[8];
+          staged_scales8(ss + (UF ? 0 : 64) + 16 * p + 8 * h, sa, s8);
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const int j = 8 * h + e;  // column 16p + j of the warp's 64
+            const float w0 = __uint_as_float(w[j]) * s8[e];
+            const float w1 = __uint_as_float(w[j + 1]) * s8[e + 1];
+            const float k0 = __uint_as_float(k[p >> 1][16 * (p & 1) + j]);
+            const float k1 = __uint_as_float(k[p >> 1][16 * (p & 1) + j + 1]);
+            const float g0 = UF ? w0 : k0, g1 = UF ? w1 : k1;
+            const float u0 = UF ? k0 : w0, u1 = UF ? k1 : w1;
+            pk[j / 2] = f32x2_to_bf16x2(silu(g0) * u0, silu(g1) * u1);
+            float h0, h1;
+            bf16x2_to_f32(pk[j / 2], h0, h1);
+            hmax = fmaxf(hmax, fmaxf(fabsf(h0), fabsf(h1)));
+          }
+        }
+        if (valid) {
+          __nv_bfloat16* dst = out + orow * args.ldo + col0 + 16 * p;
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+            if (col0 + 16 * p + 8 * q < args.n_out)
+              *reinterpret_cast<uint4*>(dst + 8 * q) =
+                  make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+      if (valid && hmax > 0.f) atomicMax(args.h_amax + orow, __float_as_uint(hmax));
+    };
+    if (r0 == 0)
+      run(std::true_type{});
+    else
+      run(std::false_type{});
+  } else {
+    const float scale = valid ? gw * sa : 0.0f;
+#pragma unroll 1
+    for (int step = 0; step < 2; ++step) {
+      const int i = step ^ r0 ^ 1;  // the N half in R1 first
+      const int region = r0 + i;
+      const uint32_t tb = tq + (uint32_t)(region * NVF4_REGION_COLS) + 64 * half;
+      uint32_t v[2][32];
+      ptx::tmem_ld32(tb, v[0]);
+      ptx::tmem_ld32(tb + 32, v[1]);
+      float my[2] = {0.f, 0.f};  // split-K: lane l fetches column l's scale
+      if (prow) {
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int cw = 128 * i + 64 * half + 32 * cc;
+          if (t.n * 256 + cw + lane < args.n_out) my[cc] = __ldg(sb0 + cw + lane);
+        }
+      }
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_addr(&slot_empty[region]));
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int col0 = t.n * 256 + 128 * i + 64 * half + 32 * cc;
+        if (prow) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float y[8];  // every lane takes part in the shuffles
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              y[e] = __uint_as_float(v[cc][8 * q + e]) * sa *
+                     __shfl_sync(0xffffffffu, my[cc], 8 * q + e);
+            if (!valid || col0 + q * 8 >= args.n_out) continue;
+            float4* d0 = reinterpret_cast<float4*>(prow + col0 + q * 8);
+            d0[0] = make_float4(y[0], y[1], y[2], y[3]);
+            d0[1] = make_float4(y[4], y[5], y[6], y[7]);
+          }
+          continue;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float sd[8];
+          staged_scales8(ss + 64 * i + 32 * cc + q * 8, scale, sd);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int j = 4 * q + jj;
+            pk[j] = f32x2_to_bf16x2(__uint_as_float(v[cc][2 * j]) * sd[2 * jj],
+                                    __uint_as_float(v[cc][2 * j + 1]) * sd[2 * jj + 1]);
+          }
+        }
+        if (!valid) continue;
+        __nv_bfloat16* dst = out + orow * args.ldo + col0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (col0 + q * 8 < args.n_out)
+            *reinterpret_cast<uint4*>(dst + q * 8) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
+    }
+  }
+}
+
 // E4M3 epilogue scales of one accumulator row: the row's A scale (x_perm row
 // or token for gate/up, H row for down) and the tile's first weight-channel
 // scales (gate, up; or down). bf16: 1 and null.
@@ -573,6 +787,7 @@ __global__ void __launch_bounds__(Op<OP>::THREADS, 1)
       ptx::mbar_init(ptx::smem_addr(&st.acc_full[i]), 1);
       ptx::mbar_init(ptx::smem_addr(&st.acc_empty[i]), G_EPI_THREADS);
     }
+    for (int i = 0; i < 3; ++i) ptx::mbar_init(ptx::smem_addr(&st.slot_empty[i]), G_EPI_THREADS);
     ptx::mbar_init(ptx::smem_addr(&st.drain), 1);
     st.abort = 0;
     ptx::fence_mbar_init();
@@ -683,19 +898,27 @@ __global__ void __launch_bounds__(Op<OP>::THREADS, 1)
     if constexpr (OP == OP_NVF4) {
       // Lane 0 waits until a stage's operands have landed and its block
       // scales are in TMEM (the last four warps, below), then issues the
-      // block-scaled MMAs. One accumulator; the scales of consecutive K
-      // blocks alternate between two TMEM buffers.
+      // block-scaled MMAs (N = 256). A unit accumulates in regions R0-R1 or
+      // R1-R2 (even and odd units) and first waits until both are free.
+      // The scales of consecutive K blocks alternate between two TMEM
+      // buffers.
       if (lane == 0) {
         int stage = 0;
-        uint32_t phase = 0, acc_phase = 0, kcount = 0;
+        uint32_t phase = 0, kcount = 0;
+        uint32_t region_phase = 0;  // bit i: parity of region i's next release
+        int r0 = 0;                 // the unit's first region: 0 or 1
         bool ok = true;
         for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x) {
-          if (!wait_phase(ptx::smem_addr(&st.acc_empty[0]), acc_phase ^ 1u, abort_flag,
-                          args.status)) {
+          if (!wait_phase(ptx::smem_addr(&st.slot_empty[r0]), ((region_phase >> r0) & 1u) ^ 1u,
+                          abort_flag, args.status) ||
+              !wait_phase(ptx::smem_addr(&st.slot_empty[r0 + 1]),
+                          ((region_phase >> (r0 + 1)) & 1u) ^ 1u, abort_flag, args.status)) {
             ok = false;
             break;
           }
+          region_phase ^= 3u << r0;
           ptx::tc_fence_after();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(r0 * NVF4_REGION_COLS);
           const int split = unit % S;
           const int kb0 = kb_begin(split, S, KB), kb1 = kb_begin(split + 1, S, KB);
           for (int kb = kb0; kb < kb1; ++kb) {
@@ -713,7 +936,7 @@ __global__ void __launch_bounds__(Op<OP>::THREADS, 1)
             const uint64_t bdesc = ptx::sdesc_k128(a_src + A_BYTES);
 #pragma unroll
             for (int k = 0; k < 4; ++k)  // +32 bytes (64 E2M1) of K per step
-              ptx::mma_nvf4(tmem_base, adesc + 2 * k, bdesc + 2 * k, idesc_op<OP>(BM, BN),
+              ptx::mma_nvf4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc_op<OP>(BM, BN),
                             sfa_t + 4 * k, sfb_t + 8 * k, (kb > kb0 || k > 0) ? 1u : 0u);
             ptx::mma_commit(ptx::smem_addr(&st.empty[stage]));
             ++kcount;
@@ -724,7 +947,7 @@ __global__ void __launch_bounds__(Op<OP>::THREADS, 1)
           }
           if (!ok) break;
           ptx::mma_commit(ptx::smem_addr(&st.acc_full[0]));
-          acc_phase ^= 1u;
+          r0 ^= 1;
         }
         if (!ok) {
           ptx::mma_commit(ptx::smem_addr(&st.drain));
@@ -839,6 +1062,7 @@ __global__ void __launch_bounds__(Op<OP>::THREADS, 1)
     __shared__ __align__(16) float ch_scales[EPI_WARPS][128];
     int acc = 0;
     uint32_t acc_phase = 0;
+    int r0 = 0;  // NVFP4: the unit's first accumulator region (unit parity)
     for (int unit = blockIdx.x; unit < total; unit += gridDim.x) {
       const int split = unit % S;
       const Tile t = decode_tile(seg, E, args.NT, unit / S);
@@ -864,10 +1088,15 @@ __global__ void __launch_bounds__(Op<OP>::THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int j = lane + 32 * i;
-            const int jj = gu_like(EPI) ? (j & 63) : j;
-            const int col = gu_like(EPI) ? t.n * 128 + 64 * half + jj : t.n * 256 + 128 * half + j;
-            const float* src = gu_like(EPI) ? (j < 64 ? sb0 : sb1) + 64 * half + jj
-                                            : sb0 + 128 * half + j;
+            // the tile column of the warp's j-th gate (then up) or down
+            // column; NVFP4 down takes 64 from each N half
+            int cw;
+            if (gu_like(EPI))
+              cw = 64 * half + (j & 63);
+            else
+              cw = OP == OP_NVF4 ? 128 * (j >> 6) + 64 * half + (j & 63) : 128 * half + j;
+            const int col = t.n * (gu_like(EPI) ? 128 : 256) + cw;
+            const float* src = (gu_like(EPI) && j >= 64 ? sb1 : sb0) + cw;
             mine[j] = col < args.n_out ? __ldg(src) : 0.0f;
           }
           __syncwarp();
@@ -877,7 +1106,13 @@ __global__ void __launch_bounds__(Op<OP>::THREADS, 1)
       bool ok = wait_phase(ptx::smem_addr(&st.acc_full[acc]), acc_phase, abort_flag, args.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
-      if (S == 1) {
+      if constexpr (OP == OP_NVF4) {
+        float* prow =
+            S == 1 ? nullptr : args.partial + ((long long)split * args.R + orow) * args.pc;
+        epilogue_nvf4<EPI>(args, tmem_base + ((uint32_t)(sub * 32) << 16), r0, st.slot_empty, t,
+                           half, valid, orow, out, sa, sb0, sb1, gw, ss, prow);
+        r0 ^= 1;
+      } else if (S == 1) {
         epilogue_fused<EPI, OP>(args, tbase, t, half, valid, orow, out, sa, sb0, sb1, gw, ss);
         ptx::tc_fence_before();
         ptx::mbar_arrive(ptx::smem_addr(&st.acc_empty[acc]));
