@@ -109,8 +109,8 @@ constexpr int B_MN_BOX_BYTES = 64 * 128;  // one TMA box: 64 K rows x 64 bf16 co
 // NVFP4: one fp32 scale per A row and per weight output channel) differ.
 // NVFP4 stages also carry the E4M3 block scales of their 256 K elements
 // (16 a row: 2 KB for A, 4 KB for B), which the MMA reads from Tensor
-// Memory; they take TMEM columns, so the NVFP4 kernel keeps a single
-// accumulator (1-CTA tiles only).
+// Memory; they take 128 TMEM columns, so the NVFP4 kernel's consecutive
+// accumulators share columns (the regions below; 1-CTA tiles only).
 enum { OP_BF16 = 0, OP_E4M3 = 1, OP_NVF4 = 2 };
 template <int OP>
 struct Op {
@@ -120,6 +120,8 @@ struct Op {
   static constexpr int SF_A = OP == OP_NVF4 ? BM * 16 : 0;
   static constexpr int SF_B = OP == OP_NVF4 ? BN * 16 : 0;
   static constexpr int STAGE = STAGE_BYTES + SF_A + SF_B;  // 48 KB, or 54 KB for NVFP4
+  // NVFP4: one accumulator-full phase a unit; where its accumulator lies
+  // rotates through the TMEM regions below
   static constexpr int NACC = OP == OP_NVF4 ? 1 : NUM_ACC;
   static constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024;  // + 1 KB alignment slack
   // NVFP4 adds four warps (the last), one per TMEM lane quarter, that write
@@ -127,7 +129,8 @@ struct Op {
   static constexpr int THREADS = G_THREADS + (OP == OP_NVF4 ? 128 : 0);
 };
 // TMEM columns of the NVFP4 block scales: two buffers (alternate K blocks)
-// of 64 columns after the accumulator, A's 16 then B's 32 (4 and 8 a MMA).
+// of 64 columns after the accumulator regions, A's 16 then B's 32 (4 and 8
+// a MMA).
 // NVFP4 accumulators: three 128-column regions R0-R2 = columns [0, 384);
 // the scale buffers follow. Even work units of a CTA accumulate in R0-R1
 // (columns 0-255), odd ones in R1-R2 (128-383). The epilogue drains R1
