@@ -63,6 +63,10 @@ def cfg(**kw):
     ({"T": 1 << 28, "top_k": 4}, moe.MOE_ERR_UNSUPPORTED),
     ({"capacity": 1}, moe.MOE_OK),
     ({"capacity": -1}, moe.MOE_ERR_INVALID_ARG),
+    ({"capacity": 4, "overflow": moe.MOE_OVERFLOW_REROUTE}, moe.MOE_OK),
+    ({"overflow": moe.MOE_OVERFLOW_REROUTE}, moe.MOE_OK),  # no capacity: nothing to reroute
+    ({"overflow": 2}, moe.MOE_ERR_INVALID_ARG),
+    ({"overflow": -1}, moe.MOE_ERR_INVALID_ARG),
 ])
 def test_check_config(lib, kw, rc):
     assert moe.check_config(cfg(**kw)) == rc
@@ -83,6 +87,48 @@ def test_workspace_sizes(lib):
     assert moe.workspace_size(cfg(dtype=moe.MOE_F32), "backward") == 0
     assert moe.workspace_size(cfg(d_ff=96), "backward") == 0
     assert moe.workspace_size(c, "backward") >= 5 * P * 14336 * 2
+
+
+def test_reroute_workspace_sizes(lib):
+    """moe_reroute's workspace grows with the tokens and experts and is 0 for
+    an invalid configuration. The layer carves the router scores and the
+    reroute assignment only when it reroutes (capacity set and overflow =
+    MOE_OVERFLOW_REROUTE), so its workspace is larger exactly then."""
+    a = moe.workspace_size(cfg(capacity=8), "reroute")
+    b = moe.workspace_size(cfg(T=4096, capacity=8), "reroute")
+    c = moe.workspace_size(cfg(T=4096, n_experts=128, top_k=8, capacity=8), "reroute")
+    assert a > 0 and a % 256 == 0 and b > a and c > b
+    assert moe.workspace_size(cfg(overflow=3), "reroute") == 0
+    drop = moe.workspace_size(cfg(T=4096, capacity=8))
+    rr = moe.workspace_size(cfg(T=4096, capacity=8, overflow=moe.MOE_OVERFLOW_REROUTE))
+    uncapped = moe.workspace_size(cfg(T=4096, overflow=moe.MOE_OVERFLOW_REROUTE))
+    assert rr > drop and uncapped == moe.workspace_size(cfg(T=4096))
+
+
+def test_reroute_host_rejections_launch_nothing(lib):
+    """moe_reroute refuses null inputs or outputs, misaligned pointers, a bad
+    configuration and a short or misaligned workspace on the host, before any
+    CUDA call (fake addresses are never dereferenced)."""
+    c = cfg(capacity=8, overflow=moe.MOE_OVERFLOW_REROUTE)
+    before = moe.launch_count()
+    A = 0x10000
+    need = moe.workspace_size(c, "reroute")
+
+    def call(conf=c, logits=A, sel=None, idx=A, assign=A, rounds=None, ws=A, nbytes=need):
+        return lib.moe_reroute(ctypes.byref(conf), _P(logits), _P(sel), _P(idx), _P(assign),
+                               _P(rounds), _P(ws), nbytes, None)
+
+    assert call(logits=None) == moe.MOE_ERR_INVALID_ARG
+    assert call(idx=None) == moe.MOE_ERR_INVALID_ARG
+    assert call(assign=None) == moe.MOE_ERR_INVALID_ARG
+    assert call(logits=A + 4) == moe.MOE_ERR_MISALIGNED
+    assert call(sel=A + 8) == moe.MOE_ERR_MISALIGNED
+    assert call(rounds=A + 2) == moe.MOE_ERR_MISALIGNED
+    assert call(conf=cfg(overflow=5)) == moe.MOE_ERR_INVALID_ARG
+    assert call(nbytes=need - 256) == moe.MOE_ERR_WORKSPACE
+    assert call(ws=A + 16) == moe.MOE_ERR_MISALIGNED
+    assert call(ws=None) == moe.MOE_ERR_INVALID_ARG
+    assert moe.launch_count() == before
 
 
 def test_status_strings(lib):
